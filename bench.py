@@ -1,0 +1,423 @@
+"""Benchmark of the deferred-RoPE attention path on GB300.
+
+Headline (the ``value`` of the JSON line): decode KV GB/s on the decode-step workload
+(64 requests x 8 Zipf(1.0) docs of 512 tokens + 65-token private segment, 32/8/128 bf16, RoPE
+base 5e5, page size 16). One step = append each request's new token to its private segment
+(kv_pool_write_tokens) + lazy_attn_decode (split-KV kernel + log-sum-exp combine).
+GB/s counts the logical K+V bytes each request attends (4096 B per key); L2 is flushed (a 512 MB
+write) before every timed step so shared documents are re-read from HBM.
+
+Extra objects on the same line:
+  prefill       TFLOP/s of lazy_attn_prefill on the prefill workload (8 requests x 16 docs of
+                1024 + 256-token causal question), causal-visible QK^T + PV FLOPs only.
+  long_decode   KV GB/s and tokens/s on the long-context decode (16 x 131073 keys).
+  roofline      of the dominant kernel (the decode call), against MEASURED_PEAKS.json.
+  cpu_baseline  the fp64 oracle on the host cores over a bounded sample of the same workload.
+  e2e           the decode step through the public API from pinned host buffers, copies inside
+                the timed region.
+
+--impl reference times the oracle (the only reference arm this path has) on the host cores.
+Multi-GPU: replicas only (the path needs no exchange); value = units of all ranks / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+L2_FLUSH_BYTES = 512 << 20
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(
+            p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed work runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1:
+        import torch.distributed as dist
+        local = int(os.environ.get("LOCAL_RANK", "0"))
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+        return dist.get_rank(), ws, local
+    return 0, 1, 0
+
+
+def _barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(x, ws):
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------------------------------------
+# Our arm
+# ------------------------------------------------------------------------------------------------
+def _timed_steps(fn, steps, flush, stream):
+    """Run `steps` calls of fn, each after an untimed L2 flush; return per-step ms (events)."""
+    import torch
+    times = []
+    for _ in range(steps):
+        flush()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        times.append((a, b))
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in times]
+
+
+def bench_ours(args):
+    import numpy as np
+    import torch
+
+    import position_independent_kv_lazy_gb300 as pk
+    import workload as W
+    from position_independent_kv_lazy_gb300 import harness as H
+
+    rank, ws, local = _dist()
+    torch.cuda.set_device(local)
+    pk.build_library()
+    pk.load_library()
+    hbm_peak, tc_peak, tc_sus, peak_kind = _peaks()
+    stream = torch.cuda.current_stream()
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    def flush():
+        flush_buf.zero_()
+
+    # ---------------- decode-step workload (headline)
+    wl = W.decode_workload()
+    src = H.DeviceSource(wl)
+    res = H.build_resident(wl, src)
+    db = H.decode_batch(wl, res, src)
+    kv_bytes = db.n_keys * wl.kv_bytes_per_token()  # K and V, 4096 B per key
+    B = wl.batch
+    ws_bytes = pk.lazy_decode_workspace_bytes(res.pool, B, wl.Hq)
+    workspace = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(db.q)
+    lse = torch.empty((B, wl.Hq), dtype=torch.float32, device="cuda")
+
+    def decode_call():
+        pk.lazy_attn_decode(res.pool, db.q, db.q_pos, db.words, db.cu_pages,
+                            sm_scale=wl.sm_scale, out=out, lse=lse, workspace=workspace)
+
+    def step():
+        pk.kv_pool_write_tokens(res.pool, db.new_k, db.new_v, db.slot_mapping, db.local_pos)
+        decode_call()
+
+    launches_per_step = 3  # encode (append) + decode split + combine
+
+    # e2e buffers: pinned host inputs/outputs of one step
+    h_q = db.q.cpu().pin_memory()
+    h_k = db.new_k.cpu().pin_memory()
+    h_v = db.new_v.cpu().pin_memory()
+    h_words = db.words.cpu().pin_memory()
+    h_cu = db.cu_pages.cpu().pin_memory()
+    h_pos = db.q_pos.cpu().pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    d_q, d_k, d_v = torch.empty_like(db.q), torch.empty_like(db.new_k), torch.empty_like(db.new_v)
+    d_words, d_cu, d_pos = (torch.empty_like(db.words), torch.empty_like(db.cu_pages),
+                            torch.empty_like(db.q_pos))
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_words, h_cu, h_pos))
+    d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
+
+    def e2e_step():
+        for d, h in ((d_q, h_q), (d_k, h_k), (d_v, h_v), (d_words, h_words), (d_cu, h_cu),
+                     (d_pos, h_pos)):
+            d.copy_(h, non_blocking=True)
+        pk.kv_pool_write_tokens(res.pool, d_k, d_v, db.slot_mapping, db.local_pos)
+        pk.lazy_attn_decode(res.pool, d_q, d_pos, d_words, d_cu, sm_scale=wl.sm_scale, out=out,
+                            lse=lse, workspace=workspace)
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+
+    # ---------------- prefill workload (extra object)
+    pwl = W.prefill_workload()
+    psrc = H.DeviceSource(pwl)
+    pres = H.build_resident(pwl, psrc)
+    pb = H.prefill_batch(pwl, pres, psrc)
+    pout = torch.empty_like(pb.q)
+    plse = torch.empty((pb.total_q, pwl.Hq), dtype=torch.float32, device="cuda")
+
+    def prefill_call():
+        pk.lazy_attn_prefill(pres.pool, pb.q, pb.k_new, pb.v_new, pb.cu_q, pb.q_pos0, pb.words,
+                             pb.cu_pages, pb.max_q_len, sm_scale=pwl.sm_scale, out=pout, lse=plse)
+
+    # ---------------- long-context decode (extra object)
+    lwl = W.long_decode_workload()
+    lsrc = H.DeviceSource(lwl)
+    lres = H.build_resident(lwl, lsrc)
+    ldb = H.decode_batch(lwl, lres, lsrc)
+    lws = torch.empty(pk.lazy_decode_workspace_bytes(lres.pool, lwl.batch, lwl.Hq),
+                      dtype=torch.uint8, device="cuda")
+    lout = torch.empty_like(ldb.q)
+    llse = torch.empty((lwl.batch, lwl.Hq), dtype=torch.float32, device="cuda")
+    l_bytes = ldb.n_keys * lwl.kv_bytes_per_token()
+
+    def long_call():
+        pk.lazy_attn_decode(lres.pool, ldb.q, ldb.q_pos, ldb.words, ldb.cu_pages,
+                            sm_scale=lwl.sm_scale, out=lout, lse=llse, workspace=lws)
+
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        flush(); step(); e2e_step(); prefill_call(); long_call()
+    torch.cuda.synchronize()
+    for pool in (res.pool, pres.pool, lres.pool):
+        if pk.lazy_get_device_error(pool) != 0:
+            raise RuntimeError("device error during warm-up")
+
+    with ClockSampler(local) as clk:
+        _barrier(ws)
+        torch.cuda.synchronize()
+        step_ms = _timed_steps(step, args.steps, flush, stream)
+        torch.cuda.synchronize()
+        _barrier(ws)
+        dec_ms = _timed_steps(decode_call, args.steps, flush, stream)
+        e2e_ms = _timed_steps(e2e_step, args.steps, flush, stream)
+        pre_ms = _timed_steps(prefill_call, max(3, args.steps // 2), flush, stream)
+        long_ms = _timed_steps(long_call, max(3, args.steps // 2), flush, stream)
+        torch.cuda.synchronize()
+    clocks = clk.summary()
+
+    total_ms = _max_over_ranks(sum(step_ms), ws)
+    ms_per_step = total_ms / args.steps
+    value = ws * kv_bytes / (ms_per_step * 1e-3) / 1e9
+    dec_avg = sum(dec_ms) / len(dec_ms)
+    achieved = kv_bytes / (dec_avg * 1e-3) / 1e9
+    e2e_avg = sum(e2e_ms) / len(e2e_ms)
+    pre_avg = sum(pre_ms) / len(pre_ms)
+    long_avg = sum(long_ms) / len(long_ms)
+    tflops = pb.flops / (pre_avg * 1e-3) / 1e12
+
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "decode_split_traffic.json")
+    if os.path.exists(prof):
+        try:
+            with open(prof) as f:
+                t = json.load(f)
+            if t.get("kernel_hash") == _kernel_hash():
+                traffic = t.get("bytes_per_launch")
+        except Exception:
+            traffic = None
+
+    line = {
+        "metric": "decode KV GB/s (LazyAttention decode step, deferred RoPE, paged pool)",
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) values, Zipf document draws)",
+        "config": {"workload": "decode_b64: 64 req x (8 Zipf(1.0) docs x 512 + 65 private) keys, "
+                               "Hq32/Hkv8/D128, base 5e5, page 16",
+                   "keys_per_step": db.n_keys, "kv_bytes_per_step": kv_bytes,
+                   "l2": "flushed (512 MB write) before every timed step",
+                   "parallelism": f"replicas x{ws}"},
+        "gpu_launches": launches_per_step * args.steps,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
+                     "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
+                     "traffic": traffic, "peak_kind": peak_kind,
+                     "kernel": "lazy_attn_decode (decode_split_kernel + combine_kernel)"},
+        "e2e": {"value": round(ws * kv_bytes / (e2e_avg * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_avg, 5)},
+        "prefill": {"workload": "prefill_b8: 8 req x (16 Zipf(1.0) docs x 1024 + 256 causal "
+                                "question), Hq32/Hkv8/D128 bf16",
+                    "value": round(tflops, 2), "unit": "TFLOP/s",
+                    "ms_per_call": round(pre_avg, 4), "flops_per_call": pb.flops,
+                    "roofline": {"bound": "tensor", "achieved": round(tflops, 2),
+                                 "peak": tc_peak, "unit": "TFLOP/s",
+                                 "frac": round(tflops / tc_peak, 4), "peak_kind": peak_kind}},
+        "long_decode": {"workload": "long_decode_b16: 16 req x 131073 keys (64 Zipf(1.2) docs "
+                                    "x 2048 + 1)",
+                        "value": round(l_bytes / (long_avg * 1e-3) / 1e9, 2), "unit": "GB/s",
+                        "tokens_per_s": round(lwl.batch / (long_avg * 1e-3), 1),
+                        "ms_per_step": round(long_avg, 4),
+                        "frac": round(l_bytes / (long_avg * 1e-3) / 1e9 / hbm_peak, 4)},
+        "decode_tokens_per_s": round(ws * B / (ms_per_step * 1e-3), 1),
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, src, kv_bytes, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def _kernel_hash():
+    import hashlib
+    h = hashlib.sha256()
+    p = os.path.join(ROOT, "position_independent_kv_lazy_gb300", "csrc", "decode.cu")
+    with open(p, "rb") as f:
+        h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def cpu_baseline(wl, src, kv_bytes_total, budget_s):
+    """The oracle as it stands, on the host cores, over a bounded sample of the workload's
+    requests (all heads), scaled to GB/s of logical KV."""
+    import oracle
+    view = src.host_view() if hasattr(src, "host_view") else wl
+    threads = oracle.default_threads()
+    per_req = kv_bytes_total / wl.batch
+    t0 = time.perf_counter()
+    oracle.attend_request(wl, 0, src=view, threads=threads)
+    t1 = time.perf_counter() - t0
+    n = max(1, min(wl.batch - 1, int(budget_s / max(t1, 1e-3))))
+    t0 = time.perf_counter()
+    for b in range(1, 1 + n):
+        oracle.attend_request(wl, b, src=view, threads=threads)
+    dt = time.perf_counter() - t0
+    return {"value": round(n * per_req / dt / 1e9, 4), "unit": "GB/s", "cores": threads,
+            "kind": "oracle",
+            "sample": f"{n} of {wl.batch} requests, all 32 heads ({n * per_req / 1e9:.3f} GB "
+                      f"logical KV, {dt:.1f} s), fp64 C oracle form A"}
+
+
+# ------------------------------------------------------------------------------------------------
+# Reference arm: the oracle (fp64 CPU), the only other implementation of this path
+# ------------------------------------------------------------------------------------------------
+def bench_reference(args):
+    import workload as W
+    import oracle
+
+    rank = int(os.environ.get("RANK", "0"))
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    wl = W.decode_workload()
+    kv_per_req = (len(wl.requests[0].docs) * wl.doc_len + wl.requests[0].priv_len) * \
+        wl.kv_bytes_per_token()
+    threads = oracle.default_threads()
+    # each step: one request of the workload, all heads (a bounded sample of the decode step)
+    for i in range(args.warmup):
+        oracle.attend_request(wl, i % wl.batch, threads=threads)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle.attend_request(wl, (args.warmup + i) % wl.batch, threads=threads)
+    dt = time.perf_counter() - t0
+    value = args.steps * kv_per_req / dt / 1e9
+    line = {
+        "impl": "reference",
+        "metric": "decode KV GB/s (LazyAttention decode step, deferred RoPE, paged pool)",
+        "value": round(value, 4), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) values, Zipf document draws)",
+        "config": {"workload": "decode_b64: 64 req x (8 Zipf(1.0) docs x 512 + 65 private) keys, "
+                               "Hq32/Hkv8/D128, base 5e5, page 16",
+                   "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle",
+                         "sample": "each step = one request of the decode workload, all heads"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        bench_reference(args)
+    else:
+        bench_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,229 @@
+/*
+ * lazy_attn.h — C ABI of the deferred-RoPE ("lazy") attention library for GB300 (sm_103a).
+ *
+ * The operation: attention in which RoPE is not baked into the cached keys. Each retrieved
+ * document's K/V is stored once, rotated only at its document-local positions 0..L-1, in a paged
+ * pool; a request attends that single copy at any logical offset o. Source: "LazyAttention:
+ * Efficient Retrieval-Augmented Generation with Deferred Positional Encoding" (technical
+ * summaries: "Core concept: deferred positional encoding", "Technical implementation" with its
+ * prefill and decode parts, "Mathematical equivalence").
+ *
+ * Conventions (fixed for the whole library):
+ *   RoPE     R(p) rotates the pair (x_i, x_{i+D/2}) by p * theta_i, theta_i = base^(-2i/D)
+ *            (half-split pairing, as in Llama-3.x, the summaries' evaluation models).
+ *   Scores   s = sm_scale * (R(m) q) . (R(o + j) k) = sm_scale * (R(m - o) q) . (R(j) k);
+ *            the pool stores R(j) k, so a page attended at offset o needs only R(m - o) on q
+ *            (decode) or one relative rotation of the key tile (prefill).
+ *   lse      natural log of sum_k exp(s_k) over the visible keys (s already scaled).
+ *   GQA      query head qh reads kv head qh / (num_q_heads / num_kv_heads).
+ *   Layout   pool pages K_pool, V_pool: [num_blocks][num_kv_heads][page_size][head_dim],
+ *            row-major, pool dtype; one (block, kv head) page is contiguous.
+ *            q: [tokens][num_q_heads][head_dim]; k/v inputs: [tokens][num_kv_heads][head_dim].
+ *   Page word (one uint64 per page of a request's page table; see lazy_pack_page):
+ *            bits 0-31 block id, bits 32-57 logical offset o of the segment the page belongs to
+ *            (26 bits), bits 58-63 n_valid - 1 (tokens valid in the page, 1..64).
+ *   Pointers Arguments named d_* or documented "device" are device pointers; the rest are
+ *            host pointers. All device buffers are owned by the caller. The pool handle owns
+ *            only host metadata and a few bytes of device state (error word, angle table).
+ *   Streams  Every device operation is enqueued on the given stream and returns without
+ *            waiting. Argument errors are returned synchronously; faults the kernels detect
+ *            (a corrupt page word, an expired bounded wait) set bits in the pool's device error
+ *            word, read by lazy_get_device_error. Kernels never trap.
+ *   Status   Every function returns LAZY_OK (0) or a negative LAZY_ERR_* code.
+ */
+#ifndef LAZY_ATTN_H
+#define LAZY_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct lazy_pool lazy_pool;
+/* Same type as cudaStream_t; 0 is the legacy default stream. */
+typedef struct CUstream_st *lazy_stream_t;
+
+enum {
+    LAZY_OK = 0,
+    LAZY_ERR_INVALID_ARG = -1,   /* null pointer, bad size, inconsistent shapes */
+    LAZY_ERR_OUT_OF_BLOCKS = -2, /* the pool's free list cannot satisfy the request */
+    LAZY_ERR_UNSUPPORTED = -3,   /* dtype / head_dim / page_size / group size not built */
+    LAZY_ERR_CUDA = -4,          /* a CUDA runtime call failed (message: lazy_last_error) */
+    LAZY_ERR_BAD_PAGE = -5,      /* device error word: a page word pointed outside the pool */
+    LAZY_ERR_TIMEOUT = -6        /* device error word: a bounded wait inside a kernel expired */
+};
+
+enum { LAZY_DTYPE_BF16 = 0, LAZY_DTYPE_FP32 = 1 };
+
+/* Bits of the device error word. */
+enum { LAZY_DEVERR_BAD_PAGE = 1, LAZY_DEVERR_TIMEOUT = 2 };
+
+/* Prefill kernel choice (lazy_attn_prefill `flags`). */
+enum {
+    LAZY_PREFILL_AUTO = 0,  /* tensor-core kernel when bf16 and head_dim 128, else CUDA-core */
+    LAZY_PREFILL_SIMT = 1,  /* CUDA-core kernel, fp32 arithmetic, any supported shape */
+    LAZY_PREFILL_TC = 2     /* tcgen05/TMEM kernel; LAZY_ERR_UNSUPPORTED if the shape is not */
+};
+
+/* ---------------------------------------------------------------------------------------
+ * Library information
+ * --------------------------------------------------------------------------------------- */
+/* Version as 10000*major + 100*minor + patch. */
+int lazy_version(void);
+/* Static string for a status code. */
+const char *lazy_status_string(int status);
+/* Message of the last failing CUDA call made by this thread (static buffer, never null). */
+const char *lazy_last_error(void);
+
+/* ---------------------------------------------------------------------------------------
+ * Paged KV pool ("cache stores purely content-based keys and values", summaries' core concept)
+ * --------------------------------------------------------------------------------------- */
+/*
+ * Create a pool over caller-owned device buffers d_k_pages / d_v_pages, each
+ * num_blocks * num_kv_heads * page_size * head_dim elements of `dtype`, 16-byte aligned.
+ * page_size must be 16; head_dim 64 or 128; rope_base > 0. No device memory is touched here:
+ * on the first device call the pool allocates its device state (error word, angle table) on
+ * the current device and zero-fills both page buffers (synchronously), so that never-written
+ * slots hold finite values. *out receives the handle. Not thread-safe against destroy.
+ */
+int lazy_pool_create(lazy_pool **out, void *d_k_pages, void *d_v_pages, int32_t num_blocks,
+                     int32_t page_size, int32_t num_kv_heads, int32_t head_dim, int32_t dtype,
+                     double rope_base);
+/* Free the pool's host metadata and device state (not the page buffers). */
+int lazy_pool_destroy(lazy_pool *pool);
+/* Bound, in nanoseconds, on every spin wait inside the kernels (default 2e9). After it
+ * expires the kernel sets LAZY_DEVERR_TIMEOUT, drains its own copies and returns. */
+int lazy_pool_set_wait_limit(lazy_pool *pool, uint64_t ns);
+
+/* Block allocator (host-side free list with reference counts; thread-safe).
+ * kv_pool_alloc pops n blocks (refcount 1) into block_ids; LAZY_ERR_OUT_OF_BLOCKS leaves the
+ * pool unchanged. retain adds a reference (a second request sharing a cached document);
+ * release drops one and returns the block to the free list at zero. Releasing a free block is
+ * LAZY_ERR_INVALID_ARG and changes nothing. */
+int kv_pool_alloc(lazy_pool *pool, int32_t n, int32_t *block_ids);
+int kv_pool_retain(lazy_pool *pool, const int32_t *block_ids, int32_t n);
+int kv_pool_release(lazy_pool *pool, const int32_t *block_ids, int32_t n);
+int kv_pool_num_free(lazy_pool *pool, int32_t *n_free);
+int kv_pool_refcount(lazy_pool *pool, int32_t block_id, int32_t *refcount);
+
+/*
+ * Encode one segment's tokens into the pool (north-star step "doc-KV encode"; the cache keeps
+ * position-free content, summaries' core concept): for the tokens at document-local positions
+ * j = local_pos0 .. local_pos0 + n_tokens - 1,
+ *     K page row  = R(j) k_raw[t]   (fp32 arithmetic, rounded to the pool dtype, RNE)
+ *     V page row  = v[t]
+ * written to block block_ids[j / page_size], slot j % page_size, every kv head.
+ *   d_k_raw, d_v : device [n_tokens][num_kv_heads][head_dim], pool dtype.
+ *   block_ids    : host, in/out. On entry the first *n_blocks entries are blocks the segment
+ *                  already owns (appending to a segment); blocks still missing for
+ *                  positions < local_pos0 + n_tokens are allocated and appended, and
+ *                  *n_blocks is updated. max_blocks is the capacity of block_ids.
+ * On LAZY_ERR_OUT_OF_BLOCKS nothing is allocated or written.
+ */
+int kv_pool_insert_doc(lazy_pool *pool, const void *d_k_raw, const void *d_v, int32_t n_tokens,
+                       int32_t local_pos0, int32_t *block_ids, int32_t *n_blocks,
+                       int32_t max_blocks, lazy_stream_t stream);
+/*
+ * Scattered form of the same encode for batches of appended tokens (one decode step adds one
+ * token to each request's private segment): token t goes to slot d_slot_mapping[t]
+ * (= block * page_size + slot) with local position d_local_pos[t]. Device arrays, n_tokens
+ * entries; entries < 0 are skipped. Blocks must already be allocated.
+ */
+int kv_pool_write_tokens(lazy_pool *pool, const void *d_k_raw, const void *d_v, int32_t n_tokens,
+                         const int32_t *d_slot_mapping, const int32_t *d_local_pos,
+                         lazy_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Page words ("(block ID, offset) bit-packed in a single register", summaries' decoding part)
+ * --------------------------------------------------------------------------------------- */
+/* Pack (block_id < 2^32, offset < 2^26, 1 <= n_valid <= 64) into *word; host only. */
+int lazy_pack_page(uint32_t block_id, uint32_t offset, uint32_t n_valid, uint64_t *word);
+int lazy_unpack_page(uint64_t word, uint32_t *block_id, uint32_t *offset, uint32_t *n_valid);
+/* Pack n words from host arrays; stops at the first invalid entry and returns
+ * LAZY_ERR_INVALID_ARG (words before it are written). */
+int lazy_pack_pages(int32_t n, const uint32_t *block_ids, const uint32_t *offsets,
+                    const uint32_t *n_valid, uint64_t *words);
+
+/* ---------------------------------------------------------------------------------------
+ * Decode (summaries' decoding part: M = 1, rotation fused in the inner loop, q re-rotated only
+ * when the offset changes at a document boundary; spec: split-KV GQA decode streaming
+ * pages, warp-shuffle reductions, log-sum-exp combine)
+ * --------------------------------------------------------------------------------------- */
+/*
+ * One query token per request attends exactly the keys its page words list:
+ *   d_q          device [batch][num_q_heads][head_dim], pool dtype, RAW (unrotated)
+ *   d_q_pos      device int32 [batch]: logical position m of each query
+ *   d_page_words device uint64 [d_cu_pages[batch]]; request b owns
+ *                words d_cu_pages[b] .. d_cu_pages[b+1]-1 (CSR; d_cu_pages device int32
+ *                [batch+1], nondecreasing, d_cu_pages[0] = 0). Word order within a request
+ *                does not change the result, only how often q is re-rotated.
+ *   sm_scale     score scale (1/sqrt(head_dim) for standard attention)
+ *   grid_ctas    0 = one persistent wave sized to the GPU; otherwise that many CTAs
+ *   d_out        device [batch][num_q_heads][head_dim], pool dtype
+ *   d_lse        device float [batch][num_q_heads]; -inf (and out = 0) for a request with no keys
+ *   d_workspace  device scratch of at least lazy_decode_workspace_bytes(...) bytes, 16-byte
+ *                aligned; holds partial (o, lse) per split. Not read before it is written.
+ * Requires num_q_heads % num_kv_heads == 0; group sizes 1, 2, 4, 8 run natively, larger groups
+ * (MQA) in chunks of 8 query heads (K/V then streamed once per chunk).
+ */
+int lazy_decode_workspace_bytes(lazy_pool *pool, int32_t batch, int32_t num_q_heads,
+                                int32_t grid_ctas, size_t *bytes);
+int lazy_attn_decode(lazy_pool *pool, const void *d_q, const int32_t *d_q_pos,
+                     const uint64_t *d_page_words, const int32_t *d_cu_pages, int32_t batch,
+                     int32_t num_q_heads, float sm_scale, int32_t grid_ctas, void *d_out,
+                     float *d_lse, void *d_workspace, size_t workspace_bytes,
+                     lazy_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Prefill (summaries' prefill part: compute-bound, KV blocks loaded from the cache, one
+ * relative rotation of each key tile by the offset between query tile and document instead
+ * of an un-rotate plus re-rotate)
+ * --------------------------------------------------------------------------------------- */
+/*
+ * Question tokens of each request attend (a) every key of the pages listed by its page words
+ * (fully visible) and (b) the question's own keys causally (key position <= query position):
+ *   d_q          device [total_q][num_q_heads][head_dim], RAW; request b owns rows
+ *                d_cu_q[b] .. d_cu_q[b+1]-1 (device int32 [batch+1])
+ *   d_k_new,
+ *   d_v_new      device [total_q][num_kv_heads][head_dim], RAW question keys/values, or both
+ *                null for no question keys. They are not written to the pool (insert them with
+ *                kv_pool_insert_doc / kv_pool_write_tokens if a decode follows).
+ *   d_q_pos0     device int32 [batch]: logical position of request b's first question token;
+ *                token t of the request sits at d_q_pos0[b] + t.
+ *   d_page_words,
+ *   d_cu_pages   as for decode.
+ *   total_q      host: d_cu_q[batch]; max_q_len host: max_b (d_cu_q[b+1]-d_cu_q[b]).
+ *   d_out        device [total_q][num_q_heads][head_dim] pool dtype; d_lse float [total_q][Hq].
+ *   d_workspace  device scratch of lazy_prefill_workspace_bytes(...) bytes (may be 0).
+ *   flags        LAZY_PREFILL_AUTO / _SIMT / _TC.
+ */
+int lazy_prefill_workspace_bytes(lazy_pool *pool, int32_t batch, int32_t total_q,
+                                 int32_t max_q_len, int32_t num_q_heads, int32_t flags,
+                                 size_t *bytes);
+int lazy_attn_prefill(lazy_pool *pool, const void *d_q, const void *d_k_new, const void *d_v_new,
+                      const int32_t *d_cu_q, const int32_t *d_q_pos0,
+                      const uint64_t *d_page_words, const int32_t *d_cu_pages, int32_t batch,
+                      int32_t total_q, int32_t max_q_len, int32_t num_q_heads, float sm_scale,
+                      void *d_out, float *d_lse, void *d_workspace, size_t workspace_bytes,
+                      int32_t flags, lazy_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Errors and test hooks
+ * --------------------------------------------------------------------------------------- */
+/* Wait for `stream`, return the device error word's bits in *err and clear it. */
+int lazy_get_device_error(lazy_pool *pool, int32_t *err, lazy_stream_t stream);
+/*
+ * Test hook: gather the pages the words address using the kernels' own device unpack and
+ * address arithmetic. d_k_out, d_v_out: device [n_words][num_kv_heads][page_size][head_dim];
+ * d_fields: device uint32 [n_words][3] = (block id, offset, n_valid) as unpacked on the device.
+ * Words whose block id is outside the pool set LAZY_DEVERR_BAD_PAGE and gather block 0.
+ */
+int lazy_debug_gather(lazy_pool *pool, const uint64_t *d_page_words, int32_t n_words,
+                      void *d_k_out, void *d_v_out, uint32_t *d_fields, lazy_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LAZY_ATTN_H */

@@ -1,0 +1,350 @@
+"""Python binding of ``liblazyattn.so``: deferred-RoPE attention over a position-agnostic paged
+KV cache for GB300 (sm_103a).
+
+Argument marshalling only: every step of the attention path runs in the library's CUDA kernels
+(``include/lazy_attn.h`` documents each call). PyTorch supplies device memory and streams. If the
+library is not built the import of any call raises: there is no fallback implementation.
+
+The functions keep the C names: ``kv_pool_insert_doc``, ``lazy_attn_prefill``,
+``lazy_attn_decode`` and the pool / page-word / error helpers.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import List, Optional, Sequence, Tuple
+
+import numpy as np
+
+from ._build import build_library, library_path  # noqa: F401
+
+LAZY_OK = 0
+LAZY_ERR_INVALID_ARG = -1
+LAZY_ERR_OUT_OF_BLOCKS = -2
+LAZY_ERR_UNSUPPORTED = -3
+LAZY_ERR_CUDA = -4
+LAZY_ERR_BAD_PAGE = -5
+LAZY_ERR_TIMEOUT = -6
+LAZY_DTYPE_BF16 = 0
+LAZY_DTYPE_FP32 = 1
+LAZY_DEVERR_BAD_PAGE = 1
+LAZY_DEVERR_TIMEOUT = 2
+LAZY_PREFILL_AUTO = 0
+LAZY_PREFILL_SIMT = 1
+LAZY_PREFILL_TC = 2
+
+# Every symbol declared in include/lazy_attn.h (checked by the tests).
+EXPORTS = [
+    "lazy_version", "lazy_status_string", "lazy_last_error", "lazy_pool_create",
+    "lazy_pool_destroy", "lazy_pool_set_wait_limit", "kv_pool_alloc", "kv_pool_retain",
+    "kv_pool_release", "kv_pool_num_free", "kv_pool_refcount", "kv_pool_insert_doc",
+    "kv_pool_write_tokens", "lazy_pack_page", "lazy_unpack_page", "lazy_pack_pages",
+    "lazy_decode_workspace_bytes", "lazy_attn_decode", "lazy_prefill_workspace_bytes",
+    "lazy_attn_prefill", "lazy_get_device_error", "lazy_debug_gather",
+]
+
+
+class LazyError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        lib = _LIB
+        msg = lib.lazy_status_string(status).decode() if lib else str(status)
+        extra = ""
+        if status == LAZY_ERR_CUDA and lib:
+            extra = ": " + lib.lazy_last_error().decode()
+        super().__init__(f"{fn} failed: {msg} ({status}){extra}")
+        self.status = status
+
+
+_LIB = None
+
+_vp = ctypes.c_void_p
+_i32 = ctypes.c_int32
+_u32 = ctypes.c_uint32
+_u64 = ctypes.c_uint64
+_f32 = ctypes.c_float
+_pi32 = ctypes.POINTER(ctypes.c_int32)
+_pu32 = ctypes.POINTER(ctypes.c_uint32)
+_pu64 = ctypes.POINTER(ctypes.c_uint64)
+_psz = ctypes.POINTER(ctypes.c_size_t)
+
+_SIGS = {
+    "lazy_version": ([], ctypes.c_int),
+    "lazy_status_string": ([ctypes.c_int], ctypes.c_char_p),
+    "lazy_last_error": ([], ctypes.c_char_p),
+    "lazy_pool_create": ([ctypes.POINTER(_vp), _vp, _vp, _i32, _i32, _i32, _i32, _i32,
+                          ctypes.c_double], ctypes.c_int),
+    "lazy_pool_destroy": ([_vp], ctypes.c_int),
+    "lazy_pool_set_wait_limit": ([_vp, _u64], ctypes.c_int),
+    "kv_pool_alloc": ([_vp, _i32, _pi32], ctypes.c_int),
+    "kv_pool_retain": ([_vp, _pi32, _i32], ctypes.c_int),
+    "kv_pool_release": ([_vp, _pi32, _i32], ctypes.c_int),
+    "kv_pool_num_free": ([_vp, _pi32], ctypes.c_int),
+    "kv_pool_refcount": ([_vp, _i32, _pi32], ctypes.c_int),
+    "kv_pool_insert_doc": ([_vp, _vp, _vp, _i32, _i32, _pi32, _pi32, _i32, _vp], ctypes.c_int),
+    "kv_pool_write_tokens": ([_vp, _vp, _vp, _i32, _vp, _vp, _vp], ctypes.c_int),
+    "lazy_pack_page": ([_u32, _u32, _u32, _pu64], ctypes.c_int),
+    "lazy_unpack_page": ([_u64, _pu32, _pu32, _pu32], ctypes.c_int),
+    "lazy_pack_pages": ([_i32, _pu32, _pu32, _pu32, _pu64], ctypes.c_int),
+    "lazy_decode_workspace_bytes": ([_vp, _i32, _i32, _i32, _psz], ctypes.c_int),
+    "lazy_attn_decode": ([_vp, _vp, _vp, _vp, _vp, _i32, _i32, _f32, _i32, _vp, _vp, _vp,
+                          ctypes.c_size_t, _vp], ctypes.c_int),
+    "lazy_prefill_workspace_bytes": ([_vp, _i32, _i32, _i32, _i32, _i32, _psz], ctypes.c_int),
+    "lazy_attn_prefill": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _f32,
+                           _vp, _vp, _vp, ctypes.c_size_t, _i32, _vp], ctypes.c_int),
+    "lazy_get_device_error": ([_vp, _pi32, _vp], ctypes.c_int),
+    "lazy_debug_gather": ([_vp, _vp, _i32, _vp, _vp, _vp, _vp], ctypes.c_int),
+}
+
+
+def load_library(path: Optional[str] = None):
+    """Load the built library (raises if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        path = path or library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'` (no fallback exists)")
+        lib = ctypes.CDLL(path)
+        for name, (args, res) in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _LIB = lib
+    return _LIB
+
+
+def _check(fn: str, status: int):
+    if status != LAZY_OK:
+        raise LazyError(fn, status)
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dtype_code(dtype) -> int:
+    import torch
+    if dtype == torch.bfloat16:
+        return LAZY_DTYPE_BF16
+    if dtype == torch.float32:
+        return LAZY_DTYPE_FP32
+    raise ValueError(f"unsupported pool dtype {dtype}")
+
+
+# ------------------------------------------------------------------------------------------------
+# Pool
+# ------------------------------------------------------------------------------------------------
+class LazyPool:
+    """A paged KV pool: page buffers [num_blocks][Hkv][16][D] allocated with torch on `device`."""
+
+    def __init__(self, num_blocks: int, num_kv_heads: int, head_dim: int, dtype, rope_base: float,
+                 page_size: int = 16, device="cuda"):
+        import torch
+        lib = load_library()
+        self.num_blocks, self.hkv, self.d, self.page_size = num_blocks, num_kv_heads, head_dim, page_size
+        self.dtype = dtype
+        self.rope_base = rope_base
+        shape = (num_blocks, num_kv_heads, page_size, head_dim)
+        self.k_pages = torch.empty(shape, dtype=dtype, device=device)
+        self.v_pages = torch.empty(shape, dtype=dtype, device=device)
+        h = _vp()
+        _check("lazy_pool_create", lib.lazy_pool_create(
+            ctypes.byref(h), self.k_pages.data_ptr(), self.v_pages.data_ptr(), num_blocks,
+            page_size, num_kv_heads, head_dim, _dtype_code(dtype), float(rope_base)))
+        self.handle = h
+
+    def close(self):
+        if getattr(self, "handle", None):
+            load_library().lazy_pool_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def lazy_pool_set_wait_limit(pool: LazyPool, ns: int):
+    _check("lazy_pool_set_wait_limit", load_library().lazy_pool_set_wait_limit(pool.handle, ns))
+
+
+def kv_pool_alloc(pool: LazyPool, n: int) -> List[int]:
+    ids = (ctypes.c_int32 * max(n, 1))()
+    _check("kv_pool_alloc", load_library().kv_pool_alloc(pool.handle, n, ids))
+    return list(ids[:n])
+
+
+def kv_pool_retain(pool: LazyPool, ids: Sequence[int]):
+    arr = (ctypes.c_int32 * max(len(ids), 1))(*ids)
+    _check("kv_pool_retain", load_library().kv_pool_retain(pool.handle, arr, len(ids)))
+
+
+def kv_pool_release(pool: LazyPool, ids: Sequence[int]):
+    arr = (ctypes.c_int32 * max(len(ids), 1))(*ids)
+    _check("kv_pool_release", load_library().kv_pool_release(pool.handle, arr, len(ids)))
+
+
+def kv_pool_num_free(pool: LazyPool) -> int:
+    n = ctypes.c_int32()
+    _check("kv_pool_num_free", load_library().kv_pool_num_free(pool.handle, ctypes.byref(n)))
+    return n.value
+
+
+def kv_pool_refcount(pool: LazyPool, block: int) -> int:
+    n = ctypes.c_int32()
+    _check("kv_pool_refcount", load_library().kv_pool_refcount(pool.handle, block, ctypes.byref(n)))
+    return n.value
+
+
+def kv_pool_insert_doc(pool: LazyPool, k_raw, v, local_pos0: int = 0,
+                       block_ids: Optional[Sequence[int]] = None, stream=None) -> List[int]:
+    """Encode a segment's tokens (k rotated at local positions local_pos0.., v copied) into the
+    pool; returns the segment's block ids (existing ones first, new ones appended)."""
+    n = int(k_raw.shape[0])
+    owned = list(block_ids or [])
+    cap = max(len(owned), (local_pos0 + n + pool.page_size - 1) // pool.page_size, 1)
+    arr = (ctypes.c_int32 * cap)(*owned)
+    nb = ctypes.c_int32(len(owned))
+    _check("kv_pool_insert_doc", load_library().kv_pool_insert_doc(
+        pool.handle, _ptr(k_raw.contiguous()), _ptr(v.contiguous()), n, local_pos0, arr,
+        ctypes.byref(nb), cap, _stream(stream)))
+    return list(arr[: nb.value])
+
+
+def kv_pool_write_tokens(pool: LazyPool, k_raw, v, slot_mapping, local_pos, stream=None):
+    _check("kv_pool_write_tokens", load_library().kv_pool_write_tokens(
+        pool.handle, _ptr(k_raw), _ptr(v), int(k_raw.shape[0]), _ptr(slot_mapping),
+        _ptr(local_pos), _stream(stream)))
+
+
+# ------------------------------------------------------------------------------------------------
+# Page words
+# ------------------------------------------------------------------------------------------------
+def lazy_pack_page(block_id: int, offset: int, n_valid: int) -> int:
+    w = ctypes.c_uint64()
+    _check("lazy_pack_page", load_library().lazy_pack_page(block_id, offset, n_valid,
+                                                           ctypes.byref(w)))
+    return w.value
+
+
+def lazy_unpack_page(word: int) -> Tuple[int, int, int]:
+    a, b, c = ctypes.c_uint32(), ctypes.c_uint32(), ctypes.c_uint32()
+    _check("lazy_unpack_page", load_library().lazy_unpack_page(
+        word, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)))
+    return a.value, b.value, c.value
+
+
+def lazy_pack_pages(block_ids, offsets, n_valid) -> np.ndarray:
+    b = np.ascontiguousarray(block_ids, dtype=np.uint32)
+    o = np.ascontiguousarray(offsets, dtype=np.uint32)
+    v = np.ascontiguousarray(n_valid, dtype=np.uint32)
+    out = np.zeros(b.shape[0], dtype=np.uint64)
+    _check("lazy_pack_pages", load_library().lazy_pack_pages(
+        b.shape[0], b.ctypes.data_as(_pu32), o.ctypes.data_as(_pu32), v.ctypes.data_as(_pu32),
+        out.ctypes.data_as(_pu64)))
+    return out
+
+
+def build_page_table(requests: Sequence[Sequence[Tuple[Sequence[int], int, int]]],
+                     page_size: int = 16) -> Tuple[np.ndarray, np.ndarray]:
+    """Page table of a batch: ``requests[b]`` lists segments (block_ids, logical offset, length).
+    Returns (words uint64 [total pages], cu_pages int32 [B+1])."""
+    blk, off, nv, cu = [], [], [], [0]
+    for segs in requests:
+        for ids, o, length in segs:
+            n_pages = (length + page_size - 1) // page_size
+            if len(ids) < n_pages:
+                raise ValueError("segment has fewer blocks than pages")
+            for i in range(n_pages):
+                blk.append(ids[i])
+                off.append(o)
+                nv.append(min(page_size, length - i * page_size))
+        cu.append(len(blk))
+    return lazy_pack_pages(blk, off, nv), np.asarray(cu, dtype=np.int32)
+
+
+# ------------------------------------------------------------------------------------------------
+# Attention
+# ------------------------------------------------------------------------------------------------
+def lazy_decode_workspace_bytes(pool: LazyPool, batch: int, num_q_heads: int,
+                                grid_ctas: int = 0) -> int:
+    n = ctypes.c_size_t()
+    _check("lazy_decode_workspace_bytes", load_library().lazy_decode_workspace_bytes(
+        pool.handle, batch, num_q_heads, grid_ctas, ctypes.byref(n)))
+    return n.value
+
+
+def lazy_attn_decode(pool: LazyPool, q, q_pos, page_words, cu_pages, sm_scale=None,
+                     grid_ctas: int = 0, out=None, lse=None, workspace=None, stream=None):
+    """q [B,Hq,D] raw; q_pos int32 [B]; page_words uint64/int64 [P]; cu_pages int32 [B+1]
+    (all device tensors). Returns (out [B,Hq,D], lse [B,Hq] float32)."""
+    import torch
+    B, Hq, D = q.shape
+    if sm_scale is None:
+        sm_scale = 1.0 / float(D) ** 0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        nbytes = lazy_decode_workspace_bytes(pool, B, Hq, grid_ctas)
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    _check("lazy_attn_decode", load_library().lazy_attn_decode(
+        pool.handle, _ptr(q), _ptr(q_pos), _ptr(page_words), _ptr(cu_pages), B, Hq,
+        float(sm_scale), grid_ctas, _ptr(out), _ptr(lse), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out, lse
+
+
+def lazy_attn_prefill(pool: LazyPool, q, k_new, v_new, cu_q, q_pos0, page_words, cu_pages,
+                      max_q_len: int, sm_scale=None, out=None, lse=None, flags: int = 0,
+                      stream=None):
+    """q [Tq,Hq,D] raw; k_new/v_new [Tq,Hkv,D] raw or None; cu_q, q_pos0, cu_pages int32;
+    page_words uint64 (device). Returns (out [Tq,Hq,D], lse [Tq,Hq] float32)."""
+    import torch
+    Tq, Hq, D = q.shape
+    B = int(cu_q.shape[0]) - 1
+    if sm_scale is None:
+        sm_scale = 1.0 / float(D) ** 0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((Tq, Hq), dtype=torch.float32, device=q.device)
+    n = ctypes.c_size_t()
+    lib = load_library()
+    _check("lazy_prefill_workspace_bytes", lib.lazy_prefill_workspace_bytes(
+        pool.handle, B, Tq, max_q_len, Hq, flags, ctypes.byref(n)))
+    ws = torch.empty(max(n.value, 1), dtype=torch.uint8, device=q.device)
+    _check("lazy_attn_prefill", lib.lazy_attn_prefill(
+        pool.handle, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(cu_q), _ptr(q_pos0),
+        _ptr(page_words), _ptr(cu_pages), B, Tq, max_q_len, Hq, float(sm_scale), _ptr(out),
+        _ptr(lse), _ptr(ws), n.value, flags, _stream(stream)))
+    return out, lse
+
+
+def lazy_get_device_error(pool: LazyPool, stream=None) -> int:
+    e = ctypes.c_int32()
+    _check("lazy_get_device_error", load_library().lazy_get_device_error(
+        pool.handle, ctypes.byref(e), _stream(stream)))
+    return e.value
+
+
+def lazy_debug_gather(pool: LazyPool, page_words, stream=None):
+    import torch
+    n = int(page_words.shape[0])
+    shape = (n, pool.hkv, pool.page_size, pool.d)
+    k = torch.empty(shape, dtype=pool.dtype, device=page_words.device)
+    v = torch.empty(shape, dtype=pool.dtype, device=page_words.device)
+    f = torch.empty((n, 3), dtype=torch.int32, device=page_words.device)
+    _check("lazy_debug_gather", load_library().lazy_debug_gather(
+        pool.handle, _ptr(page_words), n, _ptr(k), _ptr(v), _ptr(f), _stream(stream)))
+    return k, v, f

@@ -1,0 +1,213 @@
+// Doc-KV encode: K page row = R(j) k_raw (document-local position j), V copied; scattered into
+// the paged pool. The cache thereby holds position-free content ("keys and values purely based on
+// content", LazyAttention summaries, core concept) and one copy serves every logical offset.
+//
+// Also: lazy_debug_gather, a test hook that reads pages through the same device unpack and
+// address arithmetic the attention kernels use.
+#include <algorithm>
+
+#include "lazy_common.cuh"
+#include "pool_internal.h"
+
+namespace lazy {
+namespace {
+
+constexpr int kMaxIdsPerLaunch = 512;
+
+struct BlockList {
+  int32_t first_page;  // page index (within the segment) of ids[0]
+  int32_t n;
+  int32_t ids[kMaxIdsPerLaunch];
+};
+
+// One thread = (token, kv head, 16-byte chunk of the lower half); it also handles the matching
+// chunk of the upper half, which holds the rotation partners (pairs (i, i + D/2)).
+template <typename T, int D>
+__global__ void __launch_bounds__(256) encode_kernel(
+    const T *__restrict__ k_raw, const T *__restrict__ v, int32_t n_tokens, int32_t hkv,
+    T *__restrict__ k_pool, T *__restrict__ v_pool, const uint64_t *__restrict__ turn,
+    int32_t tok0, int32_t local_pos0, BlockList blocks, const int32_t *__restrict__ slot_map,
+    const int32_t *__restrict__ local_pos) {
+  constexpr int EPL = 16 / (int)sizeof(T);
+  constexpr int CH = (D / 2) / EPL;
+  const int64_t total = (int64_t)n_tokens * hkv * CH;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int c = (int)(idx % CH);
+    const int64_t rest = idx / CH;
+    const int h = (int)(rest % hkv);
+    const int32_t t = tok0 + (int32_t)(rest / hkv);
+    int32_t j, blk, slot;
+    if (slot_map) {
+      const int32_t s = slot_map[t];
+      if (s < 0) continue;
+      j = local_pos[t];
+      blk = s / kPage;
+      slot = s % kPage;
+    } else {
+      j = local_pos0 + t;
+      blk = blocks.ids[j / kPage - blocks.first_page];
+      slot = j % kPage;
+    }
+    const size_t src = ((size_t)t * hkv + h) * D;
+    const size_t dst = (((size_t)blk * hkv + h) * kPage + slot) * D;
+    float lo[EPL], hi[EPL];
+    unpack16<T>(*reinterpret_cast<const uint4 *>(k_raw + src + c * EPL), lo);
+    unpack16<T>(*reinterpret_cast<const uint4 *>(k_raw + src + D / 2 + c * EPL), hi);
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      float cs, sn;
+      rope_cos_sin((int64_t)j, turn[c * EPL + e], cs, sn);
+      const float x = lo[e], y = hi[e];
+      lo[e] = x * cs - y * sn;
+      hi[e] = x * sn + y * cs;
+    }
+    *reinterpret_cast<uint4 *>(k_pool + dst + c * EPL) = pack16<T>(lo);
+    *reinterpret_cast<uint4 *>(k_pool + dst + D / 2 + c * EPL) = pack16<T>(hi);
+    *reinterpret_cast<uint4 *>(v_pool + dst + c * EPL) =
+        *reinterpret_cast<const uint4 *>(v + src + c * EPL);
+    *reinterpret_cast<uint4 *>(v_pool + dst + D / 2 + c * EPL) =
+        *reinterpret_cast<const uint4 *>(v + src + D / 2 + c * EPL);
+  }
+}
+
+template <typename T, int D>
+int launch_encode(lazy_pool *p, const void *k_raw, const void *v, int32_t n_tokens, int32_t tok0,
+                  int32_t local_pos0, const BlockList &bl, const int32_t *slot_map,
+                  const int32_t *local_pos, cudaStream_t s) {
+  constexpr int EPL = 16 / (int)sizeof(T);
+  const int64_t total = (int64_t)n_tokens * p->hkv * ((D / 2) / EPL);
+  const int threads = 256;
+  const int64_t want = (total + threads - 1) / threads;
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)p->num_sms * 16));
+  encode_kernel<T, D><<<grid, threads, 0, s>>>(
+      (const T *)k_raw, (const T *)v, n_tokens, p->hkv, (T *)p->k, (T *)p->v, p->d_turn, tok0,
+      local_pos0, bl, slot_map, local_pos);
+  LAZY_CUDA_TRY(cudaGetLastError());
+  return LAZY_OK;
+}
+
+int dispatch_encode(lazy_pool *p, const void *k_raw, const void *v, int32_t n_tokens,
+                    int32_t tok0, int32_t local_pos0, const BlockList &bl,
+                    const int32_t *slot_map, const int32_t *local_pos, cudaStream_t s) {
+  if (p->dtype == LAZY_DTYPE_BF16) {
+    if (p->d == 128)
+      return launch_encode<__nv_bfloat16, 128>(p, k_raw, v, n_tokens, tok0, local_pos0, bl,
+                                               slot_map, local_pos, s);
+    return launch_encode<__nv_bfloat16, 64>(p, k_raw, v, n_tokens, tok0, local_pos0, bl,
+                                            slot_map, local_pos, s);
+  }
+  if (p->d == 128)
+    return launch_encode<float, 128>(p, k_raw, v, n_tokens, tok0, local_pos0, bl, slot_map,
+                                     local_pos, s);
+  return launch_encode<float, 64>(p, k_raw, v, n_tokens, tok0, local_pos0, bl, slot_map,
+                                  local_pos, s);
+}
+
+// ----------------------------------------------------------------------------------------------
+// Debug gather: same unpack (word_block / word_offset / word_nvalid) and page addressing as the
+// attention kernels.
+// ----------------------------------------------------------------------------------------------
+__global__ void gather_kernel(const uint64_t *__restrict__ words, int32_t n_words, int32_t hkv,
+                              int32_t num_blocks, size_t page_bytes, const uint8_t *k_pool,
+                              const uint8_t *v_pool, uint8_t *k_out, uint8_t *v_out,
+                              uint32_t *fields, int32_t *err) {
+  const int32_t w = blockIdx.x;
+  if (w >= n_words) return;
+  const uint64_t word = words[w];
+  uint32_t blk = word_block(word);
+  if (threadIdx.x == 0) {
+    fields[3 * w + 0] = blk;
+    fields[3 * w + 1] = word_offset(word);
+    fields[3 * w + 2] = word_nvalid(word);
+  }
+  if (blk >= (uint32_t)num_blocks) {
+    if (threadIdx.x == 0) set_error(err, LAZY_DEVERR_BAD_PAGE);
+    blk = 0;
+  }
+  const size_t per_word = page_bytes * hkv;
+  const uint4 *ks = reinterpret_cast<const uint4 *>(k_pool + (size_t)blk * per_word);
+  const uint4 *vs = reinterpret_cast<const uint4 *>(v_pool + (size_t)blk * per_word);
+  uint4 *kd = reinterpret_cast<uint4 *>(k_out + (size_t)w * per_word);
+  uint4 *vd = reinterpret_cast<uint4 *>(v_out + (size_t)w * per_word);
+  for (size_t i = threadIdx.x; i < per_word / 16; i += blockDim.x) {
+    kd[i] = ks[i];
+    vd[i] = vs[i];
+  }
+}
+
+}  // namespace
+}  // namespace lazy
+
+using namespace lazy;
+
+extern "C" int kv_pool_insert_doc(lazy_pool *p, const void *k_raw, const void *v,
+                                  int32_t n_tokens, int32_t local_pos0, int32_t *block_ids,
+                                  int32_t *n_blocks, int32_t max_blocks, lazy_stream_t stream) {
+  if (!p || n_tokens < 0 || local_pos0 < 0 || !n_blocks || *n_blocks < 0 || max_blocks < 0)
+    return LAZY_ERR_INVALID_ARG;
+  if (n_tokens > 0 && (!k_raw || !v || !block_ids)) return LAZY_ERR_INVALID_ARG;
+  if (((uintptr_t)k_raw & 15) || ((uintptr_t)v & 15)) return LAZY_ERR_INVALID_ARG;
+  if (n_tokens == 0) return LAZY_OK;
+  const int64_t end = (int64_t)local_pos0 + n_tokens;
+  if (end > (1ll << 26)) return LAZY_ERR_INVALID_ARG;
+  const int32_t need = (int32_t)((end + kPage - 1) / kPage);
+  if (need > max_blocks || *n_blocks > max_blocks) return LAZY_ERR_INVALID_ARG;
+  int rc = ensure_device(p);
+  if (rc != LAZY_OK) return rc;
+  for (int32_t i = 0; i < std::min(*n_blocks, need); ++i)
+    if (block_ids[i] < 0 || block_ids[i] >= p->num_blocks) return LAZY_ERR_INVALID_ARG;
+  if (need > *n_blocks) {
+    rc = kv_pool_alloc(p, need - *n_blocks, block_ids + *n_blocks);
+    if (rc != LAZY_OK) return rc;
+    *n_blocks = need;
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  const int32_t first_page = local_pos0 / kPage, last_page = (int32_t)((end - 1) / kPage);
+  for (int32_t pg = first_page; pg <= last_page; pg += kMaxIdsPerLaunch) {
+    BlockList bl;
+    bl.first_page = pg;
+    bl.n = std::min(kMaxIdsPerLaunch, last_page - pg + 1);
+    for (int i = 0; i < bl.n; ++i) bl.ids[i] = block_ids[pg + i];
+    const int64_t pos_lo = std::max<int64_t>(local_pos0, (int64_t)pg * kPage);
+    const int64_t pos_hi = std::min<int64_t>(end, (int64_t)(pg + bl.n) * kPage);
+    rc = dispatch_encode(p, k_raw, v, (int32_t)(pos_hi - local_pos0) - (int32_t)(pos_lo - local_pos0),
+                         (int32_t)(pos_lo - local_pos0), local_pos0, bl, nullptr, nullptr, s);
+    if (rc != LAZY_OK) return rc;
+  }
+  return LAZY_OK;
+}
+
+// Scattered encode: token t goes to slot_mapping[t] with local position local_pos[t].
+extern "C" int kv_pool_write_tokens(lazy_pool *p, const void *k_raw, const void *v,
+                                    int32_t n_tokens, const int32_t *slot_mapping,
+                                    const int32_t *local_pos, lazy_stream_t stream) {
+  if (!p || n_tokens < 0) return LAZY_ERR_INVALID_ARG;
+  if (n_tokens == 0) return LAZY_OK;
+  if (!k_raw || !v || !slot_mapping || !local_pos) return LAZY_ERR_INVALID_ARG;
+  if (((uintptr_t)k_raw & 15) || ((uintptr_t)v & 15)) return LAZY_ERR_INVALID_ARG;
+  int rc = ensure_device(p);
+  if (rc != LAZY_OK) return rc;
+  BlockList bl;
+  bl.first_page = 0;
+  bl.n = 0;
+  return dispatch_encode(p, k_raw, v, n_tokens, 0, 0, bl, slot_mapping, local_pos,
+                         (cudaStream_t)stream);
+}
+
+extern "C" int lazy_debug_gather(lazy_pool *p, const uint64_t *words, int32_t n_words,
+                                 void *k_out, void *v_out, uint32_t *fields,
+                                 lazy_stream_t stream) {
+  if (!p || n_words < 0) return LAZY_ERR_INVALID_ARG;
+  if (n_words == 0) return LAZY_OK;
+  if (!words || !k_out || !v_out || !fields) return LAZY_ERR_INVALID_ARG;
+  if (((uintptr_t)k_out & 15) || ((uintptr_t)v_out & 15)) return LAZY_ERR_INVALID_ARG;
+  int rc = ensure_device(p);
+  if (rc != LAZY_OK) return rc;
+  const size_t page_bytes = (size_t)p->page_size * p->d * elem_bytes(p->dtype);
+  gather_kernel<<<n_words, 256, 0, (cudaStream_t)stream>>>(
+      words, n_words, p->hkv, p->num_blocks, page_bytes, (const uint8_t *)p->k,
+      (const uint8_t *)p->v, (uint8_t *)k_out, (uint8_t *)v_out, fields, p->d_err);
+  LAZY_CUDA_TRY(cudaGetLastError());
+  return LAZY_OK;
+}

@@ -1,0 +1,50 @@
+// Host-side pool state shared by the translation units of the library (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+#include <vector>
+
+#include "lazy_attn.h"
+
+struct lazy_pool {
+  void *k = nullptr;
+  void *v = nullptr;
+  int32_t num_blocks = 0, page_size = 0, hkv = 0, d = 0, dtype = 0;
+  double base = 0.0;
+
+  std::mutex mu;                    // guards the allocator and lazy device set-up
+  std::vector<int32_t> free_list;   // stack of free block ids (top = back)
+  std::vector<int32_t> refcount;    // per block
+  std::vector<uint64_t> turn;       // frac(theta_i / 2pi) * 2^64, i < d/2
+
+  bool dev_ready = false;
+  int device = -1;
+  int num_sms = 0;
+  int32_t *d_err = nullptr;         // device error word
+  uint64_t *d_turn = nullptr;       // device copy of `turn`
+  uint64_t wait_limit_ns = 2000000000ull;
+
+  // Tensor maps of the page buffers for the tensor-core prefill (built lazily).
+  bool tmaps_ready = false;
+  alignas(64) unsigned char tmap_k[128];
+  alignas(64) unsigned char tmap_v[128];
+};
+
+namespace lazy {
+int record_cuda(cudaError_t e, const char *what);
+void record_msg(const char *msg);
+int ensure_device(lazy_pool *p);
+inline size_t elem_bytes(int32_t dtype) { return dtype == LAZY_DTYPE_BF16 ? 2 : 4; }
+inline size_t pool_bytes(const lazy_pool *p) {
+  return (size_t)p->num_blocks * p->hkv * p->page_size * p->d * elem_bytes(p->dtype);
+}
+}  // namespace lazy
+
+#define LAZY_CUDA_TRY(call)                                      \
+  do {                                                           \
+    cudaError_t e_ = (call);                                     \
+    if (e_ != cudaSuccess) return lazy::record_cuda(e_, #call);  \
+  } while (0)

@@ -1,0 +1,35 @@
+// Parameters shared by the prefill kernels (internal).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pool_internal.h"
+
+namespace lazy {
+
+struct PrefillParams {
+  const void *q;
+  const void *k_new;
+  const void *v_new;
+  const int32_t *cu_q;
+  const int32_t *q_pos0;
+  const uint64_t *words;
+  const int32_t *cu_pages;
+  const void *k_pool;
+  const void *v_pool;
+  const uint64_t *turn;
+  void *out;
+  float *lse;
+  int32_t *err;
+  int32_t batch, hkv, hq, num_blocks, G, TQ, total_q;
+  float scale_log2;
+  uint64_t wait_ns;
+};
+
+int prefill_simt(lazy_pool *p, const PrefillParams &pp, int32_t max_q_len, cudaStream_t s);
+// Tensor-core path; LAZY_ERR_UNSUPPORTED when the shape is not built.
+int prefill_tc_supported(const lazy_pool *p, int32_t hq);
+int prefill_tc(lazy_pool *p, const PrefillParams &pp, int32_t max_q_len, cudaStream_t s);
+
+}  // namespace lazy

@@ -1,0 +1,203 @@
+"""Turn a seeded workload (``workload.Workload``) into device state for the library: a resident
+pool holding each retrieved document once, page tables with (block, offset, n_valid) words, and
+the per-request device inputs of a prefill or decode call. Used by the tests, the bench and the
+smoke check; every computation on the path itself happens in the library's kernels.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Dict, List, Optional
+
+import numpy as np
+
+from . import (LazyPool, build_page_table, kv_pool_insert_doc)
+
+
+def _torch_dtype(wl):
+    import torch
+    return torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+
+
+class HostSource:
+    """Host arrays of the workload (numpy float32, bf16-exact for bf16 workloads)."""
+
+    def __init__(self, wl):
+        self.wl = wl
+
+    def doc_kv(self, d, device):
+        import torch
+        dt = _torch_dtype(self.wl)
+        return (torch.from_numpy(self.wl.doc_k(d)).to(device=device, dtype=dt),
+                torch.from_numpy(self.wl.doc_v(d)).to(device=device, dtype=dt))
+
+    def q(self, b, device):
+        import torch
+        return torch.from_numpy(self.wl.q(b)).to(device=device, dtype=_torch_dtype(self.wl))
+
+    def new_kv(self, b, device):
+        import torch
+        dt = _torch_dtype(self.wl)
+        return (torch.from_numpy(self.wl.new_k(b)).to(device=device, dtype=dt),
+                torch.from_numpy(self.wl.new_v(b)).to(device=device, dtype=dt))
+
+
+class DeviceSource:
+    """Device-side draws (``workload.normal_torch``) for workloads too large to draw on the host.
+    ``host_view()`` exposes the same tensors to the oracle (copied back) for sampled checks."""
+
+    def __init__(self, wl):
+        self.wl = wl
+        self._docs: Dict[int, tuple] = {}
+        self._q: Dict[int, object] = {}
+        self._new: Dict[int, tuple] = {}
+
+    def doc_kv(self, d, device):
+        if d not in self._docs:
+            self._docs[d] = self.wl.doc_kv_torch(d, device)
+        return self._docs[d]
+
+    def q(self, b, device):
+        if b not in self._q:
+            self._q[b] = self.wl.q_torch(b, device)
+        return self._q[b]
+
+    def new_kv(self, b, device):
+        if b not in self._new:
+            self._new[b] = self.wl.new_kv_torch(b, device)
+        return self._new[b]
+
+    def forget_docs(self):
+        """Drop the raw document tensors once encoded (the pool holds the cache)."""
+        self._docs.clear()
+
+    def host_view(self, device="cuda"):
+        src = self
+
+        def h(t):
+            return t.float().cpu().numpy()
+
+        class View:
+            def doc_k(self, d): return h(src.doc_kv(d, device)[0])
+            def doc_v(self, d): return h(src.doc_kv(d, device)[1])
+            def q(self, b): return h(src.q(b, device))
+            def new_k(self, b): return h(src.new_kv(b, device)[0])
+            def new_v(self, b): return h(src.new_kv(b, device)[1])
+        return View()
+
+
+@dataclasses.dataclass
+class Resident:
+    pool: LazyPool
+    doc_blocks: Dict[int, List[int]]
+    priv_blocks: Dict[int, List[int]]
+
+
+def pool_blocks_needed(wl, resident_pool: bool = True) -> int:
+    per_doc = -(-wl.doc_len // wl.page_size)
+    n_docs = wl.n_pool_docs if resident_pool else len(wl.used_docs())
+    priv = sum(-(-r.priv_len // wl.page_size) for r in wl.decode_requests())
+    return n_docs * per_doc + priv
+
+
+def build_resident(wl, src, device="cuda", resident_pool: bool = True, stream=None,
+                   drop_raw: bool = True) -> Resident:
+    """Create the pool (sized for the whole document pool when ``resident_pool``) and encode every
+    document some request retrieved, once, plus each decode request's private segment."""
+    import torch
+    pool = LazyPool(pool_blocks_needed(wl, resident_pool), wl.Hkv, wl.D, _torch_dtype(wl),
+                    wl.rope_base, wl.page_size, device)
+    doc_blocks: Dict[int, List[int]] = {}
+    for d in wl.used_docs():
+        k, v = src.doc_kv(d, device)
+        doc_blocks[d] = kv_pool_insert_doc(pool, k, v, 0, None, stream)
+    priv_blocks: Dict[int, List[int]] = {}
+    for r in wl.decode_requests():
+        k, v = src.new_kv(r.index, device)
+        priv_blocks[r.index] = kv_pool_insert_doc(pool, k, v, 0, None, stream)
+    torch.cuda.synchronize()
+    if drop_raw and hasattr(src, "forget_docs"):
+        src.forget_docs()
+    return Resident(pool, doc_blocks, priv_blocks)
+
+
+def page_table(wl, res: Resident, reqs, with_private: bool):
+    segs = []
+    for r in reqs:
+        s = [(res.doc_blocks[d], o, wl.doc_len) for d, o in zip(r.docs, r.offsets)]
+        if with_private:
+            s.append((res.priv_blocks[r.index], r.priv_offset, r.priv_len))
+        segs.append(s)
+    return build_page_table(segs, wl.page_size)
+
+
+@dataclasses.dataclass
+class DecodeBatch:
+    reqs: list
+    q: object
+    q_pos: object
+    words: object
+    cu_pages: object
+    # the new token of each request (last slot of its private segment) for the append step
+    new_k: object
+    new_v: object
+    slot_mapping: object
+    local_pos: object
+    n_keys: int
+
+
+def decode_batch(wl, res: Resident, src, device="cuda", reqs=None) -> DecodeBatch:
+    import torch
+    reqs = reqs if reqs is not None else wl.decode_requests()
+    words, cu = page_table(wl, res, reqs, with_private=True)
+    q = torch.cat([src.q(r.index, device) for r in reqs], dim=0).contiguous()
+    q_pos = torch.tensor([r.m for r in reqs], dtype=torch.int32, device=device)
+    nk, nv, slots, lpos = [], [], [], []
+    for r in reqs:
+        k, v = src.new_kv(r.index, device)
+        j = r.priv_len - 1
+        nk.append(k[j:j + 1]); nv.append(v[j:j + 1])
+        blk = res.priv_blocks[r.index][j // wl.page_size]
+        slots.append(blk * wl.page_size + j % wl.page_size)
+        lpos.append(j)
+    n_keys = sum(len(r.docs) * wl.doc_len + r.priv_len for r in reqs)
+    return DecodeBatch(
+        reqs, q, q_pos,
+        torch.from_numpy(words.view(np.int64)).to(device),
+        torch.from_numpy(cu).to(device),
+        torch.cat(nk).contiguous(), torch.cat(nv).contiguous(),
+        torch.tensor(slots, dtype=torch.int32, device=device),
+        torch.tensor(lpos, dtype=torch.int32, device=device), n_keys)
+
+
+@dataclasses.dataclass
+class PrefillBatch:
+    reqs: list
+    q: object
+    k_new: object
+    v_new: object
+    cu_q: object
+    q_pos0: object
+    words: object
+    cu_pages: object
+    total_q: int
+    max_q_len: int
+    flops: float   # causal-visible QK^T and PV FLOPs
+
+
+def prefill_batch(wl, res: Resident, src, device="cuda", reqs=None) -> PrefillBatch:
+    import torch
+    reqs = reqs if reqs is not None else wl.prefill_requests()
+    words, cu = page_table(wl, res, reqs, with_private=False)
+    q = torch.cat([src.q(r.index, device) for r in reqs], dim=0).contiguous()
+    kn = torch.cat([src.new_kv(r.index, device)[0] for r in reqs], dim=0).contiguous()
+    vn = torch.cat([src.new_kv(r.index, device)[1] for r in reqs], dim=0).contiguous()
+    cu_q = np.concatenate([[0], np.cumsum([r.T for r in reqs])]).astype(np.int32)
+    flops = 0.0
+    for r in reqs:
+        n_doc = len(r.docs) * wl.doc_len
+        flops += 4.0 * wl.D * wl.Hq * (r.T * n_doc + r.T * (r.T + 1) / 2)
+    return PrefillBatch(
+        reqs, q, kn, vn, torch.from_numpy(cu_q).to(device),
+        torch.tensor([r.q_pos0 for r in reqs], dtype=torch.int32, device=device),
+        torch.from_numpy(words.view(np.int64)).to(device), torch.from_numpy(cu).to(device),
+        int(cu_q[-1]), max(r.T for r in reqs), flops)

@@ -1,0 +1,304 @@
+"""GPU parity: the library's kernels (through the C ABI) against the fp64 oracle.
+
+Tolerances (fixed by the contract of this path): bf16 pools 2e-2 absolute on outputs and 1e-3
+absolute on log-sum-exp; fp32 pools 1e-5 on both; page-word and page indexing bit-exact.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import workload as W
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+def _tol(wl):
+    return (2e-2, 1e-3) if wl.dtype == "bf16" else (1e-5, 1e-5)
+
+
+@pytest.fixture(scope="module")
+def pk(lazylib, cuda_ok):
+    import position_independent_kv_lazy_gb300 as m
+    return m
+
+
+def _h():
+    from position_independent_kv_lazy_gb300 import harness
+    return harness
+
+
+def _decode(pk, wl, src=None, grid_ctas=0):
+    H = _h()
+    src = src or H.HostSource(wl)
+    res = H.build_resident(wl, src, resident_pool=False)
+    db = H.decode_batch(wl, res, src)
+    out, lse = pk.lazy_attn_decode(res.pool, db.q, db.q_pos, db.words, db.cu_pages,
+                                   sm_scale=wl.sm_scale, grid_ctas=grid_ctas)
+    torch.cuda.synchronize()
+    assert pk.lazy_get_device_error(res.pool) == 0
+    return res, db, out.float().cpu().numpy(), lse.cpu().numpy()
+
+
+def _check_decode(wl, out, lse, reqs=None, kv_heads=None, src=None):
+    to, tl = _tol(wl)
+    reqs = reqs if reqs is not None else range(wl.batch)
+    G = wl.Hq // wl.Hkv
+    for i, b in enumerate(reqs):
+        ro, rl = oracle.attend_request(wl, b, kv_heads=kv_heads, src=src)
+        heads = range(wl.Hq) if kv_heads is None else [h * G + g for h in kv_heads for g in range(G)]
+        heads = list(heads)
+        do = np.abs(out[i][heads] - ro[0][heads]).max()
+        dl = np.abs(lse[i][heads] - rl[0][heads]).max()
+        assert do <= to, (b, do)
+        assert dl <= tl, (b, dl)
+
+
+def _edge_decode_workload(D, Hq, Hkv, dtype, doc_len=40):
+    # gaps, an overlap, the same doc at two offsets, offset 0, ragged private segments
+    segs = [[(0, 0), (1, 40), (2, 80)],
+            [(2, 5), (0, 300), (2, 1000)],
+            [(1, 0)],
+            [(3, 77), (0, 77)]]
+    priv = [(120, 9), (1040, 16), (40, 33), (117, 1)]
+    return W.custom("decode", segs, doc_len=doc_len, n_pool=4, Hq=Hq, Hkv=Hkv, D=D, dtype=dtype,
+                    base=500000.0 if D == 128 else 10000.0, priv=priv, seed=3)
+
+
+# ------------------------------------------------------------------ indexing (bit-exact)
+def test_debug_gather_indexing_bit_exact(pk):
+    H = _h()
+    wl = _edge_decode_workload(128, 8, 2, "bf16")
+    src = H.HostSource(wl)
+    res = H.build_resident(wl, src, resident_pool=False)
+    db = H.decode_batch(wl, res, src)
+    k, v, f = pk.lazy_debug_gather(res.pool, db.words)
+    torch.cuda.synchronize()
+    words = db.words.cpu().numpy().view(np.uint64)
+    f = f.cpu().numpy().view(np.uint32)
+    for i, w in enumerate(words):
+        assert tuple(f[i]) == oracle.unpack_page(int(w))
+    blk = torch.from_numpy(f[:, 0].astype(np.int64)).cuda()
+    assert torch.equal(k, res.pool.k_pages[blk]) and torch.equal(v, res.pool.v_pages[blk])
+    # V pages are verbatim copies of the raw values; K pages hold R(j) k at local positions
+    d = wl.requests[0].docs[1]
+    ids = res.doc_blocks[d]
+    vr = wl.doc_v(d)
+    kr = wl.doc_k(d)
+    for j in range(wl.doc_len):
+        gv = res.pool.v_pages[ids[j // 16], :, j % 16].float().cpu().numpy()
+        assert np.array_equal(gv, vr[j])
+        gk = res.pool.k_pages[ids[j // 16], :, j % 16].float().cpu().numpy()
+        for h in range(wl.Hkv):
+            exact = oracle.rope(kr[j, h], j, wl.rope_base)
+            assert np.abs(gk[h] - exact).max() <= 2 ** -8 * max(1.0, np.abs(exact).max())
+    assert pk.lazy_get_device_error(res.pool) == 0
+
+
+# ------------------------------------------------------------------ decode
+@pytest.mark.parametrize("D,Hq,Hkv,dtype", [
+    (128, 32, 8, "bf16"), (128, 8, 8, "bf16"), (64, 16, 8, "bf16"), (64, 16, 2, "bf16"),
+    (128, 32, 2, "bf16"), (64, 8, 2, "fp32"), (128, 4, 1, "fp32")])
+def test_decode_parity_edge_layouts(pk, D, Hq, Hkv, dtype):
+    wl = _edge_decode_workload(D, Hq, Hkv, dtype)
+    _, _, out, lse = _decode(pk, wl)
+    _check_decode(wl, out, lse)
+
+
+@pytest.mark.parametrize("grid", [1, 2, 5, 37, 1000])
+def test_decode_any_grid_same_result(pk, grid):
+    wl = W.decode_workload(batch=5, docs_per_req=3, doc_len=100, n_pool=6, question=21, seed=1)
+    _, _, out, lse = _decode(pk, wl, grid_ctas=grid)
+    _check_decode(wl, out, lse)
+
+
+def test_decode_request_without_keys(pk):
+    H = _h()
+    wl = _edge_decode_workload(128, 8, 2, "bf16")
+    src = H.HostSource(wl)
+    res = H.build_resident(wl, src, resident_pool=False)
+    db = H.decode_batch(wl, res, src)
+    # request 1 keeps no page: its rows must be 0 with lse = -inf; the others are unaffected
+    cu = db.cu_pages.cpu().numpy()
+    words = db.words.cpu().numpy()
+    keep = np.r_[0:cu[1], cu[2]:cu[-1]]
+    cu2 = cu.copy()
+    cu2[2:] -= cu[2] - cu[1]
+    out, lse = pk.lazy_attn_decode(res.pool, db.q, db.q_pos,
+                                   torch.from_numpy(words[keep]).cuda(),
+                                   torch.from_numpy(cu2).cuda(), sm_scale=wl.sm_scale)
+    torch.cuda.synchronize()
+    out = out.float().cpu().numpy()
+    lse = lse.cpu().numpy()
+    assert np.all(out[1] == 0) and np.all(np.isneginf(lse[1]))
+    _check_decode(wl, out[[0, 2, 3]], lse[[0, 2, 3]], reqs=[0, 2, 3])
+
+
+def test_decode_shift_invariance(pk):
+    wl = _edge_decode_workload(128, 8, 2, "bf16")
+    _, _, out0, lse0 = _decode(pk, wl)
+    for r in wl.requests:
+        r.offsets = [o + 123457 for o in r.offsets]
+        r.priv_offset += 123457
+        r.m += 123457
+    _, _, out1, lse1 = _decode(pk, wl)
+    assert np.abs(out0 - out1).max() <= 2e-2 and np.abs(lse0 - lse1).max() <= 1e-3
+    _check_decode(wl, out1, lse1)
+
+
+def test_decode_after_token_append(pk):
+    # the bench's step: write the new token's k/v into its slot, then decode
+    H = _h()
+    wl = W.decode_workload(batch=6, docs_per_req=2, doc_len=64, n_pool=5, question=30, seed=2)
+    src = H.HostSource(wl)
+    res = H.build_resident(wl, src, resident_pool=False)
+    db = H.decode_batch(wl, res, src)
+    for b in range(wl.batch):   # scribble over the new-token slot first
+        blk = res.priv_blocks[b][(wl.requests[b].priv_len - 1) // 16]
+        res.pool.k_pages[blk, :, (wl.requests[b].priv_len - 1) % 16] = 7.0
+    pk.kv_pool_write_tokens(res.pool, db.new_k, db.new_v, db.slot_mapping, db.local_pos)
+    out, lse = pk.lazy_attn_decode(res.pool, db.q, db.q_pos, db.words, db.cu_pages,
+                                   sm_scale=wl.sm_scale)
+    torch.cuda.synchronize()
+    _check_decode(wl, out.float().cpu().numpy(), lse.cpu().numpy())
+
+
+def test_decode_full_size_sampled(pk):
+    # 64 requests x 4161 keys, 32/8/128 bf16, in the bench's launch configuration
+    H = _h()
+    wl = W.decode_workload()
+    src = H.DeviceSource(wl)
+    res = H.build_resident(wl, src, drop_raw=False)
+    db = H.decode_batch(wl, res, src)
+    out, lse = pk.lazy_attn_decode(res.pool, db.q, db.q_pos, db.words, db.cu_pages,
+                                   sm_scale=wl.sm_scale)
+    torch.cuda.synchronize()
+    assert pk.lazy_get_device_error(res.pool) == 0
+    out = out.float().cpu().numpy()
+    lse = lse.cpu().numpy()
+    reqs = [0, 17, 63]
+    _check_decode(wl, out[reqs], lse[reqs], reqs=reqs, kv_heads=[0, 5], src=src.host_view())
+
+
+def test_long_decode_full_size_sampled(pk):
+    # 16 requests x 131073 keys (64 docs of 2048), split-KV across the whole GPU
+    H = _h()
+    wl = W.long_decode_workload()
+    src = H.DeviceSource(wl)
+    res = H.build_resident(wl, src, drop_raw=False)
+    db = H.decode_batch(wl, res, src)
+    out, lse = pk.lazy_attn_decode(res.pool, db.q, db.q_pos, db.words, db.cu_pages,
+                                   sm_scale=wl.sm_scale)
+    torch.cuda.synchronize()
+    assert pk.lazy_get_device_error(res.pool) == 0
+    out = out.float().cpu().numpy()
+    lse = lse.cpu().numpy()
+    _check_decode(wl, out[[9]], lse[[9]], reqs=[9], kv_heads=[3], src=src.host_view())
+
+
+# ------------------------------------------------------------------ device-detected errors
+def test_bad_page_word_sets_flag_without_fault(pk):
+    H = _h()
+    wl = _edge_decode_workload(128, 8, 2, "bf16")
+    src = H.HostSource(wl)
+    res = H.build_resident(wl, src, resident_pool=False)
+    db = H.decode_batch(wl, res, src)
+    words = db.words.clone()
+    words[3] = int(pk.lazy_pack_page(res.pool.num_blocks + 5, 0, 16))
+    pk.lazy_attn_decode(res.pool, db.q, db.q_pos, words, db.cu_pages, sm_scale=wl.sm_scale)
+    assert pk.lazy_get_device_error(res.pool) & pk.LAZY_DEVERR_BAD_PAGE
+    assert pk.lazy_get_device_error(res.pool) == 0          # read-and-clear
+    out, lse = pk.lazy_attn_decode(res.pool, db.q, db.q_pos, db.words, db.cu_pages,
+                                   sm_scale=wl.sm_scale)
+    torch.cuda.synchronize()
+    _check_decode(wl, out.float().cpu().numpy(), lse.cpu().numpy())
+
+
+def test_expired_wait_sets_flag_and_context_survives(pk):
+    H = _h()
+    wl = W.decode_workload(batch=16, docs_per_req=4, doc_len=512, n_pool=8, question=8, seed=4)
+    src = H.HostSource(wl)
+    res = H.build_resident(wl, src, resident_pool=False)
+    db = H.decode_batch(wl, res, src)
+    pk.lazy_pool_set_wait_limit(res.pool, 1)   # 1 ns: the first wait for a page gives up
+    pk.lazy_attn_decode(res.pool, db.q, db.q_pos, db.words, db.cu_pages, sm_scale=wl.sm_scale)
+    assert pk.lazy_get_device_error(res.pool) & pk.LAZY_DEVERR_TIMEOUT
+    pk.lazy_pool_set_wait_limit(res.pool, 2_000_000_000)
+    out, lse = pk.lazy_attn_decode(res.pool, db.q, db.q_pos, db.words, db.cu_pages,
+                                   sm_scale=wl.sm_scale)
+    torch.cuda.synchronize()
+    assert pk.lazy_get_device_error(res.pool) == 0
+    _check_decode(wl, out.float().cpu().numpy(), lse.cpu().numpy(), reqs=range(4))
+
+
+# ------------------------------------------------------------------ prefill
+def _prefill(pk, wl, flags, src=None):
+    H = _h()
+    src = src or H.HostSource(wl)
+    res = H.build_resident(wl, src, resident_pool=False, drop_raw=False)
+    pb = H.prefill_batch(wl, res, src)
+    out, lse = pk.lazy_attn_prefill(res.pool, pb.q, pb.k_new, pb.v_new, pb.cu_q, pb.q_pos0,
+                                    pb.words, pb.cu_pages, pb.max_q_len, sm_scale=wl.sm_scale,
+                                    flags=flags)
+    torch.cuda.synchronize()
+    assert pk.lazy_get_device_error(res.pool) == 0
+    return res, pb, out.float().cpu().numpy(), lse.cpu().numpy()
+
+
+def _check_prefill(wl, pb, out, lse, reqs=None, kv_heads=None, queries=None, src=None):
+    to, tl = _tol(wl)
+    cu = pb.cu_q.cpu().numpy()
+    G = wl.Hq // wl.Hkv
+    reqs = range(wl.batch) if reqs is None else reqs
+    for b in reqs:
+        ro, rl = oracle.attend_request(wl, b, kv_heads=kv_heads, queries=queries, src=src)
+        rows = np.arange(cu[b], cu[b + 1])
+        qi = np.arange(len(rows)) if queries is None else np.asarray(queries)
+        heads = list(range(wl.Hq)) if kv_heads is None else \
+            [h * G + g for h in kv_heads for g in range(G)]
+        o = out[rows[qi]][:, heads]
+        l = lse[rows[qi]][:, heads]
+        do = np.abs(o - ro[qi][:, heads]).max()
+        dl = np.abs(l - rl[qi][:, heads]).max()
+        assert do <= to, (b, do)
+        assert dl <= tl, (b, dl)
+
+
+def test_prefill_tiny_fp32_matches_oracle_and_golden(pk):
+    import json, os
+    wl = W.tiny_fp32()
+    _, pb, out, lse = _prefill(pk, wl, pk.LAZY_PREFILL_AUTO)
+    _check_prefill(wl, pb, out, lse)
+    with open(os.path.join(os.path.dirname(__file__), "golden", "tiny_fp32_oracle.json")) as f:
+        g = json.load(f)
+    assert np.abs(out - np.array(g["out"])).max() <= 1e-5
+    assert np.abs(lse - np.array(g["lse"])).max() <= 1e-5
+
+
+def _edge_prefill_workload(D, Hq, Hkv, dtype):
+    segs = [[(0, 0), (1, 40), (0, 200)], [(2, 3)], [(1, 1000), (2, 17), (0, 5000)]]
+    return W.custom("prefill", segs, doc_len=40, n_pool=3, Hq=Hq, Hkv=Hkv, D=D, dtype=dtype,
+                    base=500000.0 if D == 128 else 10000.0, T=[37, 5, 130],
+                    q_pos0=[240, 43, 5040], seed=5)
+
+
+@pytest.mark.parametrize("D,Hq,Hkv,dtype", [
+    (128, 32, 8, "bf16"), (64, 8, 8, "bf16"), (128, 16, 2, "bf16"), (64, 4, 1, "fp32"),
+    (128, 8, 2, "fp32")])
+def test_prefill_simt_parity(pk, D, Hq, Hkv, dtype):
+    wl = _edge_prefill_workload(D, Hq, Hkv, dtype)
+    _, pb, out, lse = _prefill(pk, wl, pk.LAZY_PREFILL_SIMT)
+    _check_prefill(wl, pb, out, lse)
+
+
+def test_prefill_full_size_sampled(pk):
+    # 8 requests x (16 docs x 1024 + 256 causal question tokens), 32/8/128 bf16
+    H = _h()
+    wl = W.prefill_workload()
+    src = H.DeviceSource(wl)
+    _, pb, out, lse = _prefill(pk, wl, pk.LAZY_PREFILL_AUTO, src=src)
+    _check_prefill(wl, pb, out, lse, reqs=[0, 5], kv_heads=[2, 7],
+                   queries=[0, 1, 63, 64, 127, 128, 200, 255], src=src.host_view())
