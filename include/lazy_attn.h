@@ -223,6 +223,13 @@ int lazy_get_device_error(lazy_pool *pool, int32_t *err, lazy_stream_t stream);
 int lazy_debug_gather(lazy_pool *pool, const uint64_t *d_page_words, int32_t n_words,
                       void *d_k_out, void *d_v_out, uint32_t *d_fields, lazy_stream_t stream);
 
+/*
+ * Test hook for the bounded-wait path: one warp waits on a shared-memory barrier that nothing
+ * arrives at, with the same bounded wait the kernels use and a limit of limit_ns; when it gives
+ * up it sets LAZY_DEVERR_TIMEOUT and returns. The context stays usable.
+ */
+int lazy_debug_wait_timeout(lazy_pool *pool, uint64_t limit_ns, lazy_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

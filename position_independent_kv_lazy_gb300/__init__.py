@@ -40,7 +40,7 @@ EXPORTS = [
     "kv_pool_release", "kv_pool_num_free", "kv_pool_refcount", "kv_pool_insert_doc",
     "kv_pool_write_tokens", "lazy_pack_page", "lazy_unpack_page", "lazy_pack_pages",
     "lazy_decode_workspace_bytes", "lazy_attn_decode", "lazy_prefill_workspace_bytes",
-    "lazy_attn_prefill", "lazy_get_device_error", "lazy_debug_gather",
+    "lazy_attn_prefill", "lazy_get_device_error", "lazy_debug_gather", "lazy_debug_wait_timeout",
 ]
 
 
@@ -93,6 +93,7 @@ _SIGS = {
                            _vp, _vp, _vp, ctypes.c_size_t, _i32, _vp], ctypes.c_int),
     "lazy_get_device_error": ([_vp, _pi32, _vp], ctypes.c_int),
     "lazy_debug_gather": ([_vp, _vp, _i32, _vp, _vp, _vp, _vp], ctypes.c_int),
+    "lazy_debug_wait_timeout": ([_vp, _u64, _vp], ctypes.c_int),
 }
 
 
@@ -348,3 +349,8 @@ def lazy_debug_gather(pool: LazyPool, page_words, stream=None):
     _check("lazy_debug_gather", load_library().lazy_debug_gather(
         pool.handle, _ptr(page_words), n, _ptr(k), _ptr(v), _ptr(f), _stream(stream)))
     return k, v, f
+
+
+def lazy_debug_wait_timeout(pool: LazyPool, limit_ns: int, stream=None):
+    _check("lazy_debug_wait_timeout", load_library().lazy_debug_wait_timeout(
+        pool.handle, limit_ns, _stream(stream)))

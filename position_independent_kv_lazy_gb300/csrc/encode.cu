@@ -136,10 +136,31 @@ __global__ void gather_kernel(const uint64_t *__restrict__ words, int32_t n_word
   }
 }
 
+// Waits on a barrier that nothing arrives at; gives up after limit_ns (bounded wait).
+__global__ void wait_timeout_kernel(uint64_t limit_ns, int32_t *err) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+  const bool ok = mbar_wait(&bar, 0, limit_ns);
+  if (!ok && threadIdx.x == 0) set_error(err, LAZY_DEVERR_TIMEOUT);
+}
+
 }  // namespace
 }  // namespace lazy
 
 using namespace lazy;
+
+extern "C" int lazy_debug_wait_timeout(lazy_pool *p, uint64_t limit_ns, lazy_stream_t stream) {
+  if (!p || limit_ns == 0 || limit_ns > 10000000000ull) return LAZY_ERR_INVALID_ARG;
+  int rc = ensure_device(p);
+  if (rc != LAZY_OK) return rc;
+  wait_timeout_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(limit_ns, p->d_err);
+  LAZY_CUDA_TRY(cudaGetLastError());
+  return LAZY_OK;
+}
 
 extern "C" int kv_pool_insert_doc(lazy_pool *p, const void *k_raw, const void *v,
                                   int32_t n_tokens, int32_t local_pos0, int32_t *block_ids,
