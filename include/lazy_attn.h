@@ -109,7 +109,7 @@ int kv_pool_num_free(lazy_pool *pool, int32_t *n_free);
 int kv_pool_refcount(lazy_pool *pool, int32_t block_id, int32_t *refcount);
 
 /*
- * Encode one segment's tokens into the pool (north-star step "doc-KV encode"; the cache keeps
+ * Encode one segment's tokens into the pool (the doc-KV encode step; the cache keeps
  * position-free content, summaries' core concept): for the tokens at document-local positions
  * j = local_pos0 .. local_pos0 + n_tokens - 1,
  *     K page row  = R(j) k_raw[t]   (fp32 arithmetic, rounded to the pool dtype, RNE)
@@ -148,7 +148,7 @@ int lazy_pack_pages(int32_t n, const uint32_t *block_ids, const uint32_t *offset
 
 /* ---------------------------------------------------------------------------------------
  * Decode (summaries' decoding part: M = 1, rotation fused in the inner loop, q re-rotated only
- * when the offset changes at a document boundary; spec: split-KV GQA decode streaming
+ * when the offset changes at a document boundary; here a split-KV GQA decode streaming
  * pages, warp-shuffle reductions, log-sum-exp combine)
  * --------------------------------------------------------------------------------------- */
 /*
