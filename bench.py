@@ -209,28 +209,35 @@ def bench_ours(args):
         h_out.copy_(out, non_blocking=True)
         h_lse.copy_(lse, non_blocking=True)
 
+    only_decode = args.only == "decode"
+
     # ---------------- prefill workload (extra object)
-    pwl = W.prefill_workload()
-    psrc = H.DeviceSource(pwl)
-    pres = H.build_resident(pwl, psrc)
-    pb = H.prefill_batch(pwl, pres, psrc)
-    pout = torch.empty_like(pb.q)
-    plse = torch.empty((pb.total_q, pwl.Hq), dtype=torch.float32, device="cuda")
+    pwl = W.prefill_workload() if not only_decode else None
+    pools = [res.pool]
+    if not only_decode:
+        psrc = H.DeviceSource(pwl)
+        pres = H.build_resident(pwl, psrc)
+        pb = H.prefill_batch(pwl, pres, psrc)
+        pout = torch.empty_like(pb.q)
+        plse = torch.empty((pb.total_q, pwl.Hq), dtype=torch.float32, device="cuda")
+        pools.append(pres.pool)
 
     def prefill_call():
         pk.lazy_attn_prefill(pres.pool, pb.q, pb.k_new, pb.v_new, pb.cu_q, pb.q_pos0, pb.words,
                              pb.cu_pages, pb.max_q_len, sm_scale=pwl.sm_scale, out=pout, lse=plse)
 
     # ---------------- long-context decode (extra object)
-    lwl = W.long_decode_workload()
-    lsrc = H.DeviceSource(lwl)
-    lres = H.build_resident(lwl, lsrc)
-    ldb = H.decode_batch(lwl, lres, lsrc)
-    lws = torch.empty(pk.lazy_decode_workspace_bytes(lres.pool, lwl.batch, lwl.Hq),
-                      dtype=torch.uint8, device="cuda")
-    lout = torch.empty_like(ldb.q)
-    llse = torch.empty((lwl.batch, lwl.Hq), dtype=torch.float32, device="cuda")
-    l_bytes = ldb.n_keys * lwl.kv_bytes_per_token()
+    if not only_decode:
+        lwl = W.long_decode_workload()
+        lsrc = H.DeviceSource(lwl)
+        lres = H.build_resident(lwl, lsrc)
+        ldb = H.decode_batch(lwl, lres, lsrc)
+        lws = torch.empty(pk.lazy_decode_workspace_bytes(lres.pool, lwl.batch, lwl.Hq),
+                          dtype=torch.uint8, device="cuda")
+        lout = torch.empty_like(ldb.q)
+        llse = torch.empty((lwl.batch, lwl.Hq), dtype=torch.float32, device="cuda")
+        l_bytes = ldb.n_keys * lwl.kv_bytes_per_token()
+        pools.append(lres.pool)
 
     def long_call():
         pk.lazy_attn_decode(lres.pool, ldb.q, ldb.q_pos, ldb.words, ldb.cu_pages,
@@ -238,13 +245,16 @@ def bench_ours(args):
 
     torch.cuda.synchronize()
     for _ in range(args.warmup):
-        flush(); step(); e2e_step(); prefill_call(); long_call()
+        flush(); step(); e2e_step()
+        if not only_decode:
+            prefill_call(); long_call()
     torch.cuda.synchronize()
-    for pool in (res.pool, pres.pool, lres.pool):
+    for pool in pools:
         if pk.lazy_get_device_error(pool) != 0:
             raise RuntimeError("device error during warm-up")
 
     with ClockSampler(local) as clk:
+        torch.cuda.nvtx.range_push("timed_region")
         _barrier(ws)
         torch.cuda.synchronize()
         step_ms = _timed_steps(step, args.steps, flush, stream)
@@ -252,9 +262,11 @@ def bench_ours(args):
         _barrier(ws)
         dec_ms = _timed_steps(decode_call, args.steps, flush, stream)
         e2e_ms = _timed_steps(e2e_step, args.steps, flush, stream)
-        pre_ms = _timed_steps(prefill_call, max(3, args.steps // 2), flush, stream)
-        long_ms = _timed_steps(long_call, max(3, args.steps // 2), flush, stream)
+        if not only_decode:
+            pre_ms = _timed_steps(prefill_call, max(3, args.steps // 2), flush, stream)
+            long_ms = _timed_steps(long_call, max(3, args.steps // 2), flush, stream)
         torch.cuda.synchronize()
+        torch.cuda.nvtx.range_pop()
     clocks = clk.summary()
 
     total_ms = _max_over_ranks(sum(step_ms), ws)
@@ -263,9 +275,6 @@ def bench_ours(args):
     dec_avg = sum(dec_ms) / len(dec_ms)
     achieved = kv_bytes / (dec_avg * 1e-3) / 1e9
     e2e_avg = sum(e2e_ms) / len(e2e_ms)
-    pre_avg = sum(pre_ms) / len(pre_ms)
-    long_avg = sum(long_ms) / len(long_ms)
-    tflops = pb.flops / (pre_avg * 1e-3) / 1e12
 
     traffic = None
     prof = os.path.join(ROOT, "profiles", "decode_split_traffic.json")
@@ -304,22 +313,27 @@ def bench_ours(args):
         "e2e": {"value": round(ws * kv_bytes / (e2e_avg * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_avg, 5)},
-        "prefill": {"workload": "prefill_b8: 8 req x (16 Zipf(1.0) docs x 1024 + 256 causal "
-                                "question), Hq32/Hkv8/D128 bf16",
-                    "value": round(tflops, 2), "unit": "TFLOP/s",
-                    "ms_per_call": round(pre_avg, 4), "flops_per_call": pb.flops,
-                    "roofline": {"bound": "tensor", "achieved": round(tflops, 2),
-                                 "peak": tc_peak, "unit": "TFLOP/s",
-                                 "frac": round(tflops / tc_peak, 4), "peak_kind": peak_kind}},
-        "long_decode": {"workload": "long_decode_b16: 16 req x 131073 keys (64 Zipf(1.2) docs "
-                                    "x 2048 + 1)",
-                        "value": round(l_bytes / (long_avg * 1e-3) / 1e9, 2), "unit": "GB/s",
-                        "tokens_per_s": round(lwl.batch / (long_avg * 1e-3), 1),
-                        "ms_per_step": round(long_avg, 4),
-                        "frac": round(l_bytes / (long_avg * 1e-3) / 1e9 / hbm_peak, 4)},
         "decode_tokens_per_s": round(ws * B / (ms_per_step * 1e-3), 1),
         "clocks": clocks,
     }
+    if not only_decode:
+        pre_avg = sum(pre_ms) / len(pre_ms)
+        long_avg = sum(long_ms) / len(long_ms)
+        tflops = pb.flops / (pre_avg * 1e-3) / 1e12
+        line["prefill"] = {
+            "workload": "prefill_b8: 8 req x (16 Zipf(1.0) docs x 1024 + 256 causal question), "
+                        "Hq32/Hkv8/D128 bf16",
+            "value": round(tflops, 2), "unit": "TFLOP/s", "ms_per_call": round(pre_avg, 4),
+            "flops_per_call": pb.flops,
+            "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": tc_peak,
+                         "unit": "TFLOP/s", "frac": round(tflops / tc_peak, 4),
+                         "peak_kind": peak_kind}}
+        line["long_decode"] = {
+            "workload": "long_decode_b16: 16 req x 131073 keys (64 Zipf(1.2) docs x 2048 + 1)",
+            "value": round(l_bytes / (long_avg * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "tokens_per_s": round(lwl.batch / (long_avg * 1e-3), 1),
+            "ms_per_step": round(long_avg, 4),
+            "frac": round(l_bytes / (long_avg * 1e-3) / 1e9 / hbm_peak, 4)}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, src, kv_bytes, args.cpu_seconds)
     if rank == 0:
@@ -410,6 +424,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["all", "decode"], default="all",
+                    help="decode: time only the headline decode workload (smaller footprint)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
