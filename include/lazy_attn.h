@@ -52,7 +52,9 @@ enum {
     LAZY_ERR_UNSUPPORTED = -3,   /* dtype / head_dim / page_size / group size not built */
     LAZY_ERR_CUDA = -4,          /* a CUDA runtime call failed (message: lazy_last_error) */
     LAZY_ERR_BAD_PAGE = -5,      /* device error word: a page word pointed outside the pool */
-    LAZY_ERR_TIMEOUT = -6        /* device error word: a bounded wait inside a kernel expired */
+    LAZY_ERR_TIMEOUT = -6,       /* device error word: a bounded wait inside a kernel expired */
+    LAZY_ERR_SCRATCH_LIMIT = -7  /* lazy_attn_decode_noalloc: the call needs more scratch than
+                                    the library's fixed array holds */
 };
 
 enum { LAZY_DTYPE_BF16 = 0, LAZY_DTYPE_FP32 = 1 };
@@ -175,6 +177,37 @@ int lazy_attn_decode(lazy_pool *pool, const void *d_q, const int32_t *d_q_pos,
                      int32_t num_q_heads, float sm_scale, int32_t grid_ctas, void *d_out,
                      float *d_lse, void *d_workspace, size_t workspace_bytes,
                      lazy_stream_t stream);
+
+/*
+ * Allocation-free decode. The paper has no counterpart to this entry point; it exists for
+ * callers that cannot provide the workspace lazy_attn_decode needs. Examples: a plugin running
+ * inside a serving process whose memory manager has already reserved the GPU's memory and
+ * does not let libraries allocate more, or a latency-critical loop where a cudaMalloc /
+ * cudaFree pair would stall the device.
+ *
+ * Same arguments and results as lazy_attn_decode, minus the workspace: the partial results go
+ * to a scratch array of LAZY_NOALLOC_SCRATCH_BYTES (8 MiB) compiled into the library. Every
+ * GPU that loads the library holds that array until the process exits. The call allocates
+ * nothing. Rules:
+ *   - The pool must already have done its one-time device set-up on the current device (any
+ *     earlier kv_pool_insert_doc, kv_pool_write_tokens or lazy_attn_decode call does it);
+ *     otherwise LAZY_ERR_INVALID_ARG.
+ *   - The first call on each device looks up the array's device address (a driver query, not
+ *     an allocation); make that first call before any stream capture.
+ *   - If (batch * num_kv_heads * chunks + 4 * CTAs) * group * (head_dim + 1) * 4 bytes exceeds
+ *     the array (chunks = ceil(group / 8), group = num_q_heads / num_kv_heads, CTAs = the grid,
+ *     by default SMs x resident CTAs), the call returns LAZY_ERR_SCRATCH_LIMIT and launches
+ *     nothing. With 32/8/128 heads on a 152-SM GPU that allows up to ~355 requests.
+ *   - All calls share the one array, and it keeps whatever the last call left there. Each call
+ *     writes every scratch entry before reading it, so nothing has to start at zero. Calls
+ *     whose kernels overlap on the GPU (other streams, other threads) race on the array:
+ *     serialise them.
+ */
+enum { LAZY_NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024 };
+int lazy_attn_decode_noalloc(lazy_pool *pool, const void *d_q, const int32_t *d_q_pos,
+                             const uint64_t *d_page_words, const int32_t *d_cu_pages,
+                             int32_t batch, int32_t num_q_heads, float sm_scale,
+                             int32_t grid_ctas, void *d_out, float *d_lse, lazy_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
  * Prefill (summaries' prefill part: compute-bound, KV blocks loaded from the cache, one

@@ -25,6 +25,8 @@ LAZY_ERR_UNSUPPORTED = -3
 LAZY_ERR_CUDA = -4
 LAZY_ERR_BAD_PAGE = -5
 LAZY_ERR_TIMEOUT = -6
+LAZY_ERR_SCRATCH_LIMIT = -7
+LAZY_NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
 LAZY_DTYPE_BF16 = 0
 LAZY_DTYPE_FP32 = 1
 LAZY_DEVERR_BAD_PAGE = 1
@@ -41,6 +43,7 @@ EXPORTS = [
     "kv_pool_write_tokens", "lazy_pack_page", "lazy_unpack_page", "lazy_pack_pages",
     "lazy_decode_workspace_bytes", "lazy_attn_decode", "lazy_prefill_workspace_bytes",
     "lazy_attn_prefill", "lazy_get_device_error", "lazy_debug_gather", "lazy_debug_wait_timeout",
+    "lazy_attn_decode_noalloc",
 ]
 
 
@@ -94,6 +97,8 @@ _SIGS = {
     "lazy_get_device_error": ([_vp, _pi32, _vp], ctypes.c_int),
     "lazy_debug_gather": ([_vp, _vp, _i32, _vp, _vp, _vp, _vp], ctypes.c_int),
     "lazy_debug_wait_timeout": ([_vp, _u64, _vp], ctypes.c_int),
+    "lazy_attn_decode_noalloc": ([_vp, _vp, _vp, _vp, _vp, _i32, _i32, _f32, _i32, _vp, _vp, _vp],
+                                 ctypes.c_int),
 }
 
 
@@ -354,3 +359,22 @@ def lazy_debug_gather(pool: LazyPool, page_words, stream=None):
 def lazy_debug_wait_timeout(pool: LazyPool, limit_ns: int, stream=None):
     _check("lazy_debug_wait_timeout", load_library().lazy_debug_wait_timeout(
         pool.handle, limit_ns, _stream(stream)))
+
+
+def lazy_attn_decode_noalloc(pool: LazyPool, q, q_pos, page_words, cu_pages, sm_scale=None,
+                             grid_ctas: int = 0, out=None, lse=None, stream=None):
+    """Decode without a workspace: the library's fixed scratch array takes the partial results.
+    For callers that cannot allocate device memory. ``out`` and ``lse`` should be passed in by
+    such callers; when omitted they are created here for convenience."""
+    import torch
+    B, Hq, D = q.shape
+    if sm_scale is None:
+        sm_scale = 1.0 / float(D) ** 0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    _check("lazy_attn_decode_noalloc", load_library().lazy_attn_decode_noalloc(
+        pool.handle, _ptr(q), _ptr(q_pos), _ptr(page_words), _ptr(cu_pages), B, Hq,
+        float(sm_scale), grid_ctas, _ptr(out), _ptr(lse), _stream(stream)))
+    return out, lse

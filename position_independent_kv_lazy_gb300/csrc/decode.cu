@@ -593,3 +593,110 @@ extern "C" int lazy_attn_decode(lazy_pool *p, const void *q, const int32_t *q_po
   return with_decode_shape(p->dtype, p->d, gc,
                            [&](auto L) { return decltype(L)::run(p, dp, cp, grid, s); });
 }
+
+// ------------------------------------------------------------------------------------------------
+// Allocation-free decode: the same kernels, with their partial results in a fixed array compiled
+// into the library instead of a caller workspace (for callers that may not allocate).
+// ------------------------------------------------------------------------------------------------
+#include <mutex>
+
+// Scratch for lazy_attn_decode_noalloc. In host code this name is only a stand-in for the
+// symbol; the device address comes from cudaGetSymbolAddress (noalloc_scratch below).
+static __device__ __align__(256) unsigned char lazy_noalloc_scratch[LAZY_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device, looked up once per device.
+int noalloc_scratch(void **out) {
+  int dev = -1;
+  LAZY_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kMaxDevices) {
+    record_msg("allocation-free decode supports device ordinals below 64");
+    return LAZY_ERR_UNSUPPORTED;
+  }
+  std::lock_guard<std::mutex> g(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void *ptr = nullptr;
+    LAZY_CUDA_TRY(cudaGetSymbolAddress(&ptr, lazy_noalloc_scratch));
+    g_noalloc_ptr[dev] = ptr;
+  }
+  *out = g_noalloc_ptr[dev];
+  return LAZY_OK;
+}
+}  // namespace
+
+extern "C" int lazy_attn_decode_noalloc(lazy_pool *p, const void *q, const int32_t *q_pos,
+                                        const uint64_t *words, const int32_t *cu_pages,
+                                        int32_t batch, int32_t num_q_heads, float sm_scale,
+                                        int32_t grid_ctas, void *out, float *lse,
+                                        lazy_stream_t stream) {
+  if (!p || batch < 0 || grid_ctas < 0 || !(sm_scale > 0.f)) return LAZY_ERR_INVALID_ARG;
+  if (batch == 0) return LAZY_OK;
+  if (!q || !q_pos || !cu_pages || !out || !lse) return LAZY_ERR_INVALID_ARG;
+  if (((uintptr_t)q & 15) || ((uintptr_t)out & 15) || ((uintptr_t)words & 7))
+    return LAZY_ERR_INVALID_ARG;
+  {
+    std::lock_guard<std::mutex> g(p->mu);
+    if (!p->dev_ready) {
+      record_msg("pool has no device state yet: insert or write tokens before this call");
+      return LAZY_ERR_INVALID_ARG;
+    }
+  }
+  int dev = -1;
+  LAZY_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev != p->device) {
+    record_msg("the current device is not the pool's device");
+    return LAZY_ERR_INVALID_ARG;
+  }
+  int32_t gc, chunks;
+  int rc = plan_groups(num_q_heads, p->hkv, &gc, &chunks);
+  if (rc != LAZY_OK) return rc;
+  int grid;
+  rc = decode_grid(p, gc, grid_ctas, &grid);
+  if (rc != LAZY_OK) return rc;
+  const int32_t hv = p->hkv * chunks;
+  const size_t slots = (size_t)batch * hv + (size_t)grid * kWarps;
+  const size_t need = slots * gc * ((size_t)p->d + 1) * sizeof(float);
+  if (need > (size_t)LAZY_NOALLOC_SCRATCH_BYTES) {
+    record_msg("allocation-free decode: the batch needs more scratch than the fixed array");
+    return LAZY_ERR_SCRATCH_LIMIT;
+  }
+  void *scratch = nullptr;
+  rc = noalloc_scratch(&scratch);
+  if (rc != LAZY_OK) return rc;
+  DecodeParams dp;
+  dp.q = q;
+  dp.q_pos = q_pos;
+  dp.words = words;
+  dp.cu_pages = cu_pages;
+  dp.k_pool = p->k;
+  dp.v_pool = p->v;
+  dp.turn = p->d_turn;
+  dp.ws_o = reinterpret_cast<float *>(scratch);
+  dp.ws_lse = dp.ws_o + slots * gc * p->d;
+  dp.err = p->d_err;
+  dp.batch = batch;
+  dp.hkv = p->hkv;
+  dp.hq = num_q_heads;
+  dp.num_blocks = p->num_blocks;
+  dp.hv = hv;
+  dp.chunks = chunks;
+  dp.scale_log2 = sm_scale * 1.4426950408889634f;
+  dp.wait_ns = p->wait_limit_ns;
+  CombineParams cp;
+  cp.ws_o = dp.ws_o;
+  cp.ws_lse = dp.ws_lse;
+  cp.cu_pages = cu_pages;
+  cp.out = out;
+  cp.lse = lse;
+  cp.batch = batch;
+  cp.hq = num_q_heads;
+  cp.hv = hv;
+  cp.warps = (int64_t)grid * kWarps;
+  cudaStream_t s = (cudaStream_t)stream;
+  return with_decode_shape(p->dtype, p->d, gc,
+                           [&](auto L) { return decltype(L)::run(p, dp, cp, grid, s); });
+}

@@ -58,6 +58,7 @@ const char *lazy_status_string(int s) {
     case LAZY_ERR_CUDA: return "CUDA error";
     case LAZY_ERR_BAD_PAGE: return "page word outside the pool";
     case LAZY_ERR_TIMEOUT: return "bounded wait expired";
+    case LAZY_ERR_SCRATCH_LIMIT: return "call exceeds the fixed scratch of the allocation-free decode";
     default: return "unknown status";
   }
 }
