@@ -184,6 +184,21 @@ def bench_ours(args):
 
     launches_per_step = 3  # encode (append) + decode split + combine
 
+    # no-reuse control: same shapes, every request with its own documents (logical = DRAM bytes)
+    nwl = W.decode_workload(no_reuse=True, name="decode_b64_no_reuse")
+    nsrc = H.DeviceSource(nwl)
+    nres = H.build_resident(nwl, nsrc)
+    ndb = H.decode_batch(nwl, nres, nsrc)
+    n_bytes = ndb.n_keys * nwl.kv_bytes_per_token()
+    nws = torch.empty(pk.lazy_decode_workspace_bytes(nres.pool, nwl.batch, nwl.Hq),
+                      dtype=torch.uint8, device="cuda")
+    nout = torch.empty_like(ndb.q)
+    nlse = torch.empty((nwl.batch, nwl.Hq), dtype=torch.float32, device="cuda")
+
+    def no_reuse_call():
+        pk.lazy_attn_decode(nres.pool, ndb.q, ndb.q_pos, ndb.words, ndb.cu_pages,
+                            sm_scale=nwl.sm_scale, out=nout, lse=nlse, workspace=nws)
+
     # e2e buffers: pinned host inputs/outputs of one step
     h_q = db.q.cpu().pin_memory()
     h_k = db.new_k.cpu().pin_memory()
@@ -213,7 +228,7 @@ def bench_ours(args):
 
     # ---------------- prefill workload (extra object)
     pwl = W.prefill_workload() if not only_decode else None
-    pools = [res.pool]
+    pools = [res.pool, nres.pool]
     if not only_decode:
         psrc = H.DeviceSource(pwl)
         pres = H.build_resident(pwl, psrc)
@@ -245,7 +260,7 @@ def bench_ours(args):
 
     torch.cuda.synchronize()
     for _ in range(args.warmup):
-        flush(); step(); e2e_step()
+        flush(); step(); e2e_step(); no_reuse_call()
         if not only_decode:
             prefill_call(); long_call()
     torch.cuda.synchronize()
@@ -262,6 +277,7 @@ def bench_ours(args):
         _barrier(ws)
         dec_ms = _timed_steps(decode_call, args.steps, flush, stream)
         e2e_ms = _timed_steps(e2e_step, args.steps, flush, stream)
+        nr_ms = _timed_steps(no_reuse_call, args.steps, flush, stream)
         if not only_decode:
             pre_ms = _timed_steps(prefill_call, max(3, args.steps // 2), flush, stream)
             long_ms = _timed_steps(long_call, max(3, args.steps // 2), flush, stream)
@@ -313,6 +329,12 @@ def bench_ours(args):
         "e2e": {"value": round(ws * kv_bytes / (e2e_avg * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_avg, 5)},
+        "decode_no_reuse": {
+            "workload": "decode_b64_no_reuse: same shapes, every request its own 8 docs "
+                        "(no page shared, logical bytes = DRAM bytes)",
+            "value": round(n_bytes / (sum(nr_ms) / len(nr_ms) * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "ms_per_call": round(sum(nr_ms) / len(nr_ms), 5),
+            "frac": round(n_bytes / (sum(nr_ms) / len(nr_ms) * 1e-3) / 1e9 / hbm_peak, 4)},
         "decode_tokens_per_s": round(ws * B / (ms_per_step * 1e-3), 1),
         "clocks": clocks,
     }

@@ -6,8 +6,9 @@
 // page words; a virtual head is one kv head and a chunk of at most 8 of its query heads. All
 // units' pages are flattened in (b, hv, page) order and cut into equal contiguous ranges, one per
 // warp of a single persistent wave (grid = SMs x resident CTAs). A warp streams its range through
-// its own ring of shared-memory stages filled by 1-D bulk async copies (one 4 KB K page and one
-// 4 KB V page per stage for bf16, D = 128), so the pipeline never drains at unit boundaries and
+// its own two-stage ring of shared-memory stages filled by 1-D bulk async copies (one 4 KB K page
+// and one 4 KB V page per stage for bf16, D = 128), so the pipeline never drains at unit
+// boundaries and
 // every SM moves the same number of bytes. Each (unit, warp) piece leaves a partial
 // (o / l, log2-sum-exp) in the workspace at slot (unit + warp); combine_kernel merges the pieces
 // of a unit (log-sum-exp combine).
@@ -112,6 +113,7 @@ template <typename T, int D, int GC, int WARPS, int STAGES>
 __global__ void __launch_bounds__(WARPS * 32) decode_split_kernel(const DecodeParams p) {
   using S = DecodeSmem<T, D, GC, STAGES>;
   constexpr int EPL = 16 / (int)sizeof(T);  // elements per 16-byte load
+  constexpr int EP2 = EPL / 2;              // float2 pairs per 16-byte load
   constexpr int LPR = D / EPL;              // lanes per key row
   constexpr int KPI = 32 / LPR;             // keys per load instruction
   constexpr int NIT = kPage / KPI;          // load iterations per page
@@ -130,12 +132,18 @@ __global__ void __launch_bounds__(WARPS * 32) decode_split_kernel(const DecodePa
   uint64_t *meta_w = reinterpret_cast<uint64_t *>(ws + S::kWord);
   int32_t *meta_u = reinterpret_cast<int32_t *>(ws + S::kUnit);
 
+  // Everything this kernel reads may come from the preceding kernel in the stream (a token
+  // append launched ahead of it); wait for it (no-op without programmatic dependent launch).
+  cudaGridDependencySynchronize();
   const int32_t B = p.batch, HV = p.hv;
   const int64_t N = (int64_t)HV * p.cu_pages[B];
   const int64_t WT = (int64_t)gridDim.x * WARPS;
   const int64_t wg = (int64_t)blockIdx.x * WARPS + warp;
   const int64_t x0 = wg * N / WT, x1 = (wg + 1) * N / WT;
-  if (x0 >= x1) return;
+  if (x0 >= x1) {
+    cudaTriggerProgrammaticLaunchCompletion();
+    return;
+  }
   const int64_t n_mine = x1 - x0;
 
   if (lane == 0) {
@@ -147,11 +155,14 @@ __global__ void __launch_bounds__(WARPS * 32) decode_split_kernel(const DecodePa
   const T *kpool = reinterpret_cast<const T *>(p.k_pool);
   const T *vpool = reinterpret_cast<const T *>(p.v_pool);
 
-  // Producer (lane 0): fill stage s with the page the walker points at.
+  // Producer (lane 0): fill stage s with the page the walker points at. The word of the next
+  // page to issue is loaded one issue ahead, so its latency never stalls the warp.
   Walker prod;
   prod.init(x0, p.cu_pages, B, HV);
+  uint64_t w_next = 0;
+  if (lane == 0) w_next = p.words[prod.wbase + prod.pg];
   auto issue = [&](int s) {
-    const uint64_t w = p.words[prod.wbase + prod.pg];
+    const uint64_t w = w_next;
     uint32_t blk = word_block(w);
     if (blk >= (uint32_t)p.num_blocks || word_nvalid(w) > (uint32_t)kPage) {
       set_error(p.err, LAZY_DEVERR_BAD_PAGE);
@@ -164,14 +175,18 @@ __global__ void __launch_bounds__(WARPS * 32) decode_split_kernel(const DecodePa
     bulk_g2s(kbuf + s * kPage * D, kpool + page, S::kPageBytes, &bars[s]);
     bulk_g2s(vbuf + s * kPage * D, vpool + page, S::kPageBytes, &bars[s]);
   };
-  for (int s = 0; s < STAGES && s < n_mine; ++s) {
+  int64_t issued = 0;
+  auto issue_next = [&](int s) {
     if (lane == 0) issue(s);
     prod.advance(p.cu_pages, B, HV);
-  }
+    ++issued;
+    if (lane == 0 && issued < n_mine) w_next = p.words[prod.wbase + prod.pg];
+  };
+  for (int s = 0; s < STAGES && s < n_mine; ++s) issue_next(s);
 
   const int gq = lane / LPR, r = lane % LPR;
-  float qr[GC][EPL];     // rotated query slice, pre-scaled by sm_scale * log2(e)
-  float acc[GC][EPL];    // unnormalised output slice
+  float2 qr[GC][EP2];    // rotated query slice, pre-scaled by sm_scale * log2(e)
+  float2 acc[GC][EP2];   // unnormalised output slice
   float m_run[GC], lsum[GC];
   int32_t cur_unit = -1, cur_b = 0;
   uint32_t cur_off = 0xFFFFFFFFu;
@@ -186,7 +201,10 @@ __global__ void __launch_bounds__(WARPS * 32) decode_split_kernel(const DecodePa
       for (int g = 0; g < GC; ++g) {
         lsum[g] += __shfl_xor_sync(0xffffffffu, lsum[g], mk);
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) acc[g][e] += __shfl_xor_sync(0xffffffffu, acc[g][e], mk);
+        for (int e = 0; e < EP2; ++e) {
+          acc[g][e].x += __shfl_xor_sync(0xffffffffu, acc[g][e].x, mk);
+          acc[g][e].y += __shfl_xor_sync(0xffffffffu, acc[g][e].y, mk);
+        }
       }
     }
     const int64_t slot = (int64_t)unit + wg;
@@ -196,17 +214,16 @@ __global__ void __launch_bounds__(WARPS * 32) decode_split_kernel(const DecodePa
         const float inv = lsum[g] > 0.f ? 1.f / lsum[g] : 0.f;
         float *dst = p.ws_o + ((size_t)slot * GC + g) * D + r * EPL;
 #pragma unroll
-        for (int e = 0; e < EPL; e += 4)
-          *reinterpret_cast<float4 *>(dst + e) =
-              make_float4(acc[g][e] * inv, acc[g][e + 1] * inv, acc[g][e + 2] * inv,
-                          acc[g][e + 3] * inv);
+        for (int e = 0; e < EP2; e += 2)
+          *reinterpret_cast<float4 *>(dst + 2 * e) =
+              make_float4(acc[g][e].x * inv, acc[g][e].y * inv, acc[g][e + 1].x * inv,
+                          acc[g][e + 1].y * inv);
       }
     }
     if (lane == 0) {
 #pragma unroll
       for (int g = 0; g < GC; ++g)
-        p.ws_lse[(size_t)slot * GC + g] =
-            lsum[g] > 0.f ? m_run[g] + __log2f(lsum[g]) : -INFINITY;
+        p.ws_lse[(size_t)slot * GC + g] = lsum[g] > 0.f ? m_run[g] + log2f(lsum[g]) : -INFINITY;
     }
   };
 
@@ -239,7 +256,7 @@ __global__ void __launch_bounds__(WARPS * 32) decode_split_kernel(const DecodePa
         m_run[g] = -INFINITY;
         lsum[g] = 0.f;
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) acc[g][e] = 0.f;
+        for (int e = 0; e < EP2; ++e) acc[g][e] = make_float2(0.f, 0.f);
       }
       cur_off = 0xFFFFFFFFu;
     }
@@ -261,14 +278,14 @@ __global__ void __launch_bounds__(WARPS * 32) decode_split_kernel(const DecodePa
 #pragma unroll
           for (int g = 0; g < GC; ++g) {
             const float x = qraw[g * D + d], y = qraw[g * D + pd];
-            const float rot = d < D / 2 ? x * cs - y * sn : y * sn + x * cs;
-            qr[g][e] = rot * p.scale_log2;
+            const float rot = (d < D / 2 ? x * cs - y * sn : y * sn + x * cs) * p.scale_log2;
+            if (e & 1) qr[g][e / 2].y = rot; else qr[g][e / 2].x = rot;
           }
         }
       }
       const T *K = kbuf + s * kPage * D;
       const T *V = vbuf + s * kPage * D;
-      // ---- scores: partial dots over this lane's 16 bytes of each key row
+      // ---- scores: partial dots over this lane's 16 bytes of each key row (packed f32x2 FMA)
       float part[NV0];
 #pragma unroll
       for (int it = 0; it < NIT; ++it) {
@@ -276,40 +293,62 @@ __global__ void __launch_bounds__(WARPS * 32) decode_split_kernel(const DecodePa
         unpack16<T>(*reinterpret_cast<const uint4 *>(K + (it * KPI + gq) * D + r * EPL), kf);
 #pragma unroll
         for (int g = 0; g < GC; ++g) {
-          float a = 0.f;
+          float2 a = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int e = 0; e < EPL; ++e) a = fmaf(qr[g][e], kf[e], a);
-          part[it * GC + g] = a;
+          for (int e = 0; e < EP2; ++e)
+            a = __ffma2_rn(qr[g][e], make_float2(kf[2 * e], kf[2 * e + 1]), a);
+          part[it * GC + g] = a.x + a.y;
         }
       }
       int base = 0;
       reduce_scatter<NV0, LPR / 2>(part, lane, base);
-      // part[0..NF) now hold full (log2-domain) scores of flat indices base .. base+NF-1,
+      // part[0..NF) hold full (log2-domain) scores of flat indices base .. base+NF-1,
       // index = it * GC + g  ->  key it * KPI + gq, head g.
-      float pmax[GC];
+      if (nv < (uint32_t)kPage) {
 #pragma unroll
-      for (int g = 0; g < GC; ++g) pmax[g] = -INFINITY;
+        for (int j = 0; j < NF; ++j)
+          if (((base + j) / GC) * KPI + gq >= (int)nv) part[j] = -INFINITY;
+      }
+      // The running max only moves when some score exceeds it (rare after the first pages):
+      // a warp vote skips the butterfly otherwise.
+      bool above = false;
 #pragma unroll
       for (int j = 0; j < NF; ++j) {
-        const int idx = base + j;
-        const int key = (idx / GC) * KPI + gq;
-        const int g = idx % GC;
-        if (key >= (int)nv) part[j] = -INFINITY;
+        const int g = (base + j) % GC;
 #pragma unroll
         for (int gg = 0; gg < GC; ++gg)
-          if (gg == g) pmax[gg] = fmaxf(pmax[gg], part[j]);
+          if (gg == g) above |= part[j] > m_run[gg];
       }
+      if (__any_sync(0xffffffffu, above)) {
+        float pmax[GC];
 #pragma unroll
-      for (int mk = 16; mk >= 1; mk >>= 1)
+        for (int g = 0; g < GC; ++g) pmax[g] = -INFINITY;
 #pragma unroll
-        for (int g = 0; g < GC; ++g)
-          pmax[g] = fmaxf(pmax[g], __shfl_xor_sync(0xffffffffu, pmax[g], mk));
-      float m_new[GC];
-      bool grow = false;
+        for (int j = 0; j < NF; ++j) {
+          const int g = (base + j) % GC;
 #pragma unroll
-      for (int g = 0; g < GC; ++g) {
-        m_new[g] = fmaxf(m_run[g], pmax[g]);
-        grow |= m_new[g] > m_run[g];
+          for (int gg = 0; gg < GC; ++gg)
+            if (gg == g) pmax[gg] = fmaxf(pmax[gg], part[j]);
+        }
+#pragma unroll
+        for (int mk = 16; mk >= 1; mk >>= 1)
+#pragma unroll
+          for (int g = 0; g < GC; ++g)
+            pmax[g] = fmaxf(pmax[g], __shfl_xor_sync(0xffffffffu, pmax[g], mk));
+#pragma unroll
+        for (int g = 0; g < GC; ++g) {
+          const float m_new = fmaxf(m_run[g], pmax[g]);
+          if (m_new > m_run[g]) {  // identical in every lane
+            const float alpha = m_run[g] == -INFINITY ? 0.f : exp2f(m_run[g] - m_new);
+            lsum[g] *= alpha;
+#pragma unroll
+            for (int e = 0; e < EP2; ++e) {
+              acc[g][e].x *= alpha;
+              acc[g][e].y *= alpha;
+            }
+            m_run[g] = m_new;
+          }
+        }
       }
 #pragma unroll
       for (int j = 0; j < NF; ++j) {
@@ -319,28 +358,18 @@ __global__ void __launch_bounds__(WARPS * 32) decode_split_kernel(const DecodePa
         float mg = 0.f;
 #pragma unroll
         for (int gg = 0; gg < GC; ++gg)
-          if (gg == g) mg = m_new[gg];
-        const float pr = part[j] == -INFINITY ? 0.f : exp2f(part[j] - mg);
-        psm[key * GC + g] = pr;
-      }
-      if (grow) {  // warp-uniform: the maxima are identical in every lane
-#pragma unroll
-        for (int g = 0; g < GC; ++g) {
-          const float alpha = m_run[g] == -INFINITY ? 0.f : exp2f(m_run[g] - m_new[g]);
-          lsum[g] *= alpha;
-#pragma unroll
-          for (int e = 0; e < EPL; ++e) acc[g][e] *= alpha;
-          m_run[g] = m_new[g];
-        }
+          if (gg == g) mg = m_run[gg];
+        psm[key * GC + g] = part[j] == -INFINITY ? 0.f : exp2f(part[j] - mg);
       }
       __syncwarp();
-      // ---- PV
+      // ---- PV (packed f32x2 FMA); masked keys of a partial page contribute exactly zero
+      const bool partial = nv < (uint32_t)kPage;
 #pragma unroll
       for (int it = 0; it < NIT; ++it) {
         const int key = it * KPI + gq;
         float vf[EPL];
         unpack16<T>(*reinterpret_cast<const uint4 *>(V + key * D + r * EPL), vf);
-        if (nv < (uint32_t)kPage && key >= (int)nv) {
+        if (partial && key >= (int)nv) {
 #pragma unroll
           for (int e = 0; e < EPL; ++e) vf[e] = 0.f;
         }
@@ -358,17 +387,17 @@ __global__ void __launch_bounds__(WARPS * 32) decode_split_kernel(const DecodePa
 #pragma unroll
         for (int g = 0; g < GC; ++g) {
           lsum[g] += pk[g];
+          const float2 pp = make_float2(pk[g], pk[g]);
 #pragma unroll
-          for (int e = 0; e < EPL; ++e) acc[g][e] = fmaf(pk[g], vf[e], acc[g][e]);
+          for (int e = 0; e < EP2; ++e)
+            acc[g][e] = __ffma2_rn(pp, make_float2(vf[2 * e], vf[2 * e + 1]), acc[g][e]);
         }
       }
     }
     __syncwarp();
-    if (i + STAGES < n_mine) {
-      if (lane == 0) issue(s);
-      prod.advance(p.cu_pages, B, HV);
-    }
+    if (issued < n_mine) issue_next(s);
   }
+  cudaTriggerProgrammaticLaunchCompletion();
   if (!timed_out && cur_unit >= 0) flush(cur_unit);
 }
 
@@ -386,6 +415,7 @@ struct CombineParams {
 // intersect it) with a log-sum-exp combine and writes the final rows.
 template <typename T, int D, int GC>
 __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
+  cudaGridDependencySynchronize();  // partials of the decode kernel launched just before
   const int32_t u = blockIdx.x;
   const int32_t b = u / p.hv, hv = u % p.hv;
   const int32_t wbase = p.cu_pages[b], np = p.cu_pages[b + 1] - wbase;
@@ -433,17 +463,36 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
   }
 }
 
-constexpr int kWarps = 4;
-constexpr int kStages = 3;
+constexpr int kWarps = 4;  // warps per CTA of every decode variant
 
-template <typename T, int D, int GC>
+// Two stages (one page in flight while the other is consumed) keep a warp's ring at 16 KB, so
+// three 4-warp CTAs fit per SM: 12 warps per SM hide the fixed-latency chains better than
+// deeper rings with fewer warps (measured on GB300: 86% vs 75% of copy bandwidth).
+constexpr int kStages = 2;
+
+template <typename K, typename... Args>
+cudaError_t launch_pdl(K kernel, int grid, int block, int smem, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+template <typename T, int D, int GC, int STAGES>
 struct DecodeLaunch {
-  using S = DecodeSmem<T, D, GC, kStages>;
+  using S = DecodeSmem<T, D, GC, STAGES>;
   static constexpr int kSmem = S::kBytes * kWarps;
   static int ctas_per_sm() {
     static int cached = -1;
     if (cached < 0) {
-      auto fn = decode_split_kernel<T, D, GC, kWarps, kStages>;
+      auto fn = decode_split_kernel<T, D, GC, kWarps, STAGES>;
       if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
           cudaSuccess)
         return -1;
@@ -457,11 +506,10 @@ struct DecodeLaunch {
   }
   static int run(lazy_pool *pl, const DecodeParams &dp, const CombineParams &cp, int grid,
                  cudaStream_t s) {
-    decode_split_kernel<T, D, GC, kWarps, kStages><<<grid, kWarps * 32, kSmem, s>>>(dp);
-    LAZY_CUDA_TRY(cudaGetLastError());
-    combine_kernel<T, D, GC><<<dp.batch * dp.hv, 128, 0, s>>>(cp);
-    LAZY_CUDA_TRY(cudaGetLastError());
     (void)pl;
+    LAZY_CUDA_TRY(launch_pdl(decode_split_kernel<T, D, GC, kWarps, STAGES>, grid, kWarps * 32,
+                             kSmem, s, dp));
+    LAZY_CUDA_TRY(launch_pdl(combine_kernel<T, D, GC>, dp.batch * dp.hv, 128, 0, s, cp));
     return LAZY_OK;
   }
 };
@@ -470,10 +518,10 @@ template <typename F>
 int with_decode_shape(int32_t dtype, int32_t d, int32_t gc, F &&f) {
 #define LAZY_GC_CASES(T, DD)                                        \
   switch (gc) {                                                     \
-    case 1: return f(DecodeLaunch<T, DD, 1>{});                     \
-    case 2: return f(DecodeLaunch<T, DD, 2>{});                     \
-    case 4: return f(DecodeLaunch<T, DD, 4>{});                     \
-    case 8: return f(DecodeLaunch<T, DD, 8>{});                     \
+    case 1: return f(DecodeLaunch<T, DD, 1, kStages>{});            \
+    case 2: return f(DecodeLaunch<T, DD, 2, kStages>{});            \
+    case 4: return f(DecodeLaunch<T, DD, 4, kStages>{});            \
+    case 8: return f(DecodeLaunch<T, DD, 8, kStages>{});            \
     default: return LAZY_ERR_UNSUPPORTED;                           \
   }
   if (dtype == LAZY_DTYPE_BF16) {

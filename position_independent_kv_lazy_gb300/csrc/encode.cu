@@ -30,6 +30,9 @@ __global__ void __launch_bounds__(256) encode_kernel(
     const int32_t *__restrict__ local_pos) {
   constexpr int EPL = 16 / (int)sizeof(T);
   constexpr int CH = (D / 2) / EPL;
+  // A decode launched right after this append may start its launch early; it waits for this
+  // grid to finish before reading anything (programmatic dependent launch).
+  cudaTriggerProgrammaticLaunchCompletion();
   const int64_t total = (int64_t)n_tokens * hkv * CH;
   for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
        idx += (int64_t)gridDim.x * blockDim.x) {

@@ -237,14 +237,23 @@ def tiny_fp32(seed: int = 0) -> Workload:
 
 
 def decode_workload(batch=64, docs_per_req=8, doc_len=512, n_pool=1000, alpha=1.0, question=64,
-                    Hq=32, Hkv=8, D=128, base=500000.0, seed=0, name="decode_b64") -> Workload:
+                    Hq=32, Hkv=8, D=128, base=500000.0, seed=0, name="decode_b64",
+                    no_reuse=False) -> Workload:
     """Decode step: each request holds ``docs_per_req`` distinct Zipf docs in random order at
     offsets 0, L, 2L, ..., then a private segment (question + the new token) right after them;
-    the query is the new token."""
+    the query is the new token. ``no_reuse`` gives every request its own documents (pool =
+    batch x docs_per_req), the control in which no page is shared between requests."""
     rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence(seed)))
+    if no_reuse:
+        n_pool = batch * docs_per_req
     reqs = []
     for b in range(batch):
-        docs, offs = _docs_at_offsets(rng, n_pool, alpha, docs_per_req, doc_len)
+        if no_reuse:
+            order = rng.permutation(docs_per_req)
+            docs = [b * docs_per_req + int(i) for i in order]
+            offs = [i * doc_len for i in range(docs_per_req)]
+        else:
+            docs, offs = _docs_at_offsets(rng, n_pool, alpha, docs_per_req, doc_len)
         o_priv = docs_per_req * doc_len
         plen = question + 1
         reqs.append(Request(index=b, mode="decode", docs=docs, offsets=offs,
