@@ -1,14 +1,691 @@
-// Tensor-core (tcgen05/TMEM/TMA) prefill: not built yet.
+// Tensor-core prefill with deferred RoPE for bf16 pools, head_dim 128 (tcgen05 + TMEM + TMA).
+//
+// Follows the LazyAttention summaries' prefill part: KV blocks are loaded from the cache and each
+// key tile receives ONE relative rotation, by the offset between its document and the query
+// tile, instead of an un-rotate followed by a re-rotate. Here the query tile's reference position
+// is m0 = the CTA's first question token: queries are rotated by R(m - m0), a cached page of a
+// segment at offset o (rows already carry R(j)) by R(o - m0), a question key at p by R(p - m0).
+//
+// CTA = (request b, kv head h, 2 x TQ question tokens): two 128-row Q tiles, rows ordered
+// (token, query head of the group), TQ = 128 / G. 16 warps:
+//   warp 0      TMA producer: Q tiles once, then per 128-key tile 8 page boxes (16 rows x 64
+//               dims, 128B swizzle) of K and of V into a 2-stage ring; question keys by
+//               128-token boxes.
+//   warp 1      TMEM owner (512 columns) and single-thread tcgen05.mma issuer:
+//               S_i = Q_i K^T (SS), then O_i += P_i V (P from TMEM, V MN-major).
+//   warps 4-7   softmax of Q tile 0, warps 8-11 of Q tile 1 (TMEM lane quadrant = warp % 4):
+//               online softmax in the log2 domain with a lazy rescale (the running max only
+//               moves when a row max exceeds it by more than 8), P written back into S's TMEM
+//               columns as bf16 pairs.
+//   warps 12-15 rotation: Q tiles once, each K tile in shared memory, in place (the pair
+//               (i, i+64) sits at the same swizzled offset of the two 64-dim boxes).
+// TMEM: S_0 [0,128) S_1 [128,256) O_0 [256,384) O_1 [384,512) fp32 columns.
+// Every wait is bounded; a timeout sets LAZY_DEVERR_TIMEOUT, raises a CTA abort flag that
+// releases the other roles, drains outstanding copies and MMAs, frees TMEM and returns.
+#include <cuda.h>
+#include <string.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "lazy_common.cuh"
 #include "prefill.h"
 
 namespace lazy {
+namespace {
+
+constexpr int kTile = 128;
+constexpr int kNS = 2;
+constexpr int kThreads = 512;
+constexpr int kTileBytes = kTile * 128 * 2;  // 32 KB: 128 rows x 128 bf16
+constexpr int kHalfBytes = kTileBytes / 2;   // one 64-dim box column
+
+// Shared-memory map (offsets from a 1024-aligned base).
+constexpr int kOffQ = 0;                               // 2 Q tiles
+constexpr int kOffK = kOffQ + 2 * kTileBytes;          // kNS K stages
+constexpr int kOffV = kOffK + kNS * kTileBytes;        // kNS V stages
+constexpr int kOffTab = kOffV + kNS * kTileBytes;      // float2 [8 pages][64]
+constexpr int kOffMeta = kOffTab + 8 * 64 * 8;         // TileMeta [kNS]
+constexpr int kOffBar = kOffMeta + kNS * 128;          // barriers
+constexpr int kSmemBytes = kOffBar + 256 + 1024;       // + alignment slack
+
+struct TileMeta {
+  int32_t kind;      // 0 = document pages, 1 = question keys
+  int32_t c0;        // question tile: first key token
+  int32_t full;      // document tile: every page present and full
+  int32_t pad;
+  int32_t off[8];    // document tile: logical offset of each page
+  int32_t nv[8];     // document tile: valid tokens per page (0 = absent / bad)
+};
+
+struct TcParams {
+  CUtensorMap tm_q, tm_knew, tm_vnew, tm_k, tm_v;
+  const int32_t *cu_q;
+  const int32_t *q_pos0;
+  const uint64_t *words;
+  const int32_t *cu_pages;
+  const uint64_t *turn;
+  __nv_bfloat16 *out;
+  float *lse;
+  int32_t *err;
+  int32_t batch, hkv, hq, num_blocks, G, TQ, has_new;
+  float scale_log2;
+  uint64_t wait_ns;
+};
+
+// ---------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ void tma2d(void *dst, const CUtensorMap *m, int x, int y,
+                                      uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
+      "{%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"((uint64_t)m), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma3d(void *dst, const CUtensorMap *m, int x, int y, int z,
+                                      uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
+      "{%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"((uint64_t)m), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+// Shared-memory matrix descriptor: 128B swizzle, version 1.
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr & 0x3FFFF) >> 4) | ((uint64_t)(lbo >> 4) << 16) |
+         ((uint64_t)(sbo >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                       int acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                       int acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
+}
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+#define LAZY_R32(r)                                                                          \
+  "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),        \
+      "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), \
+      "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),           \
+      "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),           \
+      "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+#define LAZY_W32(r)                                                                          \
+  "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),    \
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),       \
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),     \
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),     \
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+
+// 32 consecutive fp32 TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : LAZY_R32(r)
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(
+          taddr),
+      LAZY_W32(r)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// Rotate, in place, 8 consecutive rows of a 128-row swizzled bf16 tile at 16-byte chunk c of
+// both 64-dim boxes: x_i <- x_i cos - x_{i+64} sin, x_{i+64} <- x_i sin + x_{i+64} cos,
+// i = 8c .. 8c+7. cs[e] = (cos, sin) of frequency 8c + e for each row (per-row tables when
+// `per_row`).
+__device__ __forceinline__ void rotate_row_chunk(uint8_t *tile, int row, int c,
+                                                 const float2 (&cs)[8]) {
+  const int phys = (c ^ (row & 7)) * 16;
+  uint4 *lo = reinterpret_cast<uint4 *>(tile + row * 128 + phys);
+  uint4 *hi = reinterpret_cast<uint4 *>(tile + kHalfBytes + row * 128 + phys);
+  const uint4 a = *lo, b = *hi;
+  float x[8], y[8];
+  unpack16<__nv_bfloat16>(a, x);
+  unpack16<__nv_bfloat16>(b, y);
+  float xo[8], yo[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    xo[e] = x[e] * cs[e].x - y[e] * cs[e].y;
+    yo[e] = x[e] * cs[e].y + y[e] * cs[e].x;
+  }
+  *lo = pack16<__nv_bfloat16>(xo);
+  *hi = pack16<__nv_bfloat16>(yo);
+}
+
+// Bounded wait that also gives up when another role raised the CTA abort flag.
+__device__ __forceinline__ bool cta_wait(uint64_t *bar, uint32_t par, volatile int *abort,
+                                         uint64_t limit, int32_t *err) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait(a, par)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(a, par)) {
+    if (*abort) return false;
+    if (global_timer_ns() - t0 > limit) {
+      *abort = 1;
+      set_error(err, LAZY_DEVERR_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *sm = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t *Qs = sm + kOffQ;
+  uint8_t *Ks = sm + kOffK;
+  uint8_t *Vs = sm + kOffV;
+  float2 *tab = reinterpret_cast<float2 *>(sm + kOffTab);
+  TileMeta *meta = reinterpret_cast<TileMeta *>(sm + kOffMeta);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kOffBar);
+  uint64_t *q_full = bars + 0, *q_rot = bars + 1;
+  uint64_t *k_full = bars + 2, *v_full = bars + 4, *k_rot = bars + 6, *kv_empty = bars + 8;
+  uint64_t *s_full = bars + 10, *p_ready = bars + 12, *o_final = bars + 14;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 16);
+  volatile int *abort = reinterpret_cast<volatile int *>(bars + 17);  // bars + 18: rotation flag
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b = blockIdx.z, h = blockIdx.y;
+  const int G = p.G, TQ = p.TQ;
+  const int t0 = blockIdx.x * 2 * TQ;
+  const int32_t qbeg = p.cu_q[b];
+  const int32_t Tb = p.cu_q[b + 1] - qbeg;
+  if (t0 >= Tb) return;
+  const int32_t m0 = p.q_pos0[b] + t0;
+  const int32_t pg0 = p.cu_pages[b], npg = p.cu_pages[b + 1] - pg0;
+  const int n_doc = (npg + 7) / 8;
+  const int t_end = min(t0 + 2 * TQ, Tb);
+  const int n_new = p.has_new ? (t_end + kTile - 1) / kTile : 0;
+  const int n_tiles = n_doc + n_new;
+
+  if (tid == 0) {
+    mbar_init(q_full, 1);
+    mbar_init(q_rot, 128);
+    for (int s = 0; s < kNS; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&k_rot[s], 128);
+      mbar_init(&kv_empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_ready[i], 128);
+    }
+    mbar_init(o_final, 1);
+    *abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    asm volatile(
+        "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
+            smem_u32(tmem_slot)));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint64_t lim = p.wait_ns;
+
+  if (warp == 0) {
+    // ============================== producer
+    if (lane == 0) {
+      mbar_arrive_expect_tx(q_full, 2 * kTileBytes);
+      for (int i = 0; i < 2; ++i)
+        for (int cb = 0; cb < 2; ++cb)
+          tma3d(Qs + i * kTileBytes + cb * kHalfBytes, &p.tm_q, cb * 64, h * G,
+                qbeg + t0 + i * TQ, q_full);
+      int issued[kNS] = {0, 0};
+      for (int j = 0; j < n_tiles; ++j) {
+        const int s = j % kNS;
+        if (j >= kNS && !cta_wait(&kv_empty[s], ((j / kNS) - 1) & 1, abort, lim, p.err)) break;
+        TileMeta &mt = meta[s];
+        uint8_t *kd = Ks + s * kTileBytes, *vd = Vs + s * kTileBytes;
+        if (j < n_doc) {
+          int32_t rows[8];
+          int full = 1;
+          for (int pp = 0; pp < 8; ++pp) {
+            const int pg = j * 8 + pp;
+            const uint64_t w = p.words[pg0 + min(pg, npg - 1)];
+            uint32_t blk = word_block(w);
+            int nv = (int)word_nvalid(w);
+            if (blk >= (uint32_t)p.num_blocks || nv > kPage) {
+              set_error(p.err, LAZY_DEVERR_BAD_PAGE);
+              blk = 0;
+              nv = 0;
+            }
+            if (pg >= npg) nv = 0;  // absent page: the last one is loaded again, masked
+            full &= (nv == kPage);
+            mt.off[pp] = (int32_t)word_offset(w);
+            mt.nv[pp] = nv;
+            rows[pp] = (int32_t)((blk * (uint32_t)p.hkv + (uint32_t)h) * kPage);
+          }
+          mt.kind = 0;
+          mt.full = full;
+          mbar_arrive_expect_tx(&k_full[s], kTileBytes);
+          for (int pp = 0; pp < 8; ++pp)
+            for (int cb = 0; cb < 2; ++cb)
+              tma2d(kd + cb * kHalfBytes + pp * 2048, &p.tm_k, cb * 64, rows[pp], &k_full[s]);
+          mbar_arrive_expect_tx(&v_full[s], kTileBytes);
+          for (int pp = 0; pp < 8; ++pp)
+            for (int cb = 0; cb < 2; ++cb)
+              tma2d(vd + cb * kHalfBytes + pp * 2048, &p.tm_v, cb * 64, rows[pp], &v_full[s]);
+        } else {
+          const int c0 = (j - n_doc) * kTile;
+          mt.kind = 1;
+          mt.c0 = c0;
+          mt.full = 0;
+          mbar_arrive_expect_tx(&k_full[s], kTileBytes);
+          for (int cb = 0; cb < 2; ++cb)
+            tma3d(kd + cb * kHalfBytes, &p.tm_knew, cb * 64, h, qbeg + c0, &k_full[s]);
+          mbar_arrive_expect_tx(&v_full[s], kTileBytes);
+          for (int cb = 0; cb < 2; ++cb)
+            tma3d(vd + cb * kHalfBytes, &p.tm_vnew, cb * 64, h, qbeg + c0, &v_full[s]);
+        }
+        ++issued[s];
+      }
+      // Drain: every copy issued into a stage has landed before the CTA may exit.
+      mbar_wait(q_full, 0, lim);
+      for (int s = 0; s < kNS; ++s)
+        if (issued[s] > 0) {
+          mbar_wait(&k_full[s], (issued[s] - 1) & 1, lim);
+          mbar_wait(&v_full[s], (issued[s] - 1) & 1, lim);
+        }
+    }
+  } else if (warp == 1) {
+    // ============================== MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_qk = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) |
+                                ((128u >> 4) << 24);
+      const uint32_t idesc_pv = idesc_qk | (1u << 16);  // B (= V) MN-major
+      const uint32_t q_addr = smem_u32(Qs), k_addr = smem_u32(Ks), v_addr = smem_u32(Vs);
+      bool ok = cta_wait(q_rot, 0, abort, lim, p.err);
+      tc_fence_after();
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        const int s = j % kNS;
+        const uint32_t par = (j / kNS) & 1;
+        if (!cta_wait(&k_rot[s], par, abort, lim, p.err)) break;
+        tc_fence_after();
+        for (int i = 0; i < 2; ++i) {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+            mma_ss(tmem + i * 128, sdesc(q_addr + i * kTileBytes + off, 16, 1024),
+                   sdesc(k_addr + s * kTileBytes + off, 16, 1024), idesc_qk, kk > 0);
+          }
+          mma_commit(&s_full[i]);
+        }
+        if (!cta_wait(&v_full[s], par, abort, lim, p.err)) break;
+        for (int i = 0; i < 2 && ok; ++i) {
+          if (!cta_wait(&p_ready[i], j & 1, abort, lim, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tmem + 256 + i * 128, tmem + i * 128 + kk * 8,
+                   sdesc(v_addr + s * kTileBytes + kk * 2048, kHalfBytes, 1024), idesc_pv,
+                   (j > 0 || kk > 0) ? 1 : 0);
+        }
+        mma_commit(&kv_empty[s]);
+      }
+      mma_commit(o_final);
+      // MMAs still in flight must finish before TMEM is released.
+      mbar_wait(o_final, 0, lim);
+    }
+  } else if (warp >= 4 && warp < 12) {
+    // ============================== softmax (Q tile i, TMEM lane quadrant warp % 4)
+    const int i = (warp - 4) >> 2;
+    const int row = (warp & 3) * 32 + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint32_t s_col = lane_base + i * 128, o_col = lane_base + 256 + i * 128;
+    const int t_row = t0 + i * TQ + row / G;
+    const float sl2 = p.scale_log2;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_tiles; ++j) {
+      if (!cta_wait(&s_full[i], j & 1, abort, lim, p.err)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const TileMeta &mt = meta[j % kNS];
+      const bool doc = mt.kind == 0;
+      const bool need_mask = !(doc && mt.full);
+      // Valid keys as a 128-bit mask (bit c = key column c).
+      uint32_t vm[4] = {0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu};
+      if (need_mask) {
+        if (doc) {
+#pragma unroll
+          for (int pp = 0; pp < 8; ++pp) {
+            const int nv = mt.nv[pp];
+            const uint32_t bits = nv >= 16 ? 0xFFFFu : ((1u << nv) - 1u);
+            vm[pp >> 1] = (pp & 1) ? ((vm[pp >> 1] & 0x0000FFFFu) | (bits << 16))
+                                   : ((vm[pp >> 1] & 0xFFFF0000u) | bits);
+          }
+        } else {
+          // key token kt = c0 + c visible iff kt <= t_row and kt < Tb
+          const int lim_tok = min(t_row, Tb - 1) - mt.c0;  // last visible column
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            const int hi = lim_tok - 32 * w;  // columns 32w .. 32w + hi visible
+            vm[w] = hi < 0 ? 0u : (hi >= 31 ? 0xFFFFFFFFu : ((2u << hi) - 1u));
+          }
+        }
+      }
+      // pass 1: row max of the raw scores
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tmem_ld32(s_col + c * 32, r);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float v = ((vm[c] >> e) & 1u) ? __uint_as_float(r[e]) : -INFINITY;
+          mx = fmaxf(mx, v);
+        }
+      }
+      const float mx2 = mx * sl2;
+      float m_use = m_run, alpha = 1.f;
+      if (mx2 > m_run + 8.f) {  // includes the first finite max (m_run = -inf)
+        m_use = mx2;
+        alpha = (m_run == -INFINITY) ? 0.f : exp2f(m_run - mx2);
+      }
+      // O *= alpha for rows whose max moved (warp-collective TMEM access); O holds data only
+      // after the first tile's PV.
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tmem_ld32(o_col + c * 32, r);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+          tmem_st32(o_col + c * 32, r);
+        }
+      }
+      // pass 2: p = 2^(s*scale*log2e - m), packed to bf16 pairs into S's first 64 columns
+      float lp = 0.f;
+      const float neg_m = (m_use == -INFINITY) ? 0.f : -m_use;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pw[32];
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c = half * 2 + cc;
+          uint32_t r[32];
+          tmem_ld32(s_col + c * 32, r);
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float s0 = ((vm[c] >> e) & 1u)
+                                 ? exp2f(fmaf(__uint_as_float(r[e]), sl2, neg_m)) : 0.f;
+            const float s1 = ((vm[c] >> (e + 1)) & 1u)
+                                 ? exp2f(fmaf(__uint_as_float(r[e + 1]), sl2, neg_m)) : 0.f;
+            lp += s0 + s1;
+            pw[cc * 16 + e / 2] = pack_bf2(s0, s1);
+          }
+        }
+        tmem_st32(s_col + half * 32, pw);
+      }
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      l_run = l_run * alpha + lp;
+      m_run = m_use;
+      tc_fence_before();
+      mbar_arrive(&p_ready[i]);
+    }
+    // epilogue: O / l -> bf16 rows, lse
+    ok = ok && cta_wait(o_final, 0, abort, lim, p.err);
+    if (ok) {
+      tc_fence_after();
+      const bool valid_row = t_row < Tb;
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      const int qh = h * G + row % G;
+      __nv_bfloat16 *dst = p.out + ((size_t)(qbeg + t_row) * p.hq + qh) * 128;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tmem_ld32(o_col + c * 32, r);
+        if (valid_row) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 8) {
+            float f[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) f[k] = l_run > 0.f ? __uint_as_float(r[e + k]) * inv : 0.f;
+            *reinterpret_cast<uint4 *>(dst + c * 32 + e) = pack16<__nv_bfloat16>(f);
+          }
+        }
+      }
+      if (valid_row)
+        p.lse[(size_t)(qbeg + t_row) * p.hq + qh] =
+            l_run > 0.f ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+    }
+  } else if (warp >= 12) {
+    // ============================== rotation (128 threads: chunk c, 8 consecutive rows)
+    // One thread takes every bounded-wait decision and broadcasts it, so the group's named
+    // barriers are always reached by all 128 threads.
+    const int tr = tid - 384;
+    const int c = tr & 7, rg = tr >> 3;  // rows 8rg .. 8rg+7
+    const uint64_t *turn = p.turn;
+    volatile int *decision = reinterpret_cast<volatile int *>(bars + 18);
+    if (tr == 0) *decision = cta_wait(q_full, 0, abort, lim, p.err) ? 1 : 0;
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    bool ok = *decision != 0;
+    if (ok) {
+      mbar_wait(q_full, 0, lim);  // completed: acquires the copied tile for this thread
+      for (int i = 0; i < 2; ++i) {
+        for (int rr = 0; rr < 8; ++rr) {
+          const int row = rg * 8 + rr;
+          const int64_t delta = (int64_t)(i * TQ + row / G);  // query position - m0
+          float2 cs[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) rope_cos_sin(delta, turn[c * 8 + e], cs[e].x, cs[e].y);
+          rotate_row_chunk(Qs + i * kTileBytes, row, c, cs);
+        }
+      }
+      fence_async_smem();
+    }
+    mbar_arrive(q_rot);
+    // table slot of this thread: page tp, frequencies 4*tf .. 4*tf+3
+    const int tp = tr >> 4, tf = tr & 15;
+    int64_t cached_off = INT64_MIN;
+    for (int j = 0; ok && j < n_tiles; ++j) {
+      const int s = j % kNS;
+      const uint32_t par = (j / kNS) & 1;
+      asm volatile("bar.sync 1, 128;" ::: "memory");  // everyone read the last decision
+      if (tr == 0) *decision = cta_wait(&k_full[s], par, abort, lim, p.err) ? 1 : 0;
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (*decision == 0) break;
+      mbar_wait(&k_full[s], par, lim);  // completed: acquires the copied tile for this thread
+      const TileMeta &mt = meta[s];
+      uint8_t *kt = Ks + s * kTileBytes;
+      if (mt.kind == 0) {
+        // one relative rotation R(o - m0) per page: a (cos, sin) table per page offset
+        const int64_t d = (int64_t)mt.off[tp] - m0;
+        if (d != cached_off) {
+          cached_off = d;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float cc, ss;
+            rope_cos_sin(d, turn[tf * 4 + e], cc, ss);
+            tab[tp * 64 + tf * 4 + e] = make_float2(cc, ss);
+          }
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        const int pg = rg >> 1;  // 8 rows of one 16-row page
+        float2 cs[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) cs[e] = tab[pg * 64 + c * 8 + e];
+#pragma unroll
+        for (int rr = 0; rr < 8; ++rr) rotate_row_chunk(kt, rg * 8 + rr, c, cs);
+      } else {
+        // question keys: raw, rotated by R(p - m0) row by row
+        for (int rr = 0; rr < 8; ++rr) {
+          const int row = rg * 8 + rr;
+          const int64_t delta = (int64_t)(mt.c0 + row - t0);
+          float2 cs[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) rope_cos_sin(delta, turn[c * 8 + e], cs[e].x, cs[e].y);
+          rotate_row_chunk(kt, row, c, cs);
+        }
+      }
+      fence_async_smem();
+      mbar_arrive(&k_rot[s]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem));
+  }
+}
+
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// bf16 tensor [dims[rank-1]]...[dims[0]] (dims innermost first), 128B swizzle, zero OOB fill.
+int make_map(CUtensorMap *m, void *base, int rank, const cuuint64_t *dims,
+             const cuuint64_t *strides_bytes, const cuuint32_t *box) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) {
+    record_msg("cuTensorMapEncodeTiled is unavailable");
+    return LAZY_ERR_CUDA;
+  }
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, base, dims, strides_bytes, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    record_msg("cuTensorMapEncodeTiled rejected a tensor map");
+    return LAZY_ERR_CUDA;
+  }
+  return LAZY_OK;
+}
+
+}  // namespace
+
 int prefill_tc_supported(const lazy_pool *p, int32_t hq) {
-  (void)p;
-  (void)hq;
-  return LAZY_ERR_UNSUPPORTED;
+  if (p->dtype != LAZY_DTYPE_BF16 || p->d != 128 || p->page_size != kPage)
+    return LAZY_ERR_UNSUPPORTED;
+  if (hq % p->hkv) return LAZY_ERR_INVALID_ARG;
+  const int g = hq / p->hkv;
+  if (g != 1 && g != 2 && g != 4 && g != 8) return LAZY_ERR_UNSUPPORTED;
+  return LAZY_OK;
 }
+
 int prefill_tc(lazy_pool *p, const PrefillParams &pp, int32_t max_q_len, cudaStream_t s) {
-  (void)p; (void)pp; (void)max_q_len; (void)s;
-  return LAZY_ERR_UNSUPPORTED;
+  TcParams tp;
+  memset(&tp, 0, sizeof(tp));
+  int rc;
+  {
+    // Pool page maps: rows (block * Hkv + h) * 16 + slot, 128 dims; box 16 rows x 64 dims.
+    std::lock_guard<std::mutex> g(p->mu);
+    if (!p->tmaps_ready) {
+      const cuuint64_t dims[2] = {128, (cuuint64_t)p->num_blocks * p->hkv * kPage};
+      const cuuint64_t strides[1] = {256};
+      const cuuint32_t box[2] = {64, 16};
+      rc = make_map(reinterpret_cast<CUtensorMap *>(p->tmap_k), p->k, 2, dims, strides, box);
+      if (rc != LAZY_OK) return rc;
+      rc = make_map(reinterpret_cast<CUtensorMap *>(p->tmap_v), p->v, 2, dims, strides, box);
+      if (rc != LAZY_OK) return rc;
+      p->tmaps_ready = true;
+    }
+    memcpy(&tp.tm_k, p->tmap_k, sizeof(CUtensorMap));
+    memcpy(&tp.tm_v, p->tmap_v, sizeof(CUtensorMap));
+  }
+  const int G = pp.G, TQ = 128 / G;
+  {
+    const cuuint64_t dims[3] = {128, (cuuint64_t)pp.hq, (cuuint64_t)pp.total_q};
+    const cuuint64_t strides[2] = {256, (cuuint64_t)pp.hq * 256};
+    const cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)TQ};
+    rc = make_map(&tp.tm_q, const_cast<void *>(pp.q), 3, dims, strides, box);
+    if (rc != LAZY_OK) return rc;
+  }
+  if (pp.k_new) {
+    const cuuint64_t dims[3] = {128, (cuuint64_t)pp.hkv, (cuuint64_t)pp.total_q};
+    const cuuint64_t strides[2] = {256, (cuuint64_t)pp.hkv * 256};
+    const cuuint32_t box[3] = {64, 1, 128};
+    rc = make_map(&tp.tm_knew, const_cast<void *>(pp.k_new), 3, dims, strides, box);
+    if (rc != LAZY_OK) return rc;
+    rc = make_map(&tp.tm_vnew, const_cast<void *>(pp.v_new), 3, dims, strides, box);
+    if (rc != LAZY_OK) return rc;
+  }
+  tp.cu_q = pp.cu_q;
+  tp.q_pos0 = pp.q_pos0;
+  tp.words = pp.words;
+  tp.cu_pages = pp.cu_pages;
+  tp.turn = pp.turn;
+  tp.out = reinterpret_cast<__nv_bfloat16 *>(pp.out);
+  tp.lse = pp.lse;
+  tp.err = pp.err;
+  tp.batch = pp.batch;
+  tp.hkv = pp.hkv;
+  tp.hq = pp.hq;
+  tp.num_blocks = pp.num_blocks;
+  tp.G = G;
+  tp.TQ = TQ;
+  tp.has_new = pp.k_new != nullptr;
+  tp.scale_log2 = pp.scale_log2;
+  tp.wait_ns = pp.wait_ns;
+  static bool attr = false;
+  if (!attr) {
+    LAZY_CUDA_TRY(cudaFuncSetAttribute(prefill_tc_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes));
+    attr = true;
+  }
+  dim3 grid((max_q_len + 2 * TQ - 1) / (2 * TQ), pp.hkv, pp.batch);
+  prefill_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(tp);
+  LAZY_CUDA_TRY(cudaGetLastError());
+  return LAZY_OK;
 }
+
 }  // namespace lazy
