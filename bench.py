@@ -143,6 +143,45 @@ def _timed_steps(fn, steps, flush, stream):
     return [a.elapsed_time(b) for a, b in times]
 
 
+def bench_prefill_only(args):
+    """Prefill workload alone (pool sized to the documents used): for profiling runs."""
+    import torch
+
+    import position_independent_kv_lazy_gb300 as pk
+    import workload as W
+    from position_independent_kv_lazy_gb300 import harness as H
+
+    pk.build_library()
+    pk.load_library()
+    _, tc_peak, _, peak_kind = _peaks()
+    stream = torch.cuda.current_stream()
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    pwl = W.prefill_workload()
+    psrc = H.DeviceSource(pwl)
+    pres = H.build_resident(pwl, psrc, resident_pool=False)
+    pb = H.prefill_batch(pwl, pres, psrc)
+    pout = torch.empty_like(pb.q)
+    plse = torch.empty((pb.total_q, pwl.Hq), dtype=torch.float32, device="cuda")
+
+    def prefill_call():
+        pk.lazy_attn_prefill(pres.pool, pb.q, pb.k_new, pb.v_new, pb.cu_q, pb.q_pos0, pb.words,
+                             pb.cu_pages, pb.max_q_len, sm_scale=pwl.sm_scale, out=pout, lse=plse)
+
+    for _ in range(args.warmup):
+        prefill_call()
+    torch.cuda.synchronize()
+    if pk.lazy_get_device_error(pres.pool) != 0:
+        raise RuntimeError("device error during warm-up")
+    torch.cuda.nvtx.range_push("timed_region")
+    ms = _timed_steps(prefill_call, args.steps, flush_buf.zero_, stream)
+    torch.cuda.nvtx.range_pop()
+    avg = sum(ms) / len(ms)
+    tflops = pb.flops / (avg * 1e-3) / 1e12
+    print(json.dumps({"mode": "prefill only", "value": round(tflops, 2), "unit": "TFLOP/s",
+                      "ms_per_call": round(avg, 4), "frac": round(tflops / tc_peak, 4),
+                      "peak_kind": peak_kind, "steps": args.steps}), flush=True)
+
+
 def bench_ours(args):
     import numpy as np
     import torch
@@ -446,13 +485,16 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["all", "decode"], default="all",
-                    help="decode: time only the headline decode workload (smaller footprint)")
+    ap.add_argument("--only", choices=["all", "decode", "prefill"], default="all",
+                    help="decode / prefill: time only that workload (smaller footprint, for "
+                         "profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         bench_reference(args)
+    elif args.only == "prefill":
+        bench_prefill_only(args)
     else:
         bench_ours(args)
 

@@ -35,27 +35,38 @@ namespace lazy {
 namespace {
 
 constexpr int kTile = 128;
-constexpr int kNS = 2;
+constexpr int kNK = 3;  // K ring: a K tile is free again as soon as both QK products read it
+constexpr int kNV = 2;  // V ring: freed after both PV products
 constexpr int kThreads = 512;
 constexpr int kTileBytes = kTile * 128 * 2;  // 32 KB: 128 rows x 128 bf16
 constexpr int kHalfBytes = kTileBytes / 2;   // one 64-dim box column
 
 // Shared-memory map (offsets from a 1024-aligned base).
 constexpr int kOffQ = 0;                               // 2 Q tiles
-constexpr int kOffK = kOffQ + 2 * kTileBytes;          // kNS K stages
-constexpr int kOffV = kOffK + kNS * kTileBytes;        // kNS V stages
-constexpr int kOffTab = kOffV + kNS * kTileBytes;      // float2 [8 pages][64]
-constexpr int kOffMeta = kOffTab + 8 * 64 * 8;         // TileMeta [kNS]
-constexpr int kOffBar = kOffMeta + kNS * 128;          // barriers
-constexpr int kSmemBytes = kOffBar + 256 + 1024;       // + alignment slack
+constexpr int kOffK = kOffQ + 2 * kTileBytes;          // kNK K stages
+constexpr int kOffV = kOffK + kNK * kTileBytes;        // kNV V stages
+constexpr int kNM = 4;  // softmax metadata ring (see SMeta)
+constexpr int kOffMetaK = kOffV + kNV * kTileBytes;    // KMeta [kNK]
+constexpr int kOffMetaS = kOffMetaK + kNK * 48;        // SMeta [kNM]
+constexpr int kOffBar = kOffMetaS + kNM * 48 + 16;     // barriers (8-byte aligned)
+constexpr int kSmemBytes = kOffBar + 192 + 1024;       // + alignment slack
 
-struct TileMeta {
-  int32_t kind;      // 0 = document pages, 1 = question keys
-  int32_t c0;        // question tile: first key token
-  int32_t full;      // document tile: every page present and full
+// Read by the rotation group (valid until the K stage is refilled, after QK of this tile).
+struct KMeta {
+  int32_t kind;   // 0 = document pages, 1 = question keys
+  int32_t c0;     // question tile: first key token
+  int32_t off[8]; // document tile: logical offset of each page
+  int32_t pad[2];
+};
+// Read by the softmax groups. Written when tile j's K copy is issued, which precedes S_j; the
+// slot is rewritten for tile j + 4, whose K copy waits for QK of tile j + 1, which the MMA
+// issuer only starts after both softmax groups released tile j.
+struct SMeta {
+  int32_t kind;
+  int32_t c0;
+  int32_t full;   // document tile: every page present and full
   int32_t pad;
-  int32_t off[8];    // document tile: logical offset of each page
-  int32_t nv[8];     // document tile: valid tokens per page (0 = absent / bad)
+  int32_t nv[8];  // document tile: valid tokens per page (0 = absent / bad)
 };
 
 struct TcParams {
@@ -156,32 +167,55 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       : "memory");
 }
 
+// 2^x with one MUFU instruction (inputs here are <= 8, results in (0, 256]; -inf gives 0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// Rotate, in place, 8 consecutive rows of a 128-row swizzled bf16 tile at 16-byte chunk c of
-// both 64-dim boxes: x_i <- x_i cos - x_{i+64} sin, x_{i+64} <- x_i sin + x_{i+64} cos,
-// i = 8c .. 8c+7. cs[e] = (cos, sin) of frequency 8c + e for each row (per-row tables when
-// `per_row`).
+// Rotate, in place, one row of a 128-row swizzled bf16 tile at 16-byte chunk c of both 64-dim
+// boxes: x_i <- x_i cos - x_{i+64} sin, x_{i+64} <- x_i sin + x_{i+64} cos for i = 8c .. 8c+7.
+// cs2[k] = (cos, cos) pairs and sn2[k] = (sin, sin) pairs of frequencies 8c+2k, 8c+2k+1.
 __device__ __forceinline__ void rotate_row_chunk(uint8_t *tile, int row, int c,
-                                                 const float2 (&cs)[8]) {
+                                                 const float2 (&co)[4], const float2 (&si)[4]) {
   const int phys = (c ^ (row & 7)) * 16;
   uint4 *lo = reinterpret_cast<uint4 *>(tile + row * 128 + phys);
   uint4 *hi = reinterpret_cast<uint4 *>(tile + kHalfBytes + row * 128 + phys);
   const uint4 a = *lo, b = *hi;
-  float x[8], y[8];
-  unpack16<__nv_bfloat16>(a, x);
-  unpack16<__nv_bfloat16>(b, y);
-  float xo[8], yo[8];
+  const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+  uint32_t xo[4], yo[4];
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    xo[e] = x[e] * cs[e].x - y[e] * cs[e].y;
-    yo[e] = x[e] * cs[e].y + y[e] * cs[e].x;
+  for (int k = 0; k < 4; ++k) {
+    const float2 x = make_float2(__uint_as_float(aw[k] << 16), __uint_as_float(aw[k] & 0xFFFF0000u));
+    const float2 y = make_float2(__uint_as_float(bw[k] << 16), __uint_as_float(bw[k] & 0xFFFF0000u));
+    const float2 nsi = make_float2(-si[k].x, -si[k].y);
+    const float2 xr = __ffma2_rn(y, nsi, __fmul2_rn(x, co[k]));
+    const float2 yr = __ffma2_rn(x, si[k], __fmul2_rn(y, co[k]));
+    __nv_bfloat162 hx = __floats2bfloat162_rn(xr.x, xr.y), hy = __floats2bfloat162_rn(yr.x, yr.y);
+    xo[k] = *reinterpret_cast<uint32_t *>(&hx);
+    yo[k] = *reinterpret_cast<uint32_t *>(&hy);
   }
-  *lo = pack16<__nv_bfloat16>(xo);
-  *hi = pack16<__nv_bfloat16>(yo);
+  *lo = make_uint4(xo[0], xo[1], xo[2], xo[3]);
+  *hi = make_uint4(yo[0], yo[1], yo[2], yo[3]);
+}
+
+// (cos, sin) of delta * theta_i for i = 8c .. 8c+7, as pairs.
+__device__ __forceinline__ void chunk_angles(int64_t delta, const uint64_t *turn, int c,
+                                             float2 (&co)[4], float2 (&si)[4]) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    float c0, s0, c1, s1;
+    rope_cos_sin(delta, turn[c * 8 + 2 * k], c0, s0);
+    rope_cos_sin(delta, turn[c * 8 + 2 * k + 1], c1, s1);
+    co[k] = make_float2(c0, c1);
+    si[k] = make_float2(s0, s1);
+  }
 }
 
 // Bounded wait that also gives up when another role raised the CTA abort flag.
@@ -207,14 +241,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   uint8_t *Qs = sm + kOffQ;
   uint8_t *Ks = sm + kOffK;
   uint8_t *Vs = sm + kOffV;
-  float2 *tab = reinterpret_cast<float2 *>(sm + kOffTab);
-  TileMeta *meta = reinterpret_cast<TileMeta *>(sm + kOffMeta);
+  KMeta *meta_k = reinterpret_cast<KMeta *>(sm + kOffMetaK);
+  SMeta *meta_s = reinterpret_cast<SMeta *>(sm + kOffMetaS);
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kOffBar);
   uint64_t *q_full = bars + 0, *q_rot = bars + 1;
-  uint64_t *k_full = bars + 2, *v_full = bars + 4, *k_rot = bars + 6, *kv_empty = bars + 8;
-  uint64_t *s_full = bars + 10, *p_ready = bars + 12, *o_final = bars + 14;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 16);
-  volatile int *abort = reinterpret_cast<volatile int *>(bars + 17);  // bars + 18: rotation flag
+  uint64_t *k_full = bars + 2, *k_rot = bars + 5, *k_empty = bars + 8;     // [kNK]
+  uint64_t *v_full = bars + 11, *v_empty = bars + 13;                     // [kNV]
+  uint64_t *s_full = bars + 15, *p_ready = bars + 17, *o_final = bars + 19;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 20);
+  volatile int *abort = reinterpret_cast<volatile int *>(bars + 21);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.z, h = blockIdx.y;
@@ -233,11 +268,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   if (tid == 0) {
     mbar_init(q_full, 1);
     mbar_init(q_rot, 128);
-    for (int s = 0; s < kNS; ++s) {
+    for (int s = 0; s < kNK; ++s) {
       mbar_init(&k_full[s], 1);
-      mbar_init(&v_full[s], 1);
       mbar_init(&k_rot[s], 128);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < kNV; ++s) {
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
@@ -260,69 +298,104 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   const uint64_t lim = p.wait_ns;
 
   if (warp == 0) {
-    // ============================== producer
+    // ============================== producer: K runs one tile ahead of V
     if (lane == 0) {
       mbar_arrive_expect_tx(q_full, 2 * kTileBytes);
       for (int i = 0; i < 2; ++i)
         for (int cb = 0; cb < 2; ++cb)
           tma3d(Qs + i * kTileBytes + cb * kHalfBytes, &p.tm_q, cb * 64, h * G,
                 qbeg + t0 + i * TQ, q_full);
-      int issued[kNS] = {0, 0};
-      for (int j = 0; j < n_tiles; ++j) {
-        const int s = j % kNS;
-        if (j >= kNS && !cta_wait(&kv_empty[s], ((j / kNS) - 1) & 1, abort, lim, p.err)) break;
-        TileMeta &mt = meta[s];
-        uint8_t *kd = Ks + s * kTileBytes, *vd = Vs + s * kTileBytes;
-        if (j < n_doc) {
-          int32_t rows[8];
-          int full = 1;
-          for (int pp = 0; pp < 8; ++pp) {
-            const int pg = j * 8 + pp;
-            const uint64_t w = p.words[pg0 + min(pg, npg - 1)];
-            uint32_t blk = word_block(w);
-            int nv = (int)word_nvalid(w);
-            if (blk >= (uint32_t)p.num_blocks || nv > kPage) {
-              set_error(p.err, LAZY_DEVERR_BAD_PAGE);
-              blk = 0;
-              nv = 0;
-            }
-            if (pg >= npg) nv = 0;  // absent page: the last one is loaded again, masked
-            full &= (nv == kPage);
-            mt.off[pp] = (int32_t)word_offset(w);
-            mt.nv[pp] = nv;
-            rows[pp] = (int32_t)((blk * (uint32_t)p.hkv + (uint32_t)h) * kPage);
+      // page words of the next document tile, loaded one tile ahead
+      uint64_t wnext[8];
+      auto load_words = [&](int j) {
+#pragma unroll
+        for (int pp = 0; pp < 8; ++pp) wnext[pp] = p.words[pg0 + min(j * 8 + pp, npg - 1)];
+      };
+      if (n_doc > 0) load_words(0);
+      int32_t rows[kNK][8];
+      int k_issued[kNK] = {0, 0, 0}, v_issued[kNV] = {0, 0};
+      bool ok = true;
+      for (int e = 0; ok && e <= n_tiles; ++e) {
+        if (e < n_tiles) {  // ---- K of tile e
+          const int j = e, s = j % kNK;
+          if (j >= kNK && !cta_wait(&k_empty[s], ((j / kNK) - 1) & 1, abort, lim, p.err)) {
+            ok = false;
+            break;
           }
-          mt.kind = 0;
-          mt.full = full;
-          mbar_arrive_expect_tx(&k_full[s], kTileBytes);
-          for (int pp = 0; pp < 8; ++pp)
+          KMeta &mk = meta_k[s];
+          SMeta &ms = meta_s[j % kNM];
+          uint8_t *kd = Ks + s * kTileBytes;
+          if (j < n_doc) {
+            int full = 1;
+            uint64_t w[8];
+#pragma unroll
+            for (int pp = 0; pp < 8; ++pp) w[pp] = wnext[pp];
+            if (j + 1 < n_doc) load_words(j + 1);
+            mk.kind = 0;
+#pragma unroll
+            for (int pp = 0; pp < 8; ++pp) {
+              uint32_t blk = word_block(w[pp]);
+              int nv = (int)word_nvalid(w[pp]);
+              if (blk >= (uint32_t)p.num_blocks || nv > kPage) {
+                set_error(p.err, LAZY_DEVERR_BAD_PAGE);
+                blk = 0;
+                nv = 0;
+              }
+              if (j * 8 + pp >= npg) nv = 0;  // absent page: the last one is loaded again, masked
+              ms.nv[pp] = nv;
+              full &= (nv == kPage);
+              mk.off[pp] = (int32_t)word_offset(w[pp]);
+              rows[s][pp] = (int32_t)((blk * (uint32_t)p.hkv + (uint32_t)h) * kPage);
+            }
+            ms.kind = 0;
+            ms.full = full;
+            mbar_arrive_expect_tx(&k_full[s], kTileBytes);
+#pragma unroll
+            for (int pp = 0; pp < 8; ++pp)
+              for (int cb = 0; cb < 2; ++cb)
+                tma2d(kd + cb * kHalfBytes + pp * 2048, &p.tm_k, cb * 64, rows[s][pp],
+                      &k_full[s]);
+          } else {
+            const int c0 = (j - n_doc) * kTile;
+            mk.kind = 1;
+            mk.c0 = c0;
+            ms.kind = 1;
+            ms.c0 = c0;
+            ms.full = 0;
+            mbar_arrive_expect_tx(&k_full[s], kTileBytes);
             for (int cb = 0; cb < 2; ++cb)
-              tma2d(kd + cb * kHalfBytes + pp * 2048, &p.tm_k, cb * 64, rows[pp], &k_full[s]);
-          mbar_arrive_expect_tx(&v_full[s], kTileBytes);
-          for (int pp = 0; pp < 8; ++pp)
-            for (int cb = 0; cb < 2; ++cb)
-              tma2d(vd + cb * kHalfBytes + pp * 2048, &p.tm_v, cb * 64, rows[pp], &v_full[s]);
-        } else {
-          const int c0 = (j - n_doc) * kTile;
-          mt.kind = 1;
-          mt.c0 = c0;
-          mt.full = 0;
-          mbar_arrive_expect_tx(&k_full[s], kTileBytes);
-          for (int cb = 0; cb < 2; ++cb)
-            tma3d(kd + cb * kHalfBytes, &p.tm_knew, cb * 64, h, qbeg + c0, &k_full[s]);
-          mbar_arrive_expect_tx(&v_full[s], kTileBytes);
-          for (int cb = 0; cb < 2; ++cb)
-            tma3d(vd + cb * kHalfBytes, &p.tm_vnew, cb * 64, h, qbeg + c0, &v_full[s]);
+              tma3d(kd + cb * kHalfBytes, &p.tm_knew, cb * 64, h, qbeg + c0, &k_full[s]);
+          }
+          ++k_issued[s];
         }
-        ++issued[s];
+        if (e >= 1) {  // ---- V of tile e - 1
+          const int j = e - 1, s = j % kNV, sk = j % kNK;
+          if (j >= kNV && !cta_wait(&v_empty[s], ((j / kNV) - 1) & 1, abort, lim, p.err)) {
+            ok = false;
+            break;
+          }
+          uint8_t *vd = Vs + s * kTileBytes;
+          mbar_arrive_expect_tx(&v_full[s], kTileBytes);
+          if (j < n_doc) {
+#pragma unroll
+            for (int pp = 0; pp < 8; ++pp)
+              for (int cb = 0; cb < 2; ++cb)
+                tma2d(vd + cb * kHalfBytes + pp * 2048, &p.tm_v, cb * 64, rows[sk][pp],
+                      &v_full[s]);
+          } else {
+            const int c0 = (j - n_doc) * kTile;
+            for (int cb = 0; cb < 2; ++cb)
+              tma3d(vd + cb * kHalfBytes, &p.tm_vnew, cb * 64, h, qbeg + c0, &v_full[s]);
+          }
+          ++v_issued[s];
+        }
       }
       // Drain: every copy issued into a stage has landed before the CTA may exit.
       mbar_wait(q_full, 0, lim);
-      for (int s = 0; s < kNS; ++s)
-        if (issued[s] > 0) {
-          mbar_wait(&k_full[s], (issued[s] - 1) & 1, lim);
-          mbar_wait(&v_full[s], (issued[s] - 1) & 1, lim);
-        }
+      for (int s = 0; s < kNK; ++s)
+        if (k_issued[s] > 0) mbar_wait(&k_full[s], (k_issued[s] - 1) & 1, lim);
+      for (int s = 0; s < kNV; ++s)
+        if (v_issued[s] > 0) mbar_wait(&v_full[s], (v_issued[s] - 1) & 1, lim);
     }
   } else if (warp == 1) {
     // ============================== MMA issuer
@@ -331,36 +404,57 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                                 ((128u >> 4) << 24);
       const uint32_t idesc_pv = idesc_qk | (1u << 16);  // B (= V) MN-major
       const uint32_t q_addr = smem_u32(Qs), k_addr = smem_u32(Ks), v_addr = smem_u32(Vs);
+      // Issue order keeps both softmax groups busy: QK for Q tile 0 of the next key tile is
+      // issued as soon as P_0 of this tile is consumed, while group 1 still works on S_1.
+      auto qk = [&](int j, int i) {
+        const int s = j % kNK;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+          mma_ss(tmem + i * 128, sdesc(q_addr + i * kTileBytes + off, 16, 1024),
+                 sdesc(k_addr + s * kTileBytes + off, 16, 1024), idesc_qk, kk > 0);
+        }
+        mma_commit(&s_full[i]);
+      };
+      auto pv = [&](int j, int i) {
+        const int s = j % kNV;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tmem + 256 + i * 128, tmem + i * 128 + kk * 8,
+                 sdesc(v_addr + s * kTileBytes + kk * 2048, kHalfBytes, 1024), idesc_pv,
+                 (j > 0 || kk > 0) ? 1 : 0);
+      };
       bool ok = cta_wait(q_rot, 0, abort, lim, p.err);
       tc_fence_after();
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        const int s = j % kNS;
-        const uint32_t par = (j / kNS) & 1;
-        if (!cta_wait(&k_rot[s], par, abort, lim, p.err)) break;
-        tc_fence_after();
-        for (int i = 0; i < 2; ++i) {
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-            mma_ss(tmem + i * 128, sdesc(q_addr + i * kTileBytes + off, 16, 1024),
-                   sdesc(k_addr + s * kTileBytes + off, 16, 1024), idesc_qk, kk > 0);
-          }
-          mma_commit(&s_full[i]);
-        }
-        if (!cta_wait(&v_full[s], par, abort, lim, p.err)) break;
-        for (int i = 0; i < 2 && ok; ++i) {
-          if (!cta_wait(&p_ready[i], j & 1, abort, lim, p.err)) {
-            ok = false;
-            break;
-          }
+      if (ok && n_tiles > 0) {
+        ok = cta_wait(&k_rot[0], 0, abort, lim, p.err);
+        if (ok) {
           tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ts(tmem + 256 + i * 128, tmem + i * 128 + kk * 8,
-                   sdesc(v_addr + s * kTileBytes + kk * 2048, kHalfBytes, 1024), idesc_pv,
-                   (j > 0 || kk > 0) ? 1 : 0);
+          qk(0, 0);
+          qk(0, 1);
+          mma_commit(&k_empty[0]);
         }
-        mma_commit(&kv_empty[s]);
+      }
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        const bool more = j + 1 < n_tiles;
+        const int sn = (j + 1) % kNK;
+        if (!cta_wait(&v_full[j % kNV], (j / kNV) & 1, abort, lim, p.err)) break;
+        if (!cta_wait(&p_ready[0], j & 1, abort, lim, p.err)) break;
+        tc_fence_after();
+        pv(j, 0);
+        if (more) {
+          if (!cta_wait(&k_rot[sn], ((j + 1) / kNK) & 1, abort, lim, p.err)) break;
+          tc_fence_after();
+          qk(j + 1, 0);
+        }
+        if (!cta_wait(&p_ready[1], j & 1, abort, lim, p.err)) break;
+        tc_fence_after();
+        pv(j, 1);
+        mma_commit(&v_empty[j % kNV]);
+        if (more) {
+          qk(j + 1, 1);
+          mma_commit(&k_empty[sn]);
+        }
       }
       mma_commit(o_final);
       // MMAs still in flight must finish before TMEM is released.
@@ -382,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         break;
       }
       tc_fence_after();
-      const TileMeta &mt = meta[j % kNS];
+      const SMeta &mt = meta_s[j % kNM];
       const bool doc = mt.kind == 0;
       const bool need_mask = !(doc && mt.full);
       // Valid keys as a 128-bit mask (bit c = key column c).
@@ -408,21 +502,30 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       }
       // pass 1: row max of the raw scores
       float mx = -INFINITY;
+      if (need_mask) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld32(s_col + c * 32, r);
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tmem_ld32(s_col + c * 32, r);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float v = ((vm[c] >> e) & 1u) ? __uint_as_float(r[e]) : -INFINITY;
-          mx = fmaxf(mx, v);
+          for (int e = 0; e < 32; ++e)
+            mx = fmaxf(mx, ((vm[c] >> e) & 1u) ? __uint_as_float(r[e]) : -INFINITY);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tmem_ld32(s_col + c * 32, r);
+#pragma unroll
+          for (int e = 0; e < 32; e += 2)
+            mx = fmaxf(mx, fmaxf(__uint_as_float(r[e]), __uint_as_float(r[e + 1])));
         }
       }
       const float mx2 = mx * sl2;
       float m_use = m_run, alpha = 1.f;
       if (mx2 > m_run + 8.f) {  // includes the first finite max (m_run = -inf)
         m_use = mx2;
-        alpha = (m_run == -INFINITY) ? 0.f : exp2f(m_run - mx2);
+        alpha = (m_run == -INFINITY) ? 0.f : ex2(m_run - mx2);
       }
       // O *= alpha for rows whose max moved (warp-collective TMEM access); O holds data only
       // after the first tile's PV.
@@ -437,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         }
       }
       // pass 2: p = 2^(s*scale*log2e - m), packed to bf16 pairs into S's first 64 columns
-      float lp = 0.f;
+      float2 lp2 = make_float2(0.f, 0.f);
       const float neg_m = (m_use == -INFINITY) ? 0.f : -m_use;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
@@ -447,18 +550,31 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           const int c = half * 2 + cc;
           uint32_t r[32];
           tmem_ld32(s_col + c * 32, r);
+          if (need_mask) {
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const float s0 = ((vm[c] >> e) & 1u)
-                                 ? exp2f(fmaf(__uint_as_float(r[e]), sl2, neg_m)) : 0.f;
-            const float s1 = ((vm[c] >> (e + 1)) & 1u)
-                                 ? exp2f(fmaf(__uint_as_float(r[e + 1]), sl2, neg_m)) : 0.f;
-            lp += s0 + s1;
-            pw[cc * 16 + e / 2] = pack_bf2(s0, s1);
+            for (int e = 0; e < 32; e += 2) {
+              const float s0 = ((vm[c] >> e) & 1u)
+                                   ? ex2(fmaf(__uint_as_float(r[e]), sl2, neg_m)) : 0.f;
+              const float s1 = ((vm[c] >> (e + 1)) & 1u)
+                                   ? ex2(fmaf(__uint_as_float(r[e + 1]), sl2, neg_m)) : 0.f;
+              lp2 = __fadd2_rn(lp2, make_float2(s0, s1));
+              pw[cc * 16 + e / 2] = pack_bf2(s0, s1);
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              const float2 t = __ffma2_rn(
+                  make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])),
+                  make_float2(sl2, sl2), make_float2(neg_m, neg_m));
+              const float s0 = ex2(t.x), s1 = ex2(t.y);
+              lp2 = __fadd2_rn(lp2, make_float2(s0, s1));
+              pw[cc * 16 + e / 2] = pack_bf2(s0, s1);
+            }
           }
         }
         tmem_st32(s_col + half * 32, pw);
       }
+      const float lp = lp2.x + lp2.y;
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       l_run = l_run * alpha + lp;
       m_run = m_use;
@@ -493,71 +609,48 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     }
   } else if (warp >= 12) {
     // ============================== rotation (128 threads: chunk c, 8 consecutive rows)
-    // One thread takes every bounded-wait decision and broadcasts it, so the group's named
-    // barriers are always reached by all 128 threads.
+    // No group barrier: every thread waits for the tile itself, rotates its 8 rows x 16 bytes
+    // (one page) and arrives; (cos, sin) of its page offset stay in registers until the offset
+    // changes (at a document boundary).
     const int tr = tid - 384;
-    const int c = tr & 7, rg = tr >> 3;  // rows 8rg .. 8rg+7
+    const int c = tr & 7, rg = tr >> 3;  // rows 8rg .. 8rg+7, page rg / 2
     const uint64_t *turn = p.turn;
-    volatile int *decision = reinterpret_cast<volatile int *>(bars + 18);
-    if (tr == 0) *decision = cta_wait(q_full, 0, abort, lim, p.err) ? 1 : 0;
-    asm volatile("bar.sync 1, 128;" ::: "memory");
-    bool ok = *decision != 0;
+    bool ok = cta_wait(q_full, 0, abort, lim, p.err);
     if (ok) {
-      mbar_wait(q_full, 0, lim);  // completed: acquires the copied tile for this thread
       for (int i = 0; i < 2; ++i) {
         for (int rr = 0; rr < 8; ++rr) {
           const int row = rg * 8 + rr;
-          const int64_t delta = (int64_t)(i * TQ + row / G);  // query position - m0
-          float2 cs[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) rope_cos_sin(delta, turn[c * 8 + e], cs[e].x, cs[e].y);
-          rotate_row_chunk(Qs + i * kTileBytes, row, c, cs);
+          float2 co[4], si[4];
+          chunk_angles((int64_t)(i * TQ + row / G), turn, c, co, si);  // query pos - m0
+          rotate_row_chunk(Qs + i * kTileBytes, row, c, co, si);
         }
       }
       fence_async_smem();
     }
     mbar_arrive(q_rot);
-    // table slot of this thread: page tp, frequencies 4*tf .. 4*tf+3
-    const int tp = tr >> 4, tf = tr & 15;
-    int64_t cached_off = INT64_MIN;
+    int64_t cached = INT64_MIN;
+    float2 co[4], si[4];
     for (int j = 0; ok && j < n_tiles; ++j) {
-      const int s = j % kNS;
-      const uint32_t par = (j / kNS) & 1;
-      asm volatile("bar.sync 1, 128;" ::: "memory");  // everyone read the last decision
-      if (tr == 0) *decision = cta_wait(&k_full[s], par, abort, lim, p.err) ? 1 : 0;
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-      if (*decision == 0) break;
-      mbar_wait(&k_full[s], par, lim);  // completed: acquires the copied tile for this thread
-      const TileMeta &mt = meta[s];
+      const int s = j % kNK;
+      if (!cta_wait(&k_full[s], (j / kNK) & 1, abort, lim, p.err)) break;
+      const KMeta &mt = meta_k[s];
       uint8_t *kt = Ks + s * kTileBytes;
       if (mt.kind == 0) {
-        // one relative rotation R(o - m0) per page: a (cos, sin) table per page offset
-        const int64_t d = (int64_t)mt.off[tp] - m0;
-        if (d != cached_off) {
-          cached_off = d;
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float cc, ss;
-            rope_cos_sin(d, turn[tf * 4 + e], cc, ss);
-            tab[tp * 64 + tf * 4 + e] = make_float2(cc, ss);
-          }
+        // one relative rotation R(o - m0) per page
+        const int64_t d = (int64_t)mt.off[rg >> 1] - m0;
+        if (d != cached) {
+          cached = d;
+          chunk_angles(d, turn, c, co, si);
         }
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        const int pg = rg >> 1;  // 8 rows of one 16-row page
-        float2 cs[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) cs[e] = tab[pg * 64 + c * 8 + e];
-#pragma unroll
-        for (int rr = 0; rr < 8; ++rr) rotate_row_chunk(kt, rg * 8 + rr, c, cs);
+        for (int rr = 0; rr < 8; ++rr) rotate_row_chunk(kt, rg * 8 + rr, c, co, si);
       } else {
         // question keys: raw, rotated by R(p - m0) row by row
         for (int rr = 0; rr < 8; ++rr) {
           const int row = rg * 8 + rr;
-          const int64_t delta = (int64_t)(mt.c0 + row - t0);
-          float2 cs[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) rope_cos_sin(delta, turn[c * 8 + e], cs[e].x, cs[e].y);
-          rotate_row_chunk(kt, row, c, cs);
+          float2 cq[4], sq[4];
+          chunk_angles((int64_t)(mt.c0 + row - t0), turn, c, cq, sq);
+          rotate_row_chunk(kt, row, c, cq, sq);
         }
       }
       fence_async_smem();
