@@ -29,8 +29,10 @@ struct lazy_pool {
 
   // Tensor maps of the page buffers for the tensor-core prefill (built lazily).
   bool tmaps_ready = false;
-  alignas(64) unsigned char tmap_k[128];
+  alignas(64) unsigned char tmap_k[128];   // 2-D view: 16-row page boxes
   alignas(64) unsigned char tmap_v[128];
+  alignas(64) unsigned char tmap_k8[128];  // 4-D view: 8 consecutive blocks of one kv head
+  alignas(64) unsigned char tmap_v8[128];
 };
 
 namespace lazy {

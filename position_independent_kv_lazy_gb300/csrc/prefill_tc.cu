@@ -70,7 +70,7 @@ struct SMeta {
 };
 
 struct TcParams {
-  CUtensorMap tm_q, tm_knew, tm_vnew, tm_k, tm_v;
+  CUtensorMap tm_q, tm_knew, tm_vnew, tm_k, tm_v, tm_k8, tm_v8;
   const int32_t *cu_q;
   const int32_t *q_pos0;
   const uint64_t *words;
@@ -99,6 +99,14 @@ __device__ __forceinline__ void tma3d(void *dst, const CUtensorMap *m, int x, in
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
       "{%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
       "l"((uint64_t)m), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma4d(void *dst, const CUtensorMap *m, int x, int y, int z, int w,
+                                      uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
+      "{%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
+      "l"((uint64_t)m), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
       : "memory");
 }
 // Shared-memory matrix descriptor: 128B swizzle, version 1.
@@ -313,6 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       };
       if (n_doc > 0) load_words(0);
       int32_t rows[kNK][8];
+      int32_t run8[kNK];  // first block id when the tile's 8 blocks are consecutive, else -1
       int k_issued[kNK] = {0, 0, 0}, v_issued[kNV] = {0, 0};
       bool ok = true;
       for (int e = 0; ok && e <= n_tiles; ++e) {
@@ -349,12 +358,24 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             }
             ms.kind = 0;
             ms.full = full;
-            mbar_arrive_expect_tx(&k_full[s], kTileBytes);
+            // Documents are encoded into freshly allocated, usually consecutive blocks: then one
+            // 8-block box per 64-dim half replaces 8 page boxes.
+            bool consec = full != 0;
 #pragma unroll
-            for (int pp = 0; pp < 8; ++pp)
+            for (int pp = 1; pp < 8; ++pp)
+              consec &= (rows[s][pp] == rows[s][0] + pp * p.hkv * kPage);
+            run8[s] = consec ? (rows[s][0] / kPage - h) / p.hkv : -1;
+            mbar_arrive_expect_tx(&k_full[s], kTileBytes);
+            if (consec) {
               for (int cb = 0; cb < 2; ++cb)
-                tma2d(kd + cb * kHalfBytes + pp * 2048, &p.tm_k, cb * 64, rows[s][pp],
-                      &k_full[s]);
+                tma4d(kd + cb * kHalfBytes, &p.tm_k8, cb * 64, 0, h, run8[s], &k_full[s]);
+            } else {
+#pragma unroll
+              for (int pp = 0; pp < 8; ++pp)
+                for (int cb = 0; cb < 2; ++cb)
+                  tma2d(kd + cb * kHalfBytes + pp * 2048, &p.tm_k, cb * 64, rows[s][pp],
+                        &k_full[s]);
+            }
           } else {
             const int c0 = (j - n_doc) * kTile;
             mk.kind = 1;
@@ -377,11 +398,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           uint8_t *vd = Vs + s * kTileBytes;
           mbar_arrive_expect_tx(&v_full[s], kTileBytes);
           if (j < n_doc) {
-#pragma unroll
-            for (int pp = 0; pp < 8; ++pp)
+            if (run8[sk] >= 0) {
               for (int cb = 0; cb < 2; ++cb)
-                tma2d(vd + cb * kHalfBytes + pp * 2048, &p.tm_v, cb * 64, rows[sk][pp],
-                      &v_full[s]);
+                tma4d(vd + cb * kHalfBytes, &p.tm_v8, cb * 64, 0, h, run8[sk], &v_full[s]);
+            } else {
+#pragma unroll
+              for (int pp = 0; pp < 8; ++pp)
+                for (int cb = 0; cb < 2; ++cb)
+                  tma2d(vd + cb * kHalfBytes + pp * 2048, &p.tm_v, cb * 64, rows[sk][pp],
+                        &v_full[s]);
+            }
           } else {
             const int c0 = (j - n_doc) * kTile;
             for (int cb = 0; cb < 2; ++cb)
@@ -693,7 +719,7 @@ int make_map(CUtensorMap *m, void *base, int rank, const cuuint64_t *dims,
     record_msg("cuTensorMapEncodeTiled is unavailable");
     return LAZY_ERR_CUDA;
   }
-  cuuint32_t es[3] = {1, 1, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, base, dims, strides_bytes, box, es,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -730,10 +756,21 @@ int prefill_tc(lazy_pool *p, const PrefillParams &pp, int32_t max_q_len, cudaStr
       if (rc != LAZY_OK) return rc;
       rc = make_map(reinterpret_cast<CUtensorMap *>(p->tmap_v), p->v, 2, dims, strides, box);
       if (rc != LAZY_OK) return rc;
+      // [block][kv head][slot][dim]; box = 64 dims x 16 slots x 1 head x 8 blocks
+      const cuuint64_t dims4[4] = {128, (cuuint64_t)kPage, (cuuint64_t)p->hkv,
+                                   (cuuint64_t)p->num_blocks};
+      const cuuint64_t strides4[3] = {256, 256 * kPage, (cuuint64_t)256 * kPage * p->hkv};
+      const cuuint32_t box4[4] = {64, (cuuint32_t)kPage, 1, 8};
+      rc = make_map(reinterpret_cast<CUtensorMap *>(p->tmap_k8), p->k, 4, dims4, strides4, box4);
+      if (rc != LAZY_OK) return rc;
+      rc = make_map(reinterpret_cast<CUtensorMap *>(p->tmap_v8), p->v, 4, dims4, strides4, box4);
+      if (rc != LAZY_OK) return rc;
       p->tmaps_ready = true;
     }
     memcpy(&tp.tm_k, p->tmap_k, sizeof(CUtensorMap));
     memcpy(&tp.tm_v, p->tmap_v, sizeof(CUtensorMap));
+    memcpy(&tp.tm_k8, p->tmap_k8, sizeof(CUtensorMap));
+    memcpy(&tp.tm_v8, p->tmap_v8, sizeof(CUtensorMap));
   }
   const int G = pp.G, TQ = 128 / G;
   {
