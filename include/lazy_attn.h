@@ -179,6 +179,13 @@ int lazy_attn_decode(lazy_pool *pool, const void *d_q, const int32_t *d_q_pos,
                      lazy_stream_t stream);
 
 /*
+ * Test hook: y[i] = 2^x[i] computed by the FMA-pipe exponential that the tensor-core prefill
+ * uses for part of its softmax weights (range reduction to [-1/2, 1/2] plus a fitted degree-5
+ * polynomial). d_x, d_y: device float [n]. Inputs below -126 return ~1e-38.
+ */
+int lazy_debug_exp2(const float *d_x, float *d_y, int32_t n, lazy_stream_t stream);
+
+/*
  * Allocation-free decode. The paper has no counterpart to this entry point; it exists for
  * callers that cannot provide the workspace lazy_attn_decode needs. Examples: a plugin running
  * inside a serving process whose memory manager has already reserved the GPU's memory and

@@ -38,6 +38,13 @@ constexpr int kTile = 128;
 constexpr int kNK = 3;  // K ring: a K tile is free again as soon as both QK products read it
 constexpr int kNV = 2;  // V ring: freed after both PV products
 constexpr int kThreads = 512;
+// One softmax exponential pair in kPolyEvery on the FMA pipe (exp2_poly2) instead of MUFU;
+// 0 = all on MUFU. Measured on GB300: the softmax is issue-bound, not MUFU-bound, and every
+// offload ratio from 1/2 to 1/64 was slower, so it is off.
+#ifndef LAZY_POLY_EVERY
+#define LAZY_POLY_EVERY 0
+#endif
+constexpr int kPolyEvery = LAZY_POLY_EVERY;
 constexpr int kTileBytes = kTile * 128 * 2;  // 32 KB: 128 rows x 128 bf16
 constexpr int kHalfBytes = kTileBytes / 2;   // one 64-dim box column
 
@@ -166,6 +173,64 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+#define LAZY_R64(r)                                                                          \
+  LAZY_R32(r), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]),   \
+      "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]),             \
+      "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]),             \
+      "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),             \
+      "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]),             \
+      "=r"(r[62]), "=r"(r[63])
+// 64 consecutive fp32 TMEM columns of this thread's lane (one round trip).
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,"
+      "%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,"
+      "%58,%59,%60,%61,%62,%63}, [%64];"
+      : LAZY_R64(r)
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+// Asynchronous 32-column load; the registers are valid only after tmem_wait_ld on them.
+__device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : LAZY_R32(r)
+      : "r"(taddr));
+}
+// Waits for this thread's outstanding TMEM loads; `r` is threaded through so that no use of the
+// loaded registers can be scheduled before the wait.
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                 "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                 "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                 "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+}
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
@@ -188,41 +253,42 @@ __device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
 }
 
 // Rotate, in place, one row of a 128-row swizzled bf16 tile at 16-byte chunk c of both 64-dim
-// boxes: x_i <- x_i cos - x_{i+64} sin, x_{i+64} <- x_i sin + x_{i+64} cos for i = 8c .. 8c+7.
-// cs2[k] = (cos, cos) pairs and sn2[k] = (sin, sin) pairs of frequencies 8c+2k, 8c+2k+1.
+// boxes: x_i <- x_i cos - x_{i+64} sin, x_{i+64} <- x_i sin + x_{i+64} cos for i = 8c .. 8c+7,
+// in packed bf16x2 arithmetic (the operands are bf16 and so is the result the MMA reads;
+// 4 fused instructions per 2 pairs). co/si/nsi hold (cos, cos'), (sin, sin'), (-sin, -sin') of
+// frequencies 8c+2k, 8c+2k+1.
+struct RotPairs {
+  __nv_bfloat162 co[4], si[4], nsi[4];
+};
 __device__ __forceinline__ void rotate_row_chunk(uint8_t *tile, int row, int c,
-                                                 const float2 (&co)[4], const float2 (&si)[4]) {
+                                                 const RotPairs &rp) {
   const int phys = (c ^ (row & 7)) * 16;
   uint4 *lo = reinterpret_cast<uint4 *>(tile + row * 128 + phys);
   uint4 *hi = reinterpret_cast<uint4 *>(tile + kHalfBytes + row * 128 + phys);
-  const uint4 a = *lo, b = *hi;
-  const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
-  uint32_t xo[4], yo[4];
+  uint4 a = *lo, b = *hi;
+  __nv_bfloat162 *x = reinterpret_cast<__nv_bfloat162 *>(&a);
+  __nv_bfloat162 *y = reinterpret_cast<__nv_bfloat162 *>(&b);
+  __nv_bfloat162 xo[4], yo[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    const float2 x = make_float2(__uint_as_float(aw[k] << 16), __uint_as_float(aw[k] & 0xFFFF0000u));
-    const float2 y = make_float2(__uint_as_float(bw[k] << 16), __uint_as_float(bw[k] & 0xFFFF0000u));
-    const float2 nsi = make_float2(-si[k].x, -si[k].y);
-    const float2 xr = __ffma2_rn(y, nsi, __fmul2_rn(x, co[k]));
-    const float2 yr = __ffma2_rn(x, si[k], __fmul2_rn(y, co[k]));
-    __nv_bfloat162 hx = __floats2bfloat162_rn(xr.x, xr.y), hy = __floats2bfloat162_rn(yr.x, yr.y);
-    xo[k] = *reinterpret_cast<uint32_t *>(&hx);
-    yo[k] = *reinterpret_cast<uint32_t *>(&hy);
+    xo[k] = __hfma2(y[k], rp.nsi[k], __hmul2(x[k], rp.co[k]));
+    yo[k] = __hfma2(x[k], rp.si[k], __hmul2(y[k], rp.co[k]));
   }
-  *lo = make_uint4(xo[0], xo[1], xo[2], xo[3]);
-  *hi = make_uint4(yo[0], yo[1], yo[2], yo[3]);
+  *lo = *reinterpret_cast<uint4 *>(xo);
+  *hi = *reinterpret_cast<uint4 *>(yo);
 }
 
-// (cos, sin) of delta * theta_i for i = 8c .. 8c+7, as pairs.
+// (cos, sin) of delta * theta_i for i = 8c .. 8c+7 (exact fp32 angles), as bf16 pairs.
 __device__ __forceinline__ void chunk_angles(int64_t delta, const uint64_t *turn, int c,
-                                             float2 (&co)[4], float2 (&si)[4]) {
+                                             RotPairs &rp) {
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     float c0, s0, c1, s1;
     rope_cos_sin(delta, turn[c * 8 + 2 * k], c0, s0);
     rope_cos_sin(delta, turn[c * 8 + 2 * k + 1], c1, s1);
-    co[k] = make_float2(c0, c1);
-    si[k] = make_float2(s0, s1);
+    rp.co[k] = __floats2bfloat162_rn(c0, c1);
+    rp.si[k] = __floats2bfloat162_rn(s0, s1);
+    rp.nsi[k] = __floats2bfloat162_rn(-s0, -s1);
   }
 }
 
@@ -526,32 +592,97 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           }
         }
       }
-      // pass 1: row max of the raw scores
-      float mx = -INFINITY;
-      if (need_mask) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          tmem_ld32(s_col + c * 32, r);
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            mx = fmaxf(mx, ((vm[c] >> e) & 1u) ? __uint_as_float(r[e]) : -INFINITY);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          tmem_ld32(s_col + c * 32, r);
-#pragma unroll
-          for (int e = 0; e < 32; e += 2)
-            mx = fmaxf(mx, fmaxf(__uint_as_float(r[e]), __uint_as_float(r[e + 1])));
-        }
-      }
-      const float mx2 = mx * sl2;
+      // One pass over S in two 64-column halves, each loaded once: the half's max is taken on
+      // registers, then its weights are formed. The running max m_use only moves when a half's
+      // max exceeds it by more than 8 (log2 domain, so weights stay <= 2^8); then the weights
+      // already written for this tile, this tile's partial sum and (below) O are scaled by
+      // 2^(m_old - m_new).
       float m_use = m_run, alpha = 1.f;
-      if (mx2 > m_run + 8.f) {  // includes the first finite max (m_run = -inf)
-        m_use = mx2;
-        alpha = (m_run == -INFINITY) ? 0.f : ex2(m_run - mx2);
+      float2 lp2[4];  // row-sum partials, four independent chains
+#pragma unroll
+      for (int k = 0; k < 4; ++k) lp2[k] = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t r[64];
+        tmem_ld64(s_col + hf * 64, r);
+        // max over the half with four independent chains (a single running max would be a
+        // 64-long dependency chain)
+        float cmk[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (need_mask) {
+#pragma unroll
+          for (int e = 0; e < 64; ++e)
+            cmk[e & 3] = fmaxf(cmk[e & 3], ((vm[2 * hf + (e >> 5)] >> (e & 31)) & 1u)
+                                               ? __uint_as_float(r[e]) : -INFINITY);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 64; e += 8) {
+            cmk[0] = fmaxf(cmk[0], fmaxf(__uint_as_float(r[e]), __uint_as_float(r[e + 1])));
+            cmk[1] = fmaxf(cmk[1], fmaxf(__uint_as_float(r[e + 2]), __uint_as_float(r[e + 3])));
+            cmk[2] = fmaxf(cmk[2], fmaxf(__uint_as_float(r[e + 4]), __uint_as_float(r[e + 5])));
+            cmk[3] = fmaxf(cmk[3], fmaxf(__uint_as_float(r[e + 6]), __uint_as_float(r[e + 7])));
+          }
+        }
+        const float cm = fmaxf(fmaxf(cmk[0], cmk[1]), fmaxf(cmk[2], cmk[3]));
+        const float cm2 = cm * sl2;
+        const bool raise = cm2 > m_use + 8.f;  // includes the first finite max (m_use = -inf)
+        float a = 1.f;
+        if (raise) {
+          a = (m_use == -INFINITY) ? 0.f : ex2(m_use - cm2);
+          m_use = cm2;
+          alpha *= a;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            lp2[k].x *= a;
+            lp2[k].y *= a;
+          }
+        }
+        if (hf == 1 && __any_sync(0xffffffffu, raise && a != 0.f)) {
+          // rare: rescale the weights of the first half, already written as bf16 pairs
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            uint32_t w[16];
+            tmem_ld16(s_col + k * 16, w);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const float lo = __uint_as_float(w[e] << 16) * a;
+              const float hi = __uint_as_float(w[e] & 0xFFFF0000u) * a;
+              w[e] = pack_bf2(lo, hi);
+            }
+            tmem_st16(s_col + k * 16, w);
+          }
+        }
+        const float neg_m = (m_use == -INFINITY) ? 0.f : -m_use;
+#pragma unroll
+        for (int q4 = 0; q4 < 2; ++q4) {
+          uint32_t pw[16];
+#pragma unroll
+          for (int e2 = 0; e2 < 32; e2 += 2) {
+            const int e = q4 * 32 + e2;
+            float s0, s1;
+            if (need_mask) {
+              const uint32_t bits = vm[2 * hf + q4];
+              s0 = ((bits >> e2) & 1u) ? ex2(fmaf(__uint_as_float(r[e]), sl2, neg_m)) : 0.f;
+              s1 = ((bits >> (e2 + 1)) & 1u) ? ex2(fmaf(__uint_as_float(r[e + 1]), sl2, neg_m))
+                                             : 0.f;
+            } else {
+              const float2 t = __ffma2_rn(
+                  make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])),
+                  make_float2(sl2, sl2), make_float2(neg_m, neg_m));
+              if (kPolyEvery > 0 &&
+                  ((e2 >> 1) % (kPolyEvery > 0 ? kPolyEvery : 1)) == kPolyEvery - 1) {
+                const float2 y = exp2_poly2(t);
+                s0 = y.x;
+                s1 = y.y;
+              } else {
+                s0 = ex2(t.x);
+                s1 = ex2(t.y);
+              }
+            }
+            lp2[(e2 >> 1) & 3] = __fadd2_rn(lp2[(e2 >> 1) & 3], make_float2(s0, s1));
+            pw[e2 / 2] = pack_bf2(s0, s1);
+          }
+          tmem_st16(s_col + hf * 32 + q4 * 16, pw);
+        }
       }
       // O *= alpha for rows whose max moved (warp-collective TMEM access); O holds data only
       // after the first tile's PV.
@@ -565,42 +696,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           tmem_st32(o_col + c * 32, r);
         }
       }
-      // pass 2: p = 2^(s*scale*log2e - m), packed to bf16 pairs into S's first 64 columns
-      float2 lp2 = make_float2(0.f, 0.f);
-      const float neg_m = (m_use == -INFINITY) ? 0.f : -m_use;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t pw[32];
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int c = half * 2 + cc;
-          uint32_t r[32];
-          tmem_ld32(s_col + c * 32, r);
-          if (need_mask) {
-#pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-              const float s0 = ((vm[c] >> e) & 1u)
-                                   ? ex2(fmaf(__uint_as_float(r[e]), sl2, neg_m)) : 0.f;
-              const float s1 = ((vm[c] >> (e + 1)) & 1u)
-                                   ? ex2(fmaf(__uint_as_float(r[e + 1]), sl2, neg_m)) : 0.f;
-              lp2 = __fadd2_rn(lp2, make_float2(s0, s1));
-              pw[cc * 16 + e / 2] = pack_bf2(s0, s1);
-            }
-          } else {
-#pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-              const float2 t = __ffma2_rn(
-                  make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])),
-                  make_float2(sl2, sl2), make_float2(neg_m, neg_m));
-              const float s0 = ex2(t.x), s1 = ex2(t.y);
-              lp2 = __fadd2_rn(lp2, make_float2(s0, s1));
-              pw[cc * 16 + e / 2] = pack_bf2(s0, s1);
-            }
-          }
-        }
-        tmem_st32(s_col + half * 32, pw);
-      }
-      const float lp = lp2.x + lp2.y;
+      const float2 lps = __fadd2_rn(__fadd2_rn(lp2[0], lp2[1]), __fadd2_rn(lp2[2], lp2[3]));
+      const float lp = lps.x + lps.y;
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       l_run = l_run * alpha + lp;
       m_run = m_use;
@@ -646,16 +743,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       for (int i = 0; i < 2; ++i) {
         for (int rr = 0; rr < 8; ++rr) {
           const int row = rg * 8 + rr;
-          float2 co[4], si[4];
-          chunk_angles((int64_t)(i * TQ + row / G), turn, c, co, si);  // query pos - m0
-          rotate_row_chunk(Qs + i * kTileBytes, row, c, co, si);
+          RotPairs rq;
+          chunk_angles((int64_t)(i * TQ + row / G), turn, c, rq);  // query pos - m0
+          rotate_row_chunk(Qs + i * kTileBytes, row, c, rq);
         }
       }
       fence_async_smem();
     }
     mbar_arrive(q_rot);
     int64_t cached = INT64_MIN;
-    float2 co[4], si[4];
+    RotPairs rp;
     for (int j = 0; ok && j < n_tiles; ++j) {
       const int s = j % kNK;
       if (!cta_wait(&k_full[s], (j / kNK) & 1, abort, lim, p.err)) break;
@@ -666,17 +763,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         const int64_t d = (int64_t)mt.off[rg >> 1] - m0;
         if (d != cached) {
           cached = d;
-          chunk_angles(d, turn, c, co, si);
+          chunk_angles(d, turn, c, rp);
         }
 #pragma unroll
-        for (int rr = 0; rr < 8; ++rr) rotate_row_chunk(kt, rg * 8 + rr, c, co, si);
+        for (int rr = 0; rr < 8; ++rr) rotate_row_chunk(kt, rg * 8 + rr, c, rp);
       } else {
         // question keys: raw, rotated by R(p - m0) row by row
         for (int rr = 0; rr < 8; ++rr) {
           const int row = rg * 8 + rr;
-          float2 cq[4], sq[4];
-          chunk_angles((int64_t)(mt.c0 + row - t0), turn, c, cq, sq);
-          rotate_row_chunk(kt, row, c, cq, sq);
+          RotPairs rk;
+          chunk_angles((int64_t)(mt.c0 + row - t0), turn, c, rk);
+          rotate_row_chunk(kt, row, c, rk);
         }
       }
       fence_async_smem();
