@@ -297,6 +297,9 @@ def bench_ours(args):
         pk.lazy_attn_decode(lres.pool, ldb.q, ldb.q_pos, ldb.words, ldb.cu_pages,
                             sm_scale=lwl.sm_scale, out=lout, lse=llse, workspace=lws)
 
+    # ---------------- mixed serving step, skew sweep (extra object; built and timed one alpha
+    # at a time after the main timed region, see mixed_sweep)
+
     torch.cuda.synchronize()
     for _ in range(args.warmup):
         flush(); step(); e2e_step(); no_reuse_call()
@@ -395,6 +398,11 @@ def bench_ours(args):
             "tokens_per_s": round(lwl.batch / (long_avg * 1e-3), 1),
             "ms_per_step": round(long_avg, 4),
             "frac": round(l_bytes / (long_avg * 1e-3) / 1e9 / hbm_peak, 4)}
+    if not only_decode:
+        # free the other workloads' pools before the 17 GB mixed pools
+        del pres, pb, pout, plse, lres, ldb, lws, lout, llse
+        torch.cuda.empty_cache()
+        line["mixed"] = mixed_sweep(args, flush, stream, hbm_peak)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, src, kv_bytes, args.cpu_seconds)
     if rank == 0:
@@ -402,6 +410,65 @@ def bench_ours(args):
     if ws > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def mixed_sweep(args, flush, stream, hbm_peak):
+    """Mixed serving step on the skew-sweep workload for alpha in (0.6, 0.9, 1.2): one prefill
+    launch (32 requests, 128-512-token questions) and one decode step (96 requests: append +
+    split-KV decode + combine) back to back on one stream; aggregate tokens/s plus the KV bytes
+    the pool keeps against position-baked copies."""
+    import torch
+
+    import position_independent_kv_lazy_gb300 as pk
+    import workload as W
+    from position_independent_kv_lazy_gb300 import harness as H
+
+    out = {"workload": "mixed: pool 4096 docs x 1024, 128 req x U{8..32} Zipf(alpha) docs, "
+                       "32 prefill (U{128..512} question) + 96 decode (U{128..512}+1 private)",
+           "unit": "tokens/s", "alphas": {}}
+    steps = max(3, args.steps // 5)
+    for alpha in (0.6, 0.9, 1.2):
+        wl = W.mixed_workload(alpha)
+        src = H.DeviceSource(wl)
+        res = H.build_resident(wl, src)
+        pb = H.prefill_batch(wl, res, src)
+        db = H.decode_batch(wl, res, src)
+        ws = torch.empty(pk.lazy_decode_workspace_bytes(res.pool, len(db.reqs), wl.Hq),
+                         dtype=torch.uint8, device="cuda")
+        dout = torch.empty_like(db.q)
+        dlse = torch.empty((len(db.reqs), wl.Hq), dtype=torch.float32, device="cuda")
+        pout = torch.empty_like(pb.q)
+        plse = torch.empty((pb.total_q, wl.Hq), dtype=torch.float32, device="cuda")
+
+        def mixed_step():
+            pk.lazy_attn_prefill(res.pool, pb.q, pb.k_new, pb.v_new, pb.cu_q, pb.q_pos0,
+                                 pb.words, pb.cu_pages, pb.max_q_len, sm_scale=wl.sm_scale,
+                                 out=pout, lse=plse)
+            pk.kv_pool_write_tokens(res.pool, db.new_k, db.new_v, db.slot_mapping, db.local_pos)
+            pk.lazy_attn_decode(res.pool, db.q, db.q_pos, db.words, db.cu_pages,
+                                sm_scale=wl.sm_scale, out=dout, lse=dlse, workspace=ws)
+
+        for _ in range(args.warmup):
+            flush(); mixed_step()
+        torch.cuda.synchronize()
+        if pk.lazy_get_device_error(res.pool) != 0:
+            raise RuntimeError("device error in the mixed step")
+        ms = _timed_steps(mixed_step, steps, flush, stream)
+        avg = sum(ms) / len(ms)
+        tokens = pb.total_q + len(db.reqs)
+        acct = H.kv_bytes_accounting(wl)
+        out["alphas"][str(alpha)] = {
+            "tokens_per_step": tokens, "ms_per_step": round(avg, 4),
+            "tokens_per_s": round(tokens / (avg * 1e-3), 1),
+            "prefill_tokens": pb.total_q, "decode_tokens": len(db.reqs),
+            "unique_docs": len(wl.used_docs()),
+            "kv_bytes_resident": acct["resident"],
+            "kv_bytes_materialised": acct["materialised"],
+            "kv_bytes_per_request_copies": acct["per_request"],
+            "materialised_over_resident": round(acct["materialised"] / acct["resident"], 3)}
+        del res, pb, db, ws, dout, dlse, pout, plse, src
+        torch.cuda.empty_cache()
+    return out
 
 
 def _kernel_hash():

@@ -201,3 +201,23 @@ def prefill_batch(wl, res: Resident, src, device="cuda", reqs=None) -> PrefillBa
         torch.tensor([r.q_pos0 for r in reqs], dtype=torch.int32, device=device),
         torch.from_numpy(words.view(np.int64)).to(device), torch.from_numpy(cu).to(device),
         int(cu_q[-1]), max(r.T for r in reqs), flops)
+
+
+def kv_bytes_accounting(wl) -> Dict[str, int]:
+    """Bytes of K+V the pool keeps for a workload versus copies that bake positions in.
+
+    resident:      every retrieved document once (position-free pages) + private segments
+    materialised:  one re-encoded copy per distinct (document, logical offset) pair, the
+                   position-aware alternative + private segments
+    per_request:   every request's own copy of each document it holds + private segments
+    """
+    per_tok = wl.kv_bytes_per_token()
+    priv = sum(r.priv_len for r in wl.decode_requests()) * per_tok
+    pairs = set()
+    for r in wl.requests:
+        pairs.update(zip(r.docs, r.offsets))
+    return {
+        "resident": len(wl.used_docs()) * wl.doc_len * per_tok + priv,
+        "materialised": len(pairs) * wl.doc_len * per_tok + priv,
+        "per_request": sum(len(r.docs) for r in wl.requests) * wl.doc_len * per_tok + priv,
+    }

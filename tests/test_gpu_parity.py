@@ -378,3 +378,40 @@ def test_fma_pipe_exp2_against_cuda(pk):
     ref = torch.exp2(x.double())
     rel = ((y.double() - ref).abs() / ref).max().item()
     assert rel <= 4e-7, rel
+
+
+def test_mixed_step_full_size_sampled(pk):
+    # skew-sweep mixed step (alpha 1.2): one prefill launch (32 ragged questions) and one decode
+    # step (96 requests) over the same resident 4096-doc pool; sampled against the oracle
+    H = _h()
+    wl = W.mixed_workload(1.2)
+    src = H.DeviceSource(wl)
+    res = H.build_resident(wl, src, drop_raw=False)
+    pb = H.prefill_batch(wl, res, src)
+    db = H.decode_batch(wl, res, src)
+    pout, plse = pk.lazy_attn_prefill(res.pool, pb.q, pb.k_new, pb.v_new, pb.cu_q, pb.q_pos0,
+                                      pb.words, pb.cu_pages, pb.max_q_len, sm_scale=wl.sm_scale)
+    pk.kv_pool_write_tokens(res.pool, db.new_k, db.new_v, db.slot_mapping, db.local_pos)
+    dout, dlse = pk.lazy_attn_decode(res.pool, db.q, db.q_pos, db.words, db.cu_pages,
+                                     sm_scale=wl.sm_scale)
+    torch.cuda.synchronize()
+    assert pk.lazy_get_device_error(res.pool) == 0
+    view = src.host_view()
+    # prefill: request pb.reqs[3] (its rows in the packed batch), kv heads 1 and 6
+    pr = pb.reqs[3]
+    cu = pb.cu_q.cpu().numpy()
+    ro, rl = oracle.attend_request(wl, pr.index, kv_heads=[1, 6], queries=[0, pr.T // 2, pr.T - 1],
+                                   src=view)
+    heads = [4, 5, 6, 7, 24, 25, 26, 27]
+    rows = cu[3] + np.array([0, pr.T // 2, pr.T - 1])
+    o = pout.float().cpu().numpy()[rows][:, heads]
+    l = plse.cpu().numpy()[rows][:, heads]
+    qi = [0, pr.T // 2, pr.T - 1]
+    assert np.abs(o - ro[qi][:, heads]).max() <= 2e-2
+    assert np.abs(l - rl[qi][:, heads]).max() <= 1e-3
+    # decode: request db.reqs[10], kv head 3
+    dr = db.reqs[10]
+    ro, rl = oracle.attend_request(wl, dr.index, kv_heads=[3], src=view)
+    heads = [12, 13, 14, 15]
+    assert np.abs(dout.float().cpu().numpy()[10][heads] - ro[0][heads]).max() <= 2e-2
+    assert np.abs(dlse.cpu().numpy()[10][heads] - rl[0][heads]).max() <= 1e-3

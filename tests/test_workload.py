@@ -62,3 +62,15 @@ def test_zipf_skew():
     expect = 4000 * w / w.sum()
     assert abs(counts[0] / expect[0] - 1) < 0.1 and abs(counts[1] / expect[1] - 1) < 0.15
     assert counts[:5].sum() > counts[25:].sum()
+
+
+def test_kv_bytes_accounting():
+    from position_independent_kv_lazy_gb300 import harness as H
+    # doc 0 at offsets 0 and 100 in request 0 and at 0 in request 1; doc 1 at 7 in request 1
+    wl = W.custom("decode", [[(0, 0), (0, 100)], [(0, 0), (1, 7)]], doc_len=10, n_pool=2,
+                  Hq=4, Hkv=2, D=64, priv=[(200, 3), (50, 5)])
+    per_tok = 2 * 2 * 64 * 2
+    acct = H.kv_bytes_accounting(wl)
+    assert acct["resident"] == (2 * 10 + 8) * per_tok            # docs 0, 1 once + private
+    assert acct["materialised"] == (3 * 10 + 8) * per_tok        # (0,0) (0,100) (1,7)
+    assert acct["per_request"] == (4 * 10 + 8) * per_tok
