@@ -7,7 +7,7 @@
 // segment at offset o (rows already carry R(j)) by R(o - m0), a question key at p by R(p - m0).
 //
 // CTA = (request b, kv head h, 2 x TQ question tokens): two 128-row Q tiles, rows ordered
-// (token, query head of the group), TQ = 128 / G. 16 warps:
+// (token, query head of the group), TQ = 128 / G. 12 warps:
 //   warp 0      TMA producer: Q tiles once, then per 128-key tile 8 page boxes (16 rows x 64
 //               dims, 128B swizzle) of K and of V into a 2-stage ring; question keys by
 //               128-token boxes.
@@ -16,9 +16,11 @@
 //   warps 4-7   softmax of Q tile 0, warps 8-11 of Q tile 1 (TMEM lane quadrant = warp % 4):
 //               online softmax in the log2 domain with a lazy rescale (the running max only
 //               moves when a row max exceeds it by more than 8), P written back into S's TMEM
-//               columns as bf16 pairs.
-//   warps 12-15 rotation: Q tiles once, each K tile in shared memory, in place (the pair
-//               (i, i+64) sits at the same swizzled offset of the two 64-dim boxes).
+//               columns as bf16 pairs. The same 256 threads rotate the Q tiles once and each K
+//               tile in shared memory, in place (the pair (i, i+64) sits at the same swizzled
+//               offset of the two 64-dim boxes), two tiles ahead of the scores they need.
+//               (Dedicated rotation warps were measured 27% slower: their stores contended
+//               with the softmax on the critical softmax -> PV -> QK chain.)
 // TMEM: S_0 [0,128) S_1 [128,256) O_0 [256,384) O_1 [384,512) fp32 columns.
 // Every wait is bounded; a timeout sets LAZY_DEVERR_TIMEOUT, raises a CTA abort flag that
 // releases the other roles, drains outstanding copies and MMAs, frees TMEM and returns.
@@ -37,7 +39,7 @@ namespace {
 constexpr int kTile = 128;
 constexpr int kNK = 3;  // K ring: a K tile is free again as soon as both QK products read it
 constexpr int kNV = 2;  // V ring: freed after both PV products
-constexpr int kThreads = 512;
+constexpr int kThreads = 384;
 // One softmax exponential pair in kPolyEvery on the FMA pipe (exp2_poly2) instead of MUFU;
 // 0 = all on MUFU. Measured on GB300: the softmax is issue-bound, not MUFU-bound, and every
 // offload ratio from 1/2 to 1/64 was slower, so it is off.
@@ -278,17 +280,93 @@ __device__ __forceinline__ void rotate_row_chunk(uint8_t *tile, int row, int c,
   *hi = *reinterpret_cast<uint4 *>(yo);
 }
 
+// The same rotation for 8 consecutive rows (one per-page angle set): all 16 loads are issued
+// before any store, so the rows' latencies overlap instead of chaining through in-place stores
+// the compiler must keep ordered.
+__device__ __forceinline__ void rotate_8rows_chunk(uint8_t *tile, int row0, int c,
+                                                   const RotPairs &rp) {
+  uint4 a[8], b[8];
+#pragma unroll
+  for (int rr = 0; rr < 8; ++rr) {
+    const int row = row0 + rr;
+    const int phys = (c ^ (row & 7)) * 16;
+    a[rr] = *reinterpret_cast<const uint4 *>(tile + row * 128 + phys);
+    b[rr] = *reinterpret_cast<const uint4 *>(tile + kHalfBytes + row * 128 + phys);
+  }
+#pragma unroll
+  for (int rr = 0; rr < 8; ++rr) {
+    __nv_bfloat162 *x = reinterpret_cast<__nv_bfloat162 *>(&a[rr]);
+    __nv_bfloat162 *y = reinterpret_cast<__nv_bfloat162 *>(&b[rr]);
+    __nv_bfloat162 xo[4], yo[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      xo[k] = __hfma2(y[k], rp.nsi[k], __hmul2(x[k], rp.co[k]));
+      yo[k] = __hfma2(x[k], rp.si[k], __hmul2(y[k], rp.co[k]));
+    }
+    a[rr] = *reinterpret_cast<uint4 *>(xo);
+    b[rr] = *reinterpret_cast<uint4 *>(yo);
+  }
+#pragma unroll
+  for (int rr = 0; rr < 8; ++rr) {
+    const int row = row0 + rr;
+    const int phys = (c ^ (row & 7)) * 16;
+    *reinterpret_cast<uint4 *>(tile + row * 128 + phys) = a[rr];
+    *reinterpret_cast<uint4 *>(tile + kHalfBytes + row * 128 + phys) = b[rr];
+  }
+}
+
+// The same for 4 consecutive rows of one page.
+__device__ __forceinline__ void rotate_4rows_chunk(uint8_t *tile, int row0, int c,
+                                                   const RotPairs &rp) {
+  uint4 a[4], b[4];
+#pragma unroll
+  for (int rr = 0; rr < 4; ++rr) {
+    const int row = row0 + rr;
+    const int phys = (c ^ (row & 7)) * 16;
+    a[rr] = *reinterpret_cast<const uint4 *>(tile + row * 128 + phys);
+    b[rr] = *reinterpret_cast<const uint4 *>(tile + kHalfBytes + row * 128 + phys);
+  }
+#pragma unroll
+  for (int rr = 0; rr < 4; ++rr) {
+    __nv_bfloat162 *x = reinterpret_cast<__nv_bfloat162 *>(&a[rr]);
+    __nv_bfloat162 *y = reinterpret_cast<__nv_bfloat162 *>(&b[rr]);
+    __nv_bfloat162 xo[4], yo[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      xo[k] = __hfma2(y[k], rp.nsi[k], __hmul2(x[k], rp.co[k]));
+      yo[k] = __hfma2(x[k], rp.si[k], __hmul2(y[k], rp.co[k]));
+    }
+    a[rr] = *reinterpret_cast<uint4 *>(xo);
+    b[rr] = *reinterpret_cast<uint4 *>(yo);
+  }
+#pragma unroll
+  for (int rr = 0; rr < 4; ++rr) {
+    const int row = row0 + rr;
+    const int phys = (c ^ (row & 7)) * 16;
+    *reinterpret_cast<uint4 *>(tile + row * 128 + phys) = a[rr];
+    *reinterpret_cast<uint4 *>(tile + kHalfBytes + row * 128 + phys) = b[rr];
+  }
+}
+
 // (cos, sin) of delta * theta_i for i = 8c .. 8c+7 (exact fp32 angles), as bf16 pairs.
+// (cos, sin) of delta * theta for one frequency. Not inlined: the angles are needed only when
+// a page offset changes, and one shared copy keeps the softmax loop's code compact (the loop
+// is instruction-fetch bound when every call site carries its own sincospif).
+__device__ __noinline__ float2 angle_cs(int64_t delta, uint64_t turn_frac) {
+  float c, s;
+  rope_cos_sin(delta, turn_frac, c, s);
+  return make_float2(c, s);
+}
+
 __device__ __forceinline__ void chunk_angles(int64_t delta, const uint64_t *turn, int c,
                                              RotPairs &rp) {
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    float c0, s0, c1, s1;
-    rope_cos_sin(delta, turn[c * 8 + 2 * k], c0, s0);
-    rope_cos_sin(delta, turn[c * 8 + 2 * k + 1], c1, s1);
-    rp.co[k] = __floats2bfloat162_rn(c0, c1);
-    rp.si[k] = __floats2bfloat162_rn(s0, s1);
-    rp.nsi[k] = __floats2bfloat162_rn(-s0, -s1);
+    const float2 a = angle_cs(delta, turn[c * 8 + 2 * k]);
+    const float2 b = angle_cs(delta, turn[c * 8 + 2 * k + 1]);
+    rp.co[k] = __floats2bfloat162_rn(a.x, b.x);
+    rp.si[k] = __floats2bfloat162_rn(a.y, b.y);
+    rp.nsi[k] = __floats2bfloat162_rn(-a.y, -b.y);
   }
 }
 
@@ -341,10 +419,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 
   if (tid == 0) {
     mbar_init(q_full, 1);
-    mbar_init(q_rot, 128);
+    mbar_init(q_rot, 256);
     for (int s = 0; s < kNK; ++s) {
       mbar_init(&k_full[s], 1);
-      mbar_init(&k_rot[s], 128);
+      mbar_init(&k_rot[s], 256);
       mbar_init(&k_empty[s], 1);
     }
     for (int s = 0; s < kNV; ++s) {
@@ -552,17 +630,66 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       // MMAs still in flight must finish before TMEM is released.
       mbar_wait(o_final, 0, lim);
     }
-  } else if (warp >= 4 && warp < 12) {
-    // ============================== softmax (Q tile i, TMEM lane quadrant warp % 4)
+  } else if (warp >= 4) {
+    // ============================== softmax (Q tile i, TMEM lane quadrant warp % 4) + rotation
+    // The 256 softmax threads also apply the relative rotation to the key tiles, in the gap
+    // between finishing the softmax of tile j and the scores of tile j+1: right after tile j
+    // they rotate their share of tile j+2 (the K ring holds 3 tiles, so it has landed, and the
+    // MMA issuer needs it only after tile j+1). Share of a thread: 16-byte chunk c of 4
+    // consecutive rows of one page; group 0 takes rows 0-63, group 1 rows 64-127. Each thread
+    // keeps the (cos, sin) of its page's offset in registers until the offset changes.
     const int i = (warp - 4) >> 2;
     const int row = (warp & 3) * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const uint32_t s_col = lane_base + i * 128, o_col = lane_base + 256 + i * 128;
     const int t_row = t0 + i * TQ + row / G;
     const float sl2 = p.scale_log2;
+    const uint64_t *turn = p.turn;
+    const int st = tid - 128;               // 0..255
+    const int rc = st & 7, rrow0 = (st >> 3) * 4;  // rotation share: chunk rc, rows rrow0..+3
     float m_run = -INFINITY, l_run = 0.f;
-    bool ok = true;
-    for (int j = 0; j < n_tiles; ++j) {
+    bool ok = cta_wait(q_full, 0, abort, lim, p.err);
+    if (ok) {
+      // this thread's own query row of Q tile i, rotated to R(m - m0)
+#pragma unroll 1
+      for (int c = 0; c < 8; ++c) {
+        RotPairs rq;
+        chunk_angles((int64_t)(i * TQ + row / G), turn, c, rq);
+        rotate_row_chunk(Qs + i * kTileBytes, row, c, rq);
+      }
+      fence_async_smem();
+    }
+    mbar_arrive(q_rot);
+    int64_t cached = INT64_MIN;
+    RotPairs rp;
+    auto rotate_tile = [&](int jj) -> bool {
+      const int s = jj % kNK;
+      if (!cta_wait(&k_full[s], (jj / kNK) & 1, abort, lim, p.err)) return false;
+      const KMeta &mt = meta_k[s];
+      uint8_t *kt = Ks + s * kTileBytes;
+      if (mt.kind == 0) {
+        // one relative rotation R(o - m0) per page
+        const int64_t d = (int64_t)mt.off[rrow0 >> 4] - m0;
+        if (d != cached) {
+          cached = d;
+          chunk_angles(d, turn, rc, rp);
+        }
+        rotate_4rows_chunk(kt, rrow0, rc, rp);
+      } else {
+        // question keys: raw, rotated by R(p - m0) row by row
+#pragma unroll 1
+        for (int rr = 0; rr < 4; ++rr) {
+          RotPairs rk;
+          chunk_angles((int64_t)(mt.c0 + rrow0 + rr - t0), turn, rc, rk);
+          rotate_row_chunk(kt, rrow0 + rr, rc, rk);
+        }
+      }
+      fence_async_smem();
+      mbar_arrive(&k_rot[s]);
+      return true;
+    };
+    for (int jj = 0; ok && jj < 2 && jj < n_tiles; ++jj) ok = rotate_tile(jj);
+    for (int j = 0; ok && j < n_tiles; ++j) {
       if (!cta_wait(&s_full[i], j & 1, abort, lim, p.err)) {
         ok = false;
         break;
@@ -601,26 +728,27 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       float2 lp2[4];  // row-sum partials, four independent chains
 #pragma unroll
       for (int k = 0; k < 4; ++k) lp2[k] = make_float2(0.f, 0.f);
-#pragma unroll
+      // The halves run as a loop, not unrolled, so the loop body stays small (see angle_cs).
+#pragma unroll 1
       for (int hf = 0; hf < 2; ++hf) {
         uint32_t r[64];
         tmem_ld64(s_col + hf * 64, r);
+        if (need_mask) {
+          // hidden keys get -inf: they drop out of the max and ex2(-inf) = 0
+          const uint32_t m_lo = hf ? vm[2] : vm[0], m_hi = hf ? vm[3] : vm[1];
+#pragma unroll
+          for (int e = 0; e < 64; ++e)
+            if (!(((e < 32 ? m_lo : m_hi) >> (e & 31)) & 1u)) r[e] = 0xFF800000u;
+        }
         // max over the half with four independent chains (a single running max would be a
         // 64-long dependency chain)
         float cmk[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        if (need_mask) {
 #pragma unroll
-          for (int e = 0; e < 64; ++e)
-            cmk[e & 3] = fmaxf(cmk[e & 3], ((vm[2 * hf + (e >> 5)] >> (e & 31)) & 1u)
-                                               ? __uint_as_float(r[e]) : -INFINITY);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 64; e += 8) {
-            cmk[0] = fmaxf(cmk[0], fmaxf(__uint_as_float(r[e]), __uint_as_float(r[e + 1])));
-            cmk[1] = fmaxf(cmk[1], fmaxf(__uint_as_float(r[e + 2]), __uint_as_float(r[e + 3])));
-            cmk[2] = fmaxf(cmk[2], fmaxf(__uint_as_float(r[e + 4]), __uint_as_float(r[e + 5])));
-            cmk[3] = fmaxf(cmk[3], fmaxf(__uint_as_float(r[e + 6]), __uint_as_float(r[e + 7])));
-          }
+        for (int e = 0; e < 64; e += 8) {
+          cmk[0] = fmaxf(cmk[0], fmaxf(__uint_as_float(r[e]), __uint_as_float(r[e + 1])));
+          cmk[1] = fmaxf(cmk[1], fmaxf(__uint_as_float(r[e + 2]), __uint_as_float(r[e + 3])));
+          cmk[2] = fmaxf(cmk[2], fmaxf(__uint_as_float(r[e + 4]), __uint_as_float(r[e + 5])));
+          cmk[3] = fmaxf(cmk[3], fmaxf(__uint_as_float(r[e + 6]), __uint_as_float(r[e + 7])));
         }
         const float cm = fmaxf(fmaxf(cmk[0], cmk[1]), fmaxf(cmk[2], cmk[3]));
         const float cm2 = cm * sl2;
@@ -659,24 +787,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           for (int e2 = 0; e2 < 32; e2 += 2) {
             const int e = q4 * 32 + e2;
             float s0, s1;
-            if (need_mask) {
-              const uint32_t bits = vm[2 * hf + q4];
-              s0 = ((bits >> e2) & 1u) ? ex2(fmaf(__uint_as_float(r[e]), sl2, neg_m)) : 0.f;
-              s1 = ((bits >> (e2 + 1)) & 1u) ? ex2(fmaf(__uint_as_float(r[e + 1]), sl2, neg_m))
-                                             : 0.f;
+            const float2 t = __ffma2_rn(
+                make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])),
+                make_float2(sl2, sl2), make_float2(neg_m, neg_m));
+            if (kPolyEvery > 0 &&
+                ((e2 >> 1) % (kPolyEvery > 0 ? kPolyEvery : 1)) == kPolyEvery - 1) {
+              const float2 y = exp2_poly2(t);
+              s0 = y.x;
+              s1 = y.y;
             } else {
-              const float2 t = __ffma2_rn(
-                  make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])),
-                  make_float2(sl2, sl2), make_float2(neg_m, neg_m));
-              if (kPolyEvery > 0 &&
-                  ((e2 >> 1) % (kPolyEvery > 0 ? kPolyEvery : 1)) == kPolyEvery - 1) {
-                const float2 y = exp2_poly2(t);
-                s0 = y.x;
-                s1 = y.y;
-              } else {
-                s0 = ex2(t.x);
-                s1 = ex2(t.y);
-              }
+              s0 = ex2(t.x);
+              s1 = ex2(t.y);
             }
             lp2[(e2 >> 1) & 3] = __fadd2_rn(lp2[(e2 >> 1) & 3], make_float2(s0, s1));
             pw[e2 / 2] = pack_bf2(s0, s1);
@@ -703,6 +824,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       m_run = m_use;
       tc_fence_before();
       mbar_arrive(&p_ready[i]);
+      if (j + 2 < n_tiles && !rotate_tile(j + 2)) {
+        ok = false;
+        break;
+      }
     }
     // epilogue: O / l -> bf16 rows, lse
     ok = ok && cta_wait(o_final, 0, abort, lim, p.err);
@@ -729,55 +854,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       if (valid_row)
         p.lse[(size_t)(qbeg + t_row) * p.hq + qh] =
             l_run > 0.f ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
-    }
-  } else if (warp >= 12) {
-    // ============================== rotation (128 threads: chunk c, 8 consecutive rows)
-    // No group barrier: every thread waits for the tile itself, rotates its 8 rows x 16 bytes
-    // (one page) and arrives; (cos, sin) of its page offset stay in registers until the offset
-    // changes (at a document boundary).
-    const int tr = tid - 384;
-    const int c = tr & 7, rg = tr >> 3;  // rows 8rg .. 8rg+7, page rg / 2
-    const uint64_t *turn = p.turn;
-    bool ok = cta_wait(q_full, 0, abort, lim, p.err);
-    if (ok) {
-      for (int i = 0; i < 2; ++i) {
-        for (int rr = 0; rr < 8; ++rr) {
-          const int row = rg * 8 + rr;
-          RotPairs rq;
-          chunk_angles((int64_t)(i * TQ + row / G), turn, c, rq);  // query pos - m0
-          rotate_row_chunk(Qs + i * kTileBytes, row, c, rq);
-        }
-      }
-      fence_async_smem();
-    }
-    mbar_arrive(q_rot);
-    int64_t cached = INT64_MIN;
-    RotPairs rp;
-    for (int j = 0; ok && j < n_tiles; ++j) {
-      const int s = j % kNK;
-      if (!cta_wait(&k_full[s], (j / kNK) & 1, abort, lim, p.err)) break;
-      const KMeta &mt = meta_k[s];
-      uint8_t *kt = Ks + s * kTileBytes;
-      if (mt.kind == 0) {
-        // one relative rotation R(o - m0) per page
-        const int64_t d = (int64_t)mt.off[rg >> 1] - m0;
-        if (d != cached) {
-          cached = d;
-          chunk_angles(d, turn, c, rp);
-        }
-#pragma unroll
-        for (int rr = 0; rr < 8; ++rr) rotate_row_chunk(kt, rg * 8 + rr, c, rp);
-      } else {
-        // question keys: raw, rotated by R(p - m0) row by row
-        for (int rr = 0; rr < 8; ++rr) {
-          const int row = rg * 8 + rr;
-          RotPairs rk;
-          chunk_angles((int64_t)(mt.c0 + row - t0), turn, c, rk);
-          rotate_row_chunk(kt, row, c, rk);
-        }
-      }
-      fence_async_smem();
-      mbar_arrive(&k_rot[s]);
     }
   }
 
