@@ -193,6 +193,44 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
       : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+// All 128 fp32 TMEM columns of this thread's lane. Load and wait are one statement, so no use
+// of the registers can be scheduled before the wait.
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
+  asm volatile(
+      "{\n"
+      "tcgen05.ld.sync.aligned.32x32b.x128.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,"
+      "%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,"
+      "%58,%59,%60,%61,%62,%63,%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,"
+      "%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,%96,%97,%98,%99,%100,"
+      "%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,%112,%113,%114,%115,%116,%117,"
+      "%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%128];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      "}"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]),
+        "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]),
+        "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]),
+        "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]),
+        "=r"(r[62]), "=r"(r[63]), "=r"(r[64]), "=r"(r[65]), "=r"(r[66]), "=r"(r[67]),
+        "=r"(r[68]), "=r"(r[69]), "=r"(r[70]), "=r"(r[71]), "=r"(r[72]), "=r"(r[73]),
+        "=r"(r[74]), "=r"(r[75]), "=r"(r[76]), "=r"(r[77]), "=r"(r[78]), "=r"(r[79]),
+        "=r"(r[80]), "=r"(r[81]), "=r"(r[82]), "=r"(r[83]), "=r"(r[84]), "=r"(r[85]),
+        "=r"(r[86]), "=r"(r[87]), "=r"(r[88]), "=r"(r[89]), "=r"(r[90]), "=r"(r[91]),
+        "=r"(r[92]), "=r"(r[93]), "=r"(r[94]), "=r"(r[95]), "=r"(r[96]), "=r"(r[97]),
+        "=r"(r[98]), "=r"(r[99]), "=r"(r[100]), "=r"(r[101]), "=r"(r[102]), "=r"(r[103]),
+        "=r"(r[104]), "=r"(r[105]), "=r"(r[106]), "=r"(r[107]), "=r"(r[108]), "=r"(r[109]),
+        "=r"(r[110]), "=r"(r[111]), "=r"(r[112]), "=r"(r[113]), "=r"(r[114]), "=r"(r[115]),
+        "=r"(r[116]), "=r"(r[117]), "=r"(r[118]), "=r"(r[119]), "=r"(r[120]), "=r"(r[121]),
+        "=r"(r[122]), "=r"(r[123]), "=r"(r[124]), "=r"(r[125]), "=r"(r[126]), "=r"(r[127])
+      : "r"(taddr)
+      : "memory");
+}
 // Asynchronous 32-column load; the registers are valid only after tmem_wait_ld on them.
 __device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
@@ -719,91 +757,64 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           }
         }
       }
-      // One pass over S in two 64-column halves, each loaded once: the half's max is taken on
-      // registers, then its weights are formed. The running max m_use only moves when a half's
-      // max exceeds it by more than 8 (log2 domain, so weights stay <= 2^8); then the weights
-      // already written for this tile, this tile's partial sum and (below) O are scaled by
-      // 2^(m_old - m_new).
+      // The whole score row is loaded at once; the running max m_use only moves when the
+      // tile's max exceeds it by more than 8 (log2 domain, so weights stay <= 2^8), and then
+      // this row's sum and (below) O are scaled by alpha = 2^(m_old - m_new).
       float m_use = m_run, alpha = 1.f;
+      uint32_t r[128];
+      tmem_ld128(s_col, r);
+      if (need_mask) {
+        // hidden keys get -inf: they drop out of the max and ex2(-inf) = 0
+#pragma unroll
+        for (int e = 0; e < 128; ++e)
+          if (!((vm[e >> 5] >> (e & 31)) & 1u)) r[e] = 0xFF800000u;
+      }
+      // max with eight independent chains (one running max would be a 128-long chain)
+      float cmk[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        cmk[k] = fmaxf(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1]));
+#pragma unroll
+      for (int e = 16; e < 128; e += 16) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          cmk[k] = fmaxf(cmk[k], fmaxf(__uint_as_float(r[e + 2 * k]),
+                                       __uint_as_float(r[e + 2 * k + 1])));
+      }
+      const float cm = fmaxf(fmaxf(fmaxf(cmk[0], cmk[1]), fmaxf(cmk[2], cmk[3])),
+                             fmaxf(fmaxf(cmk[4], cmk[5]), fmaxf(cmk[6], cmk[7])));
+      const float cm2 = cm * sl2;
+      if (cm2 > m_use + 8.f) {  // includes the first finite max (m_use = -inf)
+        alpha = (m_use == -INFINITY) ? 0.f : ex2(m_use - cm2);
+        m_use = cm2;
+      }
+      const float neg_m = (m_use == -INFINITY) ? 0.f : -m_use;
       float2 lp2[4];  // row-sum partials, four independent chains
 #pragma unroll
       for (int k = 0; k < 4; ++k) lp2[k] = make_float2(0.f, 0.f);
-      // The halves run as a loop, not unrolled, so the loop body stays small (see angle_cs).
-#pragma unroll 1
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t r[64];
-        tmem_ld64(s_col + hf * 64, r);
-        if (need_mask) {
-          // hidden keys get -inf: they drop out of the max and ex2(-inf) = 0
-          const uint32_t m_lo = hf ? vm[2] : vm[0], m_hi = hf ? vm[3] : vm[1];
+      // weights as bf16 pairs into S's first 64 columns (all of S is in registers by now)
 #pragma unroll
-          for (int e = 0; e < 64; ++e)
-            if (!(((e < 32 ? m_lo : m_hi) >> (e & 31)) & 1u)) r[e] = 0xFF800000u;
-        }
-        // max over the half with four independent chains (a single running max would be a
-        // 64-long dependency chain)
-        float cmk[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint32_t pw[16];
 #pragma unroll
-        for (int e = 0; e < 64; e += 8) {
-          cmk[0] = fmaxf(cmk[0], fmaxf(__uint_as_float(r[e]), __uint_as_float(r[e + 1])));
-          cmk[1] = fmaxf(cmk[1], fmaxf(__uint_as_float(r[e + 2]), __uint_as_float(r[e + 3])));
-          cmk[2] = fmaxf(cmk[2], fmaxf(__uint_as_float(r[e + 4]), __uint_as_float(r[e + 5])));
-          cmk[3] = fmaxf(cmk[3], fmaxf(__uint_as_float(r[e + 6]), __uint_as_float(r[e + 7])));
-        }
-        const float cm = fmaxf(fmaxf(cmk[0], cmk[1]), fmaxf(cmk[2], cmk[3]));
-        const float cm2 = cm * sl2;
-        const bool raise = cm2 > m_use + 8.f;  // includes the first finite max (m_use = -inf)
-        float a = 1.f;
-        if (raise) {
-          a = (m_use == -INFINITY) ? 0.f : ex2(m_use - cm2);
-          m_use = cm2;
-          alpha *= a;
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            lp2[k].x *= a;
-            lp2[k].y *= a;
+        for (int e2 = 0; e2 < 32; e2 += 2) {
+          const int e = q4 * 32 + e2;
+          float s0, s1;
+          const float2 t = __ffma2_rn(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])),
+                                      make_float2(sl2, sl2), make_float2(neg_m, neg_m));
+          if (kPolyEvery > 0 &&
+              ((e2 >> 1) % (kPolyEvery > 0 ? kPolyEvery : 1)) == kPolyEvery - 1) {
+            const float2 y = exp2_poly2(t);
+            s0 = y.x;
+            s1 = y.y;
+          } else {
+            s0 = ex2(t.x);
+            s1 = ex2(t.y);
           }
+          lp2[(e2 >> 1) & 3] = __fadd2_rn(lp2[(e2 >> 1) & 3], make_float2(s0, s1));
+          pw[e2 / 2] = pack_bf2(s0, s1);
         }
-        if (hf == 1 && __any_sync(0xffffffffu, raise && a != 0.f)) {
-          // rare: rescale the weights of the first half, already written as bf16 pairs
-#pragma unroll
-          for (int k = 0; k < 2; ++k) {
-            uint32_t w[16];
-            tmem_ld16(s_col + k * 16, w);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const float lo = __uint_as_float(w[e] << 16) * a;
-              const float hi = __uint_as_float(w[e] & 0xFFFF0000u) * a;
-              w[e] = pack_bf2(lo, hi);
-            }
-            tmem_st16(s_col + k * 16, w);
-          }
-        }
-        const float neg_m = (m_use == -INFINITY) ? 0.f : -m_use;
-#pragma unroll
-        for (int q4 = 0; q4 < 2; ++q4) {
-          uint32_t pw[16];
-#pragma unroll
-          for (int e2 = 0; e2 < 32; e2 += 2) {
-            const int e = q4 * 32 + e2;
-            float s0, s1;
-            const float2 t = __ffma2_rn(
-                make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])),
-                make_float2(sl2, sl2), make_float2(neg_m, neg_m));
-            if (kPolyEvery > 0 &&
-                ((e2 >> 1) % (kPolyEvery > 0 ? kPolyEvery : 1)) == kPolyEvery - 1) {
-              const float2 y = exp2_poly2(t);
-              s0 = y.x;
-              s1 = y.y;
-            } else {
-              s0 = ex2(t.x);
-              s1 = ex2(t.y);
-            }
-            lp2[(e2 >> 1) & 3] = __fadd2_rn(lp2[(e2 >> 1) & 3], make_float2(s0, s1));
-            pw[e2 / 2] = pack_bf2(s0, s1);
-          }
-          tmem_st16(s_col + hf * 32 + q4 * 16, pw);
-        }
+        tmem_st16(s_col + q4 * 16, pw);
       }
       // O *= alpha for rows whose max moved (warp-collective TMEM access); O holds data only
       // after the first tile's PV.
