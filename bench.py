@@ -127,6 +127,40 @@ def _max_over_ranks(x, ws):
 # ------------------------------------------------------------------------------------------------
 # Our arm
 # ------------------------------------------------------------------------------------------------
+def _dist_ms(times):
+    """Median, p10 and p90 of per-step times (ms)."""
+    t = sorted(times)
+
+    def q(f):
+        x = f * (len(t) - 1)
+        lo = int(x)
+        hi = min(lo + 1, len(t) - 1)
+        return t[lo] + (t[hi] - t[lo]) * (x - lo)
+    return {"median": round(q(0.5), 5), "p10": round(q(0.1), 5), "p90": round(q(0.9), 5),
+            "n": len(t)}
+
+
+def _cpu_model():
+    try:
+        import subprocess
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                k = ln.split(":")[0].strip().lower()
+                if k in ("model name", "cpu model", "hardware"):
+                    return ln.split(":", 1)[1].strip()
+        import platform
+        return platform.processor() or platform.machine()
+    except OSError:
+        return None
+
+
 def _timed_steps(fn, steps, flush, stream):
     """Run `steps` calls of fn, each after an untimed L2 flush; return per-step ms (events)."""
     import torch
@@ -378,6 +412,8 @@ def bench_ours(args):
             "ms_per_call": round(sum(nr_ms) / len(nr_ms), 5),
             "frac": round(n_bytes / (sum(nr_ms) / len(nr_ms) * 1e-3) / 1e9 / hbm_peak, 4)},
         "decode_tokens_per_s": round(ws * B / (ms_per_step * 1e-3), 1),
+        "step_ms_dist": _dist_ms(step_ms),
+        "decode_call_ms_dist": _dist_ms(dec_ms),
         "clocks": clocks,
     }
     if not only_decode:
@@ -388,7 +424,7 @@ def bench_ours(args):
             "workload": "prefill_b8: 8 req x (16 Zipf(1.0) docs x 1024 + 256 causal question), "
                         "Hq32/Hkv8/D128 bf16",
             "value": round(tflops, 2), "unit": "TFLOP/s", "ms_per_call": round(pre_avg, 4),
-            "flops_per_call": pb.flops,
+            "ms_dist": _dist_ms(pre_ms), "flops_per_call": pb.flops,
             "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": tc_peak,
                          "unit": "TFLOP/s", "frac": round(tflops / tc_peak, 4),
                          "peak_kind": peak_kind}}
@@ -396,7 +432,7 @@ def bench_ours(args):
             "workload": "long_decode_b16: 16 req x 131073 keys (64 Zipf(1.2) docs x 2048 + 1)",
             "value": round(l_bytes / (long_avg * 1e-3) / 1e9, 2), "unit": "GB/s",
             "tokens_per_s": round(lwl.batch / (long_avg * 1e-3), 1),
-            "ms_per_step": round(long_avg, 4),
+            "ms_per_step": round(long_avg, 4), "ms_dist": _dist_ms(long_ms),
             "frac": round(l_bytes / (long_avg * 1e-3) / 1e9 / hbm_peak, 4)}
     if not only_decode:
         # free the other workloads' pools before the 17 GB mixed pools
@@ -495,10 +531,16 @@ def cpu_baseline(wl, src, kv_bytes_total, budget_s):
     for b in range(1, 1 + n):
         oracle.attend_request(wl, b, src=view, threads=threads)
     dt = time.perf_counter() - t0
+    # the same oracle on one core, one request
+    t0 = time.perf_counter()
+    oracle.attend_request(wl, wl.batch - 1, src=view, threads=1)
+    dt1 = time.perf_counter() - t0
     return {"value": round(n * per_req / dt / 1e9, 4), "unit": "GB/s", "cores": threads,
             "kind": "oracle",
             "sample": f"{n} of {wl.batch} requests, all 32 heads ({n * per_req / 1e9:.3f} GB "
-                      f"logical KV, {dt:.1f} s), fp64 C oracle form A"}
+                      f"logical KV, {dt:.1f} s), fp64 C oracle form A",
+            "one_core_value": round(per_req / dt1 / 1e9, 4),
+            "cpu_model": _cpu_model()}
 
 
 # ------------------------------------------------------------------------------------------------
@@ -536,7 +578,8 @@ def bench_reference(args):
                    "parallelism": "host cores"},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
                          "kind": "oracle",
-                         "sample": "each step = one request of the decode workload, all heads"},
+                         "sample": "each step = one request of the decode workload, all heads",
+                         "cpu_model": _cpu_model()},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "gpu_launches": 0,

@@ -8,19 +8,21 @@
 //
 // CTA = (request b, kv head h, 2 x TQ question tokens): two 128-row Q tiles, rows ordered
 // (token, query head of the group), TQ = 128 / G. 12 warps:
-//   warp 0      TMA producer: Q tiles once, then per 128-key tile 8 page boxes (16 rows x 64
-//               dims, 128B swizzle) of K and of V into a 2-stage ring; question keys by
+//   warp 0      TMA producer: Q tiles once, then per 128-key tile K into a 3-stage ring and V
+//               into a 2-stage ring (K one tile ahead of V); 8 consecutive full blocks go as one
+//               box, otherwise 8 page boxes (16 rows x 64 dims, 128B swizzle); question keys by
 //               128-token boxes.
 //   warp 1      TMEM owner (512 columns) and single-thread tcgen05.mma issuer:
 //               S_i = Q_i K^T (SS), then O_i += P_i V (P from TMEM, V MN-major).
 //   warps 4-7   softmax of Q tile 0, warps 8-11 of Q tile 1 (TMEM lane quadrant = warp % 4):
-//               online softmax in the log2 domain with a lazy rescale (the running max only
-//               moves when a row max exceeds it by more than 8), P written back into S's TMEM
-//               columns as bf16 pairs. The same 256 threads rotate the Q tiles once and each K
-//               tile in shared memory, in place (the pair (i, i+64) sits at the same swizzled
-//               offset of the two 64-dim boxes), two tiles ahead of the scores they need.
-//               (Dedicated rotation warps were measured 27% slower: their stores contended
-//               with the softmax on the critical softmax -> PV -> QK chain.)
+//               each thread holds its row's 128 scores, online softmax in the log2 domain with
+//               a lazy rescale (the running max only moves when the tile max exceeds it by more
+//               than 8), P written back into S's TMEM columns as bf16 pairs. The same 256 threads
+//               rotate their Q rows once and each K tile in shared memory, in place (the pair
+//               (i, i+64) sits at the same swizzled offset of the two 64-dim boxes), two tiles
+//               ahead of the scores that need it.
+// The softmax loop is kept compact (one shared angle routine, one code path for masked and full
+// tiles): with per-site copies the kernel was instruction-fetch bound.
 // TMEM: S_0 [0,128) S_1 [128,256) O_0 [256,384) O_1 [384,512) fp32 columns.
 // Every wait is bounded; a timeout sets LAZY_DEVERR_TIMEOUT, raises a CTA abort flag that
 // releases the other roles, drains outstanding copies and MMAs, frees TMEM and returns.
@@ -175,24 +177,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
-#define LAZY_R64(r)                                                                          \
-  LAZY_R32(r), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]),   \
-      "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]),             \
-      "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]),             \
-      "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),             \
-      "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]),             \
-      "=r"(r[62]), "=r"(r[63])
-// 64 consecutive fp32 TMEM columns of this thread's lane (one round trip).
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,"
-      "%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,"
-      "%58,%59,%60,%61,%62,%63}, [%64];"
-      : LAZY_R64(r)
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
 // All 128 fp32 TMEM columns of this thread's lane. Load and wait are one statement, so no use
 // of the registers can be scheduled before the wait.
 __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
@@ -230,37 +214,6 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
         "=r"(r[122]), "=r"(r[123]), "=r"(r[124]), "=r"(r[125]), "=r"(r[126]), "=r"(r[127])
       : "r"(taddr)
       : "memory");
-}
-// Asynchronous 32-column load; the registers are valid only after tmem_wait_ld on them.
-__device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : LAZY_R32(r)
-      : "r"(taddr));
-}
-// Waits for this thread's outstanding TMEM loads; `r` is threaded through so that no use of the
-// loaded registers can be scheduled before the wait.
-__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;"
-               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
-                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
-                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
-                 "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
-                 "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
-                 "+r"(r[30]), "+r"(r[31])
-               :
-               : "memory");
-}
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
@@ -318,42 +271,8 @@ __device__ __forceinline__ void rotate_row_chunk(uint8_t *tile, int row, int c,
   *hi = *reinterpret_cast<uint4 *>(yo);
 }
 
-// The same rotation for 8 consecutive rows (one per-page angle set): all 16 loads are issued
-// before any store, so the rows' latencies overlap instead of chaining through in-place stores
-// the compiler must keep ordered.
-__device__ __forceinline__ void rotate_8rows_chunk(uint8_t *tile, int row0, int c,
-                                                   const RotPairs &rp) {
-  uint4 a[8], b[8];
-#pragma unroll
-  for (int rr = 0; rr < 8; ++rr) {
-    const int row = row0 + rr;
-    const int phys = (c ^ (row & 7)) * 16;
-    a[rr] = *reinterpret_cast<const uint4 *>(tile + row * 128 + phys);
-    b[rr] = *reinterpret_cast<const uint4 *>(tile + kHalfBytes + row * 128 + phys);
-  }
-#pragma unroll
-  for (int rr = 0; rr < 8; ++rr) {
-    __nv_bfloat162 *x = reinterpret_cast<__nv_bfloat162 *>(&a[rr]);
-    __nv_bfloat162 *y = reinterpret_cast<__nv_bfloat162 *>(&b[rr]);
-    __nv_bfloat162 xo[4], yo[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      xo[k] = __hfma2(y[k], rp.nsi[k], __hmul2(x[k], rp.co[k]));
-      yo[k] = __hfma2(x[k], rp.si[k], __hmul2(y[k], rp.co[k]));
-    }
-    a[rr] = *reinterpret_cast<uint4 *>(xo);
-    b[rr] = *reinterpret_cast<uint4 *>(yo);
-  }
-#pragma unroll
-  for (int rr = 0; rr < 8; ++rr) {
-    const int row = row0 + rr;
-    const int phys = (c ^ (row & 7)) * 16;
-    *reinterpret_cast<uint4 *>(tile + row * 128 + phys) = a[rr];
-    *reinterpret_cast<uint4 *>(tile + kHalfBytes + row * 128 + phys) = b[rr];
-  }
-}
-
-// The same for 4 consecutive rows of one page.
+// The same rotation for 4 consecutive rows of one page (one angle set): all loads first, then
+// the math, then the stores.
 __device__ __forceinline__ void rotate_4rows_chunk(uint8_t *tile, int row0, int c,
                                                    const RotPairs &rp) {
   uint4 a[4], b[4];
