@@ -435,8 +435,10 @@ def bench_ours(args):
             "ms_per_step": round(long_avg, 4), "ms_dist": _dist_ms(long_ms),
             "frac": round(l_bytes / (long_avg * 1e-3) / 1e9 / hbm_peak, 4)}
     if not only_decode:
-        # free the other workloads' pools before the 17 GB mixed pools
+        # free the other workloads' pools before the chain's and the 17 GB mixed pools
         del pres, pb, pout, plse, lres, ldb, lws, lout, llse
+        torch.cuda.empty_cache()
+        line["chain"] = chain_bench(args, flush, stream)
         torch.cuda.empty_cache()
         line["mixed"] = mixed_sweep(args, flush, stream, hbm_peak)
     if rank == 0 and not args.no_cpu_baseline:
@@ -505,6 +507,77 @@ def mixed_sweep(args, flush, stream, hbm_peak):
         del res, pb, db, ws, dout, dlse, pout, plse, src
         torch.cuda.empty_cache()
     return out
+
+
+def chain_bench(args, flush, stream, n_steps=32, reps=3):
+    """Prefill -> decode chain on the prefill workload: one lazy_attn_prefill_append (the
+    question enters the pool as each request's private segment), then n_steps decode steps
+    (token append + decode) over documents + question + generated tokens. L2 is flushed before
+    each chain; step inputs are on the device before timing."""
+    import torch
+
+    import position_independent_kv_lazy_gb300 as pk
+    import workload as W
+    from position_independent_kv_lazy_gb300 import harness as H
+
+    wl = W.prefill_workload()
+    src = H.DeviceSource(wl)
+    res = H.build_resident(wl, src, extra_blocks=H.chain_blocks_needed(wl, n_steps))
+    ch = H.chain_setup(wl, res, src, n_steps)
+    pb = ch.pb
+    steps = [H.chain_step_batch(wl, res, ch, s, src) for s in range(n_steps)]
+    B = len(pb.reqs)
+    pout = torch.empty_like(pb.q)
+    plse = torch.empty((pb.total_q, wl.Hq), dtype=torch.float32, device="cuda")
+    dws = torch.empty(pk.lazy_decode_workspace_bytes(res.pool, B, wl.Hq), dtype=torch.uint8,
+                      device="cuda")
+    dout = torch.empty((B, wl.Hq, wl.D), dtype=torch.bfloat16, device="cuda")
+    dlse = torch.empty((B, wl.Hq), dtype=torch.float32, device="cuda")
+
+    def run_chain(events):
+        flush()
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(n_steps + 2)]
+        e[0].record(stream)
+        pk.lazy_attn_prefill_append(res.pool, pb.q, pb.k_new, pb.v_new, pb.cu_q, pb.q_pos0,
+                                    pb.words, pb.cu_pages, pb.max_q_len, ch.append_slots,
+                                    ch.append_local_pos, sm_scale=wl.sm_scale, out=pout,
+                                    lse=plse)
+        e[1].record(stream)
+        for s, db in enumerate(steps):
+            pk.kv_pool_write_tokens(res.pool, db.new_k, db.new_v, db.slot_mapping, db.local_pos)
+            pk.lazy_attn_decode(res.pool, db.q, db.q_pos, db.words, db.cu_pages,
+                                sm_scale=wl.sm_scale, out=dout, lse=dlse, workspace=dws)
+            e[s + 2].record(stream)
+        events.append(e)
+
+    warm = []
+    run_chain(warm)
+    torch.cuda.synchronize()
+    if pk.lazy_get_device_error(res.pool) != 0:
+        raise RuntimeError("device error in the prefill -> decode chain")
+    runs = []
+    for _ in range(reps):
+        run_chain(runs)
+    torch.cuda.synchronize()
+    pre = [e[0].elapsed_time(e[1]) for e in runs]
+    stp = [e[s + 1].elapsed_time(e[s + 2]) for e in runs for s in range(n_steps)]
+    tot = [e[0].elapsed_time(e[-1]) for e in runs]
+    tokens = pb.total_q + B * n_steps
+    step_bytes = sum(db.n_keys for db in steps) / n_steps * wl.kv_bytes_per_token()
+    med = sorted(tot)[len(tot) // 2]
+    res.pool.close()
+    return {
+        "workload": f"prefill_b8 question (8 x 256 tokens) kept in the pool, then {n_steps} "
+                    "decode steps of 8 requests (token append + decode), 16 docs x 1024 each",
+        "unit": "tokens/s",
+        "tokens_per_s": round(tokens / (med * 1e-3), 1),
+        "ms_per_chain": _dist_ms(tot),
+        "prefill_append_ms": _dist_ms(pre),
+        "prefill_append_tflops": round(pb.flops / (sorted(pre)[len(pre) // 2] * 1e-3) / 1e12, 2),
+        "decode_step_ms": _dist_ms(stp),
+        "decode_step_gbs": round(step_bytes / (sorted(stp)[len(stp) // 2] * 1e-3) / 1e9, 2),
+        "reps": reps,
+    }
 
 
 def _kernel_hash():

@@ -131,7 +131,9 @@ int kv_pool_insert_doc(lazy_pool *pool, const void *d_k_raw, const void *d_v, in
  * Scattered form of the same encode for batches of appended tokens (one decode step adds one
  * token to each request's private segment): token t goes to slot d_slot_mapping[t]
  * (= block * page_size + slot) with local position d_local_pos[t]. Device arrays, n_tokens
- * entries; entries < 0 are skipped. Blocks must already be allocated.
+ * entries; entries < 0 are skipped. Blocks must already be allocated. A slot whose block lies
+ * outside the pool is not written and sets LAZY_DEVERR_BAD_PAGE (read by
+ * lazy_get_device_error).
  */
 int kv_pool_write_tokens(lazy_pool *pool, const void *d_k_raw, const void *d_v, int32_t n_tokens,
                          const int32_t *d_slot_mapping, const int32_t *d_local_pos,
@@ -248,6 +250,29 @@ int lazy_attn_prefill(lazy_pool *pool, const void *d_q, const void *d_k_new, con
                       int32_t total_q, int32_t max_q_len, int32_t num_q_heads, float sm_scale,
                       void *d_out, float *d_lse, void *d_workspace, size_t workspace_bytes,
                       int32_t flags, lazy_stream_t stream);
+
+/*
+ * Prefill followed by the question's own K/V entering the pool, in one call (the summaries'
+ * prefill and decoding parts chained: after prefill the question is a cached segment that
+ * decode steps read by page word like any document). Arguments as lazy_attn_prefill, plus
+ *   d_append_slots      device int32 [total_q]: slot (block * page_size + slot) that question
+ *                       token t (row t of d_k_new / d_v_new) goes to; < 0 skips the token
+ *   d_append_local_pos  device int32 [total_q]: its local position j within the private
+ *                       segment; the pool receives R(j) k_new[t] and v_new[t], exactly as
+ *                       kv_pool_write_tokens writes them
+ * The caller owns the private segment's blocks (kv_pool_alloc) and lists them, with the
+ * segment's logical offset (normally d_q_pos0[b]), in later decode page words.
+ * d_k_new and d_v_new must be given. All arguments are checked before anything is launched;
+ * both steps are queued on `stream`.
+ */
+int lazy_attn_prefill_append(lazy_pool *pool, const void *d_q, const void *d_k_new,
+                             const void *d_v_new, const int32_t *d_cu_q, const int32_t *d_q_pos0,
+                             const uint64_t *d_page_words, const int32_t *d_cu_pages,
+                             int32_t batch, int32_t total_q, int32_t max_q_len,
+                             int32_t num_q_heads, float sm_scale, void *d_out, float *d_lse,
+                             void *d_workspace, size_t workspace_bytes, int32_t flags,
+                             const int32_t *d_append_slots, const int32_t *d_append_local_pos,
+                             lazy_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
  * Errors and test hooks

@@ -43,7 +43,7 @@ EXPORTS = [
     "kv_pool_write_tokens", "lazy_pack_page", "lazy_unpack_page", "lazy_pack_pages",
     "lazy_decode_workspace_bytes", "lazy_attn_decode", "lazy_prefill_workspace_bytes",
     "lazy_attn_prefill", "lazy_get_device_error", "lazy_debug_gather", "lazy_debug_wait_timeout",
-    "lazy_attn_decode_noalloc", "lazy_debug_exp2",
+    "lazy_attn_decode_noalloc", "lazy_debug_exp2", "lazy_attn_prefill_append",
 ]
 
 
@@ -94,6 +94,9 @@ _SIGS = {
     "lazy_prefill_workspace_bytes": ([_vp, _i32, _i32, _i32, _i32, _i32, _psz], ctypes.c_int),
     "lazy_attn_prefill": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _f32,
                            _vp, _vp, _vp, ctypes.c_size_t, _i32, _vp], ctypes.c_int),
+    "lazy_attn_prefill_append": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32,
+                                  _i32, _f32, _vp, _vp, _vp, ctypes.c_size_t, _i32, _vp, _vp,
+                                  _vp], ctypes.c_int),
     "lazy_get_device_error": ([_vp, _pi32, _vp], ctypes.c_int),
     "lazy_debug_gather": ([_vp, _vp, _i32, _vp, _vp, _vp, _vp], ctypes.c_int),
     "lazy_debug_wait_timeout": ([_vp, _u64, _vp], ctypes.c_int),
@@ -335,6 +338,34 @@ def lazy_attn_prefill(pool: LazyPool, q, k_new, v_new, cu_q, q_pos0, page_words,
         pool.handle, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(cu_q), _ptr(q_pos0),
         _ptr(page_words), _ptr(cu_pages), B, Tq, max_q_len, Hq, float(sm_scale), _ptr(out),
         _ptr(lse), _ptr(ws), n.value, flags, _stream(stream)))
+    return out, lse
+
+
+def lazy_attn_prefill_append(pool: LazyPool, q, k_new, v_new, cu_q, q_pos0, page_words, cu_pages,
+                             max_q_len: int, append_slots, append_local_pos, sm_scale=None,
+                             out=None, lse=None, flags: int = 0, stream=None):
+    """lazy_attn_prefill, then every question token t written into the pool at slot
+    append_slots[t] (int32, block * page_size + slot, < 0 skips) as R(append_local_pos[t])
+    k_new[t] and v_new[t]. Returns (out, lse)."""
+    import torch
+    Tq, Hq, D = q.shape
+    B = int(cu_q.shape[0]) - 1
+    if sm_scale is None:
+        sm_scale = 1.0 / float(D) ** 0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((Tq, Hq), dtype=torch.float32, device=q.device)
+    n = ctypes.c_size_t()
+    lib = load_library()
+    _check("lazy_prefill_workspace_bytes", lib.lazy_prefill_workspace_bytes(
+        pool.handle, B, Tq, max_q_len, Hq, flags, ctypes.byref(n)))
+    ws = torch.empty(max(n.value, 1), dtype=torch.uint8, device=q.device)
+    _check("lazy_attn_prefill_append", lib.lazy_attn_prefill_append(
+        pool.handle, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(cu_q), _ptr(q_pos0),
+        _ptr(page_words), _ptr(cu_pages), B, Tq, max_q_len, Hq, float(sm_scale), _ptr(out),
+        _ptr(lse), _ptr(ws), n.value, flags, _ptr(append_slots), _ptr(append_local_pos),
+        _stream(stream)))
     return out, lse
 
 

@@ -27,7 +27,7 @@ __global__ void __launch_bounds__(256) encode_kernel(
     const T *__restrict__ k_raw, const T *__restrict__ v, int32_t n_tokens, int32_t hkv,
     T *__restrict__ k_pool, T *__restrict__ v_pool, const uint64_t *__restrict__ turn,
     int32_t tok0, int32_t local_pos0, BlockList blocks, const int32_t *__restrict__ slot_map,
-    const int32_t *__restrict__ local_pos) {
+    const int32_t *__restrict__ local_pos, int32_t num_blocks, int32_t *err) {
   constexpr int EPL = 16 / (int)sizeof(T);
   constexpr int CH = (D / 2) / EPL;
   // A decode launched right after this append may start its launch early; it waits for this
@@ -47,6 +47,10 @@ __global__ void __launch_bounds__(256) encode_kernel(
       j = local_pos[t];
       blk = s / kPage;
       slot = s % kPage;
+      if (blk >= num_blocks) {  // a slot outside the pool: flag it, write nothing
+        if (c == 0) set_error(err, LAZY_DEVERR_BAD_PAGE);
+        continue;
+      }
     } else {
       j = local_pos0 + t;
       blk = blocks.ids[j / kPage - blocks.first_page];
@@ -85,7 +89,7 @@ int launch_encode(lazy_pool *p, const void *k_raw, const void *v, int32_t n_toke
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)p->num_sms * 16));
   encode_kernel<T, D><<<grid, threads, 0, s>>>(
       (const T *)k_raw, (const T *)v, n_tokens, p->hkv, (T *)p->k, (T *)p->v, p->d_turn, tok0,
-      local_pos0, bl, slot_map, local_pos);
+      local_pos0, bl, slot_map, local_pos, p->num_blocks, p->d_err);
   LAZY_CUDA_TRY(cudaGetLastError());
   return LAZY_OK;
 }

@@ -1,4 +1,5 @@
-// lazy_attn_prefill: argument checks and kernel choice.
+// lazy_attn_prefill: argument checks and kernel choice; lazy_attn_prefill_append: the same
+// call followed by the question's own K/V going into the pool as a private segment.
 #include "prefill.h"
 
 using namespace lazy;
@@ -64,4 +65,26 @@ extern "C" int lazy_attn_prefill(lazy_pool *p, const void *q, const void *k_new,
   }
   if (flags == LAZY_PREFILL_AUTO && tc_ok) return prefill_tc(p, pp, max_q_len, s);
   return prefill_simt(p, pp, max_q_len, s);
+}
+
+extern "C" int lazy_attn_prefill_append(lazy_pool *p, const void *q, const void *k_new,
+                                        const void *v_new, const int32_t *cu_q,
+                                        const int32_t *q_pos0, const uint64_t *words,
+                                        const int32_t *cu_pages, int32_t batch, int32_t total_q,
+                                        int32_t max_q_len, int32_t num_q_heads, float sm_scale,
+                                        void *out, float *lse, void *workspace,
+                                        size_t workspace_bytes, int32_t flags,
+                                        const int32_t *append_slots,
+                                        const int32_t *append_local_pos, lazy_stream_t stream) {
+  // Every argument of both steps is checked before anything is launched.
+  if (!p || total_q < 0) return LAZY_ERR_INVALID_ARG;
+  if (total_q > 0 && (!k_new || !v_new || !append_slots || !append_local_pos))
+    return LAZY_ERR_INVALID_ARG;
+  int rc = lazy_attn_prefill(p, q, k_new, v_new, cu_q, q_pos0, words, cu_pages, batch, total_q,
+                             max_q_len, num_q_heads, sm_scale, out, lse, workspace,
+                             workspace_bytes, flags, stream);
+  if (rc != LAZY_OK || batch == 0 || total_q == 0 || max_q_len == 0) return rc;
+  // Both steps only read k_new / v_new, so the encode needs no ordering after the attention
+  // beyond the stream's.
+  return kv_pool_write_tokens(p, k_new, v_new, total_q, append_slots, append_local_pos, stream);
 }

@@ -10,7 +10,7 @@ from typing import Dict, List, Optional
 
 import numpy as np
 
-from . import (LazyPool, build_page_table, kv_pool_insert_doc)
+from . import (LazyPool, build_page_table, kv_pool_alloc, kv_pool_insert_doc)
 
 
 def _torch_dtype(wl):
@@ -40,6 +40,17 @@ class HostSource:
         return (torch.from_numpy(self.wl.new_k(b)).to(device=device, dtype=dt),
                 torch.from_numpy(self.wl.new_v(b)).to(device=device, dtype=dt))
 
+    def step_q(self, b, step, device):
+        import torch
+        return torch.from_numpy(self.wl.step_q(b, step)).to(device=device,
+                                                            dtype=_torch_dtype(self.wl))
+
+    def step_kv(self, b, step, device):
+        import torch
+        dt = _torch_dtype(self.wl)
+        return (torch.from_numpy(self.wl.step_k(b, step)).to(device=device, dtype=dt),
+                torch.from_numpy(self.wl.step_v(b, step)).to(device=device, dtype=dt))
+
 
 class DeviceSource:
     """Device-side draws (``workload.normal_torch``) for workloads too large to draw on the host.
@@ -65,6 +76,12 @@ class DeviceSource:
         if b not in self._new:
             self._new[b] = self.wl.new_kv_torch(b, device)
         return self._new[b]
+
+    def step_q(self, b, step, device):
+        return self.wl.step_q_torch(b, step, device)
+
+    def step_kv(self, b, step, device):
+        return self.wl.step_kv_torch(b, step, device)
 
     def forget_docs(self):
         """Drop the raw document tensors once encoded (the pool holds the cache)."""
@@ -99,13 +116,19 @@ def pool_blocks_needed(wl, resident_pool: bool = True) -> int:
     return n_docs * per_doc + priv
 
 
+def chain_blocks_needed(wl, n_steps: int) -> int:
+    """Private-segment blocks a prefill -> decode chain of n_steps needs (see chain_setup)."""
+    return sum(-(-(r.T + n_steps) // wl.page_size) for r in wl.prefill_requests())
+
+
 def build_resident(wl, src, device="cuda", resident_pool: bool = True, stream=None,
-                   drop_raw: bool = True) -> Resident:
-    """Create the pool (sized for the whole document pool when ``resident_pool``) and encode every
-    document some request retrieved, once, plus each decode request's private segment."""
+                   drop_raw: bool = True, extra_blocks: int = 0) -> Resident:
+    """Create the pool (sized for the whole document pool when ``resident_pool``, plus
+    ``extra_blocks`` free blocks) and encode every document some request retrieved, once, plus
+    each decode request's private segment."""
     import torch
-    pool = LazyPool(pool_blocks_needed(wl, resident_pool), wl.Hkv, wl.D, _torch_dtype(wl),
-                    wl.rope_base, wl.page_size, device)
+    pool = LazyPool(pool_blocks_needed(wl, resident_pool) + extra_blocks, wl.Hkv, wl.D,
+                    _torch_dtype(wl), wl.rope_base, wl.page_size, device)
     doc_blocks: Dict[int, List[int]] = {}
     for d in wl.used_docs():
         k, v = src.doc_kv(d, device)
@@ -201,6 +224,65 @@ def prefill_batch(wl, res: Resident, src, device="cuda", reqs=None) -> PrefillBa
         torch.tensor([r.q_pos0 for r in reqs], dtype=torch.int32, device=device),
         torch.from_numpy(words.view(np.int64)).to(device), torch.from_numpy(cu).to(device),
         int(cu_q[-1]), max(r.T for r in reqs), flops)
+
+
+@dataclasses.dataclass
+class Chain:
+    """A prefill whose question then stays in the pool as each request's private segment, at
+    logical offset q_pos0 and local positions 0..T-1, followed by decode steps: step s appends
+    the token generated at local position T + s and decodes the query at q_pos0 + T + s."""
+    pb: PrefillBatch
+    priv_blocks: Dict[int, List[int]]
+    append_slots: object        # int32 [total_q]: block * page_size + slot of each question token
+    append_local_pos: object    # int32 [total_q]: its local position in the private segment
+    n_steps: int
+
+
+def chain_setup(wl, res: Resident, src, n_steps: int, device="cuda", reqs=None) -> Chain:
+    """Prefill inputs plus private-segment blocks sized for the question and n_steps tokens."""
+    import torch
+    pb = prefill_batch(wl, res, src, device, reqs)
+    P = wl.page_size
+    priv, slots, lpos = {}, [], []
+    for r in pb.reqs:
+        blocks = kv_pool_alloc(res.pool, -(-(r.T + n_steps) // P))
+        priv[r.index] = blocks
+        for t in range(r.T):
+            slots.append(blocks[t // P] * P + t % P)
+            lpos.append(t)
+    return Chain(pb, priv, torch.tensor(slots, dtype=torch.int32, device=device),
+                 torch.tensor(lpos, dtype=torch.int32, device=device), n_steps)
+
+
+def chain_step_batch(wl, res: Resident, ch: Chain, step: int, src, device="cuda") -> DecodeBatch:
+    """Decode inputs of chain step `step`: page words over every document plus the private
+    segment (question + tokens 0..step), the step's queries and the new token's k/v and slot."""
+    import torch
+    P = wl.page_size
+    segs, nk, nv, slots, lpos, qs, qpos = [], [], [], [], [], [], []
+    n_keys = 0
+    for r in ch.pb.reqs:
+        seg = [(res.doc_blocks[d], o, wl.doc_len) for d, o in zip(r.docs, r.offsets)]
+        j = r.T + step
+        seg.append((ch.priv_blocks[r.index], r.q_pos0, j + 1))
+        segs.append(seg)
+        n_keys += len(r.docs) * wl.doc_len + j + 1
+        k, v = src.step_kv(r.index, step, device)
+        nk.append(k)
+        nv.append(v)
+        qs.append(src.step_q(r.index, step, device))
+        blk = ch.priv_blocks[r.index][j // P]
+        slots.append(blk * P + j % P)
+        lpos.append(j)
+        qpos.append(r.q_pos0 + j)
+    words, cu = build_page_table(segs, P)
+    return DecodeBatch(
+        ch.pb.reqs, torch.cat(qs).contiguous(),
+        torch.tensor(qpos, dtype=torch.int32, device=device),
+        torch.from_numpy(words.view(np.int64)).to(device), torch.from_numpy(cu).to(device),
+        torch.cat(nk).contiguous(), torch.cat(nv).contiguous(),
+        torch.tensor(slots, dtype=torch.int32, device=device),
+        torch.tensor(lpos, dtype=torch.int32, device=device), n_keys)
 
 
 def kv_bytes_accounting(wl) -> Dict[str, int]:

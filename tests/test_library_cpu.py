@@ -134,7 +134,21 @@ def test_attention_argument_checks_return_before_device_use(lazylib):
                                      0.1, None, None, None, 0, 0, None) == pk.LAZY_ERR_INVALID_ARG
     assert lazylib.lazy_attn_prefill(h, None, None, None, None, None, None, None, 1, 4, 4, 4,
                                      0.1, None, None, None, 0, 9, None) == pk.LAZY_ERR_INVALID_ARG
+    # the fused prefill + append needs the question k/v and both append arrays
+    dummy = ctypes.c_void_p(16)
+    assert lazylib.lazy_attn_prefill_append(h, dummy, None, None, dummy, dummy, None, dummy, 1, 4,
+                                            4, 4, 0.1, dummy, dummy, None, 0, 0, dummy, dummy,
+                                            None) == pk.LAZY_ERR_INVALID_ARG
+    assert lazylib.lazy_attn_prefill_append(h, dummy, dummy, dummy, dummy, dummy, None, dummy, 1,
+                                            4, 4, 4, 0.1, dummy, dummy, None, 0, 0, None, dummy,
+                                            None) == pk.LAZY_ERR_INVALID_ARG
+    assert lazylib.lazy_attn_prefill_append(h, dummy, dummy, dummy, dummy, dummy, None, dummy, 1,
+                                            4, 4, 3, 0.1, dummy, dummy, None, 0, 0, dummy, dummy,
+                                            None) == pk.LAZY_ERR_INVALID_ARG
     # empty batches are a no-op
     assert lazylib.lazy_attn_decode(h, None, None, None, None, 0, 4, 0.1, 0, None, None, None, 0,
                                     None) == 0
+    assert lazylib.lazy_attn_prefill_append(h, None, None, None, None, None, None, None, 1, 0, 0,
+                                            4, 0.1, None, None, None, 0, 0, None, None,
+                                            None) == 0
     assert lazylib.lazy_pool_destroy(h) == 0

@@ -37,6 +37,16 @@ KIND_NEW_K = 4
 KIND_NEW_V = 5
 KIND_PRIV_K = 6
 KIND_PRIV_V = 7
+# decode steps that follow a prefill (prefill -> decode chain): the step's query and the
+# generated token's k/v, keyed by (request, step)
+KIND_STEP_Q = 8
+KIND_STEP_K = 9
+KIND_STEP_V = 10
+
+
+def step_index(b: int, step: int) -> int:
+    """Stream index of (request b, decode step `step`) for the KIND_STEP_* draws."""
+    return (b << 20) | step
 
 
 # ----------------------------------------------------------------------------------------------
@@ -172,6 +182,27 @@ class Workload:
         return self._get(KIND_PRIV_V, b, (r.priv_len, self.Hkv, self.D))
 
     # ---------------- device values (torch) ----------------
+    # ---------------- decode steps after a prefill (chain) ----------------
+    def step_q(self, b, step):
+        """Query of request b at decode step `step`: [1, Hq, D]."""
+        return self._get(KIND_STEP_Q, step_index(b, step), (1, self.Hq, self.D))
+
+    def step_k(self, b, step):
+        """Raw key of the token generated at that step: [1, Hkv, D]."""
+        return self._get(KIND_STEP_K, step_index(b, step), (1, self.Hkv, self.D))
+
+    def step_v(self, b, step):
+        return self._get(KIND_STEP_V, step_index(b, step), (1, self.Hkv, self.D))
+
+    def step_q_torch(self, b, step, device):
+        return normal_torch(self.seed, KIND_STEP_Q, step_index(b, step), (1, self.Hq, self.D),
+                            self.dtype, device)
+
+    def step_kv_torch(self, b, step, device):
+        s = (1, self.Hkv, self.D)
+        return (normal_torch(self.seed, KIND_STEP_K, step_index(b, step), s, self.dtype, device),
+                normal_torch(self.seed, KIND_STEP_V, step_index(b, step), s, self.dtype, device))
+
     def doc_kv_torch(self, d, device):
         s = (self.doc_len, self.Hkv, self.D)
         return (normal_torch(self.seed, KIND_DOC_K, d, s, self.dtype, device),
