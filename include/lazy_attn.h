@@ -64,8 +64,10 @@ enum { LAZY_DEVERR_BAD_PAGE = 1, LAZY_DEVERR_TIMEOUT = 2 };
 
 /* Prefill kernel choice (lazy_attn_prefill `flags`). */
 enum {
-    LAZY_PREFILL_AUTO = 0,  /* tensor-core kernel when bf16 and head_dim 128, else CUDA-core */
-    LAZY_PREFILL_SIMT = 1,  /* CUDA-core kernel, fp32 arithmetic, any supported shape */
+    LAZY_PREFILL_AUTO = 0,  /* tensor-core kernel when bf16, head_dim 128 and the group size
+                               (num_q_heads / num_kv_heads) is a power of two <= 32; else
+                               CUDA-core */
+    LAZY_PREFILL_SIMT = 1,  /* CUDA-core kernel, fp32 arithmetic, group size <= 64 */
     LAZY_PREFILL_TC = 2     /* tcgen05/TMEM kernel; LAZY_ERR_UNSUPPORTED if the shape is not */
 };
 

@@ -839,8 +839,10 @@ int prefill_tc_supported(const lazy_pool *p, int32_t hq) {
   if (p->dtype != LAZY_DTYPE_BF16 || p->d != 128 || p->page_size != kPage)
     return LAZY_ERR_UNSUPPORTED;
   if (hq % p->hkv) return LAZY_ERR_INVALID_ARG;
+  // a 128-row Q tile holds 128 / g whole tokens of the group; groups up to 32 (MQA with 32
+  // query heads) are the parity-tested range
   const int g = hq / p->hkv;
-  if (g != 1 && g != 2 && g != 4 && g != 8) return LAZY_ERR_UNSUPPORTED;
+  if (g < 1 || g > 32 || (g & (g - 1))) return LAZY_ERR_UNSUPPORTED;
   return LAZY_OK;
 }
 

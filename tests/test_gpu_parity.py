@@ -104,7 +104,7 @@ def test_debug_gather_indexing_bit_exact(pk):
 # ------------------------------------------------------------------ decode
 @pytest.mark.parametrize("D,Hq,Hkv,dtype", [
     (128, 32, 8, "bf16"), (128, 8, 8, "bf16"), (64, 16, 8, "bf16"), (64, 16, 2, "bf16"),
-    (128, 32, 2, "bf16"), (64, 8, 2, "fp32"), (128, 4, 1, "fp32")])
+    (128, 32, 2, "bf16"), (64, 8, 2, "fp32"), (128, 4, 1, "fp32"), (128, 32, 1, "bf16")])
 def test_decode_parity_edge_layouts(pk, D, Hq, Hkv, dtype):
     wl = _edge_decode_workload(D, Hq, Hkv, dtype)
     _, _, out, lse = _decode(pk, wl)
@@ -322,9 +322,10 @@ def test_prefill_full_size_sampled(pk):
                    src=src.host_view())
 
 
-@pytest.mark.parametrize("Hq,Hkv", [(32, 8), (8, 8), (16, 8), (16, 2)])
+@pytest.mark.parametrize("Hq,Hkv", [(32, 8), (8, 8), (16, 8), (16, 2), (32, 2), (32, 1)])
 def test_prefill_tensor_core_parity(pk, Hq, Hkv):
-    # group sizes 4, 1, 2, 8; ragged documents (200 tokens), question lengths 37 / 5 / 130
+    # group sizes 4, 1, 2, 8, 16, 32 (MQA at 32/1); ragged documents (200 tokens), question
+    # lengths 37 / 5 / 130
     wl = _edge_prefill_workload(128, Hq, Hkv, "bf16")
     _, pb, out, lse = _prefill(pk, wl, pk.LAZY_PREFILL_TC)
     _check_prefill(wl, pb, out, lse, lse_tol=TC_EDGE_LSE_TOL)
