@@ -20,6 +20,10 @@ Forms:
   C  ``attend_bruteforce``    pure Python loops, explicit cos/sin, exp-sum without max shift
   ``textbook_rope_attention`` standard RoPE causal attention over one sequence (positions 0..N-1)
 
+ALiBi variant ("Main contributions" item 4, generalisability: the mechanism also serves ALiBi):
+  ``attend_alibi`` / ``attend_request_alibi``  numpy fp64. Keys are cached unrotated; the
+  position enters only as the bias slope_h * (n - m) from logical positions at attention time.
+
 Conventions that the summaries leave open (half-split pairing, theta_i = base^(-2i/D),
 scale 1/sqrt(D), q head h -> kv head h // (Hq/Hkv), natural-log lse of the scaled scores) are the
 plainest readings; every one of them is pinned by a closed-form test in ``tests/``.
@@ -225,6 +229,67 @@ def textbook_rope_attention(q, k, v, q_positions, base, scale):
 # Page-word format (block id, offset, valid count in one 64-bit word)
 # ----------------------------------------------------------------------------------------------
 BLOCK_BITS, OFFSET_BITS, NVALID_BITS = 32, 26, 6
+
+
+def attend_alibi(k, v, key_pos, key_causal, q, q_pos, slopes, *, scale):
+    """ALiBi attention by its plain definition, fp64 (pages' "Main contributions" item 4).
+
+    k, v [n, D] (unrotated keys); key_pos [n] logical positions; key_causal [n] (a causal key is
+    visible only to queries at position >= its own; others are always visible); q [nq, G, D];
+    q_pos [nq]; slopes [G], the query heads' slopes. For query m and key n:
+        score = scale * q.k + slope * (n - m)
+    softmax over the visible keys. Returns out [nq, G, D] and lse [nq, G] (natural log of the sum
+    of exp(score)); a query with no visible key gets out 0 and lse -inf."""
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    pos = np.asarray(key_pos, np.int64)
+    caus = np.asarray(key_causal).astype(bool)
+    q = np.asarray(q, np.float64)
+    slopes = np.asarray(slopes, np.float64)
+    nq, G, D = q.shape
+    out = np.zeros((nq, G, D))
+    lse = np.full((nq, G), -np.inf)
+    for i in range(nq):
+        m = int(q_pos[i])
+        vis = ~caus | (pos <= m)
+        if not vis.any():
+            continue
+        kv, vv, dn = k[vis], v[vis], (pos[vis] - m).astype(np.float64)
+        for g in range(G):
+            s = scale * (kv @ q[i, g]) + slopes[g] * dn
+            mx = s.max()
+            w = np.exp(s - mx)
+            l = w.sum()
+            out[i, g] = (w @ vv) / l
+            lse[i, g] = mx + math.log(l)
+    return out, lse
+
+
+def attend_request_alibi(wl, b, slopes, kv_heads: Optional[Sequence[int]] = None,
+                         queries: Optional[Sequence[int]] = None, src=None):
+    """ALiBi oracle for request b of a workload (same key layout as ``attend_request``: documents
+    at their offsets, then the question / private segment), slopes [Hq]. Returns (out, lse) with
+    NaN outside the requested heads / queries."""
+    src = src or wl
+    r = wl.requests[b]
+    Hq, Hkv, D = wl.Hq, wl.Hkv, wl.D
+    G = Hq // Hkv
+    k_raw, v, off, loc, caus = request_keys(wl, b, src)
+    qa = np.asarray(src.q(b))
+    n_q = qa.shape[0]
+    q_pos = (r.q_pos0 + np.arange(n_q)) if r.mode == "prefill" else np.array([r.m])
+    qi = np.arange(n_q) if queries is None else np.asarray(list(queries))
+    heads = range(Hkv) if kv_heads is None else kv_heads
+    out = np.full((n_q, Hq, D), np.nan)
+    lse = np.full((n_q, Hq), np.nan)
+    sl = np.asarray(slopes, np.float64)
+    for h in heads:
+        o, l = attend_alibi(k_raw[:, h, :], v[:, h, :], off + loc, caus,
+                            qa[qi][:, h * G:(h + 1) * G, :], q_pos[qi], sl[h * G:(h + 1) * G],
+                            scale=wl.sm_scale)
+        out[qi, h * G:(h + 1) * G, :] = o
+        lse[qi, h * G:(h + 1) * G] = l
+    return out, lse
 
 
 def pack_page(block_id: int, offset: int, n_valid: int) -> int:

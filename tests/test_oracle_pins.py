@@ -262,3 +262,92 @@ def test_tiny_fp32_golden_regression():
     out, lse = oracle.attend_request(W.tiny_fp32(), 0)
     assert np.allclose(out, np.array(g["out"]), atol=1e-13)
     assert np.allclose(lse, np.array(g["lse"]), atol=1e-13)
+
+
+# ---------------------------------------------------------------- ALiBi variant
+# "Main contributions" item 4 (generalisability): the mechanism also serves ALiBi. Keys are
+# cached unrotated and the position enters as slope * (n - m).
+def test_alibi_slopes_standard_sequence():
+    # 8 heads: 1/2, 1/4, ..., 1/256 (ratio 2^(-8/H) between consecutive heads)
+    assert np.allclose(W.alibi_slopes(8), [2.0 ** -(h + 1) for h in range(8)], rtol=0, atol=0)
+    s32 = W.alibi_slopes(32).astype(np.float64)
+    assert np.allclose(s32[1:] / s32[:-1], 2.0 ** (-8.0 / 32), rtol=1e-6)
+
+
+@pytest.mark.parametrize("slope,N", [(0.5, 5), (0.03125, 300), (2.0 ** -8, 1000)])
+def test_alibi_q_zero_truncated_geometric_closed_form(slope, N):
+    # q = 0: weights are exp(-slope * d) for d = m - n = 0..N-1 (causal keys at m-N+1..m).
+    # lse = log((1 - e^{-sN}) / (1 - e^{-s})); with v = d the output is the truncated geometric
+    # mean e^{-s}/(1-e^{-s}) - N e^{-sN}/(1-e^{-sN}).
+    m = 10_000
+    pos = np.arange(m - N + 1, m + 1)
+    d = (m - pos).astype(np.float64)
+    k = np.random.default_rng(0).standard_normal((N, 4))
+    v = np.repeat(d[:, None], 4, axis=1)
+    out, lse = oracle.attend_alibi(k, v, pos, np.ones(N), np.zeros((1, 1, 4)), [m], [slope],
+                                   scale=0.5)
+    e1, eN = math.exp(-slope), math.exp(-slope * N)
+    assert lse[0, 0] == pytest.approx(math.log((1 - eN) / (1 - e1)), abs=1e-12)
+    assert out[0, 0, 0] == pytest.approx(e1 / (1 - e1) - N * eN / (1 - eN), rel=1e-10)
+
+
+def test_alibi_matches_library_sdpa_with_additive_bias():
+    # torch's scaled_dot_product_attention with the bias as an additive float mask (fp64, CPU),
+    # and scipy's logsumexp for lse; includes hidden (causal) keys and several slopes
+    torch = pytest.importorskip("torch")
+    sp = pytest.importorskip("scipy.special")
+    rng = np.random.default_rng(3)
+    n, D, G = 23, 8, 3
+    k = rng.standard_normal((n, D))
+    v = rng.standard_normal((n, D))
+    pos = np.concatenate([np.arange(100, 110), 200 + np.arange(13)])
+    caus = np.concatenate([np.zeros(10), np.ones(13)])
+    q = rng.standard_normal((4, G, D))
+    q_pos = np.array([200, 203, 207, 212])
+    slopes = np.array([0.5, 0.0625, 0.0])
+    scale = 1 / math.sqrt(D)
+    out, lse = oracle.attend_alibi(k, v, pos, caus, q, q_pos, slopes, scale=scale)
+    for i in range(4):
+        vis = (caus == 0) | (pos <= q_pos[i])
+        for g in range(G):
+            bias = np.where(vis, slopes[g] * (pos - q_pos[i]), -np.inf)
+            ref = torch.nn.functional.scaled_dot_product_attention(
+                torch.from_numpy(q[i, g][None, None, None, :]),
+                torch.from_numpy(k[None, None]), torch.from_numpy(v[None, None]),
+                attn_mask=torch.from_numpy(bias[None, None, None, :]), scale=scale)
+            assert np.allclose(out[i, g], ref.numpy()[0, 0, 0], atol=1e-12)
+            assert lse[i, g] == pytest.approx(sp.logsumexp(scale * (k @ q[i, g]) + bias),
+                                              abs=1e-12)
+
+
+@pytest.mark.parametrize("c", [1, 4321, 10 ** 6])
+def test_alibi_shift_invariance(c):
+    # only n - m enters: shifting every key and query position by c changes nothing
+    rng = np.random.default_rng(4)
+    k, v = rng.standard_normal((40, 16)), rng.standard_normal((40, 16))
+    pos = np.concatenate([np.arange(0, 20), 50 + np.arange(20)])
+    caus = np.concatenate([np.zeros(20), np.ones(20)])
+    q = rng.standard_normal((3, 2, 16))
+    qp = np.array([55, 60, 69])
+    a = oracle.attend_alibi(k, v, pos, caus, q, qp, [0.25, 0.01], scale=0.25)
+    b = oracle.attend_alibi(k, v, pos + c, caus, q, qp + c, [0.25, 0.01], scale=0.25)
+    assert np.allclose(a[0], b[0], atol=1e-12) and np.allclose(a[1], b[1], atol=1e-12)
+
+
+def test_alibi_request_uses_logical_positions_of_segments():
+    # the request-level oracle places document keys at offset + local index: equal to calling
+    # attend_alibi on the explicitly concatenated keys
+    wl = W.custom("decode", [[(0, 0), (1, 300)]], doc_len=20, n_pool=2, Hq=4, Hkv=2, D=8,
+                  dtype="fp32", base=1e4, priv=[(500, 3)], seed=7)
+    slopes = W.alibi_slopes(4)
+    out, lse = oracle.attend_request_alibi(wl, 0, slopes)
+    r = wl.requests[0]
+    G = 2
+    for h in range(2):
+        k = np.concatenate([wl.doc_k(0)[:, h], wl.doc_k(1)[:, h], wl.new_k(0)[:, h]])
+        v = np.concatenate([wl.doc_v(0)[:, h], wl.doc_v(1)[:, h], wl.new_v(0)[:, h]])
+        pos = np.concatenate([np.arange(20), 300 + np.arange(20), 500 + np.arange(3)])
+        o, l = oracle.attend_alibi(k, v, pos, np.zeros(43), wl.q(0)[:, h * G:(h + 1) * G],
+                                   [r.m], slopes[h * G:(h + 1) * G], scale=wl.sm_scale)
+        assert np.allclose(out[0, h * G:(h + 1) * G], o[0], atol=1e-13)
+        assert np.allclose(lse[0, h * G:(h + 1) * G], l[0], atol=1e-13)

@@ -73,6 +73,16 @@ def normal(seed: int, kind: int, index: int, shape, dtype: str) -> np.ndarray:
     return bf16_round(a) if dtype == "bf16" else a
 
 
+def alibi_slopes(n_heads: int) -> np.ndarray:
+    """ALiBi head slopes, an input of the ALiBi variant (a model parameter, not part of the
+    method): the standard geometric sequence 2^(-8 (h + 1) / H) for h = 0 .. H-1, for H a power
+    of two. Returned as float32, the precision both sides receive."""
+    if n_heads < 1 or n_heads & (n_heads - 1):
+        raise ValueError("ALiBi slopes here are defined for a power-of-two head count")
+    h = np.arange(1, n_heads + 1, dtype=np.float64)
+    return np.power(2.0, -8.0 * h / n_heads).astype(np.float32)
+
+
 def _torch_seed(seed: int, kind: int, index: int) -> int:
     h = hashlib.blake2b(f"{seed}:{kind}:{index}".encode(), digest_size=8).digest()
     return int.from_bytes(h, "little") & ((1 << 63) - 1)
