@@ -101,6 +101,32 @@ int lazy_pool_destroy(lazy_pool *pool);
  * expires the kernel sets LAZY_DEVERR_TIMEOUT, drains its own copies and returns. */
 int lazy_pool_set_wait_limit(lazy_pool *pool, uint64_t ns);
 
+/*
+ * Position encodings. The summaries state that the mechanism is not tied to RoPE and also
+ * serves ALiBi ("Main contributions" item 4, generalisability). A pool is in one mode for its
+ * whole life:
+ *   LAZY_POS_ROPE   (default) as described above.
+ *   LAZY_POS_ALIBI  K is cached as given (no rotation at all), and every score gets the bias
+ *                   slope[qh] * (n - m), with n the key's and m the query's logical position:
+ *                       s = sm_scale * q . k + slope[qh] * (n - m).
+ *                   A page word's offset field then holds the logical position of the page's
+ *                   FIRST token (segment offset + page_size * page index within the segment),
+ *                   so key slot j of the page sits at n = offset + j. Decode and prefill rotate
+ *                   nothing.
+ */
+enum { LAZY_POS_ROPE = 0, LAZY_POS_ALIBI = 1 };
+/*
+ * Switch a fresh pool to LAZY_POS_ALIBI with per-query-head slopes:
+ *   h_slopes      host float [num_q_heads], copied (finite, 0 <= slope <= 64)
+ *   num_q_heads   must be a multiple of num_kv_heads, and every later decode / prefill call on
+ *                 the pool must pass the same num_q_heads (else LAZY_ERR_INVALID_ARG).
+ * Only before the pool's first device use (insert, write, attention); LAZY_ERR_INVALID_ARG
+ * afterwards, with nothing changed.
+ */
+int lazy_pool_set_alibi(lazy_pool *pool, const float *h_slopes, int32_t num_q_heads);
+/* The pool's mode (LAZY_POS_*) and, in ALiBi mode, its number of query heads (else 0). */
+int lazy_pool_position_mode(lazy_pool *pool, int32_t *mode, int32_t *num_q_heads);
+
 /* Block allocator (host-side free list with reference counts; thread-safe).
  * kv_pool_alloc pops n blocks (refcount 1) into block_ids; LAZY_ERR_OUT_OF_BLOCKS leaves the
  * pool unchanged. retain adds a reference (a second request sharing a cached document);

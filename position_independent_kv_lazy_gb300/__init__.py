@@ -27,6 +27,8 @@ LAZY_ERR_BAD_PAGE = -5
 LAZY_ERR_TIMEOUT = -6
 LAZY_ERR_SCRATCH_LIMIT = -7
 LAZY_NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
+LAZY_POS_ROPE = 0
+LAZY_POS_ALIBI = 1
 LAZY_DTYPE_BF16 = 0
 LAZY_DTYPE_FP32 = 1
 LAZY_DEVERR_BAD_PAGE = 1
@@ -44,6 +46,7 @@ EXPORTS = [
     "lazy_decode_workspace_bytes", "lazy_attn_decode", "lazy_prefill_workspace_bytes",
     "lazy_attn_prefill", "lazy_get_device_error", "lazy_debug_gather", "lazy_debug_wait_timeout",
     "lazy_attn_decode_noalloc", "lazy_debug_exp2", "lazy_attn_prefill_append",
+    "lazy_pool_set_alibi", "lazy_pool_position_mode",
 ]
 
 
@@ -78,6 +81,8 @@ _SIGS = {
                           ctypes.c_double], ctypes.c_int),
     "lazy_pool_destroy": ([_vp], ctypes.c_int),
     "lazy_pool_set_wait_limit": ([_vp, _u64], ctypes.c_int),
+    "lazy_pool_set_alibi": ([_vp, ctypes.POINTER(ctypes.c_float), _i32], ctypes.c_int),
+    "lazy_pool_position_mode": ([_vp, _pi32, _pi32], ctypes.c_int),
     "kv_pool_alloc": ([_vp, _i32, _pi32], ctypes.c_int),
     "kv_pool_retain": ([_vp, _pi32, _i32], ctypes.c_int),
     "kv_pool_release": ([_vp, _pi32, _i32], ctypes.c_int),
@@ -156,7 +161,9 @@ class LazyPool:
     """A paged KV pool: page buffers [num_blocks][Hkv][16][D] allocated with torch on `device`."""
 
     def __init__(self, num_blocks: int, num_kv_heads: int, head_dim: int, dtype, rope_base: float,
-                 page_size: int = 16, device="cuda"):
+                 page_size: int = 16, device="cuda", alibi_slopes=None):
+        """alibi_slopes (per query head) switches the pool to ALiBi mode: K cached unrotated, a
+        bias slope * (n - m) at attention time, page words carrying page start positions."""
         import torch
         lib = load_library()
         self.num_blocks, self.hkv, self.d, self.page_size = num_blocks, num_kv_heads, head_dim, page_size
@@ -170,6 +177,12 @@ class LazyPool:
             ctypes.byref(h), self.k_pages.data_ptr(), self.v_pages.data_ptr(), num_blocks,
             page_size, num_kv_heads, head_dim, _dtype_code(dtype), float(rope_base)))
         self.handle = h
+        self.alibi_slopes = None
+        if alibi_slopes is not None:
+            sl = [float(x) for x in alibi_slopes]
+            arr = (ctypes.c_float * len(sl))(*sl)
+            _check("lazy_pool_set_alibi", lib.lazy_pool_set_alibi(h, arr, len(sl)))
+            self.alibi_slopes = sl
 
     def close(self):
         if getattr(self, "handle", None):
@@ -265,8 +278,11 @@ def lazy_pack_pages(block_ids, offsets, n_valid) -> np.ndarray:
 
 
 def build_page_table(requests: Sequence[Sequence[Tuple[Sequence[int], int, int]]],
-                     page_size: int = 16) -> Tuple[np.ndarray, np.ndarray]:
+                     page_size: int = 16, page_positions: bool = False
+                     ) -> Tuple[np.ndarray, np.ndarray]:
     """Page table of a batch: ``requests[b]`` lists segments (block_ids, logical offset, length).
+    The word's offset field is the segment's offset (RoPE pools) or, with ``page_positions``
+    (ALiBi pools), the logical position of each page's first token.
     Returns (words uint64 [total pages], cu_pages int32 [B+1])."""
     blk, off, nv, cu = [], [], [], [0]
     for segs in requests:
@@ -276,7 +292,7 @@ def build_page_table(requests: Sequence[Sequence[Tuple[Sequence[int], int, int]]
                 raise ValueError("segment has fewer blocks than pages")
             for i in range(n_pages):
                 blk.append(ids[i])
-                off.append(o)
+                off.append(o + i * page_size if page_positions else o)
                 nv.append(min(page_size, length - i * page_size))
         cu.append(len(blk))
     return lazy_pack_pages(blk, off, nv), np.asarray(cu, dtype=np.int32)

@@ -41,6 +41,7 @@ struct DecodeParams {
   int32_t chunks;  // query-head chunks per kv head
   float scale_log2;
   uint64_t wait_ns;
+  const float *slopes;  // ALiBi pools: per query head; nullptr for RoPE pools
 };
 
 // Walks the flattened (request, virtual head, page) sequence.
@@ -188,6 +189,8 @@ __global__ void __launch_bounds__(WARPS * 32) decode_split_kernel(const DecodePa
   float2 qr[GC][EP2];    // rotated query slice, pre-scaled by sm_scale * log2(e)
   float2 acc[GC][EP2];   // unnormalised output slice
   float m_run[GC], lsum[GC];
+  float sl2[GC];         // ALiBi: the unit's query-head slopes, times log2(e)
+  const bool alibi = p.slopes != nullptr;
   int32_t cur_unit = -1, cur_b = 0;
   uint32_t cur_off = 0xFFFFFFFFu;
   int32_t m_pos = 0;
@@ -253,6 +256,7 @@ __global__ void __launch_bounds__(WARPS * 32) decode_split_kernel(const DecodePa
       __syncwarp();
 #pragma unroll
       for (int g = 0; g < GC; ++g) {
+        sl2[g] = alibi ? p.slopes[hv * GC + g] * 1.4426950408889634f : 0.f;
         m_run[g] = -INFINITY;
         lsum[g] = 0.f;
 #pragma unroll
@@ -263,11 +267,13 @@ __global__ void __launch_bounds__(WARPS * 32) decode_split_kernel(const DecodePa
     const uint32_t nv = word_nvalid(word);
     const bool bad = word_block(word) >= (uint32_t)p.num_blocks || nv > (uint32_t)kPage;
     const uint32_t off = word_offset(word);
+    // ALiBi pools rotate nothing: q is only scaled, once per unit (delta 0 is the identity).
+    const uint32_t rot_off = alibi ? 0u : off;
     if (!bad) {
-      if (off != cur_off) {
+      if (rot_off != cur_off) {
         // q <- R(m - o) q: the one rotation per document boundary.
-        cur_off = off;
-        const int64_t delta = (int64_t)m_pos - (int64_t)off;
+        cur_off = rot_off;
+        const int64_t delta = alibi ? 0 : (int64_t)m_pos - (int64_t)off;
 #pragma unroll
         for (int e = 0; e < EPL; ++e) {
           const int d = r * EPL + e;
@@ -304,6 +310,19 @@ __global__ void __launch_bounds__(WARPS * 32) decode_split_kernel(const DecodePa
       reduce_scatter<NV0, LPR / 2>(part, lane, base);
       // part[0..NF) hold full (log2-domain) scores of flat indices base .. base+NF-1,
       // index = it * GC + g  ->  key it * KPI + gq, head g.
+      if (alibi) {
+        // bias slope * (n - m); the word's offset is the page's first position, n - m exact
+#pragma unroll
+        for (int j = 0; j < NF; ++j) {
+          const int idx = base + j;
+          const int g = idx % GC;
+          float sg = 0.f;
+#pragma unroll
+          for (int gg = 0; gg < GC; ++gg)
+            if (gg == g) sg = sl2[gg];
+          part[j] = fmaf(sg, (float)((int32_t)off + (idx / GC) * KPI + gq - m_pos), part[j]);
+        }
+      }
       if (nv < (uint32_t)kPage) {
 #pragma unroll
         for (int j = 0; j < NF; ++j)
@@ -572,6 +591,7 @@ using namespace lazy;
 extern "C" int lazy_decode_workspace_bytes(lazy_pool *p, int32_t batch, int32_t num_q_heads,
                                            int32_t grid_ctas, size_t *bytes) {
   if (!p || !bytes || batch < 0 || grid_ctas < 0) return LAZY_ERR_INVALID_ARG;
+  if (p->alibi && num_q_heads != (int32_t)p->slopes.size()) return LAZY_ERR_INVALID_ARG;
   int32_t gc, chunks;
   int rc = plan_groups(num_q_heads, p->hkv, &gc, &chunks);
   if (rc != LAZY_OK) return rc;
@@ -596,6 +616,7 @@ extern "C" int lazy_attn_decode(lazy_pool *p, const void *q, const int32_t *q_po
   if (((uintptr_t)q & 15) || ((uintptr_t)out & 15) || ((uintptr_t)workspace & 15) ||
       ((uintptr_t)words & 7))
     return LAZY_ERR_INVALID_ARG;
+  if (p->alibi && num_q_heads != (int32_t)p->slopes.size()) return LAZY_ERR_INVALID_ARG;
   int32_t gc, chunks;
   int rc = plan_groups(num_q_heads, p->hkv, &gc, &chunks);
   if (rc != LAZY_OK) return rc;
@@ -627,6 +648,7 @@ extern "C" int lazy_attn_decode(lazy_pool *p, const void *q, const int32_t *q_po
   dp.chunks = chunks;
   dp.scale_log2 = sm_scale * 1.4426950408889634f;
   dp.wait_ns = p->wait_limit_ns;
+  dp.slopes = p->alibi ? p->d_slopes : nullptr;
   CombineParams cp;
   cp.ws_o = dp.ws_o;
   cp.ws_lse = dp.ws_lse;
@@ -699,6 +721,7 @@ extern "C" int lazy_attn_decode_noalloc(lazy_pool *p, const void *q, const int32
     record_msg("the current device is not the pool's device");
     return LAZY_ERR_INVALID_ARG;
   }
+  if (p->alibi && num_q_heads != (int32_t)p->slopes.size()) return LAZY_ERR_INVALID_ARG;
   int32_t gc, chunks;
   int rc = plan_groups(num_q_heads, p->hkv, &gc, &chunks);
   if (rc != LAZY_OK) return rc;
@@ -734,6 +757,7 @@ extern "C" int lazy_attn_decode_noalloc(lazy_pool *p, const void *q, const int32
   dp.chunks = chunks;
   dp.scale_log2 = sm_scale * 1.4426950408889634f;
   dp.wait_ns = p->wait_limit_ns;
+  dp.slopes = p->alibi ? p->d_slopes : nullptr;
   CombineParams cp;
   cp.ws_o = dp.ws_o;
   cp.ws_lse = dp.ws_lse;

@@ -27,7 +27,7 @@ __global__ void __launch_bounds__(256) encode_kernel(
     const T *__restrict__ k_raw, const T *__restrict__ v, int32_t n_tokens, int32_t hkv,
     T *__restrict__ k_pool, T *__restrict__ v_pool, const uint64_t *__restrict__ turn,
     int32_t tok0, int32_t local_pos0, BlockList blocks, const int32_t *__restrict__ slot_map,
-    const int32_t *__restrict__ local_pos, int32_t num_blocks, int32_t *err) {
+    const int32_t *__restrict__ local_pos, int32_t num_blocks, int32_t *err, int32_t rope) {
   constexpr int EPL = 16 / (int)sizeof(T);
   constexpr int CH = (D / 2) / EPL;
   // A decode launched right after this append may start its launch early; it waits for this
@@ -61,13 +61,15 @@ __global__ void __launch_bounds__(256) encode_kernel(
     float lo[EPL], hi[EPL];
     unpack16<T>(*reinterpret_cast<const uint4 *>(k_raw + src + c * EPL), lo);
     unpack16<T>(*reinterpret_cast<const uint4 *>(k_raw + src + D / 2 + c * EPL), hi);
+    if (rope) {  // ALiBi pools keep K as given
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) {
-      float cs, sn;
-      rope_cos_sin((int64_t)j, turn[c * EPL + e], cs, sn);
-      const float x = lo[e], y = hi[e];
-      lo[e] = x * cs - y * sn;
-      hi[e] = x * sn + y * cs;
+      for (int e = 0; e < EPL; ++e) {
+        float cs, sn;
+        rope_cos_sin((int64_t)j, turn[c * EPL + e], cs, sn);
+        const float x = lo[e], y = hi[e];
+        lo[e] = x * cs - y * sn;
+        hi[e] = x * sn + y * cs;
+      }
     }
     *reinterpret_cast<uint4 *>(k_pool + dst + c * EPL) = pack16<T>(lo);
     *reinterpret_cast<uint4 *>(k_pool + dst + D / 2 + c * EPL) = pack16<T>(hi);
@@ -89,7 +91,7 @@ int launch_encode(lazy_pool *p, const void *k_raw, const void *v, int32_t n_toke
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)p->num_sms * 16));
   encode_kernel<T, D><<<grid, threads, 0, s>>>(
       (const T *)k_raw, (const T *)v, n_tokens, p->hkv, (T *)p->k, (T *)p->v, p->d_turn, tok0,
-      local_pos0, bl, slot_map, local_pos, p->num_blocks, p->d_err);
+      local_pos0, bl, slot_map, local_pos, p->num_blocks, p->d_err, p->alibi ? 0 : 1);
   LAZY_CUDA_TRY(cudaGetLastError());
   return LAZY_OK;
 }
@@ -195,6 +197,7 @@ extern "C" int kv_pool_insert_doc(lazy_pool *p, const void *k_raw, const void *v
   if (n_tokens > 0 && (!k_raw || !v || !block_ids)) return LAZY_ERR_INVALID_ARG;
   if (((uintptr_t)k_raw & 15) || ((uintptr_t)v & 15)) return LAZY_ERR_INVALID_ARG;
   if (n_tokens == 0) return LAZY_OK;
+  p->encoded = true;
   const int64_t end = (int64_t)local_pos0 + n_tokens;
   if (end > (1ll << 26)) return LAZY_ERR_INVALID_ARG;
   const int32_t need = (int32_t)((end + kPage - 1) / kPage);
@@ -234,6 +237,7 @@ extern "C" int kv_pool_write_tokens(lazy_pool *p, const void *k_raw, const void 
   if (((uintptr_t)k_raw & 15) || ((uintptr_t)v & 15)) return LAZY_ERR_INVALID_ARG;
   int rc = ensure_device(p);
   if (rc != LAZY_OK) return rc;
+  p->encoded = true;
   BlockList bl;
   bl.first_page = 0;
   bl.n = 0;

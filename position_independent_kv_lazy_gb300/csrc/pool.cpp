@@ -37,6 +37,11 @@ int ensure_device(lazy_pool *p) {
   LAZY_CUDA_TRY(cudaMemcpy(p->d_turn, p->turn.data(), sizeof(uint64_t) * p->turn.size(),
                            cudaMemcpyHostToDevice));
   LAZY_CUDA_TRY(cudaMemset(p->d_err, 0, 256));
+  if (p->alibi) {
+    LAZY_CUDA_TRY(cudaMalloc((void **)&p->d_slopes, sizeof(float) * p->slopes.size()));
+    LAZY_CUDA_TRY(cudaMemcpy(p->d_slopes, p->slopes.data(), sizeof(float) * p->slopes.size(),
+                             cudaMemcpyHostToDevice));
+  }
   LAZY_CUDA_TRY(cudaMemset(p->k, 0, pool_bytes(p)));
   LAZY_CUDA_TRY(cudaMemset(p->v, 0, pool_bytes(p)));
   LAZY_CUDA_TRY(cudaDeviceSynchronize());
@@ -100,8 +105,30 @@ int lazy_pool_destroy(lazy_pool *p) {
   if (p->dev_ready) {
     cudaFree(p->d_err);
     cudaFree(p->d_turn);
+    if (p->d_slopes) cudaFree(p->d_slopes);
   }
   delete p;
+  return LAZY_OK;
+}
+
+int lazy_pool_set_alibi(lazy_pool *p, const float *slopes, int32_t num_q_heads) {
+  if (!p || !slopes || num_q_heads <= 0 || num_q_heads % p->hkv) return LAZY_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> g(p->mu);
+  if (p->encoded || p->dev_ready) {
+    lazy::record_msg("lazy_pool_set_alibi: the pool has already been used");
+    return LAZY_ERR_INVALID_ARG;
+  }
+  for (int32_t h = 0; h < num_q_heads; ++h)
+    if (!(slopes[h] >= 0.f) || slopes[h] > 64.f) return LAZY_ERR_INVALID_ARG;  // finite, >= 0
+  p->slopes.assign(slopes, slopes + num_q_heads);
+  p->alibi = true;
+  return LAZY_OK;
+}
+
+int lazy_pool_position_mode(lazy_pool *p, int32_t *mode, int32_t *num_q_heads) {
+  if (!p || !mode) return LAZY_ERR_INVALID_ARG;
+  *mode = p->alibi ? LAZY_POS_ALIBI : LAZY_POS_ROPE;
+  if (num_q_heads) *num_q_heads = (int32_t)p->slopes.size();
   return LAZY_OK;
 }
 

@@ -27,6 +27,13 @@ struct lazy_pool {
   uint64_t *d_turn = nullptr;       // device copy of `turn`
   uint64_t wait_limit_ns = 2000000000ull;
 
+  // ALiBi mode (lazy_pool_set_alibi): K is stored unrotated and attention adds
+  // slope[head] * (n - m); page-word offsets are page start positions.
+  bool alibi = false;
+  bool encoded = false;             // something was written: the mode can no longer change
+  std::vector<float> slopes;        // per query head
+  float *d_slopes = nullptr;
+
   // Tensor maps of the page buffers for the tensor-core prefill (built lazily).
   bool tmaps_ready = false;
   alignas(64) unsigned char tmap_k[128];   // 2-D view: 16-row page boxes

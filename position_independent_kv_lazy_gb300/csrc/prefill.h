@@ -25,6 +25,7 @@ struct PrefillParams {
   int32_t batch, hkv, hq, num_blocks, G, TQ, total_q;
   float scale_log2;
   uint64_t wait_ns;
+  const float *slopes;  // ALiBi pools: per query head (device); nullptr for RoPE pools
 };
 
 int prefill_simt(lazy_pool *p, const PrefillParams &pp, int32_t max_q_len, cudaStream_t s);

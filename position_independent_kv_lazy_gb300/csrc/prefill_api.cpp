@@ -25,6 +25,7 @@ extern "C" int lazy_attn_prefill(lazy_pool *p, const void *q, const void *k_new,
   if (!p || batch < 0 || total_q < 0 || max_q_len < 0 || !(sm_scale > 0.f))
     return LAZY_ERR_INVALID_ARG;
   if (num_q_heads <= 0 || num_q_heads % p->hkv) return LAZY_ERR_INVALID_ARG;
+  if (p->alibi && num_q_heads != (int32_t)p->slopes.size()) return LAZY_ERR_INVALID_ARG;
   if (flags < LAZY_PREFILL_AUTO || flags > LAZY_PREFILL_TC) return LAZY_ERR_INVALID_ARG;
   if (batch == 0 || total_q == 0 || max_q_len == 0) return LAZY_OK;
   if (!q || !cu_q || !q_pos0 || !cu_pages || !out || !lse) return LAZY_ERR_INVALID_ARG;
@@ -57,6 +58,7 @@ extern "C" int lazy_attn_prefill(lazy_pool *p, const void *q, const void *k_new,
   pp.total_q = total_q;
   pp.scale_log2 = sm_scale * 1.4426950408889634f;
   pp.wait_ns = p->wait_limit_ns;
+  pp.slopes = p->alibi ? p->d_slopes : nullptr;
   cudaStream_t s = (cudaStream_t)stream;
   const bool tc_ok = prefill_tc_supported(p, num_q_heads) == LAZY_OK;
   if (flags == LAZY_PREFILL_TC) {

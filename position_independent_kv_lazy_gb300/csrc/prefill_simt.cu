@@ -27,7 +27,8 @@ struct SimtSmem {
   static constexpr int kV = kK + kPage * (D + 1) * 4;   // float [kPage][D]
   static constexpr int kP = kV + kPage * D * 4;         // float [kRows][kPage+1]
   static constexpr int kKt = kP + kRows * (kPage + 1) * 4;  // int32 [kPage] key token (-1 = doc)
-  static constexpr int kBytes = kKt + kPage * 4;
+  static constexpr int kKp = kKt + kPage * 4;               // int32 [kPage] key logical position
+  static constexpr int kBytes = kKp + kPage * 4;
 };
 
 template <typename T, int D>
@@ -39,6 +40,9 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(const PrefillPar
   float *Vs = reinterpret_cast<float *>(smem_raw + S::kV);
   float *Ps = reinterpret_cast<float *>(smem_raw + S::kP);
   int32_t *Kt = reinterpret_cast<int32_t *>(smem_raw + S::kKt);
+  int32_t *Kp = reinterpret_cast<int32_t *>(smem_raw + S::kKp);
+  // ALiBi pools: no rotation anywhere; scores get slope * (n - m) instead
+  const bool alibi = p.slopes != nullptr;
 
   const int b = blockIdx.z, h = blockIdx.y;
   const int G = p.G, TQ = p.TQ;
@@ -59,8 +63,8 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(const PrefillPar
     if (row < nrows) {
       const int t = t0 + row / G, qh = h * G + row % G;
       const T *src = q + ((size_t)(qbeg + t) * p.hq + qh) * D;
-      float cs, sn;
-      rope_cos_sin((int64_t)(t - t0), p.turn[i], cs, sn);
+      float cs = 1.f, sn = 0.f;
+      if (!alibi) rope_cos_sin((int64_t)(t - t0), p.turn[i], cs, sn);
       const float a = Elem<T>::to_f(src[i]), c = Elem<T>::to_f(src[i + D / 2]);
       x = (a * cs - c * sn) * p.scale_log2;
       y = (a * sn + c * cs) * p.scale_log2;
@@ -71,6 +75,8 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(const PrefillPar
 
   const int row = tid >> 1, half = tid & 1;
   const int t_row = t0 + row / G;
+  const int32_t m_row = p.q_pos0[b] + t_row;  // the row's logical position (ALiBi bias)
+  const float slope2 = alibi ? p.slopes[h * G + row % G] * 1.4426950408889634f : 0.f;
   float acc[D / 2];
 #pragma unroll
   for (int d = 0; d < D / 2; ++d) acc[d] = 0.f;
@@ -100,8 +106,8 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(const PrefillPar
         const size_t page = ((size_t)blk * p.hkv + h) * (size_t)(kPage * D);
         for (int idx = tid; idx < kPage * (D / 2); idx += kThreads) {
           const int k = idx / (D / 2), i = idx % (D / 2);
-          float cs, sn;
-          rope_cos_sin(delta, p.turn[i], cs, sn);
+          float cs = 1.f, sn = 0.f;
+          if (!alibi) rope_cos_sin(delta, p.turn[i], cs, sn);
           const float a = Elem<T>::to_f(kpool[page + k * D + i]);
           const float c = Elem<T>::to_f(kpool[page + k * D + i + D / 2]);
           Ks[k * (D + 1) + i] = a * cs - c * sn;
@@ -109,7 +115,10 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(const PrefillPar
           Vs[k * D + i] = Elem<T>::to_f(vpool[page + k * D + i]);
           Vs[k * D + i + D / 2] = Elem<T>::to_f(vpool[page + k * D + i + D / 2]);
         }
-        if (tid < kPage) Kt[tid] = -1;
+        if (tid < kPage) {
+          Kt[tid] = -1;
+          Kp[tid] = (int32_t)word_offset(w) + tid;  // ALiBi: the word holds the page start
+        }
       }
     } else {
       const int c0 = (tile - npg) * kPage;
@@ -123,14 +132,17 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(const PrefillPar
           c = Elem<T>::to_f(knew[src + i + D / 2]);
           va = Elem<T>::to_f(vnew[src + i]);
           vc = Elem<T>::to_f(vnew[src + i + D / 2]);
-          rope_cos_sin((int64_t)(kt - t0), p.turn[i], cs, sn);
+          if (!alibi) rope_cos_sin((int64_t)(kt - t0), p.turn[i], cs, sn);
         }
         Ks[k * (D + 1) + i] = a * cs - c * sn;
         Ks[k * (D + 1) + i + D / 2] = a * sn + c * cs;
         Vs[k * D + i] = va;
         Vs[k * D + i + D / 2] = vc;
       }
-      if (tid < kPage) Kt[tid] = (c0 + tid < Tb) ? c0 + tid : 0x7FFFFFFF;
+      if (tid < kPage) {
+        Kt[tid] = (c0 + tid < Tb) ? c0 + tid : 0x7FFFFFFF;
+        Kp[tid] = p.q_pos0[b] + c0 + tid;
+      }
     }
     __syncthreads();
     if (skip) continue;
@@ -150,6 +162,7 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(const PrefillPar
       const int k = half * 8 + kk;
       bool vis = k < nvalid;
       if (!doc) vis = Kt[k] <= t_row;
+      if (alibi) s[kk] = fmaf(slope2, (float)(Kp[k] - m_row), s[kk]);
       if (!vis) s[kk] = -INFINITY;
       mx = fmaxf(mx, s[kk]);
     }

@@ -59,7 +59,7 @@ constexpr int kOffV = kOffK + kNK * kTileBytes;        // kNV V stages
 constexpr int kNM = 4;  // softmax metadata ring (see SMeta)
 constexpr int kOffMetaK = kOffV + kNV * kTileBytes;    // KMeta [kNK]
 constexpr int kOffMetaS = kOffMetaK + kNK * 48;        // SMeta [kNM]
-constexpr int kOffBar = kOffMetaS + kNM * 48 + 16;     // barriers (8-byte aligned)
+constexpr int kOffBar = kOffMetaS + kNM * 80 + 16;     // barriers (8-byte aligned)
 constexpr int kSmemBytes = kOffBar + 192 + 1024;       // + alignment slack
 
 // Read by the rotation group (valid until the K stage is refilled, after QK of this tile).
@@ -75,10 +75,12 @@ struct KMeta {
 struct SMeta {
   int32_t kind;
   int32_t c0;
-  int32_t full;   // document tile: every page present and full
+  int32_t full;    // document tile: every page present and full
   int32_t pad;
-  int32_t nv[8];  // document tile: valid tokens per page (0 = absent / bad)
+  int32_t nv[8];   // document tile: valid tokens per page (0 = absent / bad)
+  int32_t pos0[8]; // ALiBi: logical position of the first key of each 16-key group
 };
+static_assert(sizeof(SMeta) == 80, "SMeta layout");
 
 struct TcParams {
   CUtensorMap tm_q, tm_knew, tm_vnew, tm_k, tm_v, tm_k8, tm_v8;
@@ -93,6 +95,7 @@ struct TcParams {
   int32_t batch, hkv, hq, num_blocks, G, TQ, has_new;
   float scale_log2;
   uint64_t wait_ns;
+  const float *slopes;  // ALiBi: per query head
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -344,6 +347,9 @@ __device__ __forceinline__ bool cta_wait(uint64_t *bar, uint32_t par, volatile i
   return true;
 }
 
+// kAlibi: the pool's ALiBi mode. Nothing is rotated (the barriers keep their order) and every
+// score gets slope * (n - m) before the row max.
+template <bool kAlibi>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -367,7 +373,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   const int32_t qbeg = p.cu_q[b];
   const int32_t Tb = p.cu_q[b + 1] - qbeg;
   if (t0 >= Tb) return;
-  const int32_t m0 = p.q_pos0[b] + t0;
+  const int32_t q_pos0_b = p.q_pos0[b];
+  const int32_t m0 = q_pos0_b + t0;
   const int32_t pg0 = p.cu_pages[b], npg = p.cu_pages[b + 1] - pg0;
   const int n_doc = (npg + 7) / 8;
   const int t_end = min(t0 + 2 * TQ, Tb);
@@ -453,6 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
               }
               if (j * 8 + pp >= npg) nv = 0;  // absent page: the last one is loaded again, masked
               ms.nv[pp] = nv;
+              ms.pos0[pp] = (int32_t)word_offset(w[pp]);  // ALiBi pools: the page start
               full &= (nv == kPage);
               mk.off[pp] = (int32_t)word_offset(w[pp]);
               rows[s][pp] = (int32_t)((blk * (uint32_t)p.hkv + (uint32_t)h) * kPage);
@@ -484,6 +492,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             ms.kind = 1;
             ms.c0 = c0;
             ms.full = 0;
+#pragma unroll
+            for (int pp = 0; pp < 8; ++pp) ms.pos0[pp] = q_pos0_b + c0 + pp * kPage;
             mbar_arrive_expect_tx(&k_full[s], kTileBytes);
             for (int cb = 0; cb < 2; ++cb)
               tma3d(kd + cb * kHalfBytes, &p.tm_knew, cb * 64, h, qbeg + c0, &k_full[s]);
@@ -601,12 +611,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     const uint32_t s_col = lane_base + i * 128, o_col = lane_base + 256 + i * 128;
     const int t_row = t0 + i * TQ + row / G;
     const float sl2 = p.scale_log2;
+    const float slope2 = kAlibi ? p.slopes[h * G + row % G] * 1.4426950408889634f : 0.f;
+    const int32_t m_row = q_pos0_b + t_row;  // the row's logical position (ALiBi)
     const uint64_t *turn = p.turn;
     const int st = tid - 128;               // 0..255
     const int rc = st & 7, rrow0 = (st >> 3) * 4;  // rotation share: chunk rc, rows rrow0..+3
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = cta_wait(q_full, 0, abort, lim, p.err);
-    if (ok) {
+    if (ok && !kAlibi) {
       // this thread's own query row of Q tile i, rotated to R(m - m0)
 #pragma unroll 1
       for (int c = 0; c < 8; ++c) {
@@ -624,7 +636,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       if (!cta_wait(&k_full[s], (jj / kNK) & 1, abort, lim, p.err)) return false;
       const KMeta &mt = meta_k[s];
       uint8_t *kt = Ks + s * kTileBytes;
-      if (mt.kind == 0) {
+      if (kAlibi) {
+        // no rotation: the tile is used as loaded
+      } else if (mt.kind == 0) {
         // one relative rotation R(o - m0) per page
         const int64_t d = (int64_t)mt.off[rrow0 >> 4] - m0;
         if (d != cached) {
@@ -641,7 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           rotate_row_chunk(kt, rrow0 + rr, rc, rk);
         }
       }
-      fence_async_smem();
+      if (!kAlibi) fence_async_smem();
       mbar_arrive(&k_rot[s]);
       return true;
     };
@@ -688,6 +702,24 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         for (int e = 0; e < 128; ++e)
           if (!((vm[e >> 5] >> (e & 31)) & 1u)) r[e] = 0xFF800000u;
       }
+      if (kAlibi) {
+        // log2-domain scores with the bias: slope * (n - m), n = pos0 of the 16-key group + e
+#pragma unroll
+        for (int pg = 0; pg < 8; ++pg) {
+          const float base = slope2 * (float)(mt.pos0[pg] - m_row);
+#pragma unroll
+          for (int e = 0; e < 16; e += 2) {
+            const float2 bias = __ffma2_rn(make_float2(slope2, slope2),
+                                           make_float2((float)e, (float)(e + 1)),
+                                           make_float2(base, base));
+            const float2 t = __ffma2_rn(
+                make_float2(__uint_as_float(r[pg * 16 + e]), __uint_as_float(r[pg * 16 + e + 1])),
+                make_float2(sl2, sl2), bias);
+            r[pg * 16 + e] = __float_as_uint(t.x);
+            r[pg * 16 + e + 1] = __float_as_uint(t.y);
+          }
+        }
+      }
       // max with eight independent chains (one running max would be a 128-long chain)
       float cmk[8];
 #pragma unroll
@@ -702,7 +734,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       }
       const float cm = fmaxf(fmaxf(fmaxf(cmk[0], cmk[1]), fmaxf(cmk[2], cmk[3])),
                              fmaxf(fmaxf(cmk[4], cmk[5]), fmaxf(cmk[6], cmk[7])));
-      const float cm2 = cm * sl2;
+      const float cm2 = kAlibi ? cm : cm * sl2;
+      const float sle = kAlibi ? 1.f : sl2;  // scale still to apply in the exponent
       if (cm2 > m_use + 8.f) {  // includes the first finite max (m_use = -inf)
         alpha = (m_use == -INFINITY) ? 0.f : ex2(m_use - cm2);
         m_use = cm2;
@@ -720,7 +753,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           const int e = q4 * 32 + e2;
           float s0, s1;
           const float2 t = __ffma2_rn(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])),
-                                      make_float2(sl2, sl2), make_float2(neg_m, neg_m));
+                                      make_float2(sle, sle), make_float2(neg_m, neg_m));
           if (kPolyEvery > 0 &&
               ((e2 >> 1) % (kPolyEvery > 0 ? kPolyEvery : 1)) == kPolyEvery - 1) {
             const float2 y = exp2_poly2(t);
@@ -911,14 +944,20 @@ int prefill_tc(lazy_pool *p, const PrefillParams &pp, int32_t max_q_len, cudaStr
   tp.has_new = pp.k_new != nullptr;
   tp.scale_log2 = pp.scale_log2;
   tp.wait_ns = pp.wait_ns;
+  tp.slopes = pp.slopes;
   static bool attr = false;
   if (!attr) {
-    LAZY_CUDA_TRY(cudaFuncSetAttribute(prefill_tc_kernel,
+    LAZY_CUDA_TRY(cudaFuncSetAttribute(prefill_tc_kernel<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes));
+    LAZY_CUDA_TRY(cudaFuncSetAttribute(prefill_tc_kernel<true>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes));
     attr = true;
   }
   dim3 grid((max_q_len + 2 * TQ - 1) / (2 * TQ), pp.hkv, pp.batch);
-  prefill_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(tp);
+  if (pp.slopes)
+    prefill_tc_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(tp);
+  else
+    prefill_tc_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(tp);
   LAZY_CUDA_TRY(cudaGetLastError());
   return LAZY_OK;
 }

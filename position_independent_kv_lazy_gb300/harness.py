@@ -122,13 +122,14 @@ def chain_blocks_needed(wl, n_steps: int) -> int:
 
 
 def build_resident(wl, src, device="cuda", resident_pool: bool = True, stream=None,
-                   drop_raw: bool = True, extra_blocks: int = 0) -> Resident:
+                   drop_raw: bool = True, extra_blocks: int = 0, alibi_slopes=None) -> Resident:
     """Create the pool (sized for the whole document pool when ``resident_pool``, plus
-    ``extra_blocks`` free blocks) and encode every document some request retrieved, once, plus
-    each decode request's private segment."""
+    ``extra_blocks`` free blocks; in ALiBi mode when ``alibi_slopes`` is given) and encode every
+    document some request retrieved, once, plus each decode request's private segment."""
     import torch
     pool = LazyPool(pool_blocks_needed(wl, resident_pool) + extra_blocks, wl.Hkv, wl.D,
-                    _torch_dtype(wl), wl.rope_base, wl.page_size, device)
+                    _torch_dtype(wl), wl.rope_base, wl.page_size, device,
+                    alibi_slopes=alibi_slopes)
     doc_blocks: Dict[int, List[int]] = {}
     for d in wl.used_docs():
         k, v = src.doc_kv(d, device)
@@ -150,7 +151,7 @@ def page_table(wl, res: Resident, reqs, with_private: bool):
         if with_private:
             s.append((res.priv_blocks[r.index], r.priv_offset, r.priv_len))
         segs.append(s)
-    return build_page_table(segs, wl.page_size)
+    return build_page_table(segs, wl.page_size, page_positions=res.pool.alibi_slopes is not None)
 
 
 @dataclasses.dataclass
@@ -275,7 +276,7 @@ def chain_step_batch(wl, res: Resident, ch: Chain, step: int, src, device="cuda"
         slots.append(blk * P + j % P)
         lpos.append(j)
         qpos.append(r.q_pos0 + j)
-    words, cu = build_page_table(segs, P)
+    words, cu = build_page_table(segs, P, page_positions=res.pool.alibi_slopes is not None)
     return DecodeBatch(
         ch.pb.reqs, torch.cat(qs).contiguous(),
         torch.tensor(qpos, dtype=torch.int32, device=device),

@@ -152,3 +152,36 @@ def test_attention_argument_checks_return_before_device_use(lazylib):
                                             4, 0.1, None, None, None, 0, 0, None, None,
                                             None) == 0
     assert lazylib.lazy_pool_destroy(h) == 0
+
+
+def test_alibi_mode_switch_checks(lazylib):
+    rc, h = _raw_pool(lazylib)
+    assert rc == 0
+    mode, nq = ctypes.c_int32(-1), ctypes.c_int32(-1)
+    assert lazylib.lazy_pool_position_mode(h, ctypes.byref(mode), ctypes.byref(nq)) == 0
+    assert mode.value == pk.LAZY_POS_ROPE and nq.value == 0
+    bad = (ctypes.c_float * 4)(0.5, -0.25, 0.125, 0.0625)    # negative slope
+    assert lazylib.lazy_pool_set_alibi(h, bad, 4) == pk.LAZY_ERR_INVALID_ARG
+    nan = (ctypes.c_float * 4)(0.5, float("nan"), 0.125, 0.0625)
+    assert lazylib.lazy_pool_set_alibi(h, nan, 4) == pk.LAZY_ERR_INVALID_ARG
+    ok = (ctypes.c_float * 4)(0.5, 0.25, 0.125, 0.0625)
+    assert lazylib.lazy_pool_set_alibi(h, ok, 3) == pk.LAZY_ERR_INVALID_ARG  # not a multiple
+    assert lazylib.lazy_pool_set_alibi(h, None, 4) == pk.LAZY_ERR_INVALID_ARG
+    assert lazylib.lazy_pool_position_mode(h, ctypes.byref(mode), None) == 0
+    assert mode.value == pk.LAZY_POS_ROPE                                      # unchanged
+    assert lazylib.lazy_pool_set_alibi(h, ok, 4) == 0
+    assert lazylib.lazy_pool_position_mode(h, ctypes.byref(mode), ctypes.byref(nq)) == 0
+    assert mode.value == pk.LAZY_POS_ALIBI and nq.value == 4
+    # attention with another head count than the slopes is rejected before any device use
+    assert lazylib.lazy_attn_prefill(h, None, None, None, None, None, None, None, 1, 4, 4, 8,
+                                     0.1, None, None, None, 0, 0, None) == pk.LAZY_ERR_INVALID_ARG
+    assert lazylib.lazy_pool_destroy(h) == 0
+
+
+def test_page_table_page_positions():
+    # ALiBi page words: each page's offset field is the position of its first token
+    w, cu = pk.build_page_table([[([7, 8, 9], 100, 40)], [([3], 5, 1)]], 16, page_positions=True)
+    fields = [pk.lazy_unpack_page(int(x)) for x in w]
+    assert [f[1] for f in fields] == [100, 116, 132, 5]
+    assert [f[2] for f in fields] == [16, 16, 8, 1]
+    assert list(cu) == [0, 3, 4]
