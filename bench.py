@@ -442,6 +442,8 @@ def bench_ours(args):
         torch.cuda.empty_cache()
         line["mqa"] = mqa_bench(args, flush, stream, hbm_peak, tc_peak)
         torch.cuda.empty_cache()
+        line["alibi"] = alibi_bench(args, flush, stream, hbm_peak, tc_peak)
+        torch.cuda.empty_cache()
         line["mixed"] = mixed_sweep(args, flush, stream, hbm_peak)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, src, kv_bytes, args.cpu_seconds)
@@ -644,6 +646,71 @@ def mqa_bench(args, flush, stream, hbm_peak, tc_peak):
     med = _dist_ms(ms)["median"]
     tf = pb.flops / (med * 1e-3) / 1e12
     out["prefill"] = {"workload": "prefill_b8 shapes with Hkv 1 (group 32, 4 tokens per Q tile)",
+                      "value": round(tf, 2), "unit": "TFLOP/s", "ms_dist": _dist_ms(ms),
+                      "frac": round(tf / tc_peak, 4)}
+    pres.pool.close()
+    return out
+
+
+def alibi_bench(args, flush, stream, hbm_peak, tc_peak):
+    """ALiBi variant on the decode and prefill workloads' shapes (32/8/128 bf16, standard
+    slopes): the same kernels with no rotation and a slope * (n - m) bias."""
+    import torch
+
+    import position_independent_kv_lazy_gb300 as pk
+    import workload as W
+    from position_independent_kv_lazy_gb300 import harness as H
+
+    steps = max(5, args.steps // 2)
+    out = {}
+    wl = W.decode_workload(name="decode_b64_alibi")
+    slopes = W.alibi_slopes(wl.Hq)
+    src = H.DeviceSource(wl)
+    res = H.build_resident(wl, src, alibi_slopes=slopes)
+    db = H.decode_batch(wl, res, src)
+    B = len(db.reqs)
+    dws = torch.empty(pk.lazy_decode_workspace_bytes(res.pool, B, wl.Hq), dtype=torch.uint8,
+                      device="cuda")
+    dout = torch.empty_like(db.q)
+    dlse = torch.empty((B, wl.Hq), dtype=torch.float32, device="cuda")
+
+    def decode_call():
+        pk.lazy_attn_decode(res.pool, db.q, db.q_pos, db.words, db.cu_pages,
+                            sm_scale=wl.sm_scale, out=dout, lse=dlse, workspace=dws)
+
+    for _ in range(args.warmup):
+        flush(); decode_call()
+    ms = _timed_steps(decode_call, steps, flush, stream)
+    med = _dist_ms(ms)["median"]
+    kv = db.n_keys * wl.kv_bytes_per_token()
+    out["decode"] = {"workload": "decode_b64 with ALiBi (32 standard slopes)",
+                     "value": round(kv / (med * 1e-3) / 1e9, 2), "unit": "GB/s",
+                     "ms_dist": _dist_ms(ms), "frac": round(kv / (med * 1e-3) / 1e9 / hbm_peak, 4)}
+    res.pool.close()
+    del res, db, dws
+    torch.cuda.empty_cache()
+
+    pwl = W.prefill_workload(name="prefill_b8_alibi")
+    psrc = H.DeviceSource(pwl)
+    pres = H.build_resident(pwl, psrc, alibi_slopes=slopes)
+    pb = H.prefill_batch(pwl, pres, psrc)
+    pout = torch.empty_like(pb.q)
+    plse = torch.empty((pb.total_q, pwl.Hq), dtype=torch.float32, device="cuda")
+
+    def prefill_call():
+        pk.lazy_attn_prefill(pres.pool, pb.q, pb.k_new, pb.v_new, pb.cu_q, pb.q_pos0, pb.words,
+                             pb.cu_pages, pb.max_q_len, sm_scale=pwl.sm_scale, out=pout,
+                             lse=plse)
+
+    for _ in range(args.warmup):
+        flush(); prefill_call()
+    torch.cuda.synchronize()
+    if pk.lazy_get_device_error(pres.pool) != 0:
+        raise RuntimeError("device error in the ALiBi runs")
+    ms = _timed_steps(prefill_call, steps, flush, stream)
+    med = _dist_ms(ms)["median"]
+    tf = pb.flops / (med * 1e-3) / 1e12
+    out["prefill"] = {"workload": "prefill_b8 with ALiBi (32 standard slopes)",
                       "value": round(tf, 2), "unit": "TFLOP/s", "ms_dist": _dist_ms(ms),
                       "frac": round(tf / tc_peak, 4)}
     pres.pool.close()

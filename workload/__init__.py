@@ -267,6 +267,14 @@ def _docs_at_offsets(rng, n_pool, alpha, k, doc_len):
     return docs, offsets
 
 
+def request_stream(n_requests: int, n_pool: int, docs_per_req: int, alpha: float,
+                   seed: int = 0) -> List[List[int]]:
+    """A stream of retrievals for the cache-hit simulator: each request draws ``docs_per_req``
+    distinct Zipf(alpha) documents and puts them in a random order, as the workloads do."""
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 99])))
+    return [_docs_at_offsets(rng, n_pool, alpha, docs_per_req, 1)[0] for _ in range(n_requests)]
+
+
 # ----------------------------------------------------------------------------------------------
 # The five workloads (and scaled-down variants with the same structure for parity tests)
 # ----------------------------------------------------------------------------------------------
