@@ -124,6 +124,17 @@ enum { LAZY_POS_ROPE = 0, LAZY_POS_ALIBI = 1 };
  * afterwards, with nothing changed.
  */
 int lazy_pool_set_alibi(lazy_pool *pool, const float *h_slopes, int32_t num_q_heads);
+/*
+ * Decode kernel choice for a pool (lazy_attn_decode / lazy_attn_decode_noalloc):
+ *   LAZY_DECODE_AUTO  (default) the tensor-core kernel (warp-level mma.sync on each page, pages
+ *                     by TMA) for bf16 pools with head_dim 128, else the CUDA-core kernel
+ *   LAZY_DECODE_SIMT  always the CUDA-core kernel (fp32 arithmetic throughout)
+ * Both give results within the library's tolerances; the setting exists for comparison. It
+ * applies to calls made after it, and the workspace size depends on it (query
+ * lazy_decode_workspace_bytes after setting it).
+ */
+enum { LAZY_DECODE_AUTO = 0, LAZY_DECODE_SIMT = 1 };
+int lazy_pool_set_decode_kernel(lazy_pool *pool, int32_t kind);
 /* The pool's mode (LAZY_POS_*) and, in ALiBi mode, its number of query heads (else 0). */
 int lazy_pool_position_mode(lazy_pool *pool, int32_t *mode, int32_t *num_q_heads);
 

@@ -27,6 +27,8 @@ LAZY_ERR_BAD_PAGE = -5
 LAZY_ERR_TIMEOUT = -6
 LAZY_ERR_SCRATCH_LIMIT = -7
 LAZY_NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
+LAZY_DECODE_AUTO = 0
+LAZY_DECODE_SIMT = 1
 LAZY_POS_ROPE = 0
 LAZY_POS_ALIBI = 1
 LAZY_DTYPE_BF16 = 0
@@ -46,7 +48,7 @@ EXPORTS = [
     "lazy_decode_workspace_bytes", "lazy_attn_decode", "lazy_prefill_workspace_bytes",
     "lazy_attn_prefill", "lazy_get_device_error", "lazy_debug_gather", "lazy_debug_wait_timeout",
     "lazy_attn_decode_noalloc", "lazy_debug_exp2", "lazy_attn_prefill_append",
-    "lazy_pool_set_alibi", "lazy_pool_position_mode",
+    "lazy_pool_set_alibi", "lazy_pool_position_mode", "lazy_pool_set_decode_kernel",
 ]
 
 
@@ -83,6 +85,7 @@ _SIGS = {
     "lazy_pool_set_wait_limit": ([_vp, _u64], ctypes.c_int),
     "lazy_pool_set_alibi": ([_vp, ctypes.POINTER(ctypes.c_float), _i32], ctypes.c_int),
     "lazy_pool_position_mode": ([_vp, _pi32, _pi32], ctypes.c_int),
+    "lazy_pool_set_decode_kernel": ([_vp, _i32], ctypes.c_int),
     "kv_pool_alloc": ([_vp, _i32, _pi32], ctypes.c_int),
     "kv_pool_retain": ([_vp, _pi32, _i32], ctypes.c_int),
     "kv_pool_release": ([_vp, _pi32, _i32], ctypes.c_int),
@@ -194,6 +197,12 @@ class LazyPool:
             self.close()
         except Exception:
             pass
+
+
+def lazy_pool_set_decode_kernel(pool: LazyPool, kind: int):
+    """LAZY_DECODE_AUTO (tensor-core decode for bf16 / head_dim 128) or LAZY_DECODE_SIMT."""
+    _check("lazy_pool_set_decode_kernel",
+           load_library().lazy_pool_set_decode_kernel(pool.handle, int(kind)))
 
 
 def lazy_pool_set_wait_limit(pool: LazyPool, ns: int):

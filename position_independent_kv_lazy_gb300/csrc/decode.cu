@@ -17,7 +17,12 @@
 // of the GC query heads are reduced across the row's lanes with a reduce-scatter of shuffles,
 // the page's per-head max with a butterfly, probabilities go through 256 B of shared memory, and
 // PV accumulates in registers (GC x 16 bytes worth of fp32 per lane).
+#include <cuda.h>
+#include <string.h>
+
 #include <algorithm>
+#include <mutex>
+#include <type_traits>
 
 #include "lazy_common.cuh"
 #include "pool_internal.h"
@@ -420,6 +425,302 @@ __global__ void __launch_bounds__(WARPS * 32) decode_split_kernel(const DecodePa
   if (!timed_out && cur_unit >= 0) flush(cur_unit);
 }
 
+
+// ------------------------------------------------------------------ tensor-core decode (bf16)
+// The same flattened warp-granular partition, page ring, partial slots and combine as
+// decode_split_kernel, but each page's two small contractions run on the tensor cores with
+// warp-level mma.sync (m16n8k16, bf16 operands, fp32 accumulate) instead of ~1000 FMA/shuffle
+// instructions per page, which made that kernel issue-bound rather than HBM-bound:
+//   S[16 x 16] = Q[16 x 128] . K_page^T   A = the query fragment held in registers,
+//                                          B = K page rows via ldmatrix (8 k-steps x 2 n-tiles)
+//   O[16 x 128] += P[16 x 16] . V_page     A = P, re-packed from the S accumulator registers,
+//                                          B = V page via ldmatrix.trans (16 n-tiles)
+// A-operand rows: row g < GC holds bf16(q_g), row g + 8 holds bf16(q_g - bf16(q_g)), so the
+// S accumulator's rows g and g + 8 - registers of the same thread - add up to the score of a
+// query with ~16 mantissa bits, as accurate as the fp32 path. Rows >= GC and P's rows g + 8
+// are zero. Pages arrive by TMA (two 16 x 64 boxes each for K and V, 128-byte swizzle), so
+// the ldmatrix row reads are bank-conflict free.
+struct MmaDecodeParams {
+  DecodeParams d;
+  CUtensorMap tm_k, tm_v;  // pool rows (block * Hkv + h) * 16 + slot, box 16 rows x 64 dims
+};
+
+constexpr int kMmaStageBytes = 8192;  // K page (2 x 2 KB boxes) + V page (2 x 2 KB boxes)
+
+template <int STAGES>
+struct MmaSmem {
+  static constexpr int kStage = 0;                                  // STAGES x 8 KB, 1024-aligned
+  static constexpr int kBar = kStage + STAGES * kMmaStageBytes;     // uint64 [STAGES]
+  static constexpr int kWord = kBar + STAGES * 8;                   // uint64 [STAGES]
+  static constexpr int kUnit = kWord + STAGES * 8;                  // int32 [STAGES]
+  static constexpr int kBytes = ((kUnit + STAGES * 4) + 1023) / 1024 * 1024;  // per warp
+};
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4],
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                        uint32_t &r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                          uint32_t &r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void tma2d_g2s(void *dst, const CUtensorMap *m, int x, int y,
+                                          uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
+      "{%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"((uint64_t)m), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&h);
+}
+// Shared-memory address of 16-byte chunk `chunk` (0..15 over the 128 dims) of page row `row`
+// (0..15) in a page stored as two 16 x 64 boxes with 128-byte swizzle.
+__device__ __forceinline__ uint32_t page_chunk(uint32_t page, int row, int chunk) {
+  return page + (chunk >> 3) * 2048 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4);
+}
+
+template <int GC, int WARPS, int STAGES>
+__global__ void __launch_bounds__(WARPS * 32)
+    decode_mma_kernel(const __grid_constant__ MmaDecodeParams mp) {
+  using S = MmaSmem<STAGES>;
+  constexpr int D = 128;
+  static_assert(GC >= 1 && GC <= 8, "a 16-row fragment holds up to 8 heads (hi and lo rows)");
+  const DecodeParams &p = mp.d;
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint8_t *base = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t *ws = base + warp * S::kBytes;
+  uint8_t *stage = ws + S::kStage;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(ws + S::kBar);
+  uint64_t *meta_w = reinterpret_cast<uint64_t *>(ws + S::kWord);
+  int32_t *meta_u = reinterpret_cast<int32_t *>(ws + S::kUnit);
+
+  cudaGridDependencySynchronize();
+  const int32_t B = p.batch, HV = p.hv;
+  const int64_t N = (int64_t)HV * p.cu_pages[B];
+  const int64_t WT = (int64_t)gridDim.x * WARPS;
+  const int64_t wg = (int64_t)blockIdx.x * WARPS + warp;
+  const int64_t x0 = wg * N / WT, x1 = (wg + 1) * N / WT;
+  if (x0 >= x1) {
+    cudaTriggerProgrammaticLaunchCompletion();
+    return;
+  }
+  const int64_t n_mine = x1 - x0;
+  if (lane == 0) {
+    for (int s = 0; s < STAGES; ++s) mbar_init(&bars[s], 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+
+  Walker prod;
+  prod.init(x0, p.cu_pages, B, HV);
+  uint64_t w_next = 0;
+  if (lane == 0) w_next = p.words[prod.wbase + prod.pg];
+  auto issue = [&](int s) {
+    const uint64_t w = w_next;
+    uint32_t blk = word_block(w);
+    if (blk >= (uint32_t)p.num_blocks || word_nvalid(w) > (uint32_t)kPage) {
+      set_error(p.err, LAZY_DEVERR_BAD_PAGE);
+      blk = 0;
+    }
+    meta_w[s] = w;
+    meta_u[s] = prod.b * HV + prod.hv;
+    const int row = (int)((blk * (uint32_t)p.hkv + (uint32_t)(prod.hv / p.chunks)) * kPage);
+    uint8_t *st = stage + s * kMmaStageBytes;
+    mbar_arrive_expect_tx(&bars[s], kMmaStageBytes);
+    tma2d_g2s(st, &mp.tm_k, 0, row, &bars[s]);
+    tma2d_g2s(st + 2048, &mp.tm_k, 64, row, &bars[s]);
+    tma2d_g2s(st + 4096, &mp.tm_v, 0, row, &bars[s]);
+    tma2d_g2s(st + 6144, &mp.tm_v, 64, row, &bars[s]);
+  };
+  int64_t issued = 0;
+  auto issue_next = [&](int s) {
+    if (lane == 0) issue(s);
+    prod.advance(p.cu_pages, B, HV);
+    ++issued;
+    if (lane == 0 && issued < n_mine) w_next = p.words[prod.wbase + prod.pg];
+  };
+  for (int s = 0; s < STAGES && s < n_mine; ++s) issue_next(s);
+
+  const int g = lane >> 2, t = lane & 3;  // fragment row group and column pair
+  const bool live = g < GC;               // this thread's row is a real query head
+  const bool alibi = p.slopes != nullptr;
+  uint32_t qa[8][4];      // A fragments of the rotated, scaled query (hi rows g, lo rows g + 8)
+  uint32_t qraw[16];      // raw query pairs of this thread: dims 16ks + 2t + {0,1}, {8,9}
+  float o[16][4];         // O accumulator (rows g valid; rows g + 8 stay zero)
+  float m_run = -INFINITY, l_run = 0.f, sl2 = 0.f;
+  int32_t cur_unit = -1, cur_b = 0, m_pos = 0;
+  uint32_t cur_off = 0xFFFFFFFFu;
+  bool timed_out = false;
+
+  auto flush = [&](int32_t unit) {
+    float l = l_run;
+    l += __shfl_xor_sync(0xffffffffu, l, 1);
+    l += __shfl_xor_sync(0xffffffffu, l, 2);
+    const int64_t slot = (int64_t)unit + wg;
+    if (live) {
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      float *dst = p.ws_o + ((size_t)slot * GC + g) * D + 2 * t;
+#pragma unroll
+      for (int nt = 0; nt < 16; ++nt)
+        *reinterpret_cast<float2 *>(dst + nt * 8) = make_float2(o[nt][0] * inv, o[nt][1] * inv);
+      if (t == 0) p.ws_lse[(size_t)slot * GC + g] = l > 0.f ? m_run + log2f(l) : -INFINITY;
+    }
+  };
+
+  for (int64_t i = 0; i < n_mine; ++i) {
+    const int s = (int)(i % STAGES);
+    const uint32_t par = (uint32_t)((i / STAGES) & 1);
+    if (!mbar_wait(&bars[s], par, p.wait_ns)) {
+      if (lane == 0) set_error(p.err, LAZY_DEVERR_TIMEOUT);
+      timed_out = true;
+      const int64_t last = (i + STAGES < n_mine) ? i + STAGES : n_mine;
+      for (int64_t k = i; k < last; ++k)
+        mbar_wait(&bars[k % STAGES], (uint32_t)((k / STAGES) & 1), p.wait_ns);
+      break;
+    }
+    const uint64_t word = meta_w[s];
+    const int32_t unit = meta_u[s];
+    if (unit != cur_unit) {
+      if (cur_unit >= 0) flush(cur_unit);
+      cur_unit = unit;
+      cur_b = unit / HV;
+      const int32_t hv = unit % HV;
+      m_pos = p.q_pos[cur_b];
+      const __nv_bfloat16 *q = reinterpret_cast<const __nv_bfloat16 *>(p.q) +
+                               ((size_t)cur_b * p.hq + hv * GC + (live ? g : 0)) * D + 2 * t;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        qraw[2 * ks] = live ? *reinterpret_cast<const uint32_t *>(q + 16 * ks) : 0u;
+        qraw[2 * ks + 1] = live ? *reinterpret_cast<const uint32_t *>(q + 16 * ks + 8) : 0u;
+      }
+      sl2 = (alibi && live) ? p.slopes[hv * GC + g] * 1.4426950408889634f : 0.f;
+      m_run = -INFINITY;
+      l_run = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < 16; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[nt][e] = 0.f;
+      cur_off = 0xFFFFFFFFu;
+    }
+    const uint32_t nv = word_nvalid(word);
+    const bool bad = word_block(word) >= (uint32_t)p.num_blocks || nv > (uint32_t)kPage;
+    const uint32_t off = word_offset(word);
+    const uint32_t rot_off = alibi ? 0u : off;
+    if (!bad) {
+      if (rot_off != cur_off) {
+        // q <- R(m - o) q (identity for ALiBi), scaled into the log2 domain, split hi + lo
+        cur_off = rot_off;
+        const int64_t delta = alibi ? 0 : (int64_t)m_pos - (int64_t)off;
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {  // dims d < 64 pair with d + 64 (k-step ks + 4)
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const uint32_t lo_raw = qraw[2 * ks + h2], hi_raw = qraw[2 * (ks + 4) + h2];
+            float x[2], y[2];
+            x[0] = __uint_as_float(lo_raw << 16);
+            x[1] = __uint_as_float(lo_raw & 0xFFFF0000u);
+            y[0] = __uint_as_float(hi_raw << 16);
+            y[1] = __uint_as_float(hi_raw & 0xFFFF0000u);
+            float rx[2], ry[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int d = 16 * ks + 8 * h2 + 2 * t + e;
+              float cs, sn;
+              rope_cos_sin(delta, p.turn[d], cs, sn);
+              rx[e] = (x[e] * cs - y[e] * sn) * p.scale_log2;
+              ry[e] = (x[e] * sn + y[e] * cs) * p.scale_log2;
+            }
+            const uint32_t xh = pack_bf16x2(rx[0], rx[1]), yh = pack_bf16x2(ry[0], ry[1]);
+            const uint32_t xl = pack_bf16x2(rx[0] - __uint_as_float(xh << 16),
+                                            rx[1] - __uint_as_float(xh & 0xFFFF0000u));
+            const uint32_t yl = pack_bf16x2(ry[0] - __uint_as_float(yh << 16),
+                                            ry[1] - __uint_as_float(yh & 0xFFFF0000u));
+            // fragment registers: [0] row g cols 2t.., [1] row g+8, [2] row g cols 2t+8..,
+            // [3] row g+8 cols 2t+8..
+            qa[ks][2 * h2] = live ? xh : 0u;
+            qa[ks][2 * h2 + 1] = live ? xl : 0u;
+            qa[ks + 4][2 * h2] = live ? yh : 0u;
+            qa[ks + 4][2 * h2 + 1] = live ? yl : 0u;
+          }
+        }
+      }
+      const uint32_t kpg = smem_u32(stage + s * kMmaStageBytes);
+      const uint32_t vpg = kpg + 4096;
+      // ---- S = Q K^T: ldmatrix matrix j = lane / 8 covers keys 8 (j >> 1) .. +7 and
+      // dims 16 ks + 8 (j & 1) .. +7; row = lane % 8
+      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      const int lrow = ((lane >> 4) << 3) + (lane & 7), lhalf = (lane >> 3) & 1;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(page_chunk(kpg, lrow, 2 * ks + lhalf), b0, b1, b2, b3);
+        mma_bf16_16816(sc[0], qa[ks], b0, b1);
+        mma_bf16_16816(sc[1], qa[ks], b2, b3);
+      }
+      // scores of keys 2t, 2t+1 (n-tile 0) and 8+2t, 9+2t (n-tile 1): hi row + lo row
+      float sv[4] = {sc[0][0] + sc[0][2], sc[0][1] + sc[0][3], sc[1][0] + sc[1][2],
+                     sc[1][1] + sc[1][3]};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int key = (e >> 1) * 8 + 2 * t + (e & 1);
+        if (alibi) sv[e] = fmaf(sl2, (float)((int32_t)off + key - m_pos), sv[e]);
+        if (key >= (int)nv || !live) sv[e] = -INFINITY;
+      }
+      float pm = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
+      pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 1));
+      pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 2));
+      if (pm > m_run) {  // the same in the 4 lanes of a row
+        const float alpha = m_run == -INFINITY ? 0.f : exp2f(m_run - pm);
+        l_run *= alpha;
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt) {
+          o[nt][0] *= alpha;
+          o[nt][1] *= alpha;
+        }
+        m_run = pm;
+      }
+      float pv[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        pv[e] = sv[e] == -INFINITY ? 0.f : exp2f(sv[e] - m_run);
+        l_run += pv[e];
+      }
+      const uint32_t pa[4] = {pack_bf16x2(pv[0], pv[1]), 0u, pack_bf16x2(pv[2], pv[3]), 0u};
+      // ---- O += P V: ldmatrix.trans matrix j covers keys 8 (j & 1) .. +7 and dims
+      // 16 dp + 8 (j >> 1) .. +7
+      const int vrow = (((lane >> 3) & 1) << 3) + (lane & 7), vhalf = lane >> 4;
+#pragma unroll
+      for (int dp = 0; dp < 8; ++dp) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(page_chunk(vpg, vrow, 2 * dp + vhalf), b0, b1, b2, b3);
+        mma_bf16_16816(o[2 * dp], pa, b0, b1);
+        mma_bf16_16816(o[2 * dp + 1], pa, b2, b3);
+      }
+    }
+    __syncwarp();
+    if (issued < n_mine) issue_next(s);
+  }
+  cudaTriggerProgrammaticLaunchCompletion();
+  if (!timed_out && cur_unit >= 0) flush(cur_unit);
+}
+
 struct CombineParams {
   const float *ws_o;
   const float *ws_lse;
@@ -504,11 +805,62 @@ cudaError_t launch_pdl(K kernel, int grid, int block, int smem, cudaStream_t s, 
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+// The tensor-core kernel serves bf16 pools with head_dim 128 unless the pool asks for the
+// CUDA-core kernel (lazy_pool_set_decode_kernel).
+bool use_mma(const lazy_pool *p) {
+  return p->decode_kernel != LAZY_DECODE_SIMT && p->dtype == LAZY_DTYPE_BF16 && p->d == 128;
+}
+
+template <int GC, int STAGES>
+struct MmaLaunch {
+  static constexpr int kSmem = MmaSmem<STAGES>::kBytes * kWarps + 1024;  // + alignment slack
+  static int ctas_per_sm() {
+    static int cached = -1;
+    if (cached < 0) {
+      auto fn = decode_mma_kernel<GC, kWarps, STAGES>;
+      if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
+          cudaSuccess)
+        return -1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kWarps * 32, kSmem) !=
+          cudaSuccess)
+        return -1;
+      cached = std::max(1, n);
+    }
+    return cached;
+  }
+  static int run(lazy_pool *pl, const DecodeParams &dp, const CombineParams &cp, int grid,
+                 cudaStream_t s) {
+    int rc = ensure_pool_tmaps(pl);
+    if (rc != LAZY_OK) return rc;
+    if (ctas_per_sm() < 0) return record_cuda(cudaGetLastError(), "decode_mma_kernel set-up");
+    MmaDecodeParams mp;
+    mp.d = dp;
+    {
+      std::lock_guard<std::mutex> g(pl->mu);
+      memcpy(&mp.tm_k, pl->tmap_k, sizeof(CUtensorMap));
+      memcpy(&mp.tm_v, pl->tmap_v, sizeof(CUtensorMap));
+    }
+    LAZY_CUDA_TRY(launch_pdl(decode_mma_kernel<GC, kWarps, STAGES>, grid, kWarps * 32, kSmem,
+                             s, mp));
+    LAZY_CUDA_TRY(launch_pdl(combine_kernel<__nv_bfloat16, 128, GC>, dp.batch * dp.hv, 128, 0,
+                             s, cp));
+    return LAZY_OK;
+  }
+};
+
 template <typename T, int D, int GC, int STAGES>
 struct DecodeLaunch {
   using S = DecodeSmem<T, D, GC, STAGES>;
   static constexpr int kSmem = S::kBytes * kWarps;
-  static int ctas_per_sm() {
+  static constexpr bool kHasMma = std::is_same<T, __nv_bfloat16>::value && D == 128;
+  static int ctas_per_sm(const lazy_pool *pl) {
+    if constexpr (kHasMma) {
+      if (use_mma(pl)) return MmaLaunch<GC, STAGES>::ctas_per_sm();
+    }
+    return simt_ctas_per_sm();
+  }
+  static int simt_ctas_per_sm() {
     static int cached = -1;
     if (cached < 0) {
       auto fn = decode_split_kernel<T, D, GC, kWarps, STAGES>;
@@ -525,7 +877,9 @@ struct DecodeLaunch {
   }
   static int run(lazy_pool *pl, const DecodeParams &dp, const CombineParams &cp, int grid,
                  cudaStream_t s) {
-    (void)pl;
+    if constexpr (kHasMma) {
+      if (use_mma(pl)) return MmaLaunch<GC, STAGES>::run(pl, dp, cp, grid, s);
+    }
     LAZY_CUDA_TRY(launch_pdl(decode_split_kernel<T, D, GC, kWarps, STAGES>, grid, kWarps * 32,
                              kSmem, s, dp));
     LAZY_CUDA_TRY(launch_pdl(combine_kernel<T, D, GC>, dp.batch * dp.hv, 128, 0, s, cp));
@@ -573,8 +927,8 @@ int decode_grid(lazy_pool *p, int32_t gc, int32_t grid_ctas, int *grid) {
     *grid = grid_ctas;
     return LAZY_OK;
   }
-  const int per_sm =
-      with_decode_shape(p->dtype, p->d, gc, [](auto L) { return decltype(L)::ctas_per_sm(); });
+  const int per_sm = with_decode_shape(p->dtype, p->d, gc,
+                                       [&](auto L) { return decltype(L)::ctas_per_sm(p); });
   if (per_sm <= 0) {
     record_msg("decode kernel occupancy query failed");
     return LAZY_ERR_CUDA;

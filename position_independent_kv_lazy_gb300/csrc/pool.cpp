@@ -125,6 +125,12 @@ int lazy_pool_set_alibi(lazy_pool *p, const float *slopes, int32_t num_q_heads) 
   return LAZY_OK;
 }
 
+int lazy_pool_set_decode_kernel(lazy_pool *p, int32_t kind) {
+  if (!p || kind < LAZY_DECODE_AUTO || kind > LAZY_DECODE_SIMT) return LAZY_ERR_INVALID_ARG;
+  p->decode_kernel = kind;
+  return LAZY_OK;
+}
+
 int lazy_pool_position_mode(lazy_pool *p, int32_t *mode, int32_t *num_q_heads) {
   if (!p || !mode) return LAZY_ERR_INVALID_ARG;
   *mode = p->alibi ? LAZY_POS_ALIBI : LAZY_POS_ROPE;

@@ -29,6 +29,7 @@ struct lazy_pool {
 
   // ALiBi mode (lazy_pool_set_alibi): K is stored unrotated and attention adds
   // slope[head] * (n - m); page-word offsets are page start positions.
+  int32_t decode_kernel = 0;        // LAZY_DECODE_* (lazy_pool_set_decode_kernel)
   bool alibi = false;
   bool encoded = false;             // something was written: the mode can no longer change
   std::vector<float> slopes;        // per query head
@@ -46,6 +47,11 @@ namespace lazy {
 int record_cuda(cudaError_t e, const char *what);
 void record_msg(const char *msg);
 int ensure_device(lazy_pool *p);
+// TMA tensor maps of the page buffers (bf16, head_dim 128, 128-byte swizzle), built once:
+//   tmap_k / tmap_v    2-D, rows (block * Hkv + h) * 16 + slot, box 16 rows x 64 dims
+//   tmap_k8 / tmap_v8  4-D [block][kv head][slot][dim], box 8 blocks x 1 head x 16 x 64
+// LAZY_ERR_UNSUPPORTED for other pools.
+int ensure_pool_tmaps(lazy_pool *p);
 inline size_t elem_bytes(int32_t dtype) { return dtype == LAZY_DTYPE_BF16 ? 2 : 4; }
 inline size_t pool_bytes(const lazy_pool *p) {
   return (size_t)p->num_blocks * p->hkv * p->page_size * p->d * elem_bytes(p->dtype);

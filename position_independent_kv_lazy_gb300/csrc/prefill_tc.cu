@@ -868,6 +868,32 @@ int make_map(CUtensorMap *m, void *base, int rank, const cuuint64_t *dims,
 
 }  // namespace
 
+int ensure_pool_tmaps(lazy_pool *p) {
+  if (p->dtype != LAZY_DTYPE_BF16 || p->d != 128 || p->page_size != kPage)
+    return LAZY_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> g(p->mu);
+  if (p->tmaps_ready) return LAZY_OK;
+  // rows (block * Hkv + h) * 16 + slot, 128 dims; box 16 rows x 64 dims
+  const cuuint64_t dims[2] = {128, (cuuint64_t)p->num_blocks * p->hkv * kPage};
+  const cuuint64_t strides[1] = {256};
+  const cuuint32_t box[2] = {64, 16};
+  int rc = make_map(reinterpret_cast<CUtensorMap *>(p->tmap_k), p->k, 2, dims, strides, box);
+  if (rc != LAZY_OK) return rc;
+  rc = make_map(reinterpret_cast<CUtensorMap *>(p->tmap_v), p->v, 2, dims, strides, box);
+  if (rc != LAZY_OK) return rc;
+  // [block][kv head][slot][dim]; box = 64 dims x 16 slots x 1 head x 8 blocks
+  const cuuint64_t dims4[4] = {128, (cuuint64_t)kPage, (cuuint64_t)p->hkv,
+                               (cuuint64_t)p->num_blocks};
+  const cuuint64_t strides4[3] = {256, 256 * kPage, (cuuint64_t)256 * kPage * p->hkv};
+  const cuuint32_t box4[4] = {64, (cuuint32_t)kPage, 1, 8};
+  rc = make_map(reinterpret_cast<CUtensorMap *>(p->tmap_k8), p->k, 4, dims4, strides4, box4);
+  if (rc != LAZY_OK) return rc;
+  rc = make_map(reinterpret_cast<CUtensorMap *>(p->tmap_v8), p->v, 4, dims4, strides4, box4);
+  if (rc != LAZY_OK) return rc;
+  p->tmaps_ready = true;
+  return LAZY_OK;
+}
+
 int prefill_tc_supported(const lazy_pool *p, int32_t hq) {
   if (p->dtype != LAZY_DTYPE_BF16 || p->d != 128 || p->page_size != kPage)
     return LAZY_ERR_UNSUPPORTED;
@@ -883,28 +909,10 @@ int prefill_tc(lazy_pool *p, const PrefillParams &pp, int32_t max_q_len, cudaStr
   TcParams tp;
   memset(&tp, 0, sizeof(tp));
   int rc;
+  rc = ensure_pool_tmaps(p);
+  if (rc != LAZY_OK) return rc;
   {
-    // Pool page maps: rows (block * Hkv + h) * 16 + slot, 128 dims; box 16 rows x 64 dims.
     std::lock_guard<std::mutex> g(p->mu);
-    if (!p->tmaps_ready) {
-      const cuuint64_t dims[2] = {128, (cuuint64_t)p->num_blocks * p->hkv * kPage};
-      const cuuint64_t strides[1] = {256};
-      const cuuint32_t box[2] = {64, 16};
-      rc = make_map(reinterpret_cast<CUtensorMap *>(p->tmap_k), p->k, 2, dims, strides, box);
-      if (rc != LAZY_OK) return rc;
-      rc = make_map(reinterpret_cast<CUtensorMap *>(p->tmap_v), p->v, 2, dims, strides, box);
-      if (rc != LAZY_OK) return rc;
-      // [block][kv head][slot][dim]; box = 64 dims x 16 slots x 1 head x 8 blocks
-      const cuuint64_t dims4[4] = {128, (cuuint64_t)kPage, (cuuint64_t)p->hkv,
-                                   (cuuint64_t)p->num_blocks};
-      const cuuint64_t strides4[3] = {256, 256 * kPage, (cuuint64_t)256 * kPage * p->hkv};
-      const cuuint32_t box4[4] = {64, (cuuint32_t)kPage, 1, 8};
-      rc = make_map(reinterpret_cast<CUtensorMap *>(p->tmap_k8), p->k, 4, dims4, strides4, box4);
-      if (rc != LAZY_OK) return rc;
-      rc = make_map(reinterpret_cast<CUtensorMap *>(p->tmap_v8), p->v, 4, dims4, strides4, box4);
-      if (rc != LAZY_OK) return rc;
-      p->tmaps_ready = true;
-    }
     memcpy(&tp.tm_k, p->tmap_k, sizeof(CUtensorMap));
     memcpy(&tp.tm_v, p->tmap_v, sizeof(CUtensorMap));
     memcpy(&tp.tm_k8, p->tmap_k8, sizeof(CUtensorMap));

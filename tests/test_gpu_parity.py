@@ -111,6 +111,44 @@ def test_decode_parity_edge_layouts(pk, D, Hq, Hkv, dtype):
     _check_decode(wl, out, lse)
 
 
+@pytest.mark.parametrize("kind", ["simt", "auto"])
+@pytest.mark.parametrize("Hq,Hkv", [(32, 8), (8, 8), (64, 8), (32, 1)])
+def test_decode_both_kernels_edge_layouts(pk, kind, Hq, Hkv):
+    # bf16 / head_dim 128 runs the tensor-core (mma.sync) kernel by default; the CUDA-core
+    # kernel stays selectable and both must meet the tolerances (groups 4, 1, 8, MQA 32)
+    H = _h()
+    wl = _edge_decode_workload(128, Hq, Hkv, "bf16")
+    src = H.HostSource(wl)
+    res = H.build_resident(wl, src, resident_pool=False)
+    pk.lazy_pool_set_decode_kernel(res.pool, pk.LAZY_DECODE_SIMT if kind == "simt"
+                                   else pk.LAZY_DECODE_AUTO)
+    db = H.decode_batch(wl, res, src)
+    out, lse = pk.lazy_attn_decode(res.pool, db.q, db.q_pos, db.words, db.cu_pages,
+                                   sm_scale=wl.sm_scale)
+    torch.cuda.synchronize()
+    assert pk.lazy_get_device_error(res.pool) == 0
+    _check_decode(wl, out.float().cpu().numpy(), lse.cpu().numpy())
+
+
+def test_decode_kernels_agree_full_size(pk):
+    # decode_b64 (64 x 4161 keys): the tensor-core and CUDA-core kernels on the same inputs
+    H = _h()
+    wl = W.decode_workload()
+    src = H.DeviceSource(wl)
+    res = H.build_resident(wl, src)
+    db = H.decode_batch(wl, res, src)
+    outs = {}
+    for kind in (pk.LAZY_DECODE_AUTO, pk.LAZY_DECODE_SIMT):
+        pk.lazy_pool_set_decode_kernel(res.pool, kind)
+        o, l = pk.lazy_attn_decode(res.pool, db.q, db.q_pos, db.words, db.cu_pages,
+                                   sm_scale=wl.sm_scale)
+        torch.cuda.synchronize()
+        outs[kind] = (o.float().cpu().numpy(), l.cpu().numpy())
+    assert pk.lazy_get_device_error(res.pool) == 0
+    (oa, la), (os_, ls) = outs[pk.LAZY_DECODE_AUTO], outs[pk.LAZY_DECODE_SIMT]
+    assert np.abs(oa - os_).max() <= 2e-2 and np.abs(la - ls).max() <= 1e-3
+
+
 @pytest.mark.parametrize("grid", [1, 2, 5, 37, 1000])
 def test_decode_any_grid_same_result(pk, grid):
     wl = W.decode_workload(batch=5, docs_per_req=3, doc_len=100, n_pool=6, question=21, seed=1)
