@@ -369,7 +369,7 @@ def bench_ours(args):
     e2e_avg = sum(e2e_ms) / len(e2e_ms)
 
     traffic = None
-    prof = os.path.join(ROOT, "profiles", "decode_split_traffic.json")
+    prof = os.path.join(ROOT, "profiles", "decode_mma_kernel_traffic.json")
     if os.path.exists(prof):
         try:
             with open(prof) as f:
@@ -401,7 +401,7 @@ def bench_ours(args):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
                      "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
                      "traffic": traffic, "peak_kind": peak_kind,
-                     "kernel": "lazy_attn_decode (decode_split_kernel + combine_kernel)"},
+                     "kernel": "lazy_attn_decode (decode_mma_kernel + combine_kernel)"},
         "e2e": {"value": round(ws * kv_bytes / (e2e_avg * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_avg, 5)},
