@@ -272,30 +272,42 @@ def bench_ours(args):
         pk.lazy_attn_decode(nres.pool, ndb.q, ndb.q_pos, ndb.words, ndb.cu_pages,
                             sm_scale=nwl.sm_scale, out=nout, lse=nlse, workspace=nws)
 
-    # e2e buffers: pinned host inputs/outputs of one step
-    h_q = db.q.cpu().pin_memory()
-    h_k = db.new_k.cpu().pin_memory()
-    h_v = db.new_v.cpu().pin_memory()
-    h_words = db.words.cpu().pin_memory()
-    h_cu = db.cu_pages.cpu().pin_memory()
-    h_pos = db.q_pos.cpu().pin_memory()
-    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    d_q, d_k, d_v = torch.empty_like(db.q), torch.empty_like(db.new_k), torch.empty_like(db.new_v)
-    d_words, d_cu, d_pos = (torch.empty_like(db.words), torch.empty_like(db.cu_pages),
-                            torch.empty_like(db.q_pos))
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_words, h_cu, h_pos))
-    d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
+    # e2e buffers: the step's inputs packed in one pinned host buffer (one H2D copy) and its
+    # outputs in one device buffer (one D2H copy), as a serving loop would stage them
+    def _layout(items):
+        offs, total = [], 0
+        for t in items:
+            offs.append(total)
+            total += (t.numel() * t.element_size() + 255) // 256 * 256
+        return offs, total
+
+    in_src = [db.q, db.new_k, db.new_v, db.words, db.cu_pages, db.q_pos, db.slot_mapping,
+              db.local_pos]
+    in_offs, in_total = _layout(in_src)
+    h_in = torch.empty(in_total, dtype=torch.uint8).pin_memory()
+    d_in = torch.empty(in_total, dtype=torch.uint8, device="cuda")
+
+    def _view(buf, off, like):
+        n = like.numel() * like.element_size()
+        return buf[off:off + n].view(like.dtype).view(like.shape)
+
+    for t, o in zip(in_src, in_offs):
+        _view(h_in, o, t).copy_(t.cpu())
+    (d_q, d_k, d_v, d_words, d_cu, d_pos, d_slot, d_lpos) = [
+        _view(d_in, o, t) for t, o in zip(in_src, in_offs)]
+    out_offs, out_total = _layout([out, lse])
+    d_res = torch.empty(out_total, dtype=torch.uint8, device="cuda")
+    h_res = torch.empty(out_total, dtype=torch.uint8).pin_memory()
+    e_out, e_lse = _view(d_res, out_offs[0], out), _view(d_res, out_offs[1], lse)
+    h2d = sum(t.numel() * t.element_size() for t in in_src)
+    d2h = out.numel() * out.element_size() + lse.numel() * lse.element_size()
 
     def e2e_step():
-        for d, h in ((d_q, h_q), (d_k, h_k), (d_v, h_v), (d_words, h_words), (d_cu, h_cu),
-                     (d_pos, h_pos)):
-            d.copy_(h, non_blocking=True)
-        pk.kv_pool_write_tokens(res.pool, d_k, d_v, db.slot_mapping, db.local_pos)
-        pk.lazy_attn_decode(res.pool, d_q, d_pos, d_words, d_cu, sm_scale=wl.sm_scale, out=out,
-                            lse=lse, workspace=workspace)
-        h_out.copy_(out, non_blocking=True)
-        h_lse.copy_(lse, non_blocking=True)
+        d_in.copy_(h_in, non_blocking=True)
+        pk.kv_pool_write_tokens(res.pool, d_k, d_v, d_slot, d_lpos)
+        pk.lazy_attn_decode(res.pool, d_q, d_pos, d_words, d_cu, sm_scale=wl.sm_scale,
+                            out=e_out, lse=e_lse, workspace=workspace)
+        h_res.copy_(d_res, non_blocking=True)
 
     only_decode = args.only == "decode"
 
