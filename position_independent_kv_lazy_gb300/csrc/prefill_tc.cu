@@ -543,23 +543,27 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       const uint32_t q_addr = smem_u32(Qs), k_addr = smem_u32(Ks), v_addr = smem_u32(Vs);
       // Issue order keeps both softmax groups busy: QK for Q tile 0 of the next key tile is
       // issued as soon as P_0 of this tile is consumed, while group 1 still works on S_1.
+      // Descriptors of the tiles' first rows. Shared-memory addresses stay below 2^18 and every
+      // offset is a multiple of 16 bytes, so the descriptor of address + off is the base
+      // descriptor + off / 16 (the start-address field never carries into the others).
+      const uint64_t dq0 = sdesc(q_addr, 16, 1024), dk0 = sdesc(k_addr, 16, 1024);
+      const uint64_t dv0 = sdesc(v_addr, kHalfBytes, 1024);
       auto qk = [&](int j, int i) {
-        const int s = j % kNK;
+        const uint64_t a0 = dq0 + (uint64_t)((i * kTileBytes) >> 4);
+        const uint64_t b0 = dk0 + (uint64_t)(((j % kNK) * kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-          mma_ss(tmem + i * 128, sdesc(q_addr + i * kTileBytes + off, 16, 1024),
-                 sdesc(k_addr + s * kTileBytes + off, 16, 1024), idesc_qk, kk > 0);
+          const uint64_t off = (uint64_t)(((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4);
+          mma_ss(tmem + i * 128, a0 + off, b0 + off, idesc_qk, kk > 0);
         }
         mma_commit(&s_full[i]);
       };
       auto pv = [&](int j, int i) {
-        const int s = j % kNV;
+        const uint64_t b0 = dv0 + (uint64_t)(((j % kNV) * kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tmem + 256 + i * 128, tmem + i * 128 + kk * 8,
-                 sdesc(v_addr + s * kTileBytes + kk * 2048, kHalfBytes, 1024), idesc_pv,
-                 (j > 0 || kk > 0) ? 1 : 0);
+          mma_ts(tmem + 256 + i * 128, tmem + i * 128 + kk * 8, b0 + (uint64_t)(kk * (2048 >> 4)),
+                 idesc_pv, (j > 0 || kk > 0) ? 1 : 0);
       };
       bool ok = cta_wait(q_rot, 0, abort, lim, p.err);
       tc_fence_after();
