@@ -46,22 +46,32 @@ def _peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled while the timed work runs."""
+    """nvidia-smi clocks and throttle reasons, sampled every 20 ms from before the warm-up until
+    after the last timed step. summary() keeps only the samples whose timestamp falls inside a
+    timed window (see _timed_steps), so the median is taken under load."""
 
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index: int):
         self.index = index
         self.proc = None
+        self.lines = []
+
+    def _start(self, interval_ms):
+        return subprocess.Popen(
+            ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+             "--format=csv,noheader,nounits", "-lms", str(interval_ms)],
+            stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
 
     def __enter__(self):
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.proc = self._start(20)
+            time.sleep(0.5)                      # let the first samples start before timing
+            if self.proc.poll() is not None:     # interval refused: fall back to 100 ms
+                self.proc = self._start(100)
+                time.sleep(0.5)
         except Exception:
             self.proc = None
         return self
@@ -77,23 +87,37 @@ class ClockSampler:
                 out, _ = self.proc.communicate()
             self.lines = [l for l in out.splitlines() if l.strip()]
 
-    def summary(self):
-        sm, mx, reasons = [], None, set()
+    @staticmethod
+    def _stamp(text):
+        import datetime
+        try:
+            return datetime.datetime.strptime(text.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
+
+    def summary(self, windows=None):
+        sm, mx, reasons, total = [], None, set(), 0
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for l in getattr(self, "lines", []):
+        for l in self.lines:
             f = [x.strip() for x in l.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
             try:
-                sm.append(float(f[1]))
-                mx = float(f[2])
+                clk, mxv = float(f[2]), float(f[3])
             except ValueError:
                 continue
-            for n, v in zip(names, f[5:9]):
+            total += 1
+            t = self._stamp(f[0])
+            if windows and t is not None and not any(a <= t <= b for a, b in windows):
+                continue
+            sm.append(clk)
+            mx = mxv
+            for n, v in zip(names, f[6:10]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "samples_total": total,
+                "timed_windows_ms": round(sum(b - a for a, b in (windows or [])) * 1e3, 1)}
 
 
 def _dist():
@@ -161,9 +185,15 @@ def _cpu_model():
         return None
 
 
+TIMED_WINDOWS = []   # host wall-clock spans of every timed region, for the clock samples
+
+
 def _timed_steps(fn, steps, flush, stream):
-    """Run `steps` calls of fn, each after an untimed L2 flush; return per-step ms (events)."""
+    """Run `steps` calls of fn, each after an untimed L2 flush; return per-step ms (events).
+    The wall-clock span of the region is appended to TIMED_WINDOWS."""
     import torch
+    torch.cuda.synchronize()
+    t0 = time.time()
     times = []
     for _ in range(steps):
         flush()
@@ -174,6 +204,7 @@ def _timed_steps(fn, steps, flush, stream):
         b.record(stream)
         times.append((a, b))
     torch.cuda.synchronize()
+    TIMED_WINDOWS.append((t0, time.time()))
     return [a.elapsed_time(b) for a, b in times]
 
 
@@ -346,6 +377,7 @@ def bench_ours(args):
     # ---------------- mixed serving step, skew sweep (extra object; built and timed one alpha
     # at a time after the main timed region, see mixed_sweep)
 
+    clk = ClockSampler(local).__enter__()
     torch.cuda.synchronize()
     for _ in range(args.warmup):
         flush(); step(); e2e_step(); no_reuse_call()
@@ -354,24 +386,23 @@ def bench_ours(args):
     torch.cuda.synchronize()
     for pool in pools:
         if pk.lazy_get_device_error(pool) != 0:
+            clk.__exit__()
             raise RuntimeError("device error during warm-up")
 
-    with ClockSampler(local) as clk:
-        torch.cuda.nvtx.range_push("timed_region")
-        _barrier(ws)
-        torch.cuda.synchronize()
-        step_ms = _timed_steps(step, args.steps, flush, stream)
-        torch.cuda.synchronize()
-        _barrier(ws)
-        dec_ms = _timed_steps(decode_call, args.steps, flush, stream)
-        e2e_ms = _timed_steps(e2e_step, args.steps, flush, stream)
-        nr_ms = _timed_steps(no_reuse_call, args.steps, flush, stream)
-        if not only_decode:
-            pre_ms = _timed_steps(prefill_call, max(3, args.steps // 2), flush, stream)
-            long_ms = _timed_steps(long_call, max(3, args.steps // 2), flush, stream)
-        torch.cuda.synchronize()
-        torch.cuda.nvtx.range_pop()
-    clocks = clk.summary()
+    torch.cuda.nvtx.range_push("timed_region")
+    _barrier(ws)
+    torch.cuda.synchronize()
+    step_ms = _timed_steps(step, args.steps, flush, stream)
+    torch.cuda.synchronize()
+    _barrier(ws)
+    dec_ms = _timed_steps(decode_call, args.steps, flush, stream)
+    e2e_ms = _timed_steps(e2e_step, args.steps, flush, stream)
+    nr_ms = _timed_steps(no_reuse_call, args.steps, flush, stream)
+    if not only_decode:
+        pre_ms = _timed_steps(prefill_call, max(3, args.steps // 2), flush, stream)
+        long_ms = _timed_steps(long_call, max(3, args.steps // 2), flush, stream)
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
 
     total_ms = _max_over_ranks(sum(step_ms), ws)
     ms_per_step = total_ms / args.steps
@@ -426,7 +457,7 @@ def bench_ours(args):
         "decode_tokens_per_s": round(ws * B / (ms_per_step * 1e-3), 1),
         "step_ms_dist": _dist_ms(step_ms),
         "decode_call_ms_dist": _dist_ms(dec_ms),
-        "clocks": clocks,
+        "clocks": None,   # filled in after the last timed section
     }
     if not only_decode:
         pre_avg = sum(pre_ms) / len(pre_ms)
@@ -457,6 +488,8 @@ def bench_ours(args):
         line["alibi"] = alibi_bench(args, flush, stream, hbm_peak, tc_peak)
         torch.cuda.empty_cache()
         line["mixed"] = mixed_sweep(args, flush, stream, hbm_peak)
+    clk.__exit__()
+    line["clocks"] = clk.summary(TIMED_WINDOWS)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, src, kv_bytes, args.cpu_seconds)
     if rank == 0:
@@ -572,9 +605,12 @@ def chain_bench(args, flush, stream, n_steps=32, reps=3):
     if pk.lazy_get_device_error(res.pool) != 0:
         raise RuntimeError("device error in the prefill -> decode chain")
     runs = []
+    torch.cuda.synchronize()
+    t0 = time.time()
     for _ in range(reps):
         run_chain(runs)
     torch.cuda.synchronize()
+    TIMED_WINDOWS.append((t0, time.time()))
     pre = [e[0].elapsed_time(e[1]) for e in runs]
     stp = [e[s + 1].elapsed_time(e[s + 2]) for e in runs for s in range(n_steps)]
     tot = [e[0].elapsed_time(e[-1]) for e in runs]
