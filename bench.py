@@ -765,13 +765,49 @@ def alibi_bench(args, flush, stream, hbm_peak, tc_peak):
     return out
 
 
+TRAFFIC_SOURCES = ("decode.cu", "lazy_common.cuh")   # what the decode kernel is built from
+TRAFFIC_COMMAND = ("ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum,"
+                   "lts__t_sector_hit_rate.pct --clock-control none -k regex:decode_mma -s 3 -c 1 "
+                   "--csv --log-file gpurun_out/decode_traffic.csv python bench.py --only decode "
+                   "--steps 3 --warmup 3 --no-cpu-baseline")
+
+
 def _kernel_hash():
+    """Hash of the sources of the decode kernel: the recorded DRAM traffic is reported only
+    while it matches."""
     import hashlib
     h = hashlib.sha256()
-    p = os.path.join(ROOT, "position_independent_kv_lazy_gb300", "csrc", "decode.cu")
-    with open(p, "rb") as f:
-        h.update(f.read())
+    for name in TRAFFIC_SOURCES:
+        with open(os.path.join(ROOT, "position_independent_kv_lazy_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
     return h.hexdigest()[:16]
+
+
+def record_traffic(csv_path):
+    """Write profiles/decode_mma_kernel_traffic.json from the CSV of TRAFFIC_COMMAND (one
+    captured launch of the bench's decode kernel), stamped with the current source hash."""
+    import csv
+    vals, kernel = {}, None
+    with open(csv_path) as f:
+        rows = [r for r in csv.reader(l for l in f if l.startswith('"'))]
+    hdr = rows[0]
+    ki, mi, vi = hdr.index("Kernel Name"), hdr.index("Metric Name"), hdr.index("Metric Value")
+    for r in rows[1:]:
+        if "decode_mma_kernel" not in r[ki]:
+            continue
+        kernel = r[ki]
+        vals[r[mi]] = float(r[vi].replace(",", ""))
+    rd, wr = int(vals["dram__bytes_read.sum"]), int(vals["dram__bytes_write.sum"])
+    out = {"kernel": kernel, "kernel_hash": _kernel_hash(),
+           "workload": "decode_b64 (64 req x 4161 keys, Hq32/Hkv8/D128 bf16)",
+           "bytes_per_launch": rd + wr, "dram_bytes_read": rd, "dram_bytes_write": wr,
+           "gpu_time_ns_under_ncu": int(vals.get("gpu__time_duration.sum", 0)),
+           "lts_sector_hit_rate_pct": vals.get("lts__t_sector_hit_rate.pct"),
+           "command": TRAFFIC_COMMAND}
+    with open(os.path.join(ROOT, "profiles", "decode_mma_kernel_traffic.json"), "w") as f:
+        json.dump(out, f, indent=1)
+        f.write("\n")
+    print(json.dumps(out))
 
 
 def cpu_baseline(wl, src, kv_bytes_total, budget_s):
@@ -856,7 +892,13 @@ def main():
     ap.add_argument("--only", choices=["all", "decode", "prefill"], default="all",
                     help="decode / prefill: time only that workload (smaller footprint, for "
                          "profiling)")
+    ap.add_argument("--record-traffic", metavar="CSV",
+                    help="write profiles/decode_mma_kernel_traffic.json from the ncu CSV of the "
+                         "traffic capture and exit (no GPU needed)")
     args = ap.parse_args()
+    if args.record_traffic:
+        record_traffic(args.record_traffic)
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
