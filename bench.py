@@ -270,7 +270,10 @@ def bench_ours(args):
     wl = W.decode_workload()
     src = H.DeviceSource(wl)
     res = H.build_resident(wl, src)
-    db = H.decode_batch(wl, res, src)
+    # each request's segments ordered so that shared documents line up across the batch (the
+    # attention result does not depend on page order); the context order is timed as a control
+    db = H.decode_batch(wl, res, src, align_shared=True)
+    cdb = H.decode_batch(wl, res, src)
     kv_bytes = db.n_keys * wl.kv_bytes_per_token()  # K and V, 4096 B per key
     B = wl.batch
     ws_bytes = pk.lazy_decode_workspace_bytes(res.pool, B, wl.Hq)
@@ -280,6 +283,10 @@ def bench_ours(args):
 
     def decode_call():
         pk.lazy_attn_decode(res.pool, db.q, db.q_pos, db.words, db.cu_pages,
+                            sm_scale=wl.sm_scale, out=out, lse=lse, workspace=workspace)
+
+    def context_order_call():
+        pk.lazy_attn_decode(res.pool, cdb.q, cdb.q_pos, cdb.words, cdb.cu_pages,
                             sm_scale=wl.sm_scale, out=out, lse=lse, workspace=workspace)
 
     def step():
@@ -362,7 +369,7 @@ def bench_ours(args):
         lwl = W.long_decode_workload()
         lsrc = H.DeviceSource(lwl)
         lres = H.build_resident(lwl, lsrc)
-        ldb = H.decode_batch(lwl, lres, lsrc)
+        ldb = H.decode_batch(lwl, lres, lsrc, align_shared=True)
         lws = torch.empty(pk.lazy_decode_workspace_bytes(lres.pool, lwl.batch, lwl.Hq),
                           dtype=torch.uint8, device="cuda")
         lout = torch.empty_like(ldb.q)
@@ -380,7 +387,7 @@ def bench_ours(args):
     clk = ClockSampler(local).__enter__()
     torch.cuda.synchronize()
     for _ in range(args.warmup):
-        flush(); step(); e2e_step(); no_reuse_call()
+        flush(); step(); e2e_step(); no_reuse_call(); context_order_call()
         if not only_decode:
             prefill_call(); long_call()
     torch.cuda.synchronize()
@@ -398,6 +405,7 @@ def bench_ours(args):
     dec_ms = _timed_steps(decode_call, args.steps, flush, stream)
     e2e_ms = _timed_steps(e2e_step, args.steps, flush, stream)
     nr_ms = _timed_steps(no_reuse_call, args.steps, flush, stream)
+    co_ms = _timed_steps(context_order_call, args.steps, flush, stream)
     if not only_decode:
         pre_ms = _timed_steps(prefill_call, max(3, args.steps // 2), flush, stream)
         long_ms = _timed_steps(long_call, max(3, args.steps // 2), flush, stream)
@@ -454,6 +462,11 @@ def bench_ours(args):
             "value": round(n_bytes / (sum(nr_ms) / len(nr_ms) * 1e-3) / 1e9, 2), "unit": "GB/s",
             "ms_per_call": round(sum(nr_ms) / len(nr_ms), 5),
             "frac": round(n_bytes / (sum(nr_ms) / len(nr_ms) * 1e-3) / 1e9 / hbm_peak, 4)},
+        "decode_context_order": {
+            "workload": "decode_b64 with each request's pages in context order (documents not "
+                        "lined up across requests)",
+            "value": round(kv_bytes / (sorted(co_ms)[len(co_ms) // 2] * 1e-3) / 1e9, 2),
+            "unit": "GB/s", "ms_per_call": round(sorted(co_ms)[len(co_ms) // 2], 5)},
         "decode_tokens_per_s": round(ws * B / (ms_per_step * 1e-3), 1),
         "step_ms_dist": _dist_ms(step_ms),
         "decode_call_ms_dist": _dist_ms(dec_ms),
@@ -519,7 +532,7 @@ def mixed_sweep(args, flush, stream, hbm_peak):
         src = H.DeviceSource(wl)
         res = H.build_resident(wl, src)
         pb = H.prefill_batch(wl, res, src)
-        db = H.decode_batch(wl, res, src)
+        db = H.decode_batch(wl, res, src, align_shared=True)
         ws = torch.empty(pk.lazy_decode_workspace_bytes(res.pool, len(db.reqs), wl.Hq),
                          dtype=torch.uint8, device="cuda")
         dout = torch.empty_like(db.q)
@@ -574,7 +587,7 @@ def chain_bench(args, flush, stream, n_steps=32, reps=3):
     res = H.build_resident(wl, src, extra_blocks=H.chain_blocks_needed(wl, n_steps))
     ch = H.chain_setup(wl, res, src, n_steps)
     pb = ch.pb
-    steps = [H.chain_step_batch(wl, res, ch, s, src) for s in range(n_steps)]
+    steps = [H.chain_step_batch(wl, res, ch, s, src, align_shared=True) for s in range(n_steps)]
     B = len(pb.reqs)
     pout = torch.empty_like(pb.q)
     plse = torch.empty((pb.total_q, wl.Hq), dtype=torch.float32, device="cuda")
@@ -646,7 +659,7 @@ def mqa_bench(args, flush, stream, hbm_peak, tc_peak):
     wl = W.decode_workload(Hkv=1, name="decode_b64_mqa")
     src = H.DeviceSource(wl)
     res = H.build_resident(wl, src)
-    db = H.decode_batch(wl, res, src)
+    db = H.decode_batch(wl, res, src, align_shared=True)
     B = len(db.reqs)
     dws = torch.empty(pk.lazy_decode_workspace_bytes(res.pool, B, wl.Hq), dtype=torch.uint8,
                       device="cuda")
@@ -715,7 +728,7 @@ def alibi_bench(args, flush, stream, hbm_peak, tc_peak):
     slopes = W.alibi_slopes(wl.Hq)
     src = H.DeviceSource(wl)
     res = H.build_resident(wl, src, alibi_slopes=slopes)
-    db = H.decode_batch(wl, res, src)
+    db = H.decode_batch(wl, res, src, align_shared=True)
     B = len(db.reqs)
     dws = torch.empty(pk.lazy_decode_workspace_bytes(res.pool, B, wl.Hq), dtype=torch.uint8,
                       device="cuda")
@@ -766,6 +779,7 @@ def alibi_bench(args, flush, stream, hbm_peak, tc_peak):
 
 
 TRAFFIC_SOURCES = ("decode.cu", "lazy_common.cuh")   # what the decode kernel is built from
+TRAFFIC_WORKLOAD = "decode_b64 (64 req x 4161 keys, Hq32/Hkv8/D128 bf16), shared documents aligned"
 TRAFFIC_COMMAND = ("ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum,"
                    "lts__t_sector_hit_rate.pct --clock-control none -k regex:decode_mma -s 3 -c 1 "
                    "--csv --log-file gpurun_out/decode_traffic.csv python bench.py --only decode "
@@ -773,10 +787,10 @@ TRAFFIC_COMMAND = ("ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu
 
 
 def _kernel_hash():
-    """Hash of the sources of the decode kernel: the recorded DRAM traffic is reported only
-    while it matches."""
+    """Hash of the decode kernel's sources and of the workload tag: the recorded DRAM traffic is
+    reported only while it matches."""
     import hashlib
-    h = hashlib.sha256()
+    h = hashlib.sha256(TRAFFIC_WORKLOAD.encode())
     for name in TRAFFIC_SOURCES:
         with open(os.path.join(ROOT, "position_independent_kv_lazy_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
@@ -799,7 +813,7 @@ def record_traffic(csv_path):
         vals[r[mi]] = float(r[vi].replace(",", ""))
     rd, wr = int(vals["dram__bytes_read.sum"]), int(vals["dram__bytes_write.sum"])
     out = {"kernel": kernel, "kernel_hash": _kernel_hash(),
-           "workload": "decode_b64 (64 req x 4161 keys, Hq32/Hkv8/D128 bf16)",
+           "workload": TRAFFIC_WORKLOAD,
            "bytes_per_launch": rd + wr, "dram_bytes_read": rd, "dram_bytes_write": wr,
            "gpu_time_ns_under_ncu": int(vals.get("gpu__time_duration.sum", 0)),
            "lts_sector_hit_rate_pct": vals.get("lts__t_sector_hit_rate.pct"),

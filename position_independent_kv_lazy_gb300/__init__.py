@@ -10,6 +10,7 @@ The functions keep the C names: ``kv_pool_insert_doc``, ``lazy_attn_prefill``,
 """
 from __future__ import annotations
 
+import collections
 import ctypes
 import os
 from typing import List, Optional, Sequence, Tuple
@@ -286,13 +287,57 @@ def lazy_pack_pages(block_ids, offsets, n_valid) -> np.ndarray:
     return out
 
 
+def align_shared_segments(requests: Sequence[Sequence[Tuple[Sequence[int], int, int]]]
+                          ) -> List[List[Tuple[Sequence[int], int, int]]]:
+    """Reorder each request's segments so that a segment cached once and used by several
+    requests (the same block ids) sits at the same index of every request's list.
+
+    Attention over a request does not depend on the order of its pages (each page word carries
+    its own offset), so the order is free. The decode kernels stream every request's pages
+    front to back at about the same rate; with a shared document at the same index everywhere,
+    its pages are read by all its requests at about the same time, and all but the first read
+    hit L2. Greedy: segments in order of decreasing use count take the index that is free in
+    most of their requests; a segment that finds it taken, and every segment used once, fills
+    the first free index, in the request's own order."""
+    keys = [[tuple(ids) for ids, _, _ in segs] for segs in requests]
+    count = collections.Counter(k for ks in keys for k in set(ks))
+    shared = sorted((k for k, c in count.items() if c > 1),
+                    key=lambda k: (-count[k], k[:1]))
+    placed = [[None] * len(segs) for segs in requests]     # index -> segment position
+    used = [set() for _ in requests]                        # segment positions placed
+    where = collections.defaultdict(list)                   # key -> [(request, position)]
+    for b, ks in enumerate(keys):
+        for i, k in enumerate(ks):
+            where[k].append((b, i))
+    for k in shared:
+        first = {}
+        for b, i in where[k]:
+            first.setdefault(b, i)                          # one occurrence per request
+        width = max(len(placed[b]) for b in first)
+        best = max(range(width), key=lambda s: (
+            sum(1 for b in first if s < len(placed[b]) and placed[b][s] is None), -s))
+        for b, i in first.items():
+            if best < len(placed[b]) and placed[b][best] is None:
+                placed[b][best] = i
+                used[b].add(i)
+    out = []
+    for b, segs in enumerate(requests):
+        rest = iter(i for i in range(len(segs)) if i not in used[b])
+        order = [i if i is not None else next(rest) for i in placed[b]]
+        out.append([segs[i] for i in order])
+    return out
+
+
 def build_page_table(requests: Sequence[Sequence[Tuple[Sequence[int], int, int]]],
-                     page_size: int = 16, page_positions: bool = False
-                     ) -> Tuple[np.ndarray, np.ndarray]:
+                     page_size: int = 16, page_positions: bool = False,
+                     align_shared: bool = False) -> Tuple[np.ndarray, np.ndarray]:
     """Page table of a batch: ``requests[b]`` lists segments (block_ids, logical offset, length).
     The word's offset field is the segment's offset (RoPE pools) or, with ``page_positions``
-    (ALiBi pools), the logical position of each page's first token.
+    (ALiBi pools), the logical position of each page's first token. ``align_shared`` orders
+    each request's segments with align_shared_segments (same attention result, more L2 reuse).
     Returns (words uint64 [total pages], cu_pages int32 [B+1])."""
+    if align_shared:
+        requests = align_shared_segments(requests)
     blk, off, nv, cu = [], [], [], [0]
     for segs in requests:
         for ids, o, length in segs:

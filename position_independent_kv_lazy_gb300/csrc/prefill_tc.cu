@@ -236,6 +236,13 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       : "memory");
 }
 
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // 2^x with one MUFU instruction (inputs here are <= 8, results in (0, 256]; -inf gives 0).
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -724,7 +731,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           }
         }
       }
-      // max with eight independent chains (one running max would be a 128-long chain)
+      // max with eight independent chains of three-input maxima (one running max would be a
+      // 128-long chain)
       float cmk[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k)
@@ -733,11 +741,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       for (int e = 16; e < 128; e += 16) {
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          cmk[k] = fmaxf(cmk[k], fmaxf(__uint_as_float(r[e + 2 * k]),
-                                       __uint_as_float(r[e + 2 * k + 1])));
+          cmk[k] = fmax3(cmk[k], __uint_as_float(r[e + 2 * k]), __uint_as_float(r[e + 2 * k + 1]));
       }
-      const float cm = fmaxf(fmaxf(fmaxf(cmk[0], cmk[1]), fmaxf(cmk[2], cmk[3])),
-                             fmaxf(fmaxf(cmk[4], cmk[5]), fmaxf(cmk[6], cmk[7])));
+      const float cm = fmax3(fmax3(cmk[0], cmk[1], cmk[2]), fmax3(cmk[3], cmk[4], cmk[5]),
+                             fmaxf(cmk[6], cmk[7]));
       const float cm2 = kAlibi ? cm : cm * sl2;
       const float sle = kAlibi ? 1.f : sl2;  // scale still to apply in the exponent
       if (cm2 > m_use + 8.f) {  // includes the first finite max (m_use = -inf)

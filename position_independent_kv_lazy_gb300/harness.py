@@ -144,14 +144,15 @@ def build_resident(wl, src, device="cuda", resident_pool: bool = True, stream=No
     return Resident(pool, doc_blocks, priv_blocks)
 
 
-def page_table(wl, res: Resident, reqs, with_private: bool):
+def page_table(wl, res: Resident, reqs, with_private: bool, align_shared: bool = False):
     segs = []
     for r in reqs:
         s = [(res.doc_blocks[d], o, wl.doc_len) for d, o in zip(r.docs, r.offsets)]
         if with_private:
             s.append((res.priv_blocks[r.index], r.priv_offset, r.priv_len))
         segs.append(s)
-    return build_page_table(segs, wl.page_size, page_positions=res.pool.alibi_slopes is not None)
+    return build_page_table(segs, wl.page_size, page_positions=res.pool.alibi_slopes is not None,
+                            align_shared=align_shared)
 
 
 @dataclasses.dataclass
@@ -169,10 +170,13 @@ class DecodeBatch:
     n_keys: int
 
 
-def decode_batch(wl, res: Resident, src, device="cuda", reqs=None) -> DecodeBatch:
+def decode_batch(wl, res: Resident, src, device="cuda", reqs=None,
+                 align_shared: bool = False) -> DecodeBatch:
+    """The batch's decode inputs. ``align_shared`` orders each request's segments so that
+    shared documents sit at the same index in every request (see align_shared_segments)."""
     import torch
     reqs = reqs if reqs is not None else wl.decode_requests()
-    words, cu = page_table(wl, res, reqs, with_private=True)
+    words, cu = page_table(wl, res, reqs, with_private=True, align_shared=align_shared)
     q = torch.cat([src.q(r.index, device) for r in reqs], dim=0).contiguous()
     q_pos = torch.tensor([r.m for r in reqs], dtype=torch.int32, device=device)
     nk, nv, slots, lpos = [], [], [], []
@@ -255,7 +259,8 @@ def chain_setup(wl, res: Resident, src, n_steps: int, device="cuda", reqs=None) 
                  torch.tensor(lpos, dtype=torch.int32, device=device), n_steps)
 
 
-def chain_step_batch(wl, res: Resident, ch: Chain, step: int, src, device="cuda") -> DecodeBatch:
+def chain_step_batch(wl, res: Resident, ch: Chain, step: int, src, device="cuda",
+                     align_shared: bool = False) -> DecodeBatch:
     """Decode inputs of chain step `step`: page words over every document plus the private
     segment (question + tokens 0..step), the step's queries and the new token's k/v and slot."""
     import torch
@@ -276,7 +281,8 @@ def chain_step_batch(wl, res: Resident, ch: Chain, step: int, src, device="cuda"
         slots.append(blk * P + j % P)
         lpos.append(j)
         qpos.append(r.q_pos0 + j)
-    words, cu = build_page_table(segs, P, page_positions=res.pool.alibi_slopes is not None)
+    words, cu = build_page_table(segs, P, page_positions=res.pool.alibi_slopes is not None,
+                                 align_shared=align_shared)
     return DecodeBatch(
         ch.pb.reqs, torch.cat(qs).contiguous(),
         torch.tensor(qpos, dtype=torch.int32, device=device),

@@ -111,6 +111,40 @@ def test_decode_parity_edge_layouts(pk, D, Hq, Hkv, dtype):
     _check_decode(wl, out, lse)
 
 
+def test_decode_aligned_page_order_parity(pk):
+    # shared documents lined up across requests: the same attention, so the oracle tolerances
+    # hold; the edge workload repeats one document at two offsets within a request
+    H = _h()
+    wl = _edge_decode_workload(128, 32, 8, "bf16")
+    src = H.HostSource(wl)
+    res = H.build_resident(wl, src, resident_pool=False)
+    db = H.decode_batch(wl, res, src, align_shared=True)
+    out, lse = pk.lazy_attn_decode(res.pool, db.q, db.q_pos, db.words, db.cu_pages,
+                                   sm_scale=wl.sm_scale)
+    torch.cuda.synchronize()
+    assert pk.lazy_get_device_error(res.pool) == 0
+    _check_decode(wl, out.float().cpu().numpy(), lse.cpu().numpy())
+
+
+def test_decode_aligned_order_full_size_matches_context_order(pk):
+    # decode_b64 in both page orders: only the summation order differs
+    H = _h()
+    wl = W.decode_workload()
+    src = H.DeviceSource(wl)
+    res = H.build_resident(wl, src)
+    res_out = []
+    for align in (False, True):
+        db = H.decode_batch(wl, res, src, align_shared=align)
+        o, l = pk.lazy_attn_decode(res.pool, db.q, db.q_pos, db.words, db.cu_pages,
+                                   sm_scale=wl.sm_scale)
+        torch.cuda.synchronize()
+        res_out.append((o.float().cpu().numpy(), l.cpu().numpy()))
+    assert pk.lazy_get_device_error(res.pool) == 0
+    (o0, l0), (o1, l1) = res_out
+    assert np.abs(l0 - l1).max() <= 1e-4
+    assert np.abs(o0 - o1).max() <= 2 ** -7 * max(1.0, np.abs(o0).max())
+
+
 @pytest.mark.parametrize("kind", ["simt", "auto"])
 @pytest.mark.parametrize("Hq,Hkv", [(32, 8), (8, 8), (64, 8), (32, 1)])
 def test_decode_both_kernels_edge_layouts(pk, kind, Hq, Hkv):
