@@ -781,7 +781,7 @@ def alibi_bench(args, flush, stream, hbm_peak, tc_peak):
 TRAFFIC_SOURCES = ("decode.cu", "lazy_common.cuh")   # what the decode kernel is built from
 TRAFFIC_WORKLOAD = "decode_b64 (64 req x 4161 keys, Hq32/Hkv8/D128 bf16), shared documents aligned"
 TRAFFIC_COMMAND = ("ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum,"
-                   "lts__t_sector_hit_rate.pct --clock-control none -k regex:decode_mma -s 3 -c 1 "
+                   "lts__t_sector_hit_rate.pct --clock-control none -k regex:decode_mma -s 4 -c 1 "
                    "--csv --log-file gpurun_out/decode_traffic.csv python bench.py --only decode "
                    "--steps 3 --warmup 3 --no-cpu-baseline")
 
