@@ -488,3 +488,53 @@ def test_mixed_step_full_size_sampled(pk):
     heads = [12, 13, 14, 15]
     assert np.abs(dout.float().cpu().numpy()[10][heads] - ro[0][heads]).max() <= 2e-2
     assert np.abs(dlse.cpu().numpy()[10][heads] - rl[0][heads]).max() <= 1e-3
+
+
+# ------------------------------------------------------------------ page order
+def _permuted_table(pk, wl, res, rng, with_private):
+    # each request's segments in a random order: attention does not depend on page order
+    segs = []
+    for r in wl.requests:
+        s = [(res.doc_blocks[d], o, wl.doc_len) for d, o in zip(r.docs, r.offsets)]
+        if with_private:
+            s.append((res.priv_blocks[r.index], r.priv_offset, r.priv_len))
+        segs.append([s[i] for i in rng.permutation(len(s))])
+    words, cu = pk.build_page_table(segs, wl.page_size)
+    return (torch.from_numpy(words.view(np.int64)).cuda(), torch.from_numpy(cu).cuda())
+
+
+@pytest.mark.parametrize("seed", [1, 2, 3])
+@pytest.mark.parametrize("kind", ["simt", "auto"])
+def test_decode_random_segment_orders(pk, seed, kind):
+    H = _h()
+    wl = _edge_decode_workload(128, 32, 8, "bf16")
+    src = H.HostSource(wl)
+    res = H.build_resident(wl, src, resident_pool=False)
+    pk.lazy_pool_set_decode_kernel(res.pool, pk.LAZY_DECODE_SIMT if kind == "simt"
+                                   else pk.LAZY_DECODE_AUTO)
+    db = H.decode_batch(wl, res, src)
+    words, cu = _permuted_table(pk, wl, res, np.random.default_rng(seed), with_private=True)
+    out, lse = pk.lazy_attn_decode(res.pool, db.q, db.q_pos, words, cu, sm_scale=wl.sm_scale)
+    torch.cuda.synchronize()
+    assert pk.lazy_get_device_error(res.pool) == 0
+    _check_decode(wl, out.float().cpu().numpy(), lse.cpu().numpy())
+
+
+@pytest.mark.parametrize("seed", [1, 2])
+@pytest.mark.parametrize("flags", ["tc", "simt"])
+def test_prefill_random_segment_orders(pk, seed, flags):
+    # permuted documents change which pages share a 128-key tile (mixed offsets within a tile)
+    H = _h()
+    wl = _edge_prefill_workload(128, 32, 8, "bf16")
+    src = H.HostSource(wl)
+    res = H.build_resident(wl, src, resident_pool=False, drop_raw=False)
+    pb = H.prefill_batch(wl, res, src)
+    words, cu = _permuted_table(pk, wl, res, np.random.default_rng(seed), with_private=False)
+    out, lse = pk.lazy_attn_prefill(res.pool, pb.q, pb.k_new, pb.v_new, pb.cu_q, pb.q_pos0,
+                                    words, cu, pb.max_q_len, sm_scale=wl.sm_scale,
+                                    flags=pk.LAZY_PREFILL_TC if flags == "tc"
+                                    else pk.LAZY_PREFILL_SIMT)
+    torch.cuda.synchronize()
+    assert pk.lazy_get_device_error(res.pool) == 0
+    _check_prefill(wl, pb, out.float().cpu().numpy(), lse.cpu().numpy(),
+                   lse_tol=TC_EDGE_LSE_TOL if flags == "tc" else None)
