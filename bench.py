@@ -501,6 +501,8 @@ def bench_ours(args):
         line["alibi"] = alibi_bench(args, flush, stream, hbm_peak, tc_peak)
         torch.cuda.empty_cache()
         line["mixed"] = mixed_sweep(args, flush, stream, hbm_peak)
+        torch.cuda.empty_cache()
+        line["encode"] = encode_bench(args, flush, stream, hbm_peak)
     clk.__exit__()
     line["clocks"] = clk.summary(TIMED_WINDOWS)
     if rank == 0 and not args.no_cpu_baseline:
@@ -510,6 +512,40 @@ def bench_ours(args):
     if ws > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def encode_bench(args, flush, stream, hbm_peak):
+    """Document encode (kv_pool_insert_doc): one 8192-token segment (Hkv 8, D 128, bf16) into
+    blocks it already owns, i.e. the K rotation at local positions, the V copy and the page
+    scatter in one launch. Bytes moved = read raw K and V + write both = 8192 B per token."""
+    import torch
+
+    import position_independent_kv_lazy_gb300 as pk
+
+    n_tok, hkv, d = 8192, 8, 128
+    pool = pk.LazyPool(num_blocks=n_tok // 16, num_kv_heads=hkv, head_dim=d,
+                       dtype=torch.bfloat16, rope_base=500000.0)
+    g = torch.Generator(device="cuda").manual_seed(0)
+    k = torch.randn((n_tok, hkv, d), generator=g, device="cuda").to(torch.bfloat16)
+    v = torch.randn((n_tok, hkv, d), generator=g, device="cuda").to(torch.bfloat16)
+    ids = pk.kv_pool_insert_doc(pool, k, v)
+
+    def insert():
+        pk.kv_pool_insert_doc(pool, k, v, block_ids=ids)
+
+    for _ in range(3):
+        flush(); insert()
+    torch.cuda.synchronize()
+    if pk.lazy_get_device_error(pool) != 0:
+        raise RuntimeError("device error in encode")
+    ms = _timed_steps(insert, max(5, args.steps // 2), flush, stream)
+    med = sorted(ms)[len(ms) // 2]
+    moved = n_tok * hkv * d * 2 * 2 * 2
+    pool.close()
+    return {"workload": "one 8192-token segment, Hkv 8, D 128, bf16, into owned blocks",
+            "value": round(moved / (med * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "bytes_moved_per_call": moved, "ms_dist": _dist_ms(ms),
+            "frac": round(moved / (med * 1e-3) / 1e9 / hbm_peak, 4)}
 
 
 def mixed_sweep(args, flush, stream, hbm_peak):
