@@ -742,6 +742,9 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
   const int64_t N = (int64_t)p.hv * p.cu_pages[p.batch];
   const int64_t W = p.warps;
   T *out = reinterpret_cast<T *>(p.out);
+  // With at least one page per warp (N >= W) no warp's range is empty, and the per-slot test
+  // (two 64-bit divisions) is skipped.
+  const bool dense = N >= W;
   int64_t wf = 0, wl = -1;
   if (np > 0) {
     const int64_t S = (int64_t)p.hv * wbase + (int64_t)hv * np, E = S + np;
@@ -752,14 +755,14 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
     const int g = idx / (D / 4), d4 = idx % (D / 4);
     float mx = -INFINITY;
     for (int64_t w = wf; w <= wl; ++w) {
-      if (w * N / W == (w + 1) * N / W) continue;  // empty range
+      if (!dense && w * N / W == (w + 1) * N / W) continue;  // empty range
       mx = fmaxf(mx, p.ws_lse[(size_t)(u + w) * GC + g]);
     }
     float sum = 0.f;
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
     if (mx != -INFINITY) {
       for (int64_t w = wf; w <= wl; ++w) {
-        if (w * N / W == (w + 1) * N / W) continue;
+        if (!dense && w * N / W == (w + 1) * N / W) continue;
         const float l = p.ws_lse[(size_t)(u + w) * GC + g];
         if (l == -INFINITY) continue;
         const float wt = exp2f(l - mx);
