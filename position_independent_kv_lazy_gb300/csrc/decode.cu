@@ -753,25 +753,37 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
   }
   for (int idx = threadIdx.x; idx < GC * (D / 4); idx += blockDim.x) {
     const int g = idx / (D / 4), d4 = idx % (D / 4);
-    float mx = -INFINITY;
-    for (int64_t w = wf; w <= wl; ++w) {
-      if (!dense && w * N / W == (w + 1) * N / W) continue;  // empty range
-      mx = fmaxf(mx, p.ws_lse[(size_t)(u + w) * GC + g]);
-    }
-    float sum = 0.f;
+    // one online pass over the unit's slots, eight at a time with their loads issued together
+    float mx = -INFINITY, sum = 0.f;
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (mx != -INFINITY) {
-      for (int64_t w = wf; w <= wl; ++w) {
-        if (!dense && w * N / W == (w + 1) * N / W) continue;
-        const float l = p.ws_lse[(size_t)(u + w) * GC + g];
-        if (l == -INFINITY) continue;
-        const float wt = exp2f(l - mx);
-        const float4 o = *reinterpret_cast<const float4 *>(p.ws_o + ((size_t)(u + w) * GC + g) * D +
-                                                           d4 * 4);
-        sum += wt;
-        a.x = fmaf(wt, o.x, a.x); a.y = fmaf(wt, o.y, a.y);
-        a.z = fmaf(wt, o.z, a.z); a.w = fmaf(wt, o.w, a.w);
+    for (int64_t w0 = wf; w0 <= wl; w0 += 8) {
+      float lv[8];
+      float4 ov[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int64_t w = w0 + k;
+        const bool use = w <= wl && (dense || w * N / W != (w + 1) * N / W);
+        lv[k] = use ? p.ws_lse[(size_t)(u + w) * GC + g] : -INFINITY;
+        ov[k] = use ? *reinterpret_cast<const float4 *>(p.ws_o + ((size_t)(u + w) * GC + g) * D +
+                                                        d4 * 4)
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
       }
+      float bm = lv[0];
+#pragma unroll
+      for (int k = 1; k < 8; ++k) bm = fmaxf(bm, lv[k]);
+      if (bm == -INFINITY) continue;
+      const float nm = fmaxf(mx, bm);
+      const float sc = mx == -INFINITY ? 0.f : exp2f(mx - nm);
+      sum *= sc;
+      a.x *= sc; a.y *= sc; a.z *= sc; a.w *= sc;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float wt = lv[k] == -INFINITY ? 0.f : exp2f(lv[k] - nm);
+        sum += wt;
+        a.x = fmaf(wt, ov[k].x, a.x); a.y = fmaf(wt, ov[k].y, a.y);
+        a.z = fmaf(wt, ov[k].z, a.z); a.w = fmaf(wt, ov[k].w, a.w);
+      }
+      mx = nm;
     }
     const float inv = sum > 0.f ? 1.f / sum : 0.f;
     const int qh = hv * GC + g;
