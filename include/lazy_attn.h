@@ -204,8 +204,11 @@ int lazy_pack_pages(int32_t n, const uint32_t *block_ids, const uint32_t *offset
  *                does not change the result, only how often q is re-rotated.
  *   sm_scale     score scale (1/sqrt(head_dim) for standard attention)
  *   grid_ctas    0 = one persistent wave sized to the GPU; otherwise that many CTAs
- *   d_out        device [batch][num_q_heads][head_dim], pool dtype
+ *   d_out        device [batch][num_q_heads][head_dim], pool dtype, 16-byte aligned
  *   d_lse        device float [batch][num_q_heads]; -inf (and out = 0) for a request with no keys
+ *                d_out and d_lse are written once, by the final merge kernel, and may also be
+ *                pinned host memory (which the GPU addresses directly): the result then reaches
+ *                the host without a separate copy.
  *   d_workspace  device scratch of at least lazy_decode_workspace_bytes(...) bytes, 16-byte
  *                aligned; holds partial (o, lse) per split. Not read before it is written.
  * Requires num_q_heads % num_kv_heads == 0; group sizes 1, 2, 4, 8 run natively, larger groups
