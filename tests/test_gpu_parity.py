@@ -146,6 +146,28 @@ def test_decode_aligned_order_full_size_matches_context_order(pk):
 
 
 @pytest.mark.parametrize("kind", ["simt", "auto"])
+def test_decode_output_to_pinned_host_memory(pk, kind):
+    # out and lse may live in pinned host memory: the merge writes them there directly
+    H = _h()
+    wl = _edge_decode_workload(128, 32, 8, "bf16")
+    src = H.HostSource(wl)
+    res = H.build_resident(wl, src, resident_pool=False)
+    pk.lazy_pool_set_decode_kernel(res.pool, pk.LAZY_DECODE_SIMT if kind == "simt"
+                                   else pk.LAZY_DECODE_AUTO)
+    db = H.decode_batch(wl, res, src)
+    o_dev, l_dev = pk.lazy_attn_decode(res.pool, db.q, db.q_pos, db.words, db.cu_pages,
+                                       sm_scale=wl.sm_scale)
+    o_host = torch.empty(tuple(o_dev.shape), dtype=o_dev.dtype).pin_memory()
+    l_host = torch.empty(tuple(l_dev.shape), dtype=torch.float32).pin_memory()
+    pk.lazy_attn_decode(res.pool, db.q, db.q_pos, db.words, db.cu_pages, sm_scale=wl.sm_scale,
+                        out=o_host, lse=l_host)
+    torch.cuda.synchronize()
+    assert pk.lazy_get_device_error(res.pool) == 0
+    assert torch.equal(o_host, o_dev.cpu()) and torch.equal(l_host, l_dev.cpu())
+    _check_decode(wl, o_host.float().numpy(), l_host.numpy())
+
+
+@pytest.mark.parametrize("kind", ["simt", "auto"])
 @pytest.mark.parametrize("Hq,Hkv", [(32, 8), (8, 8), (64, 8), (32, 1)])
 def test_decode_both_kernels_edge_layouts(pk, kind, Hq, Hkv):
     # bf16 / head_dim 128 runs the tensor-core (mma.sync) kernel by default; the CUDA-core
