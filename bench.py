@@ -143,9 +143,16 @@ def _max_over_ranks(x, ws):
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def _job_rate(units_per_rank, slowest_ms, ws):
+    """Whole-job rate (units/s): the units all ranks processed over the slowest rank's time
+    (_max_over_ranks of the per-rank times)."""
+    return ws * units_per_rank / (slowest_ms * 1e-3)
 
 
 # ------------------------------------------------------------------------------------------------
@@ -414,7 +421,7 @@ def bench_ours(args):
 
     total_ms = _max_over_ranks(sum(step_ms), ws)
     ms_per_step = total_ms / args.steps
-    value = ws * kv_bytes / (ms_per_step * 1e-3) / 1e9
+    value = _job_rate(kv_bytes * args.steps, total_ms, ws) / 1e9
     dec_avg = sum(dec_ms) / len(dec_ms)
     achieved = kv_bytes / (dec_avg * 1e-3) / 1e9
     e2e_avg = sum(e2e_ms) / len(e2e_ms)
