@@ -494,11 +494,188 @@ __device__ __forceinline__ uint32_t page_chunk(uint32_t page, int row, int chunk
   return page + (chunk >> 3) * 2048 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4);
 }
 
+// Per-warp attention state of the tensor-core decode over one unit (request, virtual head).
+template <int GC>
+struct MmaWarpState {
+  uint32_t qa[8][4];  // A fragments of the rotated, scaled query (hi rows g, lo rows g + 8)
+  uint32_t qraw[16];  // raw query pairs of this thread: dims 16ks + 2t + {0,1}, {8,9}
+  float o[16][4];     // O accumulator (rows g valid; rows g + 8 stay zero)
+  float m_run, l_run, sl2;
+  int32_t m_pos;
+  uint32_t cur_off;
+};
+
+// Start unit (request b, virtual head hv): raw query rows, ALiBi slopes, empty accumulators.
+template <int GC>
+__device__ __forceinline__ void mma_begin_unit(MmaWarpState<GC> &st, const DecodeParams &p,
+                                               int32_t b, int32_t hv, int lane) {
+  constexpr int D = 128;
+  const int g = lane >> 2, t = lane & 3;
+  const bool live = g < GC;
+  st.m_pos = p.q_pos[b];
+  const __nv_bfloat16 *q = reinterpret_cast<const __nv_bfloat16 *>(p.q) +
+                           ((size_t)b * p.hq + hv * GC + (live ? g : 0)) * D + 2 * t;
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    st.qraw[2 * ks] = live ? *reinterpret_cast<const uint32_t *>(q + 16 * ks) : 0u;
+    st.qraw[2 * ks + 1] = live ? *reinterpret_cast<const uint32_t *>(q + 16 * ks + 8) : 0u;
+  }
+  st.sl2 = (p.slopes != nullptr && live) ? p.slopes[hv * GC + g] * 1.4426950408889634f : 0.f;
+  st.m_run = -INFINITY;
+  st.l_run = 0.f;
+#pragma unroll
+  for (int nt = 0; nt < 16; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) st.o[nt][e] = 0.f;
+  st.cur_off = 0xFFFFFFFFu;
+}
+
+// One 16-key page (K at page_smem, V 4 KB after it): S = Q K^T, online softmax, O += P V.
+template <int GC>
+__device__ __forceinline__ void mma_attend_page(MmaWarpState<GC> &st, const DecodeParams &p,
+                                                uint64_t word, uint32_t page_smem, int lane) {
+  const int g = lane >> 2, t = lane & 3;  // fragment row group and column pair
+  const bool live = g < GC;               // this thread's row is a real query head
+  const bool alibi = p.slopes != nullptr;
+  const uint32_t nv = word_nvalid(word);
+  const bool bad = word_block(word) >= (uint32_t)p.num_blocks || nv > (uint32_t)kPage;
+  const uint32_t off = word_offset(word);
+  const uint32_t rot_off = alibi ? 0u : off;
+  if (!bad) {
+    if (rot_off != st.cur_off) {
+      // q <- R(m - o) q (identity for ALiBi), scaled into the log2 domain, split hi + lo
+      st.cur_off = rot_off;
+      const int64_t delta = alibi ? 0 : (int64_t)st.m_pos - (int64_t)off;
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {  // dims d < 64 pair with d + 64 (k-step ks + 4)
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const uint32_t lo_raw = st.qraw[2 * ks + h2], hi_raw = st.qraw[2 * (ks + 4) + h2];
+          float x[2], y[2];
+          x[0] = __uint_as_float(lo_raw << 16);
+          x[1] = __uint_as_float(lo_raw & 0xFFFF0000u);
+          y[0] = __uint_as_float(hi_raw << 16);
+          y[1] = __uint_as_float(hi_raw & 0xFFFF0000u);
+          float rx[2], ry[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int d = 16 * ks + 8 * h2 + 2 * t + e;
+            float cs, sn;
+            rope_cos_sin(delta, p.turn[d], cs, sn);
+            rx[e] = (x[e] * cs - y[e] * sn) * p.scale_log2;
+            ry[e] = (x[e] * sn + y[e] * cs) * p.scale_log2;
+          }
+          const uint32_t xh = pack_bf16x2(rx[0], rx[1]), yh = pack_bf16x2(ry[0], ry[1]);
+          const uint32_t xl = pack_bf16x2(rx[0] - __uint_as_float(xh << 16),
+                                          rx[1] - __uint_as_float(xh & 0xFFFF0000u));
+          const uint32_t yl = pack_bf16x2(ry[0] - __uint_as_float(yh << 16),
+                                          ry[1] - __uint_as_float(yh & 0xFFFF0000u));
+          // fragment registers: [0] row g cols 2t.., [1] row g+8, [2] row g cols 2t+8..,
+          // [3] row g+8 cols 2t+8..
+          st.qa[ks][2 * h2] = live ? xh : 0u;
+          st.qa[ks][2 * h2 + 1] = live ? xl : 0u;
+          st.qa[ks + 4][2 * h2] = live ? yh : 0u;
+          st.qa[ks + 4][2 * h2 + 1] = live ? yl : 0u;
+        }
+      }
+    }
+    const uint32_t kpg = page_smem;
+    const uint32_t vpg = kpg + 4096;
+    // ---- S = Q K^T: ldmatrix matrix j = lane / 8 covers keys 8 (j >> 1) .. +7 and
+    // dims 16 ks + 8 (j & 1) .. +7; row = lane % 8
+    float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    const int lrow = ((lane >> 4) << 3) + (lane & 7), lhalf = (lane >> 3) & 1;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(page_chunk(kpg, lrow, 2 * ks + lhalf), b0, b1, b2, b3);
+      mma_bf16_16816(sc[0], st.qa[ks], b0, b1);
+      mma_bf16_16816(sc[1], st.qa[ks], b2, b3);
+    }
+    // scores of keys 2t, 2t+1 (n-tile 0) and 8+2t, 9+2t (n-tile 1): hi row + lo row
+    float sv[4] = {sc[0][0] + sc[0][2], sc[0][1] + sc[0][3], sc[1][0] + sc[1][2],
+                   sc[1][1] + sc[1][3]};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int key = (e >> 1) * 8 + 2 * t + (e & 1);
+      if (alibi) sv[e] = fmaf(st.sl2, (float)((int32_t)off + key - st.m_pos), sv[e]);
+      if (key >= (int)nv || !live) sv[e] = -INFINITY;
+    }
+    float pm = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
+    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 1));
+    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 2));
+    if (pm > st.m_run) {  // the same in the 4 lanes of a row
+      const float alpha = st.m_run == -INFINITY ? 0.f : exp2f(st.m_run - pm);
+      st.l_run *= alpha;
+#pragma unroll
+      for (int nt = 0; nt < 16; ++nt) {
+        st.o[nt][0] *= alpha;
+        st.o[nt][1] *= alpha;
+      }
+      st.m_run = pm;
+    }
+    float pv[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      pv[e] = sv[e] == -INFINITY ? 0.f : exp2f(sv[e] - st.m_run);
+      st.l_run += pv[e];
+    }
+    const uint32_t pa[4] = {pack_bf16x2(pv[0], pv[1]), 0u, pack_bf16x2(pv[2], pv[3]), 0u};
+    // ---- O += P V: ldmatrix.trans matrix j covers keys 8 (j & 1) .. +7 and dims
+    // 16 dp + 8 (j >> 1) .. +7
+    const int vrow = (((lane >> 3) & 1) << 3) + (lane & 7), vhalf = lane >> 4;
+#pragma unroll
+    for (int dp = 0; dp < 8; ++dp) {
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_t(page_chunk(vpg, vrow, 2 * dp + vhalf), b0, b1, b2, b3);
+      mma_bf16_16816(st.o[2 * dp], pa, b0, b1);
+      mma_bf16_16816(st.o[2 * dp + 1], pa, b2, b3);
+    }
+  }
+}
+
+// The unit's partial (o / l, log2-sum-exp) to workspace slot `slot`.
+template <int GC>
+__device__ __forceinline__ void mma_flush(MmaWarpState<GC> &st, const DecodeParams &p,
+                                          int64_t slot, int lane) {
+  constexpr int D = 128;
+  const int g = lane >> 2, t = lane & 3;
+  float l = st.l_run;
+  l += __shfl_xor_sync(0xffffffffu, l, 1);
+  l += __shfl_xor_sync(0xffffffffu, l, 2);
+  if (g < GC) {
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    float *dst = p.ws_o + ((size_t)slot * GC + g) * D + 2 * t;
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt)
+      *reinterpret_cast<float2 *>(dst + nt * 8) =
+          make_float2(st.o[nt][0] * inv, st.o[nt][1] * inv);
+    if (t == 0) p.ws_lse[(size_t)slot * GC + g] = l > 0.f ? st.m_run + log2f(l) : -INFINITY;
+  }
+}
+
+// Loads page word w of the tensor-core kernels into stage `st` (K and V, two 16 x 64 boxes
+// each): bad words are flagged and replaced by block 0 (their keys are masked by the consumer).
+__device__ __forceinline__ void mma_issue_page(const MmaDecodeParams &mp, uint64_t w,
+                                               int32_t kv_head, uint8_t *st, uint64_t *bar) {
+  const DecodeParams &p = mp.d;
+  uint32_t blk = word_block(w);
+  if (blk >= (uint32_t)p.num_blocks || word_nvalid(w) > (uint32_t)kPage) {
+    set_error(p.err, LAZY_DEVERR_BAD_PAGE);
+    blk = 0;
+  }
+  const int row = (int)((blk * (uint32_t)p.hkv + (uint32_t)kv_head) * kPage);
+  mbar_arrive_expect_tx(bar, kMmaStageBytes);
+  tma2d_g2s(st, &mp.tm_k, 0, row, bar);
+  tma2d_g2s(st + 2048, &mp.tm_k, 64, row, bar);
+  tma2d_g2s(st + 4096, &mp.tm_v, 0, row, bar);
+  tma2d_g2s(st + 6144, &mp.tm_v, 64, row, bar);
+}
+
 template <int GC, int WARPS, int STAGES>
 __global__ void __launch_bounds__(WARPS * 32)
     decode_mma_kernel(const __grid_constant__ MmaDecodeParams mp) {
   using S = MmaSmem<STAGES>;
-  constexpr int D = 128;
   static_assert(GC >= 1 && GC <= 8, "a 16-row fragment holds up to 8 heads (hi and lo rows)");
   const DecodeParams &p = mp.d;
 
@@ -532,58 +709,22 @@ __global__ void __launch_bounds__(WARPS * 32)
   prod.init(x0, p.cu_pages, B, HV);
   uint64_t w_next = 0;
   if (lane == 0) w_next = p.words[prod.wbase + prod.pg];
-  auto issue = [&](int s) {
-    const uint64_t w = w_next;
-    uint32_t blk = word_block(w);
-    if (blk >= (uint32_t)p.num_blocks || word_nvalid(w) > (uint32_t)kPage) {
-      set_error(p.err, LAZY_DEVERR_BAD_PAGE);
-      blk = 0;
-    }
-    meta_w[s] = w;
-    meta_u[s] = prod.b * HV + prod.hv;
-    const int row = (int)((blk * (uint32_t)p.hkv + (uint32_t)(prod.hv / p.chunks)) * kPage);
-    uint8_t *st = stage + s * kMmaStageBytes;
-    mbar_arrive_expect_tx(&bars[s], kMmaStageBytes);
-    tma2d_g2s(st, &mp.tm_k, 0, row, &bars[s]);
-    tma2d_g2s(st + 2048, &mp.tm_k, 64, row, &bars[s]);
-    tma2d_g2s(st + 4096, &mp.tm_v, 0, row, &bars[s]);
-    tma2d_g2s(st + 6144, &mp.tm_v, 64, row, &bars[s]);
-  };
   int64_t issued = 0;
   auto issue_next = [&](int s) {
-    if (lane == 0) issue(s);
+    if (lane == 0) {
+      meta_w[s] = w_next;
+      meta_u[s] = prod.b * HV + prod.hv;
+      mma_issue_page(mp, w_next, prod.hv / p.chunks, stage + s * kMmaStageBytes, &bars[s]);
+    }
     prod.advance(p.cu_pages, B, HV);
     ++issued;
     if (lane == 0 && issued < n_mine) w_next = p.words[prod.wbase + prod.pg];
   };
   for (int s = 0; s < STAGES && s < n_mine; ++s) issue_next(s);
 
-  const int g = lane >> 2, t = lane & 3;  // fragment row group and column pair
-  const bool live = g < GC;               // this thread's row is a real query head
-  const bool alibi = p.slopes != nullptr;
-  uint32_t qa[8][4];      // A fragments of the rotated, scaled query (hi rows g, lo rows g + 8)
-  uint32_t qraw[16];      // raw query pairs of this thread: dims 16ks + 2t + {0,1}, {8,9}
-  float o[16][4];         // O accumulator (rows g valid; rows g + 8 stay zero)
-  float m_run = -INFINITY, l_run = 0.f, sl2 = 0.f;
-  int32_t cur_unit = -1, cur_b = 0, m_pos = 0;
-  uint32_t cur_off = 0xFFFFFFFFu;
+  MmaWarpState<GC> st;
+  int32_t cur_unit = -1;
   bool timed_out = false;
-
-  auto flush = [&](int32_t unit) {
-    float l = l_run;
-    l += __shfl_xor_sync(0xffffffffu, l, 1);
-    l += __shfl_xor_sync(0xffffffffu, l, 2);
-    const int64_t slot = (int64_t)unit + wg;
-    if (live) {
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      float *dst = p.ws_o + ((size_t)slot * GC + g) * D + 2 * t;
-#pragma unroll
-      for (int nt = 0; nt < 16; ++nt)
-        *reinterpret_cast<float2 *>(dst + nt * 8) = make_float2(o[nt][0] * inv, o[nt][1] * inv);
-      if (t == 0) p.ws_lse[(size_t)slot * GC + g] = l > 0.f ? m_run + log2f(l) : -INFINITY;
-    }
-  };
-
   for (int64_t i = 0; i < n_mine; ++i) {
     const int s = (int)(i % STAGES);
     const uint32_t par = (uint32_t)((i / STAGES) & 1);
@@ -598,127 +739,127 @@ __global__ void __launch_bounds__(WARPS * 32)
     const uint64_t word = meta_w[s];
     const int32_t unit = meta_u[s];
     if (unit != cur_unit) {
-      if (cur_unit >= 0) flush(cur_unit);
+      if (cur_unit >= 0) mma_flush(st, p, (int64_t)cur_unit + wg, lane);
       cur_unit = unit;
-      cur_b = unit / HV;
-      const int32_t hv = unit % HV;
-      m_pos = p.q_pos[cur_b];
-      const __nv_bfloat16 *q = reinterpret_cast<const __nv_bfloat16 *>(p.q) +
-                               ((size_t)cur_b * p.hq + hv * GC + (live ? g : 0)) * D + 2 * t;
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        qraw[2 * ks] = live ? *reinterpret_cast<const uint32_t *>(q + 16 * ks) : 0u;
-        qraw[2 * ks + 1] = live ? *reinterpret_cast<const uint32_t *>(q + 16 * ks + 8) : 0u;
-      }
-      sl2 = (alibi && live) ? p.slopes[hv * GC + g] * 1.4426950408889634f : 0.f;
-      m_run = -INFINITY;
-      l_run = 0.f;
-#pragma unroll
-      for (int nt = 0; nt < 16; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) o[nt][e] = 0.f;
-      cur_off = 0xFFFFFFFFu;
+      mma_begin_unit(st, p, unit / HV, unit % HV, lane);
     }
-    const uint32_t nv = word_nvalid(word);
-    const bool bad = word_block(word) >= (uint32_t)p.num_blocks || nv > (uint32_t)kPage;
-    const uint32_t off = word_offset(word);
-    const uint32_t rot_off = alibi ? 0u : off;
-    if (!bad) {
-      if (rot_off != cur_off) {
-        // q <- R(m - o) q (identity for ALiBi), scaled into the log2 domain, split hi + lo
-        cur_off = rot_off;
-        const int64_t delta = alibi ? 0 : (int64_t)m_pos - (int64_t)off;
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {  // dims d < 64 pair with d + 64 (k-step ks + 4)
-#pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
-            const uint32_t lo_raw = qraw[2 * ks + h2], hi_raw = qraw[2 * (ks + 4) + h2];
-            float x[2], y[2];
-            x[0] = __uint_as_float(lo_raw << 16);
-            x[1] = __uint_as_float(lo_raw & 0xFFFF0000u);
-            y[0] = __uint_as_float(hi_raw << 16);
-            y[1] = __uint_as_float(hi_raw & 0xFFFF0000u);
-            float rx[2], ry[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int d = 16 * ks + 8 * h2 + 2 * t + e;
-              float cs, sn;
-              rope_cos_sin(delta, p.turn[d], cs, sn);
-              rx[e] = (x[e] * cs - y[e] * sn) * p.scale_log2;
-              ry[e] = (x[e] * sn + y[e] * cs) * p.scale_log2;
-            }
-            const uint32_t xh = pack_bf16x2(rx[0], rx[1]), yh = pack_bf16x2(ry[0], ry[1]);
-            const uint32_t xl = pack_bf16x2(rx[0] - __uint_as_float(xh << 16),
-                                            rx[1] - __uint_as_float(xh & 0xFFFF0000u));
-            const uint32_t yl = pack_bf16x2(ry[0] - __uint_as_float(yh << 16),
-                                            ry[1] - __uint_as_float(yh & 0xFFFF0000u));
-            // fragment registers: [0] row g cols 2t.., [1] row g+8, [2] row g cols 2t+8..,
-            // [3] row g+8 cols 2t+8..
-            qa[ks][2 * h2] = live ? xh : 0u;
-            qa[ks][2 * h2 + 1] = live ? xl : 0u;
-            qa[ks + 4][2 * h2] = live ? yh : 0u;
-            qa[ks + 4][2 * h2 + 1] = live ? yl : 0u;
-          }
-        }
-      }
-      const uint32_t kpg = smem_u32(stage + s * kMmaStageBytes);
-      const uint32_t vpg = kpg + 4096;
-      // ---- S = Q K^T: ldmatrix matrix j = lane / 8 covers keys 8 (j >> 1) .. +7 and
-      // dims 16 ks + 8 (j & 1) .. +7; row = lane % 8
-      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      const int lrow = ((lane >> 4) << 3) + (lane & 7), lhalf = (lane >> 3) & 1;
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(page_chunk(kpg, lrow, 2 * ks + lhalf), b0, b1, b2, b3);
-        mma_bf16_16816(sc[0], qa[ks], b0, b1);
-        mma_bf16_16816(sc[1], qa[ks], b2, b3);
-      }
-      // scores of keys 2t, 2t+1 (n-tile 0) and 8+2t, 9+2t (n-tile 1): hi row + lo row
-      float sv[4] = {sc[0][0] + sc[0][2], sc[0][1] + sc[0][3], sc[1][0] + sc[1][2],
-                     sc[1][1] + sc[1][3]};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int key = (e >> 1) * 8 + 2 * t + (e & 1);
-        if (alibi) sv[e] = fmaf(sl2, (float)((int32_t)off + key - m_pos), sv[e]);
-        if (key >= (int)nv || !live) sv[e] = -INFINITY;
-      }
-      float pm = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
-      pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 1));
-      pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 2));
-      if (pm > m_run) {  // the same in the 4 lanes of a row
-        const float alpha = m_run == -INFINITY ? 0.f : exp2f(m_run - pm);
-        l_run *= alpha;
-#pragma unroll
-        for (int nt = 0; nt < 16; ++nt) {
-          o[nt][0] *= alpha;
-          o[nt][1] *= alpha;
-        }
-        m_run = pm;
-      }
-      float pv[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        pv[e] = sv[e] == -INFINITY ? 0.f : exp2f(sv[e] - m_run);
-        l_run += pv[e];
-      }
-      const uint32_t pa[4] = {pack_bf16x2(pv[0], pv[1]), 0u, pack_bf16x2(pv[2], pv[3]), 0u};
-      // ---- O += P V: ldmatrix.trans matrix j covers keys 8 (j & 1) .. +7 and dims
-      // 16 dp + 8 (j >> 1) .. +7
-      const int vrow = (((lane >> 3) & 1) << 3) + (lane & 7), vhalf = lane >> 4;
-#pragma unroll
-      for (int dp = 0; dp < 8; ++dp) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(page_chunk(vpg, vrow, 2 * dp + vhalf), b0, b1, b2, b3);
-        mma_bf16_16816(o[2 * dp], pa, b0, b1);
-        mma_bf16_16816(o[2 * dp + 1], pa, b2, b3);
-      }
-    }
+    mma_attend_page(st, p, word, smem_u32(stage + s * kMmaStageBytes), lane);
     __syncwarp();
     if (issued < n_mine) issue_next(s);
   }
   cudaTriggerProgrammaticLaunchCompletion();
-  if (!timed_out && cur_unit >= 0) flush(cur_unit);
+  if (!timed_out && cur_unit >= 0) mma_flush(st, p, (int64_t)cur_unit + wg, lane);
+}
+
+// Groups of more than 8 query heads per kv head (chunks == WARPS, e.g. MQA 32/1): the CTA's
+// warps are the chunks of one kv head and share one page ring, so each K/V page is loaded into
+// shared memory once for all of them instead of once per chunk. Units are (request, kv head);
+// the flattened (request, kv head, page) sequence is cut into equal ranges, one per CTA. Warp 0
+// lane 0 issues; a stage is refilled once every warp has arrived on its empty barrier. Warp w
+// leaves its partial of virtual head kv head * WARPS + w at slot (unit + CTA) * WARPS + w.
+template <int STAGES>
+struct MmaGroupSmem {
+  static constexpr int kStage = 0;                                  // STAGES x 8 KB
+  static constexpr int kFull = kStage + STAGES * kMmaStageBytes;    // uint64 [STAGES]
+  static constexpr int kEmpty = kFull + STAGES * 8;                 // uint64 [STAGES]
+  static constexpr int kWord = kEmpty + STAGES * 8;                 // uint64 [STAGES]
+  static constexpr int kUnit = kWord + STAGES * 8;                  // int32 [STAGES]
+  static constexpr int kBytes = kUnit + STAGES * 4 + 1024;          // + alignment slack
+};
+
+template <int GC, int WARPS, int STAGES>
+__global__ void __launch_bounds__(WARPS * 32)
+    decode_mma_group_kernel(const __grid_constant__ MmaDecodeParams mp) {
+  using S = MmaGroupSmem<STAGES>;
+  const DecodeParams &p = mp.d;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint8_t *base = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t *stage = base + S::kStage;
+  uint64_t *full = reinterpret_cast<uint64_t *>(base + S::kFull);
+  uint64_t *empty = reinterpret_cast<uint64_t *>(base + S::kEmpty);
+  uint64_t *meta_w = reinterpret_cast<uint64_t *>(base + S::kWord);
+  int32_t *meta_u = reinterpret_cast<int32_t *>(base + S::kUnit);
+
+  cudaGridDependencySynchronize();
+  const int32_t B = p.batch, HU = p.hkv;  // units: (request, kv head)
+  const int64_t N = (int64_t)HU * p.cu_pages[B];
+  const int64_t CT = gridDim.x, cg = blockIdx.x;
+  const int64_t x0 = cg * N / CT, x1 = (cg + 1) * N / CT;
+  if (x0 >= x1) {  // the whole CTA has no pages
+    cudaTriggerProgrammaticLaunchCompletion();
+    return;
+  }
+  const int64_t n_mine = x1 - x0;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], WARPS);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  // producer state (warp 0)
+  Walker prod;
+  uint64_t w_next = 0;
+  int64_t issued = 0;
+  if (warp == 0) {
+    prod.init(x0, p.cu_pages, B, HU);
+    if (lane == 0) w_next = p.words[prod.wbase + prod.pg];
+  }
+  auto issue_next = [&](int s) {
+    if (lane == 0) {
+      meta_w[s] = w_next;
+      meta_u[s] = prod.b * HU + prod.hv;
+      mma_issue_page(mp, w_next, prod.hv, stage + s * kMmaStageBytes, &full[s]);
+    }
+    prod.advance(p.cu_pages, B, HU);
+    ++issued;
+    if (lane == 0 && issued < n_mine) w_next = p.words[prod.wbase + prod.pg];
+  };
+  if (warp == 0)
+    for (int s = 0; s < STAGES && s < n_mine; ++s) issue_next(s);
+
+  MmaWarpState<GC> st;
+  int32_t cur_unit = -1;
+  bool timed_out = false;
+  for (int64_t i = 0; i < n_mine; ++i) {
+    const int s = (int)(i % STAGES);
+    const uint32_t par = (uint32_t)((i / STAGES) & 1);
+    if (!mbar_wait(&full[s], par, p.wait_ns)) {
+      if (lane == 0) set_error(p.err, LAZY_DEVERR_TIMEOUT);
+      timed_out = true;
+      break;
+    }
+    const uint64_t word = meta_w[s];
+    const int32_t unit = meta_u[s];
+    if (unit != cur_unit) {
+      if (cur_unit >= 0) mma_flush(st, p, ((int64_t)cur_unit + cg) * WARPS + warp, lane);
+      cur_unit = unit;
+      mma_begin_unit(st, p, unit / HU, (unit % HU) * WARPS + warp, lane);
+    }
+    mma_attend_page(st, p, word, smem_u32(stage + s * kMmaStageBytes), lane);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    if (warp == 0 && issued < n_mine) {
+      // every warp is done with this stage before it is refilled
+      if (!mbar_wait(&empty[s], par, p.wait_ns)) {
+        if (lane == 0) set_error(p.err, LAZY_DEVERR_TIMEOUT);
+        timed_out = true;
+        break;
+      }
+      issue_next(s);
+    }
+  }
+  if (warp == 0) {
+    // copies still in flight land before the CTA may exit
+    for (int64_t k = issued - STAGES; k < issued; ++k)
+      if (k >= 0) mbar_wait(&full[k % STAGES], (uint32_t)((k / STAGES) & 1), p.wait_ns);
+  }
+  cudaTriggerProgrammaticLaunchCompletion();
+  if (!timed_out && cur_unit >= 0)
+    mma_flush(st, p, ((int64_t)cur_unit + cg) * WARPS + warp, lane);
 }
 
 struct CombineParams {
@@ -728,7 +869,8 @@ struct CombineParams {
   void *out;
   float *lse;
   int32_t batch, hq, hv;
-  int64_t warps;  // total warps of the decode launch
+  int64_t warps;  // ranges of the decode launch: its warps, or its CTAs for the group kernel
+  int32_t ch;     // virtual heads sharing one range (the group kernel's warps), else 1
 };
 
 // One CTA per unit: merges the unit's pieces (slots unit + w for the warps w whose ranges
@@ -738,8 +880,11 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
   cudaGridDependencySynchronize();  // partials of the decode kernel launched just before
   const int32_t u = blockIdx.x;
   const int32_t b = u / p.hv, hv = u % p.hv;
+  // the partition's units: (request, virtual head), or (request, kv head) shared by ch chunks
+  const int32_t hu = p.hv / p.ch, kv = hv / p.ch, chunk = hv % p.ch;
+  const int32_t ub = b * hu + kv;
   const int32_t wbase = p.cu_pages[b], np = p.cu_pages[b + 1] - wbase;
-  const int64_t N = (int64_t)p.hv * p.cu_pages[p.batch];
+  const int64_t N = (int64_t)hu * p.cu_pages[p.batch];
   const int64_t W = p.warps;
   T *out = reinterpret_cast<T *>(p.out);
   // With at least one page per warp (N >= W) no warp's range is empty, and the per-slot test
@@ -747,7 +892,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
   const bool dense = N >= W;
   int64_t wf = 0, wl = -1;
   if (np > 0) {
-    const int64_t S = (int64_t)p.hv * wbase + (int64_t)hv * np, E = S + np;
+    const int64_t S = (int64_t)hu * wbase + (int64_t)kv * np, E = S + np;
     wf = ((S + 1) * W + N - 1) / N - 1;
     wl = (E * W + N - 1) / N - 1;
   }
@@ -763,9 +908,9 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
       for (int k = 0; k < 8; ++k) {
         const int64_t w = w0 + k;
         const bool use = w <= wl && (dense || w * N / W != (w + 1) * N / W);
-        lv[k] = use ? p.ws_lse[(size_t)(u + w) * GC + g] : -INFINITY;
-        ov[k] = use ? *reinterpret_cast<const float4 *>(p.ws_o + ((size_t)(u + w) * GC + g) * D +
-                                                        d4 * 4)
+        const size_t slot = (size_t)(ub + w) * p.ch + chunk;
+        lv[k] = use ? p.ws_lse[slot * GC + g] : -INFINITY;
+        ov[k] = use ? *reinterpret_cast<const float4 *>(p.ws_o + (slot * GC + g) * D + d4 * 4)
                     : make_float4(0.f, 0.f, 0.f, 0.f);
       }
       float bm = lv[0];
@@ -826,29 +971,43 @@ bool use_mma(const lazy_pool *p) {
   return p->decode_kernel != LAZY_DECODE_SIMT && p->dtype == LAZY_DTYPE_BF16 && p->d == 128;
 }
 
+constexpr int kGroupStages = 4;  // page ring of the group kernel
+constexpr int kGroupSmem = MmaGroupSmem<kGroupStages>::kBytes;
+
 template <int GC, int STAGES>
 struct MmaLaunch {
   static constexpr int kSmem = MmaSmem<STAGES>::kBytes * kWarps + 1024;  // + alignment slack
-  static int ctas_per_sm() {
-    static int cached = -1;
-    if (cached < 0) {
-      auto fn = decode_mma_kernel<GC, kWarps, STAGES>;
-      if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
+  // groups of 4 chunks of 8 query heads (e.g. MQA 32/1) share one page ring per CTA
+  static bool grouped(int32_t chunks) { return GC == 8 && chunks == kWarps; }
+  template <typename F>
+  static int occupancy(F fn, int smem, int *cached) {
+    if (*cached < 0) {
+      if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
           cudaSuccess)
         return -1;
       int n = 0;
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kWarps * 32, kSmem) !=
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kWarps * 32, smem) !=
           cudaSuccess)
         return -1;
-      cached = std::max(1, n);
+      *cached = std::max(1, n);
     }
-    return cached;
+    return *cached;
+  }
+  static int ctas_per_sm(int32_t chunks) {
+    static int cached = -1, cached_group = -1;
+    if constexpr (GC == 8) {
+      if (grouped(chunks))
+        return occupancy(decode_mma_group_kernel<GC, kWarps, kGroupStages>, kGroupSmem,
+                         &cached_group);
+    }
+    return occupancy(decode_mma_kernel<GC, kWarps, STAGES>, kSmem, &cached);
   }
   static int run(lazy_pool *pl, const DecodeParams &dp, const CombineParams &cp, int grid,
                  cudaStream_t s) {
     int rc = ensure_pool_tmaps(pl);
     if (rc != LAZY_OK) return rc;
-    if (ctas_per_sm() < 0) return record_cuda(cudaGetLastError(), "decode_mma_kernel set-up");
+    if (ctas_per_sm(dp.chunks) < 0)
+      return record_cuda(cudaGetLastError(), "decode_mma_kernel set-up");
     MmaDecodeParams mp;
     mp.d = dp;
     {
@@ -856,10 +1015,22 @@ struct MmaLaunch {
       memcpy(&mp.tm_k, pl->tmap_k, sizeof(CUtensorMap));
       memcpy(&mp.tm_v, pl->tmap_v, sizeof(CUtensorMap));
     }
-    LAZY_CUDA_TRY(launch_pdl(decode_mma_kernel<GC, kWarps, STAGES>, grid, kWarps * 32, kSmem,
-                             s, mp));
+    CombineParams c2 = cp;
+    bool launched = false;
+    if constexpr (GC == 8) {
+      if (grouped(dp.chunks)) {
+        LAZY_CUDA_TRY(launch_pdl(decode_mma_group_kernel<GC, kWarps, kGroupStages>, grid,
+                                 kWarps * 32, kGroupSmem, s, mp));
+        c2.warps = grid;  // one range per CTA, shared by its kWarps chunks
+        c2.ch = kWarps;
+        launched = true;
+      }
+    }
+    if (!launched)
+      LAZY_CUDA_TRY(launch_pdl(decode_mma_kernel<GC, kWarps, STAGES>, grid, kWarps * 32, kSmem,
+                               s, mp));
     LAZY_CUDA_TRY(launch_pdl(combine_kernel<__nv_bfloat16, 128, GC>, dp.batch * dp.hv, 128, 0,
-                             s, cp));
+                             s, c2));
     return LAZY_OK;
   }
 };
@@ -869,9 +1040,9 @@ struct DecodeLaunch {
   using S = DecodeSmem<T, D, GC, STAGES>;
   static constexpr int kSmem = S::kBytes * kWarps;
   static constexpr bool kHasMma = std::is_same<T, __nv_bfloat16>::value && D == 128;
-  static int ctas_per_sm(const lazy_pool *pl) {
+  static int ctas_per_sm(const lazy_pool *pl, int32_t chunks) {
     if constexpr (kHasMma) {
-      if (use_mma(pl)) return MmaLaunch<GC, STAGES>::ctas_per_sm();
+      if (use_mma(pl)) return MmaLaunch<GC, STAGES>::ctas_per_sm(chunks);
     }
     return simt_ctas_per_sm();
   }
@@ -937,13 +1108,13 @@ int plan_groups(int32_t hq, int32_t hkv, int32_t *gc, int32_t *chunks) {
   return LAZY_OK;
 }
 
-int decode_grid(lazy_pool *p, int32_t gc, int32_t grid_ctas, int *grid) {
+int decode_grid(lazy_pool *p, int32_t gc, int32_t chunks, int32_t grid_ctas, int *grid) {
   if (grid_ctas > 0) {
     *grid = grid_ctas;
     return LAZY_OK;
   }
-  const int per_sm = with_decode_shape(p->dtype, p->d, gc,
-                                       [&](auto L) { return decltype(L)::ctas_per_sm(p); });
+  const int per_sm = with_decode_shape(
+      p->dtype, p->d, gc, [&](auto L) { return decltype(L)::ctas_per_sm(p, chunks); });
   if (per_sm <= 0) {
     record_msg("decode kernel occupancy query failed");
     return LAZY_ERR_CUDA;
@@ -967,7 +1138,7 @@ extern "C" int lazy_decode_workspace_bytes(lazy_pool *p, int32_t batch, int32_t 
   rc = ensure_device(p);
   if (rc != LAZY_OK) return rc;
   int grid;
-  rc = decode_grid(p, gc, grid_ctas, &grid);
+  rc = decode_grid(p, gc, chunks, grid_ctas, &grid);
   if (rc != LAZY_OK) return rc;
   const size_t slots = (size_t)batch * p->hkv * chunks + (size_t)grid * kWarps;
   *bytes = slots * gc * ((size_t)p->d + 1) * sizeof(float) + 256;
@@ -994,7 +1165,7 @@ extern "C" int lazy_attn_decode(lazy_pool *p, const void *q, const int32_t *q_po
   if (rc != LAZY_OK) return rc;
   if (workspace_bytes < need) return LAZY_ERR_INVALID_ARG;
   int grid;
-  rc = decode_grid(p, gc, grid_ctas, &grid);
+  rc = decode_grid(p, gc, chunks, grid_ctas, &grid);
   if (rc != LAZY_OK) return rc;
   const int32_t hv = p->hkv * chunks;
   const size_t slots = (size_t)batch * hv + (size_t)grid * kWarps;
@@ -1028,6 +1199,7 @@ extern "C" int lazy_attn_decode(lazy_pool *p, const void *q, const int32_t *q_po
   cp.hq = num_q_heads;
   cp.hv = hv;
   cp.warps = (int64_t)grid * kWarps;
+  cp.ch = 1;
   cudaStream_t s = (cudaStream_t)stream;
   return with_decode_shape(p->dtype, p->d, gc,
                            [&](auto L) { return decltype(L)::run(p, dp, cp, grid, s); });
@@ -1095,7 +1267,7 @@ extern "C" int lazy_attn_decode_noalloc(lazy_pool *p, const void *q, const int32
   int rc = plan_groups(num_q_heads, p->hkv, &gc, &chunks);
   if (rc != LAZY_OK) return rc;
   int grid;
-  rc = decode_grid(p, gc, grid_ctas, &grid);
+  rc = decode_grid(p, gc, chunks, grid_ctas, &grid);
   if (rc != LAZY_OK) return rc;
   const int32_t hv = p->hkv * chunks;
   const size_t slots = (size_t)batch * hv + (size_t)grid * kWarps;
@@ -1137,6 +1309,7 @@ extern "C" int lazy_attn_decode_noalloc(lazy_pool *p, const void *q, const int32
   cp.hq = num_q_heads;
   cp.hv = hv;
   cp.warps = (int64_t)grid * kWarps;
+  cp.ch = 1;
   cudaStream_t s = (cudaStream_t)stream;
   return with_decode_shape(p->dtype, p->d, gc,
                            [&](auto L) { return decltype(L)::run(p, dp, cp, grid, s); });
