@@ -724,8 +724,8 @@ def mqa_bench(args, flush, stream, hbm_peak, tc_peak):
                      "ms_dist": _dist_ms(ms), "frac": round(kv / (med * 1e-3) / 1e9 / hbm_peak, 4),
                      "kv_bytes_per_step": kv,
                      "tflops": round(flops / (med * 1e-3) / 1e12, 2),
-                     "note": "32 FLOP per K/V byte; each page is read once per 8-head chunk "
-                             "(4 chunks), so the kernel, not HBM, bounds it"}
+                     "note": "32 FLOP per K/V byte; the 4 chunks of 8 heads share each page in "
+                             "shared memory; the per-page MMA chain, not HBM, bounds it"}
     res.pool.close()
     del res, db, dws
     torch.cuda.empty_cache()
