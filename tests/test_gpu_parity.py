@@ -212,6 +212,33 @@ def test_decode_any_grid_same_result(pk, grid):
     _check_decode(wl, out, lse)
 
 
+@pytest.mark.parametrize("grid", [1, 3, 7, 100, 1000])
+def test_mqa_group_kernel_any_grid(pk, grid):
+    # 32 query heads over 1 kv head: the group kernel (4 warps = 4 chunks of 8 heads sharing
+    # one page ring per CTA) and the combine's shared-range slots; 1000 CTAs exceed the pages
+    # (empty ranges)
+    wl = W.decode_workload(batch=5, docs_per_req=3, doc_len=100, n_pool=6, question=21, Hkv=1,
+                           seed=2, name="mqa_small")
+    _, _, out, lse = _decode(pk, wl, grid_ctas=grid)
+    _check_decode(wl, out, lse)
+
+
+def test_mqa_decode_full_size_sampled(pk):
+    # decode_b64 shapes with Hkv 1 (the bench's MQA line), pages aligned, default grid
+    H = _h()
+    wl = W.decode_workload(Hkv=1, name="decode_b64_mqa")
+    src = H.DeviceSource(wl)
+    res = H.build_resident(wl, src, drop_raw=False)
+    db = H.decode_batch(wl, res, src, align_shared=True)
+    out, lse = pk.lazy_attn_decode(res.pool, db.q, db.q_pos, db.words, db.cu_pages,
+                                   sm_scale=wl.sm_scale)
+    torch.cuda.synchronize()
+    assert pk.lazy_get_device_error(res.pool) == 0
+    reqs = [0, 31, 63]
+    _check_decode(wl, out.float().cpu().numpy()[reqs], lse.cpu().numpy()[reqs], reqs=reqs,
+                  src=src.host_view())
+
+
 def test_decode_request_without_keys(pk):
     H = _h()
     wl = _edge_decode_workload(128, 8, 2, "bf16")
