@@ -494,6 +494,13 @@ __device__ __forceinline__ uint32_t page_chunk(uint32_t page, int row, int chunk
   return page + (chunk >> 3) * 2048 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4);
 }
 
+// 2^x in one MUFU instruction (arguments <= 0 here; the weights are rounded to bf16 next).
+__device__ __forceinline__ float ex2_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Per-warp attention state of the tensor-core decode over one unit (request, virtual head).
 template <int GC>
 struct MmaWarpState {
@@ -605,7 +612,7 @@ __device__ __forceinline__ void mma_attend_page(MmaWarpState<GC> &st, const Deco
     pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 1));
     pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 2));
     if (pm > st.m_run) {  // the same in the 4 lanes of a row
-      const float alpha = st.m_run == -INFINITY ? 0.f : exp2f(st.m_run - pm);
+      const float alpha = st.m_run == -INFINITY ? 0.f : ex2_fast(st.m_run - pm);
       st.l_run *= alpha;
 #pragma unroll
       for (int nt = 0; nt < 16; ++nt) {
@@ -617,7 +624,7 @@ __device__ __forceinline__ void mma_attend_page(MmaWarpState<GC> &st, const Deco
     float pv[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      pv[e] = sv[e] == -INFINITY ? 0.f : exp2f(sv[e] - st.m_run);
+      pv[e] = sv[e] == -INFINITY ? 0.f : ex2_fast(sv[e] - st.m_run);
       st.l_run += pv[e];
     }
     const uint32_t pa[4] = {pack_bf16x2(pv[0], pv[1]), 0u, pack_bf16x2(pv[2], pv[3]), 0u};
