@@ -273,6 +273,39 @@ def test_decode_shift_invariance(pk):
     _check_decode(wl, out1, lse1)
 
 
+@pytest.mark.parametrize("kind", ["simt", "auto"])
+def test_decode_offsets_near_the_page_word_limit(pk, kind):
+    # every position moved up to just below 2^26 (the page word's 26-bit offset field): the
+    # fixed-point angles stay exact there, and the result matches the unshifted one and the oracle
+    H = _h()
+    wl = _edge_decode_workload(128, 32, 8, "bf16")
+    top = max(max(r.offsets) + wl.doc_len for r in wl.requests)
+    top = max(top, max(r.priv_offset + r.priv_len for r in wl.requests))
+    c = (1 << 26) - 1 - top
+    src = H.HostSource(wl)
+    res = H.build_resident(wl, src, resident_pool=False)
+    pk.lazy_pool_set_decode_kernel(res.pool, pk.LAZY_DECODE_SIMT if kind == "simt"
+                                   else pk.LAZY_DECODE_AUTO)
+    db = H.decode_batch(wl, res, src)
+    o0, l0 = pk.lazy_attn_decode(res.pool, db.q, db.q_pos, db.words, db.cu_pages,
+                                 sm_scale=wl.sm_scale)
+    for r in wl.requests:
+        r.offsets = [o + c for o in r.offsets]
+        r.priv_offset += c
+        r.m += c
+    db1 = H.decode_batch(wl, res, src)
+    o1, l1 = pk.lazy_attn_decode(res.pool, db1.q, db1.q_pos, db1.words, db1.cu_pages,
+                                 sm_scale=wl.sm_scale)
+    torch.cuda.synchronize()
+    assert pk.lazy_get_device_error(res.pool) == 0
+    words = db1.words.cpu().numpy().view(np.uint64)
+    assert max(int(w) >> 32 & ((1 << 26) - 1) for w in words) > 1 << 25
+    o0, o1 = o0.float().cpu().numpy(), o1.float().cpu().numpy()
+    l0, l1 = l0.cpu().numpy(), l1.cpu().numpy()
+    assert np.abs(o0 - o1).max() <= 2e-2 and np.abs(l0 - l1).max() <= 1e-3
+    _check_decode(wl, o1, l1)
+
+
 def test_decode_after_token_append(pk):
     # the bench's step: write the new token's k/v into its slot, then decode
     H = _h()
@@ -450,6 +483,21 @@ def test_prefill_tensor_core_parity(pk, Hq, Hkv):
     wl = _edge_prefill_workload(128, Hq, Hkv, "bf16")
     _, pb, out, lse = _prefill(pk, wl, pk.LAZY_PREFILL_TC)
     _check_prefill(wl, pb, out, lse, lse_tol=TC_EDGE_LSE_TOL)
+
+
+@pytest.mark.parametrize("flags", ["tc", "simt"])
+def test_prefill_offsets_near_the_page_word_limit(pk, flags):
+    # documents and question moved up to just below 2^26 (the offset field's limit)
+    H = _h()
+    wl = _edge_prefill_workload(128, 32, 8, "bf16")
+    top = max(max(max(r.offsets) + wl.doc_len, r.q_pos0 + r.T) for r in wl.requests)
+    c = (1 << 26) - 1 - top
+    for r in wl.requests:
+        r.offsets = [o + c for o in r.offsets]
+        r.q_pos0 += c
+    fl = pk.LAZY_PREFILL_TC if flags == "tc" else pk.LAZY_PREFILL_SIMT
+    _, pb, out, lse = _prefill(pk, wl, fl)
+    _check_prefill(wl, pb, out, lse, lse_tol=TC_EDGE_LSE_TOL if flags == "tc" else None)
 
 
 def test_prefill_tensor_core_matches_cuda_core_kernel(pk):
