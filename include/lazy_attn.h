@@ -223,9 +223,11 @@ int lazy_attn_decode(lazy_pool *pool, const void *d_q, const int32_t *d_q_pos,
                      lazy_stream_t stream);
 
 /*
- * Test hook: y[i] = 2^x[i] computed by the FMA-pipe exponential that the tensor-core prefill
- * uses for part of its softmax weights (range reduction to [-1/2, 1/2] plus a fitted degree-5
- * polynomial). d_x, d_y: device float [n]. Inputs below -126 return ~1e-38.
+ * Test hook: y[i] = 2^x[i] computed by the FMA-pipe exponential (range reduction to
+ * [-1/2, 1/2] plus a fitted degree-5 polynomial) that the tensor-core prefill can use for part
+ * of its softmax weights when built with LAZY_POLY_EVERY > 0. The default build keeps every
+ * exponential on the MUFU unit (offloading measured slower on GB300). d_x, d_y: device float
+ * [n]. Inputs below -126 return ~1e-38.
  */
 int lazy_debug_exp2(const float *d_x, float *d_y, int32_t n, lazy_stream_t stream);
 
