@@ -96,9 +96,12 @@ def test_prefill_append_matches_prefill_and_encode(pk):
         assert torch.equal(vp[n_full, :, :rows], vr[n_full, :, :rows])
 
 
-def test_chain_decode_steps_match_oracle(pk):
+@pytest.mark.parametrize("align", [False, True])
+def test_chain_decode_steps_match_oracle(pk, align):
     """Prefill with append, then N_STEPS decode steps (token append + decode); every step of
-    every request and head against the oracle's decode over documents + question + tokens."""
+    every request and head against the oracle's decode over documents + question + tokens, with
+    each step's page table in context order or with shared documents aligned (as the bench
+    runs it)."""
     wl = W.prefill_workload(batch=3, docs_per_req=2, doc_len=200, n_pool=6, T=40, Hq=8, Hkv=2)
     H, src, res, ch = _chain_setup(pk, wl)
     pb = ch.pb
@@ -106,7 +109,7 @@ def test_chain_decode_steps_match_oracle(pk):
                                 pb.cu_pages, pb.max_q_len, ch.append_slots, ch.append_local_pos,
                                 sm_scale=wl.sm_scale)
     for step in range(N_STEPS):
-        db = H.chain_step_batch(wl, res, ch, step, src)
+        db = H.chain_step_batch(wl, res, ch, step, src, align_shared=align)
         pk.kv_pool_write_tokens(res.pool, db.new_k, db.new_v, db.slot_mapping, db.local_pos)
         out, lse = pk.lazy_attn_decode(res.pool, db.q, db.q_pos, db.words, db.cu_pages,
                                        sm_scale=wl.sm_scale)

@@ -60,3 +60,13 @@ def test_decode_workload_alignment_and_words():
     assert np.array_equal(cu0, cu1)
     for b in range(len(reqs)):
         assert sorted(w0[cu0[b]:cu0[b + 1]].tolist()) == sorted(w1[cu1[b]:cu1[b + 1]].tolist())
+
+
+def test_degenerate_batches():
+    assert pk.align_shared_segments([]) == []
+    one = [[_segs(1), _segs(2), _segs(3)]]
+    assert pk.align_shared_segments(one) == one              # nothing shared: order kept
+    reqs = [[], [_segs(7)], []]
+    assert pk.align_shared_segments(reqs) == reqs             # empty requests stay empty
+    uniq = [[_segs(10 * b + i) for i in range(3)] for b in range(4)]
+    assert pk.align_shared_segments(uniq) == uniq             # all unique: order kept
