@@ -195,6 +195,14 @@ def _cpu_model():
 TIMED_WINDOWS = []   # host wall-clock spans of every timed region, for the clock samples
 
 
+def _prefill_workspace(pk, pool, pb, hq):
+    """The prefill's scratch, allocated once outside the timed region."""
+    import torch
+    n = pk.lazy_prefill_workspace_bytes(pool, int(pb.cu_q.shape[0]) - 1, pb.total_q, pb.max_q_len,
+                                        hq)
+    return torch.empty(max(n, 1), dtype=torch.uint8, device="cuda")
+
+
 def _timed_steps(fn, steps, flush, stream):
     """Run `steps` calls of fn, each after an untimed L2 flush; return per-step ms (events).
     The wall-clock span of the region is appended to TIMED_WINDOWS."""
@@ -234,10 +242,12 @@ def bench_prefill_only(args):
     pb = H.prefill_batch(pwl, pres, psrc)
     pout = torch.empty_like(pb.q)
     plse = torch.empty((pb.total_q, pwl.Hq), dtype=torch.float32, device="cuda")
+    pws = _prefill_workspace(pk, pres.pool, pb, pwl.Hq)
 
     def prefill_call():
         pk.lazy_attn_prefill(pres.pool, pb.q, pb.k_new, pb.v_new, pb.cu_q, pb.q_pos0, pb.words,
-                             pb.cu_pages, pb.max_q_len, sm_scale=pwl.sm_scale, out=pout, lse=plse)
+                             pb.cu_pages, pb.max_q_len, sm_scale=pwl.sm_scale, out=pout, lse=plse,
+                             workspace=pws)
 
     for _ in range(args.warmup):
         prefill_call()
@@ -365,11 +375,13 @@ def bench_ours(args):
         pb = H.prefill_batch(pwl, pres, psrc)
         pout = torch.empty_like(pb.q)
         plse = torch.empty((pb.total_q, pwl.Hq), dtype=torch.float32, device="cuda")
+        pws = _prefill_workspace(pk, pres.pool, pb, pwl.Hq)
         pools.append(pres.pool)
 
     def prefill_call():
         pk.lazy_attn_prefill(pres.pool, pb.q, pb.k_new, pb.v_new, pb.cu_q, pb.q_pos0, pb.words,
-                             pb.cu_pages, pb.max_q_len, sm_scale=pwl.sm_scale, out=pout, lse=plse)
+                             pb.cu_pages, pb.max_q_len, sm_scale=pwl.sm_scale, out=pout, lse=plse,
+                             workspace=pws)
 
     # ---------------- long-context decode (extra object)
     if not only_decode:
@@ -582,11 +594,12 @@ def mixed_sweep(args, flush, stream, hbm_peak):
         dlse = torch.empty((len(db.reqs), wl.Hq), dtype=torch.float32, device="cuda")
         pout = torch.empty_like(pb.q)
         plse = torch.empty((pb.total_q, wl.Hq), dtype=torch.float32, device="cuda")
+        pws = _prefill_workspace(pk, res.pool, pb, wl.Hq)
 
         def mixed_step():
             pk.lazy_attn_prefill(res.pool, pb.q, pb.k_new, pb.v_new, pb.cu_q, pb.q_pos0,
                                  pb.words, pb.cu_pages, pb.max_q_len, sm_scale=wl.sm_scale,
-                                 out=pout, lse=plse)
+                                 out=pout, lse=plse, workspace=pws)
             pk.kv_pool_write_tokens(res.pool, db.new_k, db.new_v, db.slot_mapping, db.local_pos)
             pk.lazy_attn_decode(res.pool, db.q, db.q_pos, db.words, db.cu_pages,
                                 sm_scale=wl.sm_scale, out=dout, lse=dlse, workspace=ws)
@@ -636,6 +649,7 @@ def chain_bench(args, flush, stream, n_steps=32, reps=3):
     plse = torch.empty((pb.total_q, wl.Hq), dtype=torch.float32, device="cuda")
     dws = torch.empty(pk.lazy_decode_workspace_bytes(res.pool, B, wl.Hq), dtype=torch.uint8,
                       device="cuda")
+    pws = _prefill_workspace(pk, res.pool, pb, wl.Hq)
     dout = torch.empty((B, wl.Hq, wl.D), dtype=torch.bfloat16, device="cuda")
     dlse = torch.empty((B, wl.Hq), dtype=torch.float32, device="cuda")
 
@@ -646,7 +660,7 @@ def chain_bench(args, flush, stream, n_steps=32, reps=3):
         pk.lazy_attn_prefill_append(res.pool, pb.q, pb.k_new, pb.v_new, pb.cu_q, pb.q_pos0,
                                     pb.words, pb.cu_pages, pb.max_q_len, ch.append_slots,
                                     ch.append_local_pos, sm_scale=wl.sm_scale, out=pout,
-                                    lse=plse)
+                                    lse=plse, workspace=pws)
         e[1].record(stream)
         for s, db in enumerate(steps):
             pk.kv_pool_write_tokens(res.pool, db.new_k, db.new_v, db.slot_mapping, db.local_pos)
@@ -736,11 +750,12 @@ def mqa_bench(args, flush, stream, hbm_peak, tc_peak):
     pb = H.prefill_batch(pwl, pres, psrc)
     pout = torch.empty_like(pb.q)
     plse = torch.empty((pb.total_q, pwl.Hq), dtype=torch.float32, device="cuda")
+    pws = _prefill_workspace(pk, pres.pool, pb, pwl.Hq)
 
     def prefill_call():
         pk.lazy_attn_prefill(pres.pool, pb.q, pb.k_new, pb.v_new, pb.cu_q, pb.q_pos0, pb.words,
                              pb.cu_pages, pb.max_q_len, sm_scale=pwl.sm_scale, out=pout,
-                             lse=plse)
+                             lse=plse, workspace=pws)
 
     for _ in range(args.warmup):
         flush(); prefill_call()
@@ -801,11 +816,12 @@ def alibi_bench(args, flush, stream, hbm_peak, tc_peak):
     pb = H.prefill_batch(pwl, pres, psrc)
     pout = torch.empty_like(pb.q)
     plse = torch.empty((pb.total_q, pwl.Hq), dtype=torch.float32, device="cuda")
+    pws = _prefill_workspace(pk, pres.pool, pb, pwl.Hq)
 
     def prefill_call():
         pk.lazy_attn_prefill(pres.pool, pb.q, pb.k_new, pb.v_new, pb.cu_q, pb.q_pos0, pb.words,
                              pb.cu_pages, pb.max_q_len, sm_scale=pwl.sm_scale, out=pout,
-                             lse=plse)
+                             lse=plse, workspace=pws)
 
     for _ in range(args.warmup):
         flush(); prefill_call()

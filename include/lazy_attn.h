@@ -137,6 +137,15 @@ enum { LAZY_DECODE_AUTO = 0, LAZY_DECODE_SIMT = 1 };
 int lazy_pool_set_decode_kernel(lazy_pool *pool, int32_t kind);
 /* The pool's mode (LAZY_POS_*) and, in ALiBi mode, its number of query heads (else 0). */
 int lazy_pool_position_mode(lazy_pool *pool, int32_t *mode, int32_t *num_q_heads);
+/*
+ * The number of SMs the tensor-core prefill plans its last wave for (0, the default, = the
+ * device's). When a call's units (request, kv head, 2 x 128 question rows) overflow the last wave,
+ * the units of that wave are cut into key-range chunks and merged afterwards, if the caller's
+ * workspace holds the partial results (lazy_prefill_workspace_bytes). Setting a smaller count
+ * makes small calls take that path (tests), or leaves SMs to other work. Applies to calls made
+ * after it; query lazy_prefill_workspace_bytes after setting it.
+ */
+int lazy_pool_set_schedule_sms(lazy_pool *pool, int32_t sms);
 
 /* Block allocator (host-side free list with reference counts; thread-safe).
  * kv_pool_alloc pops n blocks (refcount 1) into block_ids; LAZY_ERR_OUT_OF_BLOCKS leaves the

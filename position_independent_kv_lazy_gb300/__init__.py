@@ -49,6 +49,7 @@ EXPORTS = [
     "lazy_decode_workspace_bytes", "lazy_attn_decode", "lazy_prefill_workspace_bytes",
     "lazy_attn_prefill", "lazy_get_device_error", "lazy_debug_gather", "lazy_debug_wait_timeout",
     "lazy_attn_decode_noalloc", "lazy_debug_exp2", "lazy_attn_prefill_append",
+    "lazy_pool_set_schedule_sms",
     "lazy_pool_set_alibi", "lazy_pool_position_mode", "lazy_pool_set_decode_kernel",
 ]
 
@@ -87,6 +88,7 @@ _SIGS = {
     "lazy_pool_set_alibi": ([_vp, ctypes.POINTER(ctypes.c_float), _i32], ctypes.c_int),
     "lazy_pool_position_mode": ([_vp, _pi32, _pi32], ctypes.c_int),
     "lazy_pool_set_decode_kernel": ([_vp, _i32], ctypes.c_int),
+    "lazy_pool_set_schedule_sms": ([_vp, _i32], ctypes.c_int),
     "kv_pool_alloc": ([_vp, _i32, _pi32], ctypes.c_int),
     "kv_pool_retain": ([_vp, _pi32, _i32], ctypes.c_int),
     "kv_pool_release": ([_vp, _pi32, _i32], ctypes.c_int),
@@ -204,6 +206,12 @@ def lazy_pool_set_decode_kernel(pool: LazyPool, kind: int):
     """LAZY_DECODE_AUTO (tensor-core decode for bf16 / head_dim 128) or LAZY_DECODE_SIMT."""
     _check("lazy_pool_set_decode_kernel",
            load_library().lazy_pool_set_decode_kernel(pool.handle, int(kind)))
+
+
+def lazy_pool_set_schedule_sms(pool: LazyPool, sms: int):
+    """SMs the tensor-core prefill plans its last wave for (0 = the device's)."""
+    _check("lazy_pool_set_schedule_sms",
+           load_library().lazy_pool_set_schedule_sms(pool.handle, int(sms)))
 
 
 def lazy_pool_set_wait_limit(pool: LazyPool, ns: int):
@@ -385,11 +393,31 @@ def lazy_attn_decode(pool: LazyPool, q, q_pos, page_words, cu_pages, sm_scale=No
     return out, lse
 
 
+def lazy_prefill_workspace_bytes(pool: LazyPool, batch: int, total_q: int, max_q_len: int,
+                                 num_q_heads: int, flags: int = 0) -> int:
+    """Scratch bytes a prefill of this shape can use (0 when its schedule needs none)."""
+    n = ctypes.c_size_t()
+    _check("lazy_prefill_workspace_bytes", load_library().lazy_prefill_workspace_bytes(
+        pool.handle, batch, total_q, max_q_len, num_q_heads, flags, ctypes.byref(n)))
+    return n.value
+
+
+def _prefill_workspace(pool, q, B, max_q_len, flags, workspace):
+    import torch
+    if workspace is not None:
+        return workspace, workspace.numel() * workspace.element_size()
+    Tq, Hq, _ = q.shape
+    n = lazy_prefill_workspace_bytes(pool, B, Tq, max_q_len, Hq, flags)
+    return torch.empty(max(n, 1), dtype=torch.uint8, device=q.device), n
+
+
 def lazy_attn_prefill(pool: LazyPool, q, k_new, v_new, cu_q, q_pos0, page_words, cu_pages,
                       max_q_len: int, sm_scale=None, out=None, lse=None, flags: int = 0,
-                      stream=None):
+                      workspace=None, stream=None):
     """q [Tq,Hq,D] raw; k_new/v_new [Tq,Hkv,D] raw or None; cu_q, q_pos0, cu_pages int32;
-    page_words uint64 (device). Returns (out [Tq,Hq,D], lse [Tq,Hq] float32)."""
+    page_words uint64 (device). workspace: device scratch (default: allocated at
+    lazy_prefill_workspace_bytes); a smaller one only turns off the last-wave split.
+    Returns (out [Tq,Hq,D], lse [Tq,Hq] float32)."""
     import torch
     Tq, Hq, D = q.shape
     B = int(cu_q.shape[0]) - 1
@@ -399,21 +427,17 @@ def lazy_attn_prefill(pool: LazyPool, q, k_new, v_new, cu_q, q_pos0, page_words,
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((Tq, Hq), dtype=torch.float32, device=q.device)
-    n = ctypes.c_size_t()
-    lib = load_library()
-    _check("lazy_prefill_workspace_bytes", lib.lazy_prefill_workspace_bytes(
-        pool.handle, B, Tq, max_q_len, Hq, flags, ctypes.byref(n)))
-    ws = torch.empty(max(n.value, 1), dtype=torch.uint8, device=q.device)
-    _check("lazy_attn_prefill", lib.lazy_attn_prefill(
+    ws, nbytes = _prefill_workspace(pool, q, B, max_q_len, flags, workspace)
+    _check("lazy_attn_prefill", load_library().lazy_attn_prefill(
         pool.handle, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(cu_q), _ptr(q_pos0),
         _ptr(page_words), _ptr(cu_pages), B, Tq, max_q_len, Hq, float(sm_scale), _ptr(out),
-        _ptr(lse), _ptr(ws), n.value, flags, _stream(stream)))
+        _ptr(lse), _ptr(ws), nbytes, flags, _stream(stream)))
     return out, lse
 
 
 def lazy_attn_prefill_append(pool: LazyPool, q, k_new, v_new, cu_q, q_pos0, page_words, cu_pages,
                              max_q_len: int, append_slots, append_local_pos, sm_scale=None,
-                             out=None, lse=None, flags: int = 0, stream=None):
+                             out=None, lse=None, flags: int = 0, workspace=None, stream=None):
     """lazy_attn_prefill, then every question token t written into the pool at slot
     append_slots[t] (int32, block * page_size + slot, < 0 skips) as R(append_local_pos[t])
     k_new[t] and v_new[t]. Returns (out, lse)."""
@@ -426,15 +450,11 @@ def lazy_attn_prefill_append(pool: LazyPool, q, k_new, v_new, cu_q, q_pos0, page
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((Tq, Hq), dtype=torch.float32, device=q.device)
-    n = ctypes.c_size_t()
-    lib = load_library()
-    _check("lazy_prefill_workspace_bytes", lib.lazy_prefill_workspace_bytes(
-        pool.handle, B, Tq, max_q_len, Hq, flags, ctypes.byref(n)))
-    ws = torch.empty(max(n.value, 1), dtype=torch.uint8, device=q.device)
-    _check("lazy_attn_prefill_append", lib.lazy_attn_prefill_append(
+    ws, nbytes = _prefill_workspace(pool, q, B, max_q_len, flags, workspace)
+    _check("lazy_attn_prefill_append", load_library().lazy_attn_prefill_append(
         pool.handle, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(cu_q), _ptr(q_pos0),
         _ptr(page_words), _ptr(cu_pages), B, Tq, max_q_len, Hq, float(sm_scale), _ptr(out),
-        _ptr(lse), _ptr(ws), n.value, flags, _ptr(append_slots), _ptr(append_local_pos),
+        _ptr(lse), _ptr(ws), nbytes, flags, _ptr(append_slots), _ptr(append_local_pos),
         _stream(stream)))
     return out, lse
 

@@ -131,6 +131,12 @@ int lazy_pool_set_decode_kernel(lazy_pool *p, int32_t kind) {
   return LAZY_OK;
 }
 
+int lazy_pool_set_schedule_sms(lazy_pool *p, int32_t sms) {
+  if (!p || sms < 0) return LAZY_ERR_INVALID_ARG;
+  p->schedule_sms = sms;
+  return LAZY_OK;
+}
+
 int lazy_pool_position_mode(lazy_pool *p, int32_t *mode, int32_t *num_q_heads) {
   if (!p || !mode) return LAZY_ERR_INVALID_ARG;
   *mode = p->alibi ? LAZY_POS_ALIBI : LAZY_POS_ROPE;

@@ -30,6 +30,7 @@ struct lazy_pool {
   // ALiBi mode (lazy_pool_set_alibi): K is stored unrotated and attention adds
   // slope[head] * (n - m); page-word offsets are page start positions.
   int32_t decode_kernel = 0;        // LAZY_DECODE_* (lazy_pool_set_decode_kernel)
+  int32_t schedule_sms = 0;         // SMs the prefill schedule assumes; 0 = num_sms
   bool alibi = false;
   bool encoded = false;             // something was written: the mode can no longer change
   std::vector<float> slopes;        // per query head

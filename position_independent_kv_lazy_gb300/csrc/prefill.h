@@ -26,11 +26,16 @@ struct PrefillParams {
   float scale_log2;
   uint64_t wait_ns;
   const float *slopes;  // ALiBi pools: per query head (device); nullptr for RoPE pools
+  void *workspace;      // caller's scratch (tensor-core path: partial results of split units)
+  size_t workspace_bytes;
 };
 
 int prefill_simt(lazy_pool *p, const PrefillParams &pp, int32_t max_q_len, cudaStream_t s);
 // Tensor-core path; LAZY_ERR_UNSUPPORTED when the shape is not built.
 int prefill_tc_supported(const lazy_pool *p, int32_t hq);
 int prefill_tc(lazy_pool *p, const PrefillParams &pp, int32_t max_q_len, cudaStream_t s);
+// Scratch the tensor-core path can use for this call shape (0 when it would not split).
+int prefill_tc_workspace_bytes(lazy_pool *p, int32_t batch, int32_t max_q_len, int32_t hq,
+                               size_t *bytes);
 
 }  // namespace lazy

@@ -9,9 +9,13 @@ extern "C" int lazy_prefill_workspace_bytes(lazy_pool *p, int32_t batch, int32_t
                                             int32_t flags, size_t *bytes) {
   if (!p || !bytes || batch < 0 || total_q < 0 || max_q_len < 0 || num_q_heads <= 0)
     return LAZY_ERR_INVALID_ARG;
-  (void)flags;
-  *bytes = 0;  // neither prefill kernel needs scratch memory
-  return LAZY_OK;
+  if (flags < LAZY_PREFILL_AUTO || flags > LAZY_PREFILL_TC) return LAZY_ERR_INVALID_ARG;
+  *bytes = 0;  // the SIMT kernel needs no scratch; the tensor-core one may split its last wave
+  if (flags == LAZY_PREFILL_SIMT || batch == 0 || total_q == 0 || max_q_len == 0) return LAZY_OK;
+  if (num_q_heads % p->hkv || prefill_tc_supported(p, num_q_heads) != LAZY_OK) return LAZY_OK;
+  int rc = ensure_device(p);
+  if (rc != LAZY_OK) return rc;
+  return prefill_tc_workspace_bytes(p, batch, max_q_len, num_q_heads, bytes);
 }
 
 extern "C" int lazy_attn_prefill(lazy_pool *p, const void *q, const void *k_new,
@@ -20,8 +24,6 @@ extern "C" int lazy_attn_prefill(lazy_pool *p, const void *q, const void *k_new,
                                  int32_t total_q, int32_t max_q_len, int32_t num_q_heads,
                                  float sm_scale, void *out, float *lse, void *workspace,
                                  size_t workspace_bytes, int32_t flags, lazy_stream_t stream) {
-  (void)workspace;
-  (void)workspace_bytes;
   if (!p || batch < 0 || total_q < 0 || max_q_len < 0 || !(sm_scale > 0.f))
     return LAZY_ERR_INVALID_ARG;
   if (num_q_heads <= 0 || num_q_heads % p->hkv) return LAZY_ERR_INVALID_ARG;
@@ -59,6 +61,8 @@ extern "C" int lazy_attn_prefill(lazy_pool *p, const void *q, const void *k_new,
   pp.scale_log2 = sm_scale * 1.4426950408889634f;
   pp.wait_ns = p->wait_limit_ns;
   pp.slopes = p->alibi ? p->d_slopes : nullptr;
+  pp.workspace = workspace;
+  pp.workspace_bytes = workspace ? workspace_bytes : 0;
   cudaStream_t s = (cudaStream_t)stream;
   const bool tc_ok = prefill_tc_supported(p, num_q_heads) == LAZY_OK;
   if (flags == LAZY_PREFILL_TC) {

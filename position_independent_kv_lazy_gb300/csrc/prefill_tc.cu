@@ -30,6 +30,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <cmath>
 #include <mutex>
 
 #include "lazy_common.cuh"
@@ -56,11 +57,14 @@ constexpr int kHalfBytes = kTileBytes / 2;   // one 64-dim box column
 constexpr int kOffQ = 0;                               // 2 Q tiles
 constexpr int kOffK = kOffQ + 2 * kTileBytes;          // kNK K stages
 constexpr int kOffV = kOffK + kNK * kTileBytes;        // kNV V stages
+constexpr int kMaxSplit = 8;  // most key-range chunks of a split unit
 constexpr int kNM = 4;  // softmax metadata ring (see SMeta)
 constexpr int kOffMetaK = kOffV + kNV * kTileBytes;    // KMeta [kNK]
 constexpr int kOffMetaS = kOffMetaK + kNK * 48;        // SMeta [kNM]
 constexpr int kOffBar = kOffMetaS + kNM * 80 + 16;     // barriers (8-byte aligned)
-constexpr int kSmemBytes = kOffBar + 192 + 1024;       // + alignment slack
+constexpr int kOffTurn = kOffBar + 192;                // the 64 turn fractions (uint64)
+constexpr int kSmemBytes = kOffTurn + 64 * 8 + 1024;   // + alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory per block");
 
 // Read by the rotation group (valid until the K stage is refilled, after QK of this tile).
 struct KMeta {
@@ -96,6 +100,15 @@ struct TcParams {
   float scale_log2;
   uint64_t wait_ns;
   const float *slopes;  // ALiBi: per query head
+  // Schedule (1-D grid). Unit u = (request b, kv head h, token block x) with x fastest; blocks
+  // [0, n_full) take whole units. With ksplit > 1 the n_split units from n_full on are cut into
+  // ksplit key-range chunks each (split_item): split units go in groups of X, and a group's
+  // items run chunk by chunk, so blocks side by side read the same keys and share them through
+  // L2. Chunk results go to part_o / part_lse (item index, 256 rows: Q tile i row r at
+  // i * 128 + r) for prefill_combine_kernel.
+  int32_t X, n_full, n_split, ksplit;
+  float *part_o;    // [items][256][128] O / l
+  float *part_lse;  // [items][256] log2-domain lse (m + log2 l), -inf when no key was visible
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -315,22 +328,45 @@ __device__ __forceinline__ void rotate_4rows_chunk(uint8_t *tile, int row0, int 
   }
 }
 
-// (cos, sin) of delta * theta_i for i = 8c .. 8c+7 (exact fp32 angles), as bf16 pairs.
-// (cos, sin) of delta * theta for one frequency. Not inlined: the angles are needed only when
-// a page offset changes, and one shared copy keeps the softmax loop's code compact (the loop
-// is instruction-fetch bound when every call site carries its own sincospif).
-__device__ __noinline__ float2 angle_cs(int64_t delta, uint64_t turn_frac) {
-  float c, s;
-  rope_cos_sin(delta, turn_frac, c, s);
-  return make_float2(c, s);
+// (cos, sin) of delta * theta for two frequencies (turn fractions ta, tb), as two independent
+// chains. Not inlined: inside the tile loop the angles are needed only when a page offset
+// changes, and one shared copy keeps the loop's code compact (inlining the eight angles of a
+// chunk there was measured slower); two per call halve the latency-bound chain of one per call.
+__device__ __noinline__ float4 angle_cs2(int64_t delta, uint64_t ta, uint64_t tb) {
+  float c0, s0, c1, s1;
+  rope_cos_sin(delta, ta, c0, s0);
+  rope_cos_sin(delta, tb, c1, s1);
+  return make_float4(c0, s0, c1, s1);
 }
 
+// The same angles with the turn fractions in shared memory and the eight evaluations inlined,
+// so that they run as independent chains (one after another they are latency-bound: about
+// 300 cycles per angle with two warps per scheduler). Used for the query rows, 64 angles per
+// thread before the first product; inside the tile loop the inlined copy costs more in code
+// size than it saves (measured), so a page offset change takes chunk_angles.
+__device__ __forceinline__ void chunk_angles_ilp(int64_t delta, const uint64_t *turn_s, int c,
+                                                 RotPairs &rp) {
+  uint64_t tf[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) tf[e] = turn_s[c * 8 + e];
+  float co[8], si[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) rope_cos_sin(delta, tf[e], co[e], si[e]);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    rp.co[k] = __floats2bfloat162_rn(co[2 * k], co[2 * k + 1]);
+    rp.si[k] = __floats2bfloat162_rn(si[2 * k], si[2 * k + 1]);
+    rp.nsi[k] = __floats2bfloat162_rn(-si[2 * k], -si[2 * k + 1]);
+  }
+}
+
+// (cos, sin) of delta * theta_i for i = 8c .. 8c+7 (exact fp32 angles), as bf16 pairs.
 __device__ __forceinline__ void chunk_angles(int64_t delta, const uint64_t *turn, int c,
                                              RotPairs &rp) {
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    const float2 a = angle_cs(delta, turn[c * 8 + 2 * k]);
-    const float2 b = angle_cs(delta, turn[c * 8 + 2 * k + 1]);
+    const float4 ab = angle_cs2(delta, turn[c * 8 + 2 * k], turn[c * 8 + 2 * k + 1]);
+    const float2 a = make_float2(ab.x, ab.y), b = make_float2(ab.z, ab.w);
     rp.co[k] = __floats2bfloat162_rn(a.x, b.x);
     rp.si[k] = __floats2bfloat162_rn(a.y, b.y);
     rp.nsi[k] = __floats2bfloat162_rn(-a.y, -b.y);
@@ -354,6 +390,43 @@ __device__ __forceinline__ bool cta_wait(uint64_t *bar, uint32_t par, volatile i
   return true;
 }
 
+// Item order of the split units: group g holds split units [g X, g X + gsz), gsz = X except in
+// a short last group, and its gsz * ksplit items run chunk-major.
+__device__ __forceinline__ int split_item(const TcParams &p, int su, int chunk) {
+  const int g = su / p.X, gsz = min(p.X, p.n_split - g * p.X);
+  return g * p.X * p.ksplit + chunk * gsz + (su - g * p.X);
+}
+__device__ __forceinline__ void split_unit(const TcParams &p, int item, int *su, int *chunk) {
+  const int g = item / (p.X * p.ksplit), gsz = min(p.X, p.n_split - g * p.X);
+  const int w = item - g * p.X * p.ksplit;
+  *chunk = w / gsz;
+  *su = g * p.X + w % gsz;
+}
+
+// The unit of this block and, for a split unit, its chunk and item (item -1 for a whole unit).
+// The block index is read through asm volatile, so every call decodes it again: the softmax warps
+// call it in their epilogue instead of keeping these values in registers through the tile loop.
+struct TcUnit {
+  int b, h, t0, chunk, item;
+};
+__device__ __forceinline__ TcUnit tc_unit(const TcParams &p) {
+  int u;
+  asm volatile("mov.u32 %0, %%ctaid.x;" : "=r"(u));
+  TcUnit t;
+  t.chunk = 0;
+  t.item = -1;
+  if (p.ksplit > 1 && u >= p.n_full) {
+    t.item = u - p.n_full;
+    int su;
+    split_unit(p, t.item, &su, &t.chunk);
+    u = p.n_full + su;
+  }
+  t.b = u / (p.X * p.hkv);
+  t.h = (u / p.X) % p.hkv;
+  t.t0 = (u % p.X) * 2 * p.TQ;
+  return t;
+}
+
 // kAlibi: the pool's ALiBi mode. Nothing is rotated (the barriers keep their order) and every
 // score gets slope * (n - m) before the row max.
 template <bool kAlibi>
@@ -371,12 +444,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   uint64_t *v_full = bars + 11, *v_empty = bars + 13;                     // [kNV]
   uint64_t *s_full = bars + 15, *p_ready = bars + 17, *o_final = bars + 19;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 20);
+  uint64_t *turn_s = reinterpret_cast<uint64_t *>(sm + kOffTurn);
   volatile int *abort = reinterpret_cast<volatile int *>(bars + 21);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int b = blockIdx.z, h = blockIdx.y;
+  const TcUnit unit = tc_unit(p);
+  const int b = unit.b, h = unit.h, t0 = unit.t0;
   const int G = p.G, TQ = p.TQ;
-  const int t0 = blockIdx.x * 2 * TQ;
   const int32_t qbeg = p.cu_q[b];
   const int32_t Tb = p.cu_q[b + 1] - qbeg;
   if (t0 >= Tb) return;
@@ -386,7 +460,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   const int n_doc = (npg + 7) / 8;
   const int t_end = min(t0 + 2 * TQ, Tb);
   const int n_new = p.has_new ? (t_end + kTile - 1) / kTile : 0;
-  const int n_tiles = n_doc + n_new;
+  // key tiles [lo, lo + n_tiles) of the n_doc + n_new: all of them, or this block's chunk
+  int lo = 0, n_tiles = n_doc + n_new;
+  if (unit.item >= 0) {
+    const int n_all = n_tiles;
+    lo = (int)((int64_t)unit.chunk * n_all / p.ksplit);
+    n_tiles = (int)((int64_t)(unit.chunk + 1) * n_all / p.ksplit) - lo;
+  }
 
   if (tid == 0) {
     mbar_init(q_full, 1);
@@ -408,6 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     *abort = 0;
     fence_barrier_init();
   }
+  if (tid >= 64 && tid < 128) turn_s[tid - 64] = p.turn[tid - 64];  // warps 2-3, else idle
   if (warp == 1) {
     asm volatile(
         "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
@@ -434,14 +515,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 #pragma unroll
         for (int pp = 0; pp < 8; ++pp) wnext[pp] = p.words[pg0 + min(j * 8 + pp, npg - 1)];
       };
-      if (n_doc > 0) load_words(0);
+      if (lo < n_doc) load_words(lo);
       int32_t rows[kNK][8];
       int32_t run8[kNK];  // first block id when the tile's 8 blocks are consecutive, else -1
       int k_issued[kNK] = {0, 0, 0}, v_issued[kNV] = {0, 0};
       bool ok = true;
       for (int e = 0; ok && e <= n_tiles; ++e) {
-        if (e < n_tiles) {  // ---- K of tile e
-          const int j = e, s = j % kNK;
+        if (e < n_tiles) {  // ---- K of tile e (content tile jc = lo + e)
+          const int j = e, s = j % kNK, jc = lo + j;
           if (j >= kNK && !cta_wait(&k_empty[s], ((j / kNK) - 1) & 1, abort, lim, p.err)) {
             ok = false;
             break;
@@ -449,12 +530,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           KMeta &mk = meta_k[s];
           SMeta &ms = meta_s[j % kNM];
           uint8_t *kd = Ks + s * kTileBytes;
-          if (j < n_doc) {
+          if (jc < n_doc) {
             int full = 1;
             uint64_t w[8];
 #pragma unroll
             for (int pp = 0; pp < 8; ++pp) w[pp] = wnext[pp];
-            if (j + 1 < n_doc) load_words(j + 1);
+            if (jc + 1 < n_doc) load_words(jc + 1);
             mk.kind = 0;
 #pragma unroll
             for (int pp = 0; pp < 8; ++pp) {
@@ -465,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                 blk = 0;
                 nv = 0;
               }
-              if (j * 8 + pp >= npg) nv = 0;  // absent page: the last one is loaded again, masked
+              if (jc * 8 + pp >= npg) nv = 0;  // absent page: the last one is loaded again, masked
               ms.nv[pp] = nv;
               ms.pos0[pp] = (int32_t)word_offset(w[pp]);  // ALiBi pools: the page start
               full &= (nv == kPage);
@@ -493,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                         &k_full[s]);
             }
           } else {
-            const int c0 = (j - n_doc) * kTile;
+            const int c0 = (jc - n_doc) * kTile;
             mk.kind = 1;
             mk.c0 = c0;
             ms.kind = 1;
@@ -508,14 +589,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           ++k_issued[s];
         }
         if (e >= 1) {  // ---- V of tile e - 1
-          const int j = e - 1, s = j % kNV, sk = j % kNK;
+          const int j = e - 1, s = j % kNV, sk = j % kNK, jc = lo + j;
           if (j >= kNV && !cta_wait(&v_empty[s], ((j / kNV) - 1) & 1, abort, lim, p.err)) {
             ok = false;
             break;
           }
           uint8_t *vd = Vs + s * kTileBytes;
           mbar_arrive_expect_tx(&v_full[s], kTileBytes);
-          if (j < n_doc) {
+          if (jc < n_doc) {
             if (run8[sk] >= 0) {
               for (int cb = 0; cb < 2; ++cb)
                 tma4d(vd + cb * kHalfBytes, &p.tm_v8, cb * 64, 0, h, run8[sk], &v_full[s]);
@@ -527,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                         &v_full[s]);
             }
           } else {
-            const int c0 = (j - n_doc) * kTile;
+            const int c0 = (jc - n_doc) * kTile;
             for (int cb = 0; cb < 2; ++cb)
               tma3d(vd + cb * kHalfBytes, &p.tm_vnew, cb * 64, h, qbeg + c0, &v_full[s]);
           }
@@ -620,7 +701,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     const int row = (warp & 3) * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const uint32_t s_col = lane_base + i * 128, o_col = lane_base + 256 + i * 128;
-    const int t_row = t0 + i * TQ + row / G;
+    const int t_off = i * TQ + row / G;  // the row's token within the unit (t_row - t0)
+    const int t_row = t0 + t_off;
     const float sl2 = p.scale_log2;
     const float slope2 = kAlibi ? p.slopes[h * G + row % G] * 1.4426950408889634f : 0.f;
     const int32_t m_row = q_pos0_b + t_row;  // the row's logical position (ALiBi)
@@ -634,7 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 #pragma unroll 1
       for (int c = 0; c < 8; ++c) {
         RotPairs rq;
-        chunk_angles((int64_t)(i * TQ + row / G), turn, c, rq);
+        chunk_angles_ilp((int64_t)(i * TQ + row / G), turn_s, c, rq);
         rotate_row_chunk(Qs + i * kTileBytes, row, c, rq);
       }
       fence_async_smem();
@@ -662,7 +744,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 #pragma unroll 1
         for (int rr = 0; rr < 4; ++rr) {
           RotPairs rk;
-          chunk_angles((int64_t)(mt.c0 + rrow0 + rr - t0), turn, rc, rk);
+          chunk_angles((int64_t)(mt.c0 + rrow0 + rr - t_row + t_off), turn, rc, rk);
           rotate_row_chunk(kt, rrow0 + rr, rc, rk);
         }
       }
@@ -805,12 +887,37 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     }
     // epilogue: O / l -> bf16 rows, lse
     ok = ok && cta_wait(o_final, 0, abort, lim, p.err);
-    if (ok) {
+    const TcUnit ue = tc_unit(p);  // decoded again (see tc_unit)
+    if (ok && ue.item >= 0) {
+      // chunk of a split unit: fp32 O / l and the log2-domain lse for the combine
       tc_fence_after();
       const bool valid_row = t_row < Tb;
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      const int qh = h * G + row % G;
-      __nv_bfloat16 *dst = p.out + ((size_t)(qbeg + t_row) * p.hq + qh) * 128;
+      const size_t prow = (size_t)ue.item * 256 + i * 128 + row;
+      float *dst = p.part_o + prow * 128;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tmem_ld32(o_col + c * 32, r);
+        if (valid_row) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) {
+            // a chunk that saw no key of this row leaves O unwritten: store zeros
+            float f[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) f[k] = l_run > 0.f ? __uint_as_float(r[e + k]) * inv : 0.f;
+            *reinterpret_cast<float4 *>(dst + c * 32 + e) = make_float4(f[0], f[1], f[2], f[3]);
+          }
+        }
+      }
+      if (valid_row) p.part_lse[prow] = l_run > 0.f ? m_run + log2f(l_run) : -INFINITY;
+    } else if (ok) {
+      tc_fence_after();
+      const bool valid_row = t_row < Tb;
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      const int qh = ue.h * G + row % G;
+      const int32_t qb = p.cu_q[ue.b];
+      __nv_bfloat16 *dst = p.out + ((size_t)(qb + t_row) * p.hq + qh) * 128;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t r[32];
@@ -826,7 +933,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         }
       }
       if (valid_row)
-        p.lse[(size_t)(qbeg + t_row) * p.hq + qh] =
+        p.lse[(size_t)(qb + t_row) * p.hq + qh] =
             l_run > 0.f ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
     }
   }
@@ -837,6 +944,82 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem));
   }
+}
+
+// Merges the K = ksplit chunk results of every row of the split units: each warp takes R rows,
+// lane l holding dims 4l .. 4l + 3. With lse_c the chunks' log2-domain lse and M their max, a
+// row is sum_c 2^(lse_c - M) o_c / W, W = sum_c 2^(lse_c - M), and its lse (M + log2 W) ln 2.
+// Every chunk wrote every valid row (zeros and -inf when it saw no key), so all R K loads of a
+// warp are issued before any weight is known: one memory round trip per warp.
+template <int K, int R>
+__global__ void __launch_bounds__(256) prefill_combine_kernel(const __grid_constant__ TcParams p) {
+  const int gw = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  const int n_rows = p.n_split * 256;
+  float lse[R][K];
+  float4 o[R][K];
+  bool valid[R];
+  size_t dst[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int gr = gw * R + r;  // global row: split unit gr / 256, row gr % 256 of the unit
+    valid[r] = false;
+    dst[r] = 0;
+    if (gr < n_rows) {
+      const int su = gr >> 8, r256 = gr & 255;
+      const int u = p.n_full + su;
+      const int b = u / (p.X * p.hkv), h = (u / p.X) % p.hkv;
+      const int t0 = (u % p.X) * 2 * p.TQ;
+      const int32_t qbeg = p.cu_q[b], Tb = p.cu_q[b + 1] - qbeg;
+      const int i = r256 >> 7, row = r256 & 127;
+      const int t_row = t0 + i * p.TQ + row / p.G;
+      if (t_row < Tb) {
+        valid[r] = true;
+        dst[r] = (size_t)(qbeg + t_row) * p.hq + h * p.G + row % p.G;
+#pragma unroll
+        for (int c = 0; c < K; ++c) {
+          const size_t it = (size_t)split_item(p, su, c) * 256 + r256;
+          lse[r][c] = p.part_lse[it];
+          o[r][c] = *reinterpret_cast<const float4 *>(p.part_o + it * 128 + lane * 4);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    if (!valid[r]) continue;
+    float M = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < K; ++c) M = fmaxf(M, lse[r][c]);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float W = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int c = 0; c < K; ++c) {
+        const float w = lse[r][c] == -INFINITY ? 0.f : exp2f(lse[r][c] - M);
+        W += w;
+        acc.x += w * o[r][c].x;
+        acc.y += w * o[r][c].y;
+        acc.z += w * o[r][c].z;
+        acc.w += w * o[r][c].w;
+      }
+    }
+    const float inv = W > 0.f ? 1.f / W : 0.f;
+    __nv_bfloat162 v0 = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+    __nv_bfloat162 v1 = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+    uint2 pk;
+    pk.x = *reinterpret_cast<uint32_t *>(&v0);
+    pk.y = *reinterpret_cast<uint32_t *>(&v1);
+    *reinterpret_cast<uint2 *>(p.out + dst[r] * 128 + lane * 4) = pk;
+    if (lane == 0) p.lse[dst[r]] = W > 0.f ? (M + log2f(W)) * 0.69314718055994531f : -INFINITY;
+  }
+}
+
+// Launch of the combine for K chunks: R = 16 / K rows per warp keeps 16 loads in flight.
+template <int K>
+void launch_combine(const TcParams &tp, cudaStream_t s) {
+  constexpr int R = (16 / K) > 0 ? 16 / K : 1;
+  const int rows = tp.n_split * 256, warps = (rows + R - 1) / R;
+  prefill_combine_kernel<K, R><<<(warps + 7) / 8, 256, 0, s>>>(tp);
 }
 
 // ---------------------------------------------------------------- host side
@@ -916,6 +1099,55 @@ int prefill_tc_supported(const lazy_pool *p, int32_t hq) {
   return LAZY_OK;
 }
 
+namespace {
+// Last-wave split. A whole unit takes one unit-time T on its SM; a chunk of a unit cut into k
+// takes T / k plus a fixed cost (Q load and rotation, pipeline fill, epilogue) taken as 3% of T.
+// The units beyond the last full wave of `sms` blocks are cut into the k in 2..kMaxSplit that
+// minimises (full waves) + ceil(split units * k / sms) * (1 / k + 0.03); the split is planned
+// only when that beats ceil(units / sms) waves by 3%.
+struct TcPlan {
+  int X = 0, units = 0, n_full = 0, n_split = 0, ksplit = 1, grid = 0;
+  size_t ws_bytes = 0;  // partial results: [items][256][128] O plus [items][256] lse, fp32
+};
+
+TcPlan plan_tc(int32_t batch, int32_t hkv, int32_t TQ, int32_t max_q_len, int sms) {
+  TcPlan pl;
+  pl.X = (max_q_len + 2 * TQ - 1) / (2 * TQ);
+  pl.units = pl.X * hkv * batch;
+  pl.n_full = pl.grid = pl.units;
+  if (sms <= 0 || pl.units == 0) return pl;
+  const int waves = pl.units / sms;
+  const int n_full = waves * sms, r = pl.units - n_full;
+  if (r == 0) return pl;
+  const double whole = (double)waves + 1.0;
+  double best = 0.97 * whole;
+  int best_k = 1;
+  for (int k = 2; k <= kMaxSplit; ++k) {
+    const double t = waves + std::ceil((double)r * k / sms) * (1.0 / k + 0.03);
+    if (t < best) {
+      best = t;
+      best_k = k;
+    }
+  }
+  if (best_k == 1) return pl;
+  pl.n_full = n_full;
+  pl.n_split = r;
+  pl.ksplit = best_k;
+  pl.grid = n_full + r * best_k;
+  pl.ws_bytes = (size_t)r * best_k * 256 * (128 + 1) * sizeof(float);
+  return pl;
+}
+
+int schedule_sms(const lazy_pool *p) { return p->schedule_sms > 0 ? p->schedule_sms : p->num_sms; }
+}  // namespace
+
+int prefill_tc_workspace_bytes(lazy_pool *p, int32_t batch, int32_t max_q_len, int32_t hq,
+                               size_t *bytes) {
+  const int G = hq / p->hkv;
+  *bytes = plan_tc(batch, p->hkv, 128 / G, max_q_len, schedule_sms(p)).ws_bytes;
+  return LAZY_OK;
+}
+
 int prefill_tc(lazy_pool *p, const PrefillParams &pp, int32_t max_q_len, cudaStream_t s) {
   TcParams tp;
   memset(&tp, 0, sizeof(tp));
@@ -972,12 +1204,39 @@ int prefill_tc(lazy_pool *p, const PrefillParams &pp, int32_t max_q_len, cudaStr
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes));
     attr = true;
   }
-  dim3 grid((max_q_len + 2 * TQ - 1) / (2 * TQ), pp.hkv, pp.batch);
+  // The split runs only when the caller's workspace holds its partial results.
+  TcPlan pl = plan_tc(pp.batch, pp.hkv, TQ, max_q_len, schedule_sms(p));
+  if (pl.ksplit > 1 && (!pp.workspace || pp.workspace_bytes < pl.ws_bytes ||
+                        ((uintptr_t)pp.workspace & 15))) {
+    pl.n_full = pl.grid = pl.units;
+    pl.n_split = 0;
+    pl.ksplit = 1;
+  }
+  tp.X = pl.X;
+  tp.n_full = pl.n_full;
+  tp.n_split = pl.n_split;
+  tp.ksplit = pl.ksplit;
+  if (pl.ksplit > 1) {
+    tp.part_o = reinterpret_cast<float *>(pp.workspace);
+    tp.part_lse = tp.part_o + (size_t)pl.n_split * pl.ksplit * 256 * 128;
+  }
   if (pp.slopes)
-    prefill_tc_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(tp);
+    prefill_tc_kernel<true><<<pl.grid, kThreads, kSmemBytes, s>>>(tp);
   else
-    prefill_tc_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(tp);
+    prefill_tc_kernel<false><<<pl.grid, kThreads, kSmemBytes, s>>>(tp);
   LAZY_CUDA_TRY(cudaGetLastError());
+  if (pl.ksplit > 1) {
+    switch (pl.ksplit) {
+      case 2: launch_combine<2>(tp, s); break;
+      case 3: launch_combine<3>(tp, s); break;
+      case 4: launch_combine<4>(tp, s); break;
+      case 5: launch_combine<5>(tp, s); break;
+      case 6: launch_combine<6>(tp, s); break;
+      case 7: launch_combine<7>(tp, s); break;
+      default: launch_combine<8>(tp, s); break;
+    }
+    LAZY_CUDA_TRY(cudaGetLastError());
+  }
   return LAZY_OK;
 }
 

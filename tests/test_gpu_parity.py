@@ -500,6 +500,62 @@ def test_prefill_offsets_near_the_page_word_limit(pk, flags):
     _check_prefill(wl, pb, out, lse, lse_tol=TC_EDGE_LSE_TOL if flags == "tc" else None)
 
 
+# Last-wave split of the tensor-core prefill. The edge layout has 3 requests (question lengths
+# 37 / 5 / 130) and X = ceil(130 / (256 / group)) token blocks per (request, kv head), so
+# X * Hkv * 3 units (72 for 32/8). Planned for `sms` SMs: 1 never splits (every wave is full);
+# for 32/8, 5, 7, 20, 27, 62, 100 and 1000 cut the units past the last full wave into 5, 7, 5,
+# 3, 6, 4 and 8 key-range chunks (every combine width; groups of 3 split units, a short last
+# group at 5), and the device's own count (0) gives 2. The short request's chunks past its
+# 3 key tiles are empty.
+@pytest.mark.parametrize("Hq,Hkv", [(32, 8), (16, 2), (32, 1)])
+@pytest.mark.parametrize("sms", [1, 5, 7, 20, 27, 62, 100, 1000, 0])
+def test_prefill_last_wave_split(pk, Hq, Hkv, sms):
+    H = _h()
+    wl = _edge_prefill_workload(128, Hq, Hkv, "bf16")
+    src = H.HostSource(wl)
+    res = H.build_resident(wl, src, resident_pool=False, drop_raw=False)
+    pb = H.prefill_batch(wl, res, src)
+
+    def run(n, workspace=None):
+        pk.lazy_pool_set_schedule_sms(res.pool, n)
+        out, lse = pk.lazy_attn_prefill(res.pool, pb.q, pb.k_new, pb.v_new, pb.cu_q, pb.q_pos0,
+                                        pb.words, pb.cu_pages, pb.max_q_len,
+                                        sm_scale=wl.sm_scale, flags=pk.LAZY_PREFILL_TC,
+                                        workspace=workspace)
+        torch.cuda.synchronize()
+        assert pk.lazy_get_device_error(res.pool) == 0
+        return out.float().cpu().numpy(), lse.cpu().numpy()
+
+    out, lse = run(sms)
+    _check_prefill(wl, pb, out, lse, lse_tol=TC_EDGE_LSE_TOL)
+    # against the unsplit schedule: the chunks' fp32 partials merge to the same rows up to
+    # the bf16 rounding of the weights (chunk-local maxima) and of the output
+    o1, l1 = run(1)
+    assert np.abs(out - o1).max() <= 1e-2 and np.abs(lse - l1).max() <= 1e-4
+    # a workspace smaller than the plan's falls back to whole units, with the same result
+    o2, l2 = run(sms, workspace=torch.empty(16, dtype=torch.uint8, device="cuda"))
+    assert np.array_equal(o2, o1) and np.array_equal(l2, l1)
+
+
+def test_prefill_split_workspace_sizes(pk):
+    # 32/8 edge layout: X = 3, 72 units. 1 SM: no split. 5 SMs: 14 full waves, 2 split units
+    # x 5 chunks. 20 SMs: 3 waves, 12 split units x 5. 100 SMs: 72 split units x 4 chunks.
+    # One item holds 256 rows of 128 + 1 fp32.
+    H = _h()
+    wl = _edge_prefill_workload(128, 32, 8, "bf16")
+    src = H.HostSource(wl)
+    res = H.build_resident(wl, src, resident_pool=False)
+    pb = H.prefill_batch(wl, res, src)
+    item = 256 * 129 * 4
+    want = {1: 0, 5: 2 * 5 * item, 20: 12 * 5 * item, 100: 72 * 4 * item}
+    for sms, n in want.items():
+        pk.lazy_pool_set_schedule_sms(res.pool, sms)
+        assert pk.lazy_prefill_workspace_bytes(res.pool, wl.batch, pb.total_q, pb.max_q_len,
+                                               wl.Hq) == n, sms
+        assert pk.lazy_prefill_workspace_bytes(res.pool, wl.batch, pb.total_q, pb.max_q_len,
+                                               wl.Hq, flags=pk.LAZY_PREFILL_SIMT) == 0
+
+
 def test_prefill_tensor_core_matches_cuda_core_kernel(pk):
     wl = _edge_prefill_workload(128, 32, 8, "bf16")
     _, _, o_tc, l_tc = _prefill(pk, wl, pk.LAZY_PREFILL_TC)
