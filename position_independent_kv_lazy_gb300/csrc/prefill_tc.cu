@@ -88,6 +88,8 @@ static_assert(sizeof(SMeta) == 80, "SMeta layout");
 
 struct TcParams {
   CUtensorMap tm_q, tm_knew, tm_vnew, tm_k, tm_v, tm_k8, tm_v8;
+  CUtensorMap tm_out;   // out, the same boxes as tm_q (one Q tile per 64-dim half)
+  CUtensorMap tm_part;  // part_o as [items * 256 rows][128] fp32, box 32 dims x 128 rows
   const int32_t *cu_q;
   const int32_t *q_pos0;
   const uint64_t *words;
@@ -169,6 +171,36 @@ __device__ __forceinline__ void tc_fence_after() {
 }
 __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// TMA stores (shared -> global, bulk-group completion) and their wait. The wait is for the
+// writes themselves, not only for the reads of the source: the issuing thread leaves the kernel
+// with its stores complete, as it does with plain stores.
+__device__ __forceinline__ void tma_store2d(const CUtensorMap *m, const void *src, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+          (uint64_t)m),
+      "r"(smem_u32(src)), "r"(x), "r"(y)
+      : "memory");
+}
+__device__ __forceinline__ void tma_store3d(const CUtensorMap *m, const void *src, int x, int y,
+                                            int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          (uint64_t)m),
+      "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit_and_wait() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// Named barrier 1 + i over the 128 threads of softmax group i (immediate ids, so that only
+// barriers 0-2 are reserved).
+__device__ __forceinline__ void group_bar(int i) {
+  if (i == 0)
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+  else
+    asm volatile("bar.sync 2, 128;" ::: "memory");
 }
 
 #define LAZY_R32(r)                                                                          \
@@ -887,54 +919,90 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     }
     // epilogue: O / l -> bf16 rows, lse
     ok = ok && cta_wait(o_final, 0, abort, lim, p.err);
+    // Each thread holds one row of its group's O tile. The rows are staged in shared memory in
+    // the 128-byte-swizzled layout of a TMA box (chunk q of row r at 16 (q ^ (r & 7)), so a
+    // warp's 32 rows spread over all banks) and leave in a few TMA stores: one store per lane
+    // and row would be 32 separate segments per instruction. The Q tiles and the K/V rings are
+    // free once o_final has arrived (every MMA, hence every copy it read, is done).
     const TcUnit ue = tc_unit(p);  // decoded again (see tc_unit)
-    if (ok && ue.item >= 0) {
-      // chunk of a split unit: fp32 O / l and the log2-domain lse for the combine
-      tc_fence_after();
-      const bool valid_row = t_row < Tb;
-      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      const size_t prow = (size_t)ue.item * 256 + i * 128 + row;
-      float *dst = p.part_o + prow * 128;
+    if (ue.item >= 0) {
+      // chunk of a split unit: fp32 O / l (zeros when the chunk saw no key of the row) for the
+      // combine, staged as four 16 KB boxes of 32 dims x 128 rows in the K/V rings
+      uint8_t *stg = Ks + i * 65536;
+      if (ok) {
+        tc_fence_after();
+        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld32(o_col + c * 32, r);
-        if (valid_row) {
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tmem_ld32(o_col + c * 32, r);
 #pragma unroll
-          for (int e = 0; e < 32; e += 4) {
-            // a chunk that saw no key of this row leaves O unwritten: store zeros
+          for (int q = 0; q < 8; ++q) {
             float f[4];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) f[k] = l_run > 0.f ? __uint_as_float(r[e + k]) * inv : 0.f;
-            *reinterpret_cast<float4 *>(dst + c * 32 + e) = make_float4(f[0], f[1], f[2], f[3]);
+            for (int k = 0; k < 4; ++k)
+              f[k] = l_run > 0.f ? __uint_as_float(r[4 * q + k]) * inv : 0.f;
+            *reinterpret_cast<float4 *>(stg + c * 16384 + row * 128 + ((q ^ (row & 7)) << 4)) =
+                make_float4(f[0], f[1], f[2], f[3]);
           }
         }
+        fence_async_smem();
+        if (t_row < Tb)
+          p.part_lse[(size_t)ue.item * 256 + i * 128 + row] =
+              l_run > 0.f ? m_run + log2f(l_run) : -INFINITY;
       }
-      if (valid_row) p.part_lse[prow] = l_run > 0.f ? m_run + log2f(l_run) : -INFINITY;
-    } else if (ok) {
-      tc_fence_after();
-      const bool valid_row = t_row < Tb;
-      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      group_bar(i);
+      if (ok && row == 0) {
+        for (int c = 0; c < 4; ++c)
+          tma_store2d(&p.tm_part, stg + c * 16384, c * 32, ue.item * 256 + i * 128);
+        bulk_commit_and_wait();
+      }
+    } else {
+      // whole unit: bf16 O / l. A Q tile whose TQ tokens all belong to the request goes out as
+      // two TMA boxes (one per 64-dim half) staged in its own Q slot; a ragged last tile keeps
+      // per-row stores, since its box would reach into the next request's rows.
+      const bool full_tile = ue.t0 + (i + 1) * TQ <= Tb;
       const int qh = ue.h * G + row % G;
       const int32_t qb = p.cu_q[ue.b];
-      __nv_bfloat16 *dst = p.out + ((size_t)(qb + t_row) * p.hq + qh) * 128;
+      uint8_t *stg = Qs + i * kTileBytes;
+      if (ok) {
+        tc_fence_after();
+        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        const bool valid_row = t_row < Tb;
+        __nv_bfloat16 *dst = p.out + ((size_t)(qb + t_row) * p.hq + qh) * 128;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld32(o_col + c * 32, r);
-        if (valid_row) {
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tmem_ld32(o_col + c * 32, r);
 #pragma unroll
           for (int e = 0; e < 32; e += 8) {
             float f[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k) f[k] = l_run > 0.f ? __uint_as_float(r[e + k]) * inv : 0.f;
-            *reinterpret_cast<uint4 *>(dst + c * 32 + e) = pack16<__nv_bfloat16>(f);
+            const uint4 v = pack16<__nv_bfloat16>(f);
+            if (full_tile) {
+              const int q = (c & 1) * 4 + e / 8;  // 16-byte chunk within the 64-dim half
+              *reinterpret_cast<uint4 *>(stg + (c >> 1) * kHalfBytes + row * 128 +
+                                         ((q ^ (row & 7)) << 4)) = v;
+            } else if (valid_row) {
+              *reinterpret_cast<uint4 *>(dst + c * 32 + e) = v;
+            }
           }
         }
+        if (full_tile) fence_async_smem();
+        if (valid_row)
+          p.lse[(size_t)(qb + t_row) * p.hq + qh] =
+              l_run > 0.f ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
       }
-      if (valid_row)
-        p.lse[(size_t)(qb + t_row) * p.hq + qh] =
-            l_run > 0.f ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+      if (full_tile) {
+        group_bar(i);
+        if (ok && row == 0) {
+          for (int hb = 0; hb < 2; ++hb)
+            tma_store3d(&p.tm_out, stg + hb * kHalfBytes, hb * 64, ue.h * G,
+                        qb + ue.t0 + i * TQ);
+          bulk_commit_and_wait();
+        }
+      }
     }
   }
 
@@ -1041,16 +1109,18 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// bf16 tensor [dims[rank-1]]...[dims[0]] (dims innermost first), 128B swizzle, zero OOB fill.
+// Tensor [dims[rank-1]]...[dims[0]] (dims innermost first; bf16 unless dt says otherwise),
+// 128B swizzle, zero OOB fill.
 int make_map(CUtensorMap *m, void *base, int rank, const cuuint64_t *dims,
-             const cuuint64_t *strides_bytes, const cuuint32_t *box) {
+             const cuuint64_t *strides_bytes, const cuuint32_t *box,
+             CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) {
     record_msg("cuTensorMapEncodeTiled is unavailable");
     return LAZY_ERR_CUDA;
   }
   cuuint32_t es[4] = {1, 1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, base, dims, strides_bytes, box, es,
+  CUresult r = enc(m, dt, rank, base, dims, strides_bytes, box, es,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
@@ -1168,6 +1238,8 @@ int prefill_tc(lazy_pool *p, const PrefillParams &pp, int32_t max_q_len, cudaStr
     const cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)TQ};
     rc = make_map(&tp.tm_q, const_cast<void *>(pp.q), 3, dims, strides, box);
     if (rc != LAZY_OK) return rc;
+    rc = make_map(&tp.tm_out, pp.out, 3, dims, strides, box);
+    if (rc != LAZY_OK) return rc;
   }
   if (pp.k_new) {
     const cuuint64_t dims[3] = {128, (cuuint64_t)pp.hkv, (cuuint64_t)pp.total_q};
@@ -1217,8 +1289,14 @@ int prefill_tc(lazy_pool *p, const PrefillParams &pp, int32_t max_q_len, cudaStr
   tp.n_split = pl.n_split;
   tp.ksplit = pl.ksplit;
   if (pl.ksplit > 1) {
+    const size_t rows = (size_t)pl.n_split * pl.ksplit * 256;
     tp.part_o = reinterpret_cast<float *>(pp.workspace);
-    tp.part_lse = tp.part_o + (size_t)pl.n_split * pl.ksplit * 256 * 128;
+    tp.part_lse = tp.part_o + rows * 128;
+    const cuuint64_t dims[2] = {128, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {128 * sizeof(float)};
+    const cuuint32_t box[2] = {32, 128};
+    rc = make_map(&tp.tm_part, tp.part_o, 2, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_FLOAT32);
+    if (rc != LAZY_OK) return rc;
   }
   if (pp.slopes)
     prefill_tc_kernel<true><<<pl.grid, kThreads, kSmemBytes, s>>>(tp);
