@@ -1018,7 +1018,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 // lane l holding dims 4l .. 4l + 3. With lse_c the chunks' log2-domain lse and M their max, a
 // row is sum_c 2^(lse_c - M) o_c / W, W = sum_c 2^(lse_c - M), and its lse (M + log2 W) ln 2.
 // Every chunk wrote every valid row (zeros and -inf when it saw no key), so all R K loads of a
-// warp are issued before any weight is known: one memory round trip per warp.
+// warp are issued before any weight or row validity is known: one memory round trip per warp.
 template <int K, int R>
 __global__ void __launch_bounds__(256) prefill_combine_kernel(const __grid_constant__ TcParams p) {
   const int gw = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
@@ -1027,9 +1027,22 @@ __global__ void __launch_bounds__(256) prefill_combine_kernel(const __grid_const
   float4 o[R][K];
   bool valid[R];
   size_t dst[R];
+  // The partial loads do not wait for the row's validity (which needs cu_q): every item's 256
+  // rows exist in the workspace, and a row past its request is loaded but not used.
 #pragma unroll
   for (int r = 0; r < R; ++r) {
-    const int gr = gw * R + r;  // global row: split unit gr / 256, row gr % 256 of the unit
+    const int gr = min(gw * R + r, n_rows - 1);  // global row: split unit gr / 256, row gr % 256
+    const int su = gr >> 8, r256 = gr & 255;
+#pragma unroll
+    for (int c = 0; c < K; ++c) {
+      const size_t it = (size_t)split_item(p, su, c) * 256 + r256;
+      lse[r][c] = p.part_lse[it];
+      o[r][c] = *reinterpret_cast<const float4 *>(p.part_o + it * 128 + lane * 4);
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int gr = gw * R + r;
     valid[r] = false;
     dst[r] = 0;
     if (gr < n_rows) {
@@ -1040,16 +1053,8 @@ __global__ void __launch_bounds__(256) prefill_combine_kernel(const __grid_const
       const int32_t qbeg = p.cu_q[b], Tb = p.cu_q[b + 1] - qbeg;
       const int i = r256 >> 7, row = r256 & 127;
       const int t_row = t0 + i * p.TQ + row / p.G;
-      if (t_row < Tb) {
-        valid[r] = true;
-        dst[r] = (size_t)(qbeg + t_row) * p.hq + h * p.G + row % p.G;
-#pragma unroll
-        for (int c = 0; c < K; ++c) {
-          const size_t it = (size_t)split_item(p, su, c) * 256 + r256;
-          lse[r][c] = p.part_lse[it];
-          o[r][c] = *reinterpret_cast<const float4 *>(p.part_o + it * 128 + lane * 4);
-        }
-      }
+      valid[r] = t_row < Tb;
+      dst[r] = (size_t)(qbeg + t_row) * p.hq + h * p.G + row % p.G;
     }
   }
 #pragma unroll
