@@ -223,6 +223,64 @@ def _timed_steps(fn, steps, flush, stream):
     return [a.elapsed_time(b) for a, b in times]
 
 
+def shared_decode_bench(args, flush, stream):
+    """lazy_attn_decode_shared (identical document segments of two requests paired in one
+    fragment, one page load for both) against lazy_attn_decode, on decode_b64 and
+    long_decode_b16, with the page tables in aligned and in context order."""
+    import numpy as np
+    import torch
+
+    import position_independent_kv_lazy_gb300 as pk
+    import workload as W
+    from position_independent_kv_lazy_gb300 import harness as H
+    out = {"note": "the plan is built on the host from the page tables, outside the timed calls"}
+    for name, mk in (("decode_b64", W.decode_workload), ("long_decode_b16",
+                                                         W.long_decode_workload)):
+        wl = mk()
+        src = H.DeviceSource(wl)
+        res = H.build_resident(wl, src)
+        rec = {}
+        for order, align in (("aligned", True), ("context_order", False)):
+            db = H.decode_batch(wl, res, src, align_shared=align)
+            plan_h = pk.lazy_decode_shared_plan(db.words.cpu().numpy().view(np.uint64),
+                                                db.cu_pages.cpu().numpy())
+            plan = plan_h.to("cuda")
+            B = len(db.reqs)
+            o = torch.empty_like(db.q)
+            l = torch.empty((B, wl.Hq), dtype=torch.float32, device="cuda")
+            ws_d = torch.empty(pk.lazy_decode_workspace_bytes(res.pool, B, wl.Hq),
+                               dtype=torch.uint8, device="cuda")
+            ws_s = torch.empty(pk.lazy_decode_shared_workspace_bytes(res.pool, plan.n_units,
+                                                                      wl.Hq),
+                               dtype=torch.uint8, device="cuda")
+            kvb = db.n_keys * wl.kv_bytes_per_token()
+
+            def per_request():
+                pk.lazy_attn_decode(res.pool, db.q, db.q_pos, db.words, db.cu_pages,
+                                    sm_scale=wl.sm_scale, out=o, lse=l, workspace=ws_d)
+
+            def shared():
+                pk.lazy_attn_decode_shared(res.pool, db.q, db.q_pos, plan, sm_scale=wl.sm_scale,
+                                           out=o, lse=l, workspace=ws_s)
+
+            r = {"pages": int(db.cu_pages[-1].item()), "units": plan.n_units,
+                 "entries": plan_h.n_entries}
+            for tag, fn in (("per_request", per_request), ("shared", shared)):
+                for _ in range(args.warmup):
+                    flush(); fn()
+                ms = _timed_steps(fn, max(3, args.steps // 2), flush, stream)
+                med = sorted(ms)[len(ms) // 2]
+                r[tag] = {"value": round(kvb / (med * 1e-3) / 1e9, 2), "unit": "GB/s",
+                          "ms_per_call": round(med, 5)}
+            if pk.lazy_get_device_error(res.pool) != 0:
+                raise RuntimeError("device error in the shared decode bench")
+            rec[order] = r
+        out[name] = rec
+        del res, src
+        torch.cuda.empty_cache()
+    return out
+
+
 def bench_prefill_only(args):
     """Prefill workload alone (pool sized to the documents used): for profiling runs."""
     import torch
@@ -522,6 +580,8 @@ def bench_ours(args):
         line["mixed"] = mixed_sweep(args, flush, stream, hbm_peak)
         torch.cuda.empty_cache()
         line["encode"] = encode_bench(args, flush, stream, hbm_peak)
+        torch.cuda.empty_cache()
+        line["shared_decode"] = shared_decode_bench(args, flush, stream)
     clk.__exit__()
     line["clocks"] = clk.summary(TIMED_WINDOWS)
     if rank == 0 and not args.no_cpu_baseline:

@@ -49,7 +49,8 @@ EXPORTS = [
     "lazy_decode_workspace_bytes", "lazy_attn_decode", "lazy_prefill_workspace_bytes",
     "lazy_attn_prefill", "lazy_get_device_error", "lazy_debug_gather", "lazy_debug_wait_timeout",
     "lazy_attn_decode_noalloc", "lazy_debug_exp2", "lazy_attn_prefill_append",
-    "lazy_pool_set_schedule_sms",
+    "lazy_pool_set_schedule_sms", "lazy_decode_shared_plan", "lazy_decode_shared_workspace_bytes",
+    "lazy_attn_decode_shared",
     "lazy_pool_set_alibi", "lazy_pool_position_mode", "lazy_pool_set_decode_kernel",
 ]
 
@@ -114,6 +115,11 @@ _SIGS = {
     "lazy_debug_exp2": ([_vp, _vp, _i32, _vp], ctypes.c_int),
     "lazy_attn_decode_noalloc": ([_vp, _vp, _vp, _vp, _vp, _i32, _i32, _f32, _i32, _vp, _vp, _vp],
                                  ctypes.c_int),
+    "lazy_decode_shared_plan": ([_vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _pi32, _pi32],
+                                ctypes.c_int),
+    "lazy_decode_shared_workspace_bytes": ([_vp, _i32, _i32, _i32, _psz], ctypes.c_int),
+    "lazy_attn_decode_shared": ([_vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _i32, _i32, _f32,
+                                 _i32, _vp, _vp, _vp, ctypes.c_size_t, _vp], ctypes.c_int),
 }
 
 
@@ -388,6 +394,84 @@ def lazy_attn_decode(pool: LazyPool, q, q_pos, page_words, cu_pages, sm_scale=No
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
     _check("lazy_attn_decode", load_library().lazy_attn_decode(
         pool.handle, _ptr(q), _ptr(q_pos), _ptr(page_words), _ptr(cu_pages), B, Hq,
+        float(sm_scale), grid_ctas, _ptr(out), _ptr(lse), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out, lse
+
+
+class SharedPlan:
+    """A shared-segment decode plan (host numpy arrays; `to(device)` gives torch tensors)."""
+
+    def __init__(self, entries, cu_entries, unit_req, cu_members, members):
+        self.entries = entries          # uint64 [2 * n_entries]
+        self.cu_entries = cu_entries    # int32 [n_units + 1]
+        self.unit_req = unit_req        # int32 [2 * n_units]
+        self.cu_members = cu_members    # int32 [batch + 1]
+        self.members = members          # int32 [n_members]
+        self.n_units = int(len(cu_entries) - 1)
+
+    @property
+    def n_entries(self) -> int:
+        return int(self.cu_entries[-1])
+
+    def to(self, device):
+        import torch
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
+        d = SharedPlan(t(self.entries.view(np.int64)), t(self.cu_entries), t(self.unit_req),
+                       t(self.cu_members), t(self.members))
+        d.n_units = self.n_units
+        return d
+
+
+def lazy_decode_shared_plan(page_words, cu_pages, page_positions: bool = False) -> SharedPlan:
+    """Plan the shared-segment decode from host page tables (numpy uint64 [P], int32 [B+1]);
+    page_positions for ALiBi pools' words (each page's first position)."""
+    w = np.ascontiguousarray(np.asarray(page_words).view(np.uint64))
+    cu = np.ascontiguousarray(np.asarray(cu_pages, dtype=np.int32))
+    B = len(cu) - 1
+    P = int(cu[-1] - cu[0]) if B > 0 else 0
+    entries = np.zeros(max(2 * P, 2), dtype=np.uint64)
+    cu_e = np.zeros(P + 1, dtype=np.int32)
+    unit_req = np.zeros(max(2 * P, 2), dtype=np.int32)
+    cu_m = np.zeros(B + 1, dtype=np.int32)
+    members = np.zeros(max(P, 1), dtype=np.int32)
+    nu, ne = ctypes.c_int32(), ctypes.c_int32()
+    _check("lazy_decode_shared_plan", load_library().lazy_decode_shared_plan(
+        w.ctypes.data, cu.ctypes.data, B, int(bool(page_positions)), entries.ctypes.data,
+        cu_e.ctypes.data,
+        unit_req.ctypes.data, cu_m.ctypes.data, members.ctypes.data, ctypes.byref(nu),
+        ctypes.byref(ne)))
+    nu, ne = nu.value, ne.value
+    return SharedPlan(entries[:2 * ne].copy(), cu_e[:nu + 1].copy(), unit_req[:2 * nu].copy(),
+                      cu_m, members[:int(cu_m[-1])].copy())
+
+
+def lazy_decode_shared_workspace_bytes(pool: LazyPool, n_units: int, num_q_heads: int,
+                                       grid_ctas: int = 0) -> int:
+    n = ctypes.c_size_t()
+    _check("lazy_decode_shared_workspace_bytes", load_library().lazy_decode_shared_workspace_bytes(
+        pool.handle, n_units, num_q_heads, grid_ctas, ctypes.byref(n)))
+    return n.value
+
+
+def lazy_attn_decode_shared(pool: LazyPool, q, q_pos, plan: SharedPlan, sm_scale=None,
+                            grid_ctas: int = 0, out=None, lse=None, workspace=None, stream=None):
+    """lazy_attn_decode over a shared-segment plan (`plan` on q's device: SharedPlan.to).
+    Returns (out [B,Hq,D], lse [B,Hq] float32)."""
+    import torch
+    B, Hq, D = q.shape
+    if sm_scale is None:
+        sm_scale = 1.0 / float(D) ** 0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        nbytes = lazy_decode_shared_workspace_bytes(pool, plan.n_units, Hq, grid_ctas)
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    _check("lazy_attn_decode_shared", load_library().lazy_attn_decode_shared(
+        pool.handle, _ptr(q), _ptr(q_pos), _ptr(plan.entries), _ptr(plan.cu_entries),
+        _ptr(plan.unit_req), plan.n_units, _ptr(plan.cu_members), _ptr(plan.members), B, Hq,
         float(sm_scale), grid_ctas, _ptr(out), _ptr(lse), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
     return out, lse

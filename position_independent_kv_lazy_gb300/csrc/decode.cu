@@ -501,7 +501,11 @@ __device__ __forceinline__ float ex2_fast(float x) {
   return y;
 }
 
-// Per-warp attention state of the tensor-core decode over one unit (request, virtual head).
+// Per-warp attention state of the tensor-core decode over one unit (request, virtual head), or
+// in the shared-segment decode over one (segment unit, kv head) whose fragment rows 0-3 and
+// 4-7 belong to two requests. Everything but the page words is per row, so each thread keeps
+// its own row's position, rotation offset and softmax state. `word` in mma_attend_page is the
+// thread's row's page word (the same block for every live row).
 template <int GC>
 struct MmaWarpState {
   uint32_t qa[8][4];  // A fragments of the rotated, scaled query (hi rows g, lo rows g + 8)
@@ -510,6 +514,7 @@ struct MmaWarpState {
   float m_run, l_run, sl2;
   int32_t m_pos;
   uint32_t cur_off;
+  bool live;  // this thread's fragment row is a real query head
 };
 
 // Start unit (request b, virtual head hv): raw query rows, ALiBi slopes, empty accumulators.
@@ -519,6 +524,7 @@ __device__ __forceinline__ void mma_begin_unit(MmaWarpState<GC> &st, const Decod
   constexpr int D = 128;
   const int g = lane >> 2, t = lane & 3;
   const bool live = g < GC;
+  st.live = live;
   st.m_pos = p.q_pos[b];
   const __nv_bfloat16 *q = reinterpret_cast<const __nv_bfloat16 *>(p.q) +
                            ((size_t)b * p.hq + hv * GC + (live ? g : 0)) * D + 2 * t;
@@ -542,10 +548,12 @@ template <int GC>
 __device__ __forceinline__ void mma_attend_page(MmaWarpState<GC> &st, const DecodeParams &p,
                                                 uint64_t word, uint32_t page_smem, int lane) {
   const int g = lane >> 2, t = lane & 3;  // fragment row group and column pair
-  const bool live = g < GC;               // this thread's row is a real query head
+  const bool live = st.live;
   const bool alibi = p.slopes != nullptr;
   const uint32_t nv = word_nvalid(word);
-  const bool bad = word_block(word) >= (uint32_t)p.num_blocks || nv > (uint32_t)kPage;
+  // The page's MMAs are warp-collective: a bad word in any row skips the page for the warp.
+  const bool bad = __any_sync(0xffffffffu, word_block(word) >= (uint32_t)p.num_blocks ||
+                                               nv > (uint32_t)kPage);
   const uint32_t off = word_offset(word);
   const uint32_t rot_off = alibi ? 0u : off;
   if (!bad) {
@@ -650,7 +658,7 @@ __device__ __forceinline__ void mma_flush(MmaWarpState<GC> &st, const DecodePara
   float l = st.l_run;
   l += __shfl_xor_sync(0xffffffffu, l, 1);
   l += __shfl_xor_sync(0xffffffffu, l, 2);
-  if (g < GC) {
+  if (g < GC && st.live) {  // nobody reads a dead row's slot
     const float inv = l > 0.f ? 1.f / l : 0.f;
     float *dst = p.ws_o + ((size_t)slot * GC + g) * D + 2 * t;
 #pragma unroll
@@ -950,6 +958,275 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
   }
 }
 
+// ------------------------------------------------------------------------------------------------
+// Shared-segment decode. A document cached once sits in many requests' contexts at different
+// logical offsets; in the position-agnostic pool its pages are the same blocks for all of them,
+// and only the query rotation R(m - o) differs per request. A host plan cuts every request's
+// page list into segments (runs of pages with one offset), finds identical segments (the same
+// block and valid-count sequence) across requests and pairs them: a pair unit streams the
+// segment's pages once, with request A's query heads in fragment rows 0-3 and request B's in
+// rows 4-7 (rows the GC = 4 kernel leaves empty), so one page load and one set of MMAs serve both.
+// Unpaired segments (and private ones) are single units with rows 4-7 dead.
+//   entries      uint64 [2 * n_entries]: (word of A, word of B) per page of a unit; B's word is
+//                only read when the unit has a second request
+//   cu_entries   int32 [n_units + 1]
+//   unit_req     int32 [2 * n_units]: requests A and B (-1: none)
+//   cu_members   int32 [batch + 1], members int32: the units of request r as unit * 2 + half
+// ------------------------------------------------------------------------------------------------
+struct MmaSharedParams {
+  MmaDecodeParams m;
+  const uint64_t *entries;
+  const int32_t *cu_entries;
+  const int32_t *unit_req;
+  int32_t n_units;
+  int32_t G;  // query heads per kv head (1, 2 or 4)
+};
+
+template <int STAGES>
+struct MmaSharedSmem {
+  static constexpr int kStage = 0;                                  // STAGES x 8 KB, 1024-aligned
+  static constexpr int kBar = kStage + STAGES * kMmaStageBytes;     // uint64 [STAGES]
+  static constexpr int kWord = kBar + STAGES * 8;                   // uint64 [2 * STAGES]
+  static constexpr int kUnit = kWord + STAGES * 16;                 // int32 [STAGES]
+  static constexpr int kBytes = ((kUnit + STAGES * 4) + 1023) / 1024 * 1024;  // per warp
+};
+
+// Start (segment unit u, kv head h): rows 0-3 take request A's heads h G + r (r < G), rows 4-7
+// request B's.
+__device__ __forceinline__ void mma_begin_shared_unit(MmaWarpState<8> &st,
+                                                      const MmaSharedParams &sp, int32_t u,
+                                                      int32_t h, int lane) {
+  constexpr int D = 128;
+  const DecodeParams &p = sp.m.d;
+  const int g = lane >> 2, t = lane & 3;
+  const int half = g >> 2, r = g & 3;
+  const int32_t req = sp.unit_req[2 * u + half];
+  const bool live = r < sp.G && req >= 0;
+  st.live = live;
+  st.m_pos = live ? p.q_pos[req] : 0;
+  const __nv_bfloat16 *q = reinterpret_cast<const __nv_bfloat16 *>(p.q) +
+                           ((size_t)(live ? req : 0) * p.hq + h * sp.G + (live ? r : 0)) * D +
+                           2 * t;
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    st.qraw[2 * ks] = live ? *reinterpret_cast<const uint32_t *>(q + 16 * ks) : 0u;
+    st.qraw[2 * ks + 1] = live ? *reinterpret_cast<const uint32_t *>(q + 16 * ks + 8) : 0u;
+  }
+  st.sl2 = (p.slopes != nullptr && live) ? p.slopes[h * sp.G + r] * 1.4426950408889634f : 0.f;
+  st.m_run = -INFINITY;
+  st.l_run = 0.f;
+#pragma unroll
+  for (int nt = 0; nt < 16; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) st.o[nt][e] = 0.f;
+  st.cur_off = 0xFFFFFFFFu;
+}
+
+// The decode_mma_kernel partition over the flattened (unit, kv head, entry) sequence; the
+// partial of (unit, kv head) at warp w goes to slot (unit * Hkv + kv head) + w, 8 rows.
+template <int WARPS, int STAGES>
+__global__ void __launch_bounds__(WARPS * 32)
+    decode_shared_kernel(const __grid_constant__ MmaSharedParams sp) {
+  using S = MmaSharedSmem<STAGES>;
+  const DecodeParams &p = sp.m.d;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint8_t *base = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t *ws = base + warp * S::kBytes;
+  uint8_t *stage = ws + S::kStage;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(ws + S::kBar);
+  uint64_t *meta_w = reinterpret_cast<uint64_t *>(ws + S::kWord);
+  int32_t *meta_u = reinterpret_cast<int32_t *>(ws + S::kUnit);
+
+  cudaGridDependencySynchronize();
+  const int32_t NU = sp.n_units, HV = p.hv;
+  const int64_t N = (int64_t)HV * sp.cu_entries[NU];
+  const int64_t WT = (int64_t)gridDim.x * WARPS;
+  const int64_t wg = (int64_t)blockIdx.x * WARPS + warp;
+  const int64_t x0 = wg * N / WT, x1 = (wg + 1) * N / WT;
+  if (x0 >= x1) {
+    cudaTriggerProgrammaticLaunchCompletion();
+    return;
+  }
+  const int64_t n_mine = x1 - x0;
+  if (lane == 0) {
+    for (int s = 0; s < STAGES; ++s) mbar_init(&bars[s], 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+
+  Walker prod;
+  prod.init(x0, sp.cu_entries, NU, HV);
+  uint64_t wa_next = 0, wb_next = 0;
+  auto load_entry = [&]() {
+    const size_t e = (size_t)prod.wbase + prod.pg;
+    wa_next = sp.entries[2 * e];
+    wb_next = sp.entries[2 * e + 1];
+  };
+  if (lane == 0) load_entry();
+  int64_t issued = 0;
+  auto issue_next = [&](int s) {
+    if (lane == 0) {
+      meta_w[2 * s] = wa_next;
+      meta_w[2 * s + 1] = wb_next;
+      meta_u[s] = prod.b * HV + prod.hv;
+      mma_issue_page(sp.m, wa_next, prod.hv, stage + s * kMmaStageBytes, &bars[s]);
+    }
+    prod.advance(sp.cu_entries, NU, HV);
+    ++issued;
+    if (lane == 0 && issued < n_mine) load_entry();
+  };
+  for (int s = 0; s < STAGES && s < n_mine; ++s) issue_next(s);
+
+  MmaWarpState<8> st;
+  int32_t cur_unit = -1;
+  bool timed_out = false;
+  const int half = (lane >> 2) >> 2;
+  for (int64_t i = 0; i < n_mine; ++i) {
+    const int s = (int)(i % STAGES);
+    const uint32_t par = (uint32_t)((i / STAGES) & 1);
+    if (!mbar_wait(&bars[s], par, p.wait_ns)) {
+      if (lane == 0) set_error(p.err, LAZY_DEVERR_TIMEOUT);
+      timed_out = true;
+      const int64_t last = (i + STAGES < n_mine) ? i + STAGES : n_mine;
+      for (int64_t k = i; k < last; ++k)
+        mbar_wait(&bars[k % STAGES], (uint32_t)((k / STAGES) & 1), p.wait_ns);
+      break;
+    }
+    const int32_t unit = meta_u[s];
+    if (unit != cur_unit) {
+      if (cur_unit >= 0) mma_flush(st, p, (int64_t)cur_unit + wg, lane);
+      cur_unit = unit;
+      mma_begin_shared_unit(st, sp, unit / HV, unit % HV, lane);
+    }
+    // a dead row's word is never used for anything but the warp-wide bad-page vote: give it
+    // row A's word so that an absent B cannot veto the page
+    const uint64_t wa = meta_w[2 * s];
+    const uint64_t word = (half && st.live) ? meta_w[2 * s + 1] : wa;
+    mma_attend_page(st, p, word, smem_u32(stage + s * kMmaStageBytes), lane);
+    __syncwarp();
+    if (issued < n_mine) issue_next(s);
+  }
+  cudaTriggerProgrammaticLaunchCompletion();
+  if (!timed_out && cur_unit >= 0) mma_flush(st, p, (int64_t)cur_unit + wg, lane);
+}
+
+struct SharedCombineParams {
+  const float *ws_o;
+  const float *ws_lse;
+  const int32_t *cu_entries;
+  const int32_t *cu_members;
+  const int32_t *members;
+  void *out;
+  float *lse;
+  int32_t batch, hq, hkv, G, n_units;
+  int64_t warps;
+};
+
+// One CTA per (request, kv head): one online log-sum-exp pass over the slots of every unit the
+// request belongs to (rows half * 4 + r of each), then the final rows. The request's units are
+// taken kChunk at a time: their slot ranges are worked out by the CTA's threads in parallel into
+// shared memory, and the pass then loads eight slots at a time across unit boundaries.
+__global__ void __launch_bounds__(128) combine_shared_kernel(const SharedCombineParams p) {
+  constexpr int D = 128, kChunk = 128;
+  __shared__ int64_t s_first[kChunk];  // first slot of the unit's piece range
+  __shared__ int32_t s_count[kChunk];  // slots in the range (0: skip)
+  __shared__ int32_t s_row[kChunk];
+  cudaGridDependencySynchronize();
+  const int32_t b = blockIdx.x / p.hkv, h = blockIdx.x % p.hkv;
+  const int64_t N = (int64_t)p.hkv * p.cu_entries[p.n_units];
+  const int64_t W = p.warps;
+  const bool dense = N >= W;
+  const int32_t m0 = p.cu_members[b], m1 = p.cu_members[b + 1];
+  __nv_bfloat16 *out = reinterpret_cast<__nv_bfloat16 *>(p.out);
+  const bool mine = threadIdx.x < p.G * (D / 4);
+  const int r = threadIdx.x / (D / 4), d4 = threadIdx.x % (D / 4);
+  float mx = -INFINITY, sum = 0.f;
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int32_t c0 = m0; c0 < m1; c0 += kChunk) {
+    const int32_t nc = min(kChunk, m1 - c0);
+    __syncthreads();  // the previous chunk's ranges are no longer read
+    for (int i = threadIdx.x; i < nc; i += blockDim.x) {
+      const int32_t mem = p.members[c0 + i];
+      const int32_t unit = mem >> 1;
+      const int32_t ebase = p.cu_entries[unit], ne = p.cu_entries[unit + 1] - ebase;
+      int64_t wf = 0, wl = -1;
+      if (ne > 0) {
+        const int64_t S = (int64_t)p.hkv * ebase + (int64_t)h * ne, E = S + ne;
+        wf = ((S + 1) * W + N - 1) / N - 1;
+        wl = (E * W + N - 1) / N - 1;
+      }
+      s_first[i] = (int64_t)unit * p.hkv + h + wf;  // slot of the unit's piece at warp wf
+      s_count[i] = (int32_t)(wl - wf + 1);
+      s_row[i] = (mem & 1) * 4;
+      // pieces of warps with empty ranges are not slots (sparse partitions only)
+      if (!dense && ne > 0) {
+        int32_t n_used = 0;
+        for (int64_t w = wf; w <= wl; ++w) n_used += (w * N / W != (w + 1) * N / W);
+        if (n_used != wl - wf + 1) s_count[i] = -(int32_t)(wl - wf + 1);  // check per slot
+      }
+    }
+    __syncthreads();
+    if (!mine) continue;
+    int ci = 0, cw = 0;  // cursor: chunk unit, piece within it
+    while (ci < nc) {
+      float lv[8];
+      float4 ov[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        while (ci < nc && cw >= abs(s_count[ci])) {
+          ++ci;
+          cw = 0;
+        }
+        bool use = ci < nc;
+        size_t slot = 0;
+        int row = 0;
+        if (use) {
+          slot = (size_t)(s_first[ci] + cw);
+          row = s_row[ci] + r;
+          if (s_count[ci] < 0) {  // sparse: skip warps whose range is empty
+            const int64_t w = (int64_t)slot - ((int64_t)(p.members[c0 + ci] >> 1) * p.hkv + h);
+            use = w * N / W != (w + 1) * N / W;
+          }
+          ++cw;
+        }
+        lv[k] = use ? p.ws_lse[slot * 8 + row] : -INFINITY;
+        ov[k] = use ? *reinterpret_cast<const float4 *>(p.ws_o + (slot * 8 + row) * D + d4 * 4)
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      float bm = lv[0];
+#pragma unroll
+      for (int k = 1; k < 8; ++k) bm = fmaxf(bm, lv[k]);
+      if (bm == -INFINITY) continue;
+      const float nm = fmaxf(mx, bm);
+      const float sc = mx == -INFINITY ? 0.f : exp2f(mx - nm);
+      sum *= sc;
+      a.x *= sc; a.y *= sc; a.z *= sc; a.w *= sc;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float wt = lv[k] == -INFINITY ? 0.f : exp2f(lv[k] - nm);
+        sum += wt;
+        a.x = fmaf(wt, ov[k].x, a.x); a.y = fmaf(wt, ov[k].y, a.y);
+        a.z = fmaf(wt, ov[k].z, a.z); a.w = fmaf(wt, ov[k].w, a.w);
+      }
+      mx = nm;
+    }
+  }
+  if (!mine) return;
+  const float inv = sum > 0.f ? 1.f / sum : 0.f;
+  const int qh = h * p.G + r;
+  __nv_bfloat16 *dst = out + ((size_t)b * p.hq + qh) * D + d4 * 4;
+  __nv_bfloat162 v0 = __floats2bfloat162_rn(a.x * inv, a.y * inv);
+  __nv_bfloat162 v1 = __floats2bfloat162_rn(a.z * inv, a.w * inv);
+  uint2 pk;
+  pk.x = *reinterpret_cast<uint32_t *>(&v0);
+  pk.y = *reinterpret_cast<uint32_t *>(&v1);
+  *reinterpret_cast<uint2 *>(dst) = pk;
+  if (d4 == 0)
+    p.lse[(size_t)b * p.hq + qh] = sum > 0.f ? (mx + __log2f(sum)) * 0.69314718055994531f
+                                             : -INFINITY;
+}
+
 constexpr int kWarps = 4;  // warps per CTA of every decode variant
 
 // Two stages (one page in flight while the other is consumed) keep a warp's ring at 16 KB, so
@@ -1130,10 +1407,145 @@ int decode_grid(lazy_pool *p, int32_t gc, int32_t chunks, int32_t grid_ctas, int
   return LAZY_OK;
 }
 
+constexpr int kSharedSmem = MmaSharedSmem<kStages>::kBytes * kWarps + 1024;  // + alignment slack
+
+// CTAs per SM of the shared-segment decode (occupancy query, once).
+int shared_ctas_per_sm() {
+  static int cached = -1;
+  if (cached < 0) {
+    auto fn = decode_shared_kernel<kWarps, kStages>;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSharedSmem) !=
+        cudaSuccess)
+      return -1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kWarps * 32, kSharedSmem) !=
+        cudaSuccess)
+      return -1;
+    cached = std::max(1, n);
+  }
+  return cached;
+}
+
+// The shared-segment decode serves bf16 pools with head_dim 128 and 1, 2 or 4 query heads per
+// kv head (two requests' groups fill the 8 rows of one fragment half each).
+int shared_supported(const lazy_pool *p, int32_t hq) {
+  if (p->dtype != LAZY_DTYPE_BF16 || p->d != 128 || p->page_size != kPage)
+    return LAZY_ERR_UNSUPPORTED;
+  if (hq <= 0 || hq % p->hkv) return LAZY_ERR_INVALID_ARG;
+  const int32_t g = hq / p->hkv;
+  return (g == 1 || g == 2 || g == 4) ? LAZY_OK : LAZY_ERR_UNSUPPORTED;
+}
+
+int shared_grid(lazy_pool *p, int32_t grid_ctas, int *grid) {
+  if (grid_ctas > 0) {
+    *grid = grid_ctas;
+    return LAZY_OK;
+  }
+  const int per_sm = shared_ctas_per_sm();
+  if (per_sm <= 0) return record_cuda(cudaGetLastError(), "decode_shared_kernel set-up");
+  *grid = p->num_sms * per_sm;
+  return LAZY_OK;
+}
+
 }  // namespace
 }  // namespace lazy
 
 using namespace lazy;
+
+extern "C" int lazy_decode_shared_workspace_bytes(lazy_pool *p, int32_t n_units,
+                                                  int32_t num_q_heads, int32_t grid_ctas,
+                                                  size_t *bytes) {
+  if (!p || !bytes || n_units < 0 || grid_ctas < 0) return LAZY_ERR_INVALID_ARG;
+  int rc = shared_supported(p, num_q_heads);
+  if (rc != LAZY_OK) return rc;
+  rc = ensure_device(p);
+  if (rc != LAZY_OK) return rc;
+  int grid;
+  rc = shared_grid(p, grid_ctas, &grid);
+  if (rc != LAZY_OK) return rc;
+  const size_t slots = (size_t)n_units * p->hkv + (size_t)grid * kWarps;
+  *bytes = slots * 8 * ((size_t)p->d + 1) * sizeof(float) + 256;
+  return LAZY_OK;
+}
+
+extern "C" int lazy_attn_decode_shared(lazy_pool *p, const void *q, const int32_t *q_pos,
+                                       const uint64_t *entries, const int32_t *cu_entries,
+                                       const int32_t *unit_req, int32_t n_units,
+                                       const int32_t *cu_members, const int32_t *members,
+                                       int32_t batch, int32_t num_q_heads, float sm_scale,
+                                       int32_t grid_ctas, void *out, float *lse, void *workspace,
+                                       size_t workspace_bytes, lazy_stream_t stream) {
+  if (!p || batch < 0 || n_units < 0 || grid_ctas < 0 || !(sm_scale > 0.f))
+    return LAZY_ERR_INVALID_ARG;
+  if (batch == 0) return LAZY_OK;
+  if (!q || !q_pos || !cu_entries || !cu_members || !out || !lse || !workspace)
+    return LAZY_ERR_INVALID_ARG;
+  if (n_units > 0 && (!entries || !unit_req || !members)) return LAZY_ERR_INVALID_ARG;
+  if (((uintptr_t)q & 15) || ((uintptr_t)out & 15) || ((uintptr_t)workspace & 15) ||
+      ((uintptr_t)entries & 7))
+    return LAZY_ERR_INVALID_ARG;
+  if (p->alibi && num_q_heads != (int32_t)p->slopes.size()) return LAZY_ERR_INVALID_ARG;
+  size_t need = 0;
+  int rc = lazy_decode_shared_workspace_bytes(p, n_units, num_q_heads, grid_ctas, &need);
+  if (rc != LAZY_OK) return rc;
+  if (workspace_bytes < need) return LAZY_ERR_INVALID_ARG;
+  rc = ensure_pool_tmaps(p);
+  if (rc != LAZY_OK) return rc;
+  int grid;
+  rc = shared_grid(p, grid_ctas, &grid);
+  if (rc != LAZY_OK) return rc;
+  const size_t slots = (size_t)n_units * p->hkv + (size_t)grid * kWarps;
+  MmaSharedParams sp;
+  DecodeParams &dp = sp.m.d;
+  memset(&dp, 0, sizeof(dp));
+  dp.q = q;
+  dp.q_pos = q_pos;
+  dp.k_pool = p->k;
+  dp.v_pool = p->v;
+  dp.turn = p->d_turn;
+  dp.ws_o = reinterpret_cast<float *>(workspace);
+  dp.ws_lse = dp.ws_o + slots * 8 * p->d;
+  dp.err = p->d_err;
+  dp.batch = batch;
+  dp.hkv = p->hkv;
+  dp.hq = num_q_heads;
+  dp.num_blocks = p->num_blocks;
+  dp.hv = p->hkv;
+  dp.chunks = 1;
+  dp.scale_log2 = sm_scale * 1.4426950408889634f;
+  dp.wait_ns = p->wait_limit_ns;
+  dp.slopes = p->alibi ? p->d_slopes : nullptr;
+  {
+    std::lock_guard<std::mutex> g(p->mu);
+    memcpy(&sp.m.tm_k, p->tmap_k, sizeof(CUtensorMap));
+    memcpy(&sp.m.tm_v, p->tmap_v, sizeof(CUtensorMap));
+  }
+  sp.entries = entries;
+  sp.cu_entries = cu_entries;
+  sp.unit_req = unit_req;
+  sp.n_units = n_units;
+  sp.G = num_q_heads / p->hkv;
+  SharedCombineParams cp;
+  cp.ws_o = dp.ws_o;
+  cp.ws_lse = dp.ws_lse;
+  cp.cu_entries = cu_entries;
+  cp.cu_members = cu_members;
+  cp.members = members;
+  cp.out = out;
+  cp.lse = lse;
+  cp.batch = batch;
+  cp.hq = num_q_heads;
+  cp.hkv = p->hkv;
+  cp.G = sp.G;
+  cp.n_units = n_units;
+  cp.warps = (int64_t)grid * kWarps;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (n_units > 0)
+    LAZY_CUDA_TRY(launch_pdl(decode_shared_kernel<kWarps, kStages>, grid, kWarps * 32,
+                             kSharedSmem, s, sp));
+  LAZY_CUDA_TRY(launch_pdl(combine_shared_kernel, batch * p->hkv, 128, 0, s, cp));
+  return LAZY_OK;
+}
 
 extern "C" int lazy_decode_workspace_bytes(lazy_pool *p, int32_t batch, int32_t num_q_heads,
                                            int32_t grid_ctas, size_t *bytes) {

@@ -1,0 +1,109 @@
+// Host planner of the shared-segment decode (lazy_decode_shared_plan).
+//
+// The position-agnostic pool stores a document once, and every request that retrieves it lists
+// the same blocks, each at its own logical offset (LazyAttention summaries, core concept: the
+// cache is keyed by content only). In decode the offset only changes the query's rotation
+// R(m - o) (decoding part), so two requests holding the same document can attend its pages in
+// one pass. The planner finds those shared runs in the host copy of the page tables:
+//   - a segment is a maximal run of a request's pages whose offset field repeats (RoPE words
+//     carry the segment's offset: one document, or the private tail) or, for ALiBi words (each
+//     page's first position), advances by the previous page's valid count; it is identified by
+//     its sequence of (block, valid count) words. Any cut is correct, since the decode takes
+//     every row's offset from its own request's word; the cut only decides what can be shared;
+//   - identical segments are grouped in order of first appearance, and a group's members are
+//     paired in order: (m0, m1), (m2, m3), ...; a leftover member is a single unit;
+//   - units of one group are consecutive, so the decode's warps that run them side by side read
+//     the same pages.
+#include <map>
+#include <vector>
+
+#include "pool_internal.h"
+
+namespace {
+
+constexpr uint64_t kOffsetMask = 0x3FFFFFFull << 32;  // page-word bits 32-57
+
+uint32_t offset_of(uint64_t w) { return (uint32_t)((w >> 32) & 0x3FFFFFFu); }
+uint32_t nvalid_of(uint64_t w) { return (uint32_t)(w >> 58) + 1u; }
+
+// Page `cur` continues the segment of page `prev`.
+bool continues(uint64_t prev, uint64_t cur, bool page_positions) {
+  const uint32_t o = offset_of(cur), po = offset_of(prev);
+  return page_positions ? o == po + nvalid_of(prev) : o == po;
+}
+
+struct Segment {
+  int32_t req, start, len;
+};
+
+}  // namespace
+
+extern "C" int lazy_decode_shared_plan(const uint64_t *words, const int32_t *cu_pages,
+                                       int32_t batch, int32_t page_positions,
+                                       uint64_t *entries, int32_t *cu_entries,
+                                       int32_t *unit_req, int32_t *cu_members, int32_t *members,
+                                       int32_t *n_units, int32_t *n_entries) {
+  if (batch < 0 || !cu_pages || !cu_entries || !cu_members || !n_units || !n_entries)
+    return LAZY_ERR_INVALID_ARG;
+  for (int32_t b = 0; b < batch; ++b)
+    if (cu_pages[b] < 0 || cu_pages[b + 1] < cu_pages[b]) return LAZY_ERR_INVALID_ARG;
+  const int32_t total = batch > 0 ? cu_pages[batch] - cu_pages[0] : 0;
+  if (total > 0 && (!words || !entries || !unit_req || !members)) return LAZY_ERR_INVALID_ARG;
+
+  // segments, grouped by content
+  std::map<std::vector<uint64_t>, int32_t> index;
+  std::vector<std::vector<Segment>> groups;
+  for (int32_t b = 0; b < batch; ++b) {
+    int32_t k = cu_pages[b];
+    const int32_t end = cu_pages[b + 1];
+    while (k < end) {
+      int32_t e = k + 1;
+      while (e < end && continues(words[e - 1], words[e], page_positions != 0)) ++e;
+      std::vector<uint64_t> key(e - k);
+      for (int32_t i = k; i < e; ++i) key[i - k] = words[i] & ~kOffsetMask;
+      auto it = index.find(key);
+      int32_t gi;
+      if (it == index.end()) {
+        gi = (int32_t)groups.size();
+        index.emplace(std::move(key), gi);
+        groups.emplace_back();
+      } else {
+        gi = it->second;
+      }
+      groups[gi].push_back({b, k, e - k});
+      k = e;
+    }
+  }
+
+  // units: pairs of members of one group, then a leftover single
+  std::vector<std::vector<int32_t>> per_req(batch > 0 ? batch : 0);
+  int32_t nu = 0, ne = 0;
+  cu_entries[0] = 0;
+  for (const auto &grp : groups) {
+    for (size_t i = 0; i < grp.size(); i += 2) {
+      const Segment &a = grp[i];
+      const bool pair = i + 1 < grp.size();
+      const Segment &bseg = pair ? grp[i + 1] : grp[i];
+      for (int32_t k = 0; k < a.len; ++k) {
+        entries[2 * (size_t)ne] = words[a.start + k];
+        entries[2 * (size_t)ne + 1] = pair ? words[bseg.start + k] : 0ull;
+        ++ne;
+      }
+      unit_req[2 * nu] = a.req;
+      unit_req[2 * nu + 1] = pair ? bseg.req : -1;
+      per_req[a.req].push_back(2 * nu);
+      if (pair) per_req[bseg.req].push_back(2 * nu + 1);
+      ++nu;
+      cu_entries[nu] = ne;
+    }
+  }
+  int32_t nm = 0;
+  cu_members[0] = 0;
+  for (int32_t b = 0; b < batch; ++b) {
+    for (int32_t m : per_req[b]) members[nm++] = m;
+    cu_members[b + 1] = nm;
+  }
+  *n_units = nu;
+  *n_entries = ne;
+  return LAZY_OK;
+}
