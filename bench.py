@@ -355,8 +355,23 @@ def bench_ours(args):
     workspace = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
     out = torch.empty_like(db.q)
     lse = torch.empty((B, wl.Hq), dtype=torch.float32, device="cuda")
+    # The headline decode runs the shared-segment plan of the aligned page tables: identical
+    # document segments of two requests share one fragment and one page load. The plan is host
+    # data derived from the page tables, like them prepared by the serving layer (its build time
+    # is reported as plan_host_ms; a decode step only changes the private tail's last word).
+    t_plan = time.perf_counter()
+    plan_h = pk.lazy_decode_shared_plan(db.words.cpu().numpy().view(np.uint64),
+                                        db.cu_pages.cpu().numpy())
+    plan_host_ms = (time.perf_counter() - t_plan) * 1e3
+    plan = plan_h.to("cuda")
+    sws = torch.empty(pk.lazy_decode_shared_workspace_bytes(res.pool, plan.n_units, wl.Hq),
+                      dtype=torch.uint8, device="cuda")
 
     def decode_call():
+        pk.lazy_attn_decode_shared(res.pool, db.q, db.q_pos, plan, sm_scale=wl.sm_scale,
+                                   out=out, lse=lse, workspace=sws)
+
+    def per_request_call():
         pk.lazy_attn_decode(res.pool, db.q, db.q_pos, db.words, db.cu_pages,
                             sm_scale=wl.sm_scale, out=out, lse=lse, workspace=workspace)
 
@@ -368,7 +383,7 @@ def bench_ours(args):
         pk.kv_pool_write_tokens(res.pool, db.new_k, db.new_v, db.slot_mapping, db.local_pos)
         decode_call()
 
-    launches_per_step = 3  # encode (append) + decode split + combine
+    launches_per_step = 3  # encode (append) + shared decode + its combine
 
     # no-reuse control: same shapes, every request with its own documents (logical = DRAM bytes)
     nwl = W.decode_workload(no_reuse=True, name="decode_b64_no_reuse")
@@ -394,7 +409,8 @@ def bench_ours(args):
             total += (t.numel() * t.element_size() + 255) // 256 * 256
         return offs, total
 
-    in_src = [db.q, db.new_k, db.new_v, db.words, db.cu_pages, db.q_pos, db.slot_mapping,
+    in_src = [db.q, db.new_k, db.new_v, plan.entries, plan.cu_entries, plan.unit_req,
+              plan.cu_members, plan.members, plan.member_entries, db.q_pos, db.slot_mapping,
               db.local_pos]
     in_offs, in_total = _layout(in_src)
     h_in = torch.empty(in_total, dtype=torch.uint8).pin_memory()
@@ -406,8 +422,9 @@ def bench_ours(args):
 
     for t, o in zip(in_src, in_offs):
         _view(h_in, o, t).copy_(t.cpu())
-    (d_q, d_k, d_v, d_words, d_cu, d_pos, d_slot, d_lpos) = [
+    (d_q, d_k, d_v, d_ent, d_cue, d_ureq, d_cum, d_mem, d_ment, d_pos, d_slot, d_lpos) = [
         _view(d_in, o, t) for t, o in zip(in_src, in_offs)]
+    d_plan = pk.SharedPlan(d_ent, d_cue, d_ureq, d_cum, d_mem, d_ment)
     # the result goes device -> host through the decode itself: out and lse live in pinned
     # host memory, which the GPU addresses directly, so the combine writes them there
     out_offs, out_total = _layout([out, lse])
@@ -419,8 +436,8 @@ def bench_ours(args):
     def e2e_step():
         d_in.copy_(h_in, non_blocking=True)
         pk.kv_pool_write_tokens(res.pool, d_k, d_v, d_slot, d_lpos)
-        pk.lazy_attn_decode(res.pool, d_q, d_pos, d_words, d_cu, sm_scale=wl.sm_scale,
-                            out=e_out, lse=e_lse, workspace=workspace)
+        pk.lazy_attn_decode_shared(res.pool, d_q, d_pos, d_plan, sm_scale=wl.sm_scale,
+                                   out=e_out, lse=e_lse, workspace=sws)
 
     only_decode = args.only == "decode"
 
@@ -464,7 +481,7 @@ def bench_ours(args):
     clk = ClockSampler(local).__enter__()
     torch.cuda.synchronize()
     for _ in range(args.warmup):
-        flush(); step(); e2e_step(); no_reuse_call(); context_order_call()
+        flush(); step(); e2e_step(); no_reuse_call(); context_order_call(); per_request_call()
         if not only_decode:
             prefill_call(); long_call()
     torch.cuda.synchronize()
@@ -483,6 +500,7 @@ def bench_ours(args):
     e2e_ms = _timed_steps(e2e_step, args.steps, flush, stream)
     nr_ms = _timed_steps(no_reuse_call, args.steps, flush, stream)
     co_ms = _timed_steps(context_order_call, args.steps, flush, stream)
+    pr_ms = _timed_steps(per_request_call, args.steps, flush, stream)
     if not only_decode:
         pre_ms = _timed_steps(prefill_call, max(3, args.steps // 2), flush, stream)
         long_ms = _timed_steps(long_call, max(3, args.steps // 2), flush, stream)
@@ -497,7 +515,7 @@ def bench_ours(args):
     e2e_avg = sum(e2e_ms) / len(e2e_ms)
 
     traffic = None
-    prof = os.path.join(ROOT, "profiles", "decode_mma_kernel_traffic.json")
+    prof = os.path.join(ROOT, "profiles", TRAFFIC_FILE)
     if os.path.exists(prof):
         try:
             with open(prof) as f:
@@ -524,12 +542,16 @@ def bench_ours(args):
                                "Hq32/Hkv8/D128, base 5e5, page 16",
                    "keys_per_step": db.n_keys, "kv_bytes_per_step": kv_bytes,
                    "l2": "flushed (512 MB write) before every timed step",
+                   "decode_path": "lazy_attn_decode_shared over the aligned page tables' plan",
+                   "plan_units": plan.n_units, "plan_entries": plan_h.n_entries,
+                   "plan_host_ms": round(plan_host_ms, 3),
                    "parallelism": f"replicas x{ws}"},
         "gpu_launches": launches_per_step * args.steps,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
                      "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
                      "traffic": traffic, "peak_kind": peak_kind,
-                     "kernel": "lazy_attn_decode (decode_mma_kernel + combine_kernel)"},
+                     "kernel": "lazy_attn_decode_shared (decode_shared_kernel + "
+                               "combine_shared_kernel)"},
         "e2e": {"value": round(ws * kv_bytes / (e2e_avg * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_avg, 5)},
@@ -539,9 +561,14 @@ def bench_ours(args):
             "value": round(n_bytes / (sum(nr_ms) / len(nr_ms) * 1e-3) / 1e9, 2), "unit": "GB/s",
             "ms_per_call": round(sum(nr_ms) / len(nr_ms), 5),
             "frac": round(n_bytes / (sum(nr_ms) / len(nr_ms) * 1e-3) / 1e9 / hbm_peak, 4)},
+        "decode_per_request": {
+            "workload": "decode_b64, aligned order, through lazy_attn_decode (one unit per "
+                        "request and kv head, no segment pairing)",
+            "value": round(kv_bytes / (sorted(pr_ms)[len(pr_ms) // 2] * 1e-3) / 1e9, 2),
+            "unit": "GB/s", "ms_per_call": round(sorted(pr_ms)[len(pr_ms) // 2], 5)},
         "decode_context_order": {
-            "workload": "decode_b64 with each request's pages in context order (documents not "
-                        "lined up across requests)",
+            "workload": "decode_b64 through lazy_attn_decode with each request's pages in "
+                        "context order (documents not lined up across requests)",
             "value": round(kv_bytes / (sorted(co_ms)[len(co_ms) // 2] * 1e-3) / 1e9, 2),
             "unit": "GB/s", "ms_per_call": round(sorted(co_ms)[len(co_ms) // 2], 5)},
         "decode_tokens_per_s": round(ws * B / (ms_per_step * 1e-3), 1),
@@ -898,10 +925,14 @@ def alibi_bench(args, flush, stream, hbm_peak, tc_peak):
     return out
 
 
-TRAFFIC_SOURCES = ("decode.cu", "lazy_common.cuh")   # what the decode kernel is built from
-TRAFFIC_WORKLOAD = "decode_b64 (64 req x 4161 keys, Hq32/Hkv8/D128 bf16), shared documents aligned"
+# what the decode kernel and its work list are built from
+TRAFFIC_SOURCES = ("decode.cu", "lazy_common.cuh", "shared_plan.cpp")
+TRAFFIC_WORKLOAD = ("decode_b64 (64 req x 4161 keys, Hq32/Hkv8/D128 bf16), shared-segment plan of "
+                    "the aligned page tables")
+TRAFFIC_FILE = "decode_shared_kernel_traffic.json"
+TRAFFIC_KERNEL = "decode_shared_kernel"
 TRAFFIC_COMMAND = ("ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum,"
-                   "lts__t_sector_hit_rate.pct --clock-control none -k regex:decode_mma -s 4 -c 1 "
+                   "lts__t_sector_hit_rate.pct --clock-control none -k regex:decode_shared -s 4 -c 1 "
                    "--csv --log-file gpurun_out/decode_traffic.csv python bench.py --only decode "
                    "--steps 3 --warmup 3 --no-cpu-baseline")
 
@@ -918,7 +949,7 @@ def _kernel_hash():
 
 
 def record_traffic(csv_path):
-    """Write profiles/decode_mma_kernel_traffic.json from the CSV of TRAFFIC_COMMAND (one
+    """Write profiles/TRAFFIC_FILE from the CSV of TRAFFIC_COMMAND (one
     captured launch of the bench's decode kernel), stamped with the current source hash."""
     import csv
     vals, kernel = {}, None
@@ -927,7 +958,7 @@ def record_traffic(csv_path):
     hdr = rows[0]
     ki, mi, vi = hdr.index("Kernel Name"), hdr.index("Metric Name"), hdr.index("Metric Value")
     for r in rows[1:]:
-        if "decode_mma_kernel" not in r[ki]:
+        if TRAFFIC_KERNEL not in r[ki]:
             continue
         kernel = r[ki]
         vals[r[mi]] = float(r[vi].replace(",", ""))
@@ -938,7 +969,7 @@ def record_traffic(csv_path):
            "gpu_time_ns_under_ncu": int(vals.get("gpu__time_duration.sum", 0)),
            "lts_sector_hit_rate_pct": vals.get("lts__t_sector_hit_rate.pct"),
            "command": TRAFFIC_COMMAND}
-    with open(os.path.join(ROOT, "profiles", "decode_mma_kernel_traffic.json"), "w") as f:
+    with open(os.path.join(ROOT, "profiles", TRAFFIC_FILE), "w") as f:
         json.dump(out, f, indent=1)
         f.write("\n")
     print(json.dumps(out))
@@ -1027,8 +1058,8 @@ def main():
                     help="decode / prefill: time only that workload (smaller footprint, for "
                          "profiling)")
     ap.add_argument("--record-traffic", metavar="CSV",
-                    help="write profiles/decode_mma_kernel_traffic.json from the ncu CSV of the "
-                         "traffic capture and exit (no GPU needed)")
+                    help="write the decode traffic profile (profiles/TRAFFIC_FILE) from the "
+                         "ncu CSV of the traffic capture and exit (no GPU needed)")
     args = ap.parse_args()
     if args.record_traffic:
         record_traffic(args.record_traffic)

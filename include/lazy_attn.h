@@ -291,14 +291,14 @@ int lazy_attn_decode_noalloc(lazy_pool *pool, const void *d_q, const int32_t *d_
  *   unit_req    int32 [2 * P]: unit u's requests A and B (B = -1 in single units)
  *   cu_members  int32 [batch + 1], members int32 [P]: request r's units, as unit * 2 + half
  *               (half 0 = A, 1 = B)
- * and receives the unit and entry counts. Copy the five arrays to the device unchanged for
+ *   member_entries int32 [2 * P]: per member, its unit's (first entry, entry count)
+ * and receives the unit and entry counts. Copy the six arrays to the device unchanged for
  * lazy_attn_decode_shared. LAZY_ERR_INVALID_ARG on a null pointer or a decreasing cu_pages.
  */
 int lazy_decode_shared_plan(const uint64_t *h_words, const int32_t *h_cu_pages, int32_t batch,
                             int32_t page_positions, uint64_t *h_entries, int32_t *h_cu_entries,
-                            int32_t *h_unit_req,
-                            int32_t *h_cu_members, int32_t *h_members, int32_t *n_units,
-                            int32_t *n_entries);
+                            int32_t *h_unit_req, int32_t *h_cu_members, int32_t *h_members,
+                            int32_t *h_member_entries, int32_t *n_units, int32_t *n_entries);
 /*
  * Device scratch for lazy_attn_decode_shared: per (unit, kv head) piece of a warp's range, 8
  * rows of fp32 O and lse. grid_ctas as for lazy_attn_decode (0 = one persistent wave).
@@ -311,8 +311,8 @@ int lazy_decode_shared_workspace_bytes(lazy_pool *pool, int32_t n_units, int32_t
  * request B's in the other four, each rotated by its own R(m - o). Arguments:
  *   d_q, d_q_pos, batch, num_q_heads, sm_scale, grid_ctas, d_out, d_lse: as lazy_attn_decode
  *               (d_out / d_lse on the device)
- *   d_entries, d_cu_entries, d_unit_req, n_units, d_cu_members, d_members: the plan, on the
- *               device (entries 8-byte aligned)
+ *   d_entries, d_cu_entries, d_unit_req, n_units, d_cu_members, d_members,
+ *   d_member_entries: the plan, on the device (entries 8-byte aligned)
  *   d_workspace device scratch of lazy_decode_shared_workspace_bytes(...) bytes, 16-byte aligned
  * bf16 pools with head_dim 128 and 1, 2 or 4 query heads per kv head; LAZY_ERR_UNSUPPORTED
  * otherwise. Device errors (bad page words, wait timeouts) as for lazy_attn_decode.
@@ -320,7 +320,8 @@ int lazy_decode_shared_workspace_bytes(lazy_pool *pool, int32_t n_units, int32_t
 int lazy_attn_decode_shared(lazy_pool *pool, const void *d_q, const int32_t *d_q_pos,
                             const uint64_t *d_entries, const int32_t *d_cu_entries,
                             const int32_t *d_unit_req, int32_t n_units,
-                            const int32_t *d_cu_members, const int32_t *d_members, int32_t batch,
+                            const int32_t *d_cu_members, const int32_t *d_members,
+                            const int32_t *d_member_entries, int32_t batch,
                             int32_t num_q_heads, float sm_scale, int32_t grid_ctas, void *d_out,
                             float *d_lse, void *d_workspace, size_t workspace_bytes,
                             lazy_stream_t stream);

@@ -115,11 +115,12 @@ _SIGS = {
     "lazy_debug_exp2": ([_vp, _vp, _i32, _vp], ctypes.c_int),
     "lazy_attn_decode_noalloc": ([_vp, _vp, _vp, _vp, _vp, _i32, _i32, _f32, _i32, _vp, _vp, _vp],
                                  ctypes.c_int),
-    "lazy_decode_shared_plan": ([_vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _pi32, _pi32],
+    "lazy_decode_shared_plan": ([_vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _pi32,
+                                 _pi32],
                                 ctypes.c_int),
     "lazy_decode_shared_workspace_bytes": ([_vp, _i32, _i32, _i32, _psz], ctypes.c_int),
-    "lazy_attn_decode_shared": ([_vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _i32, _i32, _f32,
-                                 _i32, _vp, _vp, _vp, ctypes.c_size_t, _vp], ctypes.c_int),
+    "lazy_attn_decode_shared": ([_vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _i32, _i32,
+                                 _f32, _i32, _vp, _vp, _vp, ctypes.c_size_t, _vp], ctypes.c_int),
 }
 
 
@@ -402,12 +403,13 @@ def lazy_attn_decode(pool: LazyPool, q, q_pos, page_words, cu_pages, sm_scale=No
 class SharedPlan:
     """A shared-segment decode plan (host numpy arrays; `to(device)` gives torch tensors)."""
 
-    def __init__(self, entries, cu_entries, unit_req, cu_members, members):
-        self.entries = entries          # uint64 [2 * n_entries]
-        self.cu_entries = cu_entries    # int32 [n_units + 1]
-        self.unit_req = unit_req        # int32 [2 * n_units]
-        self.cu_members = cu_members    # int32 [batch + 1]
-        self.members = members          # int32 [n_members]
+    def __init__(self, entries, cu_entries, unit_req, cu_members, members, member_entries):
+        self.entries = entries                # uint64 [2 * n_entries]
+        self.cu_entries = cu_entries          # int32 [n_units + 1]
+        self.unit_req = unit_req              # int32 [2 * n_units]
+        self.cu_members = cu_members          # int32 [batch + 1]
+        self.members = members                # int32 [n_members]
+        self.member_entries = member_entries  # int32 [2 * n_members]
         self.n_units = int(len(cu_entries) - 1)
 
     @property
@@ -418,7 +420,7 @@ class SharedPlan:
         import torch
         t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
         d = SharedPlan(t(self.entries.view(np.int64)), t(self.cu_entries), t(self.unit_req),
-                       t(self.cu_members), t(self.members))
+                       t(self.cu_members), t(self.members), t(self.member_entries))
         d.n_units = self.n_units
         return d
 
@@ -435,15 +437,17 @@ def lazy_decode_shared_plan(page_words, cu_pages, page_positions: bool = False) 
     unit_req = np.zeros(max(2 * P, 2), dtype=np.int32)
     cu_m = np.zeros(B + 1, dtype=np.int32)
     members = np.zeros(max(P, 1), dtype=np.int32)
+    member_entries = np.zeros(max(2 * P, 2), dtype=np.int32)
     nu, ne = ctypes.c_int32(), ctypes.c_int32()
     _check("lazy_decode_shared_plan", load_library().lazy_decode_shared_plan(
         w.ctypes.data, cu.ctypes.data, B, int(bool(page_positions)), entries.ctypes.data,
         cu_e.ctypes.data,
-        unit_req.ctypes.data, cu_m.ctypes.data, members.ctypes.data, ctypes.byref(nu),
-        ctypes.byref(ne)))
+        unit_req.ctypes.data, cu_m.ctypes.data, members.ctypes.data, member_entries.ctypes.data,
+        ctypes.byref(nu), ctypes.byref(ne)))
     nu, ne = nu.value, ne.value
+    nm = int(cu_m[-1])
     return SharedPlan(entries[:2 * ne].copy(), cu_e[:nu + 1].copy(), unit_req[:2 * nu].copy(),
-                      cu_m, members[:int(cu_m[-1])].copy())
+                      cu_m, members[:nm].copy(), member_entries[:2 * nm].copy())
 
 
 def lazy_decode_shared_workspace_bytes(pool: LazyPool, n_units: int, num_q_heads: int,
@@ -471,7 +475,8 @@ def lazy_attn_decode_shared(pool: LazyPool, q, q_pos, plan: SharedPlan, sm_scale
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
     _check("lazy_attn_decode_shared", load_library().lazy_attn_decode_shared(
         pool.handle, _ptr(q), _ptr(q_pos), _ptr(plan.entries), _ptr(plan.cu_entries),
-        _ptr(plan.unit_req), plan.n_units, _ptr(plan.cu_members), _ptr(plan.members), B, Hq,
+        _ptr(plan.unit_req), plan.n_units, _ptr(plan.cu_members), _ptr(plan.members),
+        _ptr(plan.member_entries), B, Hq,
         float(sm_scale), grid_ctas, _ptr(out), _ptr(lse), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
     return out, lse

@@ -972,6 +972,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
 //   cu_entries   int32 [n_units + 1]
 //   unit_req     int32 [2 * n_units]: requests A and B (-1: none)
 //   cu_members   int32 [batch + 1], members int32: the units of request r as unit * 2 + half
+//   member_entries int32 [2 * n_members]: each membership's unit (first entry, entry count)
 // ------------------------------------------------------------------------------------------------
 struct MmaSharedParams {
   MmaDecodeParams m;
@@ -1117,6 +1118,7 @@ struct SharedCombineParams {
   const int32_t *cu_entries;
   const int32_t *cu_members;
   const int32_t *members;
+  const int32_t *member_entries;  // per membership: its unit's (first entry, entry count)
   void *out;
   float *lse;
   int32_t batch, hq, hkv, G, n_units;
@@ -1128,7 +1130,7 @@ struct SharedCombineParams {
 // taken kChunk at a time: their slot ranges are worked out by the CTA's threads in parallel into
 // shared memory, and the pass then loads eight slots at a time across unit boundaries.
 __global__ void __launch_bounds__(128) combine_shared_kernel(const SharedCombineParams p) {
-  constexpr int D = 128, kChunk = 128;
+  constexpr int D = 128, kChunk = 128, kBatch = 16;
   __shared__ int64_t s_first[kChunk];  // first slot of the unit's piece range
   __shared__ int32_t s_count[kChunk];  // slots in the range (0: skip)
   __shared__ int32_t s_row[kChunk];
@@ -1149,7 +1151,9 @@ __global__ void __launch_bounds__(128) combine_shared_kernel(const SharedCombine
     for (int i = threadIdx.x; i < nc; i += blockDim.x) {
       const int32_t mem = p.members[c0 + i];
       const int32_t unit = mem >> 1;
-      const int32_t ebase = p.cu_entries[unit], ne = p.cu_entries[unit + 1] - ebase;
+      // the unit's entry range, stored with the membership (no dependent load of cu_entries)
+      const int32_t ebase = p.member_entries[2 * (c0 + i)];
+      const int32_t ne = p.member_entries[2 * (c0 + i) + 1];
       int64_t wf = 0, wl = -1;
       if (ne > 0) {
         const int64_t S = (int64_t)p.hkv * ebase + (int64_t)h * ne, E = S + ne;
@@ -1170,10 +1174,10 @@ __global__ void __launch_bounds__(128) combine_shared_kernel(const SharedCombine
     if (!mine) continue;
     int ci = 0, cw = 0;  // cursor: chunk unit, piece within it
     while (ci < nc) {
-      float lv[8];
-      float4 ov[8];
+      float lv[kBatch];
+      float4 ov[kBatch];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
+      for (int k = 0; k < kBatch; ++k) {
         while (ci < nc && cw >= abs(s_count[ci])) {
           ++ci;
           cw = 0;
@@ -1196,14 +1200,14 @@ __global__ void __launch_bounds__(128) combine_shared_kernel(const SharedCombine
       }
       float bm = lv[0];
 #pragma unroll
-      for (int k = 1; k < 8; ++k) bm = fmaxf(bm, lv[k]);
+      for (int k = 1; k < kBatch; ++k) bm = fmaxf(bm, lv[k]);
       if (bm == -INFINITY) continue;
       const float nm = fmaxf(mx, bm);
       const float sc = mx == -INFINITY ? 0.f : exp2f(mx - nm);
       sum *= sc;
       a.x *= sc; a.y *= sc; a.z *= sc; a.w *= sc;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
+      for (int k = 0; k < kBatch; ++k) {
         const float wt = lv[k] == -INFINITY ? 0.f : exp2f(lv[k] - nm);
         sum += wt;
         a.x = fmaf(wt, ov[k].x, a.x); a.y = fmaf(wt, ov[k].y, a.y);
@@ -1472,7 +1476,7 @@ extern "C" int lazy_attn_decode_shared(lazy_pool *p, const void *q, const int32_
                                        const uint64_t *entries, const int32_t *cu_entries,
                                        const int32_t *unit_req, int32_t n_units,
                                        const int32_t *cu_members, const int32_t *members,
-                                       int32_t batch, int32_t num_q_heads, float sm_scale,
+                                       const int32_t *member_entries, int32_t batch, int32_t num_q_heads, float sm_scale,
                                        int32_t grid_ctas, void *out, float *lse, void *workspace,
                                        size_t workspace_bytes, lazy_stream_t stream) {
   if (!p || batch < 0 || n_units < 0 || grid_ctas < 0 || !(sm_scale > 0.f))
@@ -1480,7 +1484,8 @@ extern "C" int lazy_attn_decode_shared(lazy_pool *p, const void *q, const int32_
   if (batch == 0) return LAZY_OK;
   if (!q || !q_pos || !cu_entries || !cu_members || !out || !lse || !workspace)
     return LAZY_ERR_INVALID_ARG;
-  if (n_units > 0 && (!entries || !unit_req || !members)) return LAZY_ERR_INVALID_ARG;
+  if (n_units > 0 && (!entries || !unit_req || !members || !member_entries))
+    return LAZY_ERR_INVALID_ARG;
   if (((uintptr_t)q & 15) || ((uintptr_t)out & 15) || ((uintptr_t)workspace & 15) ||
       ((uintptr_t)entries & 7))
     return LAZY_ERR_INVALID_ARG;
@@ -1531,6 +1536,7 @@ extern "C" int lazy_attn_decode_shared(lazy_pool *p, const void *q, const int32_
   cp.cu_entries = cu_entries;
   cp.cu_members = cu_members;
   cp.members = members;
+  cp.member_entries = member_entries;
   cp.out = out;
   cp.lse = lse;
   cp.batch = batch;

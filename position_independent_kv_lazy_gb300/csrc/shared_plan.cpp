@@ -11,9 +11,13 @@
 //     its sequence of (block, valid count) words. Any cut is correct, since the decode takes
 //     every row's offset from its own request's word; the cut only decides what can be shared;
 //   - identical segments are grouped in order of first appearance, and a group's members are
-//     paired in order: (m0, m1), (m2, m3), ...; a leftover member is a single unit;
+//     paired in order: (m0, m1), (m2, m3), ...; a leftover member is a single unit, placed right
+//     after its group's pairs, so that it re-reads their pages while they are in L2;
 //   - units of one group are consecutive, so the decode's warps that run them side by side read
-//     the same pages.
+//     the same pages;
+//   - a request's segments that no other segment matches (its private tail, documents only it
+//     holds) become one single unit per request, after all groups: fewer unit switches, whose
+//     query loads stall a warp, and fewer partial slots.
 #include <map>
 #include <vector>
 
@@ -42,13 +46,15 @@ extern "C" int lazy_decode_shared_plan(const uint64_t *words, const int32_t *cu_
                                        int32_t batch, int32_t page_positions,
                                        uint64_t *entries, int32_t *cu_entries,
                                        int32_t *unit_req, int32_t *cu_members, int32_t *members,
-                                       int32_t *n_units, int32_t *n_entries) {
+                                       int32_t *member_entries, int32_t *n_units,
+                                       int32_t *n_entries) {
   if (batch < 0 || !cu_pages || !cu_entries || !cu_members || !n_units || !n_entries)
     return LAZY_ERR_INVALID_ARG;
   for (int32_t b = 0; b < batch; ++b)
     if (cu_pages[b] < 0 || cu_pages[b + 1] < cu_pages[b]) return LAZY_ERR_INVALID_ARG;
   const int32_t total = batch > 0 ? cu_pages[batch] - cu_pages[0] : 0;
-  if (total > 0 && (!words || !entries || !unit_req || !members)) return LAZY_ERR_INVALID_ARG;
+  if (total > 0 && (!words || !entries || !unit_req || !members || !member_entries))
+    return LAZY_ERR_INVALID_ARG;
 
   // segments, grouped by content
   std::map<std::vector<uint64_t>, int32_t> index;
@@ -79,7 +85,13 @@ extern "C" int lazy_decode_shared_plan(const uint64_t *words, const int32_t *cu_
   std::vector<std::vector<int32_t>> per_req(batch > 0 ? batch : 0);
   int32_t nu = 0, ne = 0;
   cu_entries[0] = 0;
+  // unshared segments, per request, for the merged single units at the end
+  std::vector<std::vector<Segment>> lone(batch > 0 ? batch : 0);
   for (const auto &grp : groups) {
+    if (grp.size() == 1) {
+      lone[grp[0].req].push_back(grp[0]);
+      continue;
+    }
     for (size_t i = 0; i < grp.size(); i += 2) {
       const Segment &a = grp[i];
       const bool pair = i + 1 < grp.size();
@@ -97,10 +109,29 @@ extern "C" int lazy_decode_shared_plan(const uint64_t *words, const int32_t *cu_
       cu_entries[nu] = ne;
     }
   }
+  for (int32_t b = 0; b < batch; ++b) {
+    if (lone[b].empty()) continue;
+    for (const Segment &sg : lone[b])
+      for (int32_t k = 0; k < sg.len; ++k) {
+        entries[2 * (size_t)ne] = words[sg.start + k];
+        entries[2 * (size_t)ne + 1] = 0ull;
+        ++ne;
+      }
+    unit_req[2 * nu] = b;
+    unit_req[2 * nu + 1] = -1;
+    per_req[b].push_back(2 * nu);
+    ++nu;
+    cu_entries[nu] = ne;
+  }
   int32_t nm = 0;
   cu_members[0] = 0;
   for (int32_t b = 0; b < batch; ++b) {
-    for (int32_t m : per_req[b]) members[nm++] = m;
+    for (int32_t m : per_req[b]) {
+      const int32_t u = m >> 1;
+      member_entries[2 * nm] = cu_entries[u];
+      member_entries[2 * nm + 1] = cu_entries[u + 1] - cu_entries[u];
+      members[nm++] = m;
+    }
     cu_members[b + 1] = nm;
   }
   *n_units = nu;

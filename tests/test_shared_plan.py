@@ -33,8 +33,12 @@ def _check_plan(words, cu, plan):
         assert sorted(seen.get(r, [])) == mine, r
         # the member list names exactly the units (and halves) that hold request r
         mem = plan.members[plan.cu_members[r]:plan.cu_members[r + 1]]
-        for m in mem:
+        ment = plan.member_entries[2 * plan.cu_members[r]:2 * plan.cu_members[r + 1]]
+        for i, m in enumerate(mem):
             assert plan.unit_req[2 * (m >> 1) + (m & 1)] == r
+            u = m >> 1
+            assert ment[2 * i] == plan.cu_entries[u]
+            assert ment[2 * i + 1] == plan.cu_entries[u + 1] - plan.cu_entries[u]
         n_units_with_r = sum(int(plan.unit_req[2 * u] == r) + int(plan.unit_req[2 * u + 1] == r)
                              for u in range(plan.n_units))
         assert len(mem) == n_units_with_r
@@ -67,7 +71,9 @@ def test_group_of_r_members_gives_r_over_2_pairs():
         _check_plan(w, cu, plan)
         pairs = sum(int(plan.unit_req[2 * u + 1] >= 0) for u in range(plan.n_units))
         assert pairs == r // 2
-        assert plan.n_units == r + (r + 1) // 2  # r private singles + the document's units
+        # r private tails (each its request's merged single unit) + the document's units; a
+        # document held by one request joins that request's single unit
+        assert plan.n_units == r + ((r + 1) // 2 if r > 1 else 0)
         assert plan.n_entries == r + 4 * ((r + 1) // 2)
 
 
@@ -136,6 +142,9 @@ def test_decode_workload_plan(align):
     plan = pk.lazy_decode_shared_plan(w, cu)
     _check_plan(w, cu, plan)
     refs = collections.Counter(d for r in wl.requests for d in r.docs)
-    want_doc_units = sum((n + 1) // 2 for n in refs.values())
+    # shared documents: ceil(n / 2) units each; every request's private tail and the documents
+    # only it holds: one merged single unit per request
+    want_doc_units = sum((n + 1) // 2 for n in refs.values() if n > 1)
     assert plan.n_units == want_doc_units + len(wl.requests)
-    assert plan.n_entries == 32 * want_doc_units + 5 * len(wl.requests)
+    lone = sum(1 for n in refs.values() if n == 1)
+    assert plan.n_entries == 32 * (want_doc_units + lone) + 5 * len(wl.requests)
