@@ -282,8 +282,9 @@ int lazy_attn_decode_noalloc(lazy_pool *pool, const void *d_q, const int32_t *d_
  * segments (same block and valid-count sequence) across requests and pairs each group's members
  * in order; a leftover member, and every unshared segment, is a single unit. A segment is a
  * maximal run of pages with one offset field (page_positions = 0: RoPE pools, whose words carry
- * the segment's offset) or whose offset advances by the previous page's valid count
- * (page_positions = 1: ALiBi pools, whose words carry each page's first position).
+ * the segment's offset) or whose offset advances by the previous page's valid count while the
+ * block id advances by one (page_positions = 1: ALiBi pools, whose words carry each page's
+ * first position). Any cut gives the same attention; the cut only decides what is shared.
  * With P = cu_pages[batch] - cu_pages[0] pages, the caller provides (host):
  *   entries     uint64 [2 * P]: per page of each unit, (word of request A, word of request B);
  *               B's word is 0 in single units

@@ -7,9 +7,11 @@
 // one pass. The planner finds those shared runs in the host copy of the page tables:
 //   - a segment is a maximal run of a request's pages whose offset field repeats (RoPE words
 //     carry the segment's offset: one document, or the private tail) or, for ALiBi words (each
-//     page's first position), advances by the previous page's valid count; it is identified by
-//     its sequence of (block, valid count) words. Any cut is correct, since the decode takes
-//     every row's offset from its own request's word; the cut only decides what can be shared;
+//     page's first position, which runs on across documents), advances by the previous page's
+//     valid count while the block id advances by one (a document is encoded into consecutive
+//     blocks; two documents rarely sit in a context in block order); it is identified by its
+//     sequence of (block, valid count) words. Any cut is correct, since the decode takes every
+//     row's offset from its own request's word; the cut only decides what can be shared;
 //   - identical segments are grouped in order of first appearance, and a group's members are
 //     paired in order: (m0, m1), (m2, m3), ...; a leftover member is a single unit, placed right
 //     after its group's pairs, so that it re-reads their pages while they are in L2;
@@ -33,7 +35,8 @@ uint32_t nvalid_of(uint64_t w) { return (uint32_t)(w >> 58) + 1u; }
 // Page `cur` continues the segment of page `prev`.
 bool continues(uint64_t prev, uint64_t cur, bool page_positions) {
   const uint32_t o = offset_of(cur), po = offset_of(prev);
-  return page_positions ? o == po + nvalid_of(prev) : o == po;
+  if (!page_positions) return o == po;
+  return o == po + nvalid_of(prev) && (uint32_t)cur == (uint32_t)prev + 1u;
 }
 
 struct Segment {

@@ -100,22 +100,32 @@ def test_empty_batch_and_empty_requests():
     assert list(plan.cu_members) == [0, 0, 1, 1]
 
 
-def test_alibi_page_positions_run_across_documents():
-    # ALiBi words carry each page's first position, which advances through the whole context,
-    # so a request is one segment: only requests whose whole page sequences match are paired
+def test_alibi_page_positions_cut_at_block_jumps():
+    # ALiBi words carry each page's first position, which runs on through the whole context;
+    # documents are cut where the block id stops advancing by one
     D = (list(range(60, 63)), 0, 40)
     reqs = [[([1], 0, 16), (D[0], 16, 40)], [(D[0], 300, 40), ([2], 340, 8)],
             [([1], 1000, 16), (D[0], 1016, 40)]]
     w, cu = pk.build_page_table(reqs, 16, page_positions=True)
     plan = pk.lazy_decode_shared_plan(w, cu, page_positions=True)
     _check_plan(w, cu, plan)
-    assert plan.n_units == 2
-    pairs = [u for u in range(plan.n_units) if plan.unit_req[2 * u + 1] >= 0]
-    assert len(pairs) == 1 and list(plan.unit_req[2 * pairs[0]:2 * pairs[0] + 2]) == [0, 2]
+    # D is shared by all three requests (one pair, one leftover next to it); [1] by requests 0
+    # and 2 (one pair); [2] only by request 1 (its merged single unit)
+    pairs = [tuple(plan.unit_req[2 * u:2 * u + 2]) for u in range(plan.n_units)
+             if plan.unit_req[2 * u + 1] >= 0]
+    assert sorted(pairs) == [(0, 1), (0, 2)]
+    assert plan.n_units == 4
+    # a document whose blocks follow another's in the context joins it in one segment
+    E = (list(range(63, 65)), 0, 32)
+    reqs = [[(D[0], 0, 48), (E[0], 48, 32)], [(D[0], 100, 48)]]
+    w, cu = pk.build_page_table(reqs, 16, page_positions=True)
+    plan = pk.lazy_decode_shared_plan(w, cu, page_positions=True)
+    _check_plan(w, cu, plan)
+    assert all(plan.unit_req[2 * u + 1] < 0 for u in range(plan.n_units))
     # the same tables read as RoPE words (one offset per segment) cut at every page
     plan = pk.lazy_decode_shared_plan(w, cu)
     _check_plan(w, cu, plan)
-    assert plan.n_entries == int(cu[-1]) - 4  # four pages of requests 0 and 2 are paired
+    assert sum(int(plan.unit_req[2 * u + 1] >= 0) for u in range(plan.n_units)) == 3
 
 
 def test_decreasing_cu_pages_is_rejected():
