@@ -551,9 +551,11 @@ __device__ __forceinline__ void mma_attend_page(MmaWarpState<GC> &st, const Deco
   const bool live = st.live;
   const bool alibi = p.slopes != nullptr;
   const uint32_t nv = word_nvalid(word);
-  // The page's MMAs are warp-collective: a bad word in any row skips the page for the warp.
+  // The page's MMAs are warp-collective: a bad word in any row skips the page for the warp,
+  // and is reported (the producer also reports the word it loads).
   const bool bad = __any_sync(0xffffffffu, word_block(word) >= (uint32_t)p.num_blocks ||
                                                nv > (uint32_t)kPage);
+  if (bad && lane == 0) set_error(p.err, LAZY_DEVERR_BAD_PAGE);
   const uint32_t off = word_offset(word);
   const uint32_t rot_off = alibi ? 0u : off;
   if (!bad) {
@@ -1101,9 +1103,14 @@ __global__ void __launch_bounds__(WARPS * 32)
       mma_begin_shared_unit(st, sp, unit / HV, unit % HV, lane);
     }
     // a dead row's word is never used for anything but the warp-wide bad-page vote: give it
-    // row A's word so that an absent B cannot veto the page
+    // row A's word so that an absent B cannot veto the page. B's word must name the block that
+    // was loaded (A's); a plan that pairs different blocks makes it a bad word.
     const uint64_t wa = meta_w[2 * s];
-    const uint64_t word = (half && st.live) ? meta_w[2 * s + 1] : wa;
+    uint64_t word = wa;
+    if (half && st.live) {
+      const uint64_t wb = meta_w[2 * s + 1];
+      word = word_block(wb) == word_block(wa) ? wb : ~0ull;
+    }
     mma_attend_page(st, p, word, smem_u32(stage + s * kMmaStageBytes), lane);
     __syncwarp();
     if (issued < n_mine) issue_next(s);

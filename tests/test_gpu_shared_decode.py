@@ -169,6 +169,38 @@ def test_shared_decode_full_size_sampled(pk):
     _check(wl, o_s, l_s, reqs=[0, 17, 63], kv_heads=[0, 5], src=src.host_view())
 
 
+@pytest.mark.parametrize("which", ["a_out_of_range", "b_out_of_range", "b_other_block"])
+def test_shared_decode_bad_entry_sets_flag_without_fault(pk, which):
+    # a corrupted entry of a pair unit (request A's word, request B's word, or a B word naming
+    # another block than A's) is reported as LAZY_DEVERR_BAD_PAGE; a clean call afterwards is exact
+    H = _h()
+    wl = _edge(32, 8)
+    src = H.HostSource(wl)
+    res = H.build_resident(wl, src, resident_pool=False)
+    db = H.decode_batch(wl, res, src)
+    host_plan, plan = _plan(pk, db)
+    u = next(u for u in range(host_plan.n_units) if host_plan.unit_req[2 * u + 1] >= 0)
+    e = int(host_plan.cu_entries[u])
+    ent = plan.entries.clone()
+    w = np.array(ent[2 * e:2 * e + 2].cpu().numpy()).view(np.uint64)
+    if which == "a_out_of_range":
+        ent[2 * e] = int(pk.lazy_pack_page(res.pool.num_blocks + 5, 0, 16))
+    elif which == "b_out_of_range":
+        ent[2 * e + 1] = int(pk.lazy_pack_page(res.pool.num_blocks + 5, 0, 16))
+    else:
+        other = (int(w[0]) & 0xFFFFFFFF) ^ 1
+        ent[2 * e + 1] = int(pk.lazy_pack_page(other, 0, 16))
+    bad = pk.SharedPlan(ent, plan.cu_entries, plan.unit_req, plan.cu_members, plan.members,
+                        plan.member_entries)
+    pk.lazy_attn_decode_shared(res.pool, db.q, db.q_pos, bad, sm_scale=wl.sm_scale)
+    assert pk.lazy_get_device_error(res.pool) & pk.LAZY_DEVERR_BAD_PAGE
+    assert pk.lazy_get_device_error(res.pool) == 0
+    out, lse = pk.lazy_attn_decode_shared(res.pool, db.q, db.q_pos, plan, sm_scale=wl.sm_scale)
+    torch.cuda.synchronize()
+    assert pk.lazy_get_device_error(res.pool) == 0
+    _check(wl, out.float().cpu().numpy(), lse.cpu().numpy())
+
+
 def test_shared_decode_rejects_unsupported_groups(pk):
     # 8 query heads per kv head fill a whole fragment half pair: not served by this path
     H = _h()
