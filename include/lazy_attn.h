@@ -68,7 +68,11 @@ enum {
                                (num_q_heads / num_kv_heads) is a power of two <= 32; else
                                CUDA-core */
     LAZY_PREFILL_SIMT = 1,  /* CUDA-core kernel, fp32 arithmetic, group size <= 64 */
-    LAZY_PREFILL_TC = 2     /* tcgen05/TMEM kernel; LAZY_ERR_UNSUPPORTED if the shape is not */
+    LAZY_PREFILL_TC = 2,    /* tcgen05/TMEM kernel; LAZY_ERR_UNSUPPORTED if the shape is not */
+    LAZY_PREFILL_SIMT_QSIDE = 3  /* the CUDA-core kernel with the query-side variant of the
+                                    relative rotation: cached key pages are used as stored
+                                    (R(j) k) and the queries take R(m - o) once per document
+                                    offset o, instead of every key page taking R(o - m0) */
 };
 
 /* ---------------------------------------------------------------------------------------
@@ -348,7 +352,7 @@ int lazy_attn_decode_shared(lazy_pool *pool, const void *d_q, const int32_t *d_q
  *   total_q      host: d_cu_q[batch]; max_q_len host: max_b (d_cu_q[b+1]-d_cu_q[b]).
  *   d_out        device [total_q][num_q_heads][head_dim] pool dtype; d_lse float [total_q][Hq].
  *   d_workspace  device scratch of lazy_prefill_workspace_bytes(...) bytes (may be 0).
- *   flags        LAZY_PREFILL_AUTO / _SIMT / _TC.
+ *   flags        LAZY_PREFILL_AUTO / _SIMT / _TC / _SIMT_QSIDE.
  */
 int lazy_prefill_workspace_bytes(lazy_pool *pool, int32_t batch, int32_t total_q,
                                  int32_t max_q_len, int32_t num_q_heads, int32_t flags,

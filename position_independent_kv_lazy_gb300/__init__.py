@@ -39,6 +39,7 @@ LAZY_DEVERR_TIMEOUT = 2
 LAZY_PREFILL_AUTO = 0
 LAZY_PREFILL_SIMT = 1
 LAZY_PREFILL_TC = 2
+LAZY_PREFILL_SIMT_QSIDE = 3
 
 # Every symbol declared in include/lazy_attn.h (checked by the tests).
 EXPORTS = [

@@ -28,6 +28,7 @@ struct PrefillParams {
   const float *slopes;  // ALiBi pools: per query head (device); nullptr for RoPE pools
   void *workspace;      // caller's scratch (tensor-core path: partial results of split units)
   size_t workspace_bytes;
+  int32_t qside;        // CUDA-core path: query-side rotation per document offset
 };
 
 int prefill_simt(lazy_pool *p, const PrefillParams &pp, int32_t max_q_len, cudaStream_t s);

@@ -8,6 +8,12 @@
 // relative rotation R(o - m0) (its rows already carry R(j) from the encode), instead of an
 // un-rotate to 0 followed by a re-rotate to the target position. The question's own keys (raw)
 // are rotated by R(p - m0) and attended causally.
+//
+// Query-side variant (QS, LAZY_PREFILL_SIMT_QSIDE; the summaries' prefill part allows rotating
+// either side): cached key pages are used as stored, R(j) k, and when the document offset o of
+// the pages changes the query rows R(m - m0) q get R(m0 - o) once, into a second buffer, so a
+// document of L_d keys costs one rotation of the 64 query rows instead of L_d key rotations.
+// (R(m0 - o) R(m - m0) q) . (R(j) k) = (R(m - o) q) . (R(j) k) = (R(m) q) . (R(o + j) k).
 #include <algorithm>
 
 #include "lazy_common.cuh"
@@ -20,7 +26,7 @@ namespace {
 constexpr int kRows = 64;
 constexpr int kThreads = 128;
 
-template <int D>
+template <int D, bool QS>
 struct SimtSmem {
   static constexpr int kQ = 0;                          // float [kRows][D+1]
   static constexpr int kK = kQ + kRows * (D + 1) * 4;   // float [kPage][D+1]
@@ -28,12 +34,15 @@ struct SimtSmem {
   static constexpr int kP = kV + kPage * D * 4;         // float [kRows][kPage+1]
   static constexpr int kKt = kP + kRows * (kPage + 1) * 4;  // int32 [kPage] key token (-1 = doc)
   static constexpr int kKp = kKt + kPage * 4;               // int32 [kPage] key logical position
-  static constexpr int kBytes = kKp + kPage * 4;
+  // QS: the query rows rotated to the current document, and that document's (cos, sin)
+  static constexpr int kQd = kKp + kPage * 4;               // float [kRows][D+1]
+  static constexpr int kCs = kQd + (QS ? kRows * (D + 1) * 4 : 0);  // float [D/2][2]
+  static constexpr int kBytes = kCs + (QS ? D * 4 : 0);
 };
 
-template <typename T, int D>
+template <typename T, int D, bool QS>
 __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(const PrefillParams p) {
-  using S = SimtSmem<D>;
+  using S = SimtSmem<D, QS>;
   extern __shared__ __align__(16) uint8_t smem_raw[];
   float *Qs = reinterpret_cast<float *>(smem_raw + S::kQ);
   float *Ks = reinterpret_cast<float *>(smem_raw + S::kK);
@@ -41,8 +50,12 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(const PrefillPar
   float *Ps = reinterpret_cast<float *>(smem_raw + S::kP);
   int32_t *Kt = reinterpret_cast<int32_t *>(smem_raw + S::kKt);
   int32_t *Kp = reinterpret_cast<int32_t *>(smem_raw + S::kKp);
+  float *Qd = reinterpret_cast<float *>(smem_raw + S::kQd);
+  float *Cs = reinterpret_cast<float *>(smem_raw + S::kCs);
   // ALiBi pools: no rotation anywhere; scores get slope * (n - m) instead
   const bool alibi = p.slopes != nullptr;
+  const bool qside = QS && !alibi;
+  uint32_t q_off = 0xFFFFFFFFu;  // document offset the rows in Qd are rotated to
 
   const int b = blockIdx.z, h = blockIdx.y;
   const int G = p.G, TQ = p.TQ;
@@ -101,6 +114,36 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(const PrefillPar
       if (blk >= (uint32_t)p.num_blocks || nvalid > kPage) {
         if (tid == 0) set_error(p.err, LAZY_DEVERR_BAD_PAGE);
         skip = true;
+      } else if (qside) {
+        // keys as stored; the query rows follow the document offset
+        const uint32_t off = word_offset(w);
+        const size_t page = ((size_t)blk * p.hkv + h) * (size_t)(kPage * D);
+        for (int idx = tid; idx < kPage * D; idx += kThreads) {
+          const int k = idx / D, i = idx % D;
+          Ks[k * (D + 1) + i] = Elem<T>::to_f(kpool[page + idx]);
+          Vs[idx] = Elem<T>::to_f(vpool[page + idx]);
+        }
+        if (tid < kPage) {
+          Kt[tid] = -1;
+          Kp[tid] = (int32_t)off + tid;
+        }
+        if (off != q_off) {  // the same word for every thread: a CTA-uniform branch
+          q_off = off;
+          if (tid < D / 2) {
+            float cs, sn;
+            rope_cos_sin((int64_t)m0 - (int64_t)off, p.turn[tid], cs, sn);
+            Cs[2 * tid] = cs;
+            Cs[2 * tid + 1] = sn;
+          }
+          __syncthreads();
+          for (int idx = tid; idx < kRows * (D / 2); idx += kThreads) {
+            const int r = idx / (D / 2), i = idx % (D / 2);
+            const float cs = Cs[2 * i], sn = Cs[2 * i + 1];
+            const float a = Qs[r * (D + 1) + i], c = Qs[r * (D + 1) + i + D / 2];
+            Qd[r * (D + 1) + i] = a * cs - c * sn;
+            Qd[r * (D + 1) + i + D / 2] = a * sn + c * cs;
+          }
+        }
       } else {
         const int64_t delta = (int64_t)word_offset(w) - m0;  // the one relative rotation
         const size_t page = ((size_t)blk * p.hkv + h) * (size_t)(kPage * D);
@@ -151,8 +194,9 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(const PrefillPar
     float s[8];
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) s[kk] = 0.f;
+    const float *Qrow = (qside && doc) ? Qd + row * (D + 1) : Qs + row * (D + 1);
     for (int d = 0; d < D; ++d) {
-      const float qv = Qs[row * (D + 1) + d];
+      const float qv = Qrow[d];
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) s[kk] = fmaf(qv, Ks[(half * 8 + kk) * (D + 1) + d], s[kk]);
     }
@@ -201,19 +245,25 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(const PrefillPar
   }
 }
 
-template <typename T, int D>
-int launch_simt(const PrefillParams &pp, int32_t max_q_len, cudaStream_t s) {
-  constexpr int smem = SimtSmem<D>::kBytes;
+template <typename T, int D, bool QS>
+int launch_simt_variant(const PrefillParams &pp, int32_t max_q_len, cudaStream_t s) {
+  constexpr int smem = SimtSmem<D, QS>::kBytes;
   static bool attr = false;
   if (!attr) {
-    LAZY_CUDA_TRY(cudaFuncSetAttribute(prefill_simt_kernel<T, D>,
+    LAZY_CUDA_TRY(cudaFuncSetAttribute(prefill_simt_kernel<T, D, QS>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
     attr = true;
   }
   dim3 grid((max_q_len + pp.TQ - 1) / pp.TQ, pp.hkv, pp.batch);
-  prefill_simt_kernel<T, D><<<grid, kThreads, smem, s>>>(pp);
+  prefill_simt_kernel<T, D, QS><<<grid, kThreads, smem, s>>>(pp);
   LAZY_CUDA_TRY(cudaGetLastError());
   return LAZY_OK;
+}
+
+template <typename T, int D>
+int launch_simt(const PrefillParams &pp, int32_t max_q_len, cudaStream_t s) {
+  return pp.qside ? launch_simt_variant<T, D, true>(pp, max_q_len, s)
+                  : launch_simt_variant<T, D, false>(pp, max_q_len, s);
 }
 
 }  // namespace

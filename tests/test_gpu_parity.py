@@ -464,6 +464,22 @@ def test_prefill_simt_parity(pk, D, Hq, Hkv, dtype):
     _check_prefill(wl, pb, out, lse)
 
 
+@pytest.mark.parametrize("D,Hq,Hkv,dtype", [
+    (128, 32, 8, "bf16"), (64, 8, 8, "bf16"), (128, 16, 2, "bf16"), (64, 4, 1, "fp32"),
+    (128, 8, 2, "fp32")])
+def test_prefill_simt_query_side_rotation_parity(pk, D, Hq, Hkv, dtype):
+    # the query-side variant: key pages as stored, the query rows rotated once per document
+    # offset; against the oracle, and against the key-side kernel (fp32: to rounding)
+    wl = _edge_prefill_workload(D, Hq, Hkv, dtype)
+    _, pb, out, lse = _prefill(pk, wl, pk.LAZY_PREFILL_SIMT_QSIDE)
+    _check_prefill(wl, pb, out, lse)
+    _, _, o_k, l_k = _prefill(pk, wl, pk.LAZY_PREFILL_SIMT)
+    if dtype == "fp32":
+        assert np.abs(out - o_k).max() <= 2e-6 and np.abs(lse - l_k).max() <= 2e-6
+    else:
+        assert np.abs(out - o_k).max() <= 1e-2 and np.abs(lse - l_k).max() <= 1e-5
+
+
 def test_prefill_full_size_sampled(pk):
     # 8 requests x (16 docs x 1024 + 256 causal question tokens), 32/8/128 bf16
     H = _h()
@@ -485,7 +501,7 @@ def test_prefill_tensor_core_parity(pk, Hq, Hkv):
     _check_prefill(wl, pb, out, lse, lse_tol=TC_EDGE_LSE_TOL)
 
 
-@pytest.mark.parametrize("flags", ["tc", "simt"])
+@pytest.mark.parametrize("flags", ["tc", "simt", "simt_qside"])
 def test_prefill_offsets_near_the_page_word_limit(pk, flags):
     # documents and question moved up to just below 2^26 (the offset field's limit)
     H = _h()
@@ -495,7 +511,8 @@ def test_prefill_offsets_near_the_page_word_limit(pk, flags):
     for r in wl.requests:
         r.offsets = [o + c for o in r.offsets]
         r.q_pos0 += c
-    fl = pk.LAZY_PREFILL_TC if flags == "tc" else pk.LAZY_PREFILL_SIMT
+    fl = {"tc": pk.LAZY_PREFILL_TC, "simt": pk.LAZY_PREFILL_SIMT,
+          "simt_qside": pk.LAZY_PREFILL_SIMT_QSIDE}[flags]
     _, pb, out, lse = _prefill(pk, wl, fl)
     _check_prefill(wl, pb, out, lse, lse_tol=TC_EDGE_LSE_TOL if flags == "tc" else None)
 
