@@ -10,10 +10,11 @@
 // are rotated by R(p - m0) and attended causally.
 //
 // Query-side variant (QS, LAZY_PREFILL_SIMT_QSIDE; the summaries' prefill part allows rotating
-// either side): cached key pages are used as stored, R(j) k, and when the document offset o of
-// the pages changes the query rows R(m - m0) q get R(m0 - o) once, into a second buffer, so a
-// document of L_d keys costs one rotation of the 64 query rows instead of L_d key rotations.
-// (R(m0 - o) R(m - m0) q) . (R(j) k) = (R(m - o) q) . (R(j) k) = (R(m) q) . (R(o + j) k).
+// either side): cached key pages are used as stored, R(j) k, and the query buffer holds
+// R(m - o) q for the current document offset o, reloaded from the raw queries when o changes
+// (and R(m - m0) q again for the question's own keys). A document of L_d keys then costs one
+// rotation of the 64 query rows instead of L_d key rotations:
+// (R(m - o) q) . (R(j) k) = (R(m) q) . (R(o + j) k).
 #include <algorithm>
 
 #include "lazy_common.cuh"
@@ -34,10 +35,7 @@ struct SimtSmem {
   static constexpr int kP = kV + kPage * D * 4;         // float [kRows][kPage+1]
   static constexpr int kKt = kP + kRows * (kPage + 1) * 4;  // int32 [kPage] key token (-1 = doc)
   static constexpr int kKp = kKt + kPage * 4;               // int32 [kPage] key logical position
-  // QS: the query rows rotated to the current document, and that document's (cos, sin)
-  static constexpr int kQd = kKp + kPage * 4;               // float [kRows][D+1]
-  static constexpr int kCs = kQd + (QS ? kRows * (D + 1) * 4 : 0);  // float [D/2][2]
-  static constexpr int kBytes = kCs + (QS ? D * 4 : 0);
+  static constexpr int kBytes = kKp + kPage * 4;
 };
 
 template <typename T, int D, bool QS>
@@ -50,12 +48,9 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(const PrefillPar
   float *Ps = reinterpret_cast<float *>(smem_raw + S::kP);
   int32_t *Kt = reinterpret_cast<int32_t *>(smem_raw + S::kKt);
   int32_t *Kp = reinterpret_cast<int32_t *>(smem_raw + S::kKp);
-  float *Qd = reinterpret_cast<float *>(smem_raw + S::kQd);
-  float *Cs = reinterpret_cast<float *>(smem_raw + S::kCs);
   // ALiBi pools: no rotation anywhere; scores get slope * (n - m) instead
   const bool alibi = p.slopes != nullptr;
   const bool qside = QS && !alibi;
-  uint32_t q_off = 0xFFFFFFFFu;  // document offset the rows in Qd are rotated to
 
   const int b = blockIdx.z, h = blockIdx.y;
   const int G = p.G, TQ = p.TQ;
@@ -69,22 +64,27 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(const PrefillPar
   const int tid = threadIdx.x;
   const T *q = reinterpret_cast<const T *>(p.q);
 
-  // ---- queries, rotated to positions relative to m0 and pre-scaled (log2 domain)
-  for (int idx = tid; idx < kRows * (D / 2); idx += kThreads) {
-    const int row = idx / (D / 2), i = idx % (D / 2);
-    float x = 0.f, y = 0.f;
-    if (row < nrows) {
-      const int t = t0 + row / G, qh = h * G + row % G;
-      const T *src = q + ((size_t)(qbeg + t) * p.hq + qh) * D;
-      float cs = 1.f, sn = 0.f;
-      if (!alibi) rope_cos_sin((int64_t)(t - t0), p.turn[i], cs, sn);
-      const float a = Elem<T>::to_f(src[i]), c = Elem<T>::to_f(src[i + D / 2]);
-      x = (a * cs - c * sn) * p.scale_log2;
-      y = (a * sn + c * cs) * p.scale_log2;
+  // ---- queries R(m - target) q, pre-scaled (log2 domain); target m0 = relative to the tile
+  // start. The QS variant reloads them whenever the target (a document offset) changes.
+  auto load_q = [&](int64_t target) {
+    for (int idx = tid; idx < kRows * (D / 2); idx += kThreads) {
+      const int row = idx / (D / 2), i = idx % (D / 2);
+      float x = 0.f, y = 0.f;
+      if (row < nrows) {
+        const int t = t0 + row / G, qh = h * G + row % G;
+        const T *src = q + ((size_t)(qbeg + t) * p.hq + qh) * D;
+        float cs = 1.f, sn = 0.f;
+        if (!alibi) rope_cos_sin((int64_t)(m0 + (t - t0)) - target, p.turn[i], cs, sn);
+        const float a = Elem<T>::to_f(src[i]), c = Elem<T>::to_f(src[i + D / 2]);
+        x = (a * cs - c * sn) * p.scale_log2;
+        y = (a * sn + c * cs) * p.scale_log2;
+      }
+      Qs[row * (D + 1) + i] = x;
+      Qs[row * (D + 1) + i + D / 2] = y;
     }
-    Qs[row * (D + 1) + i] = x;
-    Qs[row * (D + 1) + i + D / 2] = y;
-  }
+  };
+  load_q(m0);
+  int64_t q_target = m0;  // what the query buffer is rotated relative to
 
   const int row = tid >> 1, half = tid & 1;
   const int t_row = t0 + row / G;
@@ -115,7 +115,8 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(const PrefillPar
         if (tid == 0) set_error(p.err, LAZY_DEVERR_BAD_PAGE);
         skip = true;
       } else if (qside) {
-        // keys as stored; the query rows follow the document offset
+        // keys as stored; the query rows follow the document offset (the same word for every
+        // thread, so the reload is CTA-uniform)
         const uint32_t off = word_offset(w);
         const size_t page = ((size_t)blk * p.hkv + h) * (size_t)(kPage * D);
         for (int idx = tid; idx < kPage * D; idx += kThreads) {
@@ -127,22 +128,9 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(const PrefillPar
           Kt[tid] = -1;
           Kp[tid] = (int32_t)off + tid;
         }
-        if (off != q_off) {  // the same word for every thread: a CTA-uniform branch
-          q_off = off;
-          if (tid < D / 2) {
-            float cs, sn;
-            rope_cos_sin((int64_t)m0 - (int64_t)off, p.turn[tid], cs, sn);
-            Cs[2 * tid] = cs;
-            Cs[2 * tid + 1] = sn;
-          }
-          __syncthreads();
-          for (int idx = tid; idx < kRows * (D / 2); idx += kThreads) {
-            const int r = idx / (D / 2), i = idx % (D / 2);
-            const float cs = Cs[2 * i], sn = Cs[2 * i + 1];
-            const float a = Qs[r * (D + 1) + i], c = Qs[r * (D + 1) + i + D / 2];
-            Qd[r * (D + 1) + i] = a * cs - c * sn;
-            Qd[r * (D + 1) + i + D / 2] = a * sn + c * cs;
-          }
+        if ((int64_t)off != q_target) {
+          q_target = off;
+          load_q(off);
         }
       } else {
         const int64_t delta = (int64_t)word_offset(w) - m0;  // the one relative rotation
@@ -164,6 +152,10 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(const PrefillPar
         }
       }
     } else {
+      if (qside && q_target != m0) {  // the question's own keys: queries relative to m0 again
+        q_target = m0;
+        load_q(m0);
+      }
       const int c0 = (tile - npg) * kPage;
       for (int idx = tid; idx < kPage * (D / 2); idx += kThreads) {
         const int k = idx / (D / 2), i = idx % (D / 2);
@@ -194,9 +186,8 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(const PrefillPar
     float s[8];
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) s[kk] = 0.f;
-    const float *Qrow = (qside && doc) ? Qd + row * (D + 1) : Qs + row * (D + 1);
     for (int d = 0; d < D; ++d) {
-      const float qv = Qrow[d];
+      const float qv = Qs[row * (D + 1) + d];
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) s[kk] = fmaf(qv, Ks[(half * 8 + kk) * (D + 1) + d], s[kk]);
     }
