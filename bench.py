@@ -281,6 +281,40 @@ def shared_decode_bench(args, flush, stream):
     return out
 
 
+def rotation_side_bench(args, flush, stream):
+    """The CUDA-core prefill on prefill_b8 with the relative rotation on the key side (every
+    cached key page rotated by R(o - m0)) and on the query side (the query rows reloaded as
+    R(m - o) q once per document offset): same attention, 3/(4M) against 3/(4 L_d) rotation
+    work per key."""
+    import torch
+
+    import position_independent_kv_lazy_gb300 as pk
+    import workload as W
+    from position_independent_kv_lazy_gb300 import harness as H
+    wl = W.prefill_workload()
+    src = H.DeviceSource(wl)
+    res = H.build_resident(wl, src, resident_pool=False)
+    pb = H.prefill_batch(wl, res, src)
+    o = torch.empty_like(pb.q)
+    l = torch.empty((pb.total_q, wl.Hq), dtype=torch.float32, device="cuda")
+    out = {"workload": "prefill_b8 (16 docs x 1024 + 256 question tokens per request), "
+                       "CUDA-core kernel, fp32 arithmetic"}
+    for tag, fl in (("key_side", pk.LAZY_PREFILL_SIMT), ("query_side", pk.LAZY_PREFILL_SIMT_QSIDE)):
+        def call():
+            pk.lazy_attn_prefill(res.pool, pb.q, pb.k_new, pb.v_new, pb.cu_q, pb.q_pos0,
+                                 pb.words, pb.cu_pages, pb.max_q_len, sm_scale=wl.sm_scale,
+                                 out=o, lse=l, flags=fl)
+        flush(); call()
+        ms = _timed_steps(call, 3, flush, stream)
+        med = sorted(ms)[1]
+        out[tag] = {"value": round(pb.flops / (med * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                    "ms_per_call": round(med, 4)}
+    if pk.lazy_get_device_error(res.pool) != 0:
+        raise RuntimeError("device error in the rotation-side bench")
+    del res, src
+    return out
+
+
 def bench_prefill_only(args):
     """Prefill workload alone (pool sized to the documents used): for profiling runs."""
     import torch
@@ -612,6 +646,8 @@ def bench_ours(args):
         line["encode"] = encode_bench(args, flush, stream, hbm_peak)
         torch.cuda.empty_cache()
         line["shared_decode"] = shared_decode_bench(args, flush, stream)
+        torch.cuda.empty_cache()
+        line["prefill_rotation_side"] = rotation_side_bench(args, flush, stream)
     clk.__exit__()
     line["clocks"] = clk.summary(TIMED_WINDOWS)
     if rank == 0 and not args.no_cpu_baseline:
