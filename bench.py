@@ -932,8 +932,30 @@ def alibi_bench(args, flush, stream, hbm_peak, tc_peak):
     out["decode"] = {"workload": "decode_b64 with ALiBi (32 standard slopes)",
                      "value": round(kv / (med * 1e-3) / 1e9, 2), "unit": "GB/s",
                      "ms_dist": _dist_ms(ms), "frac": round(kv / (med * 1e-3) / 1e9 / hbm_peak, 4)}
+    # the same batch through the shared-segment plan (ALiBi words: page positions)
+    import numpy as np
+    plan_h = pk.lazy_decode_shared_plan(db.words.cpu().numpy().view(np.uint64),
+                                        db.cu_pages.cpu().numpy(), page_positions=True)
+    plan = plan_h.to("cuda")
+    sws = torch.empty(pk.lazy_decode_shared_workspace_bytes(res.pool, plan.n_units, wl.Hq),
+                      dtype=torch.uint8, device="cuda")
+
+    def shared_call():
+        pk.lazy_attn_decode_shared(res.pool, db.q, db.q_pos, plan, sm_scale=wl.sm_scale,
+                                   out=dout, lse=dlse, workspace=sws)
+
+    for _ in range(args.warmup):
+        flush(); shared_call()
+    ms = _timed_steps(shared_call, steps, flush, stream)
+    med = _dist_ms(ms)["median"]
+    out["decode_shared"] = {"workload": "decode_b64 with ALiBi through lazy_attn_decode_shared",
+                            "value": round(kv / (med * 1e-3) / 1e9, 2), "unit": "GB/s",
+                            "ms_per_call": round(med, 5), "units": plan.n_units,
+                            "entries": plan_h.n_entries}
+    if pk.lazy_get_device_error(res.pool) != 0:
+        raise RuntimeError("device error in the ALiBi decode bench")
     res.pool.close()
-    del res, db, dws
+    del res, db, dws, plan, sws
     torch.cuda.empty_cache()
 
     pwl = W.prefill_workload(name="prefill_b8_alibi")
