@@ -547,7 +547,7 @@ __device__ __forceinline__ void mma_begin_unit(MmaWarpState<GC> &st, const Decod
 template <int GC>
 __device__ __forceinline__ void mma_attend_page(MmaWarpState<GC> &st, const DecodeParams &p,
                                                 uint64_t word, uint32_t page_smem, int lane) {
-  const int g = lane >> 2, t = lane & 3;  // fragment row group and column pair
+  const int t = lane & 3;  // fragment column pair (the row group is in st.live)
   const bool live = st.live;
   const bool alibi = p.slopes != nullptr;
   const uint32_t nv = word_nvalid(word);
