@@ -433,12 +433,13 @@ def lazy_decode_shared_plan(page_words, cu_pages, page_positions: bool = False) 
     cu = np.ascontiguousarray(np.asarray(cu_pages, dtype=np.int32))
     B = len(cu) - 1
     P = int(cu[-1] - cu[0]) if B > 0 else 0
-    entries = np.zeros(max(2 * P, 2), dtype=np.uint64)
-    cu_e = np.zeros(P + 1, dtype=np.int32)
-    unit_req = np.zeros(max(2 * P, 2), dtype=np.int32)
-    cu_m = np.zeros(B + 1, dtype=np.int32)
-    members = np.zeros(max(P, 1), dtype=np.int32)
-    member_entries = np.zeros(max(2 * P, 2), dtype=np.int32)
+    # capacities for P pages; the planner fills the leading parts (returned as views)
+    entries = np.empty(max(2 * P, 2), dtype=np.uint64)
+    cu_e = np.empty(P + 1, dtype=np.int32)
+    unit_req = np.empty(max(2 * P, 2), dtype=np.int32)
+    cu_m = np.empty(B + 1, dtype=np.int32)
+    members = np.empty(max(P, 1), dtype=np.int32)
+    member_entries = np.empty(max(2 * P, 2), dtype=np.int32)
     nu, ne = ctypes.c_int32(), ctypes.c_int32()
     _check("lazy_decode_shared_plan", load_library().lazy_decode_shared_plan(
         w.ctypes.data, cu.ctypes.data, B, int(bool(page_positions)), entries.ctypes.data,
@@ -447,8 +448,8 @@ def lazy_decode_shared_plan(page_words, cu_pages, page_positions: bool = False) 
         ctypes.byref(nu), ctypes.byref(ne)))
     nu, ne = nu.value, ne.value
     nm = int(cu_m[-1])
-    return SharedPlan(entries[:2 * ne].copy(), cu_e[:nu + 1].copy(), unit_req[:2 * nu].copy(),
-                      cu_m, members[:nm].copy(), member_entries[:2 * nm].copy())
+    return SharedPlan(entries[:2 * ne], cu_e[:nu + 1], unit_req[:2 * nu], cu_m, members[:nm],
+                      member_entries[:2 * nm])
 
 
 def lazy_decode_shared_workspace_bytes(pool: LazyPool, n_units: int, num_q_heads: int,

@@ -20,7 +20,7 @@
 //   - a request's segments that no other segment matches (its private tail, documents only it
 //     holds) become one single unit per request, after all groups: fewer unit switches, whose
 //     query loads stall a warp, and fewer partial slots.
-#include <map>
+#include <unordered_map>
 #include <vector>
 
 #include "pool_internal.h"
@@ -43,6 +43,26 @@ struct Segment {
   int32_t req, start, len;
 };
 
+// Bucket key of a segment: its length and first (block, valid count) word, through the
+// splitmix64 finaliser. A document's first block names it in practice; members of a bucket are
+// confirmed word by word, so a collision only costs a comparison.
+uint64_t fmix(uint64_t x) {
+  x ^= x >> 30;
+  x *= 0xbf58476d1ce4e5b9ull;
+  x ^= x >> 27;
+  x *= 0x94d049bb133111ebull;
+  return x ^ (x >> 31);
+}
+uint64_t segment_hash(const uint64_t *words, const Segment &sg) {
+  return fmix((words[sg.start] & ~kOffsetMask) ^ ((uint64_t)sg.len * 0x9e3779b97f4a7c15ull));
+}
+bool same_content(const uint64_t *words, const Segment &a, const Segment &b) {
+  if (a.len != b.len) return false;
+  for (int32_t k = 0; k < a.len; ++k)
+    if ((words[a.start + k] & ~kOffsetMask) != (words[b.start + k] & ~kOffsetMask)) return false;
+  return true;
+}
+
 }  // namespace
 
 extern "C" int lazy_decode_shared_plan(const uint64_t *words, const int32_t *cu_pages,
@@ -59,8 +79,8 @@ extern "C" int lazy_decode_shared_plan(const uint64_t *words, const int32_t *cu_
   if (total > 0 && (!words || !entries || !unit_req || !members || !member_entries))
     return LAZY_ERR_INVALID_ARG;
 
-  // segments, grouped by content
-  std::map<std::vector<uint64_t>, int32_t> index;
+  // segments, grouped by content (groups in order of first appearance)
+  std::unordered_map<uint64_t, std::vector<int32_t>> index;  // hash -> groups with that hash
   std::vector<std::vector<Segment>> groups;
   for (int32_t b = 0; b < batch; ++b) {
     int32_t k = cu_pages[b];
@@ -68,18 +88,20 @@ extern "C" int lazy_decode_shared_plan(const uint64_t *words, const int32_t *cu_
     while (k < end) {
       int32_t e = k + 1;
       while (e < end && continues(words[e - 1], words[e], page_positions != 0)) ++e;
-      std::vector<uint64_t> key(e - k);
-      for (int32_t i = k; i < e; ++i) key[i - k] = words[i] & ~kOffsetMask;
-      auto it = index.find(key);
-      int32_t gi;
-      if (it == index.end()) {
+      const Segment sg{b, k, e - k};
+      std::vector<int32_t> &bucket = index[segment_hash(words, sg)];
+      int32_t gi = -1;
+      for (int32_t g : bucket)
+        if (same_content(words, groups[g][0], sg)) {
+          gi = g;
+          break;
+        }
+      if (gi < 0) {
         gi = (int32_t)groups.size();
-        index.emplace(std::move(key), gi);
+        bucket.push_back(gi);
         groups.emplace_back();
-      } else {
-        gi = it->second;
       }
-      groups[gi].push_back({b, k, e - k});
+      groups[gi].push_back(sg);
       k = e;
     }
   }

@@ -77,6 +77,21 @@ def test_group_of_r_members_gives_r_over_2_pairs():
         assert plan.n_entries == r + 4 * ((r + 1) // 2)
 
 
+def test_same_first_page_different_segments_are_not_paired():
+    # segments that share their first block and length but differ later land in one bucket of
+    # the planner's index and must still be told apart word by word
+    reqs = [[([100, 101, 102], 0, 48)], [([100, 101, 103], 0, 48)], [([100, 101, 102], 7, 48)],
+            [([100, 101, 103], 9, 48)], [([100, 101, 102], 50, 40)]]
+    w, cu = pk.build_page_table(reqs, 16)
+    plan = pk.lazy_decode_shared_plan(w, cu)
+    _check_plan(w, cu, plan)
+    pairs = sorted(tuple(plan.unit_req[2 * u:2 * u + 2]) for u in range(plan.n_units)
+                   if plan.unit_req[2 * u + 1] >= 0)
+    # (0, 2) share [100, 101, 102] with 16 valid keys on every page, (1, 3) [100, 101, 103];
+    # request 4's last page holds 8 keys, so its words differ: alone
+    assert pairs == [(0, 2), (1, 3)]
+
+
 def test_repeated_document_in_one_request_pairs_with_itself():
     D = (list(range(10, 12)), 0, 32)
     reqs = [[(D[0], 0, 32), ([3], 32, 5), (D[0], 37, 32)]]
