@@ -16,6 +16,10 @@ Positional Encoding", technical summaries):
 
 Forms:
   A  ``attend_materialised``  C, fp64, threaded (oracle.c)
+  S  ``attend_stored``        C, fp64, threaded: form A with the cache's storage step written out
+                              (a cached key is round(R(j) k) in the cache's element type, attended
+                              at its offset); it differs from A only by that rounding, which
+                              shrinks like 1/sqrt(keys) in the log-sum-exp
   B  ``attend_lazy``          C, fp64, single-threaded, small cases
   C  ``attend_bruteforce``    pure Python loops, explicit cos/sin, exp-sum without max shift
   ``textbook_rope_attention`` standard RoPE causal attention over one sequence (positions 0..N-1)
@@ -79,6 +83,12 @@ def _load():
             lib.oracle_attend_lazy.restype = ctypes.c_int
             lib.oracle_rope.argtypes = [ctypes.c_int, ctypes.c_double, ctypes.c_double, dp, dp]
             lib.oracle_rope.restype = None
+            lib.oracle_attend_stored.argtypes = [
+                ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_double, ctypes.c_int,
+                dp, dp, ip, ip, up, up, ctypes.c_int, dp, ip, ctypes.c_int, dp, dp, ctypes.c_int]
+            lib.oracle_attend_stored.restype = ctypes.c_int
+            lib.oracle_round_bf16.argtypes = [ctypes.c_double]
+            lib.oracle_round_bf16.restype = ctypes.c_double
             _lib = lib
     return _lib
 
@@ -122,6 +132,42 @@ def attend_materialised(k_raw, v, key_pos, key_causal, q, q_pos, *, base, scale,
         threads or default_threads())
     if rc != 0:
         raise ValueError("oracle_attend_materialised rejected its arguments")
+    return out, lse
+
+
+STORE = {"exact": 0, "bf16": 1, "fp32": 2}
+
+
+def round_bf16(x: float) -> float:
+    """x rounded to the nearest bfloat16 (ties to even), as the stored-key form rounds."""
+    return float(_load().oracle_round_bf16(float(x)))
+
+
+def attend_stored(k_raw, v, key_off, key_local, key_stored, key_causal, q, q_pos, *, base, scale,
+                  store="bf16", threads=None):
+    """Form S for one kv head: a key with key_stored = 1 is the cache's copy
+    round(R(local) k) in the cache's element type (``store``: "bf16", "fp32" or "exact"),
+    attended at its offset; other keys enter as R(off + local) k. Returns (out, lse)."""
+    k_raw = np.ascontiguousarray(k_raw, dtype=np.float64)
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    n, D = k_raw.shape
+    n_q, G, _ = q.shape
+    key_off = np.ascontiguousarray(key_off, dtype=np.int64)
+    key_local = np.ascontiguousarray(key_local, dtype=np.int64)
+    key_stored = np.ascontiguousarray(key_stored, dtype=np.uint8)
+    key_causal = np.ascontiguousarray(key_causal, dtype=np.uint8)
+    q_pos = np.ascontiguousarray(q_pos, dtype=np.int64)
+    out = np.zeros((n_q, G, D), dtype=np.float64)
+    lse = np.zeros((n_q, G), dtype=np.float64)
+    rc = _load().oracle_attend_stored(
+        D, G, float(base), float(scale), n, _p(k_raw, ctypes.c_double), _p(v, ctypes.c_double),
+        _p(key_off, ctypes.c_int64), _p(key_local, ctypes.c_int64),
+        _p(key_stored, ctypes.c_uint8), _p(key_causal, ctypes.c_uint8), n_q,
+        _p(q, ctypes.c_double), _p(q_pos, ctypes.c_int64), STORE[store],
+        _p(out, ctypes.c_double), _p(lse, ctypes.c_double), threads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle_attend_stored rejected its arguments")
     return out, lse
 
 
@@ -345,6 +391,9 @@ def attend_request(wl, b, kv_heads: Optional[Sequence[int]] = None,
     Only the kv heads in ``kv_heads`` (their G query heads) and the query rows in ``queries`` are
     computed; other entries are NaN. ``src`` supplies the input arrays (defaults to the workload's
     host arrays); it must expose doc_k, doc_v, q, new_k, new_v like ``workload.Workload``.
+    ``form``: "A" (materialised), "B" (lazy) or "S" (stored keys: every key the cache holds, i.e.
+    the documents and a decode request's private segment, is round(R(j) k) in the workload's
+    dtype; a prefill question's own keys are not cached and enter exactly).
     """
     src = src or wl
     r = wl.requests[b]
@@ -366,6 +415,11 @@ def attend_request(wl, b, kv_heads: Optional[Sequence[int]] = None,
         elif form == "B":
             o, l = attend_lazy(k_raw[:, h, :], v[:, h, :], off, loc, caus, qh, q_pos[qi],
                                base=wl.rope_base, scale=wl.sm_scale)
+        elif form == "S":
+            stored = np.ones(len(off), np.uint8) if r.mode == "decode" else (caus == 0)
+            o, l = attend_stored(k_raw[:, h, :], v[:, h, :], off, loc, stored, caus, qh,
+                                 q_pos[qi], base=wl.rope_base, scale=wl.sm_scale,
+                                 store=wl.dtype, threads=threads)
         else:
             raise ValueError(form)
         out[qi, h * G:(h + 1) * G, :] = o

@@ -18,6 +18,11 @@
  * Form B is the lazy form the summaries describe ("Concepto central" / decoding section):
  *   s_k = scale * (R(m - o_k) q) . (R(j_k) k_k)   with p_k = o_k + j_k,
  * i.e. a key stored once at its document-local position j_k and attended at offset o_k.
+ * Form S (the stored-key form) is form A with the cache's storage step written out: a key that
+ * the cache holds is kept as round(R(j_k) k_k), rounded to the cache's element type (bf16 or
+ * fp32; the summaries' "Core concept": the cache holds each document's keys once, rotated only
+ * at document-local positions), and attended as R(o_k) round(R(j_k) k_k); a key that is not
+ * cached (a question token's own key) enters as R(p_k) k_k. With exact storage S equals A.
  *
  * Visibility: a key flagged causal (a question token's own key) is visible to a query at m only
  * if its position p_k <= m; every other key (a cached document or private-segment key) is
@@ -43,6 +48,29 @@ static void rope_rotate(double *x, int D, double pos, double base) {
         x[i + h] = x0 * s + x1 * c;
     }
 }
+
+/* x rounded to the nearest bfloat16 (8 significant bits; ties to even under the default
+ * rounding mode). Below the smallest normal, 2^-126, the spacing stays 2^-133 (subnormals);
+ * results beyond the largest finite value, (2 - 2^-7) 2^127, become +-inf. */
+static double round_bf16(double x) {
+    if (x == 0.0 || !isfinite(x)) return x;
+    int e;
+    frexp(x, &e); /* |x| in [2^(e-1), 2^e) */
+    if (e < -125) e = -125;
+    double q = ldexp(1.0, e - 8); /* spacing of 8-bit significands in that binade */
+    double r = nearbyint(x / q) * q;
+    if (fabs(r) >= ldexp(1.0, 128)) r = copysign(INFINITY, x);
+    return r;
+}
+
+/* Storage rounding of a cached element: 0 = none (exact), 1 = bfloat16, 2 = float32. */
+static double round_store(double x, int store) {
+    if (store == 1) return round_bf16(x);
+    if (store == 2) return (double)(float)x;
+    return x;
+}
+
+double oracle_round_bf16(double x) { return round_bf16(x); }
 
 /* Exposed so tests can pin the rotation itself (norm, composition, D=2 closed form). */
 void oracle_rope(int D, double base, double pos, const double *x_in, double *x_out) {
@@ -85,6 +113,10 @@ typedef struct {
     const uint8_t *key_causal;
     double *kt, *out, *lse;
     int phase;
+    /* form S only (key_off == NULL for form A) */
+    const int64_t *key_off, *key_local;
+    const uint8_t *key_stored;
+    int store;
 } job_t;
 
 static void *worker(void *arg) {
@@ -94,7 +126,14 @@ static void *worker(void *arg) {
         for (int k = j->tid; k < j->n_keys; k += j->nt) {
             double *dst = j->kt + (size_t)k * j->D;
             memcpy(dst, j->k_raw + (size_t)k * j->D, sizeof(double) * (size_t)j->D);
-            rope_rotate(dst, j->D, (double)j->key_pos[k], j->base);
+            if (j->key_off && j->key_stored[k]) {
+                /* form S: the cache's copy R(j) k in its element type, then the offset */
+                rope_rotate(dst, j->D, (double)j->key_local[k], j->base);
+                for (int d = 0; d < j->D; ++d) dst[d] = round_store(dst[d], j->store);
+                rope_rotate(dst, j->D, (double)j->key_off[k], j->base);
+            } else {
+                rope_rotate(dst, j->D, (double)j->key_pos[k], j->base);
+            }
         }
         return NULL;
     }
@@ -114,6 +153,33 @@ static void *worker(void *arg) {
     return NULL;
 }
 
+/* Materialises every key (phase 0), then attends every (query, head) (phase 1), threaded. */
+static int run_jobs(int D, int G, double base, double scale, int n_keys, const double *k_raw,
+                    const double *v, const int64_t *key_pos, const uint8_t *key_causal, int n_q,
+                    const double *q, const int64_t *q_pos, double *out, double *lse,
+                    int n_threads, const int64_t *key_off, const int64_t *key_local,
+                    const uint8_t *key_stored, int store) {
+    if (D < 2 || (D & 1) || G < 1 || n_keys < 0 || n_q < 0) return -1;
+    if (n_threads < 1) n_threads = 1;
+    double *kt = (double *)malloc(sizeof(double) * (size_t)(n_keys > 0 ? n_keys : 1) * (size_t)D);
+    if (!kt) return -1;
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)n_threads);
+    job_t *jobs = (job_t *)malloc(sizeof(job_t) * (size_t)n_threads);
+    for (int phase = 0; phase < 2; ++phase) {
+        for (int t = 0; t < n_threads; ++t) {
+            job_t jb = {D, G, n_keys, n_q, t, n_threads, base, scale, k_raw, v, q, key_pos, q_pos,
+                        key_causal, kt, out, lse, phase, key_off, key_local, key_stored, store};
+            jobs[t] = jb;
+            pthread_create(&th[t], NULL, worker, &jobs[t]);
+        }
+        for (int t = 0; t < n_threads; ++t) pthread_join(th[t], NULL);
+    }
+    free(jobs);
+    free(th);
+    free(kt);
+    return 0;
+}
+
 /*
  * Form A for one kv head and its G query heads.
  *   k_raw, v : [n_keys][D]   raw (unrotated) keys and values
@@ -127,25 +193,30 @@ int oracle_attend_materialised(int D, int G, double base, double scale, int n_ke
                                const double *k_raw, const double *v, const int64_t *key_pos,
                                const uint8_t *key_causal, int n_q, const double *q,
                                const int64_t *q_pos, double *out, double *lse, int n_threads) {
-    if (D < 2 || (D & 1) || G < 1 || n_keys < 0 || n_q < 0) return -1;
-    if (n_threads < 1) n_threads = 1;
-    double *kt = (double *)malloc(sizeof(double) * (size_t)(n_keys > 0 ? n_keys : 1) * (size_t)D);
-    if (!kt) return -1;
-    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)n_threads);
-    job_t *jobs = (job_t *)malloc(sizeof(job_t) * (size_t)n_threads);
-    for (int phase = 0; phase < 2; ++phase) {
-        for (int t = 0; t < n_threads; ++t) {
-            job_t jb = {D, G, n_keys, n_q, t, n_threads, base, scale, k_raw, v, q, key_pos, q_pos,
-                        key_causal, kt, out, lse, phase};
-            jobs[t] = jb;
-            pthread_create(&th[t], NULL, worker, &jobs[t]);
-        }
-        for (int t = 0; t < n_threads; ++t) pthread_join(th[t], NULL);
-    }
-    free(jobs);
-    free(th);
-    free(kt);
-    return 0;
+    return run_jobs(D, G, base, scale, n_keys, k_raw, v, key_pos, key_causal, n_q, q, q_pos, out,
+                    lse, n_threads, NULL, NULL, NULL, 0);
+}
+
+/*
+ * Form S for one kv head: as form A, except that a key with key_stored[k] = 1 is the cache's
+ * copy round(R(key_local[k]) k_raw[k]) (store: 0 = exact, 1 = bfloat16, 2 = float32), attended
+ * at offset key_off[k], i.e. rotated by R(key_off[k]) in fp64 before the dot product. Keys with
+ * key_stored[k] = 0 enter as R(key_off[k] + key_local[k]) k_raw[k]. Causal visibility uses the
+ * absolute position key_off + key_local.
+ */
+int oracle_attend_stored(int D, int G, double base, double scale, int n_keys, const double *k_raw,
+                         const double *v, const int64_t *key_off, const int64_t *key_local,
+                         const uint8_t *key_stored, const uint8_t *key_causal, int n_q,
+                         const double *q, const int64_t *q_pos, int store, double *out,
+                         double *lse, int n_threads) {
+    if (store < 0 || store > 2 || n_keys < 0) return -1;
+    int64_t *pos = (int64_t *)malloc(sizeof(int64_t) * (size_t)(n_keys > 0 ? n_keys : 1));
+    if (!pos) return -1;
+    for (int k = 0; k < n_keys; ++k) pos[k] = key_off[k] + key_local[k];
+    int rc = run_jobs(D, G, base, scale, n_keys, k_raw, v, pos, key_causal, n_q, q, q_pos, out, lse,
+                      n_threads, key_off, key_local, key_stored, store);
+    free(pos);
+    return rc;
 }
 
 /*

@@ -226,6 +226,123 @@ def test_sampling_matches_full_computation():
     assert np.isnan(part[0][0]).all() and np.isnan(part[0][2][:2]).all()
 
 
+# ---------------------------------------------------------------- stored-key form (S)
+# The cache keeps each document's keys once, rotated at their document-local positions, in its
+# own element type ("Core concept: deferred positional encoding"). Form S writes that storage
+# rounding out; with exact storage it is form A.
+@pytest.mark.parametrize("x,want", [
+    (1.0 + 2 ** -8, 1.0),                         # halfway to 1 + 2^-7: ties to even (down)
+    (1.0 + 3 * 2 ** -8, 1.0 + 2 ** -6),           # halfway between 1 + 2^-7 and 1 + 2^-6 (up)
+    (1.0 + 2 ** -8 + 2 ** -30, 1.0 + 2 ** -7),    # just above halfway
+    (-(1.0 + 3 * 2 ** -8), -(1.0 + 2 ** -6)),     # sign symmetry
+    (0.1, 205 * 2.0 ** -11),                      # 0.1 in [2^-4, 2^-3): spacing 2^-11, 204.8 -> 205
+    (3 * 2.0 ** -135, 2.0 ** -133),               # below 2^-126 the spacing stays 2^-133
+    ((2 - 2 ** -7) * 2.0 ** 127, (2 - 2 ** -7) * 2.0 ** 127),   # largest finite bf16
+    ((2 - 2 ** -8) * 2.0 ** 127, math.inf),       # halfway to 2^128 rounds to even -> overflow
+    (0.0, 0.0)])
+def test_round_bf16_hand_values(x, want):
+    assert oracle.round_bf16(x) == want
+
+
+def test_round_bf16_matches_bit_level_rounding():
+    # an independent implementation (integer rounding of the float32 bit pattern)
+    rng = np.random.default_rng(7)
+    x = np.concatenate([rng.standard_normal(20000).astype(np.float32),
+                        (rng.standard_normal(2000) * 1e-30).astype(np.float32),
+                        (rng.standard_normal(2000) * 1e30).astype(np.float32)])
+    want = W.bf16_round(x).astype(np.float64)
+    got = np.array([oracle.round_bf16(float(t)) for t in x])
+    assert np.array_equal(got, want)
+
+
+def _stored_case(rng, D=16, n_docs=4, L=5, nq=3, G=2, bf16_inputs=True):
+    k = rng.standard_normal((n_docs * L, D))
+    v = rng.standard_normal((n_docs * L, D))
+    q = rng.standard_normal((nq, G, D))
+    if bf16_inputs:
+        k, v, q = (W.bf16_round(a.astype(np.float32)).astype(np.float64) for a in (k, v, q))
+    off = np.repeat(rng.integers(0, 5000, n_docs), L)
+    loc = np.tile(np.arange(L), n_docs)
+    q_pos = np.array([6000, 6100, 7777])[:nq]
+    return k, v, off, loc, q, q_pos
+
+
+def test_stored_form_with_exact_storage_is_form_a():
+    rng = np.random.default_rng(8)
+    k, v, off, loc, q, q_pos = _stored_case(rng)
+    n = len(off)
+    caus = np.zeros(n, np.uint8)
+    oa, la = oracle.attend_materialised(k, v, off + loc, caus, q, q_pos, base=1e4, scale=0.25)
+    for stored in (np.ones(n, np.uint8), np.zeros(n, np.uint8)):
+        os_, ls = oracle.attend_stored(k, v, off, loc, stored, caus, q, q_pos, base=1e4,
+                                       scale=0.25, store="exact")
+        assert np.abs(os_ - oa).max() < 1e-12 and np.abs(ls - la).max() < 1e-12
+
+
+def test_stored_form_rounds_before_the_offset_rotation():
+    # keys at local position 0 with bf16-exact raw values: R(0) k = k is already a bf16 value, so
+    # the cache's copy is exact and S equals A, whatever the offsets. Rounding R(o + j) k instead
+    # (storage after the offset) would not be exact and fails this.
+    rng = np.random.default_rng(9)
+    k, v, off, loc, q, q_pos = _stored_case(rng, L=1, n_docs=12)
+    n = len(off)
+    caus = np.zeros(n, np.uint8)
+    oa, la = oracle.attend_materialised(k, v, off, caus, q, q_pos, base=5e5, scale=0.25)
+    os_, ls = oracle.attend_stored(k, v, off, np.zeros(n), np.ones(n, np.uint8), caus, q, q_pos,
+                                   base=5e5, scale=0.25, store="bf16")
+    assert np.abs(os_ - oa).max() < 1e-12 and np.abs(ls - la).max() < 1e-12
+
+
+def test_stored_form_d2_worked_example():
+    # D=2 (theta_0 = 1): raw key (1, 0) stored at local position 1 is
+    # round_bf16((cos 1, sin 1)) = (0.5390625, 0.83984375) (hand-rounded: 138/256 and 215/256);
+    # attended at offset 2 by a query (1, 0) at m = 3, the score is
+    # scale * (R(3) q) . (R(2) stored) = scale * (cos 1 * 0.5390625 + sin 1 * 0.83984375);
+    # with a single key, lse = that score and out = v.
+    scale = 1 / math.sqrt(2)
+    want = scale * (math.cos(1.0) * 0.5390625 + math.sin(1.0) * 0.83984375)
+    out, lse = oracle.attend_stored(np.array([[1.0, 0.0]]), np.array([[0.25, -2.0]]), [2], [1],
+                                    [1], [0], np.array([[[1.0, 0.0]]]), [3], base=10.0,
+                                    scale=scale, store="bf16")
+    assert abs(lse[0, 0] - want) < 1e-14
+    assert np.allclose(out[0, 0], [0.25, -2.0], atol=1e-15)
+    # the exact form differs: cos(1)^2 + sin(1)^2 = 1
+    _, la = oracle.attend_materialised(np.array([[1.0, 0.0]]), np.array([[0.25, -2.0]]), [3], [0],
+                                       np.array([[[1.0, 0.0]]]), [3], base=10.0, scale=scale)
+    assert abs(la[0, 0] - scale) < 1e-14 and abs(lse[0, 0] - scale) > 1e-4
+
+
+def test_stored_form_differs_from_a_by_the_storage_rounding_only():
+    # fp32 storage moves lse by ~1e-7, bf16 storage by ~1e-3 on a 20-key context
+    rng = np.random.default_rng(10)
+    k, v, off, loc, q, q_pos = _stored_case(rng, D=64)
+    n = len(off)
+    caus = np.zeros(n, np.uint8)
+    st = np.ones(n, np.uint8)
+    _, la = oracle.attend_materialised(k, v, off + loc, caus, q, q_pos, base=1e4, scale=0.125)
+    _, l32 = oracle.attend_stored(k, v, off, loc, st, caus, q, q_pos, base=1e4, scale=0.125,
+                                  store="fp32")
+    _, l16 = oracle.attend_stored(k, v, off, loc, st, caus, q, q_pos, base=1e4, scale=0.125,
+                                  store="bf16")
+    assert np.abs(l32 - la).max() < 1e-5
+    assert 1e-5 < np.abs(l16 - la).max() < 2e-2
+
+
+def test_stored_form_leaves_question_keys_exact():
+    # a prefill request without documents: its question keys are not cached, so S equals A
+    wl = W.custom("prefill", [[]], doc_len=16, n_pool=1, Hq=4, Hkv=2, D=32, dtype="bf16",
+                  T=[9], q_pos0=[40], seed=4)
+    oa, la = oracle.attend_request(wl, 0, form="A")
+    os_, ls = oracle.attend_request(wl, 0, form="S")
+    assert np.abs(os_ - oa).max() < 1e-12 and np.abs(ls - la).max() < 1e-12
+    # with a document, only the document's keys are rounded: S moves away from A
+    wl = W.custom("prefill", [[(0, 0)]], doc_len=16, n_pool=1, Hq=4, Hkv=2, D=32, dtype="bf16",
+                  T=[9], q_pos0=[16], seed=4)
+    _, la = oracle.attend_request(wl, 0, form="A")
+    _, ls = oracle.attend_request(wl, 0, form="S")
+    assert 0 < np.abs(ls - la).max() < 2e-2
+
+
 # ---------------------------------------------------------------- page word spec
 def test_page_word_boundaries_exhaustive():
     for blk in (0, 1, 2**31 - 1, 2**31, 2**32 - 1):
