@@ -66,7 +66,11 @@ enum { LAZY_DEVERR_BAD_PAGE = 1, LAZY_DEVERR_TIMEOUT = 2 };
 enum {
     LAZY_PREFILL_AUTO = 0,  /* tensor-core kernel when bf16, head_dim 128 and the group size
                                (num_q_heads / num_kv_heads) is a power of two <= 32; else
-                               CUDA-core */
+                               CUDA-core. On RoPE pools the tensor-core kernel multiplies the
+                               rotated query rows and key tiles as fp16 (11 significant bits,
+                               rotated in fp32 and rounded once); query and key elements must
+                               then stay below 65504 in magnitude (use LAZY_PREFILL_SIMT for
+                               larger ones). P.V and the ALiBi mode's Q.K use bf16 operands. */
     LAZY_PREFILL_SIMT = 1,  /* CUDA-core kernel, fp32 arithmetic, group size <= 64 */
     LAZY_PREFILL_TC = 2,    /* tcgen05/TMEM kernel; LAZY_ERR_UNSUPPORTED if the shape is not */
     LAZY_PREFILL_SIMT_QSIDE = 3  /* the CUDA-core kernel with the query-side variant of the
@@ -235,14 +239,6 @@ int lazy_attn_decode(lazy_pool *pool, const void *d_q, const int32_t *d_q_pos,
                      float *d_lse, void *d_workspace, size_t workspace_bytes,
                      lazy_stream_t stream);
 
-/*
- * Test hook: y[i] = 2^x[i] computed by the FMA-pipe exponential (range reduction to
- * [-1/2, 1/2] plus a fitted degree-5 polynomial) that the tensor-core prefill can use for part
- * of its softmax weights when built with LAZY_POLY_EVERY > 0. The default build keeps every
- * exponential on the MUFU unit (offloading measured slower on GB300). d_x, d_y: device float
- * [n]. Inputs below -126 return ~1e-38.
- */
-int lazy_debug_exp2(const float *d_x, float *d_y, int32_t n, lazy_stream_t stream);
 
 /*
  * Allocation-free decode. The paper has no counterpart to this entry point; it exists for

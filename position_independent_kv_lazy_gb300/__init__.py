@@ -49,7 +49,7 @@ EXPORTS = [
     "kv_pool_write_tokens", "lazy_pack_page", "lazy_unpack_page", "lazy_pack_pages",
     "lazy_decode_workspace_bytes", "lazy_attn_decode", "lazy_prefill_workspace_bytes",
     "lazy_attn_prefill", "lazy_get_device_error", "lazy_debug_gather", "lazy_debug_wait_timeout",
-    "lazy_attn_decode_noalloc", "lazy_debug_exp2", "lazy_attn_prefill_append",
+    "lazy_attn_decode_noalloc", "lazy_attn_prefill_append",
     "lazy_pool_set_schedule_sms", "lazy_decode_shared_plan", "lazy_decode_shared_workspace_bytes",
     "lazy_attn_decode_shared",
     "lazy_pool_set_alibi", "lazy_pool_position_mode", "lazy_pool_set_decode_kernel",
@@ -113,7 +113,6 @@ _SIGS = {
     "lazy_get_device_error": ([_vp, _pi32, _vp], ctypes.c_int),
     "lazy_debug_gather": ([_vp, _vp, _i32, _vp, _vp, _vp, _vp], ctypes.c_int),
     "lazy_debug_wait_timeout": ([_vp, _u64, _vp], ctypes.c_int),
-    "lazy_debug_exp2": ([_vp, _vp, _i32, _vp], ctypes.c_int),
     "lazy_attn_decode_noalloc": ([_vp, _vp, _vp, _vp, _vp, _i32, _i32, _f32, _i32, _vp, _vp, _vp],
                                  ctypes.c_int),
     "lazy_decode_shared_plan": ([_vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _pi32,
@@ -591,12 +590,3 @@ def lazy_attn_decode_noalloc(pool: LazyPool, q, q_pos, page_words, cu_pages, sm_
         pool.handle, _ptr(q), _ptr(q_pos), _ptr(page_words), _ptr(cu_pages), B, Hq,
         float(sm_scale), grid_ctas, _ptr(out), _ptr(lse), _stream(stream)))
     return out, lse
-
-
-def lazy_debug_exp2(x, stream=None):
-    """2^x through the FMA-pipe exponential of the tensor-core softmax (test hook)."""
-    import torch
-    y = torch.empty_like(x)
-    _check("lazy_debug_exp2", load_library().lazy_debug_exp2(_ptr(x), _ptr(y), int(x.numel()),
-                                                             _stream(stream)))
-    return y

@@ -157,28 +157,10 @@ __global__ void wait_timeout_kernel(uint64_t limit_ns, int32_t *err) {
   if (!ok && threadIdx.x == 0) set_error(err, LAZY_DEVERR_TIMEOUT);
 }
 
-__global__ void exp2_kernel(const float *__restrict__ x, float *__restrict__ y, int32_t n) {
-  const int32_t i = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
-  if (i >= n) return;
-  const float2 in = make_float2(x[i], i + 1 < n ? x[i + 1] : 0.f);
-  const float2 out = exp2_poly2(in);
-  y[i] = out.x;
-  if (i + 1 < n) y[i + 1] = out.y;
-}
-
 }  // namespace
 }  // namespace lazy
 
 using namespace lazy;
-
-extern "C" int lazy_debug_exp2(const float *x, float *y, int32_t n, lazy_stream_t stream) {
-  if (n < 0 || (n > 0 && (!x || !y))) return LAZY_ERR_INVALID_ARG;
-  if (n == 0) return LAZY_OK;
-  const int pairs = (n + 1) / 2;
-  exp2_kernel<<<(pairs + 255) / 256, 256, 0, (cudaStream_t)stream>>>(x, y, n);
-  LAZY_CUDA_TRY(cudaGetLastError());
-  return LAZY_OK;
-}
 
 extern "C" int lazy_debug_wait_timeout(lazy_pool *p, uint64_t limit_ns, lazy_stream_t stream) {
   if (!p || limit_ns == 0 || limit_ns > 10000000000ull) return LAZY_ERR_INVALID_ARG;

@@ -170,38 +170,6 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
       : "memory");
 }
 
-// ------------------------------------------------------------------------------------------
-// 2^x on the FMA pipe, two values at once, for x <= 2^22. Cody-Waite reduction: j = round(x)
-// via the 1.5 * 2^23 rounding constant, f = x - j in [-1/2, 1/2], 2^f by a degree-5 polynomial
-// fitted with csrc/fit_exp2.py (max relative error 2.3e-7 in fp32), and j added to the exponent
-// field. Inputs below -126 are clamped there (the result is ~1e-38, i.e. zero for softmax
-// weights). Used to move part of the softmax exponentials off the MUFU unit.
-// ------------------------------------------------------------------------------------------
-constexpr float kExp2C0 = 1.000000119e+00f;
-constexpr float kExp2C1 = 6.931469440e-01f;
-constexpr float kExp2C2 = 2.402212024e-01f;
-constexpr float kExp2C3 = 5.550711975e-02f;
-constexpr float kExp2C4 = 9.675544687e-03f;
-constexpr float kExp2C5 = 1.327684964e-03f;
-
-__device__ __forceinline__ float2 exp2_poly2(float2 x) {
-  x.x = fmaxf(x.x, -126.f);
-  x.y = fmaxf(x.y, -126.f);
-  const float2 rnd = make_float2(12582912.f, 12582912.f);
-  const float2 t = __fadd2_rn(x, rnd);
-  const float2 j = __fadd2_rn(t, make_float2(-12582912.f, -12582912.f));
-  const float2 f = __fadd2_rn(x, make_float2(-j.x, -j.y));
-  float2 p = make_float2(kExp2C5, kExp2C5);
-  p = __ffma2_rn(p, f, make_float2(kExp2C4, kExp2C4));
-  p = __ffma2_rn(p, f, make_float2(kExp2C3, kExp2C3));
-  p = __ffma2_rn(p, f, make_float2(kExp2C2, kExp2C2));
-  p = __ffma2_rn(p, f, make_float2(kExp2C1, kExp2C1));
-  p = __ffma2_rn(p, f, make_float2(kExp2C0, kExp2C0));
-  const int jx = __float_as_int(t.x) - 0x4B400000, jy = __float_as_int(t.y) - 0x4B400000;
-  return make_float2(__int_as_float(__float_as_int(p.x) + (jx << 23)),
-                     __int_as_float(__float_as_int(p.y) + (jy << 23)));
-}
-
 __device__ __forceinline__ void set_error(int32_t *err, int32_t bits) {
   if (err) atomicOr(err, bits);
 }

@@ -27,6 +27,7 @@
 // Every wait is bounded; a timeout sets LAZY_DEVERR_TIMEOUT, raises a CTA abort flag that
 // releases the other roles, drains outstanding copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <string.h>
 
 #include <algorithm>
@@ -43,13 +44,6 @@ constexpr int kTile = 128;
 constexpr int kNK = 3;  // K ring: a K tile is free again as soon as both QK products read it
 constexpr int kNV = 2;  // V ring: freed after both PV products
 constexpr int kThreads = 384;
-// One softmax exponential pair in kPolyEvery on the FMA pipe (exp2_poly2) instead of MUFU;
-// 0 = all on MUFU. Measured on GB300: the softmax is issue-bound, not MUFU-bound, and every
-// offload ratio from 1/2 to 1/64 was slower, so it is off.
-#ifndef LAZY_POLY_EVERY
-#define LAZY_POLY_EVERY 0
-#endif
-constexpr int kPolyEvery = LAZY_POLY_EVERY;
 constexpr int kTileBytes = kTile * 128 * 2;  // 32 KB: 128 rows x 128 bf16
 constexpr int kHalfBytes = kTileBytes / 2;   // one 64-dim box column
 
@@ -300,36 +294,53 @@ __device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
   return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// Rotate, in place, one row of a 128-row swizzled bf16 tile at 16-byte chunk c of both 64-dim
-// boxes: x_i <- x_i cos - x_{i+64} sin, x_{i+64} <- x_i sin + x_{i+64} cos for i = 8c .. 8c+7,
-// in packed bf16x2 arithmetic (the operands are bf16 and so is the result the MMA reads;
-// 4 fused instructions per 2 pairs). co/si/nsi hold (cos, cos'), (sin, sin'), (-sin, -sin') of
-// frequencies 8c+2k, 8c+2k+1.
-struct RotPairs {
-  __nv_bfloat162 co[4], si[4], nsi[4];
+// (cos, sin) of the 8 frequencies of one 16-byte chunk c (dims 8c .. 8c+7 of each 64-dim half)
+// as fp32 pairs: co[k] = (cos, cos') of frequencies 8c+2k, 8c+2k+1, matching the (low, high)
+// halves of the chunk's 32-bit word k.
+struct RotF {
+  float2 co[4], si[4];
 };
-__device__ __forceinline__ void rotate_row_chunk(uint8_t *tile, int row, int c,
-                                                 const RotPairs &rp) {
+
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// The relative rotation of one row chunk, x_i <- x_i cos - x_{i+64} sin and
+// x_{i+64} <- x_i sin + x_{i+64} cos for i = 8c .. 8c+7: bf16 in (as loaded), fp16 out (the
+// operand type of the QK product), fp32 arithmetic with a single rounding at the end. fp16 keeps
+// 11 significant bits against bf16's 8, so the rotated query row, whose rounding error is the
+// same for every key it meets and does not average out, costs 8x less in the log-sum-exp.
+__device__ __forceinline__ void rot_words_f16(uint4 &a, uint4 &b, const RotF &rf) {
+  uint32_t *x = reinterpret_cast<uint32_t *>(&a);
+  uint32_t *y = reinterpret_cast<uint32_t *>(&b);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 xf = make_float2(__uint_as_float(x[k] << 16), __uint_as_float(x[k] & 0xFFFF0000u));
+    const float2 yf = make_float2(__uint_as_float(y[k] << 16), __uint_as_float(y[k] & 0xFFFF0000u));
+    const float2 ys = __fmul2_rn(yf, rf.si[k]);
+    const float2 xo = __ffma2_rn(xf, rf.co[k], make_float2(-ys.x, -ys.y));
+    const float2 yo = __ffma2_rn(xf, rf.si[k], __fmul2_rn(yf, rf.co[k]));
+    x[k] = pack_h2(xo.x, xo.y);
+    y[k] = pack_h2(yo.x, yo.y);
+  }
+}
+
+// Rotate, in place, one row of a 128-row swizzled tile at 16-byte chunk c of both 64-dim boxes
+// (the pair (i, i+64) of a row sits at the same swizzled offset of the two boxes).
+__device__ __forceinline__ void rotate_row_chunk(uint8_t *tile, int row, int c, const RotF &rf) {
   const int phys = (c ^ (row & 7)) * 16;
   uint4 *lo = reinterpret_cast<uint4 *>(tile + row * 128 + phys);
   uint4 *hi = reinterpret_cast<uint4 *>(tile + kHalfBytes + row * 128 + phys);
   uint4 a = *lo, b = *hi;
-  __nv_bfloat162 *x = reinterpret_cast<__nv_bfloat162 *>(&a);
-  __nv_bfloat162 *y = reinterpret_cast<__nv_bfloat162 *>(&b);
-  __nv_bfloat162 xo[4], yo[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    xo[k] = __hfma2(y[k], rp.nsi[k], __hmul2(x[k], rp.co[k]));
-    yo[k] = __hfma2(x[k], rp.si[k], __hmul2(y[k], rp.co[k]));
-  }
-  *lo = *reinterpret_cast<uint4 *>(xo);
-  *hi = *reinterpret_cast<uint4 *>(yo);
+  rot_words_f16(a, b, rf);
+  *lo = a;
+  *hi = b;
 }
 
 // The same rotation for 4 consecutive rows of one page (one angle set): all loads first, then
 // the math, then the stores.
-__device__ __forceinline__ void rotate_4rows_chunk(uint8_t *tile, int row0, int c,
-                                                   const RotPairs &rp) {
+__device__ __forceinline__ void rotate_4rows_chunk(uint8_t *tile, int row0, int c, const RotF &rf) {
   uint4 a[4], b[4];
 #pragma unroll
   for (int rr = 0; rr < 4; ++rr) {
@@ -339,18 +350,7 @@ __device__ __forceinline__ void rotate_4rows_chunk(uint8_t *tile, int row0, int 
     b[rr] = *reinterpret_cast<const uint4 *>(tile + kHalfBytes + row * 128 + phys);
   }
 #pragma unroll
-  for (int rr = 0; rr < 4; ++rr) {
-    __nv_bfloat162 *x = reinterpret_cast<__nv_bfloat162 *>(&a[rr]);
-    __nv_bfloat162 *y = reinterpret_cast<__nv_bfloat162 *>(&b[rr]);
-    __nv_bfloat162 xo[4], yo[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      xo[k] = __hfma2(y[k], rp.nsi[k], __hmul2(x[k], rp.co[k]));
-      yo[k] = __hfma2(x[k], rp.si[k], __hmul2(y[k], rp.co[k]));
-    }
-    a[rr] = *reinterpret_cast<uint4 *>(xo);
-    b[rr] = *reinterpret_cast<uint4 *>(yo);
-  }
+  for (int rr = 0; rr < 4; ++rr) rot_words_f16(a[rr], b[rr], rf);
 #pragma unroll
   for (int rr = 0; rr < 4; ++rr) {
     const int row = row0 + rr;
@@ -377,7 +377,7 @@ __device__ __noinline__ float4 angle_cs2(int64_t delta, uint64_t ta, uint64_t tb
 // thread before the first product; inside the tile loop the inlined copy costs more in code
 // size than it saves (measured), so a page offset change takes chunk_angles.
 __device__ __forceinline__ void chunk_angles_ilp(int64_t delta, const uint64_t *turn_s, int c,
-                                                 RotPairs &rp) {
+                                                 RotF &rf) {
   uint64_t tf[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) tf[e] = turn_s[c * 8 + e];
@@ -386,23 +386,45 @@ __device__ __forceinline__ void chunk_angles_ilp(int64_t delta, const uint64_t *
   for (int e = 0; e < 8; ++e) rope_cos_sin(delta, tf[e], co[e], si[e]);
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    rp.co[k] = __floats2bfloat162_rn(co[2 * k], co[2 * k + 1]);
-    rp.si[k] = __floats2bfloat162_rn(si[2 * k], si[2 * k + 1]);
-    rp.nsi[k] = __floats2bfloat162_rn(-si[2 * k], -si[2 * k + 1]);
+    rf.co[k] = make_float2(co[2 * k], co[2 * k + 1]);
+    rf.si[k] = make_float2(si[2 * k], si[2 * k + 1]);
   }
 }
 
-// (cos, sin) of delta * theta_i for i = 8c .. 8c+7 (exact fp32 angles), as bf16 pairs.
-__device__ __forceinline__ void chunk_angles(int64_t delta, const uint64_t *turn, int c,
-                                             RotPairs &rp) {
+// (cos, sin) of delta * theta_i for i = 8c .. 8c+7 (exact fp32 angles).
+__device__ __forceinline__ void chunk_angles(int64_t delta, const uint64_t *turn, int c, RotF &rf) {
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const float4 ab = angle_cs2(delta, turn[c * 8 + 2 * k], turn[c * 8 + 2 * k + 1]);
-    const float2 a = make_float2(ab.x, ab.y), b = make_float2(ab.z, ab.w);
-    rp.co[k] = __floats2bfloat162_rn(a.x, b.x);
-    rp.si[k] = __floats2bfloat162_rn(a.y, b.y);
-    rp.nsi[k] = __floats2bfloat162_rn(-a.y, -b.y);
+    rf.co[k] = make_float2(ab.x, ab.z);
+    rf.si[k] = make_float2(ab.y, ab.w);
   }
+}
+
+// The same angle set held compactly between tiles (a page offset usually spans several tiles):
+// fp16 pairs, 8 registers instead of 16 (the kernel runs at its register limit), widened to fp32
+// once per rotated tile. cos and sin are within 2^-12 of the fp32 values, the same order as the
+// fp16 rounding of the rotated element itself.
+struct RotH {
+  __half2 co[4], si[4];
+};
+__device__ __forceinline__ void chunk_angles_h(int64_t delta, const uint64_t *turn, int c,
+                                               RotH &rh) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float4 ab = angle_cs2(delta, turn[c * 8 + 2 * k], turn[c * 8 + 2 * k + 1]);
+    rh.co[k] = __floats2half2_rn(ab.x, ab.z);
+    rh.si[k] = __floats2half2_rn(ab.y, ab.w);
+  }
+}
+__device__ __forceinline__ RotF widen(const RotH &rh) {
+  RotF rf;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    rf.co[k] = __half22float2(rh.co[k]);
+    rf.si[k] = __half22float2(rh.si[k]);
+  }
+  return rf;
 }
 
 // Bounded wait that also gives up when another role raised the CTA abort flag.
@@ -657,9 +679,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   } else if (warp == 1) {
     // ============================== MMA issuer
     if (lane == 0) {
-      const uint32_t idesc_qk = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) |
-                                ((128u >> 4) << 24);
-      const uint32_t idesc_pv = idesc_qk | (1u << 16);  // B (= V) MN-major
+      // Instruction descriptors: fp32 accumulator (bit 4), N = 128 (bits 17-22), M = 128
+      // (bits 24-28); A type bits 7-9 and B type bits 10-12 are 0 = fp16, 1 = bf16. QK takes
+      // fp16 operands when the rotation passes wrote them (RoPE) and bf16 as loaded (ALiBi,
+      // nothing rotated); PV multiplies bf16 weights by bf16 values, V MN-major (bit 16).
+      const uint32_t idesc_base = (1u << 4) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+      const uint32_t idesc_bf16 = idesc_base | (1u << 7) | (1u << 10);
+      const uint32_t idesc_qk = kAlibi ? idesc_bf16 : idesc_base;
+      const uint32_t idesc_pv = idesc_bf16 | (1u << 16);
       const uint32_t q_addr = smem_u32(Qs), k_addr = smem_u32(Ks), v_addr = smem_u32(Vs);
       // Issue order keeps both softmax groups busy: QK for Q tile 0 of the next key tile is
       // issued as soon as P_0 of this tile is consumed, while group 1 still works on S_1.
@@ -747,7 +774,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       // this thread's own query row of Q tile i, rotated to R(m - m0)
 #pragma unroll 1
       for (int c = 0; c < 8; ++c) {
-        RotPairs rq;
+        RotF rq;
         chunk_angles_ilp((int64_t)(i * TQ + row / G), turn_s, c, rq);
         rotate_row_chunk(Qs + i * kTileBytes, row, c, rq);
       }
@@ -755,7 +782,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     }
     mbar_arrive(q_rot);
     int64_t cached = INT64_MIN;
-    RotPairs rp;
+    RotH rp;
     auto rotate_tile = [&](int jj) -> bool {
       const int s = jj % kNK;
       if (!cta_wait(&k_full[s], (jj / kNK) & 1, abort, lim, p.err)) return false;
@@ -768,14 +795,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         const int64_t d = (int64_t)mt.off[rrow0 >> 4] - m0;
         if (d != cached) {
           cached = d;
-          chunk_angles(d, turn, rc, rp);
+          chunk_angles_h(d, turn, rc, rp);
         }
-        rotate_4rows_chunk(kt, rrow0, rc, rp);
+        rotate_4rows_chunk(kt, rrow0, rc, widen(rp));
       } else {
         // question keys: raw, rotated by R(p - m0) row by row
 #pragma unroll 1
         for (int rr = 0; rr < 4; ++rr) {
-          RotPairs rk;
+          RotF rk;
           chunk_angles((int64_t)(mt.c0 + rrow0 + rr - t_row + t_off), turn, rc, rk);
           rotate_row_chunk(kt, rrow0 + rr, rc, rk);
         }
@@ -876,18 +903,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 #pragma unroll
         for (int e2 = 0; e2 < 32; e2 += 2) {
           const int e = q4 * 32 + e2;
-          float s0, s1;
           const float2 t = __ffma2_rn(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])),
                                       make_float2(sle, sle), make_float2(neg_m, neg_m));
-          if (kPolyEvery > 0 &&
-              ((e2 >> 1) % (kPolyEvery > 0 ? kPolyEvery : 1)) == kPolyEvery - 1) {
-            const float2 y = exp2_poly2(t);
-            s0 = y.x;
-            s1 = y.y;
-          } else {
-            s0 = ex2(t.x);
-            s1 = ex2(t.y);
-          }
+          const float s0 = ex2(t.x), s1 = ex2(t.y);
           lp2[(e2 >> 1) & 3] = __fadd2_rn(lp2[(e2 >> 1) & 3], make_float2(s0, s1));
           pw[e2 / 2] = pack_bf2(s0, s1);
         }

@@ -2,6 +2,13 @@
 
 Tolerances (fixed by the contract of this path): bf16 pools 2e-2 absolute on outputs and 1e-3
 absolute on log-sum-exp; fp32 pools 1e-5 on both; page-word and page indexing bit-exact.
+
+Reference forms. Layouts whose contexts hold at least 200 keys are checked against the oracle's
+form A (keys materialised at absolute positions). The pool keeps each cached key as R(j) k in its
+own element type; on a bf16 pool that storage rounding alone moves the log-sum-exp by about
+2e-3 / sqrt(keys), past 1e-3 on contexts of a few dozen keys. Small-context layouts are
+therefore checked against form S, the oracle with that storage step written out, at the same
+tolerances.
 """
 import math
 
@@ -43,12 +50,12 @@ def _decode(pk, wl, src=None, grid_ctas=0):
     return res, db, out.float().cpu().numpy(), lse.cpu().numpy()
 
 
-def _check_decode(wl, out, lse, reqs=None, kv_heads=None, src=None):
+def _check_decode(wl, out, lse, reqs=None, kv_heads=None, src=None, form="A"):
     to, tl = _tol(wl)
     reqs = reqs if reqs is not None else range(wl.batch)
     G = wl.Hq // wl.Hkv
     for i, b in enumerate(reqs):
-        ro, rl = oracle.attend_request(wl, b, kv_heads=kv_heads, src=src)
+        ro, rl = oracle.attend_request(wl, b, kv_heads=kv_heads, src=src, form=form)
         heads = range(wl.Hq) if kv_heads is None else [h * G + g for h in kv_heads for g in range(G)]
         heads = list(heads)
         do = np.abs(out[i][heads] - ro[0][heads]).max()
@@ -406,25 +413,15 @@ def _prefill(pk, wl, flags, src=None):
     return res, pb, out.float().cpu().numpy(), lse.cpu().numpy()
 
 
-# Tensor-core prefill on the small edge layouts: the MMA operands are bf16, so the rotated query
-# row R(m - m0) q and the relatively rotated key tile are rounded once more than in the fp32
-# CUDA-core path. A CPU emulation of exactly those roundings reproduces the GPU's lse to ~1e-7;
-# the query rounding is per row and does not average out over keys, giving a per-sample sigma of
-# ~1.6e-4 and a tail of 1.25e-3 over the 4160 (query, head) samples of a 700-key request. The
-# edge layouts therefore use 2e-3 on lse (~12 sigma); the full-size prefill workload keeps 1e-3.
-TC_EDGE_LSE_TOL = 2e-3
-
-
 def _check_prefill(wl, pb, out, lse, reqs=None, kv_heads=None, queries=None, src=None,
-                   lse_tol=None):
+                   form="A"):
     to, tl = _tol(wl)
-    if lse_tol is not None:
-        tl = lse_tol
     cu = pb.cu_q.cpu().numpy()
     G = wl.Hq // wl.Hkv
     reqs = range(wl.batch) if reqs is None else reqs
     for b in reqs:
-        ro, rl = oracle.attend_request(wl, b, kv_heads=kv_heads, queries=queries, src=src)
+        ro, rl = oracle.attend_request(wl, b, kv_heads=kv_heads, queries=queries, src=src,
+                                       form=form)
         rows = np.arange(cu[b], cu[b + 1])
         qi = np.arange(len(rows)) if queries is None else np.asarray(queries)
         heads = list(range(wl.Hq)) if kv_heads is None else \
@@ -498,7 +495,7 @@ def test_prefill_tensor_core_parity(pk, Hq, Hkv):
     # lengths 37 / 5 / 130
     wl = _edge_prefill_workload(128, Hq, Hkv, "bf16")
     _, pb, out, lse = _prefill(pk, wl, pk.LAZY_PREFILL_TC)
-    _check_prefill(wl, pb, out, lse, lse_tol=TC_EDGE_LSE_TOL)
+    _check_prefill(wl, pb, out, lse)
 
 
 @pytest.mark.parametrize("flags", ["tc", "simt", "simt_qside"])
@@ -514,7 +511,7 @@ def test_prefill_offsets_near_the_page_word_limit(pk, flags):
     fl = {"tc": pk.LAZY_PREFILL_TC, "simt": pk.LAZY_PREFILL_SIMT,
           "simt_qside": pk.LAZY_PREFILL_SIMT_QSIDE}[flags]
     _, pb, out, lse = _prefill(pk, wl, fl)
-    _check_prefill(wl, pb, out, lse, lse_tol=TC_EDGE_LSE_TOL if flags == "tc" else None)
+    _check_prefill(wl, pb, out, lse)
 
 
 # Last-wave split of the tensor-core prefill. The edge layout has 3 requests (question lengths
@@ -544,7 +541,7 @@ def test_prefill_last_wave_split(pk, Hq, Hkv, sms):
         return out.float().cpu().numpy(), lse.cpu().numpy()
 
     out, lse = run(sms)
-    _check_prefill(wl, pb, out, lse, lse_tol=TC_EDGE_LSE_TOL)
+    _check_prefill(wl, pb, out, lse)
     # against the unsplit schedule: the chunks' fp32 partials merge to the same rows up to
     # the bf16 rounding of the weights (chunk-local maxima) and of the output
     o1, l1 = run(1)
@@ -577,7 +574,7 @@ def test_prefill_tensor_core_matches_cuda_core_kernel(pk):
     wl = _edge_prefill_workload(128, 32, 8, "bf16")
     _, _, o_tc, l_tc = _prefill(pk, wl, pk.LAZY_PREFILL_TC)
     _, _, o_si, l_si = _prefill(pk, wl, pk.LAZY_PREFILL_SIMT)
-    assert np.abs(o_tc - o_si).max() <= 2e-2 and np.abs(l_tc - l_si).max() <= TC_EDGE_LSE_TOL
+    assert np.abs(o_tc - o_si).max() <= 2e-2 and np.abs(l_tc - l_si).max() <= 1e-3
 
 
 def test_prefill_without_question_keys(pk):
@@ -607,31 +604,22 @@ def test_prefill_without_question_keys(pk):
                     q[:, h * G:(h + 1) * G], r.q_pos0 + np.arange(r.T), base=wl.rope_base,
                     scale=wl.sm_scale)
                 rows = slice(cu[b], cu[b + 1])
-                tol = TC_EDGE_LSE_TOL if flags == pk.LAZY_PREFILL_TC else 1e-3
                 assert np.abs(out[rows, h * G:(h + 1) * G] - o).max() <= 2e-2
-                assert np.abs(lse[rows, h * G:(h + 1) * G] - l).max() <= tol
+                assert np.abs(lse[rows, h * G:(h + 1) * G] - l).max() <= 1e-3
 
 
-def test_fma_pipe_exp2_against_cuda(pk):
-    # The softmax's polynomial exponential against torch.exp2 (CUDA's exp2f) on the range the
-    # softmax feeds it (<= 8, down to the flush point), relative error <= 4e-7 (fit: 2.3e-7).
-    x = torch.cat([torch.linspace(-126.0, 8.0, 1_000_003, device="cuda"),
-                   torch.tensor([0.0, 0.5, -0.5, 1.0, -1.0, 7.5, -7.5, -100.25], device="cuda")])
-    y = pk.lazy_debug_exp2(x)
-    ref = torch.exp2(x.double())
-    rel = ((y.double() - ref).abs() / ref).max().item()
-    assert rel <= 4e-7, rel
-
-
-def test_mixed_step_full_size_sampled(pk):
-    # skew-sweep mixed step (alpha 1.2): one prefill launch (32 ragged questions) and one decode
-    # step (96 requests) over the same resident 4096-doc pool; sampled against the oracle
+@pytest.mark.parametrize("alpha", [0.6, 0.9, 1.2])
+def test_mixed_step_full_size_sampled(pk, alpha):
+    # skew-sweep mixed step: one prefill launch (32 ragged questions) and one decode step
+    # (96 requests) over the same resident 4096-doc pool, as the bench runs it; sampled against
+    # the oracle on both halves: 3 prefill requests x 2 kv heads x 4 question rows (first, middle,
+    # last and a row of the second Q tile) and 4 decode requests x 2 kv heads
     H = _h()
-    wl = W.mixed_workload(1.2)
+    wl = W.mixed_workload(alpha)
     src = H.DeviceSource(wl)
     res = H.build_resident(wl, src, drop_raw=False)
     pb = H.prefill_batch(wl, res, src)
-    db = H.decode_batch(wl, res, src)
+    db = H.decode_batch(wl, res, src, align_shared=True)
     pout, plse = pk.lazy_attn_prefill(res.pool, pb.q, pb.k_new, pb.v_new, pb.cu_q, pb.q_pos0,
                                       pb.words, pb.cu_pages, pb.max_q_len, sm_scale=wl.sm_scale)
     pk.kv_pool_write_tokens(res.pool, db.new_k, db.new_v, db.slot_mapping, db.local_pos)
@@ -640,24 +628,106 @@ def test_mixed_step_full_size_sampled(pk):
     torch.cuda.synchronize()
     assert pk.lazy_get_device_error(res.pool) == 0
     view = src.host_view()
-    # prefill: request pb.reqs[3] (its rows in the packed batch), kv heads 1 and 6
-    pr = pb.reqs[3]
+    G = wl.Hq // wl.Hkv
     cu = pb.cu_q.cpu().numpy()
-    ro, rl = oracle.attend_request(wl, pr.index, kv_heads=[1, 6], queries=[0, pr.T // 2, pr.T - 1],
-                                   src=view)
-    heads = [4, 5, 6, 7, 24, 25, 26, 27]
-    rows = cu[3] + np.array([0, pr.T // 2, pr.T - 1])
-    o = pout.float().cpu().numpy()[rows][:, heads]
-    l = plse.cpu().numpy()[rows][:, heads]
-    qi = [0, pr.T // 2, pr.T - 1]
-    assert np.abs(o - ro[qi][:, heads]).max() <= 2e-2
-    assert np.abs(l - rl[qi][:, heads]).max() <= 1e-3
-    # decode: request db.reqs[10], kv head 3
-    dr = db.reqs[10]
-    ro, rl = oracle.attend_request(wl, dr.index, kv_heads=[3], src=view)
-    heads = [12, 13, 14, 15]
-    assert np.abs(dout.float().cpu().numpy()[10][heads] - ro[0][heads]).max() <= 2e-2
-    assert np.abs(dlse.cpu().numpy()[10][heads] - rl[0][heads]).max() <= 1e-3
+    pout = pout.float().cpu().numpy()
+    plse = plse.cpu().numpy()
+    for i in (0, 3, len(pb.reqs) - 1):
+        pr = pb.reqs[i]
+        qi = sorted({0, min(40, pr.T - 1), pr.T // 2, pr.T - 1})
+        kvh = [1, 6]
+        ro, rl = oracle.attend_request(wl, pr.index, kv_heads=kvh, queries=qi, src=view)
+        heads = [h * G + g for h in kvh for g in range(G)]
+        rows = cu[i] + np.array(qi)
+        assert np.abs(pout[rows][:, heads] - ro[qi][:, heads]).max() <= 2e-2, pr.index
+        assert np.abs(plse[rows][:, heads] - rl[qi][:, heads]).max() <= 1e-3, pr.index
+    dout = dout.float().cpu().numpy()
+    dlse = dlse.cpu().numpy()
+    for i in (0, 10, 50, len(db.reqs) - 1):
+        dr = db.reqs[i]
+        kvh = [3, 7]
+        ro, rl = oracle.attend_request(wl, dr.index, kv_heads=kvh, src=view)
+        heads = [h * G + g for h in kvh for g in range(G)]
+        assert np.abs(dout[i][heads] - ro[0][heads]).max() <= 2e-2, dr.index
+        assert np.abs(dlse[i][heads] - rl[0][heads]).max() <= 1e-3, dr.index
+
+
+# ------------------------------------------------------------------ small contexts (form S)
+def _small_decode_workload(Hq, Hkv, dtype="bf16", D=128):
+    # contexts of 1 to 88 keys: 24-token documents (a whole and a half page), one document at
+    # two offsets, a request holding only its 1-token private segment (m = 0, one key)
+    segs = [[(0, 0), (1, 24)], [(2, 5)], [], [(1, 100), (0, 7), (1, 300)]]
+    priv = [(48, 3), (29, 9), (0, 1), (500, 16)]
+    return W.custom("decode", segs, doc_len=24, n_pool=3, Hq=Hq, Hkv=Hkv, D=D, dtype=dtype,
+                    base=500000.0 if D == 128 else 10000.0, priv=priv, seed=21)
+
+
+def _small_prefill_workload(Hq, Hkv, dtype="bf16", D=128):
+    # 16-token documents, a 5-token question after one document, a 100-token question with no
+    # document at all (row 0 sees one key), and questions crossing Q-tile boundaries
+    segs = [[(0, 0), (1, 16)], [(2, 3)], [], [(1, 5000), (0, 17)]]
+    return W.custom("prefill", segs, doc_len=16, n_pool=3, Hq=Hq, Hkv=Hkv, D=D, dtype=dtype,
+                    base=500000.0 if D == 128 else 10000.0, T=[37, 5, 100, 64],
+                    q_pos0=[32, 19, 0, 9000], seed=22)
+
+
+@pytest.mark.parametrize("kind", ["simt", "auto"])
+@pytest.mark.parametrize("D,Hq,Hkv,dtype", [
+    (128, 32, 8, "bf16"), (128, 8, 8, "bf16"), (128, 64, 8, "bf16"), (128, 32, 1, "bf16"),
+    (64, 16, 8, "bf16"), (64, 8, 2, "fp32")])
+def test_decode_small_contexts(pk, kind, D, Hq, Hkv, dtype):
+    H = _h()
+    wl = _small_decode_workload(Hq, Hkv, dtype, D)
+    src = H.HostSource(wl)
+    res = H.build_resident(wl, src, resident_pool=False)
+    pk.lazy_pool_set_decode_kernel(res.pool, pk.LAZY_DECODE_SIMT if kind == "simt"
+                                   else pk.LAZY_DECODE_AUTO)
+    db = H.decode_batch(wl, res, src)
+    out, lse = pk.lazy_attn_decode(res.pool, db.q, db.q_pos, db.words, db.cu_pages,
+                                   sm_scale=wl.sm_scale)
+    torch.cuda.synchronize()
+    assert pk.lazy_get_device_error(res.pool) == 0
+    out, lse = out.float().cpu().numpy(), lse.cpu().numpy()
+    _check_decode(wl, out, lse, form="S")
+    # one key: the output is that key's value and lse its score
+    G = wl.Hq // wl.Hkv
+    v = wl.new_v(2)[0]
+    assert np.abs(out[2] - np.repeat(v, G, axis=0)).max() <= (1e-2 if dtype == "bf16" else 1e-6)
+
+
+@pytest.mark.parametrize("flags", ["tc", "simt", "simt_qside"])
+@pytest.mark.parametrize("Hq,Hkv", [(32, 8), (8, 8), (16, 2), (32, 1)])
+def test_prefill_small_contexts(pk, flags, Hq, Hkv):
+    wl = _small_prefill_workload(Hq, Hkv)
+    fl = {"tc": pk.LAZY_PREFILL_TC, "simt": pk.LAZY_PREFILL_SIMT,
+          "simt_qside": pk.LAZY_PREFILL_SIMT_QSIDE}[flags]
+    _, pb, out, lse = _prefill(pk, wl, fl)
+    _check_prefill(wl, pb, out, lse, form="S")
+
+
+@pytest.mark.parametrize("flags", ["simt", "simt_qside"])
+def test_prefill_small_contexts_fp32(pk, flags):
+    wl = _small_prefill_workload(8, 2, "fp32", 64)
+    fl = pk.LAZY_PREFILL_SIMT if flags == "simt" else pk.LAZY_PREFILL_SIMT_QSIDE
+    _, pb, out, lse = _prefill(pk, wl, fl)
+    _check_prefill(wl, pb, out, lse, form="S")
+
+
+@pytest.mark.parametrize("sms", [5, 20])
+def test_prefill_small_contexts_last_wave_split(pk, sms):
+    # the tensor-core prefill's key-range chunks on short contexts (some chunks see no key)
+    H = _h()
+    wl = _small_prefill_workload(32, 8)
+    src = H.HostSource(wl)
+    res = H.build_resident(wl, src, resident_pool=False, drop_raw=False)
+    pb = H.prefill_batch(wl, res, src)
+    pk.lazy_pool_set_schedule_sms(res.pool, sms)
+    out, lse = pk.lazy_attn_prefill(res.pool, pb.q, pb.k_new, pb.v_new, pb.cu_q, pb.q_pos0,
+                                    pb.words, pb.cu_pages, pb.max_q_len, sm_scale=wl.sm_scale,
+                                    flags=pk.LAZY_PREFILL_TC)
+    torch.cuda.synchronize()
+    assert pk.lazy_get_device_error(res.pool) == 0
+    _check_prefill(wl, pb, out.float().cpu().numpy(), lse.cpu().numpy(), form="S")
 
 
 # ------------------------------------------------------------------ page order
@@ -706,5 +776,4 @@ def test_prefill_random_segment_orders(pk, seed, flags):
                                     else pk.LAZY_PREFILL_SIMT)
     torch.cuda.synchronize()
     assert pk.lazy_get_device_error(res.pool) == 0
-    _check_prefill(wl, pb, out.float().cpu().numpy(), lse.cpu().numpy(),
-                   lse_tol=TC_EDGE_LSE_TOL if flags == "tc" else None)
+    _check_prefill(wl, pb, out.float().cpu().numpy(), lse.cpu().numpy())

@@ -50,13 +50,13 @@ def _both(pk, wl, src=None, grid_ctas=0, align=False, slopes=None):
             o_d.float().cpu().numpy(), l_d.cpu().numpy())
 
 
-def _check(wl, out, lse, reqs=None, kv_heads=None, src=None):
+def _check(wl, out, lse, reqs=None, kv_heads=None, src=None, form="A"):
     reqs = reqs if reqs is not None else range(wl.batch)
     G = wl.Hq // wl.Hkv
     heads = list(range(wl.Hq)) if kv_heads is None else \
         [h * G + g for h in kv_heads for g in range(G)]
     for b in reqs:
-        ro, rl = oracle.attend_request(wl, b, kv_heads=kv_heads, src=src)
+        ro, rl = oracle.attend_request(wl, b, kv_heads=kv_heads, src=src, form=form)
         assert np.abs(out[b][heads] - ro[0][heads]).max() <= 2e-2, b
         assert np.abs(lse[b][heads] - rl[0][heads]).max() <= 1e-3, b
 
@@ -167,6 +167,37 @@ def test_shared_decode_full_size_sampled(pk):
     assert pairs >= 150 and plan.n_entries < 0.75 * (32 * refs + 5 * len(wl.requests))
     assert np.abs(o_s - o_d).max() <= 1e-2 and np.abs(l_s - l_d).max() <= 1e-4
     _check(wl, o_s, l_s, reqs=[0, 17, 63], kv_heads=[0, 5], src=src.host_view())
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(32, 8), (8, 8), (4, 1)])
+def test_shared_decode_small_contexts(pk, Hq, Hkv):
+    # contexts of 1 to 88 keys with 24-token documents shared by several requests, checked
+    # against the oracle's stored-key form (the pool's bf16 copy of R(j) k written out)
+    segs = [[(0, 0), (1, 24)], [(1, 5), (0, 77)], [], [(1, 100), (0, 7), (1, 300)]]
+    priv = [(48, 3), (29, 9), (0, 1), (500, 16)]
+    wl = W.custom("decode", segs, doc_len=24, n_pool=2, Hq=Hq, Hkv=Hkv, D=128, dtype="bf16",
+                  base=500000.0, priv=priv, seed=23)
+    plan, o_s, l_s, o_d, l_d = _both(pk, wl)
+    assert any(plan.unit_req[2 * u + 1] >= 0 for u in range(plan.n_units))
+    _check(wl, o_s, l_s, form="S")
+    assert np.abs(o_s - o_d).max() <= 1e-2 and np.abs(l_s - l_d).max() <= 1e-4
+
+
+def test_long_decode_shared_full_size_sampled(pk):
+    # long_decode_b16 (16 requests x 64 Zipf(1.2) documents x 2048 + the new token) through the
+    # shared-segment plan of the aligned tables, as the bench times it: 3 requests x 2 kv heads
+    H = _h()
+    wl = W.long_decode_workload()
+    src = H.DeviceSource(wl)
+    res = H.build_resident(wl, src, drop_raw=False)
+    db = H.decode_batch(wl, res, src, align_shared=True)
+    host_plan, plan = _plan(pk, db)
+    o_s, l_s = pk.lazy_attn_decode_shared(res.pool, db.q, db.q_pos, plan, sm_scale=wl.sm_scale)
+    torch.cuda.synchronize()
+    assert pk.lazy_get_device_error(res.pool) == 0
+    assert sum(int(host_plan.unit_req[2 * u + 1] >= 0) for u in range(host_plan.n_units)) >= 16
+    _check(wl, o_s.float().cpu().numpy(), l_s.cpu().numpy(), reqs=[0, 7, 15], kv_heads=[2, 6],
+           src=src.host_view())
 
 
 @pytest.mark.parametrize("which", ["a_out_of_range", "b_out_of_range", "b_other_block"])
