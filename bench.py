@@ -2,16 +2,22 @@
 
 Headline (the ``value`` of the JSON line): decode KV GB/s on the decode-step workload
 (64 requests x 8 Zipf(1.0) docs of 512 tokens + 65-token private segment, 32/8/128 bf16, RoPE
-base 5e5, page size 16). One step = append each request's new token to its private segment
-(kv_pool_write_tokens) + lazy_attn_decode (split-KV kernel + log-sum-exp combine).
-GB/s counts the logical K+V bytes each request attends (4096 B per key); L2 is flushed (a 512 MB
-write) before every timed step so shared documents are re-read from HBM.
+base 5e5, page size 16), each request's segments in the aligned order (documents shared by
+several requests at the same index). One step = append each request's new token to its private
+segment (kv_pool_write_tokens) + lazy_attn_decode (split-KV kernel + log-sum-exp combine).
+GB/s counts the logical K+V bytes each request attends (4096 B per key). Before every timed step
+the L2 is flushed: a 512 MB write, then a 512 MB read, so that shared documents come from HBM
+and the cache holds clean lines (the write-back of the flush's own dirty lines stays outside
+the timed region; a control line times the write-only flush).
 
 Extra objects on the same line:
+  roofline      of the decode call against MEASURED_PEAKS.json: achieved = the step's unique
+                K+V bytes (each distinct cached page once, the least any schedule must read)
+                over the call's time; beside it the DRAM bytes ncu counted for the kernel, the
+                logical-byte rate and the no-reuse control.
   prefill       TFLOP/s of lazy_attn_prefill on the prefill workload (8 requests x 16 docs of
                 1024 + 256-token causal question), causal-visible QK^T + PV FLOPs only.
   long_decode   KV GB/s and tokens/s on the long-context decode (16 x 131073 keys).
-  roofline      of the dominant kernel (the decode call), against MEASURED_PEAKS.json.
   cpu_baseline  the fp64 oracle on the host cores over a bounded sample of the same workload.
   e2e           the decode step through the public API from pinned host buffers, transfers inside
                 the timed region.
@@ -327,7 +333,7 @@ def bench_prefill_only(args):
     pk.load_library()
     _, tc_peak, _, peak_kind = _peaks()
     stream = torch.cuda.current_stream()
-    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    flush, _ = _make_flush(torch)
     pwl = W.prefill_workload()
     psrc = H.DeviceSource(pwl)
     pres = H.build_resident(pwl, psrc, resident_pool=False)
@@ -347,12 +353,98 @@ def bench_prefill_only(args):
     if pk.lazy_get_device_error(pres.pool) != 0:
         raise RuntimeError("device error during warm-up")
     torch.cuda.nvtx.range_push("timed_region")
-    ms = _timed_steps(prefill_call, args.steps, flush_buf.zero_, stream)
+    ms = _timed_steps(prefill_call, args.steps, flush, stream)
     torch.cuda.nvtx.range_pop()
     avg = sum(ms) / len(ms)
     tflops = pb.flops / (avg * 1e-3) / 1e12
     print(json.dumps({"mode": "prefill only", "value": round(tflops, 2), "unit": "TFLOP/s",
                       "ms_per_call": round(avg, 4), "frac": round(tflops / tc_peak, 4),
+                      "peak_kind": peak_kind, "steps": args.steps}), flush=True)
+
+
+def _unique_kv_bytes(words_u64, per_token):
+    """K+V bytes of the distinct pages a batch's page words address: each (block) once, with its
+    valid tokens (the least any schedule must read from HBM)."""
+    import numpy as np
+    w = np.asarray(words_u64, dtype=np.uint64)
+    blk = (w & np.uint64(0xFFFFFFFF)).astype(np.int64)
+    nv = ((w >> np.uint64(58)) + np.uint64(1)).astype(np.int64)
+    order = np.lexsort((-nv, blk))
+    blk, nv = blk[order], nv[order]
+    first = np.ones(len(blk), dtype=bool)
+    first[1:] = blk[1:] != blk[:-1]
+    return int(nv[first].sum()) * per_token
+
+
+def _make_flush(torch):
+    """L2 flush between timed steps: a 512 MB write, then a 512 MB read. The read evicts the
+    write's dirty lines (their write-back happens here, untimed) and leaves the cache holding
+    clean lines of a buffer the timed work never touches."""
+    wbuf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    rbuf = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+
+    def flush():
+        wbuf.zero_()
+        rbuf.sum()
+
+    def flush_write_only():
+        wbuf.zero_()
+    return flush, flush_write_only
+
+
+def _traffic(name):
+    """The recorded ncu DRAM bytes per launch for a workload (profiles/TRAFFIC_FILE), or None
+    when the kernel sources have changed since the capture."""
+    prof = os.path.join(ROOT, "profiles", TRAFFIC_FILE)
+    try:
+        with open(prof) as f:
+            rec = json.load(f).get(name)
+        if rec and rec.get("kernel_hash") == _kernel_hash(name):
+            return rec
+    except (OSError, ValueError):
+        pass
+    return None
+
+
+def bench_long_decode_only(args):
+    """Long-context decode alone (resident pool of its 512 documents): for profiling runs."""
+    import numpy as np
+    import torch
+
+    import position_independent_kv_lazy_gb300 as pk
+    import workload as W
+    from position_independent_kv_lazy_gb300 import harness as H
+
+    pk.build_library()
+    pk.load_library()
+    hbm_peak, _, _, peak_kind = _peaks()
+    stream = torch.cuda.current_stream()
+    flush, _ = _make_flush(torch)
+    lwl = W.long_decode_workload()
+    lsrc = H.DeviceSource(lwl)
+    lres = H.build_resident(lwl, lsrc)
+    ldb = H.decode_batch(lwl, lres, lsrc, align_shared=True)
+    lws = torch.empty(pk.lazy_decode_workspace_bytes(lres.pool, lwl.batch, lwl.Hq),
+                      dtype=torch.uint8, device="cuda")
+    lout = torch.empty_like(ldb.q)
+    llse = torch.empty((lwl.batch, lwl.Hq), dtype=torch.float32, device="cuda")
+    l_bytes = ldb.n_keys * lwl.kv_bytes_per_token()
+    l_uniq = _unique_kv_bytes(ldb.words.cpu().numpy().view(np.uint64), lwl.kv_bytes_per_token())
+
+    def long_call():
+        pk.lazy_attn_decode(lres.pool, ldb.q, ldb.q_pos, ldb.words, ldb.cu_pages,
+                            sm_scale=lwl.sm_scale, out=lout, lse=llse, workspace=lws)
+
+    for _ in range(args.warmup):
+        flush(); long_call()
+    torch.cuda.synchronize()
+    if pk.lazy_get_device_error(lres.pool) != 0:
+        raise RuntimeError("device error during warm-up")
+    ms = _timed_steps(long_call, args.steps, flush, stream)
+    avg = sum(ms) / len(ms)
+    print(json.dumps({"mode": "long decode only", "value": round(l_bytes / avg / 1e6, 2),
+                      "unit": "GB/s", "ms_per_call": round(avg, 4), "unique_bytes": l_uniq,
+                      "frac_unique": round(l_uniq / avg / 1e6 / hbm_peak, 4),
                       "peak_kind": peak_kind, "steps": args.steps}), flush=True)
 
 
@@ -370,10 +462,7 @@ def bench_ours(args):
     pk.load_library()
     hbm_peak, tc_peak, tc_sus, peak_kind = _peaks()
     stream = torch.cuda.current_stream()
-    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
-
-    def flush():
-        flush_buf.zero_()
+    flush, flush_write_only = _make_flush(torch)
 
     # ---------------- decode-step workload (headline)
     wl = W.decode_workload()
@@ -383,29 +472,17 @@ def bench_ours(args):
     # attention result does not depend on page order); the context order is timed as a control
     db = H.decode_batch(wl, res, src, align_shared=True)
     cdb = H.decode_batch(wl, res, src)
-    kv_bytes = db.n_keys * wl.kv_bytes_per_token()  # K and V, 4096 B per key
+    per_tok = wl.kv_bytes_per_token()
+    kv_bytes = db.n_keys * per_tok  # K and V, 4096 B per key of every request's context
+    words_h = db.words.cpu().numpy().view(np.uint64)
+    uniq_bytes = _unique_kv_bytes(words_h, per_tok)
     B = wl.batch
     ws_bytes = pk.lazy_decode_workspace_bytes(res.pool, B, wl.Hq)
     workspace = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
     out = torch.empty_like(db.q)
     lse = torch.empty((B, wl.Hq), dtype=torch.float32, device="cuda")
-    # The headline decode runs the shared-segment plan of the aligned page tables: identical
-    # document segments of two requests share one fragment and one page load. The plan is host
-    # data derived from the page tables, like them prepared by the serving layer (its build time
-    # is reported as plan_host_ms; a decode step only changes the private tail's last word).
-    t_plan = time.perf_counter()
-    plan_h = pk.lazy_decode_shared_plan(db.words.cpu().numpy().view(np.uint64),
-                                        db.cu_pages.cpu().numpy())
-    plan_host_ms = (time.perf_counter() - t_plan) * 1e3
-    plan = plan_h.to("cuda")
-    sws = torch.empty(pk.lazy_decode_shared_workspace_bytes(res.pool, plan.n_units, wl.Hq),
-                      dtype=torch.uint8, device="cuda")
 
     def decode_call():
-        pk.lazy_attn_decode_shared(res.pool, db.q, db.q_pos, plan, sm_scale=wl.sm_scale,
-                                   out=out, lse=lse, workspace=sws)
-
-    def per_request_call():
         pk.lazy_attn_decode(res.pool, db.q, db.q_pos, db.words, db.cu_pages,
                             sm_scale=wl.sm_scale, out=out, lse=lse, workspace=workspace)
 
@@ -413,11 +490,24 @@ def bench_ours(args):
         pk.lazy_attn_decode(res.pool, cdb.q, cdb.q_pos, cdb.words, cdb.cu_pages,
                             sm_scale=wl.sm_scale, out=out, lse=lse, workspace=workspace)
 
+    # the shared-segment path over the same tables (control): its plan is host data rebuilt
+    # from the page tables; its build time is reported beside it
+    t_plan = time.perf_counter()
+    plan_h = pk.lazy_decode_shared_plan(words_h, db.cu_pages.cpu().numpy())
+    plan_host_ms = (time.perf_counter() - t_plan) * 1e3
+    plan = plan_h.to("cuda")
+    sws = torch.empty(pk.lazy_decode_shared_workspace_bytes(res.pool, plan.n_units, wl.Hq),
+                      dtype=torch.uint8, device="cuda")
+
+    def shared_call():
+        pk.lazy_attn_decode_shared(res.pool, db.q, db.q_pos, plan, sm_scale=wl.sm_scale,
+                                   out=out, lse=lse, workspace=sws)
+
     def step():
         pk.kv_pool_write_tokens(res.pool, db.new_k, db.new_v, db.slot_mapping, db.local_pos)
         decode_call()
 
-    launches_per_step = 3  # encode (append) + shared decode + its combine
+    launches_per_step = 3  # encode (append) + decode kernel + its combine
 
     # no-reuse control: same shapes, every request with its own documents (logical = DRAM bytes)
     nwl = W.decode_workload(no_reuse=True, name="decode_b64_no_reuse")
@@ -434,8 +524,8 @@ def bench_ours(args):
         pk.lazy_attn_decode(nres.pool, ndb.q, ndb.q_pos, ndb.words, ndb.cu_pages,
                             sm_scale=nwl.sm_scale, out=nout, lse=nlse, workspace=nws)
 
-    # e2e buffers: the step's inputs packed in one pinned host buffer (one H2D copy) and its
-    # outputs in one device buffer (one D2H copy), as a serving loop would stage them
+    # e2e buffers: the step's inputs packed in one pinned host buffer (one H2D copy); the result
+    # reaches the host through the decode itself (see e2e_step)
     def _layout(items):
         offs, total = [], 0
         for t in items:
@@ -443,8 +533,7 @@ def bench_ours(args):
             total += (t.numel() * t.element_size() + 255) // 256 * 256
         return offs, total
 
-    in_src = [db.q, db.new_k, db.new_v, plan.entries, plan.cu_entries, plan.unit_req,
-              plan.cu_members, plan.members, plan.member_entries, db.q_pos, db.slot_mapping,
+    in_src = [db.q, db.new_k, db.new_v, db.words, db.cu_pages, db.q_pos, db.slot_mapping,
               db.local_pos]
     in_offs, in_total = _layout(in_src)
     h_in = torch.empty(in_total, dtype=torch.uint8).pin_memory()
@@ -456,11 +545,10 @@ def bench_ours(args):
 
     for t, o in zip(in_src, in_offs):
         _view(h_in, o, t).copy_(t.cpu())
-    (d_q, d_k, d_v, d_ent, d_cue, d_ureq, d_cum, d_mem, d_ment, d_pos, d_slot, d_lpos) = [
+    (d_q, d_k, d_v, d_words, d_cu, d_pos, d_slot, d_lpos) = [
         _view(d_in, o, t) for t, o in zip(in_src, in_offs)]
-    d_plan = pk.SharedPlan(d_ent, d_cue, d_ureq, d_cum, d_mem, d_ment)
-    # the result goes device -> host through the decode itself: out and lse live in pinned
-    # host memory, which the GPU addresses directly, so the combine writes them there
+    # out and lse live in pinned host memory, which the GPU addresses directly, so the combine
+    # writes the result there
     out_offs, out_total = _layout([out, lse])
     h_res = torch.empty(out_total, dtype=torch.uint8).pin_memory()
     e_out, e_lse = _view(h_res, out_offs[0], out), _view(h_res, out_offs[1], lse)
@@ -470,8 +558,8 @@ def bench_ours(args):
     def e2e_step():
         d_in.copy_(h_in, non_blocking=True)
         pk.kv_pool_write_tokens(res.pool, d_k, d_v, d_slot, d_lpos)
-        pk.lazy_attn_decode_shared(res.pool, d_q, d_pos, d_plan, sm_scale=wl.sm_scale,
-                                   out=e_out, lse=e_lse, workspace=sws)
+        pk.lazy_attn_decode(res.pool, d_q, d_pos, d_words, d_cu, sm_scale=wl.sm_scale,
+                            out=e_out, lse=e_lse, workspace=workspace)
 
     only_decode = args.only == "decode"
 
@@ -498,18 +586,18 @@ def bench_ours(args):
         lsrc = H.DeviceSource(lwl)
         lres = H.build_resident(lwl, lsrc)
         ldb = H.decode_batch(lwl, lres, lsrc, align_shared=True)
-        lplan = pk.lazy_decode_shared_plan(ldb.words.cpu().numpy().view(np.uint64),
-                                           ldb.cu_pages.cpu().numpy()).to("cuda")
-        lws = torch.empty(pk.lazy_decode_shared_workspace_bytes(lres.pool, lplan.n_units, lwl.Hq),
+        lws = torch.empty(pk.lazy_decode_workspace_bytes(lres.pool, lwl.batch, lwl.Hq),
                           dtype=torch.uint8, device="cuda")
         lout = torch.empty_like(ldb.q)
         llse = torch.empty((lwl.batch, lwl.Hq), dtype=torch.float32, device="cuda")
         l_bytes = ldb.n_keys * lwl.kv_bytes_per_token()
+        l_uniq = _unique_kv_bytes(ldb.words.cpu().numpy().view(np.uint64),
+                                  lwl.kv_bytes_per_token())
         pools.append(lres.pool)
 
     def long_call():
-        pk.lazy_attn_decode_shared(lres.pool, ldb.q, ldb.q_pos, lplan, sm_scale=lwl.sm_scale,
-                                   out=lout, lse=llse, workspace=lws)
+        pk.lazy_attn_decode(lres.pool, ldb.q, ldb.q_pos, ldb.words, ldb.cu_pages,
+                            sm_scale=lwl.sm_scale, out=lout, lse=llse, workspace=lws)
 
     # ---------------- mixed serving step, skew sweep (extra object; built and timed one alpha
     # at a time after the main timed region, see mixed_sweep)
@@ -517,7 +605,7 @@ def bench_ours(args):
     clk = ClockSampler(local).__enter__()
     torch.cuda.synchronize()
     for _ in range(args.warmup):
-        flush(); step(); e2e_step(); no_reuse_call(); context_order_call(); per_request_call()
+        flush(); step(); e2e_step(); no_reuse_call(); context_order_call(); shared_call()
         if not only_decode:
             prefill_call(); long_call()
     torch.cuda.synchronize()
@@ -536,7 +624,8 @@ def bench_ours(args):
     e2e_ms = _timed_steps(e2e_step, args.steps, flush, stream)
     nr_ms = _timed_steps(no_reuse_call, args.steps, flush, stream)
     co_ms = _timed_steps(context_order_call, args.steps, flush, stream)
-    pr_ms = _timed_steps(per_request_call, args.steps, flush, stream)
+    sh_ms = _timed_steps(shared_call, args.steps, flush, stream)
+    wo_ms = _timed_steps(decode_call, args.steps, flush_write_only, stream)
     if not only_decode:
         pre_ms = _timed_steps(prefill_call, max(3, args.steps // 2), flush, stream)
         long_ms = _timed_steps(long_call, max(3, args.steps // 2), flush, stream)
@@ -547,20 +636,31 @@ def bench_ours(args):
     ms_per_step = total_ms / args.steps
     value = _job_rate(kv_bytes * args.steps, total_ms, ws) / 1e9
     dec_avg = sum(dec_ms) / len(dec_ms)
-    achieved = kv_bytes / (dec_avg * 1e-3) / 1e9
     e2e_avg = sum(e2e_ms) / len(e2e_ms)
+    nr_avg = sum(nr_ms) / len(nr_ms)
 
-    traffic = None
-    prof = os.path.join(ROOT, "profiles", TRAFFIC_FILE)
-    if os.path.exists(prof):
-        try:
-            with open(prof) as f:
-                t = json.load(f)
-            if t.get("kernel_hash") == _kernel_hash():
-                traffic = t.get("bytes_per_launch")
-        except Exception:
-            traffic = None
+    def rate(nbytes, ms):
+        return nbytes / (ms * 1e-3) / 1e9
 
+    med = lambda t: sorted(t)[len(t) // 2]  # noqa: E731
+    tr = _traffic("decode_b64")
+    traffic = tr["bytes_per_launch"] if tr else None
+    achieved = rate(uniq_bytes, dec_avg)
+    roofline = {
+        "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+        "frac": round(achieved / hbm_peak, 4), "traffic": traffic, "peak_kind": peak_kind,
+        "kernel": "lazy_attn_decode (decode_mma_kernel + combine_kernel), mean call time",
+        "algorithmic_bytes": uniq_bytes,
+        "algorithmic": "unique K+V of the step: every distinct cached page once (4096 B per "
+                       "valid key per kv-head set), the least any schedule must read",
+        "logical_bytes": kv_bytes,
+        "logical_frac": round(rate(kv_bytes, dec_avg) / hbm_peak, 4),
+        "dram_frac": round(rate(traffic, dec_avg) / hbm_peak, 4) if traffic else None,
+        "no_reuse_control": {"achieved": round(rate(n_bytes, nr_avg), 1),
+                             "frac": round(rate(n_bytes, nr_avg) / hbm_peak, 4),
+                             "bytes": n_bytes,
+                             "note": "every request its own documents: logical = unique = "
+                                     "DRAM bytes"}}
     line = {
         "metric": "decode KV GB/s (LazyAttention decode step, deferred RoPE, paged pool)",
         "value": round(value, 2),
@@ -577,36 +677,38 @@ def bench_ours(args):
         "config": {"workload": "decode_b64: 64 req x (8 Zipf(1.0) docs x 512 + 65 private) keys, "
                                "Hq32/Hkv8/D128, base 5e5, page 16",
                    "keys_per_step": db.n_keys, "kv_bytes_per_step": kv_bytes,
-                   "l2": "flushed (512 MB write) before every timed step",
-                   "decode_path": "lazy_attn_decode_shared over the aligned page tables' plan",
-                   "plan_units": plan.n_units, "plan_entries": plan_h.n_entries,
-                   "plan_host_ms": round(plan_host_ms, 3),
+                   "unique_kv_bytes_per_step": uniq_bytes,
+                   "l2": "flushed before every timed step: 512 MB write, then 512 MB read",
+                   "decode_path": "lazy_attn_decode over the aligned page tables",
                    "parallelism": f"replicas x{ws}"},
         "gpu_launches": launches_per_step * args.steps,
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
-                     "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
-                     "traffic": traffic, "peak_kind": peak_kind,
-                     "kernel": "lazy_attn_decode_shared (decode_shared_kernel + "
-                               "combine_shared_kernel)"},
-        "e2e": {"value": round(ws * kv_bytes / (e2e_avg * 1e-3) / 1e9, 2), "unit": "GB/s",
+        "roofline": roofline,
+        "e2e": {"value": round(ws * rate(kv_bytes, e2e_avg), 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_avg, 5)},
         "decode_no_reuse": {
             "workload": "decode_b64_no_reuse: same shapes, every request its own 8 docs "
                         "(no page shared, logical bytes = DRAM bytes)",
-            "value": round(n_bytes / (sum(nr_ms) / len(nr_ms) * 1e-3) / 1e9, 2), "unit": "GB/s",
-            "ms_per_call": round(sum(nr_ms) / len(nr_ms), 5),
-            "frac": round(n_bytes / (sum(nr_ms) / len(nr_ms) * 1e-3) / 1e9 / hbm_peak, 4)},
-        "decode_per_request": {
-            "workload": "decode_b64, aligned order, through lazy_attn_decode (one unit per "
-                        "request and kv head, no segment pairing)",
-            "value": round(kv_bytes / (sorted(pr_ms)[len(pr_ms) // 2] * 1e-3) / 1e9, 2),
-            "unit": "GB/s", "ms_per_call": round(sorted(pr_ms)[len(pr_ms) // 2], 5)},
+            "value": round(rate(n_bytes, nr_avg), 2), "unit": "GB/s",
+            "ms_per_call": round(nr_avg, 5), "frac": round(rate(n_bytes, nr_avg) / hbm_peak, 4)},
+        "decode_shared_plan": {
+            "workload": "decode_b64, aligned order, through lazy_attn_decode_shared (identical "
+                        "document segments of two requests paired in one fragment)",
+            "value": round(rate(kv_bytes, med(sh_ms)), 2), "unit": "GB/s",
+            "ms_per_call": round(med(sh_ms), 5), "plan_units": plan.n_units,
+            "plan_entries": plan_h.n_entries, "plan_host_ms": round(plan_host_ms, 3),
+            "note": "the plan is rebuilt on the host from the page tables (plan_host_ms, not "
+                    "in ms_per_call)"},
         "decode_context_order": {
             "workload": "decode_b64 through lazy_attn_decode with each request's pages in "
                         "context order (documents not lined up across requests)",
-            "value": round(kv_bytes / (sorted(co_ms)[len(co_ms) // 2] * 1e-3) / 1e9, 2),
-            "unit": "GB/s", "ms_per_call": round(sorted(co_ms)[len(co_ms) // 2], 5)},
+            "value": round(rate(kv_bytes, med(co_ms)), 2),
+            "unit": "GB/s", "ms_per_call": round(med(co_ms), 5)},
+        "decode_write_only_flush": {
+            "workload": "the headline decode call after a write-only L2 flush (512 MB of dirty "
+                        "lines left in the cache, written back inside the timed call)",
+            "value": round(rate(kv_bytes, med(wo_ms)), 2), "unit": "GB/s",
+            "ms_per_call": round(med(wo_ms), 5)},
         "decode_tokens_per_s": round(ws * B / (ms_per_step * 1e-3), 1),
         "step_ms_dist": _dist_ms(step_ms),
         "decode_call_ms_dist": _dist_ms(dec_ms),
@@ -624,16 +726,22 @@ def bench_ours(args):
             "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": tc_peak,
                          "unit": "TFLOP/s", "frac": round(tflops / tc_peak, 4),
                          "peak_kind": peak_kind}}
+        ltr = _traffic("long_decode_b16")
         line["long_decode"] = {
             "workload": "long_decode_b16: 16 req x 131073 keys (64 Zipf(1.2) docs x 2048 + 1), "
-                        "shared-segment plan of the aligned tables",
-            "value": round(l_bytes / (long_avg * 1e-3) / 1e9, 2), "unit": "GB/s",
+                        "aligned page tables, lazy_attn_decode",
+            "value": round(rate(l_bytes, long_avg), 2), "unit": "GB/s",
             "tokens_per_s": round(lwl.batch / (long_avg * 1e-3), 1),
             "ms_per_step": round(long_avg, 4), "ms_dist": _dist_ms(long_ms),
-            "frac": round(l_bytes / (long_avg * 1e-3) / 1e9 / hbm_peak, 4)}
+            "logical_bytes": l_bytes, "unique_bytes": l_uniq,
+            "frac": round(rate(l_uniq, long_avg) / hbm_peak, 4),
+            "logical_frac": round(rate(l_bytes, long_avg) / hbm_peak, 4),
+            "traffic": ltr["bytes_per_launch"] if ltr else None,
+            "dram_frac": round(rate(ltr["bytes_per_launch"], long_avg) / hbm_peak, 4)
+            if ltr else None}
     if not only_decode:
         # free the other workloads' pools before the chain's and the 17 GB mixed pools
-        del pres, pb, pout, plse, lres, ldb, lplan, lws, lout, llse
+        del pres, pb, pout, plse, lres, ldb, lws, lout, llse
         torch.cuda.empty_cache()
         line["chain"] = chain_bench(args, flush, stream)
         torch.cuda.empty_cache()
@@ -986,54 +1094,73 @@ def alibi_bench(args, flush, stream, hbm_peak, tc_peak):
     return out
 
 
-# what the decode kernel and its work list are built from
-TRAFFIC_SOURCES = ("decode.cu", "lazy_common.cuh", "shared_plan.cpp")
-TRAFFIC_WORKLOAD = ("decode_b64 (64 req x 4161 keys, Hq32/Hkv8/D128 bf16), shared-segment plan of "
-                    "the aligned page tables")
-TRAFFIC_FILE = "decode_shared_kernel_traffic.json"
-TRAFFIC_KERNEL = "decode_shared_kernel"
-TRAFFIC_COMMAND = ("ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum,"
-                   "lts__t_sector_hit_rate.pct --clock-control none -k regex:decode_shared -s 4 -c 1 "
-                   "--csv --log-file gpurun_out/decode_traffic.csv python bench.py --only decode "
-                   "--steps 3 --warmup 3 --no-cpu-baseline")
+# DRAM traffic of the decode kernel, one captured launch per workload (ncu, --clock-control
+# none), kept in profiles/TRAFFIC_FILE and reported only while the kernel's sources still hash to
+# the recorded value. Capture: run the workload's command below with the CSV path in place of
+# {csv}, then `python bench.py --record-traffic NAME CSV`.
+TRAFFIC_FILE = "decode_traffic.json"
+TRAFFIC_SOURCES = ("decode.cu", "lazy_common.cuh")
+TRAFFIC_RUNS = {
+    "decode_b64": {
+        "workload": "decode_b64 (64 req x 4161 keys, Hq32/Hkv8/D128 bf16), aligned page tables, "
+                    "lazy_attn_decode",
+        "kernel": "decode_mma_kernel",
+        "command": "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,"
+                   "gpu__time_duration.sum --clock-control none -k regex:decode_mma_kernel -s 4 "
+                   "-c 1 --csv --log-file {csv} python bench.py --only decode --steps 3 "
+                   "--warmup 3 --no-cpu-baseline"},
+    "long_decode_b16": {
+        "workload": "long_decode_b16 (16 req x 131073 keys, Hq32/Hkv8/D128 bf16), aligned page "
+                    "tables, lazy_attn_decode",
+        "kernel": "decode_mma_kernel",
+        "command": "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,"
+                   "gpu__time_duration.sum --clock-control none -k regex:decode_mma_kernel -s 4 "
+                   "-c 1 --csv --log-file {csv} python bench.py --only long_decode --steps 3 "
+                   "--warmup 3"},
+}
 
 
-def _kernel_hash():
-    """Hash of the decode kernel's sources and of the workload tag: the recorded DRAM traffic is
-    reported only while it matches."""
+def _kernel_hash(name):
+    """Hash of the decode kernel's sources and of the workload's description."""
     import hashlib
-    h = hashlib.sha256(TRAFFIC_WORKLOAD.encode())
-    for name in TRAFFIC_SOURCES:
-        with open(os.path.join(ROOT, "position_independent_kv_lazy_gb300", "csrc", name), "rb") as f:
+    h = hashlib.sha256(TRAFFIC_RUNS[name]["workload"].encode())
+    for src in TRAFFIC_SOURCES:
+        with open(os.path.join(ROOT, "position_independent_kv_lazy_gb300", "csrc", src), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def record_traffic(csv_path):
-    """Write profiles/TRAFFIC_FILE from the CSV of TRAFFIC_COMMAND (one
-    captured launch of the bench's decode kernel), stamped with the current source hash."""
+def record_traffic(name, csv_path):
+    """Add the record of workload `name` to profiles/TRAFFIC_FILE from the CSV its command wrote
+    (one captured launch), stamped with the current source hash."""
     import csv
+    run = TRAFFIC_RUNS[name]
     vals, kernel = {}, None
     with open(csv_path) as f:
         rows = [r for r in csv.reader(l for l in f if l.startswith('"'))]
     hdr = rows[0]
     ki, mi, vi = hdr.index("Kernel Name"), hdr.index("Metric Name"), hdr.index("Metric Value")
     for r in rows[1:]:
-        if TRAFFIC_KERNEL not in r[ki]:
+        if run["kernel"] not in r[ki]:
             continue
         kernel = r[ki]
         vals[r[mi]] = float(r[vi].replace(",", ""))
     rd, wr = int(vals["dram__bytes_read.sum"]), int(vals["dram__bytes_write.sum"])
-    out = {"kernel": kernel, "kernel_hash": _kernel_hash(),
-           "workload": TRAFFIC_WORKLOAD,
+    rec = {"kernel": kernel, "kernel_hash": _kernel_hash(name), "workload": run["workload"],
            "bytes_per_launch": rd + wr, "dram_bytes_read": rd, "dram_bytes_write": wr,
            "gpu_time_ns_under_ncu": int(vals.get("gpu__time_duration.sum", 0)),
-           "lts_sector_hit_rate_pct": vals.get("lts__t_sector_hit_rate.pct"),
-           "command": TRAFFIC_COMMAND}
-    with open(os.path.join(ROOT, "profiles", TRAFFIC_FILE), "w") as f:
-        json.dump(out, f, indent=1)
+           "command": run["command"]}
+    path = os.path.join(ROOT, "profiles", TRAFFIC_FILE)
+    try:
+        with open(path) as f:
+            allrec = json.load(f)
+    except (OSError, ValueError):
+        allrec = {}
+    allrec[name] = rec
+    with open(path, "w") as f:
+        json.dump(allrec, f, indent=1, sort_keys=True)
         f.write("\n")
-    print(json.dumps(out))
+    print(json.dumps(rec))
 
 
 def cpu_baseline(wl, src, kv_bytes_total, budget_s):
@@ -1115,15 +1242,16 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["all", "decode", "prefill"], default="all",
-                    help="decode / prefill: time only that workload (smaller footprint, for "
-                         "profiling)")
-    ap.add_argument("--record-traffic", metavar="CSV",
-                    help="write the decode traffic profile (profiles/TRAFFIC_FILE) from the "
-                         "ncu CSV of the traffic capture and exit (no GPU needed)")
+    ap.add_argument("--only", choices=["all", "decode", "prefill", "long_decode"],
+                    default="all",
+                    help="decode / prefill / long_decode: time only that workload (smaller "
+                         "footprint, for profiling)")
+    ap.add_argument("--record-traffic", nargs=2, metavar=("NAME", "CSV"),
+                    help="add workload NAME's decode traffic record (profiles/TRAFFIC_FILE) from "
+                         "the ncu CSV of its capture and exit (no GPU needed)")
     args = ap.parse_args()
     if args.record_traffic:
-        record_traffic(args.record_traffic)
+        record_traffic(*args.record_traffic)
         return
     if args.warmup < 3:
         args.warmup = 3
@@ -1131,6 +1259,8 @@ def main():
         bench_reference(args)
     elif args.only == "prefill":
         bench_prefill_only(args)
+    elif args.only == "long_decode":
+        bench_long_decode_only(args)
     else:
         bench_ours(args)
 

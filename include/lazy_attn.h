@@ -205,6 +205,19 @@ int lazy_unpack_page(uint64_t word, uint32_t *block_id, uint32_t *offset, uint32
  * LAZY_ERR_INVALID_ARG (words before it are written). */
 int lazy_pack_pages(int32_t n, const uint32_t *block_ids, const uint32_t *offsets,
                     const uint32_t *n_valid, uint64_t *words);
+/*
+ * The page words of one segment: `length` tokens held in blocks block_ids[0 .. n_pages-1],
+ * n_pages = ceil(length / page_size), attended at logical offset `offset`. Word i is
+ * (block_ids[i], position, min(page_size, length - i * page_size)) with position = offset for
+ * RoPE pools (page_positions = 0: every page of a segment carries the segment's offset) or
+ * offset + i * page_size for ALiBi pools (page_positions = 1: each page carries its first
+ * token's position). Host arrays; words has room for max_words; *n_words receives n_pages.
+ * LAZY_ERR_INVALID_ARG if n_blocks or max_words < n_pages, a position reaches 2^26, or
+ * page_size is outside 1..64 (words before the failing page are written).
+ */
+int lazy_pack_segment(const uint32_t *block_ids, int32_t n_blocks, uint32_t offset,
+                      int32_t length, int32_t page_size, int32_t page_positions,
+                      uint64_t *words, int32_t max_words, int32_t *n_words);
 
 /* ---------------------------------------------------------------------------------------
  * Decode (summaries' decoding part: M = 1, rotation fused in the inner loop, q re-rotated only

@@ -47,7 +47,8 @@ EXPORTS = [
     "lazy_pool_destroy", "lazy_pool_set_wait_limit", "kv_pool_alloc", "kv_pool_retain",
     "kv_pool_release", "kv_pool_num_free", "kv_pool_refcount", "kv_pool_insert_doc",
     "kv_pool_write_tokens", "lazy_pack_page", "lazy_unpack_page", "lazy_pack_pages",
-    "lazy_decode_workspace_bytes", "lazy_attn_decode", "lazy_prefill_workspace_bytes",
+    "lazy_pack_segment", "lazy_decode_workspace_bytes", "lazy_attn_decode",
+    "lazy_prefill_workspace_bytes",
     "lazy_attn_prefill", "lazy_get_device_error", "lazy_debug_gather", "lazy_debug_wait_timeout",
     "lazy_attn_decode_noalloc", "lazy_attn_prefill_append",
     "lazy_pool_set_schedule_sms", "lazy_decode_shared_plan", "lazy_decode_shared_workspace_bytes",
@@ -101,6 +102,8 @@ _SIGS = {
     "lazy_pack_page": ([_u32, _u32, _u32, _pu64], ctypes.c_int),
     "lazy_unpack_page": ([_u64, _pu32, _pu32, _pu32], ctypes.c_int),
     "lazy_pack_pages": ([_i32, _pu32, _pu32, _pu32, _pu64], ctypes.c_int),
+    "lazy_pack_segment": ([_pu32, _i32, ctypes.c_uint32, _i32, _i32, _i32, _pu64, _i32, _pi32],
+                          ctypes.c_int),
     "lazy_decode_workspace_bytes": ([_vp, _i32, _i32, _i32, _psz], ctypes.c_int),
     "lazy_attn_decode": ([_vp, _vp, _vp, _vp, _vp, _i32, _i32, _f32, _i32, _vp, _vp, _vp,
                           ctypes.c_size_t, _vp], ctypes.c_int),
@@ -353,18 +356,23 @@ def build_page_table(requests: Sequence[Sequence[Tuple[Sequence[int], int, int]]
     Returns (words uint64 [total pages], cu_pages int32 [B+1])."""
     if align_shared:
         requests = align_shared_segments(requests)
-    blk, off, nv, cu = [], [], [], [0]
+    lib = load_library()
+    parts, cu = [], [0]
     for segs in requests:
+        total = cu[-1]
         for ids, o, length in segs:
-            n_pages = (length + page_size - 1) // page_size
-            if len(ids) < n_pages:
-                raise ValueError("segment has fewer blocks than pages")
-            for i in range(n_pages):
-                blk.append(ids[i])
-                off.append(o + i * page_size if page_positions else o)
-                nv.append(min(page_size, length - i * page_size))
-        cu.append(len(blk))
-    return lazy_pack_pages(blk, off, nv), np.asarray(cu, dtype=np.int32)
+            b = np.ascontiguousarray(ids, dtype=np.uint32)
+            w = np.zeros(max(1, b.shape[0]), dtype=np.uint64)
+            n = ctypes.c_int32()
+            _check("lazy_pack_segment", lib.lazy_pack_segment(
+                b.ctypes.data_as(_pu32), b.shape[0], int(o), int(length), page_size,
+                1 if page_positions else 0, w.ctypes.data_as(_pu64), w.shape[0],
+                ctypes.byref(n)))
+            parts.append(w[:n.value])
+            total += n.value
+        cu.append(total)
+    words = np.concatenate(parts) if parts else np.zeros(0, dtype=np.uint64)
+    return words, np.asarray(cu, dtype=np.int32)
 
 
 # ------------------------------------------------------------------------------------------------

@@ -226,6 +226,26 @@ int lazy_pack_pages(int32_t n, const uint32_t *block_ids, const uint32_t *offset
   return LAZY_OK;
 }
 
+int lazy_pack_segment(const uint32_t *block_ids, int32_t n_blocks, uint32_t offset,
+                      int32_t length, int32_t page_size, int32_t page_positions,
+                      uint64_t *words, int32_t max_words, int32_t *n_words) {
+  if (!n_words || length < 0 || page_size < 1 || page_size > 64 ||
+      (page_positions != 0 && page_positions != 1))
+    return LAZY_ERR_INVALID_ARG;
+  const int32_t n_pages = (int32_t)(((int64_t)length + page_size - 1) / page_size);
+  if (n_pages > 0 && (!block_ids || !words)) return LAZY_ERR_INVALID_ARG;
+  if (n_blocks < n_pages || max_words < n_pages) return LAZY_ERR_INVALID_ARG;
+  for (int32_t i = 0; i < n_pages; ++i) {
+    const uint64_t pos = (uint64_t)offset + (page_positions ? (uint64_t)i * page_size : 0);
+    if (pos >= (1ull << 26)) return LAZY_ERR_INVALID_ARG;
+    const int32_t nv = length - i * page_size < page_size ? length - i * page_size : page_size;
+    int rc = lazy_pack_page(block_ids[i], (uint32_t)pos, (uint32_t)nv, &words[i]);
+    if (rc != LAZY_OK) return rc;
+  }
+  *n_words = n_pages;
+  return LAZY_OK;
+}
+
 int lazy_get_device_error(lazy_pool *p, int32_t *err, lazy_stream_t stream) {
   if (!p || !err) return LAZY_ERR_INVALID_ARG;
   int rc = lazy::ensure_device(p);

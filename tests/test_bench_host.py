@@ -29,3 +29,19 @@ def test_clock_summary_reads_reason_columns():
     r = s.summary([(t0 - 0.01, t0 + 0.01)])
     assert r["reasons"] == ["sw_power_cap"]    # the hw_slowdown sample lies outside the window
     assert bench.ClockSampler(0).summary()["sm_mhz"] is None
+
+
+def test_unique_kv_bytes_counts_each_page_once():
+    # words: (block 5, 16 valid) twice, (block 7, 3 valid), (block 9, 16 valid); bit layout
+    # block | offset << 32 | (n_valid - 1) << 58
+    import numpy as np
+    w = np.array([5 | (100 << 32) | (15 << 58), 5 | (900 << 32) | (15 << 58),
+                  7 | (2 << 58), 9 | (15 << 58)], dtype=np.uint64)
+    assert bench._unique_kv_bytes(w, 4096) == (16 + 3 + 16) * 4096
+    assert bench._unique_kv_bytes(np.zeros(0, dtype=np.uint64), 4096) == 0
+
+
+def test_traffic_commands_name_no_scratch_path():
+    for name, run in bench.TRAFFIC_RUNS.items():
+        assert "{csv}" in run["command"] and "gpurun" not in run["command"], name
+        assert len(bench._kernel_hash(name)) == 16

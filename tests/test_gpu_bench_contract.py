@@ -35,6 +35,10 @@ def test_bench_decode_line_has_the_contract_keys():
         assert k in rf, k
     assert rf["bound"] == "hbm" and rf["unit"] == "GB/s"
     assert abs(rf["frac"] - rf["achieved"] / rf["peak"]) < 1e-3
+    # achieved counts each distinct page once, so it cannot exceed what HBM delivers by much
+    assert 0 < rf["frac"] <= 1.2
+    assert rf["algorithmic_bytes"] <= rf["logical_bytes"]
+    assert 0 < rf["no_reuse_control"]["frac"] <= 1.2
     e = d["e2e"]
     assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
     assert e["unit"] == d["unit"]

@@ -185,3 +185,39 @@ def test_page_table_page_positions():
     assert [f[1] for f in fields] == [100, 116, 132, 5]
     assert [f[2] for f in fields] == [16, 16, 8, 1]
     assert list(cu) == [0, 3, 4]
+
+
+def test_pack_segment_matches_the_page_word_spec():
+    # one segment's words from the C helper against the oracle's independent page-word spec
+    import oracle
+    ids = [11, 12, 13, 2 ** 32 - 1]
+    for page_positions in (0, 1):
+        w, cu = pk.build_page_table([[(ids, 1000, 61)]], 16, page_positions=bool(page_positions))
+        want = [oracle.pack_page(b, 1000 + (16 * i if page_positions else 0),
+                                 min(16, 61 - 16 * i)) for i, b in enumerate(ids)]
+        assert [int(x) for x in w] == want and list(cu) == [0, 4]
+    # an empty segment, and a request without segments
+    w, cu = pk.build_page_table([[([], 0, 0)], []], 16)
+    assert len(w) == 0 and list(cu) == [0, 0, 0]
+
+
+def test_pack_segment_rejects_bad_arguments(lazylib):
+    b = (ctypes.c_uint32 * 4)(1, 2, 3, 4)
+    w = (ctypes.c_uint64 * 4)()
+    n = ctypes.c_int32()
+    ok = lazylib.lazy_pack_segment(b, 4, 0, 64, 16, 0, w, 4, ctypes.byref(n))
+    assert ok == 0 and n.value == 4
+    # fewer blocks or word slots than pages
+    assert lazylib.lazy_pack_segment(b, 3, 0, 64, 16, 0, w, 4, ctypes.byref(n)) == \
+        pk.LAZY_ERR_INVALID_ARG
+    assert lazylib.lazy_pack_segment(b, 4, 0, 64, 16, 0, w, 3, ctypes.byref(n)) == \
+        pk.LAZY_ERR_INVALID_ARG
+    # a page position at 2^26 (ALiBi words) or a segment offset past the field
+    assert lazylib.lazy_pack_segment(b, 4, (1 << 26) - 40, 64, 16, 1, w, 4, ctypes.byref(n)) == \
+        pk.LAZY_ERR_INVALID_ARG
+    assert lazylib.lazy_pack_segment(b, 4, (1 << 26) - 40, 64, 16, 0, w, 4, ctypes.byref(n)) == 0
+    assert lazylib.lazy_pack_segment(b, 4, 1 << 26, 64, 16, 0, w, 4, ctypes.byref(n)) == \
+        pk.LAZY_ERR_INVALID_ARG
+    # page sizes outside 1..64
+    assert lazylib.lazy_pack_segment(b, 4, 0, 64, 65, 0, w, 4, ctypes.byref(n)) == \
+        pk.LAZY_ERR_INVALID_ARG
