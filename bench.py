@@ -756,6 +756,8 @@ def bench_ours(args):
         line["shared_decode"] = shared_decode_bench(args, flush, stream)
         torch.cuda.empty_cache()
         line["prefill_rotation_side"] = rotation_side_bench(args, flush, stream)
+        torch.cuda.empty_cache()
+        line["materialised"] = materialised_bench(args, flush, stream, hbm_peak, tc_peak)
     clk.__exit__()
     line["clocks"] = clk.summary(TIMED_WINDOWS)
     if rank == 0 and not args.no_cpu_baseline:
@@ -858,6 +860,133 @@ def mixed_sweep(args, flush, stream, hbm_peak):
             "materialised_over_resident": round(acct["materialised"] / acct["resident"], 3)}
         del res, pb, db, ws, dout, dlse, pout, plse, src
         torch.cuda.empty_cache()
+    return out
+
+
+def materialised_bench(args, flush, stream, hbm_peak, tc_peak):
+    """The copy-per-offset baseline (a document re-encoded for each offset it is used at, by
+    kv_pool_materialise) against the lazy path on identical inputs: the copies' cost (bytes
+    resident, time to write them), decode and prefill over the copies, and the rotation
+    overhead of the lazy path (the same kernels, keys stored once vs keys at absolute
+    positions needing no per-document rotation)."""
+    import numpy as np
+    import torch
+
+    import position_independent_kv_lazy_gb300 as pk
+    import workload as W
+    from position_independent_kv_lazy_gb300 import harness as H
+
+    def med_ms(fn, n):
+        for _ in range(args.warmup):
+            flush(); fn()
+        return sorted(_timed_steps(fn, n, flush, stream))[n // 2]
+
+    n_t = max(5, args.steps // 2)
+    out = {"note": "copies: one per distinct (document, offset) pair, written by "
+                   "kv_pool_materialise (un-rotate by R(-j), re-rotate by R(o + j)); decode over "
+                   "copies uses page words of offset 0, prefill over copies "
+                   "LAZY_PREFILL_ABSOLUTE_KEYS (reference position 0, bf16 Q.K, no rotation "
+                   "pass for offset-0 pages)"}
+    # ---- decode: decode_b64 (shared documents) and its no-reuse control
+    for name, wl in (("decode_b64", W.decode_workload()),
+                     ("decode_b64_no_reuse", W.decode_workload(no_reuse=True,
+                                                               name="decode_b64_no_reuse"))):
+        src = H.DeviceSource(wl)
+        res = H.build_resident(wl, src, resident_pool=False,
+                               extra_blocks=H.materialised_blocks_needed(wl))
+        db = H.decode_batch(wl, res, src, align_shared=True)
+        torch.cuda.synchronize()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        ev[0].record(stream)
+        copies = H.materialise_copies(wl, res)
+        ev[1].record(stream)
+        torch.cuda.synchronize()
+        copy_ms = ev[0].elapsed_time(ev[1])
+        words, cu = H.copy_page_table(wl, res, copies, db.reqs, with_private=True)
+        cw = torch.from_numpy(words.view(np.int64)).cuda()
+        ccu = torch.from_numpy(cu).cuda()
+        B = wl.batch
+        o = torch.empty_like(db.q)
+        l = torch.empty((B, wl.Hq), dtype=torch.float32, device="cuda")
+        wsd = torch.empty(pk.lazy_decode_workspace_bytes(res.pool, B, wl.Hq), dtype=torch.uint8,
+                          device="cuda")
+        kvb = db.n_keys * wl.kv_bytes_per_token()
+        per_doc = wl.doc_len * wl.kv_bytes_per_token()
+
+        def lazy_call():
+            pk.lazy_attn_decode(res.pool, db.q, db.q_pos, db.words, db.cu_pages,
+                                sm_scale=wl.sm_scale, out=o, lse=l, workspace=wsd)
+
+        def copy_call():
+            pk.lazy_attn_decode(res.pool, db.q, db.q_pos, cw, ccu, sm_scale=wl.sm_scale,
+                                out=o, lse=l, workspace=wsd)
+
+        t_lazy, t_copy = med_ms(lazy_call, n_t), med_ms(copy_call, n_t)
+        if pk.lazy_get_device_error(res.pool) != 0:
+            raise RuntimeError("device error in the materialised decode bench")
+        out[name] = {
+            "distinct_doc_offset_pairs": len(copies), "unique_docs": len(wl.used_docs()),
+            "kv_bytes_documents_lazy": len(wl.used_docs()) * per_doc,
+            "kv_bytes_documents_copies": len(copies) * per_doc,
+            "copy_ms": round(copy_ms, 4), "copy_launches": len(copies),
+            "copy_gbs": round(2 * len(copies) * per_doc / (copy_ms * 1e-3) / 1e9, 1),
+            "lazy": {"ms_per_call": round(t_lazy, 5),
+                     "value": round(kvb / (t_lazy * 1e-3) / 1e9, 2), "unit": "GB/s"},
+            "copies": {"ms_per_call": round(t_copy, 5),
+                       "value": round(kvb / (t_copy * 1e-3) / 1e9, 2), "unit": "GB/s"},
+            "lazy_over_copies": round(t_lazy / t_copy, 4)}
+        del res, db, copies, cw, ccu, src
+        torch.cuda.empty_cache()
+    out["decode_b64_no_reuse"]["rotation_overhead"] = round(
+        out["decode_b64_no_reuse"]["lazy_over_copies"] - 1.0, 4)
+    # ---- prefill: prefill_b8
+    wl = W.prefill_workload()
+    src = H.DeviceSource(wl)
+    res = H.build_resident(wl, src, resident_pool=False,
+                           extra_blocks=H.materialised_blocks_needed(wl))
+    pb = H.prefill_batch(wl, res, src)
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    ev[0].record(stream)
+    copies = H.materialise_copies(wl, res)
+    ev[1].record(stream)
+    torch.cuda.synchronize()
+    copy_ms = ev[0].elapsed_time(ev[1])
+    words, cu = H.copy_page_table(wl, res, copies, pb.reqs, with_private=False)
+    cw = torch.from_numpy(words.view(np.int64)).cuda()
+    ccu = torch.from_numpy(cu).cuda()
+    po = torch.empty_like(pb.q)
+    pl = torch.empty((pb.total_q, wl.Hq), dtype=torch.float32, device="cuda")
+    pws = _prefill_workspace(pk, res.pool, pb, wl.Hq)
+    per_doc = wl.doc_len * wl.kv_bytes_per_token()
+
+    def prefill(words_, cu_, flags):
+        def f():
+            pk.lazy_attn_prefill(res.pool, pb.q, pb.k_new, pb.v_new, pb.cu_q, pb.q_pos0, words_,
+                                 cu_, pb.max_q_len, sm_scale=wl.sm_scale, out=po, lse=pl,
+                                 workspace=pws, flags=flags)
+        return f
+
+    t_lazy = med_ms(prefill(pb.words, pb.cu_pages, pk.LAZY_PREFILL_AUTO), n_t)
+    t_abs = med_ms(prefill(cw, ccu, pk.LAZY_PREFILL_AUTO | pk.LAZY_PREFILL_ABSOLUTE_KEYS), n_t)
+    t_rel = med_ms(prefill(cw, ccu, pk.LAZY_PREFILL_AUTO), n_t)
+    if pk.lazy_get_device_error(res.pool) != 0:
+        raise RuntimeError("device error in the materialised prefill bench")
+    tf = lambda t: round(pb.flops / (t * 1e-3) / 1e12, 2)  # noqa: E731
+    out["prefill_b8"] = {
+        "distinct_doc_offset_pairs": len(copies), "unique_docs": len(wl.used_docs()),
+        "kv_bytes_documents_lazy": len(wl.used_docs()) * per_doc,
+        "kv_bytes_documents_copies": len(copies) * per_doc,
+        "copy_ms": round(copy_ms, 4),
+        "copy_gbs": round(2 * len(copies) * per_doc / (copy_ms * 1e-3) / 1e9, 1),
+        "lazy": {"ms_per_call": round(t_lazy, 5), "tflops": tf(t_lazy)},
+        "copies_absolute_keys": {"ms_per_call": round(t_abs, 5), "tflops": tf(t_abs)},
+        "copies_relative_kernel": {"ms_per_call": round(t_rel, 5), "tflops": tf(t_rel),
+                                   "note": "the lazy kernel over the copies at offset 0"},
+        "rotation_overhead": round(t_lazy / t_abs - 1.0, 4),
+        "rotation_overhead_analytic_flops": round(3.0 / (4 * 128), 4)}
+    del res, pb, copies, cw, ccu, src
+    torch.cuda.empty_cache()
     return out
 
 

@@ -73,10 +73,18 @@ enum {
                                larger ones). P.V and the ALiBi mode's Q.K use bf16 operands. */
     LAZY_PREFILL_SIMT = 1,  /* CUDA-core kernel, fp32 arithmetic, group size <= 64 */
     LAZY_PREFILL_TC = 2,    /* tcgen05/TMEM kernel; LAZY_ERR_UNSUPPORTED if the shape is not */
-    LAZY_PREFILL_SIMT_QSIDE = 3  /* the CUDA-core kernel with the query-side variant of the
+    LAZY_PREFILL_SIMT_QSIDE = 3, /* the CUDA-core kernel with the query-side variant of the
                                     relative rotation: cached key pages are used as stored
                                     (R(j) k) and the queries take R(m - o) once per document
                                     offset o, instead of every key page taking R(o - m0) */
+    /* Added to one of the above: the cached pages hold keys at absolute positions (copies
+       written by kv_pool_materialise) and are listed with offset 0. The attention is the same;
+       the tensor-core kernel then takes position 0 as its reference (queries rotated by R(m),
+       question keys by R(p)), uses offset-0 pages as stored with no rotation pass, and
+       multiplies Q.K in bf16 like a kernel over materialised keys (the rotated query row is
+       rounded to bf16; on contexts of a few hundred keys that moves lse by up to ~2e-3). The
+       CUDA-core kernels ignore it. */
+    LAZY_PREFILL_ABSOLUTE_KEYS = 16
 };
 
 /* ---------------------------------------------------------------------------------------
@@ -195,6 +203,26 @@ int kv_pool_write_tokens(lazy_pool *pool, const void *d_k_raw, const void *d_v, 
                          const int32_t *d_slot_mapping, const int32_t *d_local_pos,
                          lazy_stream_t stream);
 
+/*
+ * Materialised copy: the position-aware alternative the summaries compare the method against
+ * ("Problem statement": a cached document re-encoded for each position it is used at; the
+ * prefill part describes that re-encoding as two rotations, one back to position 0 and one to
+ * the target). For the n_tokens tokens of a cached segment held in src_block_ids (K rows
+ * R(j) k at local positions j), writes to dst_block_ids:
+ *     K row = R(offset + j) R(-j) (cached K row)   (fp32 arithmetic, one rounding to the pool
+ *                                                    type)
+ *     V row = cached V row
+ * src_block_ids, dst_block_ids: host int32 [ceil(n_tokens / page_size)], blocks the caller
+ * owns (kv_pool_alloc); no destination block may be one of the source blocks. The copy's keys
+ * sit at absolute positions: attend its pages with page words of offset 0 (decode), and, for
+ * the tensor-core prefill, with LAZY_PREFILL_ABSOLUTE_KEYS. RoPE pools only
+ * (LAZY_ERR_UNSUPPORTED on ALiBi pools, whose keys carry no rotation); offset + n_tokens must
+ * stay below 2^26. Exists to measure the method against the copy-per-offset baseline.
+ */
+int kv_pool_materialise(lazy_pool *pool, const int32_t *src_block_ids,
+                        const int32_t *dst_block_ids, int32_t n_tokens, int32_t offset,
+                        lazy_stream_t stream);
+
 /* ---------------------------------------------------------------------------------------
  * Page words ("(block ID, offset) bit-packed in a single register", summaries' decoding part)
  * --------------------------------------------------------------------------------------- */
@@ -268,11 +296,14 @@ int lazy_attn_decode(lazy_pool *pool, const void *d_q, const int32_t *d_q_pos,
  *     earlier kv_pool_insert_doc, kv_pool_write_tokens or lazy_attn_decode call does it);
  *     otherwise LAZY_ERR_INVALID_ARG.
  *   - The first call on each device looks up the array's device address (a driver query, not
- *     an allocation); make that first call before any stream capture.
+ *     an allocation) and keeps it for the life of the process; make that first call before
+ *     any stream capture. Do not use the library across a cudaDeviceReset (the array may then
+ *     sit at another address).
  *   - If (batch * num_kv_heads * chunks + 4 * CTAs) * group * (head_dim + 1) * 4 bytes exceeds
  *     the array (chunks = ceil(group / 8), group = num_q_heads / num_kv_heads, CTAs = the grid,
  *     by default SMs x resident CTAs), the call returns LAZY_ERR_SCRATCH_LIMIT and launches
- *     nothing. With 32/8/128 heads on a 152-SM GPU that allows up to ~355 requests.
+ *     nothing. With 32/8/128 heads on a 152-SM GPU running 3 decode CTAs per SM (456 CTAs,
+ *     the tensor-core decode's occupancy) that allows up to 280 requests.
  *   - All calls share the one array, and it keeps whatever the last call left there. Each call
  *     writes every scratch entry before reading it, so nothing has to start at zero. Calls
  *     whose kernels overlap on the GPU (other streams, other threads) race on the array:

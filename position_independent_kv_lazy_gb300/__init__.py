@@ -40,13 +40,15 @@ LAZY_PREFILL_AUTO = 0
 LAZY_PREFILL_SIMT = 1
 LAZY_PREFILL_TC = 2
 LAZY_PREFILL_SIMT_QSIDE = 3
+LAZY_PREFILL_ABSOLUTE_KEYS = 16
 
 # Every symbol declared in include/lazy_attn.h (checked by the tests).
 EXPORTS = [
     "lazy_version", "lazy_status_string", "lazy_last_error", "lazy_pool_create",
     "lazy_pool_destroy", "lazy_pool_set_wait_limit", "kv_pool_alloc", "kv_pool_retain",
     "kv_pool_release", "kv_pool_num_free", "kv_pool_refcount", "kv_pool_insert_doc",
-    "kv_pool_write_tokens", "lazy_pack_page", "lazy_unpack_page", "lazy_pack_pages",
+    "kv_pool_write_tokens", "kv_pool_materialise", "lazy_pack_page", "lazy_unpack_page",
+    "lazy_pack_pages",
     "lazy_pack_segment", "lazy_decode_workspace_bytes", "lazy_attn_decode",
     "lazy_prefill_workspace_bytes",
     "lazy_attn_prefill", "lazy_get_device_error", "lazy_debug_gather", "lazy_debug_wait_timeout",
@@ -99,6 +101,7 @@ _SIGS = {
     "kv_pool_refcount": ([_vp, _i32, _pi32], ctypes.c_int),
     "kv_pool_insert_doc": ([_vp, _vp, _vp, _i32, _i32, _pi32, _pi32, _i32, _vp], ctypes.c_int),
     "kv_pool_write_tokens": ([_vp, _vp, _vp, _i32, _vp, _vp, _vp], ctypes.c_int),
+    "kv_pool_materialise": ([_vp, _pi32, _pi32, _i32, _i32, _vp], ctypes.c_int),
     "lazy_pack_page": ([_u32, _u32, _u32, _pu64], ctypes.c_int),
     "lazy_unpack_page": ([_u64, _pu32, _pu32, _pu32], ctypes.c_int),
     "lazy_pack_pages": ([_i32, _pu32, _pu32, _pu32, _pu64], ctypes.c_int),
@@ -275,6 +278,21 @@ def kv_pool_write_tokens(pool: LazyPool, k_raw, v, slot_mapping, local_pos, stre
     _check("kv_pool_write_tokens", load_library().kv_pool_write_tokens(
         pool.handle, _ptr(k_raw), _ptr(v), int(k_raw.shape[0]), _ptr(slot_mapping),
         _ptr(local_pos), _stream(stream)))
+
+
+def kv_pool_materialise(pool: LazyPool, src_block_ids: Sequence[int], n_tokens: int,
+                        offset: int, dst_block_ids: Optional[Sequence[int]] = None,
+                        stream=None) -> List[int]:
+    """Re-encode a cached segment (n_tokens tokens in src_block_ids) for logical offset
+    `offset` into blocks of its own (allocated here unless dst_block_ids is given): keys at
+    absolute positions, the copy-per-offset baseline. Returns the copy's block ids."""
+    n_pages = (n_tokens + pool.page_size - 1) // pool.page_size
+    dst = list(dst_block_ids) if dst_block_ids is not None else kv_pool_alloc(pool, n_pages)
+    src = (ctypes.c_int32 * max(n_pages, 1))(*list(src_block_ids)[:n_pages])
+    dd = (ctypes.c_int32 * max(n_pages, 1))(*dst[:n_pages])
+    _check("kv_pool_materialise", load_library().kv_pool_materialise(
+        pool.handle, src, dd, n_tokens, offset, _stream(stream)))
+    return dst[:n_pages]
 
 
 # ------------------------------------------------------------------------------------------------

@@ -21,6 +21,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 #include <type_traits>
 
@@ -904,27 +905,32 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
   const int64_t N = (int64_t)hu * p.cu_pages[p.batch];
   const int64_t W = p.warps;
   T *out = reinterpret_cast<T *>(p.out);
-  // With at least one page per warp (N >= W) no warp's range is empty, and the per-slot test
-  // (two 64-bit divisions) is skipped.
+  // The unit's pieces. With at least one page per warp (N >= W) every warp range is non-empty
+  // and the pieces are the warps wf..wl whose ranges meet the unit. With fewer pages than warps
+  // each non-empty range holds exactly one page, so the pieces are the unit's np pages, page x
+  // (flattened index) in the range of warp ceil((x + 1) W / N) - 1: walking the pages instead of
+  // the warps skips the empty ranges without testing them.
   const bool dense = N >= W;
-  int64_t wf = 0, wl = -1;
+  int64_t wf = 0, S = 0;
+  int64_t n_pieces = 0;
   if (np > 0) {
-    const int64_t S = (int64_t)hu * wbase + (int64_t)kv * np, E = S + np;
+    S = (int64_t)hu * wbase + (int64_t)kv * np;
+    const int64_t E = S + np;
     wf = ((S + 1) * W + N - 1) / N - 1;
-    wl = (E * W + N - 1) / N - 1;
+    n_pieces = dense ? (E * W + N - 1) / N - 1 - wf + 1 : np;
   }
   for (int idx = threadIdx.x; idx < GC * (D / 4); idx += blockDim.x) {
     const int g = idx / (D / 4), d4 = idx % (D / 4);
     // one online pass over the unit's slots, eight at a time with their loads issued together
     float mx = -INFINITY, sum = 0.f;
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int64_t w0 = wf; w0 <= wl; w0 += 8) {
+    for (int64_t k0 = 0; k0 < n_pieces; k0 += 8) {
       float lv[8];
       float4 ov[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        const int64_t w = w0 + k;
-        const bool use = w <= wl && (dense || w * N / W != (w + 1) * N / W);
+        const bool use = k0 + k < n_pieces;
+        const int64_t w = dense ? wf + k0 + k : ((S + k0 + k + 1) * W + N - 1) / N - 1;
         const size_t slot = (size_t)(ub + w) * p.ch + chunk;
         lv[k] = use ? p.ws_lse[slot * GC + g] : -INFINITY;
         ov[k] = use ? *reinterpret_cast<const float4 *>(p.ws_o + (slot * GC + g) * D + d4 * 4)
@@ -1138,8 +1144,9 @@ struct SharedCombineParams {
 // shared memory, and the pass then loads eight slots at a time across unit boundaries.
 __global__ void __launch_bounds__(128) combine_shared_kernel(const SharedCombineParams p) {
   constexpr int D = 128, kChunk = 128, kBatch = 16;
-  __shared__ int64_t s_first[kChunk];  // first slot of the unit's piece range
-  __shared__ int32_t s_count[kChunk];  // slots in the range (0: skip)
+  __shared__ int64_t s_first[kChunk];  // dense: slot of the first piece; sparse: first page index
+  __shared__ int64_t s_base[kChunk];   // sparse: slot of warp 0 for the unit (unit * hkv + h)
+  __shared__ int32_t s_count[kChunk];  // pieces of the unit (0: none)
   __shared__ int32_t s_row[kChunk];
   cudaGridDependencySynchronize();
   const int32_t b = blockIdx.x / p.hkv, h = blockIdx.x % p.hkv;
@@ -1161,20 +1168,21 @@ __global__ void __launch_bounds__(128) combine_shared_kernel(const SharedCombine
       // the unit's entry range, stored with the membership (no dependent load of cu_entries)
       const int32_t ebase = p.member_entries[2 * (c0 + i)];
       const int32_t ne = p.member_entries[2 * (c0 + i) + 1];
-      int64_t wf = 0, wl = -1;
-      if (ne > 0) {
-        const int64_t S = (int64_t)p.hkv * ebase + (int64_t)h * ne, E = S + ne;
-        wf = ((S + 1) * W + N - 1) / N - 1;
-        wl = (E * W + N - 1) / N - 1;
-      }
-      s_first[i] = (int64_t)unit * p.hkv + h + wf;  // slot of the unit's piece at warp wf
-      s_count[i] = (int32_t)(wl - wf + 1);
+      // Pieces as in combine_kernel: the warps meeting the unit's entries (dense), or, with
+      // fewer entries than warps, the entries themselves, entry x in warp ceil((x+1) W / N) - 1.
+      const int64_t S = (int64_t)p.hkv * ebase + (int64_t)h * ne;
+      s_base[i] = (int64_t)unit * p.hkv + h;
       s_row[i] = (mem & 1) * 4;
-      // pieces of warps with empty ranges are not slots (sparse partitions only)
-      if (!dense && ne > 0) {
-        int32_t n_used = 0;
-        for (int64_t w = wf; w <= wl; ++w) n_used += (w * N / W != (w + 1) * N / W);
-        if (n_used != wl - wf + 1) s_count[i] = -(int32_t)(wl - wf + 1);  // check per slot
+      if (ne <= 0) {
+        s_first[i] = 0;
+        s_count[i] = 0;
+      } else if (dense) {
+        const int64_t wf = ((S + 1) * W + N - 1) / N - 1, wl = ((S + ne) * W + N - 1) / N - 1;
+        s_first[i] = s_base[i] + wf;
+        s_count[i] = (int32_t)(wl - wf + 1);
+      } else {
+        s_first[i] = S;
+        s_count[i] = ne;
       }
     }
     __syncthreads();
@@ -1185,20 +1193,17 @@ __global__ void __launch_bounds__(128) combine_shared_kernel(const SharedCombine
       float4 ov[kBatch];
 #pragma unroll
       for (int k = 0; k < kBatch; ++k) {
-        while (ci < nc && cw >= abs(s_count[ci])) {
+        while (ci < nc && cw >= s_count[ci]) {
           ++ci;
           cw = 0;
         }
-        bool use = ci < nc;
+        const bool use = ci < nc;
         size_t slot = 0;
         int row = 0;
         if (use) {
-          slot = (size_t)(s_first[ci] + cw);
+          slot = dense ? (size_t)(s_first[ci] + cw)
+                       : (size_t)(s_base[ci] + ((s_first[ci] + cw + 1) * W + N - 1) / N - 1);
           row = s_row[ci] + r;
-          if (s_count[ci] < 0) {  // sparse: skip warps whose range is empty
-            const int64_t w = (int64_t)slot - ((int64_t)(p.members[c0 + ci] >> 1) * p.hkv + h);
-            use = w * N / W != (w + 1) * N / W;
-          }
           ++cw;
         }
         lv[k] = use ? p.ws_lse[slot * 8 + row] : -INFINITY;
@@ -1274,9 +1279,12 @@ struct MmaLaunch {
   static constexpr int kSmem = MmaSmem<STAGES>::kBytes * kWarps + 1024;  // + alignment slack
   // groups of 4 chunks of 8 query heads (e.g. MQA 32/1) share one page ring per CTA
   static bool grouped(int32_t chunks) { return GC == 8 && chunks == kWarps; }
+  // Occupancy, queried once. The cache is atomic: calls from several threads may run the
+  // (idempotent) query concurrently, and each then stores the same value.
   template <typename F>
-  static int occupancy(F fn, int smem, int *cached) {
-    if (*cached < 0) {
+  static int occupancy(F fn, int smem, std::atomic<int> *cached) {
+    int c = cached->load(std::memory_order_acquire);
+    if (c < 0) {
       if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
           cudaSuccess)
         return -1;
@@ -1284,12 +1292,13 @@ struct MmaLaunch {
       if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kWarps * 32, smem) !=
           cudaSuccess)
         return -1;
-      *cached = std::max(1, n);
+      c = std::max(1, n);
+      cached->store(c, std::memory_order_release);
     }
-    return *cached;
+    return c;
   }
   static int ctas_per_sm(int32_t chunks) {
-    static int cached = -1, cached_group = -1;
+    static std::atomic<int> cached{-1}, cached_group{-1};
     if constexpr (GC == 8) {
       if (grouped(chunks))
         return occupancy(decode_mma_group_kernel<GC, kWarps, kGroupStages>, kGroupSmem,
@@ -1342,19 +1351,9 @@ struct DecodeLaunch {
     return simt_ctas_per_sm();
   }
   static int simt_ctas_per_sm() {
-    static int cached = -1;
-    if (cached < 0) {
-      auto fn = decode_split_kernel<T, D, GC, kWarps, STAGES>;
-      if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
-          cudaSuccess)
-        return -1;
-      int n = 0;
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kWarps * 32, kSmem) !=
-          cudaSuccess)
-        return -1;
-      cached = std::max(1, n);
-    }
-    return cached;
+    static std::atomic<int> cached{-1};
+    return MmaLaunch<GC, STAGES>::occupancy(decode_split_kernel<T, D, GC, kWarps, STAGES>, kSmem,
+                                            &cached);
   }
   static int run(lazy_pool *pl, const DecodeParams &dp, const CombineParams &cp, int grid,
                  cudaStream_t s) {
@@ -1422,19 +1421,9 @@ constexpr int kSharedSmem = MmaSharedSmem<kStages>::kBytes * kWarps + 1024;  // 
 
 // CTAs per SM of the shared-segment decode (occupancy query, once).
 int shared_ctas_per_sm() {
-  static int cached = -1;
-  if (cached < 0) {
-    auto fn = decode_shared_kernel<kWarps, kStages>;
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSharedSmem) !=
-        cudaSuccess)
-      return -1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kWarps * 32, kSharedSmem) !=
-        cudaSuccess)
-      return -1;
-    cached = std::max(1, n);
-  }
-  return cached;
+  static std::atomic<int> cached{-1};
+  return MmaLaunch<4, kStages>::occupancy(decode_shared_kernel<kWarps, kStages>, kSharedSmem,
+                                          &cached);
 }
 
 // The shared-segment decode serves bf16 pools with head_dim 128 and 1, 2 or 4 query heads per

@@ -5,6 +5,7 @@
 // Also: lazy_debug_gather, a test hook that reads pages through the same device unpack and
 // address arithmetic the attention kernels use.
 #include <algorithm>
+#include <vector>
 
 #include "lazy_common.cuh"
 #include "pool_internal.h"
@@ -111,6 +112,73 @@ int dispatch_encode(lazy_pool *p, const void *k_raw, const void *v, int32_t n_to
                                      local_pos, s);
   return launch_encode<float, 64>(p, k_raw, v, n_tokens, tok0, local_pos0, bl, slot_map,
                                   local_pos, s);
+}
+
+// ----------------------------------------------------------------------------------------------
+// Materialised copy (the position-aware baseline the summaries compare against, "Problem
+// statement" and the prefill part: a cached block re-encoded for one target position by two
+// rotations, one resetting it to position 0 and one to the target). Token j of a cached segment
+// (K row R(j) k) becomes K row R(offset + j) R(-j) (R(j) k) in the copy, fp32 arithmetic and one
+// rounding to the pool type; V is copied. One thread = (token, kv head, 16-byte chunk of the
+// lower half) and the matching chunk of the upper half, as in the encode.
+// ----------------------------------------------------------------------------------------------
+constexpr int kMaxMatIds = 256;
+struct MatBlocks {
+  int32_t first_page;
+  int32_t n;
+  int32_t src[kMaxMatIds];
+  int32_t dst[kMaxMatIds];
+};
+
+template <typename T, int D>
+__global__ void __launch_bounds__(256) materialise_kernel(
+    T *__restrict__ k_pool, T *__restrict__ v_pool, const uint64_t *__restrict__ turn,
+    int32_t hkv, int32_t tok_lo, int32_t n_tokens, int32_t offset, MatBlocks mb) {
+  constexpr int EPL = 16 / (int)sizeof(T);
+  constexpr int CH = (D / 2) / EPL;
+  const int64_t total = (int64_t)n_tokens * hkv * CH;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int c = (int)(idx % CH);
+    const int64_t rest = idx / CH;
+    const int h = (int)(rest % hkv);
+    const int32_t j = tok_lo + (int32_t)(rest / hkv);
+    const int pg = j / kPage - mb.first_page, slot = j % kPage;
+    const size_t src = (((size_t)mb.src[pg] * hkv + h) * kPage + slot) * D;
+    const size_t dst = (((size_t)mb.dst[pg] * hkv + h) * kPage + slot) * D;
+    float lo[EPL], hi[EPL];
+    unpack16<T>(*reinterpret_cast<const uint4 *>(k_pool + src + c * EPL), lo);
+    unpack16<T>(*reinterpret_cast<const uint4 *>(k_pool + src + D / 2 + c * EPL), hi);
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      float cs, sn;
+      rope_cos_sin(-(int64_t)j, turn[c * EPL + e], cs, sn);   // reset to position 0
+      const float x = lo[e] * cs - hi[e] * sn, y = lo[e] * sn + hi[e] * cs;
+      rope_cos_sin((int64_t)offset + j, turn[c * EPL + e], cs, sn);  // to the target position
+      lo[e] = x * cs - y * sn;
+      hi[e] = x * sn + y * cs;
+    }
+    *reinterpret_cast<uint4 *>(k_pool + dst + c * EPL) = pack16<T>(lo);
+    *reinterpret_cast<uint4 *>(k_pool + dst + D / 2 + c * EPL) = pack16<T>(hi);
+    *reinterpret_cast<uint4 *>(v_pool + dst + c * EPL) =
+        *reinterpret_cast<const uint4 *>(v_pool + src + c * EPL);
+    *reinterpret_cast<uint4 *>(v_pool + dst + D / 2 + c * EPL) =
+        *reinterpret_cast<const uint4 *>(v_pool + src + D / 2 + c * EPL);
+  }
+}
+
+template <typename T, int D>
+int launch_materialise(lazy_pool *p, int32_t tok_lo, int32_t n_tokens, int32_t offset,
+                       const MatBlocks &mb, cudaStream_t s) {
+  constexpr int EPL = 16 / (int)sizeof(T);
+  const int64_t total = (int64_t)n_tokens * p->hkv * ((D / 2) / EPL);
+  const int threads = 256;
+  const int64_t want = (total + threads - 1) / threads;
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)p->num_sms * 16));
+  materialise_kernel<T, D><<<grid, threads, 0, s>>>((T *)p->k, (T *)p->v, p->d_turn, p->hkv,
+                                                   tok_lo, n_tokens, offset, mb);
+  LAZY_CUDA_TRY(cudaGetLastError());
+  return LAZY_OK;
 }
 
 // ----------------------------------------------------------------------------------------------
@@ -225,6 +293,49 @@ extern "C" int kv_pool_write_tokens(lazy_pool *p, const void *k_raw, const void 
   bl.n = 0;
   return dispatch_encode(p, k_raw, v, n_tokens, 0, 0, bl, slot_mapping, local_pos,
                          (cudaStream_t)stream);
+}
+
+extern "C" int kv_pool_materialise(lazy_pool *p, const int32_t *src_block_ids,
+                                   const int32_t *dst_block_ids, int32_t n_tokens,
+                                   int32_t offset, lazy_stream_t stream) {
+  if (!p || n_tokens < 0 || offset < 0) return LAZY_ERR_INVALID_ARG;
+  if (n_tokens == 0) return LAZY_OK;
+  if (!src_block_ids || !dst_block_ids) return LAZY_ERR_INVALID_ARG;
+  if (p->alibi) return LAZY_ERR_UNSUPPORTED;  // ALiBi pools cache K unrotated
+  if ((int64_t)offset + n_tokens > (1ll << 26)) return LAZY_ERR_INVALID_ARG;
+  const int32_t n_pages = (n_tokens + kPage - 1) / kPage;
+  std::vector<int32_t> src_sorted(src_block_ids, src_block_ids + n_pages);
+  std::sort(src_sorted.begin(), src_sorted.end());
+  for (int32_t i = 0; i < n_pages; ++i) {
+    if (src_block_ids[i] < 0 || src_block_ids[i] >= p->num_blocks || dst_block_ids[i] < 0 ||
+        dst_block_ids[i] >= p->num_blocks)
+      return LAZY_ERR_INVALID_ARG;
+    // the copy must not overwrite the pages it reads
+    if (std::binary_search(src_sorted.begin(), src_sorted.end(), dst_block_ids[i]))
+      return LAZY_ERR_INVALID_ARG;
+  }
+  int rc = ensure_device(p);
+  if (rc != LAZY_OK) return rc;
+  p->encoded = true;
+  cudaStream_t s = (cudaStream_t)stream;
+  for (int32_t pg = 0; pg < n_pages; pg += kMaxMatIds) {
+    MatBlocks mb;
+    mb.first_page = pg;
+    mb.n = std::min(kMaxMatIds, n_pages - pg);
+    for (int i = 0; i < mb.n; ++i) {
+      mb.src[i] = src_block_ids[pg + i];
+      mb.dst[i] = dst_block_ids[pg + i];
+    }
+    const int32_t lo = pg * kPage, hi = std::min(n_tokens, (pg + mb.n) * kPage);
+    if (p->dtype == LAZY_DTYPE_BF16)
+      rc = p->d == 128 ? launch_materialise<__nv_bfloat16, 128>(p, lo, hi - lo, offset, mb, s)
+                       : launch_materialise<__nv_bfloat16, 64>(p, lo, hi - lo, offset, mb, s);
+    else
+      rc = p->d == 128 ? launch_materialise<float, 128>(p, lo, hi - lo, offset, mb, s)
+                       : launch_materialise<float, 64>(p, lo, hi - lo, offset, mb, s);
+    if (rc != LAZY_OK) return rc;
+  }
+  return LAZY_OK;
 }
 
 extern "C" int lazy_debug_gather(lazy_pool *p, const uint64_t *words, int32_t n_words,

@@ -29,6 +29,7 @@ struct PrefillParams {
   void *workspace;      // caller's scratch (tensor-core path: partial results of split units)
   size_t workspace_bytes;
   int32_t qside;        // CUDA-core path: query-side rotation per document offset
+  int32_t absolute;     // tensor-core path: reference position 0 (LAZY_PREFILL_ABSOLUTE_KEYS)
 };
 
 int prefill_simt(lazy_pool *p, const PrefillParams &pp, int32_t max_q_len, cudaStream_t s);

@@ -307,11 +307,13 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
 }
 
 // The relative rotation of one row chunk, x_i <- x_i cos - x_{i+64} sin and
-// x_{i+64} <- x_i sin + x_{i+64} cos for i = 8c .. 8c+7: bf16 in (as loaded), fp16 out (the
-// operand type of the QK product), fp32 arithmetic with a single rounding at the end. fp16 keeps
-// 11 significant bits against bf16's 8, so the rotated query row, whose rounding error is the
-// same for every key it meets and does not average out, costs 8x less in the log-sum-exp.
-__device__ __forceinline__ void rot_words_f16(uint4 &a, uint4 &b, const RotF &rf) {
+// x_{i+64} <- x_i sin + x_{i+64} cos for i = 8c .. 8c+7: bf16 in (as loaded), out in the operand
+// type of the QK product (kF16: fp16, else bf16), fp32 arithmetic with a single rounding at the
+// end. fp16 keeps 11 significant bits against bf16's 8, so the rotated query row, whose rounding
+// error is the same for every key it meets and does not average out, costs 8x less in the
+// log-sum-exp.
+template <bool kF16>
+__device__ __forceinline__ void rot_words(uint4 &a, uint4 &b, const RotF &rf) {
   uint32_t *x = reinterpret_cast<uint32_t *>(&a);
   uint32_t *y = reinterpret_cast<uint32_t *>(&b);
 #pragma unroll
@@ -321,25 +323,27 @@ __device__ __forceinline__ void rot_words_f16(uint4 &a, uint4 &b, const RotF &rf
     const float2 ys = __fmul2_rn(yf, rf.si[k]);
     const float2 xo = __ffma2_rn(xf, rf.co[k], make_float2(-ys.x, -ys.y));
     const float2 yo = __ffma2_rn(xf, rf.si[k], __fmul2_rn(yf, rf.co[k]));
-    x[k] = pack_h2(xo.x, xo.y);
-    y[k] = pack_h2(yo.x, yo.y);
+    x[k] = kF16 ? pack_h2(xo.x, xo.y) : pack_bf2(xo.x, xo.y);
+    y[k] = kF16 ? pack_h2(yo.x, yo.y) : pack_bf2(yo.x, yo.y);
   }
 }
 
 // Rotate, in place, one row of a 128-row swizzled tile at 16-byte chunk c of both 64-dim boxes
 // (the pair (i, i+64) of a row sits at the same swizzled offset of the two boxes).
+template <bool kF16>
 __device__ __forceinline__ void rotate_row_chunk(uint8_t *tile, int row, int c, const RotF &rf) {
   const int phys = (c ^ (row & 7)) * 16;
   uint4 *lo = reinterpret_cast<uint4 *>(tile + row * 128 + phys);
   uint4 *hi = reinterpret_cast<uint4 *>(tile + kHalfBytes + row * 128 + phys);
   uint4 a = *lo, b = *hi;
-  rot_words_f16(a, b, rf);
+  rot_words<kF16>(a, b, rf);
   *lo = a;
   *hi = b;
 }
 
 // The same rotation for 4 consecutive rows of one page (one angle set): all loads first, then
 // the math, then the stores.
+template <bool kF16>
 __device__ __forceinline__ void rotate_4rows_chunk(uint8_t *tile, int row0, int c, const RotF &rf) {
   uint4 a[4], b[4];
 #pragma unroll
@@ -350,7 +354,7 @@ __device__ __forceinline__ void rotate_4rows_chunk(uint8_t *tile, int row0, int 
     b[rr] = *reinterpret_cast<const uint4 *>(tile + kHalfBytes + row * 128 + phys);
   }
 #pragma unroll
-  for (int rr = 0; rr < 4; ++rr) rot_words_f16(a[rr], b[rr], rf);
+  for (int rr = 0; rr < 4; ++rr) rot_words<kF16>(a[rr], b[rr], rf);
 #pragma unroll
   for (int rr = 0; rr < 4; ++rr) {
     const int row = row0 + rr;
@@ -481,10 +485,18 @@ __device__ __forceinline__ TcUnit tc_unit(const TcParams &p) {
   return t;
 }
 
-// kAlibi: the pool's ALiBi mode. Nothing is rotated (the barriers keep their order) and every
-// score gets slope * (n - m) before the row max.
-template <bool kAlibi>
+// Modes. kRelative: RoPE pools, reference position m0 = the CTA's first question token, QK in
+// fp16 from the rotation passes. kAbsolute (LAZY_PREFILL_ABSOLUTE_KEYS): reference position 0,
+// so pages listed at offset 0 (keys materialised at absolute positions) need no rotation and
+// are used as stored, QK in bf16. kAlibi: the pool's ALiBi mode; nothing is rotated (the
+// barriers keep their order) and every score gets slope * (n - m) before the row max.
+enum { kRelative = 0, kAbsolute = 1, kAlibiMode = 2 };
+
+template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ TcParams p) {
+  constexpr bool kAlibi = kMode == kAlibiMode;
+  constexpr bool kAbs = kMode == kAbsolute;
+  constexpr bool kF16 = kMode == kRelative;  // operand type of the QK product
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t *Qs = sm + kOffQ;
@@ -509,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   const int32_t Tb = p.cu_q[b + 1] - qbeg;
   if (t0 >= Tb) return;
   const int32_t q_pos0_b = p.q_pos0[b];
-  const int32_t m0 = q_pos0_b + t0;
+  const int32_t m0 = kAbs ? 0 : q_pos0_b + t0;  // reference position of the rotations
   const int32_t pg0 = p.cu_pages[b], npg = p.cu_pages[b + 1] - pg0;
   const int n_doc = (npg + 7) / 8;
   const int t_end = min(t0 + 2 * TQ, Tb);
@@ -685,7 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       // nothing rotated); PV multiplies bf16 weights by bf16 values, V MN-major (bit 16).
       const uint32_t idesc_base = (1u << 4) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
       const uint32_t idesc_bf16 = idesc_base | (1u << 7) | (1u << 10);
-      const uint32_t idesc_qk = kAlibi ? idesc_bf16 : idesc_base;
+      const uint32_t idesc_qk = kF16 ? idesc_base : idesc_bf16;
       const uint32_t idesc_pv = idesc_bf16 | (1u << 16);
       const uint32_t q_addr = smem_u32(Qs), k_addr = smem_u32(Ks), v_addr = smem_u32(Vs);
       // Issue order keeps both softmax groups busy: QK for Q tile 0 of the next key tile is
@@ -775,8 +787,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 #pragma unroll 1
       for (int c = 0; c < 8; ++c) {
         RotF rq;
-        chunk_angles_ilp((int64_t)(i * TQ + row / G), turn_s, c, rq);
-        rotate_row_chunk(Qs + i * kTileBytes, row, c, rq);
+        chunk_angles_ilp(kAbs ? (int64_t)(q_pos0_b + t_row) : (int64_t)(i * TQ + row / G),
+                         turn_s, c, rq);
+        rotate_row_chunk<kF16>(Qs + i * kTileBytes, row, c, rq);
       }
       fence_async_smem();
     }
@@ -793,18 +806,24 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       } else if (mt.kind == 0) {
         // one relative rotation R(o - m0) per page
         const int64_t d = (int64_t)mt.off[rrow0 >> 4] - m0;
-        if (d != cached) {
-          cached = d;
-          chunk_angles_h(d, turn, rc, rp);
+        if (!kAbs || d != 0) {  // absolute keys at offset 0 are used as stored
+          if (d != cached) {
+            cached = d;
+            chunk_angles_h(d, turn, rc, rp);
+          }
+          rotate_4rows_chunk<kF16>(kt, rrow0, rc, widen(rp));
         }
-        rotate_4rows_chunk(kt, rrow0, rc, widen(rp));
       } else {
-        // question keys: raw, rotated by R(p - m0) row by row
+        // question keys: raw, rotated by R(p - m0) row by row (the absolute mode re-reads the
+        // request's first position here rather than keeping it in a register)
+        const int64_t q0 = kAbs ? (int64_t)p.q_pos0[tc_unit(p).b] : 0;
 #pragma unroll 1
         for (int rr = 0; rr < 4; ++rr) {
           RotF rk;
-          chunk_angles((int64_t)(mt.c0 + rrow0 + rr - t_row + t_off), turn, rc, rk);
-          rotate_row_chunk(kt, rrow0 + rr, rc, rk);
+          chunk_angles(kAbs ? q0 + mt.c0 + rrow0 + rr
+                            : (int64_t)(mt.c0 + rrow0 + rr - t_row + t_off),
+                       turn, rc, rk);
+          rotate_row_chunk<kF16>(kt, rrow0 + rr, rc, rk);
         }
       }
       if (!kAlibi) fence_async_smem();
@@ -1291,14 +1310,17 @@ int prefill_tc(lazy_pool *p, const PrefillParams &pp, int32_t max_q_len, cudaStr
   tp.scale_log2 = pp.scale_log2;
   tp.wait_ns = pp.wait_ns;
   tp.slopes = pp.slopes;
-  static bool attr = false;
-  if (!attr) {
-    LAZY_CUDA_TRY(cudaFuncSetAttribute(prefill_tc_kernel<false>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes));
-    LAZY_CUDA_TRY(cudaFuncSetAttribute(prefill_tc_kernel<true>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes));
-    attr = true;
-  }
+  static std::once_flag attr_once;
+  static cudaError_t attr_rc = cudaSuccess;
+  std::call_once(attr_once, [] {
+    for (auto fn : {prefill_tc_kernel<kRelative>, prefill_tc_kernel<kAbsolute>,
+                    prefill_tc_kernel<kAlibiMode>}) {
+      const cudaError_t e = cudaFuncSetAttribute(
+          fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+      if (e != cudaSuccess && attr_rc == cudaSuccess) attr_rc = e;
+    }
+  });
+  LAZY_CUDA_TRY(attr_rc);
   // The split runs only when the caller's workspace holds its partial results.
   TcPlan pl = plan_tc(pp.batch, pp.hkv, TQ, max_q_len, schedule_sms(p));
   if (pl.ksplit > 1 && (!pp.workspace || pp.workspace_bytes < pl.ws_bytes ||
@@ -1322,9 +1344,11 @@ int prefill_tc(lazy_pool *p, const PrefillParams &pp, int32_t max_q_len, cudaStr
     if (rc != LAZY_OK) return rc;
   }
   if (pp.slopes)
-    prefill_tc_kernel<true><<<pl.grid, kThreads, kSmemBytes, s>>>(tp);
+    prefill_tc_kernel<kAlibiMode><<<pl.grid, kThreads, kSmemBytes, s>>>(tp);
+  else if (pp.absolute)
+    prefill_tc_kernel<kAbsolute><<<pl.grid, kThreads, kSmemBytes, s>>>(tp);
   else
-    prefill_tc_kernel<false><<<pl.grid, kThreads, kSmemBytes, s>>>(tp);
+    prefill_tc_kernel<kRelative><<<pl.grid, kThreads, kSmemBytes, s>>>(tp);
   LAZY_CUDA_TRY(cudaGetLastError());
   if (pl.ksplit > 1) {
     switch (pl.ksplit) {

@@ -10,7 +10,8 @@ from typing import Dict, List, Optional
 
 import numpy as np
 
-from . import (LazyPool, build_page_table, kv_pool_alloc, kv_pool_insert_doc)
+from . import (LazyPool, build_page_table, kv_pool_alloc, kv_pool_insert_doc,
+               kv_pool_materialise)
 
 
 def _torch_dtype(wl):
@@ -290,6 +291,39 @@ def chain_step_batch(wl, res: Resident, ch: Chain, step: int, src, device="cuda"
         torch.cat(nk).contiguous(), torch.cat(nv).contiguous(),
         torch.tensor(slots, dtype=torch.int32, device=device),
         torch.tensor(lpos, dtype=torch.int32, device=device), n_keys)
+
+
+def materialised_blocks_needed(wl, reqs=None) -> int:
+    """Blocks that one materialised copy per distinct (document, offset) pair takes."""
+    reqs = reqs if reqs is not None else wl.requests
+    pairs = {(d, o) for r in reqs for d, o in zip(r.docs, r.offsets)}
+    return len(pairs) * (-(-wl.doc_len // wl.page_size))
+
+
+def materialise_copies(wl, res: Resident, reqs=None, stream=None) -> Dict[tuple, List[int]]:
+    """The copy-per-offset baseline: one re-encoded copy (keys at absolute positions, written by
+    kv_pool_materialise) of every distinct (document, offset) pair the requests use. Returns
+    {(doc, offset): block ids}."""
+    reqs = reqs if reqs is not None else wl.requests
+    copies: Dict[tuple, List[int]] = {}
+    for r in reqs:
+        for d, o in zip(r.docs, r.offsets):
+            if (d, o) not in copies:
+                copies[(d, o)] = kv_pool_materialise(res.pool, res.doc_blocks[d], wl.doc_len, o,
+                                                     stream=stream)
+    return copies
+
+
+def copy_page_table(wl, res: Resident, copies, reqs, with_private: bool):
+    """Page words over the materialised copies: every document page at offset 0 (its keys
+    already carry their absolute positions); the private segment as in page_table."""
+    segs = []
+    for r in reqs:
+        s = [(copies[(d, o)], 0, wl.doc_len) for d, o in zip(r.docs, r.offsets)]
+        if with_private:
+            s.append((res.priv_blocks[r.index], r.priv_offset, r.priv_len))
+        segs.append(s)
+    return build_page_table(segs, wl.page_size)
 
 
 def kv_bytes_accounting(wl) -> Dict[str, int]:

@@ -1,0 +1,143 @@
+"""GPU checks of the copy-per-offset baseline: kv_pool_materialise writes a document re-encoded
+for one logical offset (keys at absolute positions), the decode reads such copies through page
+words of offset 0, and the tensor-core prefill reads them with LAZY_PREFILL_ABSOLUTE_KEYS. The
+attention over the copies is the same attention, so the oracle tolerances hold.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workload as W
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def pk(lazylib, cuda_ok):
+    import position_independent_kv_lazy_gb300 as m
+    return m
+
+
+def _h():
+    from position_independent_kv_lazy_gb300 import harness
+    return harness
+
+
+@pytest.mark.parametrize("dtype,D", [("bf16", 128), ("fp32", 64)])
+def test_materialised_pages_hold_keys_at_absolute_positions(pk, dtype, D):
+    # a 40-token document (the last page partial) re-encoded for offset 123457: K rows equal
+    # R(offset + j) k up to the cache's rounding (twice: the cached copy, then the re-encoded
+    # one); V rows are the raw values
+    H = _h()
+    wl = W.custom("decode", [[(0, 123457)]], doc_len=40, n_pool=1, Hq=4, Hkv=2, D=D, dtype=dtype,
+                  base=500000.0, priv=[(123497, 1)], seed=31)
+    src = H.HostSource(wl)
+    res = H.build_resident(wl, src, resident_pool=False, extra_blocks=4)
+    o = wl.requests[0].offsets[0]
+    blocks = pk.kv_pool_materialise(res.pool, res.doc_blocks[0], wl.doc_len, o)
+    torch.cuda.synchronize()
+    assert pk.lazy_get_device_error(res.pool) == 0
+    assert not set(blocks) & set(res.doc_blocks[0])
+    kr, vr = wl.doc_k(0), wl.doc_v(0)
+    tol = 2 ** -7 if dtype == "bf16" else 1e-6
+    for j in range(wl.doc_len):
+        gk = res.pool.k_pages[blocks[j // 16], :, j % 16].float().cpu().numpy()
+        gv = res.pool.v_pages[blocks[j // 16], :, j % 16].float().cpu().numpy()
+        assert np.array_equal(gv, vr[j])
+        for h in range(wl.Hkv):
+            exact = oracle.rope(kr[j, h], o + j, wl.rope_base)
+            pair = np.hypot(exact[:D // 2], exact[D // 2:])
+            err = np.abs(gk[h] - exact)
+            assert (err <= tol * np.maximum(1.0, np.concatenate([pair, pair]))).all(), (j, h)
+
+
+def test_materialise_rejects_in_place_and_alibi(pk):
+    H = _h()
+    wl = W.custom("decode", [[(0, 5)]], doc_len=32, n_pool=1, Hq=4, Hkv=2, D=128, dtype="bf16",
+                  base=500000.0, priv=[(37, 1)], seed=32)
+    src = H.HostSource(wl)
+    res = H.build_resident(wl, src, resident_pool=False, extra_blocks=2)
+    ids = res.doc_blocks[0]
+    with pytest.raises(pk.LazyError):
+        pk.kv_pool_materialise(res.pool, ids, 32, 7, dst_block_ids=[ids[1], ids[0]])
+    ares = H.build_resident(wl, src, resident_pool=False, extra_blocks=2,
+                            alibi_slopes=W.alibi_slopes(4))
+    with pytest.raises(pk.LazyError):
+        pk.kv_pool_materialise(ares.pool, ares.doc_blocks[0], 32, 7)
+
+
+def _copy_setup(pk, wl, src):
+    H = _h()
+    res = H.build_resident(wl, src, resident_pool=False, drop_raw=False,
+                           extra_blocks=H.materialised_blocks_needed(wl))
+    copies = H.materialise_copies(wl, res)
+    torch.cuda.synchronize()
+    assert pk.lazy_get_device_error(res.pool) == 0
+    return res, copies
+
+
+def test_decode_over_materialised_copies(pk):
+    # gaps, overlaps, one document at several offsets (one copy each). A copy holds each key
+    # rounded twice (the cache's R(j) k, then R(o + j) k), so contexts are kept at a thousand
+    # keys or more: on a few hundred keys that double storage rounding alone reaches 1e-3 of lse
+    H = _h()
+    segs = [[(0, 0), (1, 1024), (2, 2048)], [(2, 5), (0, 4000), (2, 9000)], [(1, 0)],
+            [(3, 1000), (0, 1000)]]
+    wl = W.custom("decode", segs, doc_len=1024, n_pool=4, Hq=32, Hkv=8, D=128, dtype="bf16",
+                  base=500000.0, priv=[(3072, 9), (10100, 16), (1024, 33), (2100, 1)], seed=3)
+    src = H.HostSource(wl)
+    res, copies = _copy_setup(pk, wl, src)
+    assert len(copies) == 9  # distinct (doc, offset) pairs
+    words, cu = H.copy_page_table(wl, res, copies, wl.requests, with_private=True)
+    db = H.decode_batch(wl, res, src)
+    out, lse = pk.lazy_attn_decode(res.pool, db.q, db.q_pos,
+                                   torch.from_numpy(words.view(np.int64)).cuda(),
+                                   torch.from_numpy(cu).cuda(), sm_scale=wl.sm_scale)
+    torch.cuda.synchronize()
+    assert pk.lazy_get_device_error(res.pool) == 0
+    out, lse = out.float().cpu().numpy(), lse.cpu().numpy()
+    for b in range(wl.batch):
+        ro, rl = oracle.attend_request(wl, b)
+        assert np.abs(out[b] - ro[0]).max() <= 2e-2
+        assert np.abs(lse[b] - rl[0]).max() <= 1e-3
+
+
+def _prefill_wl():
+    # 1024-token documents (the tensor-core absolute mode rounds R(m) q to bf16, a per-row error
+    # that needs a few thousand keys to stay under 1e-3 of lse); one document at two offsets
+    segs = [[(0, 0), (1, 1024), (0, 4096)], [(2, 3)], [(1, 5000), (2, 17), (0, 9000)]]
+    return W.custom("prefill", segs, doc_len=1024, n_pool=3, Hq=32, Hkv=8, D=128, dtype="bf16",
+                    base=500000.0, T=[37, 200, 130], q_pos0=[5200, 1100, 10100], seed=33)
+
+
+@pytest.mark.parametrize("sms", [0, 20])
+def test_prefill_absolute_keys_over_copies(pk, sms):
+    H = _h()
+    wl = _prefill_wl()
+    src = H.HostSource(wl)
+    res, copies = _copy_setup(pk, wl, src)
+    pb = H.prefill_batch(wl, res, src)
+    words, cu = H.copy_page_table(wl, res, copies, pb.reqs, with_private=False)
+    d_words = torch.from_numpy(words.view(np.int64)).cuda()
+    d_cu = torch.from_numpy(cu).cuda()
+    pk.lazy_pool_set_schedule_sms(res.pool, sms)
+    results = {}
+    for name, fl, w, c in (
+            ("abs_copies", pk.LAZY_PREFILL_TC | pk.LAZY_PREFILL_ABSOLUTE_KEYS, d_words, d_cu),
+            ("rel_copies", pk.LAZY_PREFILL_TC, d_words, d_cu),
+            ("abs_lazy", pk.LAZY_PREFILL_TC | pk.LAZY_PREFILL_ABSOLUTE_KEYS, pb.words,
+             pb.cu_pages)):
+        out, lse = pk.lazy_attn_prefill(res.pool, pb.q, pb.k_new, pb.v_new, pb.cu_q, pb.q_pos0,
+                                        w, c, pb.max_q_len, sm_scale=wl.sm_scale, flags=fl)
+        torch.cuda.synchronize()
+        assert pk.lazy_get_device_error(res.pool) == 0
+        results[name] = (out.float().cpu().numpy(), lse.cpu().numpy())
+    cuq = pb.cu_q.cpu().numpy()
+    for b in range(wl.batch):
+        ro, rl = oracle.attend_request(wl, b)
+        rows = slice(cuq[b], cuq[b + 1])
+        for name, (o, l) in results.items():
+            assert np.abs(o[rows] - ro).max() <= 2e-2, (name, b)
+            assert np.abs(l[rows] - rl).max() <= 1e-3, (name, b)
