@@ -105,11 +105,14 @@ def test_decode_over_materialised_copies(pk):
 
 
 def _prefill_wl():
-    # 1024-token documents (the tensor-core absolute mode rounds R(m) q to bf16, a per-row error
-    # that needs a few thousand keys to stay under 1e-3 of lse); one document at two offsets
-    segs = [[(0, 0), (1, 1024), (0, 4096)], [(2, 3)], [(1, 5000), (2, 17), (0, 9000)]]
-    return W.custom("prefill", segs, doc_len=1024, n_pool=3, Hq=32, Hkv=8, D=128, dtype="bf16",
-                    base=500000.0, T=[37, 200, 130], q_pos0=[5200, 1100, 10100], seed=33)
+    # 8 documents of 1024 tokens per request, some listed at two offsets (two copies). The
+    # absolute-keys mode rounds R(m) q to bf16, a per-row error that shrinks like 1/sqrt(keys):
+    # about 1.5e-3 of lse at 1.2K keys, under 6e-4 at 8K, so every context here holds 8K+ keys.
+    segs = [[(d, 1024 * i) for i, d in enumerate([0, 1, 2, 3, 4, 5, 6, 0])],
+            [(d, 1024 * i + 3) for i, d in enumerate([7, 2, 5, 1, 3, 6, 4, 8])],
+            [(d, 1024 * i + 700) for i, d in enumerate([9, 8, 7, 6, 5, 4, 3, 2])]]
+    return W.custom("prefill", segs, doc_len=1024, n_pool=10, Hq=32, Hkv=8, D=128, dtype="bf16",
+                    base=500000.0, T=[37, 100, 130], q_pos0=[8192, 8195, 9000], seed=33)
 
 
 @pytest.mark.parametrize("sms", [0, 20])
