@@ -105,14 +105,19 @@ def test_decode_over_materialised_copies(pk):
 
 
 def _prefill_wl():
-    # 8 documents of 1024 tokens per request, some listed at two offsets (two copies). The
-    # absolute-keys mode rounds R(m) q to bf16, a per-row error that shrinks like 1/sqrt(keys):
-    # about 1.5e-3 of lse at 1.2K keys, under 6e-4 at 8K, so every context here holds 8K+ keys.
-    segs = [[(d, 1024 * i) for i, d in enumerate([0, 1, 2, 3, 4, 5, 6, 0])],
-            [(d, 1024 * i + 3) for i, d in enumerate([7, 2, 5, 1, 3, 6, 4, 8])],
-            [(d, 1024 * i + 700) for i, d in enumerate([9, 8, 7, 6, 5, 4, 3, 2])]]
-    return W.custom("prefill", segs, doc_len=1024, n_pool=10, Hq=32, Hkv=8, D=128, dtype="bf16",
-                    base=500000.0, T=[37, 100, 130], q_pos0=[8192, 8195, 9000], seed=33)
+    # 16 documents of 1024 tokens per request (the prefill configuration's context), some
+    # listed at two offsets (two copies). The absolute-keys mode multiplies Q.K in bf16, so its
+    # per-row rounding of R(m) q (and, on the lazy tables, of each rotated key tile) is the
+    # error of a standard bf16 kernel: about 1e-3 of lse at 8K keys, shrinking like
+    # 1/sqrt(keys); at 16K keys it stays under 1e-3.
+    rng = __import__("numpy").random.default_rng(7)
+    segs = []
+    for b, shift in enumerate((0, 3, 700)):
+        docs = [int(d) for d in rng.permutation(16)]
+        docs[-1] = docs[0]  # one document twice in the request: two copies
+        segs.append([(d, 1024 * i + shift) for i, d in enumerate(docs)])
+    return W.custom("prefill", segs, doc_len=1024, n_pool=16, Hq=32, Hkv=8, D=128, dtype="bf16",
+                    base=500000.0, T=[37, 100, 130], q_pos0=[16384, 16387, 17200], seed=33)
 
 
 @pytest.mark.parametrize("sms", [0, 20])
