@@ -406,6 +406,19 @@ def _traffic(name):
     return None
 
 
+def bench_materialised_only(args):
+    """The copy-per-offset baseline section alone."""
+    import torch
+
+    import position_independent_kv_lazy_gb300 as pk
+    pk.build_library()
+    pk.load_library()
+    hbm_peak, tc_peak, _, _ = _peaks()
+    flush, _ = _make_flush(torch)
+    print(json.dumps({"mode": "materialised only", "materialised": materialised_bench(
+        args, flush, torch.cuda.current_stream(), hbm_peak, tc_peak)}), flush=True)
+
+
 def bench_long_decode_only(args):
     """Long-context decode alone (resident pool of its 512 documents): for profiling runs."""
     import numpy as np
@@ -885,8 +898,8 @@ def materialised_bench(args, flush, stream, hbm_peak, tc_peak):
     out = {"note": "copies: one per distinct (document, offset) pair, written by "
                    "kv_pool_materialise (un-rotate by R(-j), re-rotate by R(o + j)); decode over "
                    "copies uses page words of offset 0, prefill over copies "
-                   "LAZY_PREFILL_ABSOLUTE_KEYS (reference position 0, bf16 Q.K, no rotation "
-                   "pass for offset-0 pages)"}
+                   "LAZY_PREFILL_ABSOLUTE_KEYS (reference position 0: offset-0 pages are only "
+                   "converted to the fp16 Q.K operand type, not rotated)"}
     # ---- decode: decode_b64 (shared documents) and its no-reuse control
     for name, wl in (("decode_b64", W.decode_workload()),
                      ("decode_b64_no_reuse", W.decode_workload(no_reuse=True,
@@ -1371,7 +1384,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["all", "decode", "prefill", "long_decode"],
+    ap.add_argument("--only", choices=["all", "decode", "prefill", "long_decode", "materialised"],
                     default="all",
                     help="decode / prefill / long_decode: time only that workload (smaller "
                          "footprint, for profiling)")
@@ -1390,6 +1403,8 @@ def main():
         bench_prefill_only(args)
     elif args.only == "long_decode":
         bench_long_decode_only(args)
+    elif args.only == "materialised":
+        bench_materialised_only(args)
     else:
         bench_ours(args)
 

@@ -80,10 +80,8 @@ enum {
     /* Added to one of the above: the cached pages hold keys at absolute positions (copies
        written by kv_pool_materialise) and are listed with offset 0. The attention is the same;
        the tensor-core kernel then takes position 0 as its reference (queries rotated by R(m),
-       question keys by R(p)), uses offset-0 pages as stored with no rotation pass, and
-       multiplies Q.K in bf16 like a kernel over materialised keys (the rotated query row is
-       rounded to bf16; on contexts of a few hundred keys that moves lse by up to ~2e-3). The
-       CUDA-core kernels ignore it. */
+       question keys by R(p)) and gives offset-0 pages no rotation, only their conversion to
+       the fp16 operand type of its Q.K product. The CUDA-core kernels ignore it. */
     LAZY_PREFILL_ABSOLUTE_KEYS = 16
 };
 

@@ -364,6 +364,26 @@ __device__ __forceinline__ void rotate_4rows_chunk(uint8_t *tile, int row0, int 
   }
 }
 
+// The identity on 4 rows of one page at chunk c: bf16 in, fp16 out (the absolute-keys mode's
+// pages listed at offset 0 need no rotation, only the operand type of the QK product).
+__device__ __forceinline__ void convert_4rows_chunk(uint8_t *tile, int row0, int c) {
+#pragma unroll
+  for (int rr = 0; rr < 4; ++rr) {
+    const int row = row0 + rr;
+    const int phys = (c ^ (row & 7)) * 16;
+#pragma unroll
+    for (int hb = 0; hb < 2; ++hb) {
+      uint4 *ptr = reinterpret_cast<uint4 *>(tile + hb * kHalfBytes + row * 128 + phys);
+      uint4 a = *ptr;
+      uint32_t *x = reinterpret_cast<uint32_t *>(&a);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        x[k] = pack_h2(__uint_as_float(x[k] << 16), __uint_as_float(x[k] & 0xFFFF0000u));
+      *ptr = a;
+    }
+  }
+}
+
 // (cos, sin) of delta * theta for two frequencies (turn fractions ta, tb), as two independent
 // chains. Not inlined: inside the tile loop the angles are needed only when a page offset
 // changes, and one shared copy keeps the loop's code compact (inlining the eight angles of a
@@ -487,16 +507,17 @@ __device__ __forceinline__ TcUnit tc_unit(const TcParams &p) {
 
 // Modes. kRelative: RoPE pools, reference position m0 = the CTA's first question token, QK in
 // fp16 from the rotation passes. kAbsolute (LAZY_PREFILL_ABSOLUTE_KEYS): reference position 0,
-// so pages listed at offset 0 (keys materialised at absolute positions) need no rotation and
-// are used as stored, QK in bf16. kAlibi: the pool's ALiBi mode; nothing is rotated (the
-// barriers keep their order) and every score gets slope * (n - m) before the row max.
+// so pages listed at offset 0 (keys materialised at absolute positions) need no rotation, only
+// a conversion to fp16; everything else as kRelative. kAlibi: the pool's ALiBi mode; nothing
+// is rotated (the barriers keep their order), QK in bf16 as loaded, and every score gets
+// slope * (n - m) before the row max.
 enum { kRelative = 0, kAbsolute = 1, kAlibiMode = 2 };
 
 template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ TcParams p) {
   constexpr bool kAlibi = kMode == kAlibiMode;
   constexpr bool kAbs = kMode == kAbsolute;
-  constexpr bool kF16 = kMode == kRelative;  // operand type of the QK product
+  constexpr bool kF16 = kMode != kAlibiMode;  // operand type of the QK product
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t *Qs = sm + kOffQ;
@@ -806,7 +827,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       } else if (mt.kind == 0) {
         // one relative rotation R(o - m0) per page
         const int64_t d = (int64_t)mt.off[rrow0 >> 4] - m0;
-        if (!kAbs || d != 0) {  // absolute keys at offset 0 are used as stored
+        if (kAbs && d == 0) {  // absolute keys at offset 0: no rotation, only the operand type
+          convert_4rows_chunk(kt, rrow0, rc);
+        } else {
           if (d != cached) {
             cached = d;
             chunk_angles_h(d, turn, rc, rp);

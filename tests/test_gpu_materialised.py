@@ -105,11 +105,9 @@ def test_decode_over_materialised_copies(pk):
 
 
 def _prefill_wl():
-    # 16 documents of 1024 tokens per request (the prefill configuration's context), some
-    # listed at two offsets (two copies). The absolute-keys mode multiplies Q.K in bf16, so its
-    # per-row rounding of R(m) q (and, on the lazy tables, of each rotated key tile) is the
-    # error of a standard bf16 kernel: about 1e-3 of lse at 8K keys, shrinking like
-    # 1/sqrt(keys); at 16K keys it stays under 1e-3.
+    # 16 documents of 1024 tokens per request (the prefill configuration's context), one
+    # listed at two offsets (two copies). Copies hold each key rounded twice (the cache's
+    # R(j) k, then R(o + j) k), an error that averages out over many keys.
     rng = __import__("numpy").random.default_rng(7)
     segs = []
     for b, shift in enumerate((0, 3, 700)):
