@@ -264,14 +264,15 @@ def kv_pool_insert_doc(pool: LazyPool, k_raw, v, local_pos0: int = 0,
     """Encode a segment's tokens (k rotated at local positions local_pos0.., v copied) into the
     pool; returns the segment's block ids (existing ones first, new ones appended)."""
     n = int(k_raw.shape[0])
-    owned = list(block_ids or [])
-    cap = max(len(owned), (local_pos0 + n + pool.page_size - 1) // pool.page_size, 1)
-    arr = (ctypes.c_int32 * cap)(*owned)
-    nb = ctypes.c_int32(len(owned))
+    owned = np.asarray(block_ids if block_ids is not None else [], dtype=np.int32)
+    cap = max(owned.shape[0], (local_pos0 + n + pool.page_size - 1) // pool.page_size, 1)
+    arr = np.zeros(cap, dtype=np.int32)
+    arr[: owned.shape[0]] = owned
+    nb = ctypes.c_int32(owned.shape[0])
     _check("kv_pool_insert_doc", load_library().kv_pool_insert_doc(
-        pool.handle, _ptr(k_raw.contiguous()), _ptr(v.contiguous()), n, local_pos0, arr,
-        ctypes.byref(nb), cap, _stream(stream)))
-    return list(arr[: nb.value])
+        pool.handle, _ptr(k_raw.contiguous()), _ptr(v.contiguous()), n, local_pos0,
+        arr.ctypes.data_as(_pi32), ctypes.byref(nb), cap, _stream(stream)))
+    return arr[: nb.value].tolist()
 
 
 def kv_pool_write_tokens(pool: LazyPool, k_raw, v, slot_mapping, local_pos, stream=None):

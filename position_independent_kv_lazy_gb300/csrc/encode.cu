@@ -21,12 +21,14 @@ struct BlockList {
   int32_t ids[kMaxIdsPerLaunch];
 };
 
-// One thread = (token, kv head, 16-byte chunk of the lower half); it also handles the matching
-// chunk of the upper half, which holds the rotation partners (pairs (i, i + D/2)).
+// One thread = (token, group of hpt kv heads, 16-byte chunk of the lower half): it also handles
+// the matching chunk of the upper half, which holds the rotation partners (pairs (i, i + D/2)).
+// The angles depend only on the position and the frequency, so a thread evaluates them once
+// for its hpt heads (large inserts: several heads per thread; a decode step's few tokens: one).
 template <typename T, int D>
 __global__ void __launch_bounds__(256) encode_kernel(
     const T *__restrict__ k_raw, const T *__restrict__ v, int32_t n_tokens, int32_t hkv,
-    T *__restrict__ k_pool, T *__restrict__ v_pool, const uint64_t *__restrict__ turn,
+    int32_t hpt, T *__restrict__ k_pool, T *__restrict__ v_pool, const uint64_t *__restrict__ turn,
     int32_t tok0, int32_t local_pos0, BlockList blocks, const int32_t *__restrict__ slot_map,
     const int32_t *__restrict__ local_pos, int32_t num_blocks, int32_t *err, int32_t rope) {
   constexpr int EPL = 16 / (int)sizeof(T);
@@ -34,13 +36,14 @@ __global__ void __launch_bounds__(256) encode_kernel(
   // A decode launched right after this append may start its launch early; it waits for this
   // grid to finish before reading anything (programmatic dependent launch).
   cudaTriggerProgrammaticLaunchCompletion();
-  const int64_t total = (int64_t)n_tokens * hkv * CH;
+  const int32_t groups = hkv / hpt;
+  const int64_t total = (int64_t)n_tokens * groups * CH;
   for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
        idx += (int64_t)gridDim.x * blockDim.x) {
     const int c = (int)(idx % CH);
     const int64_t rest = idx / CH;
-    const int h = (int)(rest % hkv);
-    const int32_t t = tok0 + (int32_t)(rest / hkv);
+    const int h0 = (int)(rest % groups) * hpt;
+    const int32_t t = tok0 + (int32_t)(rest / groups);
     int32_t j, blk, slot;
     if (slot_map) {
       const int32_t s = slot_map[t];
@@ -49,7 +52,7 @@ __global__ void __launch_bounds__(256) encode_kernel(
       blk = s / kPage;
       slot = s % kPage;
       if (blk >= num_blocks) {  // a slot outside the pool: flag it, write nothing
-        if (c == 0) set_error(err, LAZY_DEVERR_BAD_PAGE);
+        if (c == 0 && h0 == 0) set_error(err, LAZY_DEVERR_BAD_PAGE);
         continue;
       }
     } else {
@@ -57,28 +60,44 @@ __global__ void __launch_bounds__(256) encode_kernel(
       blk = blocks.ids[j / kPage - blocks.first_page];
       slot = j % kPage;
     }
-    const size_t src = ((size_t)t * hkv + h) * D;
-    const size_t dst = (((size_t)blk * hkv + h) * kPage + slot) * D;
-    float lo[EPL], hi[EPL];
-    unpack16<T>(*reinterpret_cast<const uint4 *>(k_raw + src + c * EPL), lo);
-    unpack16<T>(*reinterpret_cast<const uint4 *>(k_raw + src + D / 2 + c * EPL), hi);
+    float cs[EPL], sn[EPL];
     if (rope) {  // ALiBi pools keep K as given
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) {
-        float cs, sn;
-        rope_cos_sin((int64_t)j, turn[c * EPL + e], cs, sn);
-        const float x = lo[e], y = hi[e];
-        lo[e] = x * cs - y * sn;
-        hi[e] = x * sn + y * cs;
-      }
+      for (int e = 0; e < EPL; ++e) rope_cos_sin((int64_t)j, turn[c * EPL + e], cs[e], sn[e]);
     }
-    *reinterpret_cast<uint4 *>(k_pool + dst + c * EPL) = pack16<T>(lo);
-    *reinterpret_cast<uint4 *>(k_pool + dst + D / 2 + c * EPL) = pack16<T>(hi);
-    *reinterpret_cast<uint4 *>(v_pool + dst + c * EPL) =
-        *reinterpret_cast<const uint4 *>(v + src + c * EPL);
-    *reinterpret_cast<uint4 *>(v_pool + dst + D / 2 + c * EPL) =
-        *reinterpret_cast<const uint4 *>(v + src + D / 2 + c * EPL);
+#pragma unroll 2
+    for (int h = h0; h < h0 + hpt; ++h) {
+      const size_t src = ((size_t)t * hkv + h) * D;
+      const size_t dst = (((size_t)blk * hkv + h) * kPage + slot) * D;
+      const uint4 ka = *reinterpret_cast<const uint4 *>(k_raw + src + c * EPL);
+      const uint4 kb = *reinterpret_cast<const uint4 *>(k_raw + src + D / 2 + c * EPL);
+      const uint4 va = *reinterpret_cast<const uint4 *>(v + src + c * EPL);
+      const uint4 vb = *reinterpret_cast<const uint4 *>(v + src + D / 2 + c * EPL);
+      float lo[EPL], hi[EPL];
+      unpack16<T>(ka, lo);
+      unpack16<T>(kb, hi);
+      if (rope) {
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+          const float x = lo[e], y = hi[e];
+          lo[e] = x * cs[e] - y * sn[e];
+          hi[e] = x * sn[e] + y * cs[e];
+        }
+      }
+      *reinterpret_cast<uint4 *>(k_pool + dst + c * EPL) = pack16<T>(lo);
+      *reinterpret_cast<uint4 *>(k_pool + dst + D / 2 + c * EPL) = pack16<T>(hi);
+      *reinterpret_cast<uint4 *>(v_pool + dst + c * EPL) = va;
+      *reinterpret_cast<uint4 *>(v_pool + dst + D / 2 + c * EPL) = vb;
+    }
   }
+}
+
+// kv heads per thread: the largest of 8, 4, 2, 1 dividing Hkv that still leaves two 256-thread
+// CTAs per SM (fewer, longer threads would expose the memory latency of short launches).
+int heads_per_thread(const lazy_pool *p, int64_t rows) {
+  for (int hpt = 8; hpt > 1; hpt >>= 1)
+    if (p->hkv % hpt == 0 && rows * (p->hkv / hpt) >= (int64_t)p->num_sms * 512) return hpt;
+  return 1;
 }
 
 template <typename T, int D>
@@ -86,12 +105,14 @@ int launch_encode(lazy_pool *p, const void *k_raw, const void *v, int32_t n_toke
                   int32_t local_pos0, const BlockList &bl, const int32_t *slot_map,
                   const int32_t *local_pos, cudaStream_t s) {
   constexpr int EPL = 16 / (int)sizeof(T);
-  const int64_t total = (int64_t)n_tokens * p->hkv * ((D / 2) / EPL);
+  const int64_t rows = (int64_t)n_tokens * ((D / 2) / EPL);
+  const int hpt = heads_per_thread(p, rows);
+  const int64_t total = rows * (p->hkv / hpt);
   const int threads = 256;
   const int64_t want = (total + threads - 1) / threads;
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)p->num_sms * 16));
   encode_kernel<T, D><<<grid, threads, 0, s>>>(
-      (const T *)k_raw, (const T *)v, n_tokens, p->hkv, (T *)p->k, (T *)p->v, p->d_turn, tok0,
+      (const T *)k_raw, (const T *)v, n_tokens, p->hkv, hpt, (T *)p->k, (T *)p->v, p->d_turn, tok0,
       local_pos0, bl, slot_map, local_pos, p->num_blocks, p->d_err, p->alibi ? 0 : 1);
   LAZY_CUDA_TRY(cudaGetLastError());
   return LAZY_OK;
@@ -133,37 +154,47 @@ struct MatBlocks {
 template <typename T, int D>
 __global__ void __launch_bounds__(256) materialise_kernel(
     T *__restrict__ k_pool, T *__restrict__ v_pool, const uint64_t *__restrict__ turn,
-    int32_t hkv, int32_t tok_lo, int32_t n_tokens, int32_t offset, MatBlocks mb) {
+    int32_t hkv, int32_t hpt, int32_t tok_lo, int32_t n_tokens, int32_t offset, MatBlocks mb) {
   constexpr int EPL = 16 / (int)sizeof(T);
   constexpr int CH = (D / 2) / EPL;
-  const int64_t total = (int64_t)n_tokens * hkv * CH;
+  const int32_t groups = hkv / hpt;
+  const int64_t total = (int64_t)n_tokens * groups * CH;
   for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
        idx += (int64_t)gridDim.x * blockDim.x) {
     const int c = (int)(idx % CH);
     const int64_t rest = idx / CH;
-    const int h = (int)(rest % hkv);
-    const int32_t j = tok_lo + (int32_t)(rest / hkv);
+    const int h0 = (int)(rest % groups) * hpt;
+    const int32_t j = tok_lo + (int32_t)(rest / groups);
     const int pg = j / kPage - mb.first_page, slot = j % kPage;
-    const size_t src = (((size_t)mb.src[pg] * hkv + h) * kPage + slot) * D;
-    const size_t dst = (((size_t)mb.dst[pg] * hkv + h) * kPage + slot) * D;
-    float lo[EPL], hi[EPL];
-    unpack16<T>(*reinterpret_cast<const uint4 *>(k_pool + src + c * EPL), lo);
-    unpack16<T>(*reinterpret_cast<const uint4 *>(k_pool + src + D / 2 + c * EPL), hi);
+    // the two rotations' angles, once per token and chunk for the thread's kv heads
+    float c0[EPL], s0[EPL], c1[EPL], s1[EPL];
 #pragma unroll
     for (int e = 0; e < EPL; ++e) {
-      float cs, sn;
-      rope_cos_sin(-(int64_t)j, turn[c * EPL + e], cs, sn);   // reset to position 0
-      const float x = lo[e] * cs - hi[e] * sn, y = lo[e] * sn + hi[e] * cs;
-      rope_cos_sin((int64_t)offset + j, turn[c * EPL + e], cs, sn);  // to the target position
-      lo[e] = x * cs - y * sn;
-      hi[e] = x * sn + y * cs;
+      rope_cos_sin(-(int64_t)j, turn[c * EPL + e], c0[e], s0[e]);          // back to position 0
+      rope_cos_sin((int64_t)offset + j, turn[c * EPL + e], c1[e], s1[e]);  // to the target
     }
-    *reinterpret_cast<uint4 *>(k_pool + dst + c * EPL) = pack16<T>(lo);
-    *reinterpret_cast<uint4 *>(k_pool + dst + D / 2 + c * EPL) = pack16<T>(hi);
-    *reinterpret_cast<uint4 *>(v_pool + dst + c * EPL) =
-        *reinterpret_cast<const uint4 *>(v_pool + src + c * EPL);
-    *reinterpret_cast<uint4 *>(v_pool + dst + D / 2 + c * EPL) =
-        *reinterpret_cast<const uint4 *>(v_pool + src + D / 2 + c * EPL);
+#pragma unroll 2
+    for (int h = h0; h < h0 + hpt; ++h) {
+      const size_t src = (((size_t)mb.src[pg] * hkv + h) * kPage + slot) * D;
+      const size_t dst = (((size_t)mb.dst[pg] * hkv + h) * kPage + slot) * D;
+      const uint4 ka = *reinterpret_cast<const uint4 *>(k_pool + src + c * EPL);
+      const uint4 kb = *reinterpret_cast<const uint4 *>(k_pool + src + D / 2 + c * EPL);
+      const uint4 va = *reinterpret_cast<const uint4 *>(v_pool + src + c * EPL);
+      const uint4 vb = *reinterpret_cast<const uint4 *>(v_pool + src + D / 2 + c * EPL);
+      float lo[EPL], hi[EPL];
+      unpack16<T>(ka, lo);
+      unpack16<T>(kb, hi);
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) {
+        const float x = lo[e] * c0[e] - hi[e] * s0[e], y = lo[e] * s0[e] + hi[e] * c0[e];
+        lo[e] = x * c1[e] - y * s1[e];
+        hi[e] = x * s1[e] + y * c1[e];
+      }
+      *reinterpret_cast<uint4 *>(k_pool + dst + c * EPL) = pack16<T>(lo);
+      *reinterpret_cast<uint4 *>(k_pool + dst + D / 2 + c * EPL) = pack16<T>(hi);
+      *reinterpret_cast<uint4 *>(v_pool + dst + c * EPL) = va;
+      *reinterpret_cast<uint4 *>(v_pool + dst + D / 2 + c * EPL) = vb;
+    }
   }
 }
 
@@ -171,12 +202,14 @@ template <typename T, int D>
 int launch_materialise(lazy_pool *p, int32_t tok_lo, int32_t n_tokens, int32_t offset,
                        const MatBlocks &mb, cudaStream_t s) {
   constexpr int EPL = 16 / (int)sizeof(T);
-  const int64_t total = (int64_t)n_tokens * p->hkv * ((D / 2) / EPL);
+  const int64_t rows = (int64_t)n_tokens * ((D / 2) / EPL);
+  const int hpt = heads_per_thread(p, rows);
+  const int64_t total = rows * (p->hkv / hpt);
   const int threads = 256;
   const int64_t want = (total + threads - 1) / threads;
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)p->num_sms * 16));
   materialise_kernel<T, D><<<grid, threads, 0, s>>>((T *)p->k, (T *)p->v, p->d_turn, p->hkv,
-                                                   tok_lo, n_tokens, offset, mb);
+                                                   hpt, tok_lo, n_tokens, offset, mb);
   LAZY_CUDA_TRY(cudaGetLastError());
   return LAZY_OK;
 }
