@@ -2,8 +2,8 @@
 
 Headline (the ``value`` of the JSON line): decode KV GB/s on the decode-step workload
 (64 requests x 8 Zipf(1.0) docs of 512 tokens + 65-token private segment, 32/8/128 bf16, RoPE
-base 5e5, page size 16), each request's segments in the aligned order (documents shared by
-several requests at the same index). One step = append each request's new token to its private
+base 5e5, page size 16), each request's segments in the phase-aligned order (a document shared
+by several requests placed where the decode's warps reach it at about the same time). One step = append each request's new token to its private
 segment (kv_pool_write_tokens) + lazy_attn_decode (split-KV kernel + log-sum-exp combine).
 GB/s counts the logical K+V bytes each request attends (4096 B per key). Before every timed step
 the L2 is flushed: a 512 MB write, then a 512 MB read, so that shared documents come from HBM
@@ -436,7 +436,7 @@ def bench_long_decode_only(args):
     lwl = W.long_decode_workload()
     lsrc = H.DeviceSource(lwl)
     lres = H.build_resident(lwl, lsrc)
-    ldb = H.decode_batch(lwl, lres, lsrc, align_shared=True)
+    ldb = H.decode_batch(lwl, lres, lsrc, phase_order=True)
     lws = torch.empty(pk.lazy_decode_workspace_bytes(lres.pool, lwl.batch, lwl.Hq),
                       dtype=torch.uint8, device="cuda")
     lout = torch.empty_like(ldb.q)
@@ -481,9 +481,11 @@ def bench_ours(args):
     wl = W.decode_workload()
     src = H.DeviceSource(wl)
     res = H.build_resident(wl, src)
-    # each request's segments ordered so that shared documents line up across the batch (the
-    # attention result does not depend on page order); the context order is timed as a control
-    db = H.decode_batch(wl, res, src, align_shared=True)
+    # each request's segments in the phase-aligned order: the decode's warps read a document
+    # shared by several requests at about the same time (the attention result does not depend
+    # on page order); the index-aligned and the context order are timed as controls
+    db = H.decode_batch(wl, res, src, phase_order=True)
+    adb = H.decode_batch(wl, res, src, align_shared=True)
     cdb = H.decode_batch(wl, res, src)
     per_tok = wl.kv_bytes_per_token()
     kv_bytes = db.n_keys * per_tok  # K and V, 4096 B per key of every request's context
@@ -503,17 +505,29 @@ def bench_ours(args):
         pk.lazy_attn_decode(res.pool, cdb.q, cdb.q_pos, cdb.words, cdb.cu_pages,
                             sm_scale=wl.sm_scale, out=out, lse=lse, workspace=workspace)
 
-    # the shared-segment path over the same tables (control): its plan is host data rebuilt
-    # from the page tables; its build time is reported beside it
+    def aligned_order_call():
+        pk.lazy_attn_decode(res.pool, adb.q, adb.q_pos, adb.words, adb.cu_pages,
+                            sm_scale=wl.sm_scale, out=out, lse=lse, workspace=workspace)
+
+    t_order = time.perf_counter()
+    pk.order_segments_by_phase(
+        [[(res.doc_blocks[d], o, wl.doc_len) for d, o in zip(r.docs, r.offsets)] +
+         [(res.priv_blocks[r.index], r.priv_offset, r.priv_len)] for r in wl.requests],
+        *pk.lazy_decode_partition(res.pool, wl.Hq))
+    order_host_ms = (time.perf_counter() - t_order) * 1e3
+
+    # the shared-segment path over the index-aligned tables (control): its plan is host data
+    # rebuilt from the page tables; its build time is reported beside it
     t_plan = time.perf_counter()
-    plan_h = pk.lazy_decode_shared_plan(words_h, db.cu_pages.cpu().numpy())
+    plan_h = pk.lazy_decode_shared_plan(adb.words.cpu().numpy().view(np.uint64),
+                                        adb.cu_pages.cpu().numpy())
     plan_host_ms = (time.perf_counter() - t_plan) * 1e3
     plan = plan_h.to("cuda")
     sws = torch.empty(pk.lazy_decode_shared_workspace_bytes(res.pool, plan.n_units, wl.Hq),
                       dtype=torch.uint8, device="cuda")
 
     def shared_call():
-        pk.lazy_attn_decode_shared(res.pool, db.q, db.q_pos, plan, sm_scale=wl.sm_scale,
+        pk.lazy_attn_decode_shared(res.pool, adb.q, adb.q_pos, plan, sm_scale=wl.sm_scale,
                                    out=out, lse=lse, workspace=sws)
 
     def step():
@@ -598,7 +612,7 @@ def bench_ours(args):
         lwl = W.long_decode_workload()
         lsrc = H.DeviceSource(lwl)
         lres = H.build_resident(lwl, lsrc)
-        ldb = H.decode_batch(lwl, lres, lsrc, align_shared=True)
+        ldb = H.decode_batch(lwl, lres, lsrc, phase_order=True)
         lws = torch.empty(pk.lazy_decode_workspace_bytes(lres.pool, lwl.batch, lwl.Hq),
                           dtype=torch.uint8, device="cuda")
         lout = torch.empty_like(ldb.q)
@@ -619,6 +633,7 @@ def bench_ours(args):
     torch.cuda.synchronize()
     for _ in range(args.warmup):
         flush(); step(); e2e_step(); no_reuse_call(); context_order_call(); shared_call()
+        aligned_order_call()
         if not only_decode:
             prefill_call(); long_call()
     torch.cuda.synchronize()
@@ -637,6 +652,7 @@ def bench_ours(args):
     e2e_ms = _timed_steps(e2e_step, args.steps, flush, stream)
     nr_ms = _timed_steps(no_reuse_call, args.steps, flush, stream)
     co_ms = _timed_steps(context_order_call, args.steps, flush, stream)
+    al_ms = _timed_steps(aligned_order_call, args.steps, flush, stream)
     sh_ms = _timed_steps(shared_call, args.steps, flush, stream)
     wo_ms = _timed_steps(decode_call, args.steps, flush_write_only, stream)
     if not only_decode:
@@ -692,7 +708,8 @@ def bench_ours(args):
                    "keys_per_step": db.n_keys, "kv_bytes_per_step": kv_bytes,
                    "unique_kv_bytes_per_step": uniq_bytes,
                    "l2": "flushed before every timed step: 512 MB write, then 512 MB read",
-                   "decode_path": "lazy_attn_decode over the aligned page tables",
+                   "decode_path": "lazy_attn_decode over the phase-aligned page tables",
+                   "order_host_ms": round(order_host_ms, 3),
                    "parallelism": f"replicas x{ws}"},
         "gpu_launches": launches_per_step * args.steps,
         "roofline": roofline,
@@ -704,9 +721,14 @@ def bench_ours(args):
                         "(no page shared, logical bytes = DRAM bytes)",
             "value": round(rate(n_bytes, nr_avg), 2), "unit": "GB/s",
             "ms_per_call": round(nr_avg, 5), "frac": round(rate(n_bytes, nr_avg) / hbm_peak, 4)},
+        "decode_aligned_order": {
+            "workload": "decode_b64 through lazy_attn_decode with shared documents at the same "
+                        "index of every request (index-aligned order)",
+            "value": round(rate(kv_bytes, med(al_ms)), 2),
+            "unit": "GB/s", "ms_per_call": round(med(al_ms), 5)},
         "decode_shared_plan": {
-            "workload": "decode_b64, aligned order, through lazy_attn_decode_shared (identical "
-                        "document segments of two requests paired in one fragment)",
+            "workload": "decode_b64, index-aligned order, through lazy_attn_decode_shared "
+                        "(identical document segments of two requests paired in one fragment)",
             "value": round(rate(kv_bytes, med(sh_ms)), 2), "unit": "GB/s",
             "ms_per_call": round(med(sh_ms), 5), "plan_units": plan.n_units,
             "plan_entries": plan_h.n_entries, "plan_host_ms": round(plan_host_ms, 3),
@@ -742,7 +764,7 @@ def bench_ours(args):
         ltr = _traffic("long_decode_b16")
         line["long_decode"] = {
             "workload": "long_decode_b16: 16 req x 131073 keys (64 Zipf(1.2) docs x 2048 + 1), "
-                        "aligned page tables, lazy_attn_decode",
+                        "phase-aligned page tables, lazy_attn_decode",
             "value": round(rate(l_bytes, long_avg), 2), "unit": "GB/s",
             "tokens_per_s": round(lwl.batch / (long_avg * 1e-3), 1),
             "ms_per_step": round(long_avg, 4), "ms_dist": _dist_ms(long_ms),
@@ -847,7 +869,7 @@ def mixed_sweep(args, flush, stream, hbm_peak):
         src = H.DeviceSource(wl)
         res = H.build_resident(wl, src)
         pb = H.prefill_batch(wl, res, src)
-        db = H.decode_batch(wl, res, src, align_shared=True)
+        db = H.decode_batch(wl, res, src, phase_order=True)
         ws = torch.empty(pk.lazy_decode_workspace_bytes(res.pool, len(db.reqs), wl.Hq),
                          dtype=torch.uint8, device="cuda")
         dout = torch.empty_like(db.q)
@@ -918,7 +940,7 @@ def materialised_bench(args, flush, stream, hbm_peak, tc_peak):
         src = H.DeviceSource(wl)
         res = H.build_resident(wl, src, resident_pool=False,
                                extra_blocks=H.materialised_blocks_needed(wl))
-        db = H.decode_batch(wl, res, src, align_shared=True)
+        db = H.decode_batch(wl, res, src, phase_order=True)
         torch.cuda.synchronize()
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
         ev[0].record(stream)
@@ -1249,22 +1271,24 @@ def alibi_bench(args, flush, stream, hbm_peak, tc_peak):
 
 # DRAM traffic of the decode kernel, one captured launch per workload (ncu, --clock-control
 # none), kept in profiles/TRAFFIC_FILE and reported only while the kernel's sources still hash to
-# the recorded value. Capture: run the workload's command below with the CSV path in place of
+# the recorded value. decode_b64's capture skips the five decode launches of the first warm-up
+# iteration (headline step, e2e step, no-reuse, context-order and index-aligned controls) and
+# takes the second iteration's headline step. Capture: run the workload's command below with the CSV path in place of
 # {csv}, then `python bench.py --record-traffic NAME CSV`.
 TRAFFIC_FILE = "decode_traffic.json"
 TRAFFIC_SOURCES = ("decode.cu", "lazy_common.cuh")
 TRAFFIC_RUNS = {
     "decode_b64": {
-        "workload": "decode_b64 (64 req x 4161 keys, Hq32/Hkv8/D128 bf16), aligned page tables, "
-                    "lazy_attn_decode",
+        "workload": "decode_b64 (64 req x 4161 keys, Hq32/Hkv8/D128 bf16), phase-aligned page "
+                    "tables, lazy_attn_decode",
         "kernel": "decode_mma_kernel",
         "command": "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,"
-                   "gpu__time_duration.sum --clock-control none -k regex:decode_mma_kernel -s 4 "
+                   "gpu__time_duration.sum --clock-control none -k regex:decode_mma_kernel -s 5 "
                    "-c 1 --csv --log-file {csv} python bench.py --only decode --steps 3 "
                    "--warmup 3 --no-cpu-baseline"},
     "long_decode_b16": {
-        "workload": "long_decode_b16 (16 req x 131073 keys, Hq32/Hkv8/D128 bf16), aligned page "
-                    "tables, lazy_attn_decode",
+        "workload": "long_decode_b16 (16 req x 131073 keys, Hq32/Hkv8/D128 bf16), phase-aligned "
+                    "page tables, lazy_attn_decode",
         "kernel": "decode_mma_kernel",
         "command": "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,"
                    "gpu__time_duration.sum --clock-control none -k regex:decode_mma_kernel -s 4 "

@@ -313,6 +313,37 @@ int lazy_attn_decode_noalloc(lazy_pool *pool, const void *d_q, const int32_t *d_
                              int32_t batch, int32_t num_q_heads, float sm_scale,
                              int32_t grid_ctas, void *d_out, float *d_lse, lazy_stream_t stream);
 
+/*
+ * How lazy_attn_decode (and lazy_attn_decode_noalloc) partitions its work for this pool, head
+ * count and grid_ctas (0 = the default grid): the flattened (request, unit, page) sequence, with
+ * *units_per_request units per request (kv heads, or virtual heads of up to 8 query heads), is
+ * cut into *ranges equal contiguous ranges that run side by side. For lazy_order_segments.
+ */
+int lazy_decode_partition(lazy_pool *pool, int32_t num_q_heads, int32_t grid_ctas,
+                          int32_t *units_per_request, int64_t *ranges);
+/*
+ * Host scheduling helper: an order of each request's segments under which the decode reads a
+ * document shared by several requests at nearly the same time, so that its pages come from DRAM
+ * once and from L2 for the other requests (the result does not depend on the order; only the
+ * DRAM traffic does). Page x of the flattened sequence is read at about step x mod R of its
+ * range, R = units_per_request * (all pages) / ranges; the helper places each shared segment,
+ * most used first, in the slot of every request holding it whose step is closest to a common
+ * target, summed over the request's units.
+ *   cu_segs      host int32 [batch + 1]: request b's segments are cu_segs[b] .. cu_segs[b+1]-1
+ *   seg_key      host int64 [n]: equal keys = the same cached segment (e.g. its first block id)
+ *   seg_pages    host int32 [n]: pages of each segment (its page words)
+ *   pinned       host uint8 [n]: 1 = keep after the movable segments (a private tail)
+ *   units_per_request, ranges: from lazy_decode_partition
+ *   perm         host int32 [n] out: for each request, the segment index (within the request)
+ *                placed at each position
+ * Requests whose movable segments have different page counts keep their order (pinned
+ * segments still go last). LAZY_ERR_INVALID_ARG on a null pointer, a decreasing cu_segs or a
+ * negative page count.
+ */
+int lazy_order_segments(int32_t batch, const int32_t *cu_segs, const int64_t *seg_key,
+                        const int32_t *seg_pages, const uint8_t *pinned,
+                        int32_t units_per_request, int64_t ranges, int32_t *perm);
+
 /* ---------------------------------------------------------------------------------------
  * Shared-segment decode (the summaries' core concept carried into decode: one cached copy of a
  * document serves every request at its own offset, so requests holding the same document can

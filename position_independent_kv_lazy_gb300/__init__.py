@@ -50,6 +50,7 @@ EXPORTS = [
     "kv_pool_write_tokens", "kv_pool_materialise", "lazy_pack_page", "lazy_unpack_page",
     "lazy_pack_pages",
     "lazy_pack_segment", "lazy_decode_workspace_bytes", "lazy_attn_decode",
+    "lazy_decode_partition", "lazy_order_segments",
     "lazy_prefill_workspace_bytes",
     "lazy_attn_prefill", "lazy_get_device_error", "lazy_debug_gather", "lazy_debug_wait_timeout",
     "lazy_attn_decode_noalloc", "lazy_attn_prefill_append",
@@ -108,6 +109,11 @@ _SIGS = {
     "lazy_pack_segment": ([_pu32, _i32, ctypes.c_uint32, _i32, _i32, _i32, _pu64, _i32, _pi32],
                           ctypes.c_int),
     "lazy_decode_workspace_bytes": ([_vp, _i32, _i32, _i32, _psz], ctypes.c_int),
+    "lazy_decode_partition": ([_vp, _i32, _i32, _pi32, ctypes.POINTER(ctypes.c_int64)],
+                              ctypes.c_int),
+    "lazy_order_segments": ([_i32, _pi32, ctypes.POINTER(ctypes.c_int64), _pi32,
+                             ctypes.POINTER(ctypes.c_uint8), _i32, ctypes.c_int64, _pi32],
+                            ctypes.c_int),
     "lazy_attn_decode": ([_vp, _vp, _vp, _vp, _vp, _i32, _i32, _f32, _i32, _vp, _vp, _vp,
                           ctypes.c_size_t, _vp], ctypes.c_int),
     "lazy_prefill_workspace_bytes": ([_vp, _i32, _i32, _i32, _i32, _i32, _psz], ctypes.c_int),
@@ -363,6 +369,43 @@ def align_shared_segments(requests: Sequence[Sequence[Tuple[Sequence[int], int, 
         order = [i if i is not None else next(rest) for i in placed[b]]
         out.append([segs[i] for i in order])
     return out
+
+
+def lazy_decode_partition(pool: LazyPool, num_q_heads: int, grid_ctas: int = 0):
+    """(units per request, ranges) of the decode's work partition (see the C header)."""
+    u = ctypes.c_int32()
+    r = ctypes.c_int64()
+    _check("lazy_decode_partition", load_library().lazy_decode_partition(
+        pool.handle, num_q_heads, grid_ctas, ctypes.byref(u), ctypes.byref(r)))
+    return u.value, r.value
+
+
+def order_segments_by_phase(requests: Sequence[Sequence[Tuple[Sequence[int], int, int]]],
+                            units_per_request: int, ranges: int, page_size: int = 16,
+                            pin_last: bool = True) -> List[List[Tuple[Sequence[int], int, int]]]:
+    """Reorder each request's segments (block_ids, offset, length) with lazy_order_segments:
+    a segment is identified by its first block id; with ``pin_last`` each request's last
+    segment (its private tail) stays last. The attention does not change; the decode reads a
+    shared document's pages for all its requests at about the same time."""
+    cu, keys, pages, pin = [0], [], [], []
+    for segs in requests:
+        for i, (ids, _, length) in enumerate(segs):
+            keys.append(int(ids[0]) if len(ids) else -1 - len(keys))
+            pages.append((int(length) + page_size - 1) // page_size)
+            pin.append(1 if (pin_last and i == len(segs) - 1) else 0)
+        cu.append(len(keys))
+    n = len(keys)
+    cu_a = np.asarray(cu, dtype=np.int32)
+    key_a = np.asarray(keys, dtype=np.int64)
+    pg_a = np.asarray(pages, dtype=np.int32)
+    pin_a = np.asarray(pin, dtype=np.uint8)
+    perm = np.zeros(max(n, 1), dtype=np.int32)
+    _check("lazy_order_segments", load_library().lazy_order_segments(
+        len(requests), cu_a.ctypes.data_as(_pi32), key_a.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+        pg_a.ctypes.data_as(_pi32), pin_a.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)),
+        units_per_request, ranges, perm.ctypes.data_as(_pi32)))
+    return [[segs[int(perm[cu[b] + i])] for i in range(len(segs))]
+            for b, segs in enumerate(requests)]
 
 
 def build_page_table(requests: Sequence[Sequence[Tuple[Sequence[int], int, int]]],

@@ -1566,6 +1566,26 @@ extern "C" int lazy_decode_workspace_bytes(lazy_pool *p, int32_t batch, int32_t 
   return LAZY_OK;
 }
 
+extern "C" int lazy_decode_partition(lazy_pool *p, int32_t num_q_heads, int32_t grid_ctas,
+                                     int32_t *units_per_request, int64_t *ranges) {
+  if (!p || !units_per_request || !ranges || grid_ctas < 0) return LAZY_ERR_INVALID_ARG;
+  int32_t gc, chunks;
+  int rc = plan_groups(num_q_heads, p->hkv, &gc, &chunks);
+  if (rc != LAZY_OK) return rc;
+  rc = ensure_device(p);
+  if (rc != LAZY_OK) return rc;
+  int grid;
+  rc = decode_grid(p, gc, chunks, grid_ctas, &grid);
+  if (rc != LAZY_OK) return rc;
+  // the group kernel (chunks of 8 heads sharing a CTA's page ring) cuts (request, kv head)
+  // units into one range per CTA; every other decode kernel cuts (request, virtual head) units
+  // into one range per warp
+  const bool grouped = use_mma(p) && gc == 8 && chunks == kWarps;
+  *units_per_request = grouped ? p->hkv : p->hkv * chunks;
+  *ranges = grouped ? (int64_t)grid : (int64_t)grid * kWarps;
+  return LAZY_OK;
+}
+
 extern "C" int lazy_attn_decode(lazy_pool *p, const void *q, const int32_t *q_pos,
                                 const uint64_t *words, const int32_t *cu_pages, int32_t batch,
                                 int32_t num_q_heads, float sm_scale, int32_t grid_ctas, void *out,

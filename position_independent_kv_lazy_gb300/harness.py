@@ -11,7 +11,7 @@ from typing import Dict, List, Optional
 import numpy as np
 
 from . import (LazyPool, build_page_table, kv_pool_alloc, kv_pool_insert_doc,
-               kv_pool_materialise)
+               kv_pool_materialise, lazy_decode_partition, order_segments_by_phase)
 
 
 def _torch_dtype(wl):
@@ -145,13 +145,21 @@ def build_resident(wl, src, device="cuda", resident_pool: bool = True, stream=No
     return Resident(pool, doc_blocks, priv_blocks)
 
 
-def page_table(wl, res: Resident, reqs, with_private: bool, align_shared: bool = False):
+def page_table(wl, res: Resident, reqs, with_private: bool, align_shared: bool = False,
+               phase=None):
+    """Page words of the requests' documents (and private segments). ``align_shared``: shared
+    documents at the same index of every request; ``phase`` = (units per request, ranges) of
+    the decode's partition: the phase-aligned order of order_segments_by_phase instead."""
     segs = []
     for r in reqs:
         s = [(res.doc_blocks[d], o, wl.doc_len) for d, o in zip(r.docs, r.offsets)]
         if with_private:
             s.append((res.priv_blocks[r.index], r.priv_offset, r.priv_len))
         segs.append(s)
+    if phase is not None:
+        segs = order_segments_by_phase(segs, phase[0], phase[1], wl.page_size,
+                                       pin_last=with_private)
+        align_shared = False
     return build_page_table(segs, wl.page_size, page_positions=res.pool.alibi_slopes is not None,
                             align_shared=align_shared)
 
@@ -172,12 +180,17 @@ class DecodeBatch:
 
 
 def decode_batch(wl, res: Resident, src, device="cuda", reqs=None,
-                 align_shared: bool = False) -> DecodeBatch:
+                 align_shared: bool = False, phase_order: bool = False,
+                 grid_ctas: int = 0) -> DecodeBatch:
     """The batch's decode inputs. ``align_shared`` orders each request's segments so that
-    shared documents sit at the same index in every request (see align_shared_segments)."""
+    shared documents sit at the same index in every request (see align_shared_segments);
+    ``phase_order`` so that the decode (default grid, or ``grid_ctas``) reads them at about the
+    same time (see order_segments_by_phase)."""
     import torch
     reqs = reqs if reqs is not None else wl.decode_requests()
-    words, cu = page_table(wl, res, reqs, with_private=True, align_shared=align_shared)
+    phase = lazy_decode_partition(res.pool, wl.Hq, grid_ctas) if phase_order else None
+    words, cu = page_table(wl, res, reqs, with_private=True, align_shared=align_shared,
+                           phase=phase)
     q = torch.cat([src.q(r.index, device) for r in reqs], dim=0).contiguous()
     q_pos = torch.tensor([r.m for r in reqs], dtype=torch.int32, device=device)
     nk, nv, slots, lpos = [], [], [], []

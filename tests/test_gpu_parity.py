@@ -133,15 +133,18 @@ def test_decode_aligned_page_order_parity(pk):
     _check_decode(wl, out.float().cpu().numpy(), lse.cpu().numpy())
 
 
-def test_decode_aligned_order_full_size_matches_context_order(pk):
-    # decode_b64 in both page orders: only the summation order differs
+@pytest.mark.parametrize("order", ["aligned", "phase"])
+def test_decode_ordered_full_size_matches_context_order(pk, order):
+    # decode_b64 in the context order and in the index- or phase-aligned order: only the
+    # summation order differs
     H = _h()
     wl = W.decode_workload()
     src = H.DeviceSource(wl)
     res = H.build_resident(wl, src)
     res_out = []
-    for align in (False, True):
-        db = H.decode_batch(wl, res, src, align_shared=align)
+    for ordered in (False, True):
+        db = H.decode_batch(wl, res, src, align_shared=ordered and order == "aligned",
+                            phase_order=ordered and order == "phase")
         o, l = pk.lazy_attn_decode(res.pool, db.q, db.q_pos, db.words, db.cu_pages,
                                    sm_scale=wl.sm_scale)
         torch.cuda.synchronize()
@@ -331,12 +334,13 @@ def test_decode_after_token_append(pk):
 
 
 def test_decode_full_size_sampled(pk):
-    # 64 requests x 4161 keys, 32/8/128 bf16, in the bench's launch configuration
+    # 64 requests x 4161 keys, 32/8/128 bf16, in the bench's launch configuration (default grid,
+    # phase-aligned page order)
     H = _h()
     wl = W.decode_workload()
     src = H.DeviceSource(wl)
     res = H.build_resident(wl, src, drop_raw=False)
-    db = H.decode_batch(wl, res, src)
+    db = H.decode_batch(wl, res, src, phase_order=True)
     out, lse = pk.lazy_attn_decode(res.pool, db.q, db.q_pos, db.words, db.cu_pages,
                                    sm_scale=wl.sm_scale)
     torch.cuda.synchronize()
@@ -348,19 +352,21 @@ def test_decode_full_size_sampled(pk):
 
 
 def test_long_decode_full_size_sampled(pk):
-    # 16 requests x 131073 keys (64 docs of 2048), split-KV across the whole GPU
+    # 16 requests x 131073 keys (64 docs of 2048), split-KV across the whole GPU, phase-aligned
+    # page order as the bench runs it: 3 requests x 2 kv heads
     H = _h()
     wl = W.long_decode_workload()
     src = H.DeviceSource(wl)
     res = H.build_resident(wl, src, drop_raw=False)
-    db = H.decode_batch(wl, res, src)
+    db = H.decode_batch(wl, res, src, phase_order=True)
     out, lse = pk.lazy_attn_decode(res.pool, db.q, db.q_pos, db.words, db.cu_pages,
                                    sm_scale=wl.sm_scale)
     torch.cuda.synchronize()
     assert pk.lazy_get_device_error(res.pool) == 0
     out = out.float().cpu().numpy()
     lse = lse.cpu().numpy()
-    _check_decode(wl, out[[9]], lse[[9]], reqs=[9], kv_heads=[3], src=src.host_view())
+    reqs = [2, 9, 15]
+    _check_decode(wl, out[reqs], lse[reqs], reqs=reqs, kv_heads=[3, 6], src=src.host_view())
 
 
 # ------------------------------------------------------------------ device-detected errors
@@ -619,7 +625,7 @@ def test_mixed_step_full_size_sampled(pk, alpha):
     src = H.DeviceSource(wl)
     res = H.build_resident(wl, src, drop_raw=False)
     pb = H.prefill_batch(wl, res, src)
-    db = H.decode_batch(wl, res, src, align_shared=True)
+    db = H.decode_batch(wl, res, src, phase_order=True)
     pout, plse = pk.lazy_attn_prefill(res.pool, pb.q, pb.k_new, pb.v_new, pb.cu_q, pb.q_pos0,
                                       pb.words, pb.cu_pages, pb.max_q_len, sm_scale=wl.sm_scale)
     pk.kv_pool_write_tokens(res.pool, db.new_k, db.new_v, db.slot_mapping, db.local_pos)
