@@ -13,14 +13,15 @@
 //               box, otherwise 8 page boxes (16 rows x 64 dims, 128B swizzle); question keys by
 //               128-token boxes.
 //   warp 1      TMEM owner (512 columns) and single-thread tcgen05.mma issuer:
-//               S_i = Q_i K^T (SS), then O_i += P_i V (P from TMEM, V MN-major).
+//               S_i = Q_i K^T (SS; fp16 operands written by the rotation passes, bf16 in the
+//               ALiBi mode), then O_i += P_i V (bf16; P from TMEM, V MN-major).
 //   warps 4-7   softmax of Q tile 0, warps 8-11 of Q tile 1 (TMEM lane quadrant = warp % 4):
 //               each thread holds its row's 128 scores, online softmax in the log2 domain with
 //               a lazy rescale (the running max only moves when the tile max exceeds it by more
 //               than 8), P written back into S's TMEM columns as bf16 pairs. The same 256 threads
 //               rotate their Q rows once and each K tile in shared memory, in place (the pair
 //               (i, i+64) sits at the same swizzled offset of the two 64-dim boxes), two tiles
-//               ahead of the scores that need it.
+//               ahead of the scores that need it: fp32 arithmetic, rounded once to fp16.
 // The softmax loop is kept compact (one shared angle routine, one code path for masked and full
 // tiles): with per-site copies the kernel was instruction-fetch bound.
 // TMEM: S_0 [0,128) S_1 [128,256) O_0 [256,384) O_1 [384,512) fp32 columns.
