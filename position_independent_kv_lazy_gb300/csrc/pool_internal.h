@@ -42,6 +42,8 @@ struct lazy_pool {
   alignas(64) unsigned char tmap_v[128];
   alignas(64) unsigned char tmap_k8[128];  // 4-D view: 8 consecutive blocks of one kv head
   alignas(64) unsigned char tmap_v8[128];
+  alignas(64) unsigned char tmap_k3[128];  // 3-D view: one whole page per box
+  alignas(64) unsigned char tmap_v3[128];
 };
 
 namespace lazy {
@@ -51,6 +53,8 @@ int ensure_device(lazy_pool *p);
 // TMA tensor maps of the page buffers (bf16, head_dim 128, 128-byte swizzle), built once:
 //   tmap_k / tmap_v    2-D, rows (block * Hkv + h) * 16 + slot, box 16 rows x 64 dims
 //   tmap_k8 / tmap_v8  4-D [block][kv head][slot][dim], box 8 blocks x 1 head x 16 x 64
+//   tmap_k3 / tmap_v3  3-D (64 dims, rows, 2 halves of 128 B), box 64 x 16 x 2: one page in one
+//                      copy, landing as the two 16 x 64 boxes of the 2-D view, half-major
 // LAZY_ERR_UNSUPPORTED for other pools.
 int ensure_pool_tmaps(lazy_pool *p);
 inline size_t elem_bytes(int32_t dtype) { return dtype == LAZY_DTYPE_BF16 ? 2 : 4; }

@@ -1220,6 +1220,15 @@ int ensure_pool_tmaps(lazy_pool *p) {
   if (rc != LAZY_OK) return rc;
   rc = make_map(reinterpret_cast<CUtensorMap *>(p->tmap_v8), p->v, 4, dims4, strides4, box4);
   if (rc != LAZY_OK) return rc;
+  // one page per box: the halves (dims 0-63, 64-127) are an outer dimension of stride 128 B, so
+  // the box lands half-major, exactly as two boxes of the 2-D view would
+  const cuuint64_t dims3[3] = {64, (cuuint64_t)p->num_blocks * p->hkv * kPage, 2};
+  const cuuint64_t strides3[2] = {256, 128};
+  const cuuint32_t box3[3] = {64, (cuuint32_t)kPage, 2};
+  rc = make_map(reinterpret_cast<CUtensorMap *>(p->tmap_k3), p->k, 3, dims3, strides3, box3);
+  if (rc != LAZY_OK) return rc;
+  rc = make_map(reinterpret_cast<CUtensorMap *>(p->tmap_v3), p->v, 3, dims3, strides3, box3);
+  if (rc != LAZY_OK) return rc;
   p->tmaps_ready = true;
   return LAZY_OK;
 }
