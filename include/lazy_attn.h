@@ -259,7 +259,9 @@ int lazy_pack_segment(const uint32_t *block_ids, int32_t n_blocks, uint32_t offs
  *                [batch+1], nondecreasing, d_cu_pages[0] = 0). Word order within a request
  *                does not change the result, only how often q is re-rotated.
  *   sm_scale     score scale (1/sqrt(head_dim) for standard attention)
- *   grid_ctas    0 = one persistent wave sized to the GPU; otherwise that many CTAs
+ *   grid_ctas    0 = one persistent wave sized to the GPU; otherwise that many CTAs. Either is
+ *                raised to at least ceil(virtual heads / 4) CTAs (virtual heads = num_kv_heads x
+ *                ceil(G / 8)), so that no warp's share of the pages reaches 2^31.
  *   d_out        device [batch][num_q_heads][head_dim], pool dtype, 16-byte aligned
  *   d_lse        device float [batch][num_q_heads]; -inf (and out = 0) for a request with no keys
  *                d_out and d_lse are written once, by the final merge kernel, and may also be

@@ -705,15 +705,12 @@ __device__ __forceinline__ void mma_flush(MmaWarpState<GC> &st, const DecodePara
 }
 
 // Loads page word w of the tensor-core kernels into stage `st` (K and V, one page-view copy
-// each, landing as two 16 x 64 boxes): bad words are flagged and replaced by block 0 (their keys are masked by the consumer).
+// each, landing as two 16 x 64 boxes). A word whose block is out of range loads block 0; the
+// consumer's warp vote on the same word skips that page and reports it.
 __device__ __forceinline__ void mma_issue_page(const MmaDecodeParams &mp, uint64_t w,
                                                int32_t kv_head, uint8_t *st, uint64_t *bar) {
   const DecodeParams &p = mp.d;
-  uint32_t blk = word_block(w);
-  if (blk >= (uint32_t)p.num_blocks || word_nvalid(w) > (uint32_t)kPage) {
-    set_error(p.err, LAZY_DEVERR_BAD_PAGE);
-    blk = 0;
-  }
+  const uint32_t blk = word_block(w) < (uint32_t)p.num_blocks ? word_block(w) : 0u;
   const int row = (int)((blk * (uint32_t)p.hkv + (uint32_t)kv_head) * kPage);
   mbar_arrive_expect_tx(bar, kMmaStageBytes);
   tma_page_g2s(st, &mp.tm_k, row, bar);
@@ -746,7 +743,6 @@ __global__ void __launch_bounds__(WARPS * 32)
     cudaTriggerProgrammaticLaunchCompletion();
     return;
   }
-  const int64_t n_mine = x1 - x0;
   if (lane == 0) {
     for (int s = 0; s < STAGES; ++s) mbar_init(&bars[s], 1);
     fence_barrier_init();
@@ -757,7 +753,10 @@ __global__ void __launch_bounds__(WARPS * 32)
   prod.init(x0, p.cu_pages, B, HV);
   uint64_t w_next = 0;
   if (lane == 0) w_next = p.words[prod.wbase + prod.pg];
-  int64_t issued = 0;
+  // 32-bit page counters (64-bit ones cost ~3% here): decode_grid gives every launch at least
+  // as many warps as virtual heads, so a warp's range is shorter than the page table (< 2^31)
+  const int32_t n_mine = (int32_t)(x1 - x0);
+  int32_t issued = 0;
   auto issue_next = [&](int s) {
     if (lane == 0) {
       meta_w[s] = w_next;
@@ -774,14 +773,14 @@ __global__ void __launch_bounds__(WARPS * 32)
   MmaWarpState<GC> st;
   int32_t cur_unit = -1;
   bool timed_out = false;
-  for (int64_t i = 0; i < n_mine; ++i) {
-    const int s = (int)(i % STAGES);
+  for (int32_t i = 0; i < n_mine; ++i) {
+    const int s = i % STAGES;
     const uint32_t par = (uint32_t)((i / STAGES) & 1);
     if (!mbar_wait(&bars[s], par, p.wait_ns)) {
       if (lane == 0) set_error(p.err, LAZY_DEVERR_TIMEOUT);
       timed_out = true;
-      const int64_t last = (i + STAGES < n_mine) ? i + STAGES : n_mine;
-      for (int64_t k = i; k < last; ++k)
+      const int32_t last = (i + STAGES < n_mine) ? i + STAGES : n_mine;
+      for (int32_t k = i; k < last; ++k)
         mbar_wait(&bars[k % STAGES], (uint32_t)((k / STAGES) & 1), p.wait_ns);
       break;
     }
@@ -1433,9 +1432,13 @@ int plan_groups(int32_t hq, int32_t hkv, int32_t *gc, int32_t *chunks) {
   return LAZY_OK;
 }
 
+// The decode grid: grid_ctas, or one persistent wave, raised to at least one warp per virtual
+// head. The tensor-core decode counts a warp's pages in 32 bits: N = virtual heads x pages
+// (< 2^31) split over at least virtual-heads warps leaves every range below 2^31.
 int decode_grid(lazy_pool *p, int32_t gc, int32_t chunks, int32_t grid_ctas, int *grid) {
+  const int min_grid = (p->hkv * chunks + kWarps - 1) / kWarps;
   if (grid_ctas > 0) {
-    *grid = grid_ctas;
+    *grid = std::max<int>(grid_ctas, min_grid);
     return LAZY_OK;
   }
   const int per_sm = with_decode_shape(
@@ -1444,7 +1447,7 @@ int decode_grid(lazy_pool *p, int32_t gc, int32_t chunks, int32_t grid_ctas, int
     record_msg("decode kernel occupancy query failed");
     return LAZY_ERR_CUDA;
   }
-  *grid = p->num_sms * per_sm;
+  *grid = std::max<int>(p->num_sms * per_sm, min_grid);
   return LAZY_OK;
 }
 
