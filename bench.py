@@ -807,9 +807,9 @@ def bench_ours(args):
 def encode_bench(args, flush, stream, hbm_peak):
     """Document encode (kv_pool_insert_doc) into blocks the segment already owns, i.e. the K
     rotation at local positions, the V copy and the page scatter, for an 8192-token segment
-    (one launch) and a 65536-token segment (eight launches of 512 pages, 537 MB moved: shows
-    whether the short launch is bound by its tail). Bytes moved = read raw K and V + write
-    both = 8192 B per token (Hkv 8, D 128, bf16)."""
+    and a 65536-token segment (537 MB moved; each is one launch of up to 4096 pages: the large
+    one shows whether the short launch is bound by its tail). Bytes moved = read raw K and V +
+    write both = 8192 B per token (Hkv 8, D 128, bf16)."""
     import torch
 
     import position_independent_kv_lazy_gb300 as pk
@@ -838,7 +838,7 @@ def encode_bench(args, flush, stream, hbm_peak):
         pool.close()
         del k, v
         rec = {"workload": f"one {n_tok}-token segment, Hkv 8, D 128, bf16, into owned blocks "
-                           f"({-(-n_tok // 8192)} launch(es))",
+                           f"({-(-n_tok // 65536)} launch(es))",
                "value": round(moved / (med * 1e-3) / 1e9, 2), "unit": "GB/s",
                "bytes_moved_per_call": moved, "ms_dist": _dist_ms(ms),
                "frac": round(moved / (med * 1e-3) / 1e9 / hbm_peak, 4)}

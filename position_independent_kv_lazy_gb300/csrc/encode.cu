@@ -13,23 +13,31 @@
 namespace lazy {
 namespace {
 
-constexpr int kMaxIdsPerLaunch = 512;
+// A document insert passes its block ids in the launch's parameters: up to 4096 pages (65,536
+// tokens, 16 KB of the 32 KB parameter space) per launch, so a long document is one launch.
+// Inserts of up to 512 pages take a 2 KB list (a 16 KB parameter block costs a short launch
+// about 1 us), and the scattered append (a decode step's tokens, located by a slot map) a
+// one-entry list.
+constexpr int kMaxIdsPerLaunch = 4096;
+constexpr int kSmallIds = 512;
 
+template <int N>
 struct BlockList {
   int32_t first_page;  // page index (within the segment) of ids[0]
   int32_t n;
-  int32_t ids[kMaxIdsPerLaunch];
+  int32_t ids[N];
 };
 
 // One thread = (token, group of hpt kv heads, 16-byte chunk of the lower half): it also handles
 // the matching chunk of the upper half, which holds the rotation partners (pairs (i, i + D/2)).
 // The angles depend only on the position and the frequency, so a thread evaluates them once
 // for its hpt heads (large inserts: several heads per thread; a decode step's few tokens: one).
-template <typename T, int D>
+template <typename T, int D, int NIDS>
 __global__ void __launch_bounds__(256) encode_kernel(
     const T *__restrict__ k_raw, const T *__restrict__ v, int32_t n_tokens, int32_t hkv,
     int32_t hpt, T *__restrict__ k_pool, T *__restrict__ v_pool, const uint64_t *__restrict__ turn,
-    int32_t tok0, int32_t local_pos0, BlockList blocks, const int32_t *__restrict__ slot_map,
+    int32_t tok0, int32_t local_pos0, const __grid_constant__ BlockList<NIDS> blocks,
+    const int32_t *__restrict__ slot_map,
     const int32_t *__restrict__ local_pos, int32_t num_blocks, int32_t *err, int32_t rope) {
   constexpr int EPL = 16 / (int)sizeof(T);
   constexpr int CH = (D / 2) / EPL;
@@ -100,9 +108,9 @@ int heads_per_thread(const lazy_pool *p, int64_t rows) {
   return 1;
 }
 
-template <typename T, int D>
+template <typename T, int D, int NIDS>
 int launch_encode(lazy_pool *p, const void *k_raw, const void *v, int32_t n_tokens, int32_t tok0,
-                  int32_t local_pos0, const BlockList &bl, const int32_t *slot_map,
+                  int32_t local_pos0, const BlockList<NIDS> &bl, const int32_t *slot_map,
                   const int32_t *local_pos, cudaStream_t s) {
   constexpr int EPL = 16 / (int)sizeof(T);
   const int64_t rows = (int64_t)n_tokens * ((D / 2) / EPL);
@@ -111,27 +119,28 @@ int launch_encode(lazy_pool *p, const void *k_raw, const void *v, int32_t n_toke
   const int threads = 256;
   const int64_t want = (total + threads - 1) / threads;
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)p->num_sms * 16));
-  encode_kernel<T, D><<<grid, threads, 0, s>>>(
+  encode_kernel<T, D, NIDS><<<grid, threads, 0, s>>>(
       (const T *)k_raw, (const T *)v, n_tokens, p->hkv, hpt, (T *)p->k, (T *)p->v, p->d_turn, tok0,
       local_pos0, bl, slot_map, local_pos, p->num_blocks, p->d_err, p->alibi ? 0 : 1);
   LAZY_CUDA_TRY(cudaGetLastError());
   return LAZY_OK;
 }
 
+template <int NIDS>
 int dispatch_encode(lazy_pool *p, const void *k_raw, const void *v, int32_t n_tokens,
-                    int32_t tok0, int32_t local_pos0, const BlockList &bl,
+                    int32_t tok0, int32_t local_pos0, const BlockList<NIDS> &bl,
                     const int32_t *slot_map, const int32_t *local_pos, cudaStream_t s) {
   if (p->dtype == LAZY_DTYPE_BF16) {
     if (p->d == 128)
-      return launch_encode<__nv_bfloat16, 128>(p, k_raw, v, n_tokens, tok0, local_pos0, bl,
+      return launch_encode<__nv_bfloat16, 128, NIDS>(p, k_raw, v, n_tokens, tok0, local_pos0, bl,
                                                slot_map, local_pos, s);
-    return launch_encode<__nv_bfloat16, 64>(p, k_raw, v, n_tokens, tok0, local_pos0, bl,
+    return launch_encode<__nv_bfloat16, 64, NIDS>(p, k_raw, v, n_tokens, tok0, local_pos0, bl,
                                             slot_map, local_pos, s);
   }
   if (p->d == 128)
-    return launch_encode<float, 128>(p, k_raw, v, n_tokens, tok0, local_pos0, bl, slot_map,
+    return launch_encode<float, 128, NIDS>(p, k_raw, v, n_tokens, tok0, local_pos0, bl, slot_map,
                                      local_pos, s);
-  return launch_encode<float, 64>(p, k_raw, v, n_tokens, tok0, local_pos0, bl, slot_map,
+  return launch_encode<float, 64, NIDS>(p, k_raw, v, n_tokens, tok0, local_pos0, bl, slot_map,
                                   local_pos, s);
 }
 
@@ -296,18 +305,30 @@ extern "C" int kv_pool_insert_doc(lazy_pool *p, const void *k_raw, const void *v
   }
   cudaStream_t s = (cudaStream_t)stream;
   const int32_t first_page = local_pos0 / kPage, last_page = (int32_t)((end - 1) / kPage);
-  for (int32_t pg = first_page; pg <= last_page; pg += kMaxIdsPerLaunch) {
-    BlockList bl;
-    bl.first_page = pg;
-    bl.n = std::min(kMaxIdsPerLaunch, last_page - pg + 1);
-    for (int i = 0; i < bl.n; ++i) bl.ids[i] = block_ids[pg + i];
-    const int64_t pos_lo = std::max<int64_t>(local_pos0, (int64_t)pg * kPage);
-    const int64_t pos_hi = std::min<int64_t>(end, (int64_t)(pg + bl.n) * kPage);
-    rc = dispatch_encode(p, k_raw, v, (int32_t)(pos_hi - local_pos0) - (int32_t)(pos_lo - local_pos0),
-                         (int32_t)(pos_lo - local_pos0), local_pos0, bl, nullptr, nullptr, s);
-    if (rc != LAZY_OK) return rc;
+  // one parameter block per call (kept off the stack of the caller's thread)
+  const int32_t pages = last_page - first_page + 1;
+  auto run = [&](auto &bl, int32_t max_ids) -> int {
+    for (int32_t pg = first_page; pg <= last_page; pg += max_ids) {
+      bl.first_page = pg;
+      bl.n = std::min(max_ids, last_page - pg + 1);
+      for (int i = 0; i < bl.n; ++i) bl.ids[i] = block_ids[pg + i];
+      const int64_t pos_lo = std::max<int64_t>(local_pos0, (int64_t)pg * kPage);
+      const int64_t pos_hi = std::min<int64_t>(end, (int64_t)(pg + bl.n) * kPage);
+      const int rc2 = dispatch_encode(p, k_raw, v, (int32_t)(pos_hi - pos_lo),
+                                      (int32_t)(pos_lo - local_pos0), local_pos0, bl, nullptr,
+                                      nullptr, s);
+      if (rc2 != LAZY_OK) return rc2;
+    }
+    return LAZY_OK;
+  };
+  if (pages <= kSmallIds) {
+    static thread_local BlockList<kSmallIds> small;
+    rc = run(small, kSmallIds);
+  } else {
+    static thread_local BlockList<kMaxIdsPerLaunch> large;
+    rc = run(large, kMaxIdsPerLaunch);
   }
-  return LAZY_OK;
+  return rc;
 }
 
 // Scattered encode: token t goes to slot_mapping[t] with local position local_pos[t].
@@ -321,9 +342,10 @@ extern "C" int kv_pool_write_tokens(lazy_pool *p, const void *k_raw, const void 
   int rc = ensure_device(p);
   if (rc != LAZY_OK) return rc;
   p->encoded = true;
-  BlockList bl;
+  BlockList<1> bl;  // unused: the slot map locates every token
   bl.first_page = 0;
   bl.n = 0;
+  bl.ids[0] = 0;
   return dispatch_encode(p, k_raw, v, n_tokens, 0, 0, bl, slot_mapping, local_pos,
                          (cudaStream_t)stream);
 }

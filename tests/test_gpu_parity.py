@@ -108,6 +108,38 @@ def test_debug_gather_indexing_bit_exact(pk):
     assert pk.lazy_get_device_error(res.pool) == 0
 
 
+def test_long_document_insert_spans_launches(pk):
+    # A 70,000-token document at local position 37 covers 4,378 pages: more than one launch's
+    # block list (4,096 pages). Sampled rows (the first and last, both sides of the launch
+    # boundary, every 997th) against the oracle: V verbatim, K within one bf16 rounding of R(j) k.
+    n, pos0, hkv, d, base = 70000, 37, 2, 128, 500000.0
+    pool = pk.LazyPool(num_blocks=(pos0 + n + 15) // 16 + 8, num_kv_heads=hkv, head_dim=d,
+                       dtype=torch.bfloat16, rope_base=base)
+    g = torch.Generator(device="cuda").manual_seed(5)
+    k = torch.randn((n, hkv, d), generator=g, device="cuda").to(torch.bfloat16)
+    v = torch.randn((n, hkv, d), generator=g, device="cuda").to(torch.bfloat16)
+    ids = pk.kv_pool_insert_doc(pool, k, v, local_pos0=pos0)
+    torch.cuda.synchronize()
+    assert pk.lazy_get_device_error(pool) == 0
+    assert len(ids) == (pos0 + n + 15) // 16
+    boundary = (pos0 // 16 + 4096) * 16 - pos0  # first token of the second launch
+    sample = sorted(set([0, 1, n - 1] + list(range(boundary - 20, boundary + 20)) +
+                        list(range(0, n, 997))))
+    pos = [pos0 + t for t in sample]
+    blk = torch.tensor([ids[j // 16] for j in pos], device="cuda")
+    slot = torch.tensor([j % 16 for j in pos], device="cuda")
+    gk = pool.k_pages[blk, :, slot].float().cpu().numpy()
+    gv = pool.v_pages[blk, :, slot].float().cpu().numpy()
+    kh = k[sample].float().cpu().numpy()
+    vh = v[sample].float().cpu().numpy()
+    assert np.array_equal(gv, vh)
+    for i, j in enumerate(pos):
+        for h in range(hkv):
+            exact = oracle.rope(kh[i, h], j, base)
+            assert np.abs(gk[i, h] - exact).max() <= 2 ** -8 * max(1.0, np.abs(exact).max())
+    pool.close()
+
+
 # ------------------------------------------------------------------ decode
 @pytest.mark.parametrize("D,Hq,Hkv,dtype", [
     (128, 32, 8, "bf16"), (128, 8, 8, "bf16"), (64, 16, 8, "bf16"), (64, 16, 2, "bf16"),
