@@ -909,6 +909,14 @@ def mixed_sweep(args, flush, stream, hbm_peak):
     return out
 
 
+def _materialise_warmup(pk, res):
+    """One one-token copy into a block that is released again: the stream-ordered allocator's
+    first use (milliseconds, once per process) stays out of the timed copies."""
+    d0 = next(iter(res.doc_blocks))
+    ids = pk.kv_pool_materialise_batch(res.pool, [(res.doc_blocks[d0], 1, 0)])
+    pk.kv_pool_release(res.pool, ids[0])
+
+
 def materialised_bench(args, flush, stream, hbm_peak, tc_peak):
     """The copy-per-offset baseline (a document re-encoded for each offset it is used at, by
     kv_pool_materialise) against the lazy path on identical inputs: the copies' cost (bytes
@@ -941,6 +949,7 @@ def materialised_bench(args, flush, stream, hbm_peak, tc_peak):
         res = H.build_resident(wl, src, resident_pool=False,
                                extra_blocks=H.materialised_blocks_needed(wl))
         db = H.decode_batch(wl, res, src, phase_order=True)
+        _materialise_warmup(pk, res)
         torch.cuda.synchronize()
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
         ev[0].record(stream)
@@ -974,7 +983,7 @@ def materialised_bench(args, flush, stream, hbm_peak, tc_peak):
             "distinct_doc_offset_pairs": len(copies), "unique_docs": len(wl.used_docs()),
             "kv_bytes_documents_lazy": len(wl.used_docs()) * per_doc,
             "kv_bytes_documents_copies": len(copies) * per_doc,
-            "copy_ms": round(copy_ms, 4), "copy_launches": len(copies),
+            "copy_ms": round(copy_ms, 4), "copy_launches": 1,  # kv_pool_materialise_batch
             "copy_gbs": round(2 * len(copies) * per_doc / (copy_ms * 1e-3) / 1e9, 1),
             "lazy": {"ms_per_call": round(t_lazy, 5),
                      "value": round(kvb / (t_lazy * 1e-3) / 1e9, 2), "unit": "GB/s"},
@@ -991,6 +1000,7 @@ def materialised_bench(args, flush, stream, hbm_peak, tc_peak):
     res = H.build_resident(wl, src, resident_pool=False,
                            extra_blocks=H.materialised_blocks_needed(wl))
     pb = H.prefill_batch(wl, res, src)
+    _materialise_warmup(pk, res)
     torch.cuda.synchronize()
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
     ev[0].record(stream)

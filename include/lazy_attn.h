@@ -220,6 +220,24 @@ int kv_pool_write_tokens(lazy_pool *pool, const void *d_k_raw, const void *d_v, 
 int kv_pool_materialise(lazy_pool *pool, const int32_t *src_block_ids,
                         const int32_t *dst_block_ids, int32_t n_tokens, int32_t offset,
                         lazy_stream_t stream);
+/*
+ * The same copies for many (segment, offset) pairs in one launch (the baseline's set-up cost
+ * without a launch per copy). Copy c re-encodes n_tokens[c] tokens held in
+ * src_block_ids[cu_pages[c] .. cu_pages[c+1]) for offset offsets[c] into the blocks
+ * dst_block_ids[cu_pages[c] .. cu_pages[c+1]), with the arithmetic of kv_pool_materialise.
+ *   cu_pages      host int32 [n_copies + 1], cu_pages[0] = 0 and
+ *                 cu_pages[c+1] - cu_pages[c] = ceil(n_tokens[c] / page_size)
+ *   src_block_ids, dst_block_ids  host int32 [cu_pages[n_copies]]
+ *   n_tokens, offsets             host int32 [n_copies]; offsets[c] + n_tokens[c] < 2^26
+ * No destination block may be a source block of any copy, nor appear twice (copies run in
+ * parallel). The page list is copied to device memory taken from the stream-ordered allocator
+ * and returned after the launch. LAZY_ERR_INVALID_ARG for any violation (nothing launched);
+ * LAZY_ERR_UNSUPPORTED on ALiBi pools.
+ */
+int kv_pool_materialise_batch(lazy_pool *pool, int32_t n_copies, const int32_t *cu_pages,
+                              const int32_t *src_block_ids, const int32_t *dst_block_ids,
+                              const int32_t *n_tokens, const int32_t *offsets,
+                              lazy_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
  * Page words ("(block ID, offset) bit-packed in a single register", summaries' decoding part)

@@ -15,6 +15,8 @@ import ctypes
 import os
 from typing import List, Optional, Sequence, Tuple
 
+import itertools
+
 import numpy as np
 
 from ._build import build_library, library_path  # noqa: F401
@@ -47,7 +49,8 @@ EXPORTS = [
     "lazy_version", "lazy_status_string", "lazy_last_error", "lazy_pool_create",
     "lazy_pool_destroy", "lazy_pool_set_wait_limit", "kv_pool_alloc", "kv_pool_retain",
     "kv_pool_release", "kv_pool_num_free", "kv_pool_refcount", "kv_pool_insert_doc",
-    "kv_pool_write_tokens", "kv_pool_materialise", "lazy_pack_page", "lazy_unpack_page",
+    "kv_pool_write_tokens", "kv_pool_materialise", "kv_pool_materialise_batch",
+    "lazy_pack_page", "lazy_unpack_page",
     "lazy_pack_pages",
     "lazy_pack_segment", "lazy_decode_workspace_bytes", "lazy_attn_decode",
     "lazy_decode_partition", "lazy_order_segments",
@@ -103,6 +106,8 @@ _SIGS = {
     "kv_pool_insert_doc": ([_vp, _vp, _vp, _i32, _i32, _pi32, _pi32, _i32, _vp], ctypes.c_int),
     "kv_pool_write_tokens": ([_vp, _vp, _vp, _i32, _vp, _vp, _vp], ctypes.c_int),
     "kv_pool_materialise": ([_vp, _pi32, _pi32, _i32, _i32, _vp], ctypes.c_int),
+    "kv_pool_materialise_batch": ([_vp, _i32, _pi32, _pi32, _pi32, _pi32, _pi32, _vp],
+                                  ctypes.c_int),
     "lazy_pack_page": ([_u32, _u32, _u32, _pu64], ctypes.c_int),
     "lazy_unpack_page": ([_u64, _pu32, _pu32, _pu32], ctypes.c_int),
     "lazy_pack_pages": ([_i32, _pu32, _pu32, _pu32, _pu64], ctypes.c_int),
@@ -300,6 +305,48 @@ def kv_pool_materialise(pool: LazyPool, src_block_ids: Sequence[int], n_tokens: 
     _check("kv_pool_materialise", load_library().kv_pool_materialise(
         pool.handle, src, dd, n_tokens, offset, _stream(stream)))
     return dst[:n_pages]
+
+
+def kv_pool_materialise_batch(pool: LazyPool, copies: Sequence[tuple], stream=None) -> List[List[int]]:
+    """kv_pool_materialise for many copies in one launch. copies: (src_block_ids, n_tokens,
+    offset) or (src_block_ids, n_tokens, offset, dst_block_ids); destination blocks are
+    allocated here (in one allocation) where not given. Returns each copy's block ids."""
+    nc = len(copies)
+    ps = pool.page_size
+    n_tok = np.fromiter((int(cp[1]) for cp in copies), dtype=np.int64, count=nc)
+    offs = np.fromiter((int(cp[2]) for cp in copies), dtype=np.int64, count=nc)
+    pages = (n_tok + ps - 1) // ps
+    cu = np.zeros(nc + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(pages)
+    total = int(cu[-1])
+    given = np.fromiter((len(cp) > 3 and cp[3] is not None for cp in copies), dtype=bool,
+                        count=nc)
+    pl = pages.tolist()
+    src = np.zeros(max(total, 1), dtype=np.int32)
+    src[:total] = np.fromiter(itertools.chain.from_iterable(
+        cp[0][:n] for cp, n in zip(copies, pl)), dtype=np.int32, count=total)
+    need = int(pages[~given].sum()) if nc else 0
+    fresh = np.asarray(kv_pool_alloc(pool, need) if need else [], dtype=np.int32)
+    if need == total:  # every destination allocated here, in copy order
+        dst = fresh if total else np.zeros(1, dtype=np.int32)
+    else:
+        dst = np.zeros(max(total, 1), dtype=np.int32)
+        k = 0
+        for c, cp in enumerate(copies):
+            lo, hi = int(cu[c]), int(cu[c + 1])
+            if given[c]:
+                dst[lo:hi] = np.asarray(list(cp[3])[: hi - lo], dtype=np.int32)
+            else:
+                dst[lo:hi] = fresh[k:k + hi - lo]
+                k += hi - lo
+    nt32, off32 = n_tok.astype(np.int32), offs.astype(np.int32)
+    if nc == 0:
+        nt32 = off32 = np.zeros(1, dtype=np.int32)
+    p32 = lambda a: a.ctypes.data_as(_pi32)
+    _check("kv_pool_materialise_batch", load_library().kv_pool_materialise_batch(
+        pool.handle, nc, p32(cu), p32(src), p32(dst), p32(nt32), p32(off32), _stream(stream)))
+    flat, cl = dst.tolist(), cu.tolist()
+    return [flat[cl[c]:cl[c + 1]] for c in range(nc)]
 
 
 # ------------------------------------------------------------------------------------------------

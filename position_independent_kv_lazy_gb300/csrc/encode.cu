@@ -207,6 +207,77 @@ __global__ void __launch_bounds__(256) materialise_kernel(
   }
 }
 
+// Many copies in one launch: one item = (page of the batch, slot, head group, chunk). The
+// page's entry gives its copy, its page index within the copy and its two blocks; the copy's
+// entry its token count and offset.
+template <typename T, int D>
+__global__ void __launch_bounds__(256) materialise_batch_kernel(
+    T *__restrict__ k_pool, T *__restrict__ v_pool, const uint64_t *__restrict__ turn,
+    int32_t hkv, int32_t hpt, const int4 *__restrict__ pages, const int2 *__restrict__ copies,
+    int32_t total_pages) {
+  constexpr int EPL = 16 / (int)sizeof(T);
+  constexpr int CH = (D / 2) / EPL;
+  const int32_t groups = hkv / hpt;
+  const int64_t total = (int64_t)total_pages * kPage * groups * CH;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int c = (int)(idx % CH);
+    int64_t rest = idx / CH;
+    const int h0 = (int)(rest % groups) * hpt;
+    rest /= groups;
+    const int slot = (int)(rest % kPage);
+    const int4 pe = pages[rest / kPage];  // (copy, page within the copy, source, destination)
+    const int2 ce = copies[pe.x];         // (tokens, offset)
+    const int32_t j = pe.y * kPage + slot;
+    if (j >= ce.x) continue;
+    float c0[EPL], s0[EPL], c1[EPL], s1[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      rope_cos_sin(-(int64_t)j, turn[c * EPL + e], c0[e], s0[e]);        // back to position 0
+      rope_cos_sin((int64_t)ce.y + j, turn[c * EPL + e], c1[e], s1[e]);  // to the target
+    }
+#pragma unroll 2
+    for (int h = h0; h < h0 + hpt; ++h) {
+      const size_t src = (((size_t)pe.z * hkv + h) * kPage + slot) * D;
+      const size_t dst = (((size_t)pe.w * hkv + h) * kPage + slot) * D;
+      const uint4 ka = *reinterpret_cast<const uint4 *>(k_pool + src + c * EPL);
+      const uint4 kb = *reinterpret_cast<const uint4 *>(k_pool + src + D / 2 + c * EPL);
+      const uint4 va = *reinterpret_cast<const uint4 *>(v_pool + src + c * EPL);
+      const uint4 vb = *reinterpret_cast<const uint4 *>(v_pool + src + D / 2 + c * EPL);
+      float lo[EPL], hi[EPL];
+      unpack16<T>(ka, lo);
+      unpack16<T>(kb, hi);
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) {
+        const float x = lo[e] * c0[e] - hi[e] * s0[e], y = lo[e] * s0[e] + hi[e] * c0[e];
+        lo[e] = x * c1[e] - y * s1[e];
+        hi[e] = x * s1[e] + y * c1[e];
+      }
+      *reinterpret_cast<uint4 *>(k_pool + dst + c * EPL) = pack16<T>(lo);
+      *reinterpret_cast<uint4 *>(k_pool + dst + D / 2 + c * EPL) = pack16<T>(hi);
+      *reinterpret_cast<uint4 *>(v_pool + dst + c * EPL) = va;
+      *reinterpret_cast<uint4 *>(v_pool + dst + D / 2 + c * EPL) = vb;
+    }
+  }
+}
+
+template <typename T, int D>
+int launch_materialise_batch(lazy_pool *p, const int4 *pages, const int2 *copies,
+                             int32_t total_pages, cudaStream_t s) {
+  constexpr int EPL = 16 / (int)sizeof(T);
+  const int64_t rows = (int64_t)total_pages * kPage * ((D / 2) / EPL);
+  const int hpt = heads_per_thread(p, rows);
+  const int64_t total = rows * (p->hkv / hpt);
+  const int threads = 256;
+  const int64_t want = (total + threads - 1) / threads;
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)p->num_sms * 16));
+  materialise_batch_kernel<T, D><<<grid, threads, 0, s>>>((T *)p->k, (T *)p->v, p->d_turn,
+                                                         p->hkv, hpt, pages, copies,
+                                                         total_pages);
+  LAZY_CUDA_TRY(cudaGetLastError());
+  return LAZY_OK;
+}
+
 template <typename T, int D>
 int launch_materialise(lazy_pool *p, int32_t tok_lo, int32_t n_tokens, int32_t offset,
                        const MatBlocks &mb, cudaStream_t s) {
@@ -390,6 +461,76 @@ extern "C" int kv_pool_materialise(lazy_pool *p, const int32_t *src_block_ids,
                        : launch_materialise<float, 64>(p, lo, hi - lo, offset, mb, s);
     if (rc != LAZY_OK) return rc;
   }
+  return LAZY_OK;
+}
+
+extern "C" int kv_pool_materialise_batch(lazy_pool *p, int32_t n_copies, const int32_t *cu_pages,
+                                         const int32_t *src_block_ids,
+                                         const int32_t *dst_block_ids, const int32_t *n_tokens,
+                                         const int32_t *offsets, lazy_stream_t stream) {
+  if (!p || n_copies < 0) return LAZY_ERR_INVALID_ARG;
+  if (n_copies == 0) return LAZY_OK;
+  if (!cu_pages || !n_tokens || !offsets || cu_pages[0] != 0) return LAZY_ERR_INVALID_ARG;
+  if (p->alibi) return LAZY_ERR_UNSUPPORTED;  // ALiBi pools cache K unrotated
+  for (int32_t c = 0; c < n_copies; ++c) {
+    if (n_tokens[c] < 0 || offsets[c] < 0 || (int64_t)offsets[c] + n_tokens[c] > (1ll << 26))
+      return LAZY_ERR_INVALID_ARG;
+    if ((int64_t)cu_pages[c + 1] - cu_pages[c] != (n_tokens[c] + kPage - 1) / kPage)
+      return LAZY_ERR_INVALID_ARG;
+  }
+  const int32_t total_pages = cu_pages[n_copies];
+  if (total_pages == 0) return LAZY_OK;
+  if (!src_block_ids || !dst_block_ids) return LAZY_ERR_INVALID_ARG;
+  // no copy may overwrite pages that any copy reads, and no two may write one block: one byte
+  // per pool block (1 = read by a copy, 2 = written by one)
+  std::vector<uint8_t> use(p->num_blocks, 0);
+  for (int32_t i = 0; i < total_pages; ++i) {
+    if (src_block_ids[i] < 0 || src_block_ids[i] >= p->num_blocks) return LAZY_ERR_INVALID_ARG;
+    use[src_block_ids[i]] = 1;
+  }
+  for (int32_t i = 0; i < total_pages; ++i) {
+    const int32_t b = dst_block_ids[i];
+    if (b < 0 || b >= p->num_blocks || use[b] != 0) return LAZY_ERR_INVALID_ARG;
+    use[b] = 2;
+  }
+  int rc = ensure_device(p);
+  if (rc != LAZY_OK) return rc;
+  p->encoded = true;
+  // the page list: (copy, page within the copy, source, destination) per page, then
+  // (tokens, offset) per copy
+  std::vector<int4> pages(total_pages);
+  std::vector<int2> copies(n_copies);
+  for (int32_t c = 0; c < n_copies; ++c) {
+    copies[c] = make_int2(n_tokens[c], offsets[c]);
+    for (int32_t pg = cu_pages[c]; pg < cu_pages[c + 1]; ++pg)
+      pages[pg] = make_int4(c, pg - cu_pages[c], src_block_ids[pg], dst_block_ids[pg]);
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  const size_t pages_bytes = sizeof(int4) * (size_t)total_pages;
+  const size_t bytes = pages_bytes + sizeof(int2) * (size_t)n_copies;
+  void *buf = nullptr;
+  LAZY_CUDA_TRY(cudaMallocAsync(&buf, bytes, s));
+  // pageable sources: each copy has read its host data when the call returns
+  cudaError_t e = cudaMemcpyAsync(buf, pages.data(), pages_bytes, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync((uint8_t *)buf + pages_bytes, copies.data(), bytes - pages_bytes,
+                        cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) {
+    cudaFreeAsync(buf, s);
+    return record_cuda(e, "kv_pool_materialise_batch page list");
+  }
+  const int4 *d_pages = reinterpret_cast<const int4 *>(buf);
+  const int2 *d_copies = reinterpret_cast<const int2 *>((uint8_t *)buf + pages_bytes);
+  if (p->dtype == LAZY_DTYPE_BF16)
+    rc = p->d == 128
+             ? launch_materialise_batch<__nv_bfloat16, 128>(p, d_pages, d_copies, total_pages, s)
+             : launch_materialise_batch<__nv_bfloat16, 64>(p, d_pages, d_copies, total_pages, s);
+  else
+    rc = p->d == 128 ? launch_materialise_batch<float, 128>(p, d_pages, d_copies, total_pages, s)
+                     : launch_materialise_batch<float, 64>(p, d_pages, d_copies, total_pages, s);
+  const cudaError_t ef = cudaFreeAsync(buf, s);
+  if (rc != LAZY_OK) return rc;
+  LAZY_CUDA_TRY(ef);
   return LAZY_OK;
 }
 

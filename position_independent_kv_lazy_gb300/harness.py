@@ -11,7 +11,7 @@ from typing import Dict, List, Optional
 import numpy as np
 
 from . import (LazyPool, build_page_table, kv_pool_alloc, kv_pool_insert_doc,
-               kv_pool_materialise, lazy_decode_partition, order_segments_by_phase)
+               kv_pool_materialise_batch, lazy_decode_partition, order_segments_by_phase)
 
 
 def _torch_dtype(wl):
@@ -315,16 +315,14 @@ def materialised_blocks_needed(wl, reqs=None) -> int:
 
 def materialise_copies(wl, res: Resident, reqs=None, stream=None) -> Dict[tuple, List[int]]:
     """The copy-per-offset baseline: one re-encoded copy (keys at absolute positions, written by
-    kv_pool_materialise) of every distinct (document, offset) pair the requests use. Returns
+    kv_pool_materialise_batch in one launch) of every distinct (document, offset) pair the requests use. Returns
     {(doc, offset): block ids}."""
     reqs = reqs if reqs is not None else wl.requests
-    copies: Dict[tuple, List[int]] = {}
-    for r in reqs:
-        for d, o in zip(r.docs, r.offsets):
-            if (d, o) not in copies:
-                copies[(d, o)] = kv_pool_materialise(res.pool, res.doc_blocks[d], wl.doc_len, o,
-                                                     stream=stream)
-    return copies
+    pairs = list(dict.fromkeys((d, o) for r in reqs for d, o in zip(r.docs, r.offsets)))
+    # one launch for all copies
+    ids = kv_pool_materialise_batch(
+        res.pool, [(res.doc_blocks[d], wl.doc_len, o) for d, o in pairs], stream=stream)
+    return dict(zip(pairs, ids))
 
 
 def copy_page_table(wl, res: Resident, copies, reqs, with_private: bool):

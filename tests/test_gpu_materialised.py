@@ -68,6 +68,61 @@ def test_materialise_rejects_in_place_and_alibi(pk):
         pk.kv_pool_materialise(ares.pool, ares.doc_blocks[0], 32, 7)
 
 
+@pytest.mark.parametrize("dtype,D", [("bf16", 128), ("fp32", 64)])
+def test_materialise_batch_equals_single_copies(pk, dtype, D):
+    # copies of three documents for different offsets (partial last pages, one offset twice
+    # for one document, one copy of 0 tokens) in one launch equal the copies written one call
+    # at a time, bit for bit
+    H = _h()
+    wl = W.custom("decode", [[(0, 9), (1, 700), (2, 123457)]], doc_len=57, n_pool=3, Hq=4,
+                  Hkv=2, D=D, dtype=dtype, base=500000.0, priv=[(123514, 1)], seed=33)
+    src = H.HostSource(wl)
+    res = H.build_resident(wl, src, resident_pool=False, extra_blocks=64)
+    jobs = [(0, 57, 9), (1, 57, 700), (2, 40, 123457), (0, 57, 3001), (1, 0, 5), (2, 57, 0)]
+    single = [pk.kv_pool_materialise(res.pool, res.doc_blocks[d], n, o) if n else []
+              for d, n, o in jobs]
+    batch = pk.kv_pool_materialise_batch(res.pool, [(res.doc_blocks[d], n, o)
+                                                     for d, n, o in jobs])
+    torch.cuda.synchronize()
+    assert pk.lazy_get_device_error(res.pool) == 0
+    for (d, n, o), a, b in zip(jobs, single, batch):
+        assert len(a) == len(b) == (n + 15) // 16
+        if n:
+            ia = torch.tensor(a, device="cuda")
+            ib = torch.tensor(b, device="cuda")
+            full = n // 16
+            for pages in (res.pool.k_pages, res.pool.v_pages):
+                if full:
+                    assert torch.equal(pages[ia[:full]], pages[ib[:full]]), (d, n, o)
+                if n % 16:  # slots past the copy's last token are not written
+                    assert torch.equal(pages[ia[full]][:, :n % 16], pages[ib[full]][:, :n % 16])
+
+
+def test_materialise_batch_rejects(pk):
+    H = _h()
+    wl = W.custom("decode", [[(0, 5)]], doc_len=32, n_pool=1, Hq=4, Hkv=2, D=128, dtype="bf16",
+                  base=500000.0, priv=[(37, 1)], seed=34)
+    src = H.HostSource(wl)
+    res = H.build_resident(wl, src, resident_pool=False, extra_blocks=8)
+    ids = res.doc_blocks[0]
+    free = pk.kv_pool_alloc(res.pool, 4)
+    bad = [
+        [(ids, 32, 7, [ids[1], ids[0]])],                          # a destination is a source
+        [(ids, 32, 7, free[:2]), (ids, 32, 9, [free[1], free[2]])],  # a block written twice
+        [(ids, 32, (1 << 26) - 16, free[:2])],                     # offset + tokens past 2^26
+        [(ids, 32, 7, [free[0], res.pool.num_blocks])],            # a block outside the pool
+    ]
+    for copies in bad:
+        with pytest.raises(pk.LazyError) as e:
+            pk.kv_pool_materialise_batch(res.pool, copies)
+        assert e.value.status == pk.LAZY_ERR_INVALID_ARG
+    ares = H.build_resident(wl, src, resident_pool=False, extra_blocks=2,
+                            alibi_slopes=W.alibi_slopes(4))
+    with pytest.raises(pk.LazyError) as e:
+        pk.kv_pool_materialise_batch(ares.pool, [(ares.doc_blocks[0], 32, 7)])
+    assert e.value.status == pk.LAZY_ERR_UNSUPPORTED
+
+
 def _copy_setup(pk, wl, src):
     H = _h()
     res = H.build_resident(wl, src, resident_pool=False, drop_raw=False,
