@@ -1139,8 +1139,8 @@ __global__ void __launch_bounds__(WARPS * 32)
       mma_begin_shared_unit(st, sp, unit / HV, unit % HV, lane);
     }
     // a dead row's word only feeds the warp-wide bad-page vote and the dead row's own (unused)
-    // scores: give it row A's word so that an absent B cannot veto the page. B's word must name the block that
-    // was loaded (A's); a plan that pairs different blocks makes it a bad word.
+    // scores: give it row A's word so that an absent B cannot veto the page. B's word must name
+    // the block that was loaded (A's); a plan that pairs different blocks makes it a bad word.
     const uint64_t wa = meta_w[2 * s];
     uint64_t word = wa;
     if (half && st.live) {
