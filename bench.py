@@ -287,11 +287,12 @@ def shared_decode_bench(args, flush, stream):
     return out
 
 
-def rotation_side_bench(args, flush, stream):
-    """The CUDA-core prefill on prefill_b8 with the relative rotation on the key side (every
-    cached key page rotated by R(o - m0)) and on the query side (the query rows reloaded as
-    R(m - o) q once per document offset): same attention, 3/(4M) against 3/(4 L_d) rotation
-    work per key."""
+def rotation_side_bench(args, flush, stream, tc_peak=None):
+    """The prefill on prefill_b8 with the relative rotation on the key side (every cached key
+    page rotated by R(o - m0)) and on the query side (the query rows reloaded as R(m - o) q once
+    per document offset): same attention, 3/(4M) against 3/(4 L_d) rotation work per key. Both
+    kernels: CUDA-core (fp32) and tensor-core (fp16 Q.K; its query-side mode still converts
+    every key tile to fp16)."""
     import torch
 
     import position_independent_kv_lazy_gb300 as pk
@@ -315,6 +316,22 @@ def rotation_side_bench(args, flush, stream):
         med = sorted(ms)[1]
         out[tag] = {"value": round(pb.flops / (med * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                     "ms_per_call": round(med, 4)}
+    ws = _prefill_workspace(pk, res.pool, pb, wl.Hq)
+    tc = {}
+    for tag, fl in (("key_side", pk.LAZY_PREFILL_TC), ("query_side", pk.LAZY_PREFILL_TC_QSIDE)):
+        def call():
+            pk.lazy_attn_prefill(res.pool, pb.q, pb.k_new, pb.v_new, pb.cu_q, pb.q_pos0,
+                                 pb.words, pb.cu_pages, pb.max_q_len, sm_scale=wl.sm_scale,
+                                 out=o, lse=l, workspace=ws, flags=fl)
+        for _ in range(3):
+            flush(); call()
+        ms = _timed_steps(call, max(5, args.steps // 2), flush, stream)
+        med = _dist_ms(ms)["median"]
+        tf = pb.flops / (med * 1e-3) / 1e12
+        tc[tag] = {"value": round(tf, 2), "unit": "TFLOP/s", "ms_per_call": round(med, 4)}
+        if tc_peak:
+            tc[tag]["frac"] = round(tf / tc_peak, 4)
+    out["tensor_core"] = tc
     if pk.lazy_get_device_error(res.pool) != 0:
         raise RuntimeError("device error in the rotation-side bench")
     del res, src
@@ -417,6 +434,19 @@ def bench_materialised_only(args):
     flush, _ = _make_flush(torch)
     print(json.dumps({"mode": "materialised only", "materialised": materialised_bench(
         args, flush, torch.cuda.current_stream(), hbm_peak, tc_peak)}), flush=True)
+
+
+def bench_rotation_side_only(args):
+    """The key-side / query-side prefill section alone."""
+    import torch
+
+    import position_independent_kv_lazy_gb300 as pk
+    pk.build_library()
+    pk.load_library()
+    _, tc_peak, _, _ = _peaks()
+    flush, _ = _make_flush(torch)
+    print(json.dumps({"mode": "rotation side only", "prefill_rotation_side": rotation_side_bench(
+        args, flush, torch.cuda.current_stream(), tc_peak)}), flush=True)
 
 
 def bench_long_decode_only(args):
@@ -790,7 +820,7 @@ def bench_ours(args):
         torch.cuda.empty_cache()
         line["shared_decode"] = shared_decode_bench(args, flush, stream)
         torch.cuda.empty_cache()
-        line["prefill_rotation_side"] = rotation_side_bench(args, flush, stream)
+        line["prefill_rotation_side"] = rotation_side_bench(args, flush, stream, tc_peak)
         torch.cuda.empty_cache()
         line["materialised"] = materialised_bench(args, flush, stream, hbm_peak, tc_peak)
     clk.__exit__()
@@ -1187,6 +1217,23 @@ def mqa_bench(args, flush, stream, hbm_peak, tc_peak):
     out["prefill"] = {"workload": "prefill_b8 shapes with Hkv 1 (group 32, 4 tokens per Q tile)",
                       "value": round(tf, 2), "unit": "TFLOP/s", "ms_dist": _dist_ms(ms),
                       "frac": round(tf / tc_peak, 4)}
+
+    # the query-side mode on the same shapes: a Q tile holds 4 tokens, so its re-rotation per
+    # document evaluates few angles
+    def prefill_qside_call():
+        pk.lazy_attn_prefill(pres.pool, pb.q, pb.k_new, pb.v_new, pb.cu_q, pb.q_pos0, pb.words,
+                             pb.cu_pages, pb.max_q_len, sm_scale=pwl.sm_scale, out=pout,
+                             lse=plse, workspace=pws, flags=pk.LAZY_PREFILL_TC_QSIDE)
+
+    for _ in range(3):
+        flush(); prefill_qside_call()
+    ms = _timed_steps(prefill_qside_call, steps, flush, stream)
+    med = _dist_ms(ms)["median"]
+    tf = pb.flops / (med * 1e-3) / 1e12
+    out["prefill_query_side"] = {"value": round(tf, 2), "unit": "TFLOP/s",
+                                 "ms_dist": _dist_ms(ms), "frac": round(tf / tc_peak, 4)}
+    if pk.lazy_get_device_error(pres.pool) != 0:
+        raise RuntimeError("device error in the MQA runs")
     pres.pool.close()
     return out
 
@@ -1429,7 +1476,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["all", "decode", "prefill", "long_decode", "materialised"],
+    ap.add_argument("--only", choices=["all", "decode", "prefill", "long_decode", "materialised",
+                                       "rotation_side"],
                     default="all",
                     help="decode / prefill / long_decode: time only that workload (smaller "
                          "footprint, for profiling)")
@@ -1450,6 +1498,8 @@ def main():
         bench_long_decode_only(args)
     elif args.only == "materialised":
         bench_materialised_only(args)
+    elif args.only == "rotation_side":
+        bench_rotation_side_only(args)
     else:
         bench_ours(args)
 

@@ -77,6 +77,14 @@ enum {
                                     relative rotation: cached key pages are used as stored
                                     (R(j) k) and the queries take R(m - o) once per document
                                     offset o, instead of every key page taking R(o - m0) */
+    LAZY_PREFILL_TC_QSIDE = 4, /* the tensor-core kernel with the query-side variant: each
+                                  128-key tile takes the offset r of its first page as its
+                                  reference; when r changes the query tiles are reloaded and
+                                  rotated to R(m - r) q, pages at offset r are only converted to
+                                  the fp16 operand type, and pages of another offset in the same
+                                  tile and the question's own keys take R(o - r) and R(p - r).
+                                  Same shapes and LAZY_ERR_UNSUPPORTED rule as LAZY_PREFILL_TC;
+                                  on ALiBi pools it is LAZY_PREFILL_TC. ([ES] "1. Prefilling") */
     /* Added to one of the above: the cached pages hold keys at absolute positions (copies
        written by kv_pool_materialise) and are listed with offset 0. The attention is the same;
        the tensor-core kernel then takes position 0 as its reference (queries rotated by R(m),
@@ -441,7 +449,8 @@ int lazy_attn_decode_shared(lazy_pool *pool, const void *d_q, const int32_t *d_q
  *   total_q      host: d_cu_q[batch]; max_q_len host: max_b (d_cu_q[b+1]-d_cu_q[b]).
  *   d_out        device [total_q][num_q_heads][head_dim] pool dtype; d_lse float [total_q][Hq].
  *   d_workspace  device scratch of lazy_prefill_workspace_bytes(...) bytes (may be 0).
- *   flags        LAZY_PREFILL_AUTO / _SIMT / _TC / _SIMT_QSIDE.
+ *   flags        LAZY_PREFILL_AUTO / _SIMT / _TC / _SIMT_QSIDE / _TC_QSIDE, optionally
+ *                + LAZY_PREFILL_ABSOLUTE_KEYS.
  */
 int lazy_prefill_workspace_bytes(lazy_pool *pool, int32_t batch, int32_t total_q,
                                  int32_t max_q_len, int32_t num_q_heads, int32_t flags,

@@ -42,6 +42,7 @@ LAZY_PREFILL_AUTO = 0
 LAZY_PREFILL_SIMT = 1
 LAZY_PREFILL_TC = 2
 LAZY_PREFILL_SIMT_QSIDE = 3
+LAZY_PREFILL_TC_QSIDE = 4
 LAZY_PREFILL_ABSOLUTE_KEYS = 16
 
 # Every symbol declared in include/lazy_attn.h (checked by the tests).

@@ -30,6 +30,7 @@ struct PrefillParams {
   size_t workspace_bytes;
   int32_t qside;        // CUDA-core path: query-side rotation per document offset
   int32_t absolute;     // tensor-core path: reference position 0 (LAZY_PREFILL_ABSOLUTE_KEYS)
+  int32_t tc_qside;     // tensor-core path: query-side rotation, reference per document
 };
 
 int prefill_simt(lazy_pool *p, const PrefillParams &pp, int32_t max_q_len, cudaStream_t s);

@@ -11,7 +11,7 @@ extern "C" int lazy_prefill_workspace_bytes(lazy_pool *p, int32_t batch, int32_t
     return LAZY_ERR_INVALID_ARG;
   if (flags & ~(15 | LAZY_PREFILL_ABSOLUTE_KEYS)) return LAZY_ERR_INVALID_ARG;
   flags &= 15;
-  if (flags < LAZY_PREFILL_AUTO || flags > LAZY_PREFILL_SIMT_QSIDE) return LAZY_ERR_INVALID_ARG;
+  if (flags < LAZY_PREFILL_AUTO || flags > LAZY_PREFILL_TC_QSIDE) return LAZY_ERR_INVALID_ARG;
   *bytes = 0;  // the SIMT kernel needs no scratch; the tensor-core one may split its last wave
   if (flags == LAZY_PREFILL_SIMT || flags == LAZY_PREFILL_SIMT_QSIDE || batch == 0 ||
       total_q == 0 || max_q_len == 0)
@@ -35,7 +35,7 @@ extern "C" int lazy_attn_prefill(lazy_pool *p, const void *q, const void *k_new,
   if (flags & ~(15 | LAZY_PREFILL_ABSOLUTE_KEYS)) return LAZY_ERR_INVALID_ARG;
   const int32_t absolute = (flags & LAZY_PREFILL_ABSOLUTE_KEYS) ? 1 : 0;
   flags &= 15;
-  if (flags < LAZY_PREFILL_AUTO || flags > LAZY_PREFILL_SIMT_QSIDE) return LAZY_ERR_INVALID_ARG;
+  if (flags < LAZY_PREFILL_AUTO || flags > LAZY_PREFILL_TC_QSIDE) return LAZY_ERR_INVALID_ARG;
   if (batch == 0 || total_q == 0 || max_q_len == 0) return LAZY_OK;
   if (!q || !cu_q || !q_pos0 || !cu_pages || !out || !lse) return LAZY_ERR_INVALID_ARG;
   if ((k_new == nullptr) != (v_new == nullptr)) return LAZY_ERR_INVALID_ARG;
@@ -72,9 +72,10 @@ extern "C" int lazy_attn_prefill(lazy_pool *p, const void *q, const void *k_new,
   pp.workspace_bytes = workspace ? workspace_bytes : 0;
   pp.qside = flags == LAZY_PREFILL_SIMT_QSIDE ? 1 : 0;
   pp.absolute = absolute && !p->alibi;
+  pp.tc_qside = flags == LAZY_PREFILL_TC_QSIDE && !p->alibi;
   cudaStream_t s = (cudaStream_t)stream;
   const bool tc_ok = prefill_tc_supported(p, num_q_heads) == LAZY_OK;
-  if (flags == LAZY_PREFILL_TC) {
+  if (flags == LAZY_PREFILL_TC || flags == LAZY_PREFILL_TC_QSIDE) {
     if (!tc_ok) return LAZY_ERR_UNSUPPORTED;
     return prefill_tc(p, pp, max_q_len, s);
   }

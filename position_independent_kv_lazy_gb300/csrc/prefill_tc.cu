@@ -57,7 +57,7 @@ constexpr int kNM = 4;  // softmax metadata ring (see SMeta)
 constexpr int kOffMetaK = kOffV + kNV * kTileBytes;    // KMeta [kNK]
 constexpr int kOffMetaS = kOffMetaK + kNK * 48;        // SMeta [kNM]
 constexpr int kOffBar = kOffMetaS + kNM * 80 + 16;     // barriers (8-byte aligned)
-constexpr int kOffTurn = kOffBar + 192;                // the 64 turn fractions (uint64)
+constexpr int kOffTurn = kOffBar + 256;                // the 64 turn fractions (uint64)
 constexpr int kSmemBytes = kOffTurn + 64 * 8 + 1024;   // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory per block");
 
@@ -66,7 +66,8 @@ struct KMeta {
   int32_t kind;   // 0 = document pages, 1 = question keys
   int32_t c0;     // question tile: first key token
   int32_t off[8]; // document tile: logical offset of each page
-  int32_t pad[2];
+  int32_t ref;    // query-side mode: the tile's reference position r (Q tiles hold R(m - r) q)
+  int32_t pad;
 };
 // Read by the softmax groups. Written when tile j's K copy is issued, which precedes S_j; the
 // slot is rewritten for tile j + 4, whose K copy waits for QK of tile j + 1, which the MMA
@@ -416,6 +417,53 @@ __device__ __forceinline__ void chunk_angles_ilp(int64_t delta, const uint64_t *
   }
 }
 
+// Query-side mode: this thread's query row, raw bf16 as loaded, replaced in place by
+// R(delta) q in fp16 (delta = m - r for the tile's reference position r). A row's 64 angles
+// depend only on its token. With 4 or more query heads per kv head, each aligned group of 4
+// lanes holds rows of one token: then every lane evaluates 2 of a chunk's 8 angles and the group
+// exchanges them by shuffles (4x fewer evaluations); otherwise each lane evaluates all 64. Two
+// chunks per step keep 4 angle chains in flight. Warp-collective when share4 is set. Not
+// inlined: the call sits in the softmax loop but runs once per document, and an inlined copy
+// there made the whole loop slower (instruction fetch), with no document change at all.
+__device__ __noinline__ void qside_rotate_row(uint8_t *tile, int row, int64_t delta,
+                                              const uint64_t *turn_s, bool share4, int lane) {
+  if (!share4) {
+#pragma unroll 1
+    for (int c = 0; c < 8; ++c) {
+      RotF rq;
+      chunk_angles_ilp(delta, turn_s, c, rq);
+      rotate_row_chunk<true>(tile, row, c, rq);
+    }
+    return;
+  }
+  const int g4 = lane & 3, src0 = lane & ~3;
+#pragma unroll 1
+  for (int c = 0; c < 8; c += 2) {
+    float ca[2], sa[2], cb[2], sb[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      rope_cos_sin(delta, turn_s[(c + u) * 8 + g4], ca[u], sa[u]);
+      rope_cos_sin(delta, turn_s[(c + u) * 8 + 4 + g4], cb[u], sb[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      float co[8], si[8];  // frequency 8(c + u) + e, held by lane src0 + e % 4
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        co[e] = __shfl_sync(0xffffffffu, e < 4 ? ca[u] : cb[u], src0 | (e & 3));
+        si[e] = __shfl_sync(0xffffffffu, e < 4 ? sa[u] : sb[u], src0 | (e & 3));
+      }
+      RotF rq;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        rq.co[k] = make_float2(co[2 * k], co[2 * k + 1]);
+        rq.si[k] = make_float2(si[2 * k], si[2 * k + 1]);
+      }
+      rotate_row_chunk<true>(tile, row, c + u, rq);
+    }
+  }
+}
+
 // (cos, sin) of delta * theta_i for i = 8c .. 8c+7 (exact fp32 angles).
 __device__ __forceinline__ void chunk_angles(int64_t delta, const uint64_t *turn, int c, RotF &rf) {
 #pragma unroll
@@ -511,13 +559,18 @@ __device__ __forceinline__ TcUnit tc_unit(const TcParams &p) {
 // so pages listed at offset 0 (keys materialised at absolute positions) need no rotation, only
 // a conversion to fp16; everything else as kRelative. kAlibi: the pool's ALiBi mode; nothing
 // is rotated (the barriers keep their order), QK in bf16 as loaded, and every score gets
-// slope * (n - m) before the row max.
-enum { kRelative = 0, kAbsolute = 1, kAlibiMode = 2 };
+// slope * (n - m) before the row max. kQuerySide (LAZY_PREFILL_TC_QSIDE): the reference moves
+// with the documents. Each key tile takes r = the offset of its first page; when r changes the
+// raw Q tiles are reloaded and rotated to R(m - r) q, so the pages of that document are only
+// converted to fp16, and only pages of another offset in the same tile (a document boundary
+// inside the tile) or question keys (R(p - r)) are rotated.
+enum { kRelative = 0, kAbsolute = 1, kAlibiMode = 2, kQuerySide = 3 };
 
 template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ TcParams p) {
   constexpr bool kAlibi = kMode == kAlibiMode;
   constexpr bool kAbs = kMode == kAbsolute;
+  constexpr bool kQS = kMode == kQuerySide;
   constexpr bool kF16 = kMode != kAlibiMode;  // operand type of the QK product
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -534,6 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 20);
   uint64_t *turn_s = reinterpret_cast<uint64_t *>(sm + kOffTurn);
   volatile int *abort = reinterpret_cast<volatile int *>(bars + 21);
+  uint64_t *q_ld = bars + 22, *q_rdy = bars + 24;  // [2] query-side mode: Q reloads, re-rotations
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const TcUnit unit = tc_unit(p);
@@ -573,6 +627,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       mbar_init(&p_ready[i], 128);
     }
     mbar_init(o_final, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&q_ld[i], 1);
+      mbar_init(&q_rdy[i], 128);
+    }
     *abort = 0;
     fence_barrier_init();
   }
@@ -607,6 +665,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       int32_t rows[kNK][8];
       int32_t run8[kNK];  // first block id when the tile's 8 blocks are consecutive, else -1
       int k_issued[kNK] = {0, 0, 0}, v_issued[kNV] = {0, 0};
+      int32_t ref_cur = q_pos0_b + t0;  // query-side mode: the reference of the last tile
       bool ok = true;
       for (int e = 0; ok && e <= n_tiles; ++e) {
         if (e < n_tiles) {  // ---- K of tile e (content tile jc = lo + e)
@@ -643,6 +702,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             }
             ms.kind = 0;
             ms.full = full;
+            if (kQS) {
+              ref_cur = mk.off[0];
+              mk.ref = ref_cur;
+            }
             // Documents are encoded into freshly allocated, usually consecutive blocks: then one
             // 8-block box per 64-dim half replaces 8 page boxes.
             bool consec = full != 0;
@@ -665,6 +728,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             const int c0 = (jc - n_doc) * kTile;
             mk.kind = 1;
             mk.c0 = c0;
+            if (kQS) mk.ref = ref_cur;  // question keys take R(p - r) for the current r
             ms.kind = 1;
             ms.c0 = c0;
             ms.full = 0;
@@ -746,11 +810,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           mma_ts(tmem + 256 + i * 128, tmem + i * 128 + kk * 8, b0 + (uint64_t)(kk * (2048 >> 4)),
                  idesc_pv, (j > 0 || kk > 0) ? 1 : 0);
       };
+      // Query-side mode: the reference of the last QK; when tile j + 1 has another, QK of each Q
+      // tile waits for that tile's re-rotation (q_rdy, phase = re-rotations so far).
+      int32_t ref_prev = 0;
+      int n_rerot = 0;
       bool ok = cta_wait(q_rot, 0, abort, lim, p.err);
       tc_fence_after();
       if (ok && n_tiles > 0) {
         ok = cta_wait(&k_rot[0], 0, abort, lim, p.err);
         if (ok) {
+          if (kQS) ref_prev = meta_k[0].ref;
           tc_fence_after();
           qk(0, 0);
           qk(0, 1);
@@ -764,8 +833,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         if (!cta_wait(&p_ready[0], j & 1, abort, lim, p.err)) break;
         tc_fence_after();
         pv(j, 0);
+        bool rerot = false;
         if (more) {
           if (!cta_wait(&k_rot[sn], ((j + 1) / kNK) & 1, abort, lim, p.err)) break;
+          if (kQS) {
+            const int32_t ref_next = meta_k[sn].ref;
+            rerot = ref_next != ref_prev;
+            ref_prev = ref_next;
+            if (rerot && !cta_wait(&q_rdy[0], n_rerot & 1, abort, lim, p.err)) break;
+          }
           tc_fence_after();
           qk(j + 1, 0);
         }
@@ -774,6 +850,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         pv(j, 1);
         mma_commit(&v_empty[j % kNV]);
         if (more) {
+          if (kQS && rerot) {
+            if (!cta_wait(&q_rdy[1], n_rerot & 1, abort, lim, p.err)) break;
+            ++n_rerot;
+            tc_fence_after();
+          }
           qk(j + 1, 1);
           mma_commit(&k_empty[sn]);
         }
@@ -798,13 +879,28 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     const int t_row = t0 + t_off;
     const float sl2 = p.scale_log2;
     const float slope2 = kAlibi ? p.slopes[h * G + row % G] * 1.4426950408889634f : 0.f;
-    const int32_t m_row = q_pos0_b + t_row;  // the row's logical position (ALiBi)
+    const int32_t m_row = q_pos0_b + t_row;  // the row's logical position
     const uint64_t *turn = p.turn;
     const int st = tid - 128;               // 0..255
     const int rc = st & 7, rrow0 = (st >> 3) * 4;  // rotation share: chunk rc, rows rrow0..+3
     float m_run = -INFINITY, l_run = 0.f;
+    int32_t cur_ref = 0;  // query-side mode: r of the rows now in this group's Q tile
+    int n_reload = 0;     // query-side mode: raw Q reloads of this tile so far
+    bool reload_open = false;
     bool ok = cta_wait(q_full, 0, abort, lim, p.err);
-    if (ok && !kAlibi) {
+    if (kQS) {
+      // the first tile's reference, then this thread's row rotated to R(m - r)
+      cur_ref = q_pos0_b + t0;
+      if (ok && n_tiles > 0) {
+        ok = cta_wait(&k_full[0], 0, abort, lim, p.err);
+        if (ok) cur_ref = meta_k[0].ref;
+      }
+      if (__all_sync(0xffffffffu, ok)) {  // the row rotation exchanges angles between lanes
+        qside_rotate_row(Qs + i * kTileBytes, row, (int64_t)m_row - cur_ref, turn_s, G >= 4,
+                         lane);
+        fence_async_smem();
+      }
+    } else if (ok && !kAlibi) {
       // this thread's own query row of Q tile i, rotated to R(m - m0)
 #pragma unroll 1
       for (int c = 0; c < 8; ++c) {
@@ -826,9 +922,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       if (kAlibi) {
         // no rotation: the tile is used as loaded
       } else if (mt.kind == 0) {
-        // one relative rotation R(o - m0) per page
-        const int64_t d = (int64_t)mt.off[rrow0 >> 4] - m0;
-        if (kAbs && d == 0) {  // absolute keys at offset 0: no rotation, only the operand type
+        // one relative rotation R(o - m0) per page (query-side mode: R(o - r))
+        const int64_t d = (int64_t)mt.off[rrow0 >> 4] - (kQS ? (int64_t)mt.ref : (int64_t)m0);
+        if ((kAbs || kQS) && d == 0) {  // offset at the reference: only the operand type
           convert_4rows_chunk(kt, rrow0, rc);
         } else {
           if (d != cached) {
@@ -840,12 +936,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       } else {
         // question keys: raw, rotated by R(p - m0) row by row (the absolute mode re-reads the
         // request's first position here rather than keeping it in a register)
-        const int64_t q0 = kAbs ? (int64_t)p.q_pos0[tc_unit(p).b] : 0;
+        const int64_t q0 = (kAbs || kQS) ? (int64_t)p.q_pos0[tc_unit(p).b] : 0;
 #pragma unroll 1
         for (int rr = 0; rr < 4; ++rr) {
           RotF rk;
-          chunk_angles(kAbs ? q0 + mt.c0 + rrow0 + rr
-                            : (int64_t)(mt.c0 + rrow0 + rr - t_row + t_off),
+          chunk_angles(kAbs  ? q0 + mt.c0 + rrow0 + rr
+                       : kQS ? q0 + mt.c0 + rrow0 + rr - mt.ref
+                             : (int64_t)(mt.c0 + rrow0 + rr - t_row + t_off),
                        turn, rc, rk);
           rotate_row_chunk<kF16>(kt, rrow0 + rr, rc, rk);
         }
@@ -861,6 +958,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         break;
       }
       tc_fence_after();
+      // Query-side mode: a new reference at tile j + 1 (its K metadata stays until QK of that
+      // tile). QK of tile j, the last product that reads this Q tile before then, is complete, so
+      // the raw rows are reloaded now and rotated after this tile's softmax.
+      int32_t ref_next = cur_ref;
+      if (kQS && j + 1 < n_tiles) {
+        ref_next = meta_k[(j + 1) % kNK].ref;
+        if (ref_next != cur_ref && row == 0) {
+          mbar_arrive_expect_tx(&q_ld[i], kTileBytes);
+          for (int cb = 0; cb < 2; ++cb)
+            tma3d(Qs + i * kTileBytes + cb * kHalfBytes, &p.tm_q, cb * 64, h * G,
+                  qbeg + t0 + i * TQ, &q_ld[i]);
+          reload_open = true;
+        }
+      }
       const SMeta &mt = meta_s[j % kNM];
       const bool doc = mt.kind == 0;
       const bool need_mask = !(doc && mt.full);
@@ -973,11 +1084,27 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       m_run = m_use;
       tc_fence_before();
       mbar_arrive(&p_ready[i]);
+      if (kQS && ref_next != cur_ref) {
+        const bool landed = cta_wait(&q_ld[i], n_reload & 1, abort, lim, p.err);
+        if (landed) reload_open = false;
+        if (!__all_sync(0xffffffffu, landed)) {  // the row rotation is warp-collective
+          ok = false;
+          break;
+        }
+        ++n_reload;
+        qside_rotate_row(Qs + i * kTileBytes, row, (int64_t)m_row - ref_next, turn_s, G >= 4,
+                         lane);
+        fence_async_smem();
+        mbar_arrive(&q_rdy[i]);
+        cur_ref = ref_next;
+      }
       if (j + 2 < n_tiles && !rotate_tile(j + 2)) {
         ok = false;
         break;
       }
     }
+    // a reload still in flight after an abort lands before the CTA exits
+    if (kQS && reload_open) mbar_wait(&q_ld[i], n_reload & 1, lim);
     // epilogue: O / l -> bf16 rows, lse
     ok = ok && cta_wait(o_final, 0, abort, lim, p.err);
     // Each thread holds one row of its group's O tile. The rows are staged in shared memory in
@@ -1347,7 +1474,7 @@ int prefill_tc(lazy_pool *p, const PrefillParams &pp, int32_t max_q_len, cudaStr
   static cudaError_t attr_rc = cudaSuccess;
   std::call_once(attr_once, [] {
     for (auto fn : {prefill_tc_kernel<kRelative>, prefill_tc_kernel<kAbsolute>,
-                    prefill_tc_kernel<kAlibiMode>}) {
+                    prefill_tc_kernel<kAlibiMode>, prefill_tc_kernel<kQuerySide>}) {
       const cudaError_t e = cudaFuncSetAttribute(
           fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
       if (e != cudaSuccess && attr_rc == cudaSuccess) attr_rc = e;
@@ -1378,6 +1505,8 @@ int prefill_tc(lazy_pool *p, const PrefillParams &pp, int32_t max_q_len, cudaStr
   }
   if (pp.slopes)
     prefill_tc_kernel<kAlibiMode><<<pl.grid, kThreads, kSmemBytes, s>>>(tp);
+  else if (pp.tc_qside)
+    prefill_tc_kernel<kQuerySide><<<pl.grid, kThreads, kSmemBytes, s>>>(tp);
   else if (pp.absolute)
     prefill_tc_kernel<kAbsolute><<<pl.grid, kThreads, kSmemBytes, s>>>(tp);
   else

@@ -189,7 +189,8 @@ def test_prefill_absolute_keys_over_copies(pk, sms):
             ("abs_copies", pk.LAZY_PREFILL_TC | pk.LAZY_PREFILL_ABSOLUTE_KEYS, d_words, d_cu),
             ("rel_copies", pk.LAZY_PREFILL_TC, d_words, d_cu),
             ("abs_lazy", pk.LAZY_PREFILL_TC | pk.LAZY_PREFILL_ABSOLUTE_KEYS, pb.words,
-             pb.cu_pages)):
+             pb.cu_pages),
+            ("qside_copies", pk.LAZY_PREFILL_TC_QSIDE, d_words, d_cu)):
         out, lse = pk.lazy_attn_prefill(res.pool, pb.q, pb.k_new, pb.v_new, pb.cu_q, pb.q_pos0,
                                         w, c, pb.max_q_len, sm_scale=wl.sm_scale, flags=fl)
         torch.cuda.synchronize()

@@ -536,7 +536,31 @@ def test_prefill_tensor_core_parity(pk, Hq, Hkv):
     _check_prefill(wl, pb, out, lse)
 
 
-@pytest.mark.parametrize("flags", ["tc", "simt", "simt_qside"])
+@pytest.mark.parametrize("Hq,Hkv", [(32, 8), (8, 8), (16, 8), (16, 2), (32, 2), (32, 1)])
+def test_prefill_tensor_core_query_side_parity(pk, Hq, Hkv):
+    # the tensor-core kernel's query-side mode: 200-token documents put two offsets in some
+    # 128-key tiles (the second document's pages rotated against the tile's reference), and
+    # every document start re-rotates the query tiles; against the oracle and the key-side mode
+    wl = _edge_prefill_workload(128, Hq, Hkv, "bf16")
+    _, pb, out, lse = _prefill(pk, wl, pk.LAZY_PREFILL_TC_QSIDE)
+    _check_prefill(wl, pb, out, lse)
+    _, _, o_k, l_k = _prefill(pk, wl, pk.LAZY_PREFILL_TC)
+    assert np.abs(out - o_k).max() <= 2e-2 and np.abs(lse - l_k).max() <= 1e-3
+
+
+def test_prefill_query_side_full_size_sampled(pk):
+    # the prefill workload (16 documents of 1024 tokens per request: 8 key tiles per reference)
+    # through the query-side mode, sampled as in the key-side test
+    H = _h()
+    wl = W.prefill_workload()
+    src = H.DeviceSource(wl)
+    _, pb, out, lse = _prefill(pk, wl, pk.LAZY_PREFILL_TC_QSIDE, src=src)
+    _check_prefill(wl, pb, out, lse, reqs=[1, 6], kv_heads=list(range(8)),
+                   queries=[0, 1, 31, 32, 63, 64, 95, 127, 128, 160, 191, 192, 200, 223, 254, 255],
+                   src=src.host_view())
+
+
+@pytest.mark.parametrize("flags", ["tc", "simt", "simt_qside", "tc_qside"])
 def test_prefill_offsets_near_the_page_word_limit(pk, flags):
     # documents and question moved up to just below 2^26 (the offset field's limit)
     H = _h()
@@ -547,7 +571,7 @@ def test_prefill_offsets_near_the_page_word_limit(pk, flags):
         r.offsets = [o + c for o in r.offsets]
         r.q_pos0 += c
     fl = {"tc": pk.LAZY_PREFILL_TC, "simt": pk.LAZY_PREFILL_SIMT,
-          "simt_qside": pk.LAZY_PREFILL_SIMT_QSIDE}[flags]
+          "simt_qside": pk.LAZY_PREFILL_SIMT_QSIDE, "tc_qside": pk.LAZY_PREFILL_TC_QSIDE}[flags]
     _, pb, out, lse = _prefill(pk, wl, fl)
     _check_prefill(wl, pb, out, lse)
 
@@ -589,6 +613,25 @@ def test_prefill_last_wave_split(pk, Hq, Hkv, sms):
     assert np.array_equal(o2, o1) and np.array_equal(l2, l1)
 
 
+@pytest.mark.parametrize("Hq,Hkv", [(32, 8), (32, 1)])
+@pytest.mark.parametrize("sms", [5, 27, 1000])
+def test_prefill_query_side_last_wave_split(pk, Hq, Hkv, sms):
+    # key-range chunks of the query-side mode start inside a document: a chunk's first tile
+    # sets its reference
+    H = _h()
+    wl = _edge_prefill_workload(128, Hq, Hkv, "bf16")
+    src = H.HostSource(wl)
+    res = H.build_resident(wl, src, resident_pool=False, drop_raw=False)
+    pb = H.prefill_batch(wl, res, src)
+    pk.lazy_pool_set_schedule_sms(res.pool, sms)
+    out, lse = pk.lazy_attn_prefill(res.pool, pb.q, pb.k_new, pb.v_new, pb.cu_q, pb.q_pos0,
+                                    pb.words, pb.cu_pages, pb.max_q_len, sm_scale=wl.sm_scale,
+                                    flags=pk.LAZY_PREFILL_TC_QSIDE)
+    torch.cuda.synchronize()
+    assert pk.lazy_get_device_error(res.pool) == 0
+    _check_prefill(wl, pb, out.float().cpu().numpy(), lse.cpu().numpy())
+
+
 def test_prefill_split_workspace_sizes(pk):
     # 32/8 edge layout: X = 3, 72 units. 1 SM: no split. 5 SMs: 14 full waves, 2 split units
     # x 5 chunks. 20 SMs: 3 waves, 12 split units x 5. 100 SMs: 72 split units x 4 chunks.
@@ -623,7 +666,7 @@ def test_prefill_without_question_keys(pk):
     res = H.build_resident(wl, src, resident_pool=False)
     pb = H.prefill_batch(wl, res, src)
     cu = pb.cu_q.cpu().numpy()
-    for flags in (pk.LAZY_PREFILL_TC, pk.LAZY_PREFILL_SIMT):
+    for flags in (pk.LAZY_PREFILL_TC, pk.LAZY_PREFILL_TC_QSIDE, pk.LAZY_PREFILL_SIMT):
         out, lse = pk.lazy_attn_prefill(res.pool, pb.q, None, None, pb.cu_q, pb.q_pos0, pb.words,
                                         pb.cu_pages, pb.max_q_len, sm_scale=wl.sm_scale,
                                         flags=flags)
@@ -733,12 +776,12 @@ def test_decode_small_contexts(pk, kind, D, Hq, Hkv, dtype):
     assert np.abs(out[2] - np.repeat(v, G, axis=0)).max() <= (1e-2 if dtype == "bf16" else 1e-6)
 
 
-@pytest.mark.parametrize("flags", ["tc", "simt", "simt_qside"])
+@pytest.mark.parametrize("flags", ["tc", "simt", "simt_qside", "tc_qside"])
 @pytest.mark.parametrize("Hq,Hkv", [(32, 8), (8, 8), (16, 2), (32, 1)])
 def test_prefill_small_contexts(pk, flags, Hq, Hkv):
     wl = _small_prefill_workload(Hq, Hkv)
     fl = {"tc": pk.LAZY_PREFILL_TC, "simt": pk.LAZY_PREFILL_SIMT,
-          "simt_qside": pk.LAZY_PREFILL_SIMT_QSIDE}[flags]
+          "simt_qside": pk.LAZY_PREFILL_SIMT_QSIDE, "tc_qside": pk.LAZY_PREFILL_TC_QSIDE}[flags]
     _, pb, out, lse = _prefill(pk, wl, fl)
     _check_prefill(wl, pb, out, lse, form="S")
 
@@ -799,7 +842,7 @@ def test_decode_random_segment_orders(pk, seed, kind):
 
 
 @pytest.mark.parametrize("seed", [1, 2])
-@pytest.mark.parametrize("flags", ["tc", "simt"])
+@pytest.mark.parametrize("flags", ["tc", "simt", "tc_qside"])
 def test_prefill_random_segment_orders(pk, seed, flags):
     # permuted documents change which pages share a 128-key tile (mixed offsets within a tile)
     H = _h()
@@ -810,8 +853,9 @@ def test_prefill_random_segment_orders(pk, seed, flags):
     words, cu = _permuted_table(pk, wl, res, np.random.default_rng(seed), with_private=False)
     out, lse = pk.lazy_attn_prefill(res.pool, pb.q, pb.k_new, pb.v_new, pb.cu_q, pb.q_pos0,
                                     words, cu, pb.max_q_len, sm_scale=wl.sm_scale,
-                                    flags=pk.LAZY_PREFILL_TC if flags == "tc"
-                                    else pk.LAZY_PREFILL_SIMT)
+                                    flags={"tc": pk.LAZY_PREFILL_TC,
+                                           "tc_qside": pk.LAZY_PREFILL_TC_QSIDE,
+                                           "simt": pk.LAZY_PREFILL_SIMT}[flags])
     torch.cuda.synchronize()
     assert pk.lazy_get_device_error(res.pool) == 0
     _check_prefill(wl, pb, out.float().cpu().numpy(), lse.cpu().numpy())

@@ -134,6 +134,8 @@ def test_attention_argument_checks_return_before_device_use(lazylib):
                                      0.1, None, None, None, 0, 0, None) == pk.LAZY_ERR_INVALID_ARG
     assert lazylib.lazy_attn_prefill(h, None, None, None, None, None, None, None, 1, 4, 4, 4,
                                      0.1, None, None, None, 0, 9, None) == pk.LAZY_ERR_INVALID_ARG
+    assert lazylib.lazy_attn_prefill(h, None, None, None, None, None, None, None, 1, 4, 4, 4,
+                                     0.1, None, None, None, 0, 5, None) == pk.LAZY_ERR_INVALID_ARG
     # the fused prefill + append needs the question k/v and both append arrays
     dummy = ctypes.c_void_p(16)
     assert lazylib.lazy_attn_prefill_append(h, dummy, None, None, dummy, dummy, None, dummy, 1, 4,
