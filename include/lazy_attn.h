@@ -321,10 +321,9 @@ int lazy_attn_decode(lazy_pool *pool, const void *d_q, const int32_t *d_q_pos,
  *   - The pool must already have done its one-time device set-up on the current device (any
  *     earlier kv_pool_insert_doc, kv_pool_write_tokens or lazy_attn_decode call does it);
  *     otherwise LAZY_ERR_INVALID_ARG.
- *   - The first call on each device looks up the array's device address (a driver query, not
- *     an allocation) and keeps it for the life of the process; make that first call before
- *     any stream capture. Do not use the library across a cudaDeviceReset (the array may then
- *     sit at another address).
+ *   - Each call looks up the array's device address in the current context (a driver query,
+ *     not an allocation), so the address stays right across a cudaDeviceReset. The first call
+ *     on a device may load the array; make it before any stream capture.
  *   - If (batch * num_kv_heads * chunks + 4 * CTAs) * group * (head_dim + 1) * 4 bytes exceeds
  *     the array (chunks = ceil(group / 8), group = num_q_heads / num_kv_heads, CTAs = the grid,
  *     by default SMs x resident CTAs), the call returns LAZY_ERR_SCRATCH_LIMIT and launches

@@ -134,9 +134,9 @@ __global__ void __launch_bounds__(WARPS * 32) decode_split_kernel(const DecodePa
   constexpr int NF = NV0 / LPR > 0 ? NV0 / LPR : 1;  // fully reduced values per lane
   static_assert(LPR <= 32 && KPI <= kPage, "shape");
 
-  extern __shared__ __align__(128) uint8_t smem_raw[];
+  extern __shared__ __align__(128) uint8_t smem_split[];  // the other kernels align theirs to 1 KB
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint8_t *ws = smem_raw + warp * S::kBytes;
+  uint8_t *ws = smem_split + warp * S::kBytes;
   T *kbuf = reinterpret_cast<T *>(ws + S::kK);
   T *vbuf = reinterpret_cast<T *>(ws + S::kV);
   float *psm = reinterpret_cast<float *>(ws + S::kP);
@@ -1684,32 +1684,18 @@ extern "C" int lazy_attn_decode(lazy_pool *p, const void *q, const int32_t *q_po
 // Allocation-free decode: the same kernels, with their partial results in a fixed array compiled
 // into the library instead of a caller workspace (for callers that may not allocate).
 // ------------------------------------------------------------------------------------------------
-#include <mutex>
 
 // Scratch for lazy_attn_decode_noalloc. In host code this name is only a stand-in for the
 // symbol; the device address comes from cudaGetSymbolAddress (noalloc_scratch below).
 static __device__ __align__(256) unsigned char lazy_noalloc_scratch[LAZY_NOALLOC_SCRATCH_BYTES];
 
 namespace {
-constexpr int kMaxDevices = 64;
-std::mutex g_noalloc_mu;
-void *g_noalloc_ptr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device, looked up once per device.
+// Device address of the scratch array in the current context. Looked up on every call rather
+// than cached: after a device reset the module is loaded again and the array may move.
 int noalloc_scratch(void **out) {
-  int dev = -1;
-  LAZY_CUDA_TRY(cudaGetDevice(&dev));
-  if (dev < 0 || dev >= kMaxDevices) {
-    record_msg("allocation-free decode supports device ordinals below 64");
-    return LAZY_ERR_UNSUPPORTED;
-  }
-  std::lock_guard<std::mutex> g(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
-    void *ptr = nullptr;
-    LAZY_CUDA_TRY(cudaGetSymbolAddress(&ptr, lazy_noalloc_scratch));
-    g_noalloc_ptr[dev] = ptr;
-  }
-  *out = g_noalloc_ptr[dev];
+  void *ptr = nullptr;
+  LAZY_CUDA_TRY(cudaGetSymbolAddress(&ptr, lazy_noalloc_scratch));
+  *out = ptr;
   return LAZY_OK;
 }
 }  // namespace
