@@ -489,6 +489,23 @@ int lazy_attn_prefill_append(lazy_pool *pool, const void *d_q, const void *d_k_n
  * --------------------------------------------------------------------------------------- */
 /* Wait for `stream`, return the device error word's bits in *err and clear it. */
 int lazy_get_device_error(lazy_pool *pool, int32_t *err, lazy_stream_t stream);
+
+/*
+ * Upload of a step's inputs: copies `bytes` from pinned host memory to device memory with a
+ * kernel whose threads read the host buffer directly over the host link (many 16-byte loads in
+ * flight), instead of a copy-engine transfer, whose start-up dominates at the size of one
+ * decode step's inputs (about a megabyte). Not an operation of the method: the serving loop's
+ * host-to-device step, for measuring a decode step end to end.
+ *   d_dst   device memory of the current device, 16-byte aligned.
+ *   h_src   pinned host memory mapped for the device (cudaHostAlloc / cudaMallocHost /
+ *           cudaHostRegister), 16-byte aligned. The caller keeps it unchanged until the copy
+ *           has completed on `stream`.
+ *   bytes   a multiple of 16; 0 is a no-op.
+ * Stream-ordered and asynchronous. LAZY_ERR_INVALID_ARG for null or misaligned pointers, a
+ * size that is not a multiple of 16, a source that is not pinned host memory, or a destination
+ * that is not memory of the current device; nothing is launched then.
+ */
+int lazy_copy_to_device(void *d_dst, const void *h_src, size_t bytes, lazy_stream_t stream);
 /*
  * Test hook: gather the pages the words address using the kernels' own device unpack and
  * address arithmetic. d_k_out, d_v_out: device [n_words][num_kv_heads][page_size][head_dim];

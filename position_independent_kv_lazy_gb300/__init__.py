@@ -61,6 +61,7 @@ EXPORTS = [
     "lazy_pool_set_schedule_sms", "lazy_decode_shared_plan", "lazy_decode_shared_workspace_bytes",
     "lazy_attn_decode_shared",
     "lazy_pool_set_alibi", "lazy_pool_position_mode", "lazy_pool_set_decode_kernel",
+    "lazy_copy_to_device",
 ]
 
 
@@ -129,6 +130,7 @@ _SIGS = {
                                   _i32, _f32, _vp, _vp, _vp, ctypes.c_size_t, _i32, _vp, _vp,
                                   _vp], ctypes.c_int),
     "lazy_get_device_error": ([_vp, _pi32, _vp], ctypes.c_int),
+    "lazy_copy_to_device": ([_vp, _vp, ctypes.c_size_t, _vp], ctypes.c_int),
     "lazy_debug_gather": ([_vp, _vp, _i32, _vp, _vp, _vp, _vp], ctypes.c_int),
     "lazy_debug_wait_timeout": ([_vp, _u64, _vp], ctypes.c_int),
     "lazy_attn_decode_noalloc": ([_vp, _vp, _vp, _vp, _vp, _i32, _i32, _f32, _i32, _vp, _vp, _vp],
@@ -672,6 +674,16 @@ def lazy_get_device_error(pool: LazyPool, stream=None) -> int:
     _check("lazy_get_device_error", load_library().lazy_get_device_error(
         pool.handle, ctypes.byref(e), _stream(stream)))
     return e.value
+
+
+def lazy_copy_to_device(dst, src, stream=None) -> None:
+    """Copy the pinned host tensor `src` into the device tensor `dst` (same number of bytes, a
+    multiple of 16) with the SM-driven upload kernel; stream-ordered and asynchronous."""
+    n = src.numel() * src.element_size()
+    if dst.numel() * dst.element_size() != n:
+        raise ValueError("lazy_copy_to_device: dst and src differ in size")
+    _check("lazy_copy_to_device", load_library().lazy_copy_to_device(
+        _ptr(dst), _ptr(src), n, _stream(stream)))
 
 
 def lazy_debug_gather(pool: LazyPool, page_words, stream=None):

@@ -147,6 +147,12 @@ def test_attention_argument_checks_return_before_device_use(lazylib):
     assert lazylib.lazy_attn_prefill_append(h, dummy, dummy, dummy, dummy, dummy, None, dummy, 1,
                                             4, 4, 3, 0.1, dummy, dummy, None, 0, 0, dummy, dummy,
                                             None) == pk.LAZY_ERR_INVALID_ARG
+    # the upload call checks pointers and size before any device query
+    assert lazylib.lazy_copy_to_device(None, dummy, 16, None) == pk.LAZY_ERR_INVALID_ARG
+    assert lazylib.lazy_copy_to_device(dummy, ctypes.c_void_p(24), 16, None) == \
+        pk.LAZY_ERR_INVALID_ARG
+    assert lazylib.lazy_copy_to_device(dummy, dummy, 24, None) == pk.LAZY_ERR_INVALID_ARG
+    assert lazylib.lazy_copy_to_device(None, None, 0, None) == 0
     # empty batches are a no-op
     assert lazylib.lazy_attn_decode(h, None, None, None, None, 0, 4, 0.1, 0, None, None, None, 0,
                                     None) == 0
