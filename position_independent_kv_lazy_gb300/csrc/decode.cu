@@ -521,7 +521,11 @@ __device__ __forceinline__ float ex2_fast(float x) {
 template <int GC>
 struct MmaWarpState {
   uint32_t qa[8][4];  // A fragments of the rotated, scaled query (hi rows g, lo rows g + 8)
-  uint32_t qraw[16];  // raw query pairs of this thread: dims 16ks + 2t + {0,1}, {8,9}
+  // This thread's raw query pairs (dims 16ks + 2t + {0,1} and {8,9} at words 8ks and 8ks + 4);
+  // null for a dead row. Read from global memory at each rotation rather than kept in 16
+  // registers for the whole page loop: the loop runs at the register limit, and those 16
+  // registers made long decode 6% slower.
+  const uint32_t *qsrc;
   float o[16][4];     // O accumulator (rows g valid; rows g + 8 stay zero)
   float m_run, l_run, sl2;
   int32_t m_pos;
@@ -540,11 +544,7 @@ __device__ __forceinline__ void mma_begin_unit(MmaWarpState<GC> &st, const Decod
   st.m_pos = p.q_pos[b];
   const __nv_bfloat16 *q = reinterpret_cast<const __nv_bfloat16 *>(p.q) +
                            ((size_t)b * p.hq + hv * GC + (live ? g : 0)) * D + 2 * t;
-#pragma unroll
-  for (int ks = 0; ks < 8; ++ks) {
-    st.qraw[2 * ks] = live ? *reinterpret_cast<const uint32_t *>(q + 16 * ks) : 0u;
-    st.qraw[2 * ks + 1] = live ? *reinterpret_cast<const uint32_t *>(q + 16 * ks + 8) : 0u;
-  }
+  st.qsrc = live ? reinterpret_cast<const uint32_t *>(q) : nullptr;
   st.sl2 = (p.slopes != nullptr && live) ? p.slopes[hv * GC + g] * 1.4426950408889634f : 0.f;
   st.m_run = -INFINITY;
   st.l_run = 0.f;
@@ -578,6 +578,12 @@ __device__ __forceinline__ void mma_attend_page(MmaWarpState<GC> &st, const Deco
       const int64_t delta = alibi ? 0 : (int64_t)st.m_pos - (int64_t)off;
       // kSameDelta: lane l evaluates rotation pairs l and l + 32; each thread then fetches its
       // 16 pairs from the lanes that own them
+      uint32_t qraw[16];
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        qraw[2 * ks] = st.qsrc ? st.qsrc[8 * ks] : 0u;
+        qraw[2 * ks + 1] = st.qsrc ? st.qsrc[8 * ks + 4] : 0u;
+      }
       float c_lo = 0.f, s_lo = 0.f, c_hi = 0.f, s_hi = 0.f;
       if constexpr (kSameDelta) {
         rope_cos_sin(delta, p.turn[lane], c_lo, s_lo);
@@ -587,7 +593,7 @@ __device__ __forceinline__ void mma_attend_page(MmaWarpState<GC> &st, const Deco
       for (int ks = 0; ks < 4; ++ks) {  // dims d < 64 pair with d + 64 (k-step ks + 4)
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
-          const uint32_t lo_raw = st.qraw[2 * ks + h2], hi_raw = st.qraw[2 * (ks + 4) + h2];
+          const uint32_t lo_raw = qraw[2 * ks + h2], hi_raw = qraw[2 * (ks + 4) + h2];
           float x[2], y[2];
           x[0] = __uint_as_float(lo_raw << 16);
           x[1] = __uint_as_float(lo_raw & 0xFFFF0000u);
@@ -1046,11 +1052,7 @@ __device__ __forceinline__ void mma_begin_shared_unit(MmaWarpState<8> &st,
   const __nv_bfloat16 *q = reinterpret_cast<const __nv_bfloat16 *>(p.q) +
                            ((size_t)(live ? req : 0) * p.hq + h * sp.G + (live ? r : 0)) * D +
                            2 * t;
-#pragma unroll
-  for (int ks = 0; ks < 8; ++ks) {
-    st.qraw[2 * ks] = live ? *reinterpret_cast<const uint32_t *>(q + 16 * ks) : 0u;
-    st.qraw[2 * ks + 1] = live ? *reinterpret_cast<const uint32_t *>(q + 16 * ks + 8) : 0u;
-  }
+  st.qsrc = live ? reinterpret_cast<const uint32_t *>(q) : nullptr;
   st.sl2 = (p.slopes != nullptr && live) ? p.slopes[h * sp.G + r] * 1.4426950408889634f : 0.f;
   st.m_run = -INFINITY;
   st.l_run = 0.f;
