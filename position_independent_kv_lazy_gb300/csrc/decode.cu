@@ -526,7 +526,9 @@ struct MmaWarpState {
   // registers for the whole page loop: the loop runs at the register limit, and those 16
   // registers made long decode 6% slower.
   const uint32_t *qsrc;
-  float o[16][4];     // O accumulator (rows g valid; rows g + 8 stay zero)
+  // O transposed, O^T = V^T P^T (dims x heads): o[mt] holds dims 16 mt + g and 16 mt + g + 8
+  // of heads 2t and 2t + 1 (registers 0, 1: dim 16 mt + g; 2, 3: dim 16 mt + g + 8)
+  float o[8][4];
   float m_run, l_run, sl2;
   int32_t m_pos;
   uint32_t cur_off;
@@ -549,9 +551,9 @@ __device__ __forceinline__ void mma_begin_unit(MmaWarpState<GC> &st, const Decod
   st.m_run = -INFINITY;
   st.l_run = 0.f;
 #pragma unroll
-  for (int nt = 0; nt < 16; ++nt)
+  for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) st.o[nt][e] = 0.f;
+    for (int e = 0; e < 4; ++e) st.o[mt][e] = 0.f;
   st.cur_off = 0xFFFFFFFFu;
 }
 
@@ -660,15 +662,23 @@ __device__ __forceinline__ void mma_attend_page(MmaWarpState<GC> &st, const Deco
     float pm = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
     pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 1));
     pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 2));
-    if (pm > st.m_run) {  // the same in the 4 lanes of a row
-      const float alpha = st.m_run == -INFINITY ? 0.f : ex2_fast(st.m_run - pm);
+    float alpha = 1.f;  // the same in the 4 lanes of a row
+    if (pm > st.m_run) {
+      alpha = st.m_run == -INFINITY ? 0.f : ex2_fast(st.m_run - pm);
       st.l_run *= alpha;
-#pragma unroll
-      for (int nt = 0; nt < 16; ++nt) {
-        st.o[nt][0] *= alpha;
-        st.o[nt][1] *= alpha;
-      }
       st.m_run = pm;
+    }
+    // O^T's columns are heads 2t and 2t + 1: their factors come from the lanes of those rows
+    if (__any_sync(0xffffffffu, alpha != 1.f)) {
+      const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * t);
+      const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * t + 4);
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        st.o[mt][0] *= a0;
+        st.o[mt][1] *= a1;
+        st.o[mt][2] *= a0;
+        st.o[mt][3] *= a1;
+      }
     }
     float pv[4];
 #pragma unroll
@@ -676,16 +686,17 @@ __device__ __forceinline__ void mma_attend_page(MmaWarpState<GC> &st, const Deco
       pv[e] = ex2_fast(sv[e] - st.m_run);  // m_run is finite (key 0 is valid): exp2(-inf) = 0
       st.l_run += pv[e];
     }
-    const uint32_t pa[4] = {pack_bf16x2(pv[0], pv[1]), 0u, pack_bf16x2(pv[2], pv[3]), 0u};
-    // ---- O += P V: ldmatrix.trans matrix j covers keys 8 (j & 1) .. +7 and dims
-    // 16 dp + 8 (j >> 1) .. +7
-    const int vrow = (((lane >> 3) & 1) << 3) + (lane & 7), vhalf = lane >> 4;
+    // ---- O^T += V^T P^T (M = 16 dims, N = 8 heads, K = 16 keys). P^T as the B operand is the
+    // S accumulator's layout as it stands: keys 2t, 2t+1 and 2t+8, 2t+9 of head g. A = V^T:
+    // ldmatrix.trans matrix j covers keys 8 (j >> 1) .. +7 and dims 16 mt + 8 (j & 1) .. +7.
+    // 8 MMAs per page, against 16 for O = P V with its 8 idle rows.
+    const uint32_t pb0 = pack_bf16x2(pv[0], pv[1]), pb1 = pack_bf16x2(pv[2], pv[3]);
+    const int vrow = ((lane >> 4) << 3) + (lane & 7), vhalf = (lane >> 3) & 1;
 #pragma unroll
-    for (int dp = 0; dp < 8; ++dp) {
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4_t(page_chunk(vpg, vrow, 2 * dp + vhalf), b0, b1, b2, b3);
-      mma_bf16_16816(st.o[2 * dp], pa, b0, b1);
-      mma_bf16_16816(st.o[2 * dp + 1], pa, b2, b3);
+    for (int mt = 0; mt < 8; ++mt) {
+      uint32_t va[4];
+      ldsm_x4_t(page_chunk(vpg, vrow, 2 * mt + vhalf), va[0], va[1], va[2], va[3]);
+      mma_bf16_16816(st.o[mt], va, pb0, pb1);
     }
   }
 }
@@ -699,15 +710,28 @@ __device__ __forceinline__ void mma_flush(MmaWarpState<GC> &st, const DecodePara
   float l = st.l_run;
   l += __shfl_xor_sync(0xffffffffu, l, 1);
   l += __shfl_xor_sync(0xffffffffu, l, 2);
-  if (g < GC && st.live) {  // nobody reads a dead row's slot
-    const float inv = l > 0.f ? 1.f / l : 0.f;
-    float *dst = p.ws_o + ((size_t)slot * GC + g) * D + 2 * t;
+  // this thread's O^T columns are heads h0 = 2t and h0 + 1: their sums and liveness come from
+  // the lanes of those rows (nobody reads a dead row's slot)
+  const int h0 = 2 * t;
+  const float l0 = __shfl_sync(0xffffffffu, l, 8 * t), l1 = __shfl_sync(0xffffffffu, l, 8 * t + 4);
+  const bool live0 = __shfl_sync(0xffffffffu, (int)st.live, 8 * t) != 0 && h0 < GC;
+  const bool live1 = __shfl_sync(0xffffffffu, (int)st.live, 8 * t + 4) != 0 && h0 + 1 < GC;
+  const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
+  float *dst0 = p.ws_o + ((size_t)slot * GC + h0) * D + g;
+  float *dst1 = dst0 + D;
 #pragma unroll
-    for (int nt = 0; nt < 16; ++nt)
-      *reinterpret_cast<float2 *>(dst + nt * 8) =
-          make_float2(st.o[nt][0] * inv, st.o[nt][1] * inv);
-    if (t == 0) p.ws_lse[(size_t)slot * GC + g] = l > 0.f ? st.m_run + log2f(l) : -INFINITY;
+  for (int mt = 0; mt < 8; ++mt) {
+    if (live0) {
+      dst0[16 * mt] = st.o[mt][0] * inv0;
+      dst0[16 * mt + 8] = st.o[mt][2] * inv0;
+    }
+    if (live1) {
+      dst1[16 * mt] = st.o[mt][1] * inv1;
+      dst1[16 * mt + 8] = st.o[mt][3] * inv1;
+    }
   }
+  if (g < GC && st.live && t == 0)
+    p.ws_lse[(size_t)slot * GC + g] = l > 0.f ? st.m_run + log2f(l) : -INFINITY;
 }
 
 // Loads page word w of the tensor-core kernels into stage `st` (K and V, one page-view copy
@@ -1057,9 +1081,9 @@ __device__ __forceinline__ void mma_begin_shared_unit(MmaWarpState<8> &st,
   st.m_run = -INFINITY;
   st.l_run = 0.f;
 #pragma unroll
-  for (int nt = 0; nt < 16; ++nt)
+  for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) st.o[nt][e] = 0.f;
+    for (int e = 0; e < 4; ++e) st.o[mt][e] = 0.f;
   st.cur_off = 0xFFFFFFFFu;
 }
 
