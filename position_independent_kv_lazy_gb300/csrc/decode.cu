@@ -441,12 +441,14 @@ __global__ void __launch_bounds__(WARPS * 32) decode_split_kernel(const DecodePa
 // instructions per page, which made that kernel issue-bound rather than HBM-bound:
 //   S[16 x 16] = Q[16 x 128] . K_page^T   A = the query fragment held in registers,
 //                                          B = K page rows via ldmatrix (8 k-steps x 2 n-tiles)
-//   O[16 x 128] += P[16 x 16] . V_page     A = P, re-packed from the S accumulator registers,
-//                                          B = V page via ldmatrix.trans (16 n-tiles)
-// A-operand rows: row g < GC holds bf16(q_g), row g + 8 holds bf16(q_g - bf16(q_g)), so the
-// S accumulator's rows g and g + 8 - registers of the same thread - add up to the score of a
-// query with ~16 mantissa bits, as accurate as the fp32 path. Rows >= GC and P's rows g + 8
-// are zero. Pages arrive by TMA (one copy each for K and V; in shared memory two 16 x 64
+//   O^T[128 x 8] += V_page^T[128 x 16] . P^T[16 x 8]
+//                                          A = V page via ldmatrix.trans (8 m-tiles of 16 dims),
+//                                          B = P^T, re-packed from the S accumulator registers
+//                                          (its layout is already the B fragment's)
+// A-operand rows of S: row g < GC holds bf16(q_g), row g + 8 holds bf16(q_g - bf16(q_g)), so
+// the S accumulator's rows g and g + 8 - registers of the same thread - add up to the score of
+// a query with ~16 mantissa bits, as accurate as the fp32 path. Rows >= GC are zero; their P
+// columns feed O^T columns that are never written out. Pages arrive by TMA (one copy each for K and V; in shared memory two 16 x 64
 // boxes with 128-byte swizzle), so the ldmatrix row reads are bank-conflict free. One copy per
 // page rather than one per box: the issuing warp is latency-bound at three warps per scheduler,
 // and fewer copy instructions shorten its per-page chain (on decode_b64 -6% instructions,
@@ -557,7 +559,8 @@ __device__ __forceinline__ void mma_begin_unit(MmaWarpState<GC> &st, const Decod
   st.cur_off = 0xFFFFFFFFu;
 }
 
-// One 16-key page (K at page_smem, V 4 KB after it): S = Q K^T, online softmax, O += P V.
+// One 16-key page (K at page_smem, V 4 KB after it): S = Q K^T, online softmax,
+// O^T += V^T P^T.
 // kSameDelta: every row of the warp has the same query position and page word (one request per
 // warp), so the 64 angles of a query rotation are evaluated once per warp rather than per row.
 template <int GC, bool kSameDelta = false>
