@@ -138,6 +138,16 @@ def test_alibi_prefill_tensor_core_parity(pk, Hq, Hkv):
         _check(wl, slopes, out[cu[b]:cu[b + 1]], lse[cu[b]:cu[b + 1]], b)
 
 
+def test_alibi_prefill_query_side_flag_runs_the_alibi_kernel(pk):
+    # an ALiBi pool rotates nothing, so the tensor-core query-side flag takes the ALiBi kernel:
+    # the same result as LAZY_PREFILL_TC, bit for bit
+    wl = _prefill_wl(128, 32, 8, "bf16")
+    slopes = W.alibi_slopes(32)
+    _, _, out_tc, lse_tc = _prefill(pk, wl, slopes, pk.LAZY_PREFILL_TC)
+    _, _, out_qs, lse_qs = _prefill(pk, wl, slopes, pk.LAZY_PREFILL_TC_QSIDE)
+    assert np.array_equal(out_tc, out_qs) and np.array_equal(lse_tc, lse_qs)
+
+
 def test_alibi_full_size_sampled(pk):
     # the bench's shapes: decode_b64 (4161 keys per request) and prefill_b8 (16 x 1024 + 256),
     # 32/8/128 bf16, device-drawn inputs read back for the oracle
