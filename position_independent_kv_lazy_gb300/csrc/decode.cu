@@ -958,7 +958,8 @@ struct CombineParams {
 // intersect it) with a log-sum-exp combine and writes the final rows.
 template <typename T, int D, int GC>
 __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
-  cudaGridDependencySynchronize();  // partials of the decode kernel launched just before
+  // The piece range comes from the page table, an input of the decode step: it is read while
+  // the decode kernel launched just before still runs, and only the partials wait for it.
   const int32_t u = blockIdx.x;
   const int32_t b = u / p.hv, hv = u % p.hv;
   // the partition's units: (request, virtual head), or (request, kv head) shared by ch chunks
@@ -982,6 +983,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
     wf = ((S + 1) * W + N - 1) / N - 1;
     n_pieces = dense ? (E * W + N - 1) / N - 1 - wf + 1 : np;
   }
+  cudaGridDependencySynchronize();  // the decode kernel's partials
   for (int idx = threadIdx.x; idx < GC * (D / 4); idx += blockDim.x) {
     const int g = idx / (D / 4), d4 = idx % (D / 4);
     // one online pass over the unit's slots, eight at a time with their loads issued together
