@@ -142,8 +142,9 @@ def test_long_document_insert_spans_launches(pk):
 
 # ------------------------------------------------------------------ decode
 @pytest.mark.parametrize("D,Hq,Hkv,dtype", [
-    (128, 32, 8, "bf16"), (128, 8, 8, "bf16"), (64, 16, 8, "bf16"), (64, 16, 2, "bf16"),
-    (128, 32, 2, "bf16"), (64, 8, 2, "fp32"), (128, 4, 1, "fp32"), (128, 32, 1, "bf16")])
+    (128, 32, 8, "bf16"), (128, 8, 8, "bf16"), (128, 16, 8, "bf16"), (64, 16, 8, "bf16"),
+    (64, 16, 2, "bf16"), (128, 32, 2, "bf16"), (64, 8, 2, "fp32"), (128, 4, 1, "fp32"),
+    (128, 32, 1, "bf16")])
 def test_decode_parity_edge_layouts(pk, D, Hq, Hkv, dtype):
     wl = _edge_decode_workload(D, Hq, Hkv, dtype)
     _, _, out, lse = _decode(pk, wl)
@@ -210,7 +211,7 @@ def test_decode_output_to_pinned_host_memory(pk, kind):
 
 
 @pytest.mark.parametrize("kind", ["simt", "auto"])
-@pytest.mark.parametrize("Hq,Hkv", [(32, 8), (8, 8), (64, 8), (32, 1)])
+@pytest.mark.parametrize("Hq,Hkv", [(32, 8), (8, 8), (16, 8), (64, 8), (32, 1)])
 def test_decode_both_kernels_edge_layouts(pk, kind, Hq, Hkv):
     # bf16 / head_dim 128 runs the tensor-core (mma.sync) kernel by default; the CUDA-core
     # kernel stays selectable and both must meet the tolerances (groups 4, 1, 8, MQA 32)
@@ -754,8 +755,8 @@ def _small_prefill_workload(Hq, Hkv, dtype="bf16", D=128):
 
 @pytest.mark.parametrize("kind", ["simt", "auto"])
 @pytest.mark.parametrize("D,Hq,Hkv,dtype", [
-    (128, 32, 8, "bf16"), (128, 8, 8, "bf16"), (128, 64, 8, "bf16"), (128, 32, 1, "bf16"),
-    (64, 16, 8, "bf16"), (64, 8, 2, "fp32")])
+    (128, 32, 8, "bf16"), (128, 8, 8, "bf16"), (128, 16, 8, "bf16"), (128, 64, 8, "bf16"),
+    (128, 32, 1, "bf16"), (64, 16, 8, "bf16"), (64, 8, 2, "fp32")])
 def test_decode_small_contexts(pk, kind, D, Hq, Hkv, dtype):
     H = _h()
     wl = _small_decode_workload(Hq, Hkv, dtype, D)
