@@ -974,10 +974,15 @@ def materialised_bench(args, flush, stream, hbm_peak, tc_peak):
                    "copies uses page words of offset 0, prefill over copies "
                    "LAZY_PREFILL_ABSOLUTE_KEYS (reference position 0: offset-0 pages are only "
                    "converted to the fp16 Q.K operand type, not rotated)"}
-    # ---- decode: decode_b64 (shared documents) and its no-reuse control
+    # ---- decode: decode_b64 (shared documents) and the no-reuse controls of decode_b64 and
+    # long_decode_b16 (every request its own documents: the same bytes both ways, so the time
+    # difference is the lazy path's per-document rotation)
     for name, wl in (("decode_b64", W.decode_workload()),
                      ("decode_b64_no_reuse", W.decode_workload(no_reuse=True,
-                                                               name="decode_b64_no_reuse"))):
+                                                               name="decode_b64_no_reuse")),
+                     ("long_decode_b16_no_reuse",
+                      W.decode_workload(16, 64, 2048, alpha=1.2, question=0, no_reuse=True,
+                                        name="long_decode_b16_no_reuse"))):
         src = H.DeviceSource(wl)
         res = H.build_resident(wl, src, resident_pool=False,
                                extra_blocks=H.materialised_blocks_needed(wl))
@@ -1025,8 +1030,8 @@ def materialised_bench(args, flush, stream, hbm_peak, tc_peak):
             "lazy_over_copies": round(t_lazy / t_copy, 4)}
         del res, db, copies, cw, ccu, src
         torch.cuda.empty_cache()
-    out["decode_b64_no_reuse"]["rotation_overhead"] = round(
-        out["decode_b64_no_reuse"]["lazy_over_copies"] - 1.0, 4)
+    for name in ("decode_b64_no_reuse", "long_decode_b16_no_reuse"):
+        out[name]["rotation_overhead"] = round(out[name]["lazy_over_copies"] - 1.0, 4)
     # ---- prefill: prefill_b8
     wl = W.prefill_workload()
     src = H.DeviceSource(wl)
