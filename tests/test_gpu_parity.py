@@ -787,6 +787,21 @@ def test_prefill_small_contexts(pk, flags, Hq, Hkv):
     _check_prefill(wl, pb, out, lse, form="S")
 
 
+@pytest.mark.parametrize("flags", ["tc", "tc_qside", "simt"])
+def test_prefill_request_without_question_tokens(pk, flags):
+    # a request with T = 0 between two others (an empty cu_q range): the other requests' rows
+    # are unaffected; the last request has a 1-token question over overlapping document offsets
+    wl = W.custom("prefill", [[(0, 0), (1, 200)], [(2, 7)], [(0, 50), (2, 1)]], doc_len=200,
+                  n_pool=3, Hq=32, Hkv=8, D=128, dtype="bf16", base=500000.0, T=[37, 0, 1],
+                  q_pos0=[400, 207, 250], seed=41)
+    fl = {"tc": pk.LAZY_PREFILL_TC, "tc_qside": pk.LAZY_PREFILL_TC_QSIDE,
+          "simt": pk.LAZY_PREFILL_SIMT}[flags]
+    _, pb, out, lse = _prefill(pk, wl, fl)
+    cu = pb.cu_q.cpu().numpy()
+    assert cu[1] == cu[2]
+    _check_prefill(wl, pb, out, lse, reqs=[0, 2])
+
+
 @pytest.mark.parametrize("flags", ["simt", "simt_qside"])
 def test_prefill_small_contexts_fp32(pk, flags):
     wl = _small_prefill_workload(8, 2, "fp32", 64)
