@@ -955,9 +955,15 @@ struct CombineParams {
 };
 
 // One CTA per unit: merges the unit's pieces (slots unit + w for the warps w whose ranges
-// intersect it) with a log-sum-exp combine and writes the final rows.
+// intersect it) with a log-sum-exp combine and writes the final rows. One thread per (head,
+// 4-dim group) of the unit (combine_threads), so that each thread makes one pass: with 8 heads
+// per unit (MQA's chunks) two passes on 128 threads took 8 us of a 47 us call.
+template <int GC, int D>
+constexpr int combine_threads() {
+  return GC * (D / 4) < 32 ? 32 : (GC * (D / 4) > 256 ? 256 : GC * (D / 4));
+}
 template <typename T, int D, int GC>
-__global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
+__global__ void __launch_bounds__(combine_threads<GC, D>()) combine_kernel(const CombineParams p) {
   // The piece range comes from the page table, an input of the decode step: it is read while
   // the decode kernel launched just before still runs, and only the partials wait for it.
   const int32_t u = blockIdx.x;
@@ -1394,8 +1400,8 @@ struct MmaLaunch {
     if (!launched)
       LAZY_CUDA_TRY(launch_pdl(decode_mma_kernel<GC, kWarps, STAGES>, grid, kWarps * 32, kSmem,
                                s, mp));
-    LAZY_CUDA_TRY(launch_pdl(combine_kernel<__nv_bfloat16, 128, GC>, dp.batch * dp.hv, 128, 0,
-                             s, c2));
+    LAZY_CUDA_TRY(launch_pdl(combine_kernel<__nv_bfloat16, 128, GC>, dp.batch * dp.hv,
+                             combine_threads<GC, 128>(), 0, s, c2));
     return LAZY_OK;
   }
 };
@@ -1423,7 +1429,8 @@ struct DecodeLaunch {
     }
     LAZY_CUDA_TRY(launch_pdl(decode_split_kernel<T, D, GC, kWarps, STAGES>, grid, kWarps * 32,
                              kSmem, s, dp));
-    LAZY_CUDA_TRY(launch_pdl(combine_kernel<T, D, GC>, dp.batch * dp.hv, 128, 0, s, cp));
+    LAZY_CUDA_TRY(launch_pdl(combine_kernel<T, D, GC>, dp.batch * dp.hv, combine_threads<GC, D>(),
+                             0, s, cp));
     return LAZY_OK;
   }
 };
