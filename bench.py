@@ -437,6 +437,19 @@ def bench_materialised_only(args):
         args, flush, torch.cuda.current_stream(), hbm_peak, tc_peak)}), flush=True)
 
 
+def bench_mqa_only(args):
+    """The MQA section alone (decode and prefill with 32 query heads per kv head)."""
+    import torch
+
+    import position_independent_kv_lazy_gb300 as pk
+    pk.build_library()
+    pk.load_library()
+    hbm_peak, tc_peak, _, _ = _peaks()
+    flush, _ = _make_flush(torch)
+    print(json.dumps({"mode": "mqa only", "mqa": mqa_bench(
+        args, flush, torch.cuda.current_stream(), hbm_peak, tc_peak)}), flush=True)
+
+
 def bench_rotation_side_only(args):
     """The key-side / query-side prefill section alone."""
     import torch
@@ -1485,7 +1498,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", choices=["all", "decode", "prefill", "long_decode", "materialised",
-                                       "rotation_side"],
+                                       "rotation_side", "mqa"],
                     default="all",
                     help="decode / prefill / long_decode: time only that workload (smaller "
                          "footprint, for profiling)")
@@ -1508,6 +1521,8 @@ def main():
         bench_materialised_only(args)
     elif args.only == "rotation_side":
         bench_rotation_side_only(args)
+    elif args.only == "mqa":
+        bench_mqa_only(args)
     else:
         bench_ours(args)
 
