@@ -967,6 +967,8 @@ def _copy_device_ms(pk, wl, res, copies, stream, reps=3):
     """Device time of kv_pool_materialise_batch alone: the same copies written again into their
     blocks (same bytes), each call queued behind a sleep kernel so the host's list building and
     launch overlap it and the event pair holds only the page-list upload and the copy kernel."""
+    import torch
+
     spec = [(res.doc_blocks[d], wl.doc_len, o, ids) for (d, o), ids in copies.items()]
     ts = []
     for _ in range(reps):
@@ -978,7 +980,7 @@ def _copy_device_ms(pk, wl, res, copies, stream, reps=3):
         ev[1].record(stream)
         torch.cuda.synchronize()
         ts.append(ev[0].elapsed_time(ev[1]))
-    return float(np.median(ts))
+    return sorted(ts)[len(ts) // 2]
 
 
 def materialised_bench(args, flush, stream, hbm_peak, tc_peak):
@@ -1001,7 +1003,8 @@ def materialised_bench(args, flush, stream, hbm_peak, tc_peak):
 
     n_t = max(5, args.steps // 2)
     out = {"note": "copies: one per distinct (document, offset) pair, written by "
-                   "kv_pool_materialise (un-rotate by R(-j), re-rotate by R(o + j)); decode over "
+                   "kv_pool_materialise (un-rotate by R(-j), re-rotate by R(o + j), applied as their "
+                   "exact composition R(o)); decode over "
                    "copies uses page words of offset 0, prefill over copies "
                    "LAZY_PREFILL_ABSOLUTE_KEYS (reference position 0: offset-0 pages are only "
                    "converted to the fp16 Q.K operand type, not rotated); copy_ms is the "

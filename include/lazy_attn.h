@@ -215,8 +215,10 @@ int kv_pool_write_tokens(lazy_pool *pool, const void *d_k_raw, const void *d_v, 
  * prefill part describes that re-encoding as two rotations, one back to position 0 and one to
  * the target). For the n_tokens tokens of a cached segment held in src_block_ids (K rows
  * R(j) k at local positions j), writes to dst_block_ids:
- *     K row = R(offset + j) R(-j) (cached K row)   (fp32 arithmetic, one rounding to the pool
- *                                                    type)
+ *     K row = R(offset + j) R(-j) (cached K row) = R(offset) (cached K row)
+ *             (the two rotations compose exactly, the angles being exact modulo a full turn;
+ *             applied as the one rotation R(offset), fp32 arithmetic, one rounding to the pool
+ *             type)
  *     V row = cached V row
  * src_block_ids, dst_block_ids: host int32 [ceil(n_tokens / page_size)], blocks the caller
  * owns (kv_pool_alloc); no destination block may be one of the source blocks. The copy's keys

@@ -148,9 +148,11 @@ int dispatch_encode(lazy_pool *p, const void *k_raw, const void *v, int32_t n_to
 // Materialised copy (the position-aware baseline the summaries compare against, "Problem
 // statement" and the prefill part: a cached block re-encoded for one target position by two
 // rotations, one resetting it to position 0 and one to the target). Token j of a cached segment
-// (K row R(j) k) becomes K row R(offset + j) R(-j) (R(j) k) in the copy, fp32 arithmetic and one
-// rounding to the pool type; V is copied. One thread = (token, kv head, 16-byte chunk of the
-// lower half) and the matching chunk of the upper half, as in the encode.
+// (K row R(j) k) becomes K row R(offset + j) R(-j) (R(j) k) in the copy; V is copied. The two
+// rotations compose to R(offset) exactly (the angle arithmetic is exact modulo a full turn), so
+// the copy applies that one rotation in fp32 with one rounding to the pool type, and its angles
+// depend only on the offset. One thread = (token, kv heads h0 .. h0 + hpt - 1, 16-byte chunk of
+// the lower half) and the matching chunk of the upper half, as in the encode.
 // ----------------------------------------------------------------------------------------------
 constexpr int kMaxMatIds = 256;
 struct MatBlocks {
@@ -159,6 +161,51 @@ struct MatBlocks {
   int32_t src[kMaxMatIds];
   int32_t dst[kMaxMatIds];
 };
+
+// Rotate one (token, chunk) of hpt consecutive kv heads from src to dst (element offsets of head
+// h0), the next head's loads issued before this head's arithmetic; the first head's loads go out
+// before the angles are evaluated.
+template <typename T, int D>
+__device__ __forceinline__ void copy_rotate_heads(T *__restrict__ k_pool, T *__restrict__ v_pool,
+                                                  const uint64_t *__restrict__ turn, int c,
+                                                  int32_t offset, int hpt, size_t src,
+                                                  size_t dst) {
+  constexpr int EPL = 16 / (int)sizeof(T);
+  constexpr size_t kHead = (size_t)kPage * D;  // elements between heads of one block
+  uint4 ka = *reinterpret_cast<const uint4 *>(k_pool + src);
+  uint4 kb = *reinterpret_cast<const uint4 *>(k_pool + src + D / 2);
+  uint4 va = *reinterpret_cast<const uint4 *>(v_pool + src);
+  uint4 vb = *reinterpret_cast<const uint4 *>(v_pool + src + D / 2);
+  float cs[EPL], sn[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) rope_cos_sin((int64_t)offset, turn[c * EPL + e], cs[e], sn[e]);
+  for (int hh = 0; hh < hpt; ++hh) {
+    uint4 nka = ka, nkb = kb, nva = va, nvb = vb;
+    if (hh + 1 < hpt) {
+      const size_t ns = src + kHead;
+      nka = *reinterpret_cast<const uint4 *>(k_pool + ns);
+      nkb = *reinterpret_cast<const uint4 *>(k_pool + ns + D / 2);
+      nva = *reinterpret_cast<const uint4 *>(v_pool + ns);
+      nvb = *reinterpret_cast<const uint4 *>(v_pool + ns + D / 2);
+    }
+    float lo[EPL], hi[EPL];
+    unpack16<T>(ka, lo);
+    unpack16<T>(kb, hi);
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      const float x = lo[e], y = hi[e];
+      lo[e] = x * cs[e] - y * sn[e];
+      hi[e] = x * sn[e] + y * cs[e];
+    }
+    *reinterpret_cast<uint4 *>(k_pool + dst) = pack16<T>(lo);
+    *reinterpret_cast<uint4 *>(k_pool + dst + D / 2) = pack16<T>(hi);
+    *reinterpret_cast<uint4 *>(v_pool + dst) = va;
+    *reinterpret_cast<uint4 *>(v_pool + dst + D / 2) = vb;
+    ka = nka, kb = nkb, va = nva, vb = nvb;
+    src += kHead;
+    dst += kHead;
+  }
+}
 
 template <typename T, int D>
 __global__ void __launch_bounds__(256) materialise_kernel(
@@ -175,35 +222,9 @@ __global__ void __launch_bounds__(256) materialise_kernel(
     const int h0 = (int)(rest % groups) * hpt;
     const int32_t j = tok_lo + (int32_t)(rest / groups);
     const int pg = j / kPage - mb.first_page, slot = j % kPage;
-    // the two rotations' angles, once per token and chunk for the thread's kv heads
-    float c0[EPL], s0[EPL], c1[EPL], s1[EPL];
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) {
-      rope_cos_sin(-(int64_t)j, turn[c * EPL + e], c0[e], s0[e]);          // back to position 0
-      rope_cos_sin((int64_t)offset + j, turn[c * EPL + e], c1[e], s1[e]);  // to the target
-    }
-#pragma unroll 2
-    for (int h = h0; h < h0 + hpt; ++h) {
-      const size_t src = (((size_t)mb.src[pg] * hkv + h) * kPage + slot) * D;
-      const size_t dst = (((size_t)mb.dst[pg] * hkv + h) * kPage + slot) * D;
-      const uint4 ka = *reinterpret_cast<const uint4 *>(k_pool + src + c * EPL);
-      const uint4 kb = *reinterpret_cast<const uint4 *>(k_pool + src + D / 2 + c * EPL);
-      const uint4 va = *reinterpret_cast<const uint4 *>(v_pool + src + c * EPL);
-      const uint4 vb = *reinterpret_cast<const uint4 *>(v_pool + src + D / 2 + c * EPL);
-      float lo[EPL], hi[EPL];
-      unpack16<T>(ka, lo);
-      unpack16<T>(kb, hi);
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) {
-        const float x = lo[e] * c0[e] - hi[e] * s0[e], y = lo[e] * s0[e] + hi[e] * c0[e];
-        lo[e] = x * c1[e] - y * s1[e];
-        hi[e] = x * s1[e] + y * c1[e];
-      }
-      *reinterpret_cast<uint4 *>(k_pool + dst + c * EPL) = pack16<T>(lo);
-      *reinterpret_cast<uint4 *>(k_pool + dst + D / 2 + c * EPL) = pack16<T>(hi);
-      *reinterpret_cast<uint4 *>(v_pool + dst + c * EPL) = va;
-      *reinterpret_cast<uint4 *>(v_pool + dst + D / 2 + c * EPL) = vb;
-    }
+    copy_rotate_heads<T, D>(k_pool, v_pool, turn, c, offset, hpt,
+                            (((size_t)mb.src[pg] * hkv + h0) * kPage + slot) * D + c * EPL,
+                            (((size_t)mb.dst[pg] * hkv + h0) * kPage + slot) * D + c * EPL);
   }
 }
 
@@ -228,36 +249,10 @@ __global__ void __launch_bounds__(256) materialise_batch_kernel(
     const int slot = (int)(rest % kPage);
     const int4 pe = pages[rest / kPage];  // (copy, page within the copy, source, destination)
     const int2 ce = copies[pe.x];         // (tokens, offset)
-    const int32_t j = pe.y * kPage + slot;
-    if (j >= ce.x) continue;
-    float c0[EPL], s0[EPL], c1[EPL], s1[EPL];
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) {
-      rope_cos_sin(-(int64_t)j, turn[c * EPL + e], c0[e], s0[e]);        // back to position 0
-      rope_cos_sin((int64_t)ce.y + j, turn[c * EPL + e], c1[e], s1[e]);  // to the target
-    }
-#pragma unroll 2
-    for (int h = h0; h < h0 + hpt; ++h) {
-      const size_t src = (((size_t)pe.z * hkv + h) * kPage + slot) * D;
-      const size_t dst = (((size_t)pe.w * hkv + h) * kPage + slot) * D;
-      const uint4 ka = *reinterpret_cast<const uint4 *>(k_pool + src + c * EPL);
-      const uint4 kb = *reinterpret_cast<const uint4 *>(k_pool + src + D / 2 + c * EPL);
-      const uint4 va = *reinterpret_cast<const uint4 *>(v_pool + src + c * EPL);
-      const uint4 vb = *reinterpret_cast<const uint4 *>(v_pool + src + D / 2 + c * EPL);
-      float lo[EPL], hi[EPL];
-      unpack16<T>(ka, lo);
-      unpack16<T>(kb, hi);
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) {
-        const float x = lo[e] * c0[e] - hi[e] * s0[e], y = lo[e] * s0[e] + hi[e] * c0[e];
-        lo[e] = x * c1[e] - y * s1[e];
-        hi[e] = x * s1[e] + y * c1[e];
-      }
-      *reinterpret_cast<uint4 *>(k_pool + dst + c * EPL) = pack16<T>(lo);
-      *reinterpret_cast<uint4 *>(k_pool + dst + D / 2 + c * EPL) = pack16<T>(hi);
-      *reinterpret_cast<uint4 *>(v_pool + dst + c * EPL) = va;
-      *reinterpret_cast<uint4 *>(v_pool + dst + D / 2 + c * EPL) = vb;
-    }
+    if (pe.y * kPage + slot >= ce.x) continue;
+    copy_rotate_heads<T, D>(k_pool, v_pool, turn, c, ce.y, hpt,
+                            (((size_t)pe.z * hkv + h0) * kPage + slot) * D + c * EPL,
+                            (((size_t)pe.w * hkv + h0) * kPage + slot) * D + c * EPL);
   }
 }
 
