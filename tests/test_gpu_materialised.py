@@ -25,14 +25,15 @@ def _h():
     return harness
 
 
+@pytest.mark.parametrize("off", [123457, (1 << 26) - 100])
 @pytest.mark.parametrize("dtype,D", [("bf16", 128), ("fp32", 64)])
-def test_materialised_pages_hold_keys_at_absolute_positions(pk, dtype, D):
-    # a 40-token document (the last page partial) re-encoded for offset 123457: K rows equal
-    # R(offset + j) k up to the cache's rounding (twice: the cached copy, then the re-encoded
-    # one); V rows are the raw values
+def test_materialised_pages_hold_keys_at_absolute_positions(pk, dtype, D, off):
+    # a 40-token document (the last page partial) re-encoded for offset `off` (the second just
+    # below the 2^26 position limit): K rows equal R(offset + j) k up to the cache's rounding
+    # (twice: the cached copy, then the re-encoded one); V rows are the raw values
     H = _h()
-    wl = W.custom("decode", [[(0, 123457)]], doc_len=40, n_pool=1, Hq=4, Hkv=2, D=D, dtype=dtype,
-                  base=500000.0, priv=[(123497, 1)], seed=31)
+    wl = W.custom("decode", [[(0, off)]], doc_len=40, n_pool=1, Hq=4, Hkv=2, D=D, dtype=dtype,
+                  base=500000.0, priv=[(off + 40, 1)], seed=31)
     src = H.HostSource(wl)
     res = H.build_resident(wl, src, resident_pool=False, extra_blocks=4)
     o = wl.requests[0].offsets[0]
