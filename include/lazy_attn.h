@@ -240,8 +240,10 @@ int kv_pool_materialise(lazy_pool *pool, const int32_t *src_block_ids,
  *   src_block_ids, dst_block_ids  host int32 [cu_pages[n_copies]]
  *   n_tokens, offsets             host int32 [n_copies]; offsets[c] + n_tokens[c] < 2^26
  * No destination block may be a source block of any copy, nor appear twice (copies run in
- * parallel). The page list is copied to device memory taken from the stream-ordered allocator
- * and returned after the launch. LAZY_ERR_INVALID_ARG for any violation (nothing launched);
+ * parallel). The page list is built in a pinned host buffer the pool keeps (grown on demand; a
+ * call first waits until the previous call's upload from it has ended), uploaded in one
+ * asynchronous copy to device memory taken from the stream-ordered allocator, and that memory
+ * is returned after the launch. LAZY_ERR_INVALID_ARG for any violation (nothing launched);
  * LAZY_ERR_UNSUPPORTED on ALiBi pools.
  */
 int kv_pool_materialise_batch(lazy_pool *pool, int32_t n_copies, const int32_t *cu_pages,

@@ -491,25 +491,37 @@ extern "C" int kv_pool_materialise_batch(lazy_pool *p, int32_t n_copies, const i
   int rc = ensure_device(p);
   if (rc != LAZY_OK) return rc;
   p->encoded = true;
+  cudaStream_t s = (cudaStream_t)stream;
+  const size_t pages_bytes = sizeof(int4) * (size_t)total_pages;
+  const size_t bytes = pages_bytes + sizeof(int2) * (size_t)n_copies;
+  // The page list is written into the pool's pinned staging buffer and uploaded from there in
+  // one asynchronous copy (a pageable source would go through the driver's staging, which cost
+  // more than the copy kernel itself). The previous call's upload from the buffer ends first.
+  std::lock_guard<std::mutex> g(p->mu);
+  if (p->stage_done) LAZY_CUDA_TRY(cudaEventSynchronize(p->stage_done));
+  else LAZY_CUDA_TRY(cudaEventCreateWithFlags(&p->stage_done, cudaEventDisableTiming));
+  if (p->h_stage_bytes < bytes) {
+    if (p->h_stage) LAZY_CUDA_TRY(cudaFreeHost(p->h_stage));
+    p->h_stage = nullptr;
+    p->h_stage_bytes = 0;
+    size_t cap = (size_t)1 << 20;
+    while (cap < bytes) cap <<= 1;
+    LAZY_CUDA_TRY(cudaHostAlloc(&p->h_stage, cap, cudaHostAllocDefault));
+    p->h_stage_bytes = cap;
+  }
   // the page list: (copy, page within the copy, source, destination) per page, then
   // (tokens, offset) per copy
-  std::vector<int4> pages(total_pages);
-  std::vector<int2> copies(n_copies);
+  int4 *pages = reinterpret_cast<int4 *>(p->h_stage);
+  int2 *copies = reinterpret_cast<int2 *>(reinterpret_cast<uint8_t *>(p->h_stage) + pages_bytes);
   for (int32_t c = 0; c < n_copies; ++c) {
     copies[c] = make_int2(n_tokens[c], offsets[c]);
     for (int32_t pg = cu_pages[c]; pg < cu_pages[c + 1]; ++pg)
       pages[pg] = make_int4(c, pg - cu_pages[c], src_block_ids[pg], dst_block_ids[pg]);
   }
-  cudaStream_t s = (cudaStream_t)stream;
-  const size_t pages_bytes = sizeof(int4) * (size_t)total_pages;
-  const size_t bytes = pages_bytes + sizeof(int2) * (size_t)n_copies;
   void *buf = nullptr;
   LAZY_CUDA_TRY(cudaMallocAsync(&buf, bytes, s));
-  // pageable sources: each copy has read its host data when the call returns
-  cudaError_t e = cudaMemcpyAsync(buf, pages.data(), pages_bytes, cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess)
-    e = cudaMemcpyAsync((uint8_t *)buf + pages_bytes, copies.data(), bytes - pages_bytes,
-                        cudaMemcpyHostToDevice, s);
+  cudaError_t e = cudaMemcpyAsync(buf, p->h_stage, bytes, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaEventRecord(p->stage_done, s);
   if (e != cudaSuccess) {
     cudaFreeAsync(buf, s);
     return record_cuda(e, "kv_pool_materialise_batch page list");

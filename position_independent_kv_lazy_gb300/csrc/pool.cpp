@@ -107,6 +107,11 @@ int lazy_pool_destroy(lazy_pool *p) {
     cudaFree(p->d_turn);
     if (p->d_slopes) cudaFree(p->d_slopes);
   }
+  if (p->stage_done) {
+    cudaEventSynchronize(p->stage_done);
+    cudaEventDestroy(p->stage_done);
+  }
+  if (p->h_stage) cudaFreeHost(p->h_stage);
   delete p;
   return LAZY_OK;
 }

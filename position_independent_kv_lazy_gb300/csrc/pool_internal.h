@@ -36,6 +36,13 @@ struct lazy_pool {
   std::vector<float> slopes;        // per query head
   float *d_slopes = nullptr;
 
+  // Pinned host staging of kv_pool_materialise_batch's page list (grown on demand, guarded by
+  // mu); stage_done marks the end of the last upload from it, which the next call waits for
+  // before refilling it.
+  void *h_stage = nullptr;
+  size_t h_stage_bytes = 0;
+  cudaEvent_t stage_done = nullptr;
+
   // Tensor maps of the page buffers for the tensor-core prefill (built lazily).
   bool tmaps_ready = false;
   alignas(64) unsigned char tmap_k[128];   // 2-D view: 16-row page boxes
