@@ -204,3 +204,31 @@ def test_prefill_absolute_keys_over_copies(pk, sms):
         for name, (o, l) in results.items():
             assert np.abs(o[rows] - ro).max() <= 2e-2, (name, b)
             assert np.abs(l[rows] - rl).max() <= 1e-3, (name, b)
+
+
+def test_materialise_batch_staging_grows_between_calls(pk):
+    # a 3-copy batch, then 70,000 one-page copies (a 1.7 MB page list: the pool's pinned staging
+    # buffer grows past its first 1 MB), then a 3-copy batch again; sampled copies equal the
+    # single-copy results bit for bit
+    H = _h()
+    wl = W.custom("decode", [[(0, 3)]], doc_len=16, n_pool=1, Hq=2, Hkv=1, D=64, dtype="bf16",
+                  base=500000.0, priv=[(19, 1)], seed=34)
+    src = H.HostSource(wl)
+    n_big = 70000
+    res = H.build_resident(wl, src, resident_pool=False, extra_blocks=n_big + 32)
+    doc = res.doc_blocks[0]
+    small = pk.kv_pool_materialise_batch(res.pool, [(doc, 16, o) for o in (5, 77, 1000)])
+    big_offs = [7 * k + 1 for k in range(n_big)]
+    big = pk.kv_pool_materialise_batch(res.pool, [(doc, 16, o) for o in big_offs])
+    small2 = pk.kv_pool_materialise_batch(res.pool, [(doc, 16, o) for o in (5, 77, 1000)])
+    torch.cuda.synchronize()
+    assert pk.lazy_get_device_error(res.pool) == 0
+    checks = [(small[i], o) for i, o in enumerate((5, 77, 1000))]
+    checks += [(small2[i], o) for i, o in enumerate((5, 77, 1000))]
+    checks += [(big[k], big_offs[k]) for k in (0, 1, 4097, 65535, n_big - 1)]
+    for ids, o in checks:
+        ref = pk.kv_pool_materialise(res.pool, doc, 16, o)
+        torch.cuda.synchronize()
+        for pages in (res.pool.k_pages, res.pool.v_pages):
+            assert torch.equal(pages[ids[0]], pages[ref[0]]), o
+        pk.kv_pool_release(res.pool, ref)
